@@ -1,0 +1,144 @@
+"""Oracle packer: float32 W [N, K] -> block-scaled codes + scales (TEST INFRASTRUCTURE ONLY).
+
+An independent restatement of the packing the pages describe; the library's own
+C++ packer must produce the same bytes.  All arithmetic is IEEE float32
+(numpy float32 ops round once per operation, no contraction).
+
+Steps, per row n and block b along K (metaltile PR #250, commit "Foundation for
+the spec-conformant nvfp4/mxfp4/mxfp8/nvfp8 formats"; rlx-cpu
+``thunk/ops/quant.rs`` ``lowp_compute_scales`` / ``lowp_snap_scale`` /
+``lowp_quantize``):
+
+1. amax = max |w| over the block;
+2. raw scale s = amax / max_finite(element), or 1.0 for an all-zero block;
+3. snap s to the stored scale grid (E8M0, E4M3 or float32);
+4. quantize every element against the *effective* (decoded, snapped) scale:
+   code = encode(w / eff), code 0 when eff == 0;
+5. pack codes LSB-first (two 4-bit codes per byte, element 2i in the low
+   nibble; one byte per 8-bit code).
+
+Readings taken where the pages are silent (each is listed in the design doc):
+
+* E8M0 snapping is ceil(log2 s): the smallest power of two >= amax/max_finite,
+  so no element needs to clip.
+* nvfp4 global scale = amax(W) / (6 * 448) (1.0 for an all-zero W), so the
+  largest micro-scale lands at 448; micro-scale u = E4M3_RNE((amax_b / 6) /
+  global); an all-zero block stores u = E4M3(1.0) = 0x38.
+* Element encoders round to nearest, ties to the even code, saturating.
+* int4 affine (MLX style, group 64): s = (max - min) / 15 (1.0 when 0), stored
+  as bf16 (RNE); bias = bf16(min); q = clamp(round_half_away((w - b) / s), 0, 15);
+  scale and bias are interleaved per group as bf16 pairs [N, K/64, 2].
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import codec
+
+FORMATS = ("mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8", "int4_affine")
+
+BLOCK = {"mxfp4": 32, "nvfp4": 16, "mxfp8_e4m3": 32, "mxfp8_e5m2": 32, "nvfp8": 16, "int4_affine": 64}
+ELEM_BITS = {"mxfp4": 4, "nvfp4": 4, "mxfp8_e4m3": 8, "mxfp8_e5m2": 8, "nvfp8": 8, "int4_affine": 4}
+SCALE_BYTES = {"mxfp4": 1, "nvfp4": 1, "mxfp8_e4m3": 1, "mxfp8_e5m2": 1, "nvfp8": 4, "int4_affine": 4}
+_ELEM = {"mxfp4": ("e2m1", codec.E2M1_MAX), "nvfp4": ("e2m1", codec.E2M1_MAX),
+         "mxfp8_e4m3": ("e4m3", codec.E4M3_MAX), "mxfp8_e5m2": ("e5m2", codec.E5M2_MAX),
+         "nvfp8": ("e4m3", codec.E4M3_MAX)}
+
+F32 = np.float32
+
+
+def codes_nbytes(fmt: str, n: int, k: int) -> int:
+    return n * k * ELEM_BITS[fmt] // 8
+
+
+def scales_nbytes(fmt: str, n: int, k: int) -> int:
+    return n * (k // BLOCK[fmt]) * SCALE_BYTES[fmt]
+
+
+def _pack_nibbles(codes: np.ndarray) -> np.ndarray:
+    """[N, K] uint8 codes (0..15) -> [N, K/2] bytes, element 2i in the low nibble."""
+    c = codes.astype(np.uint8)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def _quantize(w_blocks: np.ndarray, eff: np.ndarray, elem: str) -> np.ndarray:
+    """codes = encode(w / eff) with eff broadcast over the block; eff == 0 -> code 0."""
+    safe = np.where(eff == 0, F32(1.0), eff).astype(F32)
+    v = (w_blocks / safe[..., None]).astype(F32)
+    codes = codec.encode_rne_sat(v, elem)
+    return np.where((eff == 0)[..., None], np.uint8(0), codes)
+
+
+def pack(fmt: str, w: np.ndarray):
+    """Pack float32 W [N, K].  Returns (codes bytes, scales bytes, global_scale float32).
+
+    Raises ValueError on non-finite weights, K not a multiple of the block, or a
+    scale that overflows float32.
+    """
+    if fmt not in FORMATS:
+        raise ValueError(f"unknown format {fmt!r}")
+    w = np.ascontiguousarray(w, dtype=F32)
+    n, k = w.shape
+    blk = BLOCK[fmt]
+    if k % blk or k % 8:
+        raise ValueError("K must be a multiple of the block size and of 8")
+    if not np.all(np.isfinite(w)):
+        raise ValueError("non-finite weight")
+    wb = w.reshape(n, k // blk, blk)
+    amax = np.max(np.abs(wb), axis=2).astype(F32)          # step 1
+    glob = F32(1.0)
+
+    if fmt == "int4_affine":
+        return _pack_int4_affine(wb, n, k)
+
+    elem, maxf = _ELEM[fmt]
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2"):
+        s = np.where(amax > 0, amax / F32(maxf), F32(1.0)).astype(F32)   # step 2
+        scode = codec.e8m0_encode_ceil(s)                                  # step 3
+        eff = codec.E8M0_TABLE[scode].astype(F32)                          # exact power of two
+        scales = scode
+    elif fmt == "nvfp4":
+        amax_t = F32(np.max(amax)) if amax.size else F32(0.0)
+        glob = F32(amax_t / F32(6.0 * 448.0)) if amax_t > 0 else F32(1.0)
+        t = ((amax / F32(6.0)).astype(F32) / glob).astype(F32)
+        ucode = codec.encode_rne_sat(t, "e4m3")
+        ucode = np.where(amax > 0, ucode, np.uint8(0x38)).astype(np.uint8)
+        eff = (codec.E4M3_TABLE[ucode].astype(F32) * glob).astype(F32)
+        scales = ucode
+    else:  # nvfp8: float32 scale stored raw
+        s = np.where(amax > 0, amax / F32(maxf), F32(1.0)).astype(F32)
+        eff = s
+        scales = s
+    if not np.all(np.isfinite(eff)):
+        raise ValueError("scale overflows float32")
+
+    codes = _quantize(wb, eff, elem).reshape(n, k)                        # step 4
+    codes_b = _pack_nibbles(codes) if ELEM_BITS[fmt] == 4 else codes.astype(np.uint8)
+    scales_b = np.ascontiguousarray(scales).view(np.uint8).reshape(n, -1)
+    return codes_b, scales_b, F32(glob)
+
+
+def _round_half_away(v: np.ndarray) -> np.ndarray:
+    a = np.abs(v.astype(np.float64))
+    return np.copysign(np.floor(a + 0.5), v)
+
+
+def _pack_int4_affine(wb: np.ndarray, n: int, k: int):
+    mn = np.min(wb, axis=2).astype(F32)
+    mx = np.max(wb, axis=2).astype(F32)
+    s = ((mx - mn).astype(F32) / F32(15.0)).astype(F32)
+    s = np.where(s == 0, F32(1.0), s).astype(F32)
+    if not np.all(np.isfinite(s)):
+        raise ValueError("scale overflows float32")
+    s_bits = codec.bf16_round(s)
+    b_bits = codec.bf16_round(mn)
+    s_b = codec.decode_bf16(s_bits).astype(F32)
+    b_b = codec.decode_bf16(b_bits).astype(F32)
+    safe = np.where(s_b == 0, F32(1.0), s_b).astype(F32)
+    v = ((wb - b_b[..., None]).astype(F32) / safe[..., None]).astype(F32)
+    q = np.clip(_round_half_away(v), 0, 15).astype(np.uint8)
+    q = np.where((s_b == 0)[..., None], np.uint8(0), q)
+    codes_b = _pack_nibbles(q.reshape(n, k))
+    pair = np.stack([s_bits, b_bits], axis=-1).astype(np.uint16)     # [N, K/64, 2]
+    scales_b = np.ascontiguousarray(pair).view(np.uint8).reshape(n, -1)
+    return codes_b, scales_b, F32(1.0)

@@ -1,0 +1,132 @@
+"""Oracle dequant and dequantizing matmul (TEST INFRASTRUCTURE ONLY).
+
+* ``dequant_exact``: the spec value of every weight, exact in float64.
+* ``dequant_f32``: that value rounded once to float32 (the bit-exact contract
+  of the library's dequant kernel).
+* ``qmm_ref``: out[m, n] = sum_k x[m, k] * w[n, k] in float64 with w the exact
+  spec value, plus the error bound 2e-3 * sum_k |x||w| + 1e-6.
+
+Value definitions (page title, then the section):
+
+* mxfp4 / mxfp8: w = elem(code) * 2^(scale_bits - 127) -- metaltile PR #250,
+  commit "First spec-conformant block-scaled dequant kernel: mt_mxfp4_dequant"
+  and the commit completing the mxfp8 dequant kernels.
+* nvfp4: w = (e2m1(code) * e4m3(micro)) * global -- rlx-cpu
+  ``thunk/ops/quant.rs`` ``dequant_matmul_nvfp4`` (E2M1 nibble times the E4M3
+  block scale times the global FP32 scale, block 16 along K).  The inner
+  product is exact, so the single float32 rounding is well defined.
+* nvfp8: w = e4m3(code) * scale_f32 (block 16) -- PR #250 format list.
+* int4 affine: w = scale * q + bias with q the LSB-first nibble, group 64 --
+  metaltile-std ``tests/qmm_gpu_correctness.rs``, ``cpu_qmm_reference``;
+  scale and bias are bf16.  float64 evaluation of s*q + b is exact or, when
+  the terms are more than 2^41 apart, already rounds to the float32 answer, so
+  one float32 rounding of it equals fmaf(s, q, b).
+* qmm: "dequant-then-dot" -- PR #250 qgemv/qmm commits (the oracle the GPU
+  kernels are checked against) and rlx-cpu ``lowp_scaled_matmul`` (a
+  decode-and-accumulate reference kept for correctness, not speed).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import codec
+from .pack import BLOCK, ELEM_BITS, FORMATS
+
+BOUND_REL = 2e-3
+BOUND_ABS = 1e-6
+
+
+def unpack_codes(fmt: str, codes: np.ndarray, n: int, k: int) -> np.ndarray:
+    """Packed code bytes -> [N, K] integer codes (nibble 2i is the low nibble of byte i)."""
+    b = np.asarray(codes, dtype=np.uint8).reshape(n, -1)
+    if ELEM_BITS[fmt] == 8:
+        return b.reshape(n, k)
+    out = np.empty((n, k), dtype=np.uint8)
+    out[:, 0::2] = b & 0x0F
+    out[:, 1::2] = b >> 4
+    return out
+
+
+def block_scales(fmt: str, scales: np.ndarray, global_scale: float, n: int, k: int):
+    """Decoded per-block scale terms, each [N, K/block] float64.
+
+    Returns (mult, add): w = elem * mult (+ add for int4 affine).  For nvfp4
+    ``mult`` is the E4M3 micro-scale only; the global is applied separately so
+    that the product order (e2m1 * e4m3) * global is kept.
+    """
+    nb = k // BLOCK[fmt]
+    s = np.asarray(scales, dtype=np.uint8).reshape(n, -1)
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2"):
+        return codec.E8M0_TABLE[s.reshape(n, nb)], None
+    if fmt == "nvfp4":
+        return codec.E4M3_TABLE[s.reshape(n, nb)], None
+    if fmt == "nvfp8":
+        return np.ascontiguousarray(s).view(np.float32).reshape(n, nb).astype(np.float64), None
+    pair = np.ascontiguousarray(s).view(np.uint16).reshape(n, nb, 2)
+    return codec.decode_bf16(pair[..., 0]), codec.decode_bf16(pair[..., 1])
+
+
+def element_values(fmt: str, codes: np.ndarray) -> np.ndarray:
+    if fmt in ("mxfp4", "nvfp4"):
+        return codec.E2M1_TABLE[codes]
+    if fmt in ("mxfp8_e4m3", "nvfp8"):
+        return codec.E4M3_TABLE[codes]
+    if fmt == "mxfp8_e5m2":
+        return codec.E5M2_TABLE[codes]
+    return codes.astype(np.float64)                      # int4 affine: q itself
+
+
+def dequant_exact(fmt: str, codes, scales, global_scale, n: int, k: int) -> np.ndarray:
+    """Exact spec value of W [N, K] in float64."""
+    if fmt not in FORMATS:
+        raise ValueError(fmt)
+    blk = BLOCK[fmt]
+    e = element_values(fmt, unpack_codes(fmt, codes, n, k)).reshape(n, k // blk, blk)
+    mult, add = block_scales(fmt, scales, global_scale, n, k)
+    with np.errstate(invalid="ignore", over="ignore"):
+        w = e * mult[..., None]
+        if add is not None:
+            w = w + add[..., None]
+        if fmt == "nvfp4":
+            w = w * np.float64(np.float32(global_scale))
+    return w.reshape(n, k)
+
+
+def dequant_f32(fmt: str, codes, scales, global_scale, n: int, k: int) -> np.ndarray:
+    """Spec value rounded once to float32 (overflow to +-inf, subnormals kept)."""
+    with np.errstate(over="ignore", invalid="ignore"):
+        return dequant_exact(fmt, codes, scales, global_scale, n, k).astype(np.float32)
+
+
+def x_values(x: np.ndarray, x_dtype: str) -> np.ndarray:
+    """Activation values in float64: bf16 bit patterns (uint16) or float32."""
+    if x_dtype == "bf16":
+        return codec.decode_bf16(x)
+    if x_dtype == "f32":
+        return np.asarray(x, dtype=np.float32).astype(np.float64)
+    raise ValueError(x_dtype)
+
+
+def qmm_ref(fmt, codes, scales, global_scale, x, x_dtype, m, n, k):
+    """(ref, bound) for out = X . dequant(W)^T, both [M, N] float64."""
+    w = dequant_exact(fmt, codes, scales, global_scale, n, k)
+    xv = x_values(x, x_dtype).reshape(m, k)
+    ref = xv @ w.T
+    bound = BOUND_REL * (np.abs(xv) @ np.abs(w).T) + BOUND_ABS
+    return ref, bound
+
+
+def qmm_ref_sampled(fmt, codes, scales, global_scale, x, x_dtype, m, n, k, rows, cols):
+    """(ref, bound) at the sampled (rows[i], cols[i]) pairs only, decoding just those W rows."""
+    rows = np.asarray(rows)
+    cols = np.asarray(cols)
+    uniq, inv = np.unique(cols, return_inverse=True)
+    per_row_codes = ELEM_BITS[fmt] * k // 8
+    per_row_scales = (k // BLOCK[fmt]) * (4 if fmt in ("nvfp8", "int4_affine") else 1)
+    c = np.asarray(codes, dtype=np.uint8).reshape(n, per_row_codes)[uniq]
+    s = np.asarray(scales, dtype=np.uint8).reshape(n, per_row_scales)[uniq]
+    w = dequant_exact(fmt, c, s, global_scale, len(uniq), k)[inv]
+    xv = x_values(x, x_dtype).reshape(m, k)[rows]
+    ref = np.einsum("ik,ik->i", xv, w)
+    bound = BOUND_REL * np.einsum("ik,ik->i", np.abs(xv), np.abs(w)) + BOUND_ABS
+    return ref, bound

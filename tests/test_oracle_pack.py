@@ -1,0 +1,213 @@
+"""Pins for the oracle packer and dequant: byte layout, zero blocks, exact round trips,
+value idempotence, nearest-grid quantization, and the per-format direction floors."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_quantized_spec_gb300 import synth
+from oracle import codec, pack, reference
+
+FMTS = pack.FORMATS
+MX = ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2")
+
+
+def _elem_values_lib(fmt, codes_nk):
+    """Element values from library reinterpretations (not the oracle's tables)."""
+    if fmt in ("mxfp4", "nvfp4"):
+        c = codes_nk.astype(np.int64)
+        c3 = c & 7
+        e, m = c3 >> 1, c3 & 1
+        two_m = np.where(e == 0, m, (m + 2) * (2 ** np.maximum(e - 1, 0)))
+        return (1 - 2 * (c >> 3)) * two_m / 2.0
+    if fmt in ("mxfp8_e4m3", "nvfp8"):
+        return torch.from_numpy(codes_nk.astype(np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+    if fmt == "mxfp8_e5m2":
+        return (codes_nk.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
+    return codes_nk.astype(np.float64)
+
+
+def test_byte_sizes():
+    # PR #250: 4-bit codes pack 8 per u32 (two per byte), 8-bit one byte per code;
+    # one scale per block: E8M0/E4M3 one byte, nvfp8 FP32, int4 affine bf16 scale + bf16 bias.
+    n, k = 12, 256
+    w = synth.weights(n, k, seed=5)
+    for fmt in FMTS:
+        c, s, g = pack.pack(fmt, w)
+        bits = 4 if fmt in ("mxfp4", "nvfp4", "int4_affine") else 8
+        assert c.nbytes == n * k * bits // 8 == pack.codes_nbytes(fmt, n, k)
+        per_scale = {"nvfp8": 4, "int4_affine": 4}.get(fmt, 1)
+        assert s.nbytes == n * (k // pack.BLOCK[fmt]) * per_scale == pack.scales_nbytes(fmt, n, k)
+        assert c.dtype == np.uint8 and s.dtype == np.uint8 and isinstance(g, np.float32)
+
+
+def test_nibble_order_is_lsb_first():
+    # Element 2i in the low nibble of byte i (8 codes per little-endian u32, code k at bits 4k).
+    n, k = 1, 32
+    w = np.zeros((n, k), np.float32)
+    w[0, 0] = 6.0       # max code 7 at element 0 -> low nibble of byte 0
+    w[0, 3] = -3.0      # element 3 -> high nibble of byte 1
+    c, s, _ = pack.pack("mxfp4", w)
+    assert s[0, 0] == 127                       # amax 6 -> scale 2^0
+    assert c[0, 0] == 0x07 and c[0, 1] == 0xD0  # -3.0 = code 0xD
+    u32 = c.view("<u4")[0, 0]
+    assert (u32 >> 0) & 0xF == 7 and (u32 >> 12) & 0xF == 0xD
+
+
+def test_zero_blocks():
+    # rlx-cpu lowp_compute_scales: an all-zero block gets scale 1.0; lowp_quantize: codes 0.
+    n, k = 2, 128
+    w = np.zeros((n, k), np.float32)
+    for fmt in FMTS:
+        c, s, g = pack.pack(fmt, w)
+        assert not c.any(), fmt
+        if fmt in MX:
+            assert (s == 127).all()
+        elif fmt == "nvfp4":
+            assert (s == 0x38).all() and g == 1.0
+        elif fmt == "nvfp8":
+            assert (s.view(np.float32) == 1.0).all()
+        else:
+            pair = s.view(np.uint16).reshape(n, -1, 2)
+            assert (pair[..., 0] == 0x3F80).all() and (pair[..., 1] == 0).all()
+        assert not reference.dequant_exact(fmt, c, s, g, n, k).any()
+
+
+@pytest.mark.parametrize("fmt", MX)
+def test_exactly_representable_roundtrip_mx(fmt):
+    # W built as code values x 2^e with the block maximum at the element max: pack must
+    # return exactly those codes and scales (the snapped scale equals amax / max_finite).
+    rng = np.random.default_rng(7)
+    n, k, blk = 8, 256, 32
+    elem = {"mxfp4": "e2m1", "mxfp8_e4m3": "e4m3", "mxfp8_e5m2": "e5m2"}[fmt]
+    table = {"e2m1": codec.E2M1_TABLE, "e4m3": codec.E4M3_TABLE, "e5m2": codec.E5M2_TABLE}[elem]
+    ncode = 16 if elem == "e2m1" else 256
+    finite = np.array([c for c in range(ncode) if np.isfinite(table[c])])
+    maxcode = int(finite[np.argmax(table[finite])])
+    codes = rng.choice(finite, size=(n, k))
+    codes[:, ::blk] = maxcode
+    e = rng.integers(-20, 10, size=(n, k // blk))
+    vals = _elem_values_lib(fmt, codes).reshape(n, k // blk, blk) * (2.0 ** e)[..., None]
+    w = vals.reshape(n, k).astype(np.float32)
+    assert np.array_equal(w.astype(np.float64), vals.reshape(n, k))
+    c, s, g = pack.pack(fmt, w)
+    assert np.array_equal(s, (e + 127).astype(np.uint8))
+    got = reference.unpack_codes(fmt, c, n, k)
+    # +0 and -0 both decode to zero; compare values, then the bytes away from zeros
+    assert np.array_equal(_elem_values_lib(fmt, got), _elem_values_lib(fmt, codes))
+    nz = _elem_values_lib(fmt, codes) != 0
+    assert np.array_equal(got[nz], codes[nz].astype(np.uint8))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_value_idempotence(fmt):
+    # Packing the dequantized weights again reproduces the same values (the codes
+    # quantized against the effective scale are self-consistent, PR #250).
+    n, k = 32, 512
+    w = synth.weights(n, k, seed=11, outliers=(fmt == "nvfp4"))
+    c, s, g = pack.pack(fmt, w)
+    wd = reference.dequant_f32(fmt, c, s, g, n, k)
+    c2, s2, g2 = pack.pack(fmt, wd)
+    wd2 = reference.dequant_f32(fmt, c2, s2, g2, n, k)
+    if fmt == "int4_affine":
+        # the affine grid re-fit on dequantized data may move by one bf16 rounding of min/scale
+        scale = codec.decode_bf16(s.view(np.uint16).reshape(n, -1, 2)[..., 0])
+        tol = np.repeat(scale, 64, axis=1) * 0.51 + 1e-30
+        assert (np.abs(wd2.astype(np.float64) - wd) <= tol).all()
+    else:
+        assert np.array_equal(wd, wd2)
+
+
+FLOORS = {"mxfp4": 0.98, "nvfp4": 0.98, "int4_affine": 0.99,
+          "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999}
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_cosine_floor(fmt):
+    # PR #250: pack -> dequant judged by direction (cosine) against a per-format floor.
+    n, k = 64, 1024
+    w = synth.weights(n, k, seed=13, outliers=(fmt == "nvfp4"))
+    c, s, g = pack.pack(fmt, w)
+    wd = reference.dequant_exact(fmt, c, s, g, n, k).ravel()
+    wv = w.astype(np.float64).ravel()
+    cos = wv @ wd / np.linalg.norm(wv) / np.linalg.norm(wd)
+    assert cos >= FLOORS[fmt], (fmt, cos)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8"])
+def test_elements_are_nearest_grid_points(fmt):
+    # Brute force over every code: each dequantized element is a closest point
+    # of {value(code) * eff} to w (ties allowed either way), eff the block's effective scale.
+    n, k = 2, 64
+    w = synth.weights(n, k, seed=17, outliers=(fmt == "nvfp4"))
+    c, s, g = pack.pack(fmt, w)
+    blk = pack.BLOCK[fmt]
+    mult, _ = reference.block_scales(fmt, s, g, n, k)
+    eff = np.repeat(mult, blk, axis=1)
+    if fmt == "nvfp4":
+        eff = (eff.astype(np.float32) * g).astype(np.float64)   # effective scale is rounded to f32
+    ncode = 16 if fmt in ("mxfp4", "nvfp4") else 256
+    allv = _elem_values_lib(fmt, np.arange(ncode))
+    allv = allv[np.isfinite(allv)]
+    got = _elem_values_lib(fmt, reference.unpack_codes(fmt, c, n, k))
+    for i in range(n):
+        for j in range(k):
+            wf = Fraction(float(w[i, j]))
+            ef = Fraction(float(eff[i, j]))
+            best = min(abs(wf - Fraction(float(v)) * ef) for v in allv)
+            assert abs(wf - Fraction(float(got[i, j])) * ef) == best, (fmt, i, j)
+
+
+def test_nvfp4_two_level_global():
+    # PR #250: the global FP32 scale lets the E4M3 micro-scales fit +-448 -> the block
+    # holding the tensor maximum gets micro-scale 448 (code 0x7E); global = amax / (6 * 448).
+    n, k = 16, 256
+    w = synth.weights(n, k, seed=19, outliers=True)
+    c, s, g = pack.pack("nvfp4", w)
+    amax = np.float32(np.max(np.abs(w)))
+    assert g == np.float32(amax / np.float32(2688.0))
+    nb = k // 16
+    blk_max = np.abs(w).reshape(n, nb, 16).max(axis=2)
+    i, j = np.unravel_index(np.argmax(blk_max), blk_max.shape)
+    assert s.reshape(n, nb)[i, j] == 0x7E
+    assert not np.isin(s, [0x7F, 0xFF]).any()
+
+
+def test_no_special_codes_emitted():
+    n, k = 64, 512
+    for fmt in ("mxfp8_e4m3", "nvfp8", "mxfp8_e5m2"):
+        w = synth.weights(n, k, seed=23) * np.float32(1e3)
+        c, s, g = pack.pack(fmt, w)
+        if fmt == "mxfp8_e5m2":
+            assert not (((c >> 2) & 31) == 31).any()
+        else:
+            assert not ((c & 0x7F) == 0x7F).any()
+        assert np.isfinite(reference.dequant_exact(fmt, c, s, g, n, k)).all()
+
+
+def test_int4_affine_quantizer():
+    # scale = (max - min)/15 and bias = min, both rounded to bf16; q = round-half-away
+    # of (w - bias)/scale clamped to [0, 15]; error at most half a step (plus the
+    # bf16 rounding of bias/scale pushed through the clamp).
+    n, k = 16, 256
+    w = synth.weights(n, k, seed=29)
+    c, s, g = pack.pack("int4_affine", w)
+    pair = s.view(np.uint16).reshape(n, k // 64, 2)
+    sc = codec.decode_bf16(pair[..., 0])
+    bi = codec.decode_bf16(pair[..., 1])
+    wb = w.reshape(n, k // 64, 64).astype(np.float64)
+    assert (np.abs(bi - wb.min(axis=2)) <= np.abs(wb.min(axis=2)) * 2.0 ** -8).all()
+    true_s = (wb.max(axis=2) - wb.min(axis=2)) / 15
+    assert (np.abs(sc - true_s) <= true_s * 2.0 ** -8 * 1.01).all()
+    wd = reference.dequant_exact("int4_affine", c, s, g, n, k).reshape(n, k // 64, 64)
+    assert (np.abs(wd - wb) <= sc[..., None] * 0.5 * 1.05 + np.abs(bi)[..., None] * 2.0 ** -7).all()
+
+
+def test_pack_rejects_bad_input():
+    with pytest.raises(ValueError):
+        pack.pack("mxfp4", np.full((1, 32), np.nan, np.float32))
+    with pytest.raises(ValueError):
+        pack.pack("mxfp4", np.zeros((1, 48), np.float32))
+    with pytest.raises(ValueError):
+        pack.pack("bogus", np.zeros((1, 64), np.float32))

@@ -1,0 +1,252 @@
+"""Pins for the oracle's dequant value and dequantizing matmul.
+
+* exact rational brute force (Python Fractions, element/scale values from
+  library reinterpretations and explicit nibble loops) on tiny shapes;
+* the all-unit-scales special case equals a library matmul of the decoded codes;
+* the int4-affine algebraic split (scale * sum q x + bias * sum x) that the
+  metaltile qmm correctness test uses, on that test's deterministic pattern;
+* batch rows equal stacked single-row results;
+* planted mistakes (applied to the oracle on the CPU) are caught by these pins.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_quantized_spec_gb300 import synth
+from oracle import pack, reference
+
+FMTS = pack.FORMATS
+
+
+# ----- an independent decode: explicit loops + library reinterpretations -----
+
+def _lib_elem(fmt, c):
+    if fmt in ("mxfp4", "nvfp4"):
+        # fp_quantized_mma.rs two_m_int: subnormal 2m = mant, normal 2m = (mant+2) 2^(exp-1)
+        c3, s = c & 7, 1 - 2 * (c >> 3)
+        e, m = c3 >> 1, c3 & 1
+        two_m = m if e == 0 else (m + 2) * 2 ** (e - 1)
+        return Fraction(s * two_m, 2)
+    if fmt in ("mxfp8_e4m3", "nvfp8"):
+        v = torch.tensor([c], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()
+        return Fraction(v)
+    if fmt == "mxfp8_e5m2":
+        return Fraction(float(np.array([c << 8], np.uint16).view(np.float16)[0]))
+    return Fraction(c)
+
+
+def _lib_scale(fmt, sbytes, n, b):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2"):
+        return Fraction(2) ** (int(sbytes[n][b]) - 127), Fraction(0)
+    if fmt == "nvfp4":
+        v = torch.tensor([int(sbytes[n][b])], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()
+        return Fraction(v), Fraction(0)
+    if fmt == "nvfp8":
+        return Fraction(float(np.frombuffer(bytes(sbytes[n][4 * b:4 * b + 4]), "<f4")[0])), Fraction(0)
+    raw = bytes(sbytes[n][4 * b:4 * b + 4])
+    s_bits, b_bits = np.frombuffer(raw, "<u2")
+    f = lambda h: Fraction(float((np.array([h], np.uint32) << 16).view(np.float32)[0]))  # noqa: E731
+    return f(s_bits), f(b_bits)
+
+
+def _brute_qmm(fmt, codes, scales, g, x64, m, n, k):
+    blk = pack.BLOCK[fmt]
+    codes = [[int(v) for v in r] for r in np.asarray(codes).reshape(n, -1)]
+    scales = [[int(v) for v in r] for r in np.asarray(scales).reshape(n, -1)]
+    out = [[Fraction(0)] * n for _ in range(m)]
+    for j in range(n):
+        wrow = []
+        for kk in range(k):
+            if fmt in ("mxfp4", "nvfp4", "int4_affine"):
+                byte = codes[j][kk // 2]
+                c = (byte >> (4 * (kk % 2))) & 0xF
+            else:
+                c = codes[j][kk]
+            mul, add = _lib_scale(fmt, scales, j, kk // blk)
+            w = _lib_elem(fmt, c) * mul + add
+            if fmt == "nvfp4":
+                w *= Fraction(float(g))
+            wrow.append(w)
+        for i in range(m):
+            out[i][j] = sum(Fraction(float(x64[i][kk])) * wrow[kk] for kk in range(k))
+    return out
+
+
+def _tiny_case(fmt, m=3, n=5, k=64, seed=0):
+    w = synth.weights(n, k, seed=seed, outliers=(fmt == "nvfp4"))
+    c, s, g = pack.pack(fmt, w)
+    x = synth.activations_bf16(m, k, seed=seed + 1)
+    return c, s, g, x
+
+
+def _check_brute(fmt, m=3, n=5, k=64, seed=0):
+    c, s, g, x = _tiny_case(fmt, m, n, k, seed)
+    ref, bound = reference.qmm_ref(fmt, c, s, g, x, "bf16", m, n, k)
+    x64 = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    exact = _brute_qmm(fmt, c, s, g, x64, m, n, k)
+    for i in range(m):
+        for j in range(n):
+            # ref is an fp64 matmul: within a few fp64 ulps of the exact rational sum
+            err = abs(Fraction(ref[i, j]) - exact[i][j])
+            scale = sum(abs(Fraction(float(x64[i][kk]))) for kk in range(k)) + 1
+            assert err <= Fraction(1, 2 ** 40) * scale, (fmt, i, j)
+    return True
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_qmm_ref_matches_exact_rational_brute_force(fmt):
+    assert _check_brute(fmt)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_dequant_f32_is_one_rounding_of_exact(fmt):
+    n, k = 4, 64
+    c, s, g, _ = _tiny_case(fmt, 1, n, k, seed=3)
+    wf = reference.dequant_f32(fmt, c, s, g, n, k)
+    codes = [[int(v) for v in r] for r in np.asarray(c).reshape(n, -1)]
+    scales = [[int(v) for v in r] for r in np.asarray(s).reshape(n, -1)]
+    blk = pack.BLOCK[fmt]
+    for j in range(n):
+        for kk in range(k):
+            byte = codes[j][kk // 2] if fmt in ("mxfp4", "nvfp4", "int4_affine") else codes[j][kk]
+            cc = (byte >> (4 * (kk % 2))) & 0xF if fmt in ("mxfp4", "nvfp4", "int4_affine") else byte
+            mul, add = _lib_scale(fmt, scales, j, kk // blk)
+            w = _lib_elem(fmt, cc) * mul + add
+            if fmt == "nvfp4":
+                w *= Fraction(float(g))
+            # the float32 nearest to w (ties even) via numpy's correctly rounded conversion
+            # of the exactly representable float64 w
+            assert float(w) == w or fmt == "int4_affine"
+            assert wf[j, kk] == np.float32(float(w)), (fmt, j, kk)
+
+
+def test_unit_scales_equal_library_matmul():
+    # All E8M0 scales 127 (= 1.0): qmm reduces to X @ E(codes)^T, a plain library matmul.
+    rng = np.random.default_rng(5)
+    m, n, k = 4, 24, 128
+    for fmt, elem_dt in (("mxfp8_e4m3", torch.float8_e4m3fn), ("mxfp8_e5m2", torch.float8_e5m2)):
+        codes = rng.integers(0, 256, size=(n, k), dtype=np.uint8)
+        bad = (codes & 0x7F) == 0x7F if fmt == "mxfp8_e4m3" else ((codes >> 2) & 31) == 31
+        codes[bad] = 0
+        scales = np.full((n, k // 32), 127, np.uint8)
+        x = synth.activations_bf16(m, k, seed=6)
+        ref, _ = reference.qmm_ref(fmt, codes, scales, 1.0, x, "bf16", m, n, k)
+        e = torch.from_numpy(codes).view(elem_dt).double()
+        xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double()
+        lib = (xt @ e.T).numpy()
+        assert np.allclose(ref, lib, rtol=1e-12, atol=1e-12)
+
+
+def test_batch_rows_equal_stacked_single_rows():
+    # rlx-cpu batch-M vs row-by-row M=1 equality test idea.
+    fmt, m, n, k = "nvfp4", 6, 32, 256
+    c, s, g, x = _tiny_case(fmt, m, n, k, seed=9)
+    ref, bound = reference.qmm_ref(fmt, c, s, g, x, "bf16", m, n, k)
+    for i in range(m):
+        r1, b1 = reference.qmm_ref(fmt, c, s, g, x[i:i + 1], "bf16", 1, n, k)
+        assert np.array_equal(r1[0], ref[i]) and np.array_equal(b1[0], bound[i])
+
+
+def test_sampled_ref_equals_dense_ref():
+    fmt, m, n, k = "int4_affine", 5, 40, 256
+    c, s, g, x = _tiny_case(fmt, m, n, k, seed=10)
+    ref, bound = reference.qmm_ref(fmt, c, s, g, x, "bf16", m, n, k)
+    rows = np.array([0, 4, 2, 3, 1, 0])
+    cols = np.array([39, 0, 17, 17, 5, 38])
+    r, b = reference.qmm_ref_sampled(fmt, c, s, g, x, "bf16", m, n, k, rows, cols)
+    assert np.allclose(r, ref[rows, cols], rtol=1e-14, atol=1e-14)
+    assert np.allclose(b, bound[rows, cols], rtol=1e-14, atol=1e-14)
+
+
+def test_int4_affine_algebraic_split_on_page_pattern():
+    # metaltile-std tests/qmm_gpu_correctness.rs, mt_qmm_matches_cpu_reference_f32:
+    # m=8, n=16, k=512, group 64; packed word i holds nibble ((i + bit) & 0xF) at bits 4*bit;
+    # scales 0.1 + 0.001 i, biases 0.0001 i (rounded here to the bf16 storage);
+    # x = 1 + 0.001 i (f32).  Its CPU reference accumulates s_g * sum(q x) + bias_g * sum(x)
+    # per group: an algebraically different route to the same sums.
+    m, n, k, gs = 8, 16, 512, 64
+    words = np.array([sum(((i + bit) & 0xF) << (4 * bit) for bit in range(8))
+                      for i in range(n * k // 8)], dtype="<u4")
+    codes = words.view(np.uint8).reshape(n, k // 2)
+    ng = k // gs
+    sc = np.array([0.1 + i * 0.001 for i in range(n * ng)], np.float32)
+    bi = np.array([i * 0.0001 for i in range(n * ng)], np.float32)
+    sc_b = torch.from_numpy(sc).to(torch.bfloat16)
+    bi_b = torch.from_numpy(bi).to(torch.bfloat16)
+    pair = torch.stack([sc_b.view(torch.int16), bi_b.view(torch.int16)], dim=-1).numpy().view(np.uint16)
+    scales = pair.reshape(n, ng * 2).view(np.uint8)
+    x = np.array([1.0 + i * 0.001 for i in range(m * k)], np.float32).reshape(m, k)
+    ref, _ = reference.qmm_ref("int4_affine", codes, scales, 1.0, x, "f32", m, n, k)
+    s64, b64 = sc_b.double().numpy(), bi_b.double().numpy()
+    for r in range(m):
+        for col in range(n):
+            acc = Fraction(0)
+            for grp in range(ng):
+                qdot = Fraction(0)
+                xsum = Fraction(0)
+                for p in range(8):
+                    packed = int(words[col * k // 8 + grp * 8 + p])
+                    for bit in range(8):
+                        q = (packed >> (bit * 4)) & 0xF
+                        xv = Fraction(float(x[r, grp * gs + p * 8 + bit]))
+                        qdot += q * xv
+                        xsum += xv
+                acc += Fraction(float(s64[col * ng + grp])) * qdot + Fraction(float(b64[col * ng + grp])) * xsum
+            assert abs(Fraction(ref[r, col]) - acc) <= abs(acc) * Fraction(1, 2 ** 45), (r, col)
+
+
+def test_bound_definition():
+    fmt, m, n, k = "mxfp4", 2, 8, 64
+    c, s, g, x = _tiny_case(fmt, m, n, k, seed=12)
+    _, bound = reference.qmm_ref(fmt, c, s, g, x, "bf16", m, n, k)
+    w = reference.dequant_exact(fmt, c, s, g, n, k)
+    xv = reference.x_values(x, "bf16")
+    for i in range(m):
+        for j in range(n):
+            want = 2e-3 * sum(abs(xv[i, kk]) * abs(w[j, kk]) for kk in range(k)) + 1e-6
+            assert abs(bound[i, j] - want) <= 1e-15 * want
+
+
+# ---------------------- planted mistakes in the oracle are caught ----------------------
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    """Each plausible oracle bug (wrong nibble order, dropped global, transposed
+    operand, swapped scale/bias) must make a pin above fail."""
+    orig_unpack = reference.unpack_codes
+    orig_scales = reference.block_scales
+    orig_exact = reference.dequant_exact
+
+    def swapped_nibbles(fmt, codes, n, k):
+        out = orig_unpack(fmt, codes, n, k)
+        if fmt in ("mxfp4", "nvfp4", "int4_affine"):
+            out = out.reshape(n, k // 2, 2)[..., ::-1].reshape(n, k)
+        return out
+
+    def dropped_global(fmt, codes, scales, g, n, k):
+        return orig_exact(fmt, codes, scales, 1.0, n, k)
+
+    def swapped_affine(fmt, scales, g, n, k):
+        mul, add = orig_scales(fmt, scales, g, n, k)
+        return (add, mul) if add is not None else (mul, add)
+
+    plants = [("unpack_codes", swapped_nibbles, "mxfp4"),
+              ("dequant_exact", dropped_global, "nvfp4"),
+              ("block_scales", swapped_affine, "int4_affine")]
+    for name, fn, fmt in plants:
+        with monkeypatch.context() as mp:
+            mp.setattr(reference, name, fn)
+            with pytest.raises(AssertionError):
+                _check_brute(fmt)
+
+    # a transposed weight operand
+    def transposed_ref(fmt, codes, scales, g, x, x_dtype, m, n, k):
+        w = orig_exact(fmt, codes, scales, g, n, k)
+        xv = reference.x_values(x, x_dtype).reshape(m, k)
+        return (xv @ w.reshape(k, n)), None
+
+    with monkeypatch.context() as mp:
+        mp.setattr(reference, "qmm_ref", transposed_ref)
+        with pytest.raises(AssertionError):
+            _check_brute("mxfp8_e4m3")

@@ -1,0 +1,430 @@
+"""Benchmark of the block-scaled fused dequantizing matmul on GB300.
+
+Headline workload (one "step"): a decode pass over a stack of L distinct
+mxfp4 weight matrices, N = K = 4096 (E2M1 codes + E8M0 scale per 32-block,
+W ~ N(0, 0.02), seed 0), one qmm per layer with M = 1 bf16 activation row
+(X ~ N(0, 1)).  The L copies together exceed 3x the 129 MB L2, so every
+layer's weights come from HBM; the L launches of a step are captured in one
+CUDA graph.  value = algorithmic bytes (codes + scales + X + out, each once)
+per second, whole job.
+
+Also reported (``breakdown``): the other workloads of the method at their
+stated shapes -- the nvfp4 batch GEMV (M = 1, 8; N = 14336), the mxfp8 E4M3
+prefill GEMM (M = 2048, N = K = 4096) and the int4-affine / mxfp8 E5M2 /
+nvfp8 sweep (M = 1, 16, 128, 4096; N = 11008, K = 4096) -- GEMV rows in GB/s,
+GEMM rows in TFLOP/s, each against its roofline.
+
+``--impl reference`` times the CPU oracle (numpy decode -> float64 W ->
+float64 matmul) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "qGEMV HBM GB/s (M=1) & qGEMM TFLOP/s (M≥128), % of GB300 roofline"
+L2_BYTES = 129 * 2 ** 20
+HEADLINE = ("mxfp4", 1, 4096, 4096)
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-breakdown", action="store_true")
+    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K")
+    return p.parse_args()
+
+
+def sizes(fmt, m, n, k):
+    """Algorithmic bytes of one qmm: codes + scales + global + X (bf16) + out (bf16)."""
+    import block_scaled_quantized_spec_gb300 as q
+    b = q.qfmt_codes_bytes(fmt, n, k) + q.qfmt_scales_bytes(fmt, n, k) + 2 * m * k + 2 * m * n
+    if fmt == "nvfp4":
+        b += 4
+    return b
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """Samples nvidia-smi during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_init(args):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class Problem:
+    """L copies of one packed weight in HBM, their activations and outputs."""
+
+    def __init__(self, fmt, m, n, k, copies, seed=0):
+        import numpy as np
+        import torch
+        import block_scaled_quantized_spec_gb300 as q
+        from block_scaled_quantized_spec_gb300 import synth
+        self.fmt, self.m, self.n, self.k = fmt, m, n, k
+        rng = np.random.default_rng(seed)
+        w = synth.weights(n, k, rng=rng, outliers=(fmt == "nvfp4"))
+        xb = synth.activations_bf16(m, k, rng=rng)
+        c, s, g = q.qfmt_pack(fmt, w)
+        del w
+        self.g = g
+        dc = torch.from_numpy(c).cuda()
+        ds = torch.from_numpy(s).cuda()
+        self.codes = [dc] + [dc.clone() for _ in range(copies - 1)]
+        self.scales = [ds] + [ds.clone() for _ in range(copies - 1)]
+        self.x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16)
+        x = self.x_host.cuda()
+        self.x = [x] + [x.clone() for _ in range(copies - 1)]
+        self.out = [torch.empty((m, n), dtype=torch.bfloat16, device="cuda") for _ in range(copies)]
+        self.copies = copies
+        self.bytes = sizes(fmt, m, n, k)
+        self.flops = 2.0 * m * n * k
+
+    def step(self):
+        import block_scaled_quantized_spec_gb300 as q
+        for i in range(self.copies):
+            q.qmm(self.fmt, self.codes[i], self.scales[i], self.g, self.x[i], self.n, out=self.out[i])
+
+    def graph(self):
+        import torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step()                                   # warm the library's per-device cache
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step()
+        return g
+
+
+def time_graph(graph, steps, warmup, world, clocks_index=None):
+    import torch
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = Clocks(clocks_index) if clocks_index is not None else None
+    if clk:
+        clk.__enter__()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    if clk:
+        clk.__exit__(None, None, None)
+    barrier(world)
+    ms = e0.elapsed_time(e1) / steps
+    return max_over_ranks(ms, world), (clk.summary() if clk else None)
+
+
+def copies_for(nbytes, m):
+    if m >= 128:
+        return 2
+    return max(4, min(64, -(-3 * L2_BYTES // nbytes)))
+
+
+def measure_e2e(prob, steps, warmup):
+    """Same metric through the public call with host buffers: per step, H2D of each
+    layer's activations from pinned memory, the qmm launches, D2H of each output."""
+    import torch
+    import block_scaled_quantized_spec_gb300 as q
+    xh = [prob.x_host.pin_memory() for _ in range(prob.copies)]
+    oh = [torch.empty((prob.m, prob.n), dtype=torch.bfloat16).pin_memory() for _ in range(prob.copies)]
+
+    def one():
+        for i in range(prob.copies):
+            prob.x[i].copy_(xh[i], non_blocking=True)
+            q.qmm(prob.fmt, prob.codes[i], prob.scales[i], prob.g, prob.x[i], prob.n, out=prob.out[i])
+            oh[i].copy_(prob.out[i], non_blocking=True)
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        one()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, prob.copies * prob.m * prob.k * 2, prob.copies * prob.m * prob.n * 2
+
+
+class OracleSample:
+    """The CPU oracle as it stands, on whole calls of the workload (inputs prepared once)."""
+
+    def __init__(self, fmt, m, n, k):
+        import numpy as np
+        from block_scaled_quantized_spec_gb300 import synth
+        from oracle import pack as opack
+        rng = np.random.default_rng(0)
+        w = synth.weights(n, k, rng=rng, outliers=(fmt == "nvfp4"))
+        self.xb = synth.activations_bf16(m, k, rng=rng)
+        self.c, self.s, self.g = opack.pack(fmt, w)
+        self.fmt, self.m, self.n, self.k = fmt, m, n, k
+        self.nbytes = opack.codes_nbytes(fmt, n, k) + opack.scales_nbytes(fmt, n, k) + 2 * m * k + 2 * m * n
+
+    def run(self, budget_s, min_calls=1):
+        from oracle import reference as oref
+        times = []
+        t_end = time.perf_counter() + budget_s
+        while time.perf_counter() < t_end or len(times) < min_calls:
+            t0 = time.perf_counter()
+            oref.qmm_ref(self.fmt, self.c, self.s, self.g, self.xb, "bf16", self.m, self.n, self.k)
+            times.append(time.perf_counter() - t0)
+        return times
+
+    def summary(self, times):
+        t = statistics.median(times)
+        return {"value": self.nbytes / t / 1e9, "unit": "GB/s", "cores": _blas_threads(), "kind": "oracle",
+                "sample": f"{len(times)} whole oracle calls {self.fmt} M={self.m} N={self.n} K={self.k} "
+                          f"(median {t * 1e3:.1f} ms each; numpy decode single-threaded, float64 matmul on "
+                          f"the BLAS threads)"}
+
+
+def cpu_baseline(fmt, m, n, k, budget_s=12.0):
+    o = OracleSample(fmt, m, n, k)
+    return o.summary(o.run(budget_s, min_calls=2))
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    fmt, m, n, k = HEADLINE
+    o = OracleSample(fmt, m, n, k)
+    o.run(0.0, min_calls=max(1, args.warmup))
+    per_step, all_times = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ts = o.run(0.0, min_calls=3)        # one step: 3 whole oracle calls
+        all_times += ts
+        per_step.append(o.nbytes * len(ts) / sum(ts) / 1e9)
+    wall = time.perf_counter() - t0
+    v = statistics.median(per_step)
+    cb = o.summary(all_times)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "mxfp4 decode qGEMV M=1 N=4096 K=4096 (CPU oracle; a step = 3 whole calls)"},
+            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": v,
+                             "unit": "GB/s"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def roofline_gemv(prob, ms_step, hbm, kind):
+    per_launch_ms = ms_step / prob.copies
+    achieved = prob.bytes / (per_launch_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": None, "peak_kind": f"{kind} (STREAM copy)",
+            "kernel": f"qgemv_kernel<{prob.fmt}>", "per_launch_us": round(per_launch_ms * 1e3, 3),
+            "algorithmic_bytes_per_launch": prob.bytes}
+
+
+BREAKDOWN = [
+    ("nvfp4", 1, 14336, 4096), ("nvfp4", 8, 14336, 4096),
+    ("mxfp8_e4m3", 2048, 4096, 4096),
+    ("int4_affine", 1, 11008, 4096), ("int4_affine", 16, 11008, 4096),
+    ("int4_affine", 128, 11008, 4096), ("int4_affine", 4096, 11008, 4096),
+    ("mxfp8_e5m2", 1, 11008, 4096), ("mxfp8_e5m2", 16, 11008, 4096),
+    ("mxfp8_e5m2", 128, 11008, 4096), ("mxfp8_e5m2", 4096, 11008, 4096),
+    ("nvfp8", 1, 11008, 4096), ("nvfp8", 16, 11008, 4096),
+    ("nvfp8", 128, 11008, 4096), ("nvfp8", 4096, 11008, 4096),
+]
+
+
+def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3):
+    import torch
+    nbytes = sizes(fmt, m, n, k)
+    copies = copies_for(nbytes, m)
+    prob = Problem(fmt, m, n, k, copies)
+    g = prob.graph()
+    ms, _ = time_graph(g, steps, warmup, 1)
+    per = ms / copies
+    row = {"fmt": fmt, "M": m, "N": n, "K": k, "us": round(per * 1e3, 2), "copies": copies}
+    gbs = nbytes / (per * 1e-3) / 1e9
+    tfl = prob.flops / (per * 1e-3) / 1e12
+    row["GB/s"] = round(gbs, 1)
+    row["TFLOP/s"] = round(tfl, 2)
+    row["hbm_frac"] = round(gbs / hbm, 4)
+    if m >= 128:
+        fp_peak = {"mxfp8_e4m3": 2 * bf16, "mxfp8_e5m2": 2 * bf16, "nvfp8": 2 * bf16}.get(fmt, 6 * bf16)
+        row["bf16_frac"] = round(tfl / bf16, 4)
+        row["native_peak_frac"] = round(tfl / fp_peak, 4)
+    del prob, g
+    torch.cuda.empty_cache()
+    return row
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    from block_scaled_quantized_spec_gb300 import build
+    build.build()
+    import block_scaled_quantized_spec_gb300 as q
+    q.load()
+    rank, world, local = dist_init(args)
+    hbm, bf16, bf16_sus, kind = peaks()
+
+    fmt, m, n, k = HEADLINE
+    nbytes = sizes(fmt, m, n, k)
+    copies = copies_for(nbytes, m) if args.only is None else 4
+    if args.only:
+        f, mm, nn, kk = args.only.split(":")
+        print(json.dumps(breakdown_row(f, int(mm), int(nn), int(kk), hbm, bf16, kind, args.steps,
+                                       args.warmup)))
+        return
+    prob = Problem(fmt, m, n, k, copies, seed=rank)
+    graph = prob.graph()
+    ms, clk = time_graph(graph, args.steps, args.warmup, world, clocks_index=local)
+    total_bytes = world * copies * nbytes
+    value = total_bytes / (ms * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = measure_e2e(prob, max(3, args.steps // 2), 2)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"mxfp4 decode qGEMV M=1 N=4096 K=4096; a step = {copies} distinct weight "
+                               f"copies, one qmm each ({copies * nbytes / 1e6:.0f} MB > 3x L2)",
+                   "l2": "inputs larger than L2 (rotating weight copies), no flush",
+                   "graph": "each step's launches replayed from one CUDA graph",
+                   "accumulate": "f32"},
+        "roofline": roofline_gemv(prob, ms, hbm, kind),
+        "e2e": {"value": round(world * copies * nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "pinned-host X in, out back, per layer; weights resident"},
+        "gpu_launches": copies * args.steps,
+        "clocks": clk,
+    }
+    del graph, prob
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_breakdown and world == 1:
+        rows = []
+        for (f, mm, nn, kk) in BREAKDOWN:
+            rows.append(breakdown_row(f, mm, nn, kk, hbm, bf16, kind))
+        line["breakdown"] = rows
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(fmt, m, n, k)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,149 @@
+// Device-side element and scale decoders for the block-scaled formats.
+//
+// Two families:
+//  * exact float32 decoders (dequant kernel, float32-activation path): each
+//    code becomes its exact value; products with the block scale round once.
+//  * bf16-pair decoders feeding tensor-core fragments: a 32-bit word of codes
+//    becomes bf16x2 registers holding the *scaled* weights.  Which two codes
+//    share a register is chosen to keep the decode short; callers pair the
+//    activations the same way (any permutation of k that is applied to both
+//    operands leaves a dot product unchanged).
+//
+// Element formats: metaltile-std src/mlx/fp_quantized_mma.rs header ("fp4 E2M1
+// codebook", "fp8 E4M3 dequant"); metaltile PR #250 codec commit (E4M3 with
+// +-448 saturation and no infinity, E5M2 = high byte of an IEEE half, E8M0 =
+// 2^(bits-127)); int4 affine w = scale * q + bias (metaltile-std
+// tests/qmm_gpu_correctness.rs, cpu_qmm_reference).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace qfmt_dev {
+
+enum Fmt { MXFP4 = 1, NVFP4 = 2, MXFP8_E4M3 = 3, MXFP8_E5M2 = 4, NVFP8 = 5, INT4_AFFINE = 6 };
+
+template <int F> struct FmtTraits;
+template <> struct FmtTraits<MXFP4> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 1; };
+template <> struct FmtTraits<NVFP4> { static constexpr bool four = true; static constexpr int block = 16; static constexpr int sbytes = 1; };
+template <> struct FmtTraits<MXFP8_E4M3> { static constexpr bool four = false; static constexpr int block = 32; static constexpr int sbytes = 1; };
+template <> struct FmtTraits<MXFP8_E5M2> { static constexpr bool four = false; static constexpr int block = 32; static constexpr int sbytes = 1; };
+template <> struct FmtTraits<NVFP8> { static constexpr bool four = false; static constexpr int block = 16; static constexpr int sbytes = 4; };
+template <> struct FmtTraits<INT4_AFFINE> { static constexpr bool four = true; static constexpr int block = 64; static constexpr int sbytes = 4; };
+
+// ------------------------------------------------------------------ exact ---
+
+__device__ __forceinline__ float e2m1_f32(uint32_t c) {
+  // magnitude index i = [e1 e0 m]: i = 1 is 0.5 (subnormal), i >= 2 is
+  // 2^(e-1) * (1 + m/2): float32 exponent 126 + e, mantissa msb m.
+  const uint32_t i = c & 7u;
+  const uint32_t mag = i < 2u ? (i ? 0x3F000000u : 0u) : (((126u + (i >> 1)) << 23) | ((i & 1u) << 22));
+  return __uint_as_float(mag | ((c & 8u) << 28));
+}
+
+__device__ __forceinline__ float e4m3_f32(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  float mag;
+  if ((c & 0x7Fu) == 0x7Fu) mag = __uint_as_float(0x7FC00000u);           // the only NaN
+  else if (e == 0u) mag = __fmul_rn(float(m), 0.001953125f);              // m * 2^-9
+  else mag = __uint_as_float(((e + 120u) << 23) | (m << 20));             // 2^(e-7) (1 + m/8)
+  return (c & 0x80u) ? -mag : mag;
+}
+
+__device__ __forceinline__ float e5m2_f32(uint32_t c) {
+  return __half2float(__ushort_as_half((unsigned short)(c << 8)));        // IEEE half high byte
+}
+
+__device__ __forceinline__ float e8m0_f32(uint32_t b) {
+  if (b == 255u) return __uint_as_float(0x7FC00000u);
+  return __uint_as_float(b ? (b << 23) : 0x00400000u);                    // 2^(b-127); b=0 subnormal
+}
+
+__device__ __forceinline__ float bf16bits_f32(uint32_t h) { return __uint_as_float(h << 16); }
+
+// ------------------------------------------------------------ bf16 pairs ---
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_splat(uint32_t h) { return (h & 0xFFFFu) * 0x00010001u; }
+
+// bf16 bits of 2^(b-127) for an E8M0 byte (bf16 shares float32's exponent
+// field): b << 7, with b = 0 the subnormal 2^-127 and b = 255 a NaN.
+__device__ __forceinline__ uint32_t e8m0_bf16(uint32_t b) {
+  return b == 255u ? 0x7FC0u : (b ? (b << 7) : 0x0040u);
+}
+
+// 8 E2M1 codes (code i at bits 4i) -> bf16x2 {c0,c4} {c1,c5} {c2,c6} {c3,c7}.
+// Magnitudes come from two 8-entry byte tables (low and high byte of the bf16
+// value of {0,.5,1,1.5,2,3,4,6}) indexed by prmt; the sign bit of each code is
+// moved to bit 15 / 31 of its half.
+__device__ __forceinline__ void e2m1x8_bf16(uint32_t w, uint32_t r[4]) {
+  const uint32_t LO0 = 0xC0800000u, LO1 = 0xC0804000u;   // low bytes, entries 0-3 and 4-7
+  const uint32_t HI0 = 0x3F3F3F00u, HI1 = 0x40404040u;   // high bytes
+  const uint32_t m = w & 0x77777777u;
+  const uint32_t s1 = prmt(m, 0u, 0x0020u);  // nibbles c0 c1 c4 c5
+  const uint32_t s2 = prmt(m, 0u, 0x0031u);  // nibbles c2 c3 c6 c7
+  const uint32_t l1 = prmt(LO0, LO1, s1), h1 = prmt(HI0, HI1, s1);
+  const uint32_t l2 = prmt(LO0, LO1, s2), h2 = prmt(HI0, HI1, s2);
+  r[0] = prmt(l1, h1, 0x6240u) | ((w << 12) & 0x80008000u);
+  r[1] = prmt(l1, h1, 0x7351u) | ((w << 8) & 0x80008000u);
+  r[2] = prmt(l2, h2, 0x6240u) | ((w << 4) & 0x80008000u);
+  r[3] = prmt(l2, h2, 0x7351u) | (w & 0x80008000u);
+}
+
+// 8 unsigned 4-bit q (int4 affine) -> bf16x2 {q0,q4} {q1,q5} {q2,q6} {q3,q7},
+// each finished as fma(q, scale, bias) in bf16 (one rounding).  0x4300 | q is
+// the bf16 of 128 + q, from which 128 is subtracted exactly.
+__device__ __forceinline__ void int4x8_affine_bf16(uint32_t w, uint32_t s2, uint32_t b2, uint32_t r[4]) {
+  const uint32_t k128 = 0x43004300u;
+  #pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t t = ((w >> (4 * j)) & 0x000F000Fu) | k128;
+    uint32_t q;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(t), "r"(k128));
+    r[j] = hfma2(q, s2, b2);
+  }
+}
+
+// 4 E4M3 codes (code i in byte i) -> bf16x2 {c0,c2} {c1,c3} holding the
+// value times 2^-120: the 7 magnitude bits land in the low exponent and the
+// top mantissa bits of a bf16, which represents every E4M3 value (subnormals
+// included) scaled by 2^(7-127).
+__device__ __forceinline__ void e4m3x4_bf16_raw(uint32_t w, uint32_t r[2]) {
+  r[0] = ((w << 4) & 0x07F007F0u) | ((w << 8) & 0x80008000u);
+  r[1] = ((w >> 4) & 0x07F007F0u) | (w & 0x80008000u);
+}
+
+// 4 E5M2 codes -> bf16x2 {c0,c2} {c1,c3} holding value times 2^-112.
+__device__ __forceinline__ void e5m2x4_bf16_raw(uint32_t w, uint32_t r[2]) {
+  r[0] = ((w << 5) & 0x0FE00FE0u) | ((w << 8) & 0x80008000u);
+  r[1] = ((w >> 3) & 0x0FE00FE0u) | (w & 0x80008000u);
+}
+
+// bf16 bits of 2^e for -133 <= e <= 127.
+__device__ __forceinline__ uint32_t pow2_bf16(int e) {
+  return e >= -126 ? uint32_t(e + 127) << 7 : (0x40u >> (-127 - e));
+}
+
+__device__ __forceinline__ uint32_t f32_to_bf16bits(float f) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+}  // namespace qfmt_dev

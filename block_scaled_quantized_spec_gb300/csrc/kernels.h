@@ -1,0 +1,29 @@
+// Launchers of the device kernels (internal to libqfmt).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qfmt_dev {
+
+// out [N, K] float32 or bf16 <- dequant(codes, scales, glob).
+cudaError_t launch_dequant(int fmt, const void* codes, const void* scales, float glob, void* out,
+                           bool out_bf16, int64_t N, int64_t K, cudaStream_t st, int sms);
+
+// Decode GEMV, 1 <= M <= 16: out [M, N] (bf16 or f32) = X [M, K] bf16 . W^T.
+cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float glob, const void* x,
+                         void* out, bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st,
+                         int sms);
+
+// Float32-activation path (CUDA cores, exact products), any M.
+cudaError_t launch_qmm_f32x(int fmt, const void* codes, const void* scales, float glob,
+                            const float* x, void* out, bool out_f32, int64_t M, int64_t N,
+                            int64_t K, cudaStream_t st, int sms);
+
+// Tensor-core GEMM (tcgen05), M > 16: out [M, N] = X [M, K] bf16 . W^T.
+// Returns cudaErrorNotSupported when the device lacks tcgen05.
+cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, float glob,
+                            const void* x, void* out, bool out_f32, int64_t M, int64_t N,
+                            int64_t K, cudaStream_t st, int sms);
+
+}  // namespace qfmt_dev

@@ -1,0 +1,117 @@
+// extern "C" device entry points of libqfmt: argument validation, kernel
+// selection by batch size, and launch on the caller's stream.
+//
+// Kernel selection (the pages pick kernels by batch size as well: the
+// metaltile qmm selector routes 4 <= m <= 12 to its two-row variant, and the
+// rlx-cpu matmuls switch on m > 1): M <= 16 runs the decode GEMV, M > 16 the
+// tensor-core GEMM, float32 activations the CUDA-core path.
+#include <atomic>
+#include <cmath>
+
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "qfmt_internal.h"
+
+using namespace qfmt;
+
+namespace {
+
+std::atomic<int> g_sms[64];
+
+// SM count of the current device (cached per device).
+int device_sms(int* err) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { *err = fail(QFMT_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e)); return 0; }
+  if (dev < 0 || dev >= 64) { *err = fail(QFMT_ECUDA, "device index %d out of range", dev); return 0; }
+  int v = g_sms[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) { *err = fail(QFMT_ECUDA, "device query: %s", cudaGetErrorString(e)); return 0; }
+  g_sms[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return QFMT_OK;
+  return fail(QFMT_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int check_common(int fmt, const void* codes, const void* scales, float glob, int group) {
+  int st = check_group(fmt, group);
+  if (st) return st;
+  if ((st = check_ptr(codes, 16, "codes"))) return st;
+  if ((st = check_ptr(scales, 4, "scales"))) return st;
+  if (fmt == QFMT_NVFP4 && !(std::isfinite(glob) && glob > 0.0f))
+    return fail(QFMT_EINVAL, "nvfp4 global_scale must be finite and > 0");
+  return QFMT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qfmt_dequant(int fmt, const void* codes, const void* scales, float global_scale, void* out,
+                 int out_dtype, int64_t N, int64_t K, int group, void* stream) {
+  clear_error();
+  int st = check_group(fmt, group);
+  if (st) return st;
+  if ((st = check_shape(fmt, 0, N, K))) return st;
+  if (out_dtype != QFMT_F32 && out_dtype != QFMT_BF16) return fail(QFMT_EINVAL, "bad out_dtype %d", out_dtype);
+  if (N == 0 || K == 0) return QFMT_OK;
+  if ((st = check_common(fmt, codes, scales, global_scale, group))) return st;
+  if ((st = check_ptr(out, 16, "out"))) return st;
+  int err = QFMT_OK;
+  const int sms = device_sms(&err);
+  if (err) return err;
+  return cuda_status(qfmt_dev::launch_dequant(fmt, codes, scales, global_scale, out, out_dtype == QFMT_BF16,
+                                              N, K, static_cast<cudaStream_t>(stream), sms),
+                     "dequant launch");
+}
+
+int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale, const void* x, int x_dtype,
+           void* out, int out_dtype, int64_t M, int64_t N, int64_t K, int group, void* workspace,
+           size_t workspace_bytes, void* stream) {
+  clear_error();
+  (void)workspace;
+  (void)workspace_bytes;
+  int st = check_group(fmt, group);
+  if (st) return st;
+  if ((st = check_shape(fmt, M, N, K))) return st;
+  if (x_dtype != QFMT_F32 && x_dtype != QFMT_BF16) return fail(QFMT_EINVAL, "bad x_dtype %d", x_dtype);
+  if (out_dtype != QFMT_F32 && out_dtype != QFMT_BF16) return fail(QFMT_EINVAL, "bad out_dtype %d", out_dtype);
+  if (M == 0 || N == 0) return QFMT_OK;
+  if ((st = check_ptr(out, 16, "out"))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool out_f32 = out_dtype == QFMT_F32;
+  if (K == 0)
+    return cuda_status(cudaMemsetAsync(out, 0, size_t(M) * size_t(N) * (out_f32 ? 4 : 2), s), "memset");
+  if ((st = check_common(fmt, codes, scales, global_scale, group))) return st;
+  if ((st = check_ptr(x, 16, "x"))) return st;
+  int err = QFMT_OK;
+  const int sms = device_sms(&err);
+  if (err) return err;
+  if (x_dtype == QFMT_F32)
+    return cuda_status(qfmt_dev::launch_qmm_f32x(fmt, codes, scales, global_scale, static_cast<const float*>(x),
+                                                 out, out_f32, M, N, K, s, sms),
+                       "qmm (f32 activations) launch");
+  if (M <= 16)
+    return cuda_status(qfmt_dev::launch_qgemv(fmt, codes, scales, global_scale, x, out, out_f32, M, N, K, s, sms),
+                       "qgemv launch");
+  return cuda_status(qfmt_dev::launch_qgemm_tc(fmt, codes, scales, global_scale, x, out, out_f32, M, N, K, s, sms),
+                     "qgemm launch");
+}
+
+int qmm(int fmt, const void* codes, const void* scales, float global_scale, const void* x, void* out,
+        int64_t M, int64_t N, int64_t K, int group, void* stream) {
+  return qmm_ex(fmt, codes, scales, global_scale, x, QFMT_BF16, out, QFMT_BF16, M, N, K, group, nullptr, 0,
+                stream);
+}
+
+size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K) {
+  (void)fmt; (void)M; (void)N; (void)K;
+  return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,307 @@
+// Host side of libqfmt: element/scale encoders, the weight packer, byte-size
+// queries and the per-thread error message.
+//
+// Built with -ffp-contract=off: every float operation rounds once, so the
+// packer gives the same bytes on x86-64 and aarch64.
+//
+// The packer follows metaltile PR #250 (commit "Foundation for the
+// spec-conformant nvfp4/mxfp4/mxfp8/nvfp8 formats": per-block amax scaling
+// along K, a two-level FP32 global for nvfp4, codes quantized against the
+// effective post-encode scale) and rlx-cpu thunk/ops/quant.rs
+// (lowp_compute_scales: scale = amax / max_finite, 1.0 for an all-zero
+// block; lowp_snap_scale; lowp_quantize: code = encode(x / s), 0 if s == 0).
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "qfmt_internal.h"
+
+namespace qfmt {
+
+static thread_local char g_err[512];
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+void clear_error() { g_err[0] = '\0'; }
+
+bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_INT4_AFFINE; }
+
+int block_of(int fmt) {
+  switch (fmt) {
+    case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: return 32;
+    case QFMT_NVFP4: case QFMT_NVFP8: return 16;
+    case QFMT_INT4_AFFINE: return 64;
+    default: return 0;
+  }
+}
+
+bool is_4bit(int fmt) { return fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4 || fmt == QFMT_INT4_AFFINE; }
+
+int scale_entry_bytes(int fmt) { return (fmt == QFMT_NVFP8 || fmt == QFMT_INT4_AFFINE) ? 4 : 1; }
+
+int check_group(int fmt, int group) {
+  if (!valid_format(fmt)) return fail(QFMT_EINVAL, "unknown format %d", fmt);
+  if (group != 0 && group != block_of(fmt))
+    return fail(QFMT_EUNSUPPORTED, "group %d not supported for format %d (block %d)", group, fmt,
+                block_of(fmt));
+  return QFMT_OK;
+}
+
+int check_shape(int fmt, int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return fail(QFMT_ESHAPE, "negative size M=%lld N=%lld K=%lld",
+                                           (long long)M, (long long)N, (long long)K);
+  const int kq = fmt == QFMT_INT4_AFFINE ? 64 : 32;
+  if (K % kq) return fail(QFMT_ESHAPE, "K=%lld must be a multiple of %d", (long long)K, kq);
+  if (N > (int64_t(1) << 31) || M > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+    return fail(QFMT_ESHAPE, "size above 2^31");
+  return QFMT_OK;
+}
+
+int check_ptr(const void* p, int align, const char* what) {
+  if (!p) return fail(QFMT_EINVAL, "%s is NULL", what);
+  if (reinterpret_cast<uintptr_t>(p) % align)
+    return fail(QFMT_EALIGN, "%s not %d-byte aligned", what, align);
+  return QFMT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Element encoders.
+// ---------------------------------------------------------------------------
+
+// Round-to-nearest-even into a minifloat with `mbits` mantissa bits and
+// exponent bias `bias`, saturating to `max_code` (magnitude code of the largest
+// finite value `max_val`).  The quantum of the binade holding |v| (the
+// min-normal binade for subnormals) divides |v| exactly, nearbyintf rounds
+// ties to even, and the code is (biased exponent << mbits) + (n - 2^mbits):
+// a mantissa carry moves into the next exponent by itself, and in the
+// subnormal binade the same expression yields the subnormal code n.
+static uint32_t encode_minifloat(float v, int mbits, int bias, uint32_t max_code, float max_val,
+                                 uint32_t sign_bit) {
+  const uint32_t sign = std::signbit(v) ? sign_bit : 0u;
+  const float a = std::fabs(v);
+  if (!(a < max_val)) return max_code | sign;
+  const int min_exp = 1 - bias;
+  int e = min_exp;
+  if (a >= std::ldexp(1.0f, min_exp)) {
+    int ex;
+    std::frexp(a, &ex);  // a = f * 2^ex, f in [0.5, 1)
+    e = ex - 1;
+  }
+  const float n = std::nearbyint(a / std::ldexp(1.0f, e - mbits));
+  const uint32_t code = (uint32_t(e + bias) << mbits) + uint32_t(n) - (1u << mbits);
+  return std::min(code, max_code) | sign;
+}
+
+static inline uint32_t enc_e2m1(float v) { return encode_minifloat(v, 1, 1, 0x7, 6.0f, 0x8); }
+static inline uint32_t enc_e4m3(float v) { return encode_minifloat(v, 3, 7, 0x7E, 448.0f, 0x80); }
+static inline uint32_t enc_e5m2(float v) { return encode_minifloat(v, 2, 15, 0x7B, 57344.0f, 0x80); }
+
+static inline uint32_t f32_bits(float f) { uint32_t u; std::memcpy(&u, &f, 4); return u; }
+static inline float bits_f32(uint32_t u) { float f; std::memcpy(&f, &u, 4); return f; }
+
+// E4M3 decode (exact in float32); the packer never stores the NaN code.
+static float dec_e4m3(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15, m = c & 7;
+  float mag = (e == 0) ? std::ldexp(float(m), -9) : bits_f32(((e + 120u) << 23) | (m << 20));
+  return (c & 0x80) ? -mag : mag;
+}
+
+// E8M0 code of the smallest power of two >= s (finite s > 0): ceil(log2 s)
+// from the float32 fields, clamped to [-127, 127], biased by 127.
+static uint32_t enc_e8m0_ceil(float s) {
+  const uint32_t u = f32_bits(s);
+  const int E = int((u >> 23) & 0xFF);
+  const uint32_t M = u & 0x7FFFFF;
+  int e;
+  if (E != 0) {
+    e = E - 127 + (M != 0);
+  } else {
+    int lg = 0;                                   // ceil(log2 M), M >= 1
+    while ((uint64_t(1) << lg) < M) ++lg;
+    e = lg - 149;
+  }
+  e = std::max(-127, std::min(127, e));
+  return uint32_t(e + 127);
+}
+
+static float dec_e8m0(uint32_t b) {  // b <= 254
+  return b == 0 ? bits_f32(0x00400000u) : bits_f32(b << 23);
+}
+
+// float32 -> bfloat16, nearest with ties to even (finite inputs).
+static uint16_t bf16_rne(float f) {
+  const uint32_t u = f32_bits(f);
+  return uint16_t((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+static float bf16_f32(uint16_t h) { return bits_f32(uint32_t(h) << 16); }
+
+// ---------------------------------------------------------------------------
+// Packer.
+// ---------------------------------------------------------------------------
+
+template <class F>
+static void parallel_rows(int64_t N, F&& body) {
+  unsigned hw = std::max(1u, std::thread::hardware_concurrency());
+  int64_t nt = std::min<int64_t>(hw, std::max<int64_t>(1, N / 64));
+  if (nt <= 1) { body(0, N); return; }
+  std::vector<std::thread> ts;
+  int64_t per = (N + nt - 1) / nt;
+  for (int64_t t = 0; t < nt; ++t) {
+    int64_t r0 = t * per, r1 = std::min(N, r0 + per);
+    if (r0 >= r1) break;
+    ts.emplace_back([&, r0, r1] { body(r0, r1); });
+  }
+  for (auto& t : ts) t.join();
+}
+
+static inline void put_code(uint8_t* row, int64_t k, uint32_t code, bool four_bit) {
+  if (!four_bit) { row[k] = uint8_t(code); return; }
+  if (k & 1) row[k >> 1] |= uint8_t(code << 4);
+  else row[k >> 1] = uint8_t(code & 0xF);
+}
+
+}  // namespace qfmt
+
+using namespace qfmt;
+
+extern "C" {
+
+int qfmt_version(void) { return 100; }
+
+const char* qfmt_last_error(void) { return qfmt::g_err; }
+
+int qfmt_block_size(int fmt) { return block_of(fmt); }
+
+int64_t qfmt_codes_bytes(int fmt, int64_t N, int64_t K) {
+  if (!valid_format(fmt) || check_shape(fmt, 0, N, K) != QFMT_OK) return -1;
+  return is_4bit(fmt) ? N * K / 2 : N * K;
+}
+
+int64_t qfmt_scales_bytes(int fmt, int64_t N, int64_t K) {
+  if (!valid_format(fmt) || check_shape(fmt, 0, N, K) != QFMT_OK) return -1;
+  return N * (K / block_of(fmt)) * scale_entry_bytes(fmt);
+}
+
+int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* codes,
+              void* scales, float* global_scale) {
+  clear_error();
+  int st = check_group(fmt, group);
+  if (st) return st;
+  if ((st = check_shape(fmt, 0, N, K))) return st;
+  if (N * K > 0 && (!W || !codes || !scales))
+    return fail(QFMT_EINVAL, "NULL buffer");
+  if (!global_scale) return fail(QFMT_EINVAL, "global_scale is NULL");
+  *global_scale = 1.0f;
+  if (N == 0 || K == 0) return QFMT_OK;
+
+  const int blk = block_of(fmt);
+  const int64_t nb = K / blk;
+  const bool four = is_4bit(fmt);
+  const int64_t row_bytes = four ? K / 2 : K;
+  uint8_t* cb = static_cast<uint8_t*>(codes);
+  uint8_t* sb = static_cast<uint8_t*>(scales);
+
+  // Reject NaN/Inf weights up front (the block statistics assume finite input).
+  std::atomic<bool> bad{false};
+  parallel_rows(N, [&](int64_t r0, int64_t r1) {
+    for (int64_t i = r0 * K; i < r1 * K && !bad.load(std::memory_order_relaxed); ++i)
+      if (!std::isfinite(W[i])) bad = true;
+  });
+  if (bad) return fail(QFMT_ENONFINITE, "weights contain NaN or Inf");
+
+  float glob = 1.0f;
+  if (fmt == QFMT_NVFP4) {
+    std::vector<float> part(std::max<unsigned>(1, std::thread::hardware_concurrency()) * 4, 0.0f);
+    std::atomic<int> slot{0};
+    parallel_rows(N, [&](int64_t r0, int64_t r1) {
+      float m = 0.0f;
+      for (int64_t i = r0 * K; i < r1 * K; ++i) m = std::max(m, std::fabs(W[i]));
+      part[slot++] = m;
+    });
+    float amax_t = 0.0f;
+    for (float m : part) amax_t = std::max(amax_t, m);
+    glob = amax_t > 0.0f ? amax_t / 2688.0f : 1.0f;  // 2688 = 6 * 448
+  }
+
+  parallel_rows(N, [&](int64_t r0, int64_t r1) {
+    for (int64_t n = r0; n < r1; ++n) {
+      const float* w = W + n * K;
+      uint8_t* crow = cb + n * row_bytes;
+      for (int64_t b = 0; b < nb; ++b) {
+        const float* wb = w + b * blk;
+        if (fmt == QFMT_INT4_AFFINE) {
+          float mn = wb[0], mx = wb[0];
+          for (int j = 1; j < blk; ++j) { mn = std::min(mn, wb[j]); mx = std::max(mx, wb[j]); }
+          float s = (mx - mn) / 15.0f;
+          if (s == 0.0f) s = 1.0f;
+          if (!std::isfinite(s)) { bad = true; continue; }
+          const uint16_t sh = bf16_rne(s), bh = bf16_rne(mn);
+          const float sf = bf16_f32(sh), bfv = bf16_f32(bh);
+          uint16_t* pr = reinterpret_cast<uint16_t*>(sb + (n * nb + b) * 4);
+          pr[0] = sh;
+          pr[1] = bh;
+          for (int j = 0; j < blk; ++j) {
+            uint32_t q = 0;
+            if (sf != 0.0f) {
+              float v = std::round((wb[j] - bfv) / sf);
+              q = uint32_t(std::max(0.0f, std::min(15.0f, v)));
+            }
+            put_code(crow, b * blk + j, q, true);
+          }
+          continue;
+        }
+        float amax = 0.0f;
+        for (int j = 0; j < blk; ++j) amax = std::max(amax, std::fabs(wb[j]));
+        float eff;
+        switch (fmt) {
+          case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: {
+            const float maxf = fmt == QFMT_MXFP4 ? 6.0f : (fmt == QFMT_MXFP8_E4M3 ? 448.0f : 57344.0f);
+            const float s = amax > 0.0f ? amax / maxf : 1.0f;
+            const uint32_t code = enc_e8m0_ceil(s);
+            sb[n * nb + b] = uint8_t(code);
+            eff = dec_e8m0(code);
+            break;
+          }
+          case QFMT_NVFP4: {
+            const uint32_t u = amax > 0.0f ? enc_e4m3((amax / 6.0f) / glob) : 0x38u;
+            sb[n * nb + b] = uint8_t(u);
+            eff = dec_e4m3(u) * glob;
+            break;
+          }
+          default: {  // QFMT_NVFP8
+            const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+            std::memcpy(sb + (n * nb + b) * 4, &s, 4);
+            eff = s;
+            break;
+          }
+        }
+        if (!std::isfinite(eff)) { bad = true; continue; }
+        for (int j = 0; j < blk; ++j) {
+          uint32_t code = 0;
+          if (eff != 0.0f) {
+            const float v = wb[j] / eff;
+            code = fmt == QFMT_MXFP8_E5M2 ? enc_e5m2(v)
+                 : (fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4) ? enc_e2m1(v) : enc_e4m3(v);
+          }
+          put_code(crow, b * blk + j, code, four);
+        }
+      }
+    }
+  });
+  if (bad) return fail(QFMT_ENONFINITE, "a block scale overflows float32");
+  *global_scale = glob;
+  return QFMT_OK;
+}
+
+}  // extern "C"

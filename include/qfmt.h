@@ -1,0 +1,151 @@
+/*
+ * qfmt.h -- C ABI of libqfmt: block-scaled weight formats and the fused
+ * dequantizing matmul  out[M,N] = X[M,K] . dequant(W[N,K])^T  on one GB300 GPU.
+ *
+ * Formats (metaltile PR #250, "spec-conformant nvfp4/mxfp4/mxfp8/nvfp8"
+ * format list and codec commit; metaltile-std tests/qmm_gpu_correctness.rs
+ * for the MLX-style int4 affine format):
+ *
+ *   fmt                 element            block  scale per block
+ *   QFMT_MXFP4          E2M1 (4-bit)       32     E8M0 byte, 2^(b-127)
+ *   QFMT_NVFP4          E2M1 (4-bit)       16     E4M3 byte x one FP32 global
+ *   QFMT_MXFP8_E4M3     E4M3 (8-bit)       32     E8M0 byte
+ *   QFMT_MXFP8_E5M2     E5M2 (8-bit)       32     E8M0 byte
+ *   QFMT_NVFP8          E4M3 (8-bit)       16     FP32 (4 bytes)
+ *   QFMT_INT4_AFFINE    unsigned 4-bit q   64     bf16 scale + bf16 bias (4 bytes)
+ *
+ * Memory layouts (all row-major, no padding, little-endian):
+ *   codes   [N, K/2] bytes for 4-bit formats: element k of a row sits in byte
+ *           k/2, low nibble for even k (LSB-first; 8 codes per u32 word);
+ *           [N, K] bytes for 8-bit formats.
+ *   scales  [N, K/block] entries of the sizes above; int4 affine stores the
+ *           (scale, bias) bf16 pair of each group adjacently: [N, K/64, 2].
+ *   X       [M, K] bf16 (or f32 through qmm_ex), out [M, N] bf16 (or f32).
+ *
+ * Element values: E2M1 {0,.5,1,1.5,2,3,4,6} with sign bit 3; E4M3 bias 7,
+ * subnormal m*2^-9, only S.1111.111 is NaN (max 448, no infinity); E5M2 is
+ * the high byte of an IEEE half; E8M0 code b is 2^(b-127) (b = 0 gives the
+ * float32 subnormal 2^-127, b = 255 NaN).
+ *
+ * Ownership and synchronisation: the caller allocates and frees every
+ * buffer.  qfmt_pack works on host memory and is synchronous.  qfmt_dequant,
+ * qmm and qmm_ex take device pointers, enqueue work on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream) and return without
+ * waiting; their status reports argument and launch errors only.  The
+ * library keeps no handle and allocates no device memory; the only global
+ * state is a per-thread error message.
+ *
+ * Errors: every function returns a qfmt_status (or a size; see each), never
+ * aborts and never throws.  qfmt_last_error() describes the last failure on
+ * the calling thread.
+ */
+#ifndef QFMT_H
+#define QFMT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QFMT_MXFP4 = 1,
+  QFMT_NVFP4 = 2,
+  QFMT_MXFP8_E4M3 = 3,
+  QFMT_MXFP8_E5M2 = 4,
+  QFMT_NVFP8 = 5,
+  QFMT_INT4_AFFINE = 6
+} qfmt_format;
+
+typedef enum { QFMT_F32 = 0, QFMT_BF16 = 1 } qfmt_dtype;
+
+typedef enum {
+  QFMT_OK = 0,
+  QFMT_EINVAL = -1,        /* unknown format/dtype, NULL pointer, bad global scale */
+  QFMT_ESHAPE = -2,        /* negative size, or K not a multiple of 32 (64 for int4 affine) */
+  QFMT_EALIGN = -3,        /* a device pointer not 16-byte aligned (scales: 4-byte) */
+  QFMT_EUNSUPPORTED = -4,  /* a group size other than the format's block */
+  QFMT_ECUDA = -5,         /* a CUDA launch or device query failed */
+  QFMT_ENONFINITE = -7,    /* qfmt_pack: NaN/Inf weight, or a block scale overflowing float32 */
+  QFMT_ENOSPACE = -8       /* a caller workspace smaller than qmm_workspace_bytes() */
+} qfmt_status;
+
+/* Block (group) size of a format along K: 32, 16, 32, 32, 16, 64; 0 for an
+ * unknown format. */
+int qfmt_block_size(int fmt);
+
+/* Bytes of the codes / scales buffers for an [N, K] weight; -1 on a bad
+ * format or shape (see QFMT_ESHAPE). */
+int64_t qfmt_codes_bytes(int fmt, int64_t N, int64_t K);
+int64_t qfmt_scales_bytes(int fmt, int64_t N, int64_t K);
+
+/*
+ * qfmt_pack -- host packer: float32 W [N, K] (host) -> codes, scales (host
+ * buffers of the sizes above) and *global_scale (nvfp4; 1.0f otherwise).
+ * Per row and block along K (metaltile PR #250, commit "Foundation for the
+ * spec-conformant ... formats"; rlx-cpu thunk/ops/quant.rs
+ * lowp_compute_scales / lowp_snap_scale / lowp_quantize):
+ *   amax -> raw scale amax/max_finite (1.0 for an all-zero block) -> snapped
+ *   stored scale (E8M0 = the smallest power of two >= the raw scale; nvfp4:
+ *   global = amax(W)/2688, micro = E4M3(amax_b/6/global); nvfp8: float32)
+ *   -> codes = encode(w / effective scale), round to nearest, ties to the
+ *   even code, saturating to the largest finite value.  int4 affine: scale =
+ *   bf16((max-min)/15), bias = bf16(min), q = clamp(round_half_away((w-bias)/
+ *   scale), 0, 15).  All arithmetic is float32 with one rounding per op.
+ * `group` must be 0 (format default) or the format's block.  Returns
+ * QFMT_ENONFINITE on NaN/Inf weights.  Multi-threaded, synchronous.
+ */
+int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group,
+              void* codes, void* scales, float* global_scale);
+
+/*
+ * qfmt_dequant -- device: out[n,k] = dequant(W)[n,k] for all N*K elements
+ * (metaltile PR #250, standalone dequant kernels: out[i] =
+ * elem(code) * scale(block)).  out_dtype QFMT_F32 is bit-exact: the exact
+ * value elem * scale (nvfp4: (e2m1 * e4m3) * global; int4 affine:
+ * fmaf(scale, q, bias)) rounded once to float32, subnormals kept, overflow
+ * to +-inf.  QFMT_BF16 rounds that float32 to bf16 (nearest even).
+ * codes/out 16-byte aligned, scales 4-byte aligned.
+ */
+int qfmt_dequant(int fmt, const void* codes, const void* scales, float global_scale,
+                 void* out, int out_dtype, int64_t N, int64_t K, int group,
+                 void* stream);
+
+/*
+ * qmm -- device: out[M,N] (bf16) = X[M,K] (bf16) . dequant(W[N,K])^T with
+ * float32 accumulation (metaltile PR #250 qgemv/qmm/qmm-MMA commits:
+ * output[m,n] = sum_k dequant(weight[n,k]) * x[m,k]; rlx-cpu
+ * dequant_matmul_nvfp4 for the nvfp4 value).  M <= 16 runs the
+ * HBM-streaming decode GEMV; larger M the tensor-core GEMM.  Result within
+ * 2e-3 * sum_k |x||w| + 1e-6 of the exact value.  M == 0 or N == 0 is a
+ * no-op; K == 0 writes zeros.  No workspace is needed.
+ */
+int qmm(int fmt, const void* codes, const void* scales, float global_scale,
+        const void* x, void* out, int64_t M, int64_t N, int64_t K, int group,
+        void* stream);
+
+/*
+ * qmm_ex -- qmm with explicit activation and output dtypes (QFMT_BF16 or
+ * QFMT_F32 each).  A float32 X takes a CUDA-core float32 path (exact
+ * products, float32 accumulation) at any M.  workspace/workspace_bytes are
+ * reserved: pass NULL/0 (qmm_workspace_bytes() returns 0).
+ */
+int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale,
+           const void* x, int x_dtype, void* out, int out_dtype,
+           int64_t M, int64_t N, int64_t K, int group,
+           void* workspace, size_t workspace_bytes, void* stream);
+
+size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
+
+/* Human-readable description of the last failure on this thread ("" if none). */
+const char* qfmt_last_error(void);
+
+/* ABI version (major * 100 + minor). */
+int qfmt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QFMT_H */

@@ -1,0 +1,162 @@
+"""CPU tests of libqfmt: it loads, exports every symbol the header declares, its
+host packer matches the oracle byte for byte, and argument validation
+rejects bad calls before any device work (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import block_scaled_quantized_spec_gb300 as q
+from block_scaled_quantized_spec_gb300 import synth
+from oracle import pack as opack
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qfmt.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_scaled_quantized_spec_gb300 import build
+    build.build()
+    return q.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    for must in ("qfmt_pack", "qfmt_dequant", "qmm", "qmm_ex", "qfmt_last_error", "qfmt_codes_bytes",
+                 "qfmt_scales_bytes", "qfmt_block_size", "qmm_workspace_bytes", "qfmt_version"):
+        assert must in names, must
+
+
+def test_library_exports_every_declared_symbol(lib):
+    cdll = ctypes.CDLL(q.lib_path())
+    for name in _declared_functions():
+        assert hasattr(cdll, name), name
+    assert q.qfmt_version() >= 100
+
+
+def test_sizes_and_blocks(lib):
+    for name, f in q.FORMATS.items():
+        assert q.qfmt_block_size(name) == opack.BLOCK[name]
+        assert q.qfmt_codes_bytes(name, 7, 256) == opack.codes_nbytes(name, 7, 256)
+        assert q.qfmt_scales_bytes(name, 7, 256) == opack.scales_nbytes(name, 7, 256)
+    assert q.qfmt_block_size(99) == 0
+    assert q.qfmt_codes_bytes("mxfp4", 4, 48) == -1           # K not a multiple of 32
+    assert q.qfmt_codes_bytes("int4_affine", 4, 96) == -1     # K not a multiple of 64
+
+
+CASES = [
+    (16, 512, 0, 0.02, False),
+    (37, 1024, 1, 0.02, True),
+    (8, 256, 2, 1e-20, False),      # tiny weights: subnormal scales / codes
+    (8, 256, 3, 3e3, False),        # large weights
+    (4, 2048, 4, 0.02, True),
+]
+
+
+@pytest.mark.parametrize("fmt", list(q.FORMATS))
+@pytest.mark.parametrize("n,k,seed,std,outl", CASES)
+def test_host_pack_matches_oracle_bytes(lib, fmt, n, k, seed, std, outl):
+    w = synth.weights(n, k, seed=seed, std=std, outliers=outl)
+    c_lib, s_lib, g_lib = q.qfmt_pack(fmt, w)
+    c_or, s_or, g_or = opack.pack(fmt, w)
+    assert np.array_equal(c_lib, c_or), fmt
+    assert np.array_equal(s_lib, s_or), fmt
+    assert np.float32(g_lib) == g_or
+
+
+@pytest.mark.parametrize("fmt", list(q.FORMATS))
+def test_host_pack_special_blocks(lib, fmt):
+    n, k = 6, 256
+    w = synth.weights(n, k, seed=9)
+    w[0] = 0.0                                  # all-zero row
+    w[1, :64] = 0.0                             # zero blocks
+    w[2, 5] = -0.0
+    w[3, :] = np.float32(1e-40)                 # subnormal weights
+    w[4, 0] = np.float32(5.0e4)                 # a block with a large maximum
+    w[5, ::2] = -w[5, 1::2]                     # exact ties in magnitude
+    c_lib, s_lib, g_lib = q.qfmt_pack(fmt, w)
+    c_or, s_or, g_or = opack.pack(fmt, w)
+    assert np.array_equal(c_lib, c_or) and np.array_equal(s_lib, s_or) and np.float32(g_lib) == g_or
+
+
+def test_host_pack_exhaustive_midpoints(lib):
+    # Every representable value and midpoint of each element grid, placed in a
+    # block whose amax pins the scale to 1: the library's arithmetic encoder and
+    # the oracle's table search must agree on every tie and on saturation.
+    from oracle import codec
+    for fmt, table, maxf in (("mxfp4", codec.E2M1_TABLE[:8], 6.0),
+                             ("mxfp8_e4m3", codec.E4M3_TABLE[:127], 448.0),
+                             ("mxfp8_e5m2", codec.E5M2_TABLE[:124], 57344.0)):
+        vals = np.sort(table[np.isfinite(table)])
+        mids = (vals[:-1] + vals[1:]) / 2
+        probes = np.concatenate([vals, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                                 np.nextafter(mids.astype(np.float32), np.float32(1e9))]).astype(np.float32)
+        probes = np.concatenate([probes, -probes])
+        blocks = -(-len(probes) // 31)
+        w = np.zeros((blocks, 32), np.float32)
+        w[:, 0] = maxf
+        w[:, 1:].reshape(-1)[:len(probes)] = probes
+        w = w.reshape(1, -1)
+        c_lib, s_lib, _ = q.qfmt_pack(fmt, w)
+        c_or, s_or, _ = opack.pack(fmt, w)
+        assert (s_or == 127).all()
+        assert np.array_equal(c_lib, c_or), fmt
+        assert np.array_equal(s_lib, s_or), fmt
+
+
+def test_host_pack_rejects_bad_input(lib):
+    with pytest.raises(q.QfmtError) as e:
+        q.qfmt_pack("mxfp4", np.full((2, 32), np.inf, np.float32))
+    assert e.value.status == -7
+    with pytest.raises(q.QfmtError) as e:
+        q.qfmt_pack("mxfp4", np.zeros((2, 32), np.float32), group=16)
+    assert e.value.status == -4
+    with pytest.raises(q.QfmtError):
+        q.qfmt_pack(42, np.zeros((2, 32), np.float32))
+    with pytest.raises(q.QfmtError):
+        q.qfmt_pack("nvfp4", np.zeros((2, 40), np.float32))
+
+
+def _call_qmm(lib, **kw):
+    a = dict(fmt=1, codes=0x1000, scales=0x1000, g=1.0, x=0x1000, xd=1, out=0x1000, od=1,
+             M=4, N=4, K=64, group=0)
+    a.update(kw)
+    return lib.qmm_ex(a["fmt"], a["codes"], a["scales"], a["g"], a["x"], a["xd"], a["out"], a["od"],
+                      a["M"], a["N"], a["K"], a["group"], None, 0, None)
+
+
+def test_device_entry_validation_without_gpu(lib):
+    # each of these fails in host-side validation, before any CUDA call
+    assert _call_qmm(lib, fmt=0) == -1
+    assert _call_qmm(lib, fmt=7) == -1
+    assert _call_qmm(lib, K=48) == -2
+    assert _call_qmm(lib, M=-1) == -2
+    assert _call_qmm(lib, group=64) == -4
+    assert _call_qmm(lib, xd=5) == -1
+    assert _call_qmm(lib, od=9) == -1
+    assert _call_qmm(lib, codes=0x1008) == -3
+    assert _call_qmm(lib, x=0x1004) == -3
+    assert _call_qmm(lib, out=0x1002) == -3
+    assert _call_qmm(lib, scales=0x1002) == -3
+    assert _call_qmm(lib, codes=None) == -1
+    assert _call_qmm(lib, fmt=2, g=0.0) == -1
+    assert _call_qmm(lib, fmt=2, g=float("nan")) == -1
+    assert _call_qmm(lib, fmt=6, K=96) == -2
+    assert b"multiple" in lib.qfmt_last_error()
+    # empty problems are legal no-ops
+    assert _call_qmm(lib, M=0) == 0
+    assert _call_qmm(lib, N=0) == 0
+    assert lib.qfmt_dequant(1, None, None, 1.0, None, 0, 0, 64, 0, None) == 0
+    assert lib.qfmt_dequant(1, 0x1000, 0x1000, 1.0, 0x1000, 3, 4, 64, 0, None) == -1
+    assert lib.qfmt_dequant(1, 0x1000, 0x1000, 1.0, 0x1004, 0, 4, 64, 0, None) == -3
+    assert lib.qmm_workspace_bytes(1, 16, 16, 64) == 0

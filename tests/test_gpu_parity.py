@@ -1,0 +1,258 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+* dequant: bit-exact float32 (u32 patterns; any NaN matches any NaN).
+* qmm: |out - ref| <= 2e-3 * sum_k |x||w| + 1e-6 elementwise, ref the exact
+  float64 dequant-then-dot, plus the bf16 rounding of the stored output
+  (half an ulp of bf16: 2^-9 * |out|).
+Inputs: seeded synthetic weights packed by the oracle's packer (so no oracle
+input comes from the library), bf16 activations from the shared generator.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import block_scaled_quantized_spec_gb300 as q  # noqa: E402
+from block_scaled_quantized_spec_gb300 import synth  # noqa: E402
+from oracle import pack as opack  # noqa: E402
+from oracle import reference as oref  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+FMTS = list(q.FORMATS)
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_scaled_quantized_spec_gb300 import build
+    build.build()
+    q.load()
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _packed(fmt, n, k, seed, std=0.02):
+    w = synth.weights(n, k, seed=seed, std=std, outliers=(fmt == "nvfp4"))
+    return opack.pack(fmt, w)
+
+
+def _x(m, k, seed):
+    xb = synth.activations_bf16(m, k, seed=seed)
+    xt = _dev(xb.view(np.int16)).view(torch.bfloat16)
+    return xb, xt
+
+
+def _check_qmm(out_t, ref, bound, what):
+    out = out_t.float().cpu().numpy().astype(np.float64)
+    extra = np.abs(out) * 2.0 ** -9 if out_t.dtype == torch.bfloat16 else 0.0
+    err = np.abs(out - ref)
+    ok = err <= bound + extra
+    assert np.isfinite(out).all(), what
+    assert ok.all(), (what, float((err / bound).max()), np.argwhere(~ok)[:5].tolist())
+    return float((err / bound).max())
+
+
+# ------------------------------------------------------------------ dequant ---
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k", [(1, 64), (67, 512), (256, 2048)])
+def test_dequant_bit_exact(fmt, n, k):
+    c, s, g = _packed(fmt, n, k, seed=n + k)
+    want = oref.dequant_f32(fmt, c, s, g, n, k)
+    got = q.qfmt_dequant(fmt, _dev(c), _dev(s), g, n, k).cpu().numpy()
+    wb, gb = want.view(np.uint32), got.view(np.uint32)
+    same = (wb == gb) | (np.isnan(want) & np.isnan(got))
+    assert same.all(), (fmt, np.argwhere(~same)[:5].tolist())
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_dequant_all_codes_and_scales(fmt):
+    # every code byte against every scale class, including special values the
+    # packer never emits (NaN/Inf element codes, E8M0 0 and 255, subnormals)
+    rng = np.random.default_rng(5)
+    n, k = 64, 512
+    cb = opack.codes_nbytes(fmt, n, k)
+    codes = np.tile(np.arange(256, dtype=np.uint8), cb // 256 + 1)[:cb].reshape(n, -1)
+    sb = opack.scales_nbytes(fmt, n, k)
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp4"):
+        scales = np.tile(np.arange(256, dtype=np.uint8), sb // 256 + 1)[:sb]
+    elif fmt == "nvfp8":
+        scales = np.concatenate([rng.standard_normal(sb // 4 - 4).astype(np.float32),
+                                 np.array([1e-40, 3e38, 0.0, -2.5], np.float32)]).view(np.uint8)
+    else:
+        sc = synth.f32_to_bf16_bits(rng.standard_normal(sb // 2).astype(np.float32) * 1e-2)
+        scales = sc.view(np.uint8)
+    scales = scales.reshape(n, -1)
+    g = 0.75
+    want = oref.dequant_f32(fmt, codes, scales, g, n, k)
+    got = q.qfmt_dequant(fmt, _dev(codes), _dev(scales), g, n, k).cpu().numpy()
+    same = (want.view(np.uint32) == got.view(np.uint32)) | (np.isnan(want) & np.isnan(got))
+    assert same.all(), (fmt, np.argwhere(~same)[:5].tolist())
+
+
+def test_dequant_bf16_output_is_rounded_f32():
+    fmt, n, k = "nvfp8", 32, 256
+    c, s, g = _packed(fmt, n, k, seed=3)
+    want = synth.f32_to_bf16_bits(oref.dequant_f32(fmt, c, s, g, n, k))
+    got = q.qfmt_dequant(fmt, _dev(c), _dev(s), g, n, k, out_dtype=torch.bfloat16)
+    assert np.array_equal(got.view(torch.int16).cpu().numpy().view(np.uint16), want)
+
+
+# ---------------------------------------------------------------------- qmm ---
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("m", [1, 2, 5, 8, 9, 16])
+def test_qgemv_parity(fmt, m):
+    n, k = 200, 1024                       # 12.5 row tiles (ragged), several K chunks per warp
+    c, s, g = _packed(fmt, n, k, seed=m)
+    xb, xt = _x(m, k, seed=100 + m)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, m))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("m", [17, 64, 130, 256])
+def test_qgemm_parity(fmt, m):
+    n, k = 272, 1024
+    c, s, g = _packed(fmt, n, k, seed=m)
+    xb, xt = _x(m, k, seed=200 + m)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, m))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_short_and_odd_k(fmt):
+    # K of one block quantum and a K that leaves a partial chunk per warp
+    for k in ((64, 192) if fmt == "int4_affine" else (32, 96, 160)):
+        n, m = 33, 3
+        c, s, g = _packed(fmt, n, k, seed=k)
+        xb, xt = _x(m, k, seed=k + 1)
+        out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+        ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+        _check_qmm(out, ref, bound, (fmt, k))
+
+
+def test_tiny_config_f32_activations():
+    # mxfp4, M=8, N=16, K=512, W ~ N(0, 0.02), X f32 ~ N(0, 1), out f32, seed 0
+    fmt, m, n, k = "mxfp4", 8, 16, 512
+    rng = np.random.default_rng(0)
+    w = synth.weights(n, k, rng=rng)
+    x = synth.activations_f32(m, k, rng=rng)
+    c, s, g = opack.pack(fmt, w)
+    out = q.qmm_ex(fmt, _dev(c), _dev(s), g, _dev(x), n)
+    assert out.dtype == torch.float32
+    ref, bound = oref.qmm_ref(fmt, c, s, g, x, "f32", m, n, k)
+    _check_qmm(out, ref, bound, "tiny")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_f32_activations_all_formats(fmt):
+    m, n, k = 20, 40, 256
+    c, s, g = _packed(fmt, n, k, seed=7)
+    x = synth.activations_f32(m, k, seed=8)
+    out = q.qmm_ex(fmt, _dev(c), _dev(s), g, _dev(x), n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, x, "f32", m, n, k)
+    _check_qmm(out, ref, bound, fmt)
+
+
+def test_gemv_gemm_boundary_agree():
+    # the same rows computed by the M<=16 and M>16 kernels agree within the bound
+    fmt, n, k = "mxfp4", 256, 2048
+    c, s, g = _packed(fmt, n, k, seed=1)
+    xb, xt = _x(17, k, seed=2)
+    o16 = q.qmm(fmt, _dev(c), _dev(s), g, xt[:16].contiguous(), n).float().cpu().numpy()
+    o17 = q.qmm(fmt, _dev(c), _dev(s), g, xt, n).float().cpu().numpy()
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", 17, n, k)
+    assert (np.abs(o16 - o17[:16]) <= 2 * bound[:16] + np.abs(o16) * 2.0 ** -8).all()
+
+
+def test_batch_rows_equal_single_rows():
+    fmt, n, k, m = "nvfp4", 96, 512, 8
+    c, s, g = _packed(fmt, n, k, seed=4)
+    xb, xt = _x(m, k, seed=5)
+    dc, ds = _dev(c), _dev(s)
+    full = q.qmm(fmt, dc, ds, g, xt, n).float().cpu().numpy()
+    for i in range(m):
+        one = q.qmm(fmt, dc, ds, g, xt[i:i + 1].contiguous(), n).float().cpu().numpy()
+        ref, bound = oref.qmm_ref(fmt, c, s, g, xb[i:i + 1], "bf16", 1, n, k)
+        assert (np.abs(one[0] - full[i]) <= 2 * bound[0] + np.abs(one[0]) * 2.0 ** -8).all()
+
+
+def test_empty_and_zero_k():
+    c = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    s = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    x = torch.zeros((0, 64), dtype=torch.bfloat16, device=DEV)
+    out = q.qmm("mxfp4", c, s, 1.0, x, 4)
+    assert out.shape == (0, 4)
+    x2 = torch.zeros((3, 0), dtype=torch.bfloat16, device=DEV)
+    out2 = torch.full((3, 5), 7.0, dtype=torch.bfloat16, device=DEV)
+    q.qmm("mxfp4", c, s, 1.0, x2, 5, out=out2)
+    assert (out2.float() == 0).all()
+
+
+def test_misaligned_device_pointer_rejected():
+    fmt, n, k = "mxfp4", 16, 64
+    c, s, g = _packed(fmt, n, k, seed=1)
+    dc = _dev(np.concatenate([np.zeros(8, np.uint8), c.ravel()]))
+    xb, xt = _x(1, k, seed=1)
+    with pytest.raises(q.QfmtError) as e:
+        q.qmm(fmt, dc[8:], _dev(s), g, xt, n)
+    assert e.value.status == -3
+
+
+# ------------------------------------------------- full-size workloads, sampled
+
+FULL = [
+    ("mxfp4", 1, 4096, 4096, False),
+    ("nvfp4", 1, 14336, 4096, True),
+    ("nvfp4", 8, 14336, 4096, True),
+    ("mxfp8_e4m3", 2048, 4096, 4096, False),
+    ("int4_affine", 1, 11008, 4096, False),
+    ("int4_affine", 16, 11008, 4096, False),
+    ("int4_affine", 128, 11008, 4096, False),
+    ("int4_affine", 4096, 11008, 4096, False),
+    ("mxfp8_e5m2", 1, 11008, 4096, False),
+    ("mxfp8_e5m2", 16, 11008, 4096, False),
+    ("mxfp8_e5m2", 128, 11008, 4096, False),
+    ("mxfp8_e5m2", 4096, 11008, 4096, False),
+    ("nvfp8", 1, 11008, 4096, False),
+    ("nvfp8", 16, 11008, 4096, False),
+    ("nvfp8", 128, 11008, 4096, False),
+    ("nvfp8", 4096, 11008, 4096, False),
+]
+
+
+_PACKED = {}
+
+
+def _full_packed(fmt, n, k, outl):
+    key = (fmt, n, k, outl)
+    if key not in _PACKED:
+        _PACKED.clear()
+        w = synth.weights(n, k, seed=0, outliers=outl)
+        _PACKED[key] = opack.pack(fmt, w)
+    return _PACKED[key]
+
+
+@pytest.mark.parametrize("fmt,m,n,k,outl", FULL)
+def test_full_size_sampled(fmt, m, n, k, outl):
+    # the full workload shapes, in the launch configuration the benchmark times;
+    # the oracle checks 403 sampled outputs (including the corners)
+    c, s, g = _full_packed(fmt, n, k, outl)
+    xb = synth.activations_bf16(m, k, seed=1 + m)
+    xt = _dev(xb.view(np.int16)).view(torch.bfloat16)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n).float().cpu().numpy()
+    assert np.isfinite(out).all()
+    srng = np.random.default_rng(1)
+    rows = np.concatenate([srng.integers(0, m, 400), [0, m - 1, m - 1]])
+    cols = np.concatenate([srng.integers(0, n, 400), [n - 1, 0, n - 1]])
+    ref, bound = oref.qmm_ref_sampled(fmt, c, s, g, xb, "bf16", m, n, k, rows, cols)
+    got = out[rows, cols].astype(np.float64)
+    err = np.abs(got - ref)
+    assert (err <= bound + np.abs(got) * 2.0 ** -9).all(), float((err / bound).max())

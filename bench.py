@@ -136,13 +136,22 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Max of a per-rank float over all ranks (CUDA tensor under NCCL, CPU under gloo)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(per_rank_bytes, per_rank_ms, world):
+    """Whole-job bytes/s: every rank's units over the slowest rank's time (weak scaling)."""
+    total = per_rank_bytes * world
+    slowest = max_over_ranks(per_rank_ms, world)
+    return total / (slowest * 1e-3), slowest
 
 
 class Problem:

@@ -20,13 +20,13 @@ __all__ = [
     "FORMATS", "QfmtError", "load", "lib_path",
     "qfmt_block_size", "qfmt_codes_bytes", "qfmt_scales_bytes",
     "qfmt_pack", "qfmt_dequant", "qmm", "qmm_ex", "qmm_workspace_bytes", "qfmt_last_error",
-    "qfmt_version",
+    "qfmt_version", "qfmt_device_status", "qfmt_debug_set",
 ]
 
 FORMATS = {"mxfp4": 1, "nvfp4": 2, "mxfp8_e4m3": 3, "mxfp8_e5m2": 4, "nvfp8": 5, "int4_affine": 6}
 F32, BF16 = 0, 1
 STATUS = {0: "QFMT_OK", -1: "QFMT_EINVAL", -2: "QFMT_ESHAPE", -3: "QFMT_EALIGN", -4: "QFMT_EUNSUPPORTED",
-          -5: "QFMT_ECUDA", -7: "QFMT_ENONFINITE", -8: "QFMT_ENOSPACE"}
+          -5: "QFMT_ECUDA", -6: "QFMT_ETIMEOUT", -7: "QFMT_ENONFINITE", -8: "QFMT_ENOSPACE"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -60,6 +60,8 @@ _SIGS = {
                               ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                               ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "qmm_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]),
+    "qfmt_device_status": (ctypes.c_int, [ctypes.c_void_p]),
+    "qfmt_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_int64]),
 }
 
 
@@ -115,6 +117,18 @@ def qfmt_version() -> int:
 
 def qfmt_last_error() -> str:
     return load().qfmt_last_error().decode()
+
+
+def qfmt_device_status(stream=None) -> int:
+    """Wait for the stream; return (and clear) the device status: 0 or QFMT_ETIMEOUT (-6)."""
+    st = load().qfmt_device_status(_stream(stream))
+    if st not in (0, -6):
+        _check(st, "qfmt_device_status")
+    return st
+
+
+def qfmt_debug_set(key: int, value: int) -> None:
+    _check(load().qfmt_debug_set(key, value), "qfmt_debug_set")
 
 
 def qfmt_block_size(fmt) -> int:

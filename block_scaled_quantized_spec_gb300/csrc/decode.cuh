@@ -122,6 +122,16 @@ __device__ __forceinline__ void int4x8_affine_bf16(uint32_t w, uint32_t s2, uint
   }
 }
 
+// 8 unsigned 4-bit q -> bf16x2 {128+q0,128+q4} {128+q1,128+q5} {128+q2,128+q6}
+// {128+q3,128+q7}: exact, one logic op per pair (0x4300 | q is bf16 128 + q).
+// Callers remove the 128 offset in float32 with the block's activation sum.
+__device__ __forceinline__ void int4x8_biased_bf16(uint32_t w, uint32_t r[4]) {
+  r[0] = (w & 0x000F000Fu) | 0x43004300u;
+  r[1] = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
+  r[2] = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
+  r[3] = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
+}
+
 // 4 E4M3 codes (code i in byte i) -> bf16x2 {c0,c2} {c1,c3} holding the
 // value times 2^-120: the 7 magnitude bits land in the low exponent and the
 // top mantissa bits of a bf16, which represents every E4M3 value (subnormals
@@ -144,6 +154,136 @@ __device__ __forceinline__ uint32_t pow2_bf16(int e) {
 
 __device__ __forceinline__ uint32_t f32_to_bf16bits(float f) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// ------------------------------------------------------ 16-byte pieces ---
+// A piece is 16 bytes of one row's codes: 32 four-bit or 16 eight-bit codes,
+// always inside one scale block (mx: 1 block / half a block, nvfp4: 2 blocks,
+// int4 affine: half a group, nvfp8: 1 block).
+
+// Per-piece scale state, loaded with the codes.
+struct PieceScale {
+  uint32_t a, b;  // format-specific raw scale words
+};
+
+template <int F>
+__device__ __forceinline__ PieceScale load_piece_scale(const uint8_t* scales, int64_t row, int64_t nblk,
+                                                       int64_t k0, bool ok) {
+  PieceScale s{0u, 0u};
+  if (!ok) return s;
+  const int64_t base = row * nblk;
+  if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+    s.a = __ldg(scales + base + k0 / 32);
+  } else if constexpr (F == NVFP4) {
+    s.a = __ldg(reinterpret_cast<const unsigned short*>(scales + base + k0 / 16));
+  } else if constexpr (F == NVFP8) {
+    s.a = __ldg(reinterpret_cast<const uint32_t*>(scales) + base + k0 / 16);
+  } else {
+    s.a = __ldg(reinterpret_cast<const uint32_t*>(scales) + base + k0 / 64);
+  }
+  return s;
+}
+
+// Decode one 16-byte piece of one row into the A-fragment halves of each mma
+// step: A[s][0] feeds k slots (2t, 2t+1), A[s][1] slots (2t+8, 2t+9).
+// 4-bit: 8 steps (word j gives steps 2j, 2j+1); 8-bit: 4 steps (word j -> step j).
+template <int F>
+__device__ __forceinline__ void decode_piece(const uint4& v, const PieceScale& ps,
+                                             uint32_t A[FmtTraits<F>::four ? 8 : 4][2]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (F == MXFP4 || F == NVFP4) {
+    uint32_t sc0, sc1;
+    if constexpr (F == MXFP4) {
+      sc0 = sc1 = bf16x2_splat(e8m0_bf16(ps.a));
+    } else {
+      sc0 = bf16x2_splat(f32_to_bf16bits(e4m3_f32(ps.a & 0xFFu)));
+      sc1 = bf16x2_splat(f32_to_bf16bits(e4m3_f32(ps.a >> 8)));
+    }
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t r[4];
+      e2m1x8_bf16(w[j], r);
+      const uint32_t sc = j < 2 ? sc0 : sc1;
+      A[2 * j][0] = hmul2(r[0], sc);
+      A[2 * j][1] = hmul2(r[1], sc);
+      A[2 * j + 1][0] = hmul2(r[2], sc);
+      A[2 * j + 1][1] = hmul2(r[3], sc);
+    }
+  } else if constexpr (F == INT4_AFFINE) {
+    const uint32_t s2 = bf16x2_splat(ps.a & 0xFFFFu), b2 = bf16x2_splat(ps.a >> 16);
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t r[4];
+      int4x8_affine_bf16(w[j], s2, b2, r);
+      A[2 * j][0] = r[0];
+      A[2 * j][1] = r[1];
+      A[2 * j + 1][0] = r[2];
+      A[2 * j + 1][1] = r[3];
+    }
+  } else {
+    // 8-bit: raw bf16 = value * 2^-bias_gap; one multiply restores the bias and
+    // applies the block scale when the combined factor fits bf16, else two.
+    uint32_t m1, m2 = 0x3F803F80u;
+    bool two = false;
+    if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+      constexpr int gap = F == MXFP8_E4M3 ? 120 : 112;
+      const int b = int(ps.a);
+      if (b == 255) {
+        m1 = 0x7FC07FC0u;
+      } else if (b - 127 + gap <= 127) {
+        m1 = bf16x2_splat(pow2_bf16(b - 127 + gap));
+      } else {
+        m1 = bf16x2_splat(pow2_bf16(gap));
+        m2 = bf16x2_splat(pow2_bf16(b - 127));
+        two = true;
+      }
+    } else {  // NVFP8: float32 scale rounded once to bf16
+      const float s = __uint_as_float(ps.a);
+      if (fabsf(s) < 128.0f) {
+        m1 = bf16x2_splat(f32_to_bf16bits(s * 0x1p120f));
+      } else {
+        m1 = bf16x2_splat(pow2_bf16(120));
+        m2 = bf16x2_splat(f32_to_bf16bits(s));
+        two = true;
+      }
+    }
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t r[2];
+      if constexpr (F == MXFP8_E5M2) e5m2x4_bf16_raw(w[j], r);
+      else e4m3x4_bf16_raw(w[j], r);
+      A[j][0] = hmul2(r[0], m1);
+      A[j][1] = hmul2(r[1], m1);
+      if (two) {
+        A[j][0] = hmul2(A[j][0], m2);
+        A[j][1] = hmul2(A[j][1], m2);
+      }
+    }
+  }
+}
+
+// The same piece as bf16 pairs in natural k order: 4-bit -> 16 registers
+// (word j gives registers 4j..4j+3 = codes 8j..8j+7), 8-bit -> 8 registers.
+template <int F>
+__device__ __forceinline__ void decode_piece_natural(const uint4& v, const PieceScale& ps,
+                                                     uint32_t out[FmtTraits<F>::four ? 16 : 8]) {
+  uint32_t A[FmtTraits<F>::four ? 8 : 4][2];
+  decode_piece<F>(v, ps, A);
+  if constexpr (FmtTraits<F>::four) {
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      out[4 * j + 0] = prmt(A[2 * j][0], A[2 * j][1], 0x5410u);          // (c0, c1)
+      out[4 * j + 1] = prmt(A[2 * j + 1][0], A[2 * j + 1][1], 0x5410u);  // (c2, c3)
+      out[4 * j + 2] = prmt(A[2 * j][0], A[2 * j][1], 0x7632u);          // (c4, c5)
+      out[4 * j + 3] = prmt(A[2 * j + 1][0], A[2 * j + 1][1], 0x7632u);  // (c6, c7)
+    }
+  } else {
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      out[2 * j + 0] = prmt(A[j][0], A[j][1], 0x5410u);                  // (c0, c1)
+      out[2 * j + 1] = prmt(A[j][0], A[j][1], 0x7632u);                  // (c2, c3)
+    }
+  }
 }
 
 }  // namespace qfmt_dev

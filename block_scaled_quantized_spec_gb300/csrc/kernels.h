@@ -26,4 +26,9 @@ cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, floa
                             const void* x, void* out, bool out_f32, int64_t M, int64_t N,
                             int64_t K, cudaStream_t st, int sms);
 
+// Bounded-wait test hooks and the device status word of the tensor-core GEMM.
+void set_wait_limit_ns(uint64_t ns);
+void set_drop_arrivals(int on);
+cudaError_t read_and_clear_device_status(unsigned int* status);
+
 }  // namespace qfmt_dev

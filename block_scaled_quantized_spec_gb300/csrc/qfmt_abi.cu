@@ -109,6 +109,29 @@ int qmm(int fmt, const void* codes, const void* scales, float global_scale, cons
                 stream);
 }
 
+int qfmt_device_status(void* stream) {
+  clear_error();
+  int st = cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream sync");
+  if (st) return st;
+  unsigned int word = 0;
+  if ((st = cuda_status(qfmt_dev::read_and_clear_device_status(&word), "device status"))) return st;
+  if (word) return fail(QFMT_ETIMEOUT, "a tensor-core GEMM pipeline wait expired (status 0x%x)", word);
+  return QFMT_OK;
+}
+
+int qfmt_debug_set(int key, int64_t value) {
+  clear_error();
+  if (key == 1) {
+    qfmt_dev::set_wait_limit_ns(value > 0 ? uint64_t(value) : 2000000000ull);
+    return QFMT_OK;
+  }
+  if (key == 2) {
+    qfmt_dev::set_drop_arrivals(value ? 1 : 0);
+    return QFMT_OK;
+  }
+  return fail(QFMT_EINVAL, "unknown debug key %d", key);
+}
+
 size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K) {
   (void)fmt; (void)M; (void)N; (void)K;
   return 0;

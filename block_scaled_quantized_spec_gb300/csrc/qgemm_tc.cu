@@ -1,24 +1,474 @@
-// Prefill dequantizing GEMM, M > 16.  (Placeholder: 16-row slices through the
-// decode GEMV; replaced by the tcgen05 kernel.)
-#include <cuda_bf16.h>
+// Prefill dequantizing GEMM on the 5th-generation tensor cores, M > 16:
+//   out[M, N] = X[M, K] (bf16) . dequant(W[N, K])^T, float32 accumulation.
+//
+// The pages' prefill kernels (metaltile-std src/mlx/fp_quantized_mma.rs,
+// mt_fp4_qmm_mma / mt_fp8_e4m3_qmm_mma; the PR #250 block-scaled *_qmm_mma
+// kernels) stage X and W tiles in threadgroup memory, decode W per lane into
+// threadgroup memory and run 8x8 simdgroup MMAs.  The GB300 design keeps the
+// idea -- decode the weights once per tile into on-chip memory, then run dense
+// MMAs -- and maps it onto tcgen05:
+//
+//  * CTA tile 128 (M) x 256 (N), K step 64, four pipeline stages in shared
+//    memory (X tile 16 KiB + decoded W tile 32 KiB per stage);
+//  * warp 0: one thread issues TMA loads of the X tile (128B-swizzled, K-major)
+//    and owns the TMEM allocation;
+//  * warp 1: one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> float32 in
+//    TMEM, 128 x 256 x 16 per instruction) and commits each stage back to the
+//    producers through an mbarrier;
+//  * warps 2-9: decoders.  Each streams 16-byte pieces of codes (plus their
+//    block scales) from global memory with 128-bit loads one K step ahead,
+//    decodes them in registers to bf16 with the block scale applied (exact for
+//    power-of-two and E4M3 scales; nvfp8 and int4-affine weights round once to
+//    bf16) and writes the canonical 128B-swizzled K-major layout the MMA reads;
+//  * warps 2-5 (one per TMEM lane quadrant) then drain the accumulator with
+//    tcgen05.ld, apply the nvfp4 global scale and store bf16/float32 rows.
+//
+// Every mbarrier wait is bounded by a time limit; on expiry the kernel records
+// an error in a device status word, lets in-flight copies and MMAs finish,
+// frees its TMEM and exits (qfmt_device_status reports it).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <mutex>
+
+#include "decode.cuh"
 #include "kernels.h"
 
 namespace qfmt_dev {
 
-cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, float glob, const void* x,
-                            void* out, bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st,
-                            int sms) {
-  for (int64_t m0 = 0; m0 < M; m0 += 16) {
-    const int64_t mm = M - m0 < 16 ? M - m0 : 16;
-    const void* xs = static_cast<const __nv_bfloat16*>(x) + m0 * K;
-    void* os = out_f32 ? static_cast<void*>(static_cast<float*>(out) + m0 * N)
-                       : static_cast<void*>(static_cast<__nv_bfloat16*>(out) + m0 * N);
-    cudaError_t e = launch_qgemv(fmt, codes, scales, glob, xs, os, out_f32, mm, N, K, st, sms);
-    if (e != cudaSuccess) return e;
+__device__ unsigned int g_device_status;
+
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int DEC_WARPS = 8;
+constexpr int DEC_THREADS = DEC_WARPS * 32;
+constexpr int THREADS = (2 + DEC_WARPS) * 32;
+constexpr int TMEM_COLS = 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+
+// ----------------------------------------------------------- PTX helpers ---
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > limit_ns) return false;
   }
-  return cudaSuccess;
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major operand in the 128B-swizzle
+// canonical layout: 8-row x 128-byte atoms, atoms 1024 bytes apart (stride
+// byte offset); the leading byte offset is unused for this layout; descriptor
+// version 1; swizzle mode 2 (128B).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t(1) << 16;
+  d |= uint64_t(1024 >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D float32, A and B bf16, both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Byte offset of the 16-byte chunk `c` (8 bf16 along K) of row `r` inside a
+// 128B-swizzled K-major tile.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+  return uint32_t((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+struct Params {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  void* out;
+  float glob;
+  int M, N, K;
+  int out_f32;
+  uint64_t limit_ns;   // bound on every wait
+  int drop_arrivals;   // test hook: decoders never signal a stage (the waits must expire)
+};
+
+template <int F>
+__global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
+  using T = FmtTraits<F>;
+  constexpr int PIECE = T::four ? 32 : 16;                 // codes per 16-byte piece
+  constexpr int PIECES_PER_ROW = BK / PIECE;               // 2 or 4 per K step
+  constexpr int PIECES_PER_THREAD = BN * PIECES_PER_ROW / DEC_THREADS;   // 2 or 4
+  constexpr int ROWS_PER_PASS = DEC_THREADS / PIECES_PER_ROW;            // 128 or 64
+  constexpr int NREG = T::four ? 16 : 8;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars[0..S): A full (TMA), [S..2S): B full (decoders), [2S..3S): stage empty (MMA), [3S]: accumulator done
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 3 * STAGES + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int nkb = (p.K + BK - 1) / BK;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  auto a_full = [&](int s) { return bar0 + 8u * s; };
+  auto b_full = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  const uint32_t done_bar = bar0 + 8u * (3 * STAGES);
+  auto stage_a = [&](int s) { return sbase + uint32_t(s * STAGE_BYTES); };
+  auto stage_b = [&](int s) { return sbase + uint32_t(s * STAGE_BYTES + A_BYTES); };
+  auto fail = [&]() {
+    *abort_flag = 1u;
+    atomicOr(&g_device_status, 1u);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(a_full(s), 1);
+      mbar_init(b_full(s), DEC_WARPS);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((const void*)tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1;
+        if (*abort_flag) break;
+        if (!mbar_wait(empty(s), ph ^ 1u, p.limit_ns)) { fail(); break; }
+        mbar_arrive_expect_tx(a_full(s), A_BYTES);
+        tma_load_2d(stage_a(s), &xmap, kb * BK, m0, a_full(s));
+        issued = kb + 1;
+      }
+      // every issued copy must land before the CTA may exit
+      for (int kb = issued > STAGES ? issued - STAGES : 0; kb < issued; ++kb)
+        if (!mbar_wait(a_full(kb % STAGES), (kb / STAGES) & 1, p.limit_ns)) fail();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1;
+        if (*abort_flag) break;
+        if (!mbar_wait(a_full(s), ph, p.limit_ns) || !mbar_wait(b_full(s), ph, p.limit_ns)) { fail(); break; }
+        tc_fence_after();
+        const uint64_t ad = desc_sw128(stage_a(s)), bd = desc_sw128(stage_b(s));
+        #pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)   // +32 bytes along K per instruction
+          mma_f16(tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), (kb | kk) != 0);
+        mma_commit(empty(s));
+      }
+      mma_commit(done_bar);   // fires once every MMA issued above has completed
+    }
+  } else {
+    // -------------------------------------------------------------- decoders
+    const int dt = threadIdx.x - 64;                       // 0 .. DEC_THREADS-1
+    const int64_t row_bytes = T::four ? p.K / 2 : p.K;
+    const int64_t nblk = p.K / T::block;
+    const int sub = dt % PIECES_PER_ROW;                   // piece index within the row's K step
+    const int rbase = dt / PIECES_PER_ROW;
+    uint4 cur[PIECES_PER_THREAD];
+    PieceScale cs[PIECES_PER_THREAD];
+    auto load = [&](int kb, uint4 (&v)[PIECES_PER_THREAD], PieceScale (&sc)[PIECES_PER_THREAD]) {
+      #pragma unroll
+      for (int i = 0; i < PIECES_PER_THREAD; ++i) {
+        const int r = rbase + i * ROWS_PER_PASS;
+        const int n = n0 + r;
+        const int64_t k0 = int64_t(kb) * BK + sub * PIECE;
+        const bool ok = kb < nkb && n < p.N && k0 < p.K;
+        v[i] = ok ? ldg_stream(p.codes + int64_t(n) * row_bytes + (T::four ? k0 / 2 : k0)) : make_uint4(0, 0, 0, 0);
+        sc[i] = load_piece_scale<F>(p.scales, n, nblk, k0, ok);
+      }
+    };
+    load(0, cur, cs);
+    bool aborted = false;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = (kb / STAGES) & 1;
+      int ok = 1;
+      if (lane == 0) ok = (*abort_flag == 0u) && mbar_wait(empty(s), ph ^ 1u, p.limit_ns);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0 && *abort_flag == 0u) fail();
+        aborted = true;
+        break;
+      }
+      uint4 nxt[PIECES_PER_THREAD];
+      PieceScale ns[PIECES_PER_THREAD];
+      load(kb + 1, nxt, ns);                               // next K step's codes in flight
+      const uint32_t bs = stage_b(s);
+      #pragma unroll
+      for (int i = 0; i < PIECES_PER_THREAD; ++i) {
+        const int r = rbase + i * ROWS_PER_PASS;
+        uint32_t w[NREG];
+        decode_piece_natural<F>(cur[i], cs[i], w);
+        #pragma unroll
+        for (int c = 0; c < NREG / 4; ++c)
+          sts128(bs + sw128_off(r, sub * (NREG / 4) + c), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        cur[i] = nxt[i];
+        cs[i] = ns[i];
+      }
+      fence_proxy_async();                                 // generic-proxy stores -> tensor core reads
+      __syncwarp();
+      if (lane == 0 && !p.drop_arrivals) mbar_arrive(b_full(s));
+    }
+    (void)aborted;
+    // --------------------------------------------------------------- epilogue
+    if (warp < 6) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(done_bar, 0, p.limit_ns);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok && lane == 0) fail();
+      tc_fence_after();
+      const int q = warp & 3;                              // TMEM lane quadrant of this warp
+      const int m = m0 + q * 32 + lane;
+      const bool live = ok && *abort_flag == 0u;
+      #pragma unroll 1
+      for (int cb = 0; cb < BN / 32; ++cb) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(cb * 32), r);
+        const int nb = n0 + cb * 32;
+        if (!live || m >= p.M || nb >= p.N) continue;
+        float v[32];
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          v[j] = __uint_as_float(r[j]);
+          if constexpr (F == NVFP4) v[j] *= p.glob;
+        }
+        const int ncols = p.N - nb < 32 ? p.N - nb : 32;
+        if (p.out_f32) {
+          float* o = static_cast<float*>(p.out) + int64_t(m) * p.N + nb;
+          if (ncols == 32 && (p.N & 3) == 0) {
+            #pragma unroll
+            for (int j = 0; j < 8; ++j)
+              reinterpret_cast<float4*>(o)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          } else {
+            for (int j = 0; j < ncols; ++j) o[j] = v[j];
+          }
+        } else {
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + int64_t(m) * p.N + nb;
+          if (ncols == 32 && (p.N & 7) == 0) {
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t h[4];
+              #pragma unroll
+              for (int t = 0; t < 4; ++t)
+                h[t] = f32_to_bf16bits(v[8 * j + 2 * t]) | (f32_to_bf16bits(v[8 * j + 2 * t + 1]) << 16);
+              reinterpret_cast<uint4*>(o)[j] = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+          } else {
+            for (int j = 0; j < ncols; ++j) o[j] = __float2bfloat16_rn(v[j]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host ---
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+static std::atomic<uint64_t> g_limit_ns{2000000000ull};
+static std::atomic<int> g_drop{0};
+
+template <int F>
+static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
+                              bool out_f32, int M, int N, int K, cudaStream_t st) {
+  static std::atomic<int> attr_done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
+    e = cudaFuncSetAttribute(qgemm_tc_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done[dev].store(1);
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t gdim[2] = {cuuint64_t(K), cuuint64_t(M)};
+  const cuuint64_t gstride[1] = {cuuint64_t(K) * 2};
+  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), gdim, gstride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  Params prm;
+  prm.codes = static_cast<const uint8_t*>(codes);
+  prm.scales = static_cast<const uint8_t*>(scales);
+  prm.out = out;
+  prm.glob = glob;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.out_f32 = out_f32 ? 1 : 0;
+  prm.limit_ns = g_limit_ns.load();
+  prm.drop_arrivals = g_drop.load();
+  dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+  qgemm_tc_kernel<F><<<grid, THREADS, SMEM_BYTES, st>>>(map, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, float glob, const void* x, void* out,
+                            bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms) {
+  (void)sms;
+  const int m = int(M), n = int(N), k = int(K);
+  switch (fmt) {
+    case MXFP4: return tc::launch_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case NVFP4: return tc::launch_fmt<NVFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP8_E4M3: return tc::launch_fmt<MXFP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP8_E5M2: return tc::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case NVFP8: return tc::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    default: return tc::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+  }
+}
+
+// Test hooks for the bounded waits (see qfmt_debug_set in the C ABI).
+void set_wait_limit_ns(uint64_t ns) { tc::g_limit_ns.store(ns); }
+void set_drop_arrivals(int on) { tc::g_drop.store(on); }
+
+cudaError_t read_and_clear_device_status(unsigned int* status) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, g_device_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned int));
 }
 
 }  // namespace qfmt_dev

@@ -45,107 +45,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return v;
 }
 
-// Per-piece scale state, loaded with the codes.
-struct PieceScale {
-  uint32_t a, b;  // format-specific raw scale words
-};
-
-template <int F>
-__device__ __forceinline__ PieceScale load_piece_scale(const uint8_t* scales, int64_t row, int64_t nblk,
-                                                       int64_t k0, bool ok) {
-  PieceScale s{0u, 0u};
-  if (!ok) return s;
-  const int64_t base = row * nblk;
-  if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) {
-    s.a = __ldg(scales + base + k0 / 32);
-  } else if constexpr (F == NVFP4) {
-    s.a = __ldg(reinterpret_cast<const unsigned short*>(scales + base + k0 / 16));
-  } else if constexpr (F == NVFP8) {
-    s.a = __ldg(reinterpret_cast<const uint32_t*>(scales) + base + k0 / 16);
-  } else {
-    s.a = __ldg(reinterpret_cast<const uint32_t*>(scales) + base + k0 / 64);
-  }
-  return s;
-}
-
-// Decode one 16-byte piece of one row into the A-fragment halves of each mma
-// step: A[s][0] feeds k slots (2t, 2t+1), A[s][1] slots (2t+8, 2t+9).
-// 4-bit: 8 steps (word j gives steps 2j, 2j+1); 8-bit: 4 steps (word j -> step j).
-template <int F>
-__device__ __forceinline__ void decode_piece(const uint4& v, const PieceScale& ps,
-                                             uint32_t A[FmtTraits<F>::four ? 8 : 4][2]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  if constexpr (F == MXFP4 || F == NVFP4) {
-    uint32_t sc0, sc1;
-    if constexpr (F == MXFP4) {
-      sc0 = sc1 = bf16x2_splat(e8m0_bf16(ps.a));
-    } else {
-      sc0 = bf16x2_splat(f32_to_bf16bits(e4m3_f32(ps.a & 0xFFu)));
-      sc1 = bf16x2_splat(f32_to_bf16bits(e4m3_f32(ps.a >> 8)));
-    }
-    #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t r[4];
-      e2m1x8_bf16(w[j], r);
-      const uint32_t sc = j < 2 ? sc0 : sc1;
-      A[2 * j][0] = hmul2(r[0], sc);
-      A[2 * j][1] = hmul2(r[1], sc);
-      A[2 * j + 1][0] = hmul2(r[2], sc);
-      A[2 * j + 1][1] = hmul2(r[3], sc);
-    }
-  } else if constexpr (F == INT4_AFFINE) {
-    const uint32_t s2 = bf16x2_splat(ps.a & 0xFFFFu), b2 = bf16x2_splat(ps.a >> 16);
-    #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t r[4];
-      int4x8_affine_bf16(w[j], s2, b2, r);
-      A[2 * j][0] = r[0];
-      A[2 * j][1] = r[1];
-      A[2 * j + 1][0] = r[2];
-      A[2 * j + 1][1] = r[3];
-    }
-  } else {
-    // 8-bit: raw bf16 = value * 2^-bias_gap; one multiply restores the bias and
-    // applies the block scale when the combined factor fits bf16, else two.
-    uint32_t m1, m2 = 0x3F803F80u;
-    bool two = false;
-    if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {
-      constexpr int gap = F == MXFP8_E4M3 ? 120 : 112;
-      const int b = int(ps.a);
-      if (b == 255) {
-        m1 = 0x7FC07FC0u;
-      } else if (b - 127 + gap <= 127) {
-        m1 = bf16x2_splat(pow2_bf16(b - 127 + gap));
-      } else {
-        m1 = bf16x2_splat(pow2_bf16(gap));
-        m2 = bf16x2_splat(pow2_bf16(b - 127));
-        two = true;
-      }
-    } else {  // NVFP8: float32 scale rounded once to bf16
-      const float s = __uint_as_float(ps.a);
-      if (fabsf(s) < 128.0f) {
-        m1 = bf16x2_splat(f32_to_bf16bits(s * 0x1p120f));
-      } else {
-        m1 = bf16x2_splat(pow2_bf16(120));
-        m2 = bf16x2_splat(f32_to_bf16bits(s));
-        two = true;
-      }
-    }
-    #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t r[2];
-      if constexpr (F == MXFP8_E5M2) e5m2x4_bf16_raw(w[j], r);
-      else e4m3x4_bf16_raw(w[j], r);
-      A[j][0] = hmul2(r[0], m1);
-      A[j][1] = hmul2(r[1], m1);
-      if (two) {
-        A[j][0] = hmul2(A[j][0], m2);
-        A[j][1] = hmul2(A[j][1], m2);
-      }
-    }
-  }
-}
-
 // Activation B-fragment halves for one column (batch row) over the same k
 // slots as decode_piece: xs points at the piece's first activation.
 template <bool FOUR>
@@ -253,6 +152,172 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) qgemv_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// nvfp8 and int4 affine: the weights stay exact in bf16 (E4M3 codes, or the
+// integers 128 + q) and the block scale is applied to float32 partial sums.
+// That needs every mma.sync to draw its 16 k values from one block, so the
+// four lanes of a quad share each block: nvfp8 lanes take word t of each of
+// four consecutive 16-byte blocks (32-bit loads), int4 affine lanes take bytes
+// 8t..8t+7 of each of two 32-byte groups (64-bit loads).  int4 affine adds
+// one mma per step against a matrix of ones to get the activation sums the
+// affine bias multiplies: sum_k x (s q + b) = s sum_k x (128 + q) + (b - 128 s) sum_k x.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mma_bf16_zero(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+__device__ __forceinline__ uint32_t ldg32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ldg64(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+template <int F, int NB>
+__global__ void __launch_bounds__(GEMV_WARPS * 32) qgemv_blockacc_kernel(
+    const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, const __nv_bfloat16* __restrict__ x,
+    void* __restrict__ out, int out_f32, int M, int N, int K) {
+  constexpr bool I4 = F == INT4_AFFINE;
+  constexpr int CHUNK = I4 ? 128 : 64;         // codes per row per chunk: 2 groups / 4 blocks
+  constexpr int NSUB = I4 ? 2 : 4;             // scale blocks per chunk
+  __shared__ float red[GEMV_WARPS][16][8 * NB];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int row0 = blockIdx.x * 16;
+  const int rA = row0 + g, rB = row0 + g + 8;
+  const bool okA = rA < N, okB = rB < N;
+  const int64_t row_bytes = I4 ? K / 2 : K;
+  const int64_t nblk = K / (I4 ? 64 : 16);
+  const int nchunks = (K + CHUNK - 1) / CHUNK;
+  const uint8_t* pA = codes + int64_t(okA ? rA : 0) * row_bytes;
+  const uint8_t* pB = codes + int64_t(okB ? rB : 0) * row_bytes;
+  const int64_t sA0 = int64_t(okA ? rA : 0) * nblk, sB0 = int64_t(okB ? rB : 0) * nblk;
+
+  float acc[NB][4];
+  #pragma unroll
+  for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
+
+  for (int c0 = warp; c0 < nchunks; c0 += GEMV_WARPS * GEMV_UNROLL) {
+    // words[u][j]: nvfp8: word t of block j (4 codes); int4: word j of the lane's 8 bytes in group j/2
+    uint32_t wa[GEMV_UNROLL][4], wb[GEMV_UNROLL][4];
+    uint32_t sa[GEMV_UNROLL][NSUB], sb[GEMV_UNROLL][NSUB];
+    #pragma unroll
+    for (int u = 0; u < GEMV_UNROLL; ++u) {
+      const int c = c0 + u * GEMV_WARPS;
+      #pragma unroll
+      for (int j = 0; j < NSUB; ++j) {
+        const int64_t kb = int64_t(c) * CHUNK + j * (I4 ? 64 : 16);   // first k of the block
+        const bool ok = c < nchunks && kb < K;
+        const int64_t blk = kb / (I4 ? 64 : 16);
+        if constexpr (I4) {
+          const int64_t off = kb / 2 + 8 * t;
+          uint2 va = ok && okA ? ldg64(pA + off) : make_uint2(0, 0);
+          uint2 vb = ok && okB ? ldg64(pB + off) : make_uint2(0, 0);
+          wa[u][2 * j] = va.x; wa[u][2 * j + 1] = va.y;
+          wb[u][2 * j] = vb.x; wb[u][2 * j + 1] = vb.y;
+          sa[u][j] = ok && okA ? __ldg(reinterpret_cast<const uint32_t*>(scales) + sA0 + blk) : 0u;
+          sb[u][j] = ok && okB ? __ldg(reinterpret_cast<const uint32_t*>(scales) + sB0 + blk) : 0u;
+        } else {
+          const int64_t off = kb + 4 * t;
+          wa[u][j] = ok && okA ? ldg32(pA + off) : 0u;
+          wb[u][j] = ok && okB ? ldg32(pB + off) : 0u;
+          sa[u][j] = ok && okA ? __ldg(reinterpret_cast<const uint32_t*>(scales) + sA0 + blk) : 0u;
+          sb[u][j] = ok && okB ? __ldg(reinterpret_cast<const uint32_t*>(scales) + sB0 + blk) : 0u;
+        }
+      }
+    }
+    #pragma unroll
+    for (int u = 0; u < GEMV_UNROLL; ++u) {
+      const int c = c0 + u * GEMV_WARPS;
+      if (c >= nchunks) break;
+      #pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const int m = nb * 8 + g;
+        const bool mok = m < M;
+        const __nv_bfloat16* xr = x + int64_t(mok ? m : 0) * K;
+        #pragma unroll
+        for (int j = 0; j < NSUB; ++j) {
+          const int64_t kb = int64_t(c) * CHUNK + j * (I4 ? 64 : 16);
+          const bool ok = kb < K && mok;
+          if constexpr (I4) {
+            // lane's 16 activations of group j: k = kb + 16t .. +15 (two words of 8)
+            const uint4 v0 = ok ? __ldg(reinterpret_cast<const uint4*>(xr + kb + 16 * t)) : make_uint4(0, 0, 0, 0);
+            const uint4 v1 = ok ? __ldg(reinterpret_cast<const uint4*>(xr + kb + 16 * t + 8)) : make_uint4(0, 0, 0, 0);
+            float d[4] = {0.f, 0.f, 0.f, 0.f}, xs[4] = {0.f, 0.f, 0.f, 0.f};
+            #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 v = h ? v1 : v0;
+              uint32_t ra[4], rb[4];
+              int4x8_biased_bf16(wa[u][2 * j + h], ra);
+              int4x8_biased_bf16(wb[u][2 * j + h], rb);
+              const uint32_t b00 = prmt(v.x, v.z, 0x5410u), b01 = prmt(v.x, v.z, 0x7632u);
+              const uint32_t b10 = prmt(v.y, v.w, 0x5410u), b11 = prmt(v.y, v.w, 0x7632u);
+              mma_bf16(d, ra[0], rb[0], ra[1], rb[1], b00, b01);
+              mma_bf16(d, ra[2], rb[2], ra[3], rb[3], b10, b11);
+              const uint32_t one = 0x3F803F80u;
+              mma_bf16(xs, one, one, one, one, b00, b01);
+              mma_bf16(xs, one, one, one, one, b10, b11);
+            }
+            const float sA = bf16bits_f32(sa[u][j] & 0xFFFFu), bA = bf16bits_f32(sa[u][j] >> 16);
+            const float sB = bf16bits_f32(sb[u][j] & 0xFFFFu), bB = bf16bits_f32(sb[u][j] >> 16);
+            const float cA = __fmaf_rn(-128.0f, sA, bA), cB = __fmaf_rn(-128.0f, sB, bB);
+            acc[nb][0] = __fmaf_rn(sA, d[0], __fmaf_rn(cA, xs[0], acc[nb][0]));
+            acc[nb][1] = __fmaf_rn(sA, d[1], __fmaf_rn(cA, xs[1], acc[nb][1]));
+            acc[nb][2] = __fmaf_rn(sB, d[2], __fmaf_rn(cB, xs[2], acc[nb][2]));
+            acc[nb][3] = __fmaf_rn(sB, d[3], __fmaf_rn(cB, xs[3], acc[nb][3]));
+          } else {
+            // lane's 4 activations of block j: k = kb + 4t .. +3
+            const uint2 v = ok ? ldg64(xr + kb + 4 * t) : make_uint2(0, 0);
+            const uint32_t b0 = prmt(v.x, v.y, 0x5410u), b1 = prmt(v.x, v.y, 0x7632u);   // (x0,x2) (x1,x3)
+            uint32_t ra[2], rb[2];
+            e4m3x4_bf16_raw(wa[u][j], ra);
+            e4m3x4_bf16_raw(wb[u][j], rb);
+            const uint32_t k120 = 0x7B807B80u;                     // 2^120: exact E4M3 values
+            float d[4];
+            mma_bf16_zero(d, hmul2(ra[0], k120), hmul2(rb[0], k120), hmul2(ra[1], k120), hmul2(rb[1], k120), b0, b1);
+            const float sA = __uint_as_float(sa[u][j]), sB = __uint_as_float(sb[u][j]);
+            acc[nb][0] = __fmaf_rn(sA, d[0], acc[nb][0]);
+            acc[nb][1] = __fmaf_rn(sA, d[1], acc[nb][1]);
+            acc[nb][2] = __fmaf_rn(sB, d[2], acc[nb][2]);
+            acc[nb][3] = __fmaf_rn(sB, d[3], acc[nb][3]);
+          }
+        }
+      }
+    }
+  }
+
+  #pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    red[warp][g][nb * 8 + 2 * t] = acc[nb][0];
+    red[warp][g][nb * 8 + 2 * t + 1] = acc[nb][1];
+    red[warp][g + 8][nb * 8 + 2 * t] = acc[nb][2];
+    red[warp][g + 8][nb * 8 + 2 * t + 1] = acc[nb][3];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 16 * M; i += blockDim.x) {
+    const int r = i & 15, m = i >> 4;
+    if (row0 + r >= N) continue;
+    float sum = 0.0f;
+    #pragma unroll
+    for (int w = 0; w < GEMV_WARPS; ++w) sum += red[w][r][m];
+    const int64_t o = int64_t(m) * N + row0 + r;
+    if (out_f32) static_cast<float*>(out)[o] = sum;
+    else static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(sum);
+  }
+}
+
 template <int F>
 static cudaError_t launch_qgemv_fmt(const void* codes, const void* scales, float glob, const void* x,
                                     void* out, bool out_f32, int M, int N, int K, cudaStream_t st) {
@@ -260,8 +325,13 @@ static cudaError_t launch_qgemv_fmt(const void* codes, const void* scales, float
   auto c = static_cast<const uint8_t*>(codes);
   auto s = static_cast<const uint8_t*>(scales);
   auto xx = static_cast<const __nv_bfloat16*>(x);
-  if (M <= 8) qgemv_kernel<F, 1><<<grid, block, 0, st>>>(c, s, glob, xx, out, out_f32, M, N, K);
-  else qgemv_kernel<F, 2><<<grid, block, 0, st>>>(c, s, glob, xx, out, out_f32, M, N, K);
+  if constexpr (F == NVFP8 || F == INT4_AFFINE) {
+    if (M <= 8) qgemv_blockacc_kernel<F, 1><<<grid, block, 0, st>>>(c, s, xx, out, out_f32, M, N, K);
+    else qgemv_blockacc_kernel<F, 2><<<grid, block, 0, st>>>(c, s, xx, out, out_f32, M, N, K);
+  } else {
+    if (M <= 8) qgemv_kernel<F, 1><<<grid, block, 0, st>>>(c, s, glob, xx, out, out_f32, M, N, K);
+    else qgemv_kernel<F, 2><<<grid, block, 0, st>>>(c, s, glob, xx, out, out_f32, M, N, K);
+  }
   return cudaGetLastError();
 }
 

@@ -32,8 +32,10 @@
  * qmm and qmm_ex take device pointers, enqueue work on `stream` (a
  * cudaStream_t; NULL = the legacy default stream) and return without
  * waiting; their status reports argument and launch errors only.  The
- * library keeps no handle and allocates no device memory; the only global
- * state is a per-thread error message.
+ * library keeps no handle and allocates no device memory.  Its global state
+ * is a per-thread error message, one status word per device (written only
+ * when a kernel's bounded wait expires; see qfmt_device_status) and the
+ * process-wide test settings of qfmt_debug_set.
  *
  * Errors: every function returns a qfmt_status (or a size; see each), never
  * aborts and never throws.  qfmt_last_error() describes the last failure on
@@ -67,6 +69,7 @@ typedef enum {
   QFMT_EALIGN = -3,        /* a device pointer not 16-byte aligned (scales: 4-byte) */
   QFMT_EUNSUPPORTED = -4,  /* a group size other than the format's block */
   QFMT_ECUDA = -5,         /* a CUDA launch or device query failed */
+  QFMT_ETIMEOUT = -6,      /* a kernel's bounded pipeline wait expired (see qfmt_device_status) */
   QFMT_ENONFINITE = -7,    /* qfmt_pack: NaN/Inf weight, or a block scale overflowing float32 */
   QFMT_ENOSPACE = -8       /* a caller workspace smaller than qmm_workspace_bytes() */
 } qfmt_status;
@@ -137,6 +140,25 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale,
            void* workspace, size_t workspace_bytes, void* stream);
 
 size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
+
+/*
+ * qfmt_device_status -- waits for `stream`, then reads and clears the
+ * library's device status word for the current device.  Every pipeline wait
+ * inside the tensor-core GEMM is bounded in time; when one expires the kernel
+ * records it there, drains its in-flight copies and MMAs, frees its tensor
+ * memory and exits without writing its output tile.  Returns QFMT_OK, or
+ * QFMT_ETIMEOUT if any such kernel since the last call gave up, or QFMT_ECUDA.
+ */
+int qfmt_device_status(void* stream);
+
+/*
+ * qfmt_debug_set -- testing aid for the bounded waits (process-wide, applies
+ * to launches made afterwards): key 1 sets the wait limit in nanoseconds
+ * (value <= 0 restores the default of 2 s); key 2 with value 1 makes the GEMM's
+ * decoder warps skip signalling their stages, so the MMA warp's waits expire
+ * (value 0 restores normal operation).  Returns QFMT_EINVAL for other keys.
+ */
+int qfmt_debug_set(int key, int64_t value);
 
 /* Human-readable description of the last failure on this thread ("" if none). */
 const char* qfmt_last_error(void);

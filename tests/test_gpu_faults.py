@@ -1,0 +1,56 @@
+"""Failure detection on the GPU without a fault: every pipeline wait of the
+tensor-core GEMM is bounded.  A test hook makes the decoder warps skip
+signalling their stages (a flag that nothing sets), the MMA warp's wait runs
+out after a short limit, the kernel records QFMT_ETIMEOUT in the device status
+word and exits cleanly; the context stays usable for the next correct call."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import block_scaled_quantized_spec_gb300 as q  # noqa: E402
+from block_scaled_quantized_spec_gb300 import synth  # noqa: E402
+from oracle import pack as opack  # noqa: E402
+from oracle import reference as oref  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_scaled_quantized_spec_gb300 import build
+    build.build()
+    q.load()
+
+
+def test_expired_wait_reports_timeout_and_context_survives():
+    fmt, m, n, k = "mxfp8_e4m3", 128, 256, 512
+    w = synth.weights(n, k, seed=3)
+    c, s, g = opack.pack(fmt, w)
+    xb = synth.activations_bf16(m, k, seed=4)
+    dc = torch.from_numpy(c).cuda()
+    ds = torch.from_numpy(s).cuda()
+    xt = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    assert q.qfmt_device_status() == 0
+    q.qfmt_debug_set(1, 20_000_000)          # 20 ms per wait
+    q.qfmt_debug_set(2, 1)                   # decoders never signal
+    try:
+        q.qmm(fmt, dc, ds, g, xt, n)
+        st = q.qfmt_device_status()
+    finally:
+        q.qfmt_debug_set(2, 0)
+        q.qfmt_debug_set(1, 0)
+    assert st == -6
+    assert "expired" in q.qfmt_last_error()
+    # the context is intact: the next call is correct and reports no error
+    out = q.qmm(fmt, dc, ds, g, xt, n).float().cpu().numpy()
+    assert q.qfmt_device_status() == 0
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    assert (np.abs(out - ref) <= bound + np.abs(out) * 2.0 ** -9).all()
+
+
+def test_debug_set_rejects_unknown_key():
+    with pytest.raises(q.QfmtError):
+        q.qfmt_debug_set(99, 1)

@@ -39,11 +39,12 @@ def test_expired_wait_reports_timeout_and_context_survives():
     try:
         q.qmm(fmt, dc, ds, g, xt, n)
         st = q.qfmt_device_status()
+        msg = q.qfmt_last_error()
     finally:
         q.qfmt_debug_set(2, 0)
         q.qfmt_debug_set(1, 0)
     assert st == -6
-    assert "expired" in q.qfmt_last_error()
+    assert "expired" in msg
     # the context is intact: the next call is correct and reports no error
     out = q.qmm(fmt, dc, ds, g, xt, n).float().cpu().numpy()
     assert q.qfmt_device_status() == 0

@@ -286,4 +286,53 @@ __device__ __forceinline__ void decode_piece_natural(const uint4& v, const Piece
   }
 }
 
+// ----------------------------------------------------- hi/lo bf16 splits ---
+// nvfp8 (E4M3 x float32 scale) and int4 affine (scale * q + bias) weights are
+// not exact in bf16.  Where a kernel cannot apply the block scale to float32
+// partial sums, the float32 weight v is carried as hi + lo with hi = bf16(v)
+// and lo = bf16(v - hi) (the subtraction is exact): |v - hi - lo| <= 2^-17 |v|.
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(a, b);
+  lo = pack_bf16x2(__fsub_rn(a, __uint_as_float(hi << 16)), __fsub_rn(b, __uint_as_float(hi & 0xFFFF0000u)));
+}
+
+// One 16-byte piece of an nvfp8 (16 codes) or int4-affine (32 codes) row as
+// hi/lo bf16 pairs in natural k order (8 or 16 registers each).
+template <int F>
+__device__ __forceinline__ void decode_piece_hilo(const uint4& v, const PieceScale& ps, uint32_t* hi, uint32_t* lo) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (F == NVFP8) {
+    const float s = __uint_as_float(ps.a);
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t r[2];
+      e4m3x4_bf16_raw(w[j], r);
+      const uint32_t e02 = hmul2(r[0], 0x7B807B80u), e13 = hmul2(r[1], 0x7B807B80u);   // x 2^120: exact values
+      const float v0 = __fmul_rn(__uint_as_float(e02 << 16), s), v2 = __fmul_rn(__uint_as_float(e02 & 0xFFFF0000u), s);
+      const float v1 = __fmul_rn(__uint_as_float(e13 << 16), s), v3 = __fmul_rn(__uint_as_float(e13 & 0xFFFF0000u), s);
+      split_bf16x2(v0, v1, hi[2 * j], lo[2 * j]);
+      split_bf16x2(v2, v3, hi[2 * j + 1], lo[2 * j + 1]);
+    }
+  } else {
+    const float s = bf16bits_f32(ps.a & 0xFFFFu), b = bf16bits_f32(ps.a >> 16);
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      #pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint32_t byte = (w[j] >> (8 * p)) & 0xFFu;
+        const float q0 = __fsub_rn(__uint_as_float(0x4B000000u | (byte & 0xFu)), 8388608.0f);
+        const float q1 = __fsub_rn(__uint_as_float(0x4B000000u | (byte >> 4)), 8388608.0f);
+        split_bf16x2(__fmaf_rn(s, q0, b), __fmaf_rn(s, q1, b), hi[4 * j + p], lo[4 * j + p]);
+      }
+    }
+  }
+}
+
 }  // namespace qfmt_dev

@@ -9,7 +9,8 @@
 // MMAs -- and maps it onto tcgen05:
 //
 //  * CTA tile 128 (M) x 256 (N), K step 64, four pipeline stages in shared
-//    memory (X tile 16 KiB + decoded W tile 32 KiB per stage);
+//    memory (X tile 16 KiB + decoded W tile 32 KiB per stage); nvfp8 and int4
+//    affine use a 128 x 128 tile whose weights are hi + lo bf16 pairs;
 //  * warp 0: one thread issues TMA loads of the X tile (128B-swizzled, K-major)
 //    and owns the TMEM allocation;
 //  * warp 1: one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> float32 in
@@ -18,8 +19,9 @@
 //  * warps 2-9: decoders.  Each streams 16-byte pieces of codes (plus their
 //    block scales) from global memory with 128-bit loads one K step ahead,
 //    decodes them in registers to bf16 with the block scale applied (exact for
-//    power-of-two and E4M3 scales; nvfp8 and int4-affine weights round once to
-//    bf16) and writes the canonical 128B-swizzled K-major layout the MMA reads;
+//    power-of-two and E4M3 scales; nvfp8 and int4-affine weights become
+//    float32 then a hi + lo bf16 pair, two MMAs per K slice) and writes the
+//    canonical 128B-swizzled K-major layout the MMA reads;
 //  * warps 2-5 (one per TMEM lane quadrant) then drain the accumulator with
 //    tcgen05.ld, apply the nvfp4 global scale and store bf16/float32 rows.
 //
@@ -41,16 +43,24 @@ __device__ unsigned int g_device_status;
 
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 128, BK = 64;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KiB
+constexpr int B_BYTES = 256 * BK * 2; // 32 KiB: 256 bf16 rows, or 128 hi rows + 128 lo rows
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int DEC_WARPS = 8;
 constexpr int DEC_THREADS = DEC_WARPS * 32;
 constexpr int THREADS = (2 + DEC_WARPS) * 32;
-constexpr int TMEM_COLS = 256;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+
+// Formats whose weights are exact in bf16 use a 128 x 256 tile; nvfp8 and int4
+// affine carry each weight as a hi + lo bf16 pair (two MMAs per K slice into
+// one accumulator) on a 128 x 128 tile, so a stage holds the same bytes.
+template <int F> struct Tile {
+  static constexpr bool split = F == NVFP8 || F == INT4_AFFINE;
+  static constexpr int BN = split ? 128 : 256;
+  static constexpr int TMEM_COLS = BN;
+};
 
 // ----------------------------------------------------------- PTX helpers ---
 
@@ -125,14 +135,18 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 
 // Instruction descriptor, kind::f16: D float32, A and B bf16, both K-major,
 // N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+template <int BN>
+__host__ __device__ constexpr uint32_t idesc_bf16() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+}
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -186,11 +200,16 @@ struct Params {
 template <int F>
 __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
   using T = FmtTraits<F>;
+  constexpr bool SPLIT = Tile<F>::split;
+  constexpr int BN = Tile<F>::BN;
+  constexpr int TMEM_COLS = Tile<F>::TMEM_COLS;
+  constexpr uint32_t IDESC = idesc_bf16<BN>();
   constexpr int PIECE = T::four ? 32 : 16;                 // codes per 16-byte piece
   constexpr int PIECES_PER_ROW = BK / PIECE;               // 2 or 4 per K step
-  constexpr int PIECES_PER_THREAD = BN * PIECES_PER_ROW / DEC_THREADS;   // 2 or 4
+  constexpr int PIECES_PER_THREAD = BN * PIECES_PER_ROW / DEC_THREADS;   // 1, 2 or 4
   constexpr int ROWS_PER_PASS = DEC_THREADS / PIECES_PER_ROW;            // 128 or 64
   constexpr int NREG = T::four ? 16 : 8;
+  constexpr uint32_t LO_OFF = uint32_t(BN) * BK * 2;       // lo rows follow the hi rows
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -265,8 +284,13 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
         tc_fence_after();
         const uint64_t ad = desc_sw128(stage_a(s)), bd = desc_sw128(stage_b(s));
         #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)   // +32 bytes along K per instruction
-          mma_f16(tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), (kb | kk) != 0);
+        for (int kk = 0; kk < BK / 16; ++kk) {  // +32 bytes along K per instruction
+          mma_f16(tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), IDESC, (kb | kk) != 0);
+          if constexpr (SPLIT) {
+            const uint64_t ld = desc_sw128(stage_b(s) + LO_OFF);
+            mma_f16(tmem, ad + uint64_t(2 * kk), ld + uint64_t(2 * kk), IDESC, 1u);
+          }
+        }
         mma_commit(empty(s));
       }
       mma_commit(done_bar);   // fires once every MMA issued above has completed
@@ -311,11 +335,22 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
       #pragma unroll
       for (int i = 0; i < PIECES_PER_THREAD; ++i) {
         const int r = rbase + i * ROWS_PER_PASS;
-        uint32_t w[NREG];
-        decode_piece_natural<F>(cur[i], cs[i], w);
-        #pragma unroll
-        for (int c = 0; c < NREG / 4; ++c)
-          sts128(bs + sw128_off(r, sub * (NREG / 4) + c), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        if constexpr (SPLIT) {
+          uint32_t hi[NREG], lo[NREG];
+          decode_piece_hilo<F>(cur[i], cs[i], hi, lo);
+          #pragma unroll
+          for (int c = 0; c < NREG / 4; ++c) {
+            const uint32_t off = sw128_off(r, sub * (NREG / 4) + c);
+            sts128(bs + off, hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+            sts128(bs + LO_OFF + off, lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+          }
+        } else {
+          uint32_t w[NREG];
+          decode_piece_natural<F>(cur[i], cs[i], w);
+          #pragma unroll
+          for (int c = 0; c < NREG / 4; ++c)
+            sts128(bs + sw128_off(r, sub * (NREG / 4) + c), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        }
         cur[i] = nxt[i];
         cs[i] = ns[i];
       }
@@ -439,7 +474,7 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, float glob,
   prm.out_f32 = out_f32 ? 1 : 0;
   prm.limit_ns = g_limit_ns.load();
   prm.drop_arrivals = g_drop.load();
-  dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+  dim3 grid((N + Tile<F>::BN - 1) / Tile<F>::BN, (M + BM - 1) / BM);
   qgemm_tc_kernel<F><<<grid, THREADS, SMEM_BYTES, st>>>(map, prm);
   return cudaGetLastError();
 }

@@ -127,10 +127,12 @@ def test_qgemm_parity(fmt, m):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-def test_short_and_odd_k(fmt):
-    # K of one block quantum and a K that leaves a partial chunk per warp
+@pytest.mark.parametrize("m", [3, 40, 130])
+def test_short_and_odd_k(fmt, m):
+    # K of one block quantum and K that leave partial chunks / K steps; few terms
+    # per output, so a per-weight rounding above the bound would show
     for k in ((64, 192) if fmt == "int4_affine" else (32, 96, 160)):
-        n, m = 33, 3
+        n = 33 if m < 17 else 300
         c, s, g = _packed(fmt, n, k, seed=k)
         xb, xt = _x(m, k, seed=k + 1)
         out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)

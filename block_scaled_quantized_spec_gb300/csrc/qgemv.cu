@@ -2,92 +2,164 @@
 //   out[m, n] = sum_k x[m, k] * dequant(W)[n, k]
 // (metaltile PR #250 qgemv commits: output[row] = sum_k dequant(weight[row,k])
 // * input[k], and the multi-row qmm; rlx-cpu thunk/ops/quant.rs
-// dequant_matmul_nvfp4, whose m == 1 loop streams the packed codes once).
+// dequant_matmul_nvfp4, whose m == 1 loop streams the packed codes once and
+// folds each block scale into a per-block partial sum, and lowp_scaled_matmul,
+// which factors both operands' block scales out of each block's sum).
 //
-// The pages' Metal kernels give each row one threadgroup and reduce with a
-// scalar loop; they note it reads at a low fraction of bandwidth.  Here the
-// work is shaped for GB300 instead:
-//  * a CTA owns 16 weight rows and 8 warps split K between them; every lane
-//    streams 16-byte pieces (32 four-bit / 16 eight-bit codes) of two rows with
-//    128-bit loads, four pieces per row per warp in flight;
-//  * codes are decoded in registers straight into bf16 tensor-core fragments
-//    with the block scale applied (exact for the power-of-two and E4M3 scales;
-//    nvfp8/int4-affine weights round once to bf16), and warp-level
-//    mma.sync m16n8k16 (bf16 in, float32 accumulate) multiplies them by the
-//    activations: weights are the 16-row A operand, activations the 8-column B
-//    operand (a second B block covers 9 <= M <= 16);
-//  * the per-warp partial tiles are summed through shared memory and the
-//    nvfp4 global scale is applied once to each output.
+// The pages' Metal GEMVs give each row one threadgroup and reduce with scalar
+// code; they note it reads at a low fraction of bandwidth.  On GB300 the HBM
+// delivers about 46 four-bit codes per SM per clock, so the decode has to cost
+// well under three issue slots per code.  The design:
+//  * a CTA owns 16 weight rows; its 8 warps split K in 64-code units, several
+//    units in flight per lane, every lane loading word t of each 16-byte row
+//    segment (the four lanes of a quad share each scale block);
+//  * element codes go to f16 with the hardware conversions (E2M1, E4M3, E5M2 ->
+//    f16x2 are exact; int4 becomes the exact f16 1024 + q), and the weights
+//    are the 16-row A operand of mma.sync m16n8k16 (f16 in, float32 out);
+//  * the activations are staged once per CTA in shared memory as f16 with a
+//    power-of-two scale per (row, 64-code unit) that puts the unit's largest
+//    |x| in [2^14, 2^15): exact for every bf16 value within 2^28 of that
+//    maximum;
+//  * block scales multiply float32 partial sums (one scale block per MMA k
+//    slice), except nvfp4 whose E4M3 micro-scale times the E2M1 value is exact
+//    in f16 and is applied before the MMA; the activation scale and the nvfp4
+//    global scale follow in float32;
+//  * per-warp partial tiles are summed through shared memory.
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "decode.cuh"
 #include "kernels.h"
 
 namespace qfmt_dev {
+namespace gemv {
 
-constexpr int GEMV_WARPS = 8;
-constexpr int GEMV_UNROLL = 4;
+constexpr int WARPS = 8;
 
-__device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_f16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+__device__ __forceinline__ uint32_t ldg32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 
-// Activation B-fragment halves for one column (batch row) over the same k
-// slots as decode_piece: xs points at the piece's first activation.
-template <bool FOUR>
-__device__ __forceinline__ void load_x_piece(const __nv_bfloat16* xs, bool ok, uint32_t B[FOUR ? 8 : 4][2]) {
-  if constexpr (FOUR) {
+__device__ __forceinline__ uint32_t ldg8(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// 8 E2M1 codes -> f16x2 in natural order (c0,c1) (c2,c3) (c4,c5) (c6,c7).
+__device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t r[4]) {
+  asm("{.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
+}
+
+// 4 E4M3 (or E5M2) codes -> f16x2 (c0,c1) (c2,c3).
+template <bool E5>
+__device__ __forceinline__ void f8x4_f16(uint32_t w, uint32_t r[2]) {
+  if constexpr (E5)
+    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.f16x2.e5m2x2 %0, h0;\n\tcvt.rn.f16x2.e5m2x2 %1, h1;}"
+        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
+  else
+    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;}"
+        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
+}
+
+// One E4M3 byte -> f16x2 with the value in both halves (exact).
+__device__ __forceinline__ uint32_t e4m3_f16x2_splat(uint32_t b) {
+  uint32_t r;
+  const uint16_t h = uint16_t(b | (b << 8));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// f16 bits of 1024 + q for 8 unsigned 4-bit q, paired (q0,q4) (q1,q5) (q2,q6) (q3,q7).
+__device__ __forceinline__ void int4x8_f16_biased(uint32_t w, uint32_t r[4]) {
+  r[0] = (w & 0x000F000Fu) | 0x64006400u;
+  r[1] = ((w >> 4) & 0x000F000Fu) | 0x64006400u;
+  r[2] = ((w >> 8) & 0x000F000Fu) | 0x64006400u;
+  r[3] = ((w >> 12) & 0x000F000Fu) | 0x64006400u;
+}
+
+template <int F>
+struct Cfg {
+  static constexpr bool four = FmtTraits<F>::four;
+  static constexpr int SEGS = four ? 2 : 4;        // 16-byte row segments per 64-code unit
+  static constexpr int UNROLL = four ? 4 : 2;      // units in flight per lane
+  static constexpr int NSC = (F == NVFP8) ? 4 : (F == INT4_AFFINE ? 1 : 2);   // scale words per row per unit
+};
+
+// Raw scale words of one row for one unit (64 codes starting at k).
+template <int F>
+__device__ __forceinline__ void load_unit_scales(const uint8_t* scales, int64_t row, int64_t nblk, int64_t k, int K,
+                                                 bool ok, int t, uint32_t s[Cfg<F>::NSC]) {
+  #pragma unroll
+  for (int i = 0; i < Cfg<F>::NSC; ++i) s[i] = 0u;
+  if (!ok) return;
+  const int64_t base = row * nblk;
+  if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+    s[0] = ldg8(scales + base + k / 32);
+    if (k + 32 < K) s[1] = ldg8(scales + base + k / 32 + 1);
+  } else if constexpr (F == NVFP4) {
+    // the lane's word of segment j lies in block (k + 32 j + 8 t) / 16
+    s[0] = ldg8(scales + base + (k + 8 * t) / 16);
+    if (k + 32 < K) s[1] = ldg8(scales + base + (k + 32 + 8 * t) / 16);
+  } else if constexpr (F == NVFP8) {
+    const uint32_t* sp = reinterpret_cast<const uint32_t*>(scales) + base + k / 16;
     #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint4 v = ok ? __ldg(reinterpret_cast<const uint4*>(xs) + j) : make_uint4(0, 0, 0, 0);
-      B[2 * j][0] = prmt(v.x, v.z, 0x5410u);      // (x0, x4)
-      B[2 * j][1] = prmt(v.x, v.z, 0x7632u);      // (x1, x5)
-      B[2 * j + 1][0] = prmt(v.y, v.w, 0x5410u);  // (x2, x6)
-      B[2 * j + 1][1] = prmt(v.y, v.w, 0x7632u);  // (x3, x7)
-    }
+    for (int i = 0; i < 4; ++i)
+      if (k + 16 * i < K) s[i] = ldg32(sp + i);
   } else {
-    #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint4 v = ok ? __ldg(reinterpret_cast<const uint4*>(xs) + h) : make_uint4(0, 0, 0, 0);
-      B[2 * h][0] = prmt(v.x, v.y, 0x5410u);      // (x0, x2)
-      B[2 * h][1] = prmt(v.x, v.y, 0x7632u);      // (x1, x3)
-      B[2 * h + 1][0] = prmt(v.z, v.w, 0x5410u);
-      B[2 * h + 1][1] = prmt(v.z, v.w, 0x7632u);
-    }
+    s[0] = ldg32(reinterpret_cast<const uint32_t*>(scales) + base + k / 64);
   }
 }
 
 template <int F, int NB>
-__global__ void __launch_bounds__(GEMV_WARPS * 32) qgemv_kernel(
-    const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, float glob,
-    const __nv_bfloat16* __restrict__ x, void* __restrict__ out, int out_f32, int M, int N, int K) {
-  using T = FmtTraits<F>;
-  constexpr int PIECE = T::four ? 32 : 16;  // codes per lane per row per chunk
-  constexpr int CHUNK = PIECE * 4;          // codes per row per chunk (one quad)
-  constexpr int STEPS = T::four ? 8 : 4;    // mma k16 steps per piece
-  __shared__ float red[GEMV_WARPS][16][8 * NB];
+__global__ void __launch_bounds__(WARPS * 32) qgemv_kernel(const uint8_t* __restrict__ codes,
+                                                           const uint8_t* __restrict__ scales, float glob,
+                                                           const uint16_t* __restrict__ x, void* __restrict__ out,
+                                                           int out_f32, int M, int N, int K, int KS) {
+  using C = Cfg<F>;
+  constexpr bool FOUR = C::four;
+  constexpr int SEGS = C::SEGS, U = C::UNROLL, NSC = C::NSC;
+  constexpr bool I4 = F == INT4_AFFINE;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int xstride = KS + 8;                                   // f16 elements per staged row (+16 B pad)
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+  float* xsc = reinterpret_cast<float*>(smem + size_t(M) * xstride * 2);   // [M][KS/64] 2^-shift
+  float* xsum = xsc + M * (KS / 64);                                        // [M][KS/64] (int4 affine)
+  __shared__ float red[WARPS][16][8 * NB];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int row0 = blockIdx.x * 16;
   const int rA = row0 + g, rB = row0 + g + 8;
   const bool okA = rA < N, okB = rB < N;
-  const int64_t row_bytes = T::four ? K / 2 : K;
-  const int64_t nblk = K / T::block;
-  const int nchunks = (K + CHUNK - 1) / CHUNK;
+  const int64_t row_bytes = FOUR ? K / 2 : K;
+  const int64_t nblk = K / FmtTraits<F>::block;
   const uint8_t* pA = codes + int64_t(okA ? rA : 0) * row_bytes;
   const uint8_t* pB = codes + int64_t(okB ? rB : 0) * row_bytes;
 
@@ -95,39 +167,179 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) qgemv_kernel(
   #pragma unroll
   for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
 
-  for (int c0 = warp; c0 < nchunks; c0 += GEMV_WARPS * GEMV_UNROLL) {
-    uint4 wa[GEMV_UNROLL], wb[GEMV_UNROLL];
-    PieceScale sa[GEMV_UNROLL], sb[GEMV_UNROLL];
-    bool kin[GEMV_UNROLL];
-    #pragma unroll
-    for (int u = 0; u < GEMV_UNROLL; ++u) {
-      const int c = c0 + u * GEMV_WARPS;
-      const int64_t k0 = int64_t(c) * CHUNK + t * PIECE;
-      kin[u] = c < nchunks && k0 < K;
-      const int64_t off = T::four ? k0 / 2 : k0;
-      wa[u] = kin[u] && okA ? ldg_stream(pA + off) : make_uint4(0, 0, 0, 0);
-      wb[u] = kin[u] && okB ? ldg_stream(pB + off) : make_uint4(0, 0, 0, 0);
-      sa[u] = load_piece_scale<F>(scales, rA, nblk, k0, kin[u] && okA);
-      sb[u] = load_piece_scale<F>(scales, rB, nblk, k0, kin[u] && okB);
-    }
-    #pragma unroll
-    for (int u = 0; u < GEMV_UNROLL; ++u) {
-      const int c = c0 + u * GEMV_WARPS;
-      if (c >= nchunks) break;
-      const int64_t k0 = int64_t(c) * CHUNK + t * PIECE;
-      uint32_t A0[STEPS][2], A1[STEPS][2];
-      decode_piece<F>(wa[u], sa[u], A0);
-      decode_piece<F>(wb[u], sb[u], A1);
+  for (int ks = 0; ks < K; ks += KS) {
+    const int kn = K - ks < KS ? K - ks : KS;
+    const int units = (kn + 63) / 64;
+
+    uint32_t wa[U][SEGS], wb[U][SEGS], sa[U][NSC], sb[U][NSC];
+    auto issue = [&](int i, int slot) {
+      const int u = warp + i * WARPS;
+      const int64_t k = int64_t(ks) + int64_t(u) * 64;
+      const bool ok = u < units;
       #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        const int m = nb * 8 + g;
-        uint32_t B[STEPS][2];
-        load_x_piece<T::four>(x + int64_t(m < M ? m : 0) * K + k0, kin[u] && m < M, B);
+      for (int sgm = 0; sgm < SEGS; ++sgm) {
+        const int64_t ksg = k + sgm * (FOUR ? 32 : 16);
+        const bool v = ok && ksg < K;
+        const int64_t off = (FOUR ? ksg / 2 : ksg) + 4 * t;
+        wa[slot][sgm] = v && okA ? ldg32(pA + off) : 0u;
+        wb[slot][sgm] = v && okB ? ldg32(pB + off) : 0u;
+      }
+      load_unit_scales<F>(scales, rA, nblk, k, K, ok && okA, t, sa[slot]);
+      load_unit_scales<F>(scales, rB, nblk, k, K, ok && okB, t, sb[slot]);
+    };
+    #pragma unroll
+    for (int i = 0; i < U; ++i) issue(i, i);
+
+    // ---- stage the activations of this K range as scaled f16 -------------
+    // 8 lanes per (row, 64-code unit), 8 values each; the shift puts the
+    // unit's max |x| in [2^14, 2^15).
+    const int tasks = M * units * 8;
+    for (int i = threadIdx.x; i < ((tasks + 255) & ~255); i += blockDim.x) {
+      const bool live = i < tasks;
+      const int m = live ? i / (units * 8) : 0;
+      const int rem = live ? i - m * units * 8 : 0;
+      const int u = rem >> 3, part = rem & 7;
+      const int64_t k = int64_t(ks) + u * 64 + part * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (live && k < K) v = __ldg(reinterpret_cast<const uint4*>(x + int64_t(m) * K + k));
+      const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+      uint32_t mx = 0;
+      #pragma unroll
+      for (int j = 0; j < 4; ++j) mx = max(mx, max(h[j] & 0x7FFFu, (h[j] >> 16) & 0x7FFFu));
+      mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+      mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+      const int E = int(mx >> 7);
+      int sh = (mx == 0u || E == 255) ? 0 : 141 - E;               // 14 - (E - 127)
+      sh = sh > 126 ? 126 : sh;
+      const float up = __uint_as_float(uint32_t(sh + 127) << 23);
+      float f[8];
+      #pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        f[2 * j] = __fmul_rn(__uint_as_float(h[j] << 16), up);
+        f[2 * j + 1] = __fmul_rn(__uint_as_float(h[j] & 0xFFFF0000u), up);
+      }
+      uint32_t o[4];
+      if constexpr (I4) {    // stored as (x0,x4) (x1,x5) (x2,x6) (x3,x7), the int4 pairing
         #pragma unroll
-        for (int s = 0; s < STEPS; ++s)
-          mma_bf16(acc[nb], A0[s][0], A1[s][0], A0[s][1], A1[s][1], B[s][0], B[s][1]);
+        for (int j = 0; j < 4; ++j) o[j] = pack_f16x2(f[j], f[j + 4]);
+      } else {
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = pack_f16x2(f[2 * j], f[2 * j + 1]);
+      }
+      if (live) {
+        *reinterpret_cast<uint4*>(xs + size_t(m) * xstride + u * 64 + part * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      if constexpr (I4) {    // sum of the staged (rounded) values
+        float sm = 0.0f;
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) sm += f16x2_lo(o[j]) + f16x2_hi(o[j]);
+        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
+        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 2);
+        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 4);
+        if (live && part == 0) xsum[m * (KS / 64) + u] = sm;
+      }
+      if (live && part == 0) xsc[m * (KS / 64) + u] = __uint_as_float(uint32_t(127 - sh) << 23);
+    }
+    __syncthreads();
+
+    // ---- stream the weights -------------------------------------------------
+    #pragma unroll 1
+    for (int i0 = 0; warp + i0 * WARPS < units; i0 += U) {
+      #pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int i = i0 + j;
+        const int u = warp + i * WARPS;
+        if (u >= units) break;
+        float d64[NB][4];
+        #pragma unroll
+        for (int nb = 0; nb < NB; ++nb) d64[nb][0] = d64[nb][1] = d64[nb][2] = d64[nb][3] = 0.0f;
+        #pragma unroll
+        for (int sgm = 0; sgm < SEGS; ++sgm) {
+          if constexpr (FOUR) {
+            uint32_t fa[4], fb[4];
+            if constexpr (I4) {
+              int4x8_f16_biased(wa[j][sgm], fa);
+              int4x8_f16_biased(wb[j][sgm], fb);
+            } else {
+              e2m1x8_f16(wa[j][sgm], fa);
+              e2m1x8_f16(wb[j][sgm], fb);
+              if constexpr (F == NVFP4) {
+                const uint32_t ca = e4m3_f16x2_splat(sa[j][sgm]), cb = e4m3_f16x2_splat(sb[j][sgm]);
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  fa[q] = hmul2_f16(fa[q], ca);
+                  fb[q] = hmul2_f16(fb[q], cb);
+                }
+              }
+            }
+            #pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const int m = min(nb * 8 + g, M - 1);
+              const uint4 xv = *reinterpret_cast<const uint4*>(xs + size_t(m) * xstride + u * 64 + sgm * 32 + 8 * t);
+              if constexpr (F == MXFP4) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_f16(d, fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+                mma_f16(d, fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
+                const float swa = e8m0_f32(sa[j][sgm]), swb = e8m0_f32(sb[j][sgm]);
+                d64[nb][0] = __fmaf_rn(swa, d[0], d64[nb][0]);
+                d64[nb][1] = __fmaf_rn(swa, d[1], d64[nb][1]);
+                d64[nb][2] = __fmaf_rn(swb, d[2], d64[nb][2]);
+                d64[nb][3] = __fmaf_rn(swb, d[3], d64[nb][3]);
+              } else {
+                mma_f16(d64[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+                mma_f16(d64[nb], fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
+              }
+            }
+          } else {
+            uint32_t fa[2], fb[2];
+            f8x4_f16<F == MXFP8_E5M2>(wa[j][sgm], fa);
+            f8x4_f16<F == MXFP8_E5M2>(wb[j][sgm], fb);
+            #pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const int m = min(nb * 8 + g, M - 1);
+              const uint2 xv = *reinterpret_cast<const uint2*>(xs + size_t(m) * xstride + u * 64 + sgm * 16 + 4 * t);
+              float d[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_f16(d, fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+              float swa, swb;
+              if constexpr (F == NVFP8) {
+                swa = __uint_as_float(sa[j][sgm]);
+                swb = __uint_as_float(sb[j][sgm]);
+              } else {
+                swa = e8m0_f32(sa[j][sgm >> 1]);
+                swb = e8m0_f32(sb[j][sgm >> 1]);
+              }
+              d64[nb][0] = __fmaf_rn(swa, d[0], d64[nb][0]);
+              d64[nb][1] = __fmaf_rn(swa, d[1], d64[nb][1]);
+              d64[nb][2] = __fmaf_rn(swb, d[2], d64[nb][2]);
+              d64[nb][3] = __fmaf_rn(swb, d[3], d64[nb][3]);
+            }
+          }
+        }
+        // unit epilogue: activation scale (and the int4 affine bias term)
+        #pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const int c0 = min(nb * 8 + 2 * t, M - 1), c1 = min(nb * 8 + 2 * t + 1, M - 1);
+          const float x0 = xsc[c0 * (KS / 64) + u], x1 = xsc[c1 * (KS / 64) + u];
+          if constexpr (I4) {
+            const float sA = bf16bits_f32(sa[j][0] & 0xFFFFu), bA = bf16bits_f32(sa[j][0] >> 16);
+            const float sB = bf16bits_f32(sb[j][0] & 0xFFFFu), bB = bf16bits_f32(sb[j][0] >> 16);
+            const float cA = __fmaf_rn(-1024.0f, sA, bA), cB = __fmaf_rn(-1024.0f, sB, bB);
+            const float m0 = xsum[c0 * (KS / 64) + u], m1 = xsum[c1 * (KS / 64) + u];
+            d64[nb][0] = __fmaf_rn(sA, d64[nb][0], cA * m0);
+            d64[nb][1] = __fmaf_rn(sA, d64[nb][1], cA * m1);
+            d64[nb][2] = __fmaf_rn(sB, d64[nb][2], cB * m0);
+            d64[nb][3] = __fmaf_rn(sB, d64[nb][3], cB * m1);
+          }
+          acc[nb][0] = __fmaf_rn(x0, d64[nb][0], acc[nb][0]);
+          acc[nb][1] = __fmaf_rn(x1, d64[nb][1], acc[nb][1]);
+          acc[nb][2] = __fmaf_rn(x0, d64[nb][2], acc[nb][2]);
+          acc[nb][3] = __fmaf_rn(x1, d64[nb][3], acc[nb][3]);
+        }
+        issue(i + U, j);   // refill this slot with the unit U ahead
       }
     }
+    __syncthreads();
   }
 
   // acc[nb]: c0 = (row g, col 2t), c1 = (g, 2t+1), c2 = (g+8, 2t), c3 = (g+8, 2t+1).
@@ -144,7 +356,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) qgemv_kernel(
     if (row0 + r >= N) continue;
     float sum = 0.0f;
     #pragma unroll
-    for (int w = 0; w < GEMV_WARPS; ++w) sum += red[w][r][m];
+    for (int w = 0; w < WARPS; ++w) sum += red[w][r][m];
     if constexpr (F == NVFP4) sum *= glob;
     const int64_t o = int64_t(m) * N + row0 + r;
     if (out_f32) static_cast<float*>(out)[o] = sum;
@@ -152,291 +364,59 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) qgemv_kernel(
   }
 }
 
-// ---------------------------------------------------------------------------
-// nvfp8 and int4 affine: the weights stay exact in bf16 (E4M3 codes, or the
-// integers 128 + q) and the block scale is applied to float32 partial sums.
-// That needs every mma.sync to draw its 16 k values from one block, so the
-// four lanes of a quad share each block: nvfp8 lanes take word t of each of
-// four consecutive 16-byte blocks (32-bit loads), int4 affine lanes take bytes
-// 8t..8t+7 of each of two 32-byte groups (64-bit loads).  int4 affine adds
-// one mma per step against a matrix of ones to get the activation sums the
-// affine bias multiplies: sum_k x (s q + b) = s sum_k x (128 + q) + (b - 128 s) sum_k x.
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ void mma_bf16_zero(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%10,%10,%10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+// Activations staged per pass: all of K up to 4096 (M <= 8) or 2048 (M > 8).
+inline int stage_k(int M, int K) {
+  const int cap = M <= 8 ? 4096 : 2048;
+  const int k64 = (K + 63) / 64 * 64;
+  return k64 < cap ? k64 : cap;
 }
 
-__device__ __forceinline__ uint32_t ldg32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint2 ldg64(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
+inline size_t smem_bytes(int F, int M, int KS) {
+  return size_t(M) * (KS + 8) * 2 + size_t(M) * (KS / 64) * 4 * (F == INT4_AFFINE ? 2 : 1);
 }
 
 template <int F, int NB>
-__global__ void __launch_bounds__(GEMV_WARPS * 32) qgemv_blockacc_kernel(
-    const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, const __nv_bfloat16* __restrict__ x,
-    void* __restrict__ out, int out_f32, int M, int N, int K) {
-  constexpr bool I4 = F == INT4_AFFINE;
-  constexpr int CHUNK = I4 ? 128 : 64;         // codes per row per chunk: 2 groups / 4 blocks
-  constexpr int NSUB = I4 ? 2 : 4;             // scale blocks per chunk
-  __shared__ float red[GEMV_WARPS][16][8 * NB];
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int row0 = blockIdx.x * 16;
-  const int rA = row0 + g, rB = row0 + g + 8;
-  const bool okA = rA < N, okB = rB < N;
-  const int64_t row_bytes = I4 ? K / 2 : K;
-  const int64_t nblk = K / (I4 ? 64 : 16);
-  const int nchunks = (K + CHUNK - 1) / CHUNK;
-  const uint8_t* pA = codes + int64_t(okA ? rA : 0) * row_bytes;
-  const uint8_t* pB = codes + int64_t(okB ? rB : 0) * row_bytes;
-  const int64_t sA0 = int64_t(okA ? rA : 0) * nblk, sB0 = int64_t(okB ? rB : 0) * nblk;
-
-  float acc[NB][4];
-  #pragma unroll
-  for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
-
-  for (int c0 = warp; c0 < nchunks; c0 += GEMV_WARPS * GEMV_UNROLL) {
-    // words[u][j]: nvfp8: word t of block j (4 codes); int4: word j of the lane's 8 bytes in group j/2
-    uint32_t wa[GEMV_UNROLL][4], wb[GEMV_UNROLL][4];
-    uint32_t sa[GEMV_UNROLL][NSUB], sb[GEMV_UNROLL][NSUB];
-    #pragma unroll
-    for (int u = 0; u < GEMV_UNROLL; ++u) {
-      const int c = c0 + u * GEMV_WARPS;
-      #pragma unroll
-      for (int j = 0; j < NSUB; ++j) {
-        const int64_t kb = int64_t(c) * CHUNK + j * (I4 ? 64 : 16);   // first k of the block
-        const bool ok = c < nchunks && kb < K;
-        const int64_t blk = kb / (I4 ? 64 : 16);
-        if constexpr (I4) {
-          const int64_t off = kb / 2 + 8 * t;
-          uint2 va = ok && okA ? ldg64(pA + off) : make_uint2(0, 0);
-          uint2 vb = ok && okB ? ldg64(pB + off) : make_uint2(0, 0);
-          wa[u][2 * j] = va.x; wa[u][2 * j + 1] = va.y;
-          wb[u][2 * j] = vb.x; wb[u][2 * j + 1] = vb.y;
-          sa[u][j] = ok && okA ? __ldg(reinterpret_cast<const uint32_t*>(scales) + sA0 + blk) : 0u;
-          sb[u][j] = ok && okB ? __ldg(reinterpret_cast<const uint32_t*>(scales) + sB0 + blk) : 0u;
-        } else {
-          const int64_t off = kb + 4 * t;
-          wa[u][j] = ok && okA ? ldg32(pA + off) : 0u;
-          wb[u][j] = ok && okB ? ldg32(pB + off) : 0u;
-          sa[u][j] = ok && okA ? __ldg(reinterpret_cast<const uint32_t*>(scales) + sA0 + blk) : 0u;
-          sb[u][j] = ok && okB ? __ldg(reinterpret_cast<const uint32_t*>(scales) + sB0 + blk) : 0u;
-        }
-      }
-    }
-    #pragma unroll
-    for (int u = 0; u < GEMV_UNROLL; ++u) {
-      const int c = c0 + u * GEMV_WARPS;
-      if (c >= nchunks) break;
-      #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        const int m = nb * 8 + g;
-        const bool mok = m < M;
-        const __nv_bfloat16* xr = x + int64_t(mok ? m : 0) * K;
-        #pragma unroll
-        for (int j = 0; j < NSUB; ++j) {
-          const int64_t kb = int64_t(c) * CHUNK + j * (I4 ? 64 : 16);
-          const bool ok = kb < K && mok;
-          if constexpr (I4) {
-            // lane's 16 activations of group j: k = kb + 16t .. +15 (two words of 8)
-            const uint4 v0 = ok ? __ldg(reinterpret_cast<const uint4*>(xr + kb + 16 * t)) : make_uint4(0, 0, 0, 0);
-            const uint4 v1 = ok ? __ldg(reinterpret_cast<const uint4*>(xr + kb + 16 * t + 8)) : make_uint4(0, 0, 0, 0);
-            float d[4] = {0.f, 0.f, 0.f, 0.f}, xs[4] = {0.f, 0.f, 0.f, 0.f};
-            #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint4 v = h ? v1 : v0;
-              uint32_t ra[4], rb[4];
-              int4x8_biased_bf16(wa[u][2 * j + h], ra);
-              int4x8_biased_bf16(wb[u][2 * j + h], rb);
-              const uint32_t b00 = prmt(v.x, v.z, 0x5410u), b01 = prmt(v.x, v.z, 0x7632u);
-              const uint32_t b10 = prmt(v.y, v.w, 0x5410u), b11 = prmt(v.y, v.w, 0x7632u);
-              mma_bf16(d, ra[0], rb[0], ra[1], rb[1], b00, b01);
-              mma_bf16(d, ra[2], rb[2], ra[3], rb[3], b10, b11);
-              const uint32_t one = 0x3F803F80u;
-              mma_bf16(xs, one, one, one, one, b00, b01);
-              mma_bf16(xs, one, one, one, one, b10, b11);
-            }
-            const float sA = bf16bits_f32(sa[u][j] & 0xFFFFu), bA = bf16bits_f32(sa[u][j] >> 16);
-            const float sB = bf16bits_f32(sb[u][j] & 0xFFFFu), bB = bf16bits_f32(sb[u][j] >> 16);
-            const float cA = __fmaf_rn(-128.0f, sA, bA), cB = __fmaf_rn(-128.0f, sB, bB);
-            acc[nb][0] = __fmaf_rn(sA, d[0], __fmaf_rn(cA, xs[0], acc[nb][0]));
-            acc[nb][1] = __fmaf_rn(sA, d[1], __fmaf_rn(cA, xs[1], acc[nb][1]));
-            acc[nb][2] = __fmaf_rn(sB, d[2], __fmaf_rn(cB, xs[2], acc[nb][2]));
-            acc[nb][3] = __fmaf_rn(sB, d[3], __fmaf_rn(cB, xs[3], acc[nb][3]));
-          } else {
-            // lane's 4 activations of block j: k = kb + 4t .. +3
-            const uint2 v = ok ? ldg64(xr + kb + 4 * t) : make_uint2(0, 0);
-            const uint32_t b0 = prmt(v.x, v.y, 0x5410u), b1 = prmt(v.x, v.y, 0x7632u);   // (x0,x2) (x1,x3)
-            uint32_t ra[2], rb[2];
-            e4m3x4_bf16_raw(wa[u][j], ra);
-            e4m3x4_bf16_raw(wb[u][j], rb);
-            const uint32_t k120 = 0x7B807B80u;                     // 2^120: exact E4M3 values
-            float d[4];
-            mma_bf16_zero(d, hmul2(ra[0], k120), hmul2(rb[0], k120), hmul2(ra[1], k120), hmul2(rb[1], k120), b0, b1);
-            const float sA = __uint_as_float(sa[u][j]), sB = __uint_as_float(sb[u][j]);
-            acc[nb][0] = __fmaf_rn(sA, d[0], acc[nb][0]);
-            acc[nb][1] = __fmaf_rn(sA, d[1], acc[nb][1]);
-            acc[nb][2] = __fmaf_rn(sB, d[2], acc[nb][2]);
-            acc[nb][3] = __fmaf_rn(sB, d[3], acc[nb][3]);
-          }
-        }
-      }
-    }
+static cudaError_t launch_nb(const uint8_t* c, const uint8_t* s, float glob, const uint16_t* x, void* out,
+                             bool out_f32, int M, int N, int K, cudaStream_t st) {
+  static std::atomic<int> attr_done[64];
+  const int KS = stage_k(M, K);
+  const size_t sm = smem_bytes(F, M, KS);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
+    const size_t cap = NB == 1 ? smem_bytes(F, 8, 4096) : smem_bytes(F, 16, 2048);
+    e = cudaFuncSetAttribute(qgemv_kernel<F, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(cap));
+    if (e != cudaSuccess) return e;
+    attr_done[dev].store(1);
   }
-
-  #pragma unroll
-  for (int nb = 0; nb < NB; ++nb) {
-    red[warp][g][nb * 8 + 2 * t] = acc[nb][0];
-    red[warp][g][nb * 8 + 2 * t + 1] = acc[nb][1];
-    red[warp][g + 8][nb * 8 + 2 * t] = acc[nb][2];
-    red[warp][g + 8][nb * 8 + 2 * t + 1] = acc[nb][3];
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 16 * M; i += blockDim.x) {
-    const int r = i & 15, m = i >> 4;
-    if (row0 + r >= N) continue;
-    float sum = 0.0f;
-    #pragma unroll
-    for (int w = 0; w < GEMV_WARPS; ++w) sum += red[w][r][m];
-    const int64_t o = int64_t(m) * N + row0 + r;
-    if (out_f32) static_cast<float*>(out)[o] = sum;
-    else static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(sum);
-  }
+  qgemv_kernel<F, NB><<<dim3((N + 15) / 16), dim3(WARPS * 32), sm, st>>>(c, s, glob, x, out, out_f32, M, N, K, KS);
+  return cudaGetLastError();
 }
 
 template <int F>
-static cudaError_t launch_qgemv_fmt(const void* codes, const void* scales, float glob, const void* x,
-                                    void* out, bool out_f32, int M, int N, int K, cudaStream_t st) {
-  dim3 grid((N + 15) / 16), block(GEMV_WARPS * 32);
+static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
+                              bool out_f32, int M, int N, int K, cudaStream_t st) {
   auto c = static_cast<const uint8_t*>(codes);
   auto s = static_cast<const uint8_t*>(scales);
-  auto xx = static_cast<const __nv_bfloat16*>(x);
-  if constexpr (F == NVFP8 || F == INT4_AFFINE) {
-    if (M <= 8) qgemv_blockacc_kernel<F, 1><<<grid, block, 0, st>>>(c, s, xx, out, out_f32, M, N, K);
-    else qgemv_blockacc_kernel<F, 2><<<grid, block, 0, st>>>(c, s, xx, out, out_f32, M, N, K);
-  } else {
-    if (M <= 8) qgemv_kernel<F, 1><<<grid, block, 0, st>>>(c, s, glob, xx, out, out_f32, M, N, K);
-    else qgemv_kernel<F, 2><<<grid, block, 0, st>>>(c, s, glob, xx, out, out_f32, M, N, K);
-  }
-  return cudaGetLastError();
+  auto xx = static_cast<const uint16_t*>(x);
+  if (M <= 8) return launch_nb<F, 1>(c, s, glob, xx, out, out_f32, M, N, K, st);
+  return launch_nb<F, 2>(c, s, glob, xx, out, out_f32, M, N, K, st);
 }
 
-cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float glob, const void* x,
-                         void* out, bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st,
-                         int sms) {
+}  // namespace gemv
+
+cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float glob, const void* x, void* out,
+                         bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms) {
   (void)sms;
   const int m = int(M), n = int(N), k = int(K);
   switch (fmt) {
-    case MXFP4: return launch_qgemv_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case NVFP4: return launch_qgemv_fmt<NVFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case MXFP8_E4M3: return launch_qgemv_fmt<MXFP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case MXFP8_E5M2: return launch_qgemv_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case NVFP8: return launch_qgemv_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    default: return launch_qgemv_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Float32 activations: CUDA-core path with exact float32 weights.
-// One warp per (row n, group of up to 8 batch rows); lanes stride K by pieces.
-// ---------------------------------------------------------------------------
-
-template <int F>
-__device__ __forceinline__ float exact_weight(uint32_t code, float s, float b) {
-  if constexpr (F == MXFP4 || F == NVFP4) return __fmul_rn(e2m1_f32(code), s);
-  if constexpr (F == MXFP8_E4M3 || F == NVFP8) return __fmul_rn(e4m3_f32(code), s);
-  if constexpr (F == MXFP8_E5M2) return __fmul_rn(e5m2_f32(code), s);
-  return __fmaf_rn(s, float(code), b);
-}
-
-template <int F>
-__global__ void __launch_bounds__(256) qmm_f32x_kernel(const uint8_t* __restrict__ codes,
-                                                       const uint8_t* __restrict__ scales, float glob,
-                                                       const float* __restrict__ x, void* __restrict__ out,
-                                                       int out_f32, int M, int N, int K) {
-  using T = FmtTraits<F>;
-  constexpr int PIECE = T::four ? 32 : 16;
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int mgroups = (M + 7) / 8;
-  if (wid >= int64_t(N) * mgroups) return;
-  const int n = int(wid / mgroups), m0 = int(wid % mgroups) * 8;
-  const int64_t row_bytes = T::four ? K / 2 : K;
-  const int64_t nblk = K / T::block;
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int k0 = lane * PIECE; k0 < K; k0 += 32 * PIECE) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(codes + n * row_bytes + (T::four ? k0 / 2 : k0)));
-    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-    #pragma unroll
-    for (int i = 0; i < PIECE; ++i) {
-      const int k = k0 + i;
-      const int64_t bi = n * nblk + k / T::block;
-      float s, b = 0.0f;
-      if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) s = e8m0_f32(scales[bi]);
-      else if constexpr (F == NVFP4) s = e4m3_f32(scales[bi]);
-      else if constexpr (F == NVFP8) s = reinterpret_cast<const float*>(scales)[bi];
-      else {
-        const uint32_t p = reinterpret_cast<const uint32_t*>(scales)[bi];
-        s = bf16bits_f32(p & 0xFFFFu);
-        b = bf16bits_f32(p >> 16);
-      }
-      const uint32_t code = T::four ? (wv[i >> 3] >> (4 * (i & 7))) & 0xFu : (wv[i >> 2] >> (8 * (i & 3))) & 0xFFu;
-      const float w = exact_weight<F>(code, s, b);
-      #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (m0 + j < M) acc[j] = __fmaf_rn(x[int64_t(m0 + j) * K + k], w, acc[j]);
-    }
-  }
-  #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float v = acc[j];
-    #pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    if (lane == 0 && m0 + j < M) {
-      if constexpr (F == NVFP4) v *= glob;
-      const int64_t oi = int64_t(m0 + j) * N + n;
-      if (out_f32) static_cast<float*>(out)[oi] = v;
-      else static_cast<__nv_bfloat16*>(out)[oi] = __float2bfloat16_rn(v);
-    }
-  }
-}
-
-template <int F>
-static cudaError_t launch_f32x_fmt(const void* codes, const void* scales, float glob, const float* x,
-                                   void* out, bool out_f32, int M, int N, int K, cudaStream_t st) {
-  const int64_t warps = int64_t(N) * ((M + 7) / 8);
-  const int64_t blocks = (warps * 32 + 255) / 256;
-  qmm_f32x_kernel<F><<<dim3(unsigned(blocks)), 256, 0, st>>>(
-      static_cast<const uint8_t*>(codes), static_cast<const uint8_t*>(scales), glob, x, out, out_f32, M, N, K);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_qmm_f32x(int fmt, const void* codes, const void* scales, float glob, const float* x,
-                            void* out, bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st,
-                            int sms) {
-  (void)sms;
-  const int m = int(M), n = int(N), k = int(K);
-  switch (fmt) {
-    case MXFP4: return launch_f32x_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case NVFP4: return launch_f32x_fmt<NVFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case MXFP8_E4M3: return launch_f32x_fmt<MXFP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case MXFP8_E5M2: return launch_f32x_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case NVFP8: return launch_f32x_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    default: return launch_f32x_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP4: return gemv::launch_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case NVFP4: return gemv::launch_fmt<NVFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP8_E4M3: return gemv::launch_fmt<MXFP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP8_E5M2: return gemv::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case NVFP8: return gemv::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    default: return gemv::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }
 

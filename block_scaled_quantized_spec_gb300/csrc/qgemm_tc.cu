@@ -43,15 +43,20 @@ __device__ unsigned int g_device_status;
 
 namespace tc {
 
-constexpr int BM = 128, BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
-constexpr int B_BYTES = 256 * BK * 2; // 32 KiB: 256 bf16 rows, or 128 hi rows + 128 lo rows
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BM = 128, BK = 64;          // one MMA covers 128 rows of X
+constexpr int B_BYTES = 256 * BK * 2;     // 32 KiB: 256 bf16 rows, or 128 hi rows + 128 lo rows
 constexpr int DEC_WARPS = 8;
 constexpr int DEC_THREADS = DEC_WARPS * 32;
 constexpr int THREADS = (2 + DEC_WARPS) * 32;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+
+// MT 128-row sub-tiles of X share each decoded weight tile: MT = 2 halves the
+// decode work per FLOP (two accumulators, all 512 TMEM columns at BN = 256).
+template <int MT> struct Pipe {
+  static constexpr int A_BYTES = MT * BM * BK * 2;            // 16 or 32 KiB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;       // 48 or 64 KiB
+  static constexpr int STAGES = MT == 2 ? 3 : 4;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+};
 
 // Formats whose weights are exact in bf16 use a 128 x 256 tile; nvfp8 and int4
 // affine carry each weight as a hi + lo bf16 pair (two MMAs per K slice into
@@ -59,7 +64,6 @@ constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 template <int F> struct Tile {
   static constexpr bool split = F == NVFP8 || F == INT4_AFFINE;
   static constexpr int BN = split ? 128 : 256;
-  static constexpr int TMEM_COLS = BN;
 };
 
 // ----------------------------------------------------------- PTX helpers ---
@@ -197,12 +201,13 @@ struct Params {
   int drop_arrivals;   // test hook: decoders never signal a stage (the waits must expire)
 };
 
-template <int F>
+template <int F, int MT>
 __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
   using T = FmtTraits<F>;
   constexpr bool SPLIT = Tile<F>::split;
   constexpr int BN = Tile<F>::BN;
-  constexpr int TMEM_COLS = Tile<F>::TMEM_COLS;
+  constexpr int TMEM_COLS = BN * MT;
+  constexpr int STAGES = Pipe<MT>::STAGES, STAGE_BYTES = Pipe<MT>::STAGE_BYTES, A_BYTES = Pipe<MT>::A_BYTES;
   constexpr uint32_t IDESC = idesc_bf16<BN>();
   constexpr int PIECE = T::four ? 32 : 16;                 // codes per 16-byte piece
   constexpr int PIECES_PER_ROW = BK / PIECE;               // 2 or 4 per K step
@@ -219,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM * MT;
   const int nkb = (p.K + BK - 1) / BK;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
@@ -282,13 +287,15 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
         if (*abort_flag) break;
         if (!mbar_wait(a_full(s), ph, p.limit_ns) || !mbar_wait(b_full(s), ph, p.limit_ns)) { fail(); break; }
         tc_fence_after();
-        const uint64_t ad = desc_sw128(stage_a(s)), bd = desc_sw128(stage_b(s));
+        const uint64_t bd = desc_sw128(stage_b(s)), ld = desc_sw128(stage_b(s) + LO_OFF);
         #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {  // +32 bytes along K per instruction
-          mma_f16(tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), IDESC, (kb | kk) != 0);
-          if constexpr (SPLIT) {
-            const uint64_t ld = desc_sw128(stage_b(s) + LO_OFF);
-            mma_f16(tmem, ad + uint64_t(2 * kk), ld + uint64_t(2 * kk), IDESC, 1u);
+          #pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint64_t ad = desc_sw128(stage_a(s) + uint32_t(mt * BM * BK * 2));
+            const uint32_t d = tmem + uint32_t(mt * BN);
+            mma_f16(d, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), IDESC, (kb | kk) != 0);
+            if constexpr (SPLIT) mma_f16(d, ad + uint64_t(2 * kk), ld + uint64_t(2 * kk), IDESC, 1u);
           }
         }
         mma_commit(empty(s));
@@ -302,8 +309,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
     const int64_t nblk = p.K / T::block;
     const int sub = dt % PIECES_PER_ROW;                   // piece index within the row's K step
     const int rbase = dt / PIECES_PER_ROW;
-    uint4 cur[PIECES_PER_THREAD];
-    PieceScale cs[PIECES_PER_THREAD];
+    uint4 cur[PIECES_PER_THREAD], nxt[PIECES_PER_THREAD];
+    PieceScale cs[PIECES_PER_THREAD], ns[PIECES_PER_THREAD];
     auto load = [&](int kb, uint4 (&v)[PIECES_PER_THREAD], PieceScale (&sc)[PIECES_PER_THREAD]) {
       #pragma unroll
       for (int i = 0; i < PIECES_PER_THREAD; ++i) {
@@ -316,6 +323,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
       }
     };
     load(0, cur, cs);
+    load(1, nxt, ns);
     bool aborted = false;
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % STAGES;
@@ -328,9 +336,9 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
         aborted = true;
         break;
       }
-      uint4 nxt[PIECES_PER_THREAD];
-      PieceScale ns[PIECES_PER_THREAD];
-      load(kb + 1, nxt, ns);                               // next K step's codes in flight
+      uint4 nx2[PIECES_PER_THREAD];
+      PieceScale ns2[PIECES_PER_THREAD];
+      load(kb + 2, nx2, ns2);                              // codes two K steps ahead in flight
       const uint32_t bs = stage_b(s);
       #pragma unroll
       for (int i = 0; i < PIECES_PER_THREAD; ++i) {
@@ -353,6 +361,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
         }
         cur[i] = nxt[i];
         cs[i] = ns[i];
+        nxt[i] = nx2[i];
+        ns[i] = ns2[i];
       }
       fence_proxy_async();                                 // generic-proxy stores -> tensor core reads
       __syncwarp();
@@ -360,19 +370,20 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
     }
     (void)aborted;
     // --------------------------------------------------------------- epilogue
-    if (warp < 6) {
+    if (warp < 2 + 4 * MT) {
       int ok = 1;
       if (lane == 0) ok = mbar_wait(done_bar, 0, p.limit_ns);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok && lane == 0) fail();
       tc_fence_after();
       const int q = warp & 3;                              // TMEM lane quadrant of this warp
-      const int m = m0 + q * 32 + lane;
+      const int mt = (warp - 2) >> 2;                      // accumulator (128-row sub-tile)
+      const int m = m0 + mt * BM + q * 32 + lane;
       const bool live = ok && *abort_flag == 0u;
       #pragma unroll 1
       for (int cb = 0; cb < BN / 32; ++cb) {
         uint32_t r[32];
-        tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(cb * 32), r);
+        tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(mt * BN + cb * 32), r);
         const int nb = n0 + cb * 32;
         if (!live || m >= p.M || nb >= p.N) continue;
         float v[32];
@@ -440,24 +451,23 @@ static EncodeTiledFn encode_fn() {
 static std::atomic<uint64_t> g_limit_ns{2000000000ull};
 static std::atomic<int> g_drop{0};
 
-template <int F>
-static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
-                              bool out_f32, int M, int N, int K, cudaStream_t st) {
+template <int F, int MT>
+static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* scales, float glob, const void* x,
+                             void* out, bool out_f32, int M, int N, int K, cudaStream_t st) {
   static std::atomic<int> attr_done[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
-    e = cudaFuncSetAttribute(qgemm_tc_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(qgemm_tc_kernel<F, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Pipe<MT>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done[dev].store(1);
   }
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
   const cuuint64_t gdim[2] = {cuuint64_t(K), cuuint64_t(M)};
   const cuuint64_t gstride[1] = {cuuint64_t(K) * 2};
-  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t box[2] = {BK, cuuint32_t(BM * MT)};
   const cuuint32_t estride[2] = {1, 1};
   CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), gdim, gstride, box, estride,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -474,9 +484,19 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, float glob,
   prm.out_f32 = out_f32 ? 1 : 0;
   prm.limit_ns = g_limit_ns.load();
   prm.drop_arrivals = g_drop.load();
-  dim3 grid((N + Tile<F>::BN - 1) / Tile<F>::BN, (M + BM - 1) / BM);
-  qgemm_tc_kernel<F><<<grid, THREADS, SMEM_BYTES, st>>>(map, prm);
+  dim3 grid((N + Tile<F>::BN - 1) / Tile<F>::BN, (M + BM * MT - 1) / (BM * MT));
+  qgemm_tc_kernel<F, MT><<<grid, THREADS, Pipe<MT>::SMEM_BYTES, st>>>(map, prm);
   return cudaGetLastError();
+}
+
+// 256-row tiles once M exceeds one 128-row tile.
+template <int F>
+static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
+                              bool out_f32, int M, int N, int K, cudaStream_t st) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  if (M > BM) return launch_mt<F, 2>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st);
+  return launch_mt<F, 1>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st);
 }
 
 }  // namespace tc

@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
   const int64_t pieces_per_row = K / PIECE;
   const int64_t total = N * pieces_per_row;
   const int64_t nblk = K / T::block;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int64_t p = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; p < total;
        p += int64_t(gridDim.x) * blockDim.x) {
     const int64_t row = p / pieces_per_row;
@@ -100,9 +102,18 @@ static cudaError_t launch_dequant_fmt(const void* codes, const void* scales, flo
   if (grid < 1) grid = 1;
   auto c = static_cast<const uint8_t*>(codes);
   auto s = static_cast<const uint8_t*>(scales);
-  if (bf16) dequant_kernel<F, true><<<grid, threads, 0, st>>>(c, s, glob, out, N, K);
-  else dequant_kernel<F, false><<<grid, threads, 0, st>>>(c, s, glob, out, N, K);
-  return cudaGetLastError();
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(threads);
+  lc.stream = st;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  cudaError_t e = bf16 ? cudaLaunchKernelEx(&lc, dequant_kernel<F, true>, c, s, glob, out, N, K)
+                       : cudaLaunchKernelEx(&lc, dequant_kernel<F, false>, c, s, glob, out, N, K);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_dequant(int fmt, const void* codes, const void* scales, float glob, void* out,

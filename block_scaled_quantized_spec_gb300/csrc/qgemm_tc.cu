@@ -23,7 +23,10 @@
 //    float32 then a hi + lo bf16 pair, two MMAs per K slice) and writes the
 //    canonical 128B-swizzled K-major layout the MMA reads;
 //  * warps 2-5 (one per TMEM lane quadrant) then drain the accumulator with
-//    tcgen05.ld, apply the nvfp4 global scale and store bf16/float32 rows.
+//    tcgen05.ld, apply the nvfp4 global scale and store bf16/float32 rows;
+//  * the launch is programmatic-dependent: weight codes stream in while the
+//    preceding kernel finishes, X is read and `out` written only after
+//    griddepcontrol.wait.
 //
 // Every mbarrier wait is bounded by a time limit; on expiry the kernel records
 // an error in a device status word, lets in-flight copies and MMAs finish,
@@ -260,10 +263,15 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The next kernel in the stream may launch now; X (and `out`) are touched only
+  // after griddepcontrol.wait, the weights (not produced by the preceding kernel)
+  // stream in right away.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       int issued = 0;
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % STAGES;
@@ -380,6 +388,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
       const int mt = (warp - 2) >> 2;                      // accumulator (128-row sub-tile)
       const int m = m0 + mt * BM + q * 32 + lane;
       const bool live = ok && *abort_flag == 0u;
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       #pragma unroll 1
       for (int cb = 0; cb < BN / 32; ++cb) {
         uint32_t r[32];
@@ -484,9 +493,18 @@ static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* s
   prm.out_f32 = out_f32 ? 1 : 0;
   prm.limit_ns = g_limit_ns.load();
   prm.drop_arrivals = g_drop.load();
-  dim3 grid((N + Tile<F>::BN - 1) / Tile<F>::BN, (M + BM * MT - 1) / (BM * MT));
-  qgemm_tc_kernel<F, MT><<<grid, THREADS, Pipe<MT>::SMEM_BYTES, st>>>(map, prm);
-  return cudaGetLastError();
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.gridDim = dim3((N + Tile<F>::BN - 1) / Tile<F>::BN, (M + BM * MT - 1) / (BM * MT));
+  lc.blockDim = dim3(THREADS);
+  lc.dynamicSmemBytes = Pipe<MT>::SMEM_BYTES;
+  lc.stream = st;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&lc, qgemm_tc_kernel<F, MT>, map, prm);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // 256-row tiles once M exceeds one 128-row tile.

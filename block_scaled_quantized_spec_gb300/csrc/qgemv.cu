@@ -104,20 +104,20 @@ __device__ __forceinline__ void int4x8_f16_biased(uint32_t w, uint32_t r[4]) {
   r[3] = ((w >> 12) & 0x000F000Fu) | 0x64006400u;
 }
 
-template <int F>
+template <int F, int R>
 struct Cfg {
   static constexpr bool four = FmtTraits<F>::four;
   static constexpr int SEGS = four ? 2 : 4;        // 16-byte row segments per 64-code unit
-  static constexpr int UNROLL = four ? 4 : 2;      // units in flight per lane
+  static constexpr int UNROLL = four ? (R == 1 ? 4 : 2) : (R == 1 ? 2 : 1);   // units in flight per lane
   static constexpr int NSC = (F == NVFP8) ? 4 : (F == INT4_AFFINE ? 1 : 2);   // scale words per row per unit
 };
 
 // Raw scale words of one row for one unit (64 codes starting at k).
-template <int F>
+template <int F, int NSC>
 __device__ __forceinline__ void load_unit_scales(const uint8_t* scales, int64_t row, int64_t nblk, int64_t k, int K,
-                                                 bool ok, int t, uint32_t s[Cfg<F>::NSC]) {
+                                                 bool ok, int t, uint32_t s[NSC]) {
   #pragma unroll
-  for (int i = 0; i < Cfg<F>::NSC; ++i) s[i] = 0u;
+  for (int i = 0; i < NSC; ++i) s[i] = 0u;
   if (!ok) return;
   const int64_t base = row * nblk;
   if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) {
@@ -137,58 +137,175 @@ __device__ __forceinline__ void load_unit_scales(const uint8_t* scales, int64_t 
   }
 }
 
-template <int F, int NB>
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// One warp multiplies a 16-row weight tile (rows g and g+8 per lane) for one
+// 64-code unit against the staged activations, into d64 (float32, per column
+// block).  wa/wb: the lane's words of the two rows, sa/sb: their scale words.
+template <int F, int NB, int SEGS, int NSC>
+__device__ __forceinline__ void tile_unit(const uint32_t (&wa)[SEGS], const uint32_t (&wb)[SEGS],
+                                          const uint32_t (&sa)[NSC], const uint32_t (&sb)[NSC],
+                                          const uint16_t* xs, int xstride, int u, int M, int g, int t,
+                                          float (&d64)[NB][4]) {
+  constexpr bool FOUR = FmtTraits<F>::four;
+  constexpr bool I4 = F == INT4_AFFINE;
+  #pragma unroll
+  for (int nb = 0; nb < NB; ++nb) d64[nb][0] = d64[nb][1] = d64[nb][2] = d64[nb][3] = 0.0f;
+  #pragma unroll
+  for (int sgm = 0; sgm < SEGS; ++sgm) {
+    if constexpr (FOUR) {
+      uint32_t fa[4], fb[4];
+      if constexpr (I4) {
+        int4x8_f16_biased(wa[sgm], fa);
+        int4x8_f16_biased(wb[sgm], fb);
+      } else {
+        e2m1x8_f16(wa[sgm], fa);
+        e2m1x8_f16(wb[sgm], fb);
+        if constexpr (F == NVFP4) {
+          const uint32_t ca = e4m3_f16x2_splat(sa[sgm]), cb = e4m3_f16x2_splat(sb[sgm]);
+          #pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            fa[q] = hmul2_f16(fa[q], ca);
+            fb[q] = hmul2_f16(fb[q], cb);
+          }
+        }
+      }
+      #pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const int m = min(nb * 8 + g, M - 1);
+        const uint4 xv = *reinterpret_cast<const uint4*>(xs + size_t(m) * xstride + u * 64 + sgm * 32 + 8 * t);
+        if constexpr (F == MXFP4) {
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_f16(d, fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+          mma_f16(d, fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
+          const float swa = e8m0_f32(sa[sgm]), swb = e8m0_f32(sb[sgm]);
+          d64[nb][0] = __fmaf_rn(swa, d[0], d64[nb][0]);
+          d64[nb][1] = __fmaf_rn(swa, d[1], d64[nb][1]);
+          d64[nb][2] = __fmaf_rn(swb, d[2], d64[nb][2]);
+          d64[nb][3] = __fmaf_rn(swb, d[3], d64[nb][3]);
+        } else {
+          mma_f16(d64[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+          mma_f16(d64[nb], fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
+        }
+      }
+    } else {
+      uint32_t fa[2], fb[2];
+      f8x4_f16<F == MXFP8_E5M2>(wa[sgm], fa);
+      f8x4_f16<F == MXFP8_E5M2>(wb[sgm], fb);
+      #pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const int m = min(nb * 8 + g, M - 1);
+        const uint2 xv = *reinterpret_cast<const uint2*>(xs + size_t(m) * xstride + u * 64 + sgm * 16 + 4 * t);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16(d, fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+        float swa, swb;
+        if constexpr (F == NVFP8) {
+          swa = __uint_as_float(sa[sgm]);
+          swb = __uint_as_float(sb[sgm]);
+        } else {
+          swa = e8m0_f32(sa[sgm >> 1]);
+          swb = e8m0_f32(sb[sgm >> 1]);
+        }
+        d64[nb][0] = __fmaf_rn(swa, d[0], d64[nb][0]);
+        d64[nb][1] = __fmaf_rn(swa, d[1], d64[nb][1]);
+        d64[nb][2] = __fmaf_rn(swb, d[2], d64[nb][2]);
+        d64[nb][3] = __fmaf_rn(swb, d[3], d64[nb][3]);
+      }
+    }
+  }
+}
+
+template <int F, int NB, int R>
 __global__ void __launch_bounds__(WARPS * 32) qgemv_kernel(const uint8_t* __restrict__ codes,
                                                            const uint8_t* __restrict__ scales, float glob,
                                                            const uint16_t* __restrict__ x, void* __restrict__ out,
                                                            int out_f32, int M, int N, int K, int KS) {
-  using C = Cfg<F>;
+  using C = Cfg<F, R>;
   constexpr bool FOUR = C::four;
   constexpr int SEGS = C::SEGS, U = C::UNROLL, NSC = C::NSC;
   constexpr bool I4 = F == INT4_AFFINE;
+  constexpr int ROWS = 16 * R;
   extern __shared__ __align__(16) uint8_t smem[];
   const int xstride = KS + 8;                                   // f16 elements per staged row (+16 B pad)
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
   float* xsc = reinterpret_cast<float*>(smem + size_t(M) * xstride * 2);   // [M][KS/64] 2^-shift
   float* xsum = xsc + M * (KS / 64);                                        // [M][KS/64] (int4 affine)
-  __shared__ float red[WARPS][16][8 * NB];
+  float* red = xsum + (I4 ? M * (KS / 64) : 0);                             // [WARPS][ROWS][8 NB]
+
+  // Let the next kernel in the stream start its own weight traffic now.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
-  const int row0 = blockIdx.x * 16;
-  const int rA = row0 + g, rB = row0 + g + 8;
-  const bool okA = rA < N, okB = rB < N;
+  const int row0 = blockIdx.x * ROWS;
   const int64_t row_bytes = FOUR ? K / 2 : K;
   const int64_t nblk = K / FmtTraits<F>::block;
-  const uint8_t* pA = codes + int64_t(okA ? rA : 0) * row_bytes;
-  const uint8_t* pB = codes + int64_t(okB ? rB : 0) * row_bytes;
+  const int sbytes = FmtTraits<F>::sbytes;
 
-  float acc[NB][4];
+  // Weights do not depend on the preceding kernel: pull this CTA's rows into L2.
+  if (lane == 0) {
+    #pragma unroll 1
+    for (int rr = warp * (ROWS / WARPS); rr < (warp + 1) * (ROWS / WARPS); ++rr) {
+      const int row = row0 + rr;
+      if (row < N) {
+        prefetch_l2(codes + int64_t(row) * row_bytes, uint32_t(row_bytes));
+        const uint32_t sb = uint32_t(nblk * sbytes);
+        if ((sb & 15u) == 0 && ((int64_t(row) * nblk * sbytes) & 15) == 0)
+          prefetch_l2(scales + int64_t(row) * nblk * sbytes, sb);
+      }
+    }
+  }
+
+  const uint8_t* pA[R];
+  const uint8_t* pB[R];
+  int rowA[R], rowB[R];
+  bool okA[R], okB[R];
   #pragma unroll
-  for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
+  for (int r = 0; r < R; ++r) {
+    rowA[r] = row0 + 16 * r + g;
+    rowB[r] = rowA[r] + 8;
+    okA[r] = rowA[r] < N;
+    okB[r] = rowB[r] < N;
+    pA[r] = codes + int64_t(okA[r] ? rowA[r] : 0) * row_bytes;
+    pB[r] = codes + int64_t(okB[r] ? rowB[r] : 0) * row_bytes;
+  }
+
+  float acc[R][NB][4];
+  #pragma unroll
+  for (int r = 0; r < R; ++r)
+    #pragma unroll
+    for (int nb = 0; nb < NB; ++nb) acc[r][nb][0] = acc[r][nb][1] = acc[r][nb][2] = acc[r][nb][3] = 0.0f;
+
+  uint32_t wa[U][R][SEGS], wb[U][R][SEGS], sa[U][R][NSC], sb[U][R][NSC];
 
   for (int ks = 0; ks < K; ks += KS) {
     const int kn = K - ks < KS ? K - ks : KS;
     const int units = (kn + 63) / 64;
-
-    uint32_t wa[U][SEGS], wb[U][SEGS], sa[U][NSC], sb[U][NSC];
     auto issue = [&](int i, int slot) {
       const int u = warp + i * WARPS;
       const int64_t k = int64_t(ks) + int64_t(u) * 64;
       const bool ok = u < units;
       #pragma unroll
-      for (int sgm = 0; sgm < SEGS; ++sgm) {
-        const int64_t ksg = k + sgm * (FOUR ? 32 : 16);
-        const bool v = ok && ksg < K;
-        const int64_t off = (FOUR ? ksg / 2 : ksg) + 4 * t;
-        wa[slot][sgm] = v && okA ? ldg32(pA + off) : 0u;
-        wb[slot][sgm] = v && okB ? ldg32(pB + off) : 0u;
+      for (int r = 0; r < R; ++r) {
+        #pragma unroll
+        for (int sgm = 0; sgm < SEGS; ++sgm) {
+          const int64_t ksg = k + sgm * (FOUR ? 32 : 16);
+          const bool v = ok && ksg < K;
+          const int64_t off = (FOUR ? ksg / 2 : ksg) + 4 * t;
+          wa[slot][r][sgm] = v && okA[r] ? ldg32(pA[r] + off) : 0u;
+          wb[slot][r][sgm] = v && okB[r] ? ldg32(pB[r] + off) : 0u;
+        }
+        load_unit_scales<F, NSC>(scales, rowA[r], nblk, k, K, ok && okA[r], t, sa[slot][r]);
+        load_unit_scales<F, NSC>(scales, rowB[r], nblk, k, K, ok && okB[r], t, sb[slot][r]);
       }
-      load_unit_scales<F>(scales, rA, nblk, k, K, ok && okA, t, sa[slot]);
-      load_unit_scales<F>(scales, rB, nblk, k, K, ok && okB, t, sb[slot]);
     };
     #pragma unroll
     for (int i = 0; i < U; ++i) issue(i, i);
+
+    // The activations may be the preceding kernel's output: wait for it (once).
+    if (ks == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- stage the activations of this K range as scaled f16 -------------
     // 8 lanes per (row, 64-code unit), 8 values each; the shift puts the
@@ -227,9 +344,8 @@ __global__ void __launch_bounds__(WARPS * 32) qgemv_kernel(const uint8_t* __rest
         #pragma unroll
         for (int j = 0; j < 4; ++j) o[j] = pack_f16x2(f[2 * j], f[2 * j + 1]);
       }
-      if (live) {
+      if (live)
         *reinterpret_cast<uint4*>(xs + size_t(m) * xstride + u * 64 + part * 8) = make_uint4(o[0], o[1], o[2], o[3]);
-      }
       if constexpr (I4) {    // sum of the staged (rounded) values
         float sm = 0.0f;
         #pragma unroll
@@ -251,90 +367,29 @@ __global__ void __launch_bounds__(WARPS * 32) qgemv_kernel(const uint8_t* __rest
         const int i = i0 + j;
         const int u = warp + i * WARPS;
         if (u >= units) break;
-        float d64[NB][4];
         #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) d64[nb][0] = d64[nb][1] = d64[nb][2] = d64[nb][3] = 0.0f;
-        #pragma unroll
-        for (int sgm = 0; sgm < SEGS; ++sgm) {
-          if constexpr (FOUR) {
-            uint32_t fa[4], fb[4];
+        for (int r = 0; r < R; ++r) {
+          float d64[NB][4];
+          tile_unit<F, NB, SEGS, NSC>(wa[j][r], wb[j][r], sa[j][r], sb[j][r], xs, xstride, u, M, g, t, d64);
+          #pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            const int c0 = min(nb * 8 + 2 * t, M - 1), c1 = min(nb * 8 + 2 * t + 1, M - 1);
+            const float x0 = xsc[c0 * (KS / 64) + u], x1 = xsc[c1 * (KS / 64) + u];
             if constexpr (I4) {
-              int4x8_f16_biased(wa[j][sgm], fa);
-              int4x8_f16_biased(wb[j][sgm], fb);
-            } else {
-              e2m1x8_f16(wa[j][sgm], fa);
-              e2m1x8_f16(wb[j][sgm], fb);
-              if constexpr (F == NVFP4) {
-                const uint32_t ca = e4m3_f16x2_splat(sa[j][sgm]), cb = e4m3_f16x2_splat(sb[j][sgm]);
-                #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  fa[q] = hmul2_f16(fa[q], ca);
-                  fb[q] = hmul2_f16(fb[q], cb);
-                }
-              }
+              const float sA = bf16bits_f32(sa[j][r][0] & 0xFFFFu), bA = bf16bits_f32(sa[j][r][0] >> 16);
+              const float sB = bf16bits_f32(sb[j][r][0] & 0xFFFFu), bB = bf16bits_f32(sb[j][r][0] >> 16);
+              const float cA = __fmaf_rn(-1024.0f, sA, bA), cB = __fmaf_rn(-1024.0f, sB, bB);
+              const float m0 = xsum[c0 * (KS / 64) + u], m1 = xsum[c1 * (KS / 64) + u];
+              d64[nb][0] = __fmaf_rn(sA, d64[nb][0], cA * m0);
+              d64[nb][1] = __fmaf_rn(sA, d64[nb][1], cA * m1);
+              d64[nb][2] = __fmaf_rn(sB, d64[nb][2], cB * m0);
+              d64[nb][3] = __fmaf_rn(sB, d64[nb][3], cB * m1);
             }
-            #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-              const int m = min(nb * 8 + g, M - 1);
-              const uint4 xv = *reinterpret_cast<const uint4*>(xs + size_t(m) * xstride + u * 64 + sgm * 32 + 8 * t);
-              if constexpr (F == MXFP4) {
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_f16(d, fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
-                mma_f16(d, fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
-                const float swa = e8m0_f32(sa[j][sgm]), swb = e8m0_f32(sb[j][sgm]);
-                d64[nb][0] = __fmaf_rn(swa, d[0], d64[nb][0]);
-                d64[nb][1] = __fmaf_rn(swa, d[1], d64[nb][1]);
-                d64[nb][2] = __fmaf_rn(swb, d[2], d64[nb][2]);
-                d64[nb][3] = __fmaf_rn(swb, d[3], d64[nb][3]);
-              } else {
-                mma_f16(d64[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
-                mma_f16(d64[nb], fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
-              }
-            }
-          } else {
-            uint32_t fa[2], fb[2];
-            f8x4_f16<F == MXFP8_E5M2>(wa[j][sgm], fa);
-            f8x4_f16<F == MXFP8_E5M2>(wb[j][sgm], fb);
-            #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-              const int m = min(nb * 8 + g, M - 1);
-              const uint2 xv = *reinterpret_cast<const uint2*>(xs + size_t(m) * xstride + u * 64 + sgm * 16 + 4 * t);
-              float d[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_f16(d, fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
-              float swa, swb;
-              if constexpr (F == NVFP8) {
-                swa = __uint_as_float(sa[j][sgm]);
-                swb = __uint_as_float(sb[j][sgm]);
-              } else {
-                swa = e8m0_f32(sa[j][sgm >> 1]);
-                swb = e8m0_f32(sb[j][sgm >> 1]);
-              }
-              d64[nb][0] = __fmaf_rn(swa, d[0], d64[nb][0]);
-              d64[nb][1] = __fmaf_rn(swa, d[1], d64[nb][1]);
-              d64[nb][2] = __fmaf_rn(swb, d[2], d64[nb][2]);
-              d64[nb][3] = __fmaf_rn(swb, d[3], d64[nb][3]);
-            }
+            acc[r][nb][0] = __fmaf_rn(x0, d64[nb][0], acc[r][nb][0]);
+            acc[r][nb][1] = __fmaf_rn(x1, d64[nb][1], acc[r][nb][1]);
+            acc[r][nb][2] = __fmaf_rn(x0, d64[nb][2], acc[r][nb][2]);
+            acc[r][nb][3] = __fmaf_rn(x1, d64[nb][3], acc[r][nb][3]);
           }
-        }
-        // unit epilogue: activation scale (and the int4 affine bias term)
-        #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const int c0 = min(nb * 8 + 2 * t, M - 1), c1 = min(nb * 8 + 2 * t + 1, M - 1);
-          const float x0 = xsc[c0 * (KS / 64) + u], x1 = xsc[c1 * (KS / 64) + u];
-          if constexpr (I4) {
-            const float sA = bf16bits_f32(sa[j][0] & 0xFFFFu), bA = bf16bits_f32(sa[j][0] >> 16);
-            const float sB = bf16bits_f32(sb[j][0] & 0xFFFFu), bB = bf16bits_f32(sb[j][0] >> 16);
-            const float cA = __fmaf_rn(-1024.0f, sA, bA), cB = __fmaf_rn(-1024.0f, sB, bB);
-            const float m0 = xsum[c0 * (KS / 64) + u], m1 = xsum[c1 * (KS / 64) + u];
-            d64[nb][0] = __fmaf_rn(sA, d64[nb][0], cA * m0);
-            d64[nb][1] = __fmaf_rn(sA, d64[nb][1], cA * m1);
-            d64[nb][2] = __fmaf_rn(sB, d64[nb][2], cB * m0);
-            d64[nb][3] = __fmaf_rn(sB, d64[nb][3], cB * m1);
-          }
-          acc[nb][0] = __fmaf_rn(x0, d64[nb][0], acc[nb][0]);
-          acc[nb][1] = __fmaf_rn(x1, d64[nb][1], acc[nb][1]);
-          acc[nb][2] = __fmaf_rn(x0, d64[nb][2], acc[nb][2]);
-          acc[nb][3] = __fmaf_rn(x1, d64[nb][3], acc[nb][3]);
         }
         issue(i + U, j);   // refill this slot with the unit U ahead
       }
@@ -342,21 +397,25 @@ __global__ void __launch_bounds__(WARPS * 32) qgemv_kernel(const uint8_t* __rest
     __syncthreads();
   }
 
-  // acc[nb]: c0 = (row g, col 2t), c1 = (g, 2t+1), c2 = (g+8, 2t), c3 = (g+8, 2t+1).
+  // acc[r][nb]: c0 = (row 16r+g, col 2t), c1 = (16r+g, 2t+1), c2 = (16r+g+8, 2t), c3 = (16r+g+8, 2t+1).
+  constexpr int RC = 8 * NB;
   #pragma unroll
-  for (int nb = 0; nb < NB; ++nb) {
-    red[warp][g][nb * 8 + 2 * t] = acc[nb][0];
-    red[warp][g][nb * 8 + 2 * t + 1] = acc[nb][1];
-    red[warp][g + 8][nb * 8 + 2 * t] = acc[nb][2];
-    red[warp][g + 8][nb * 8 + 2 * t + 1] = acc[nb][3];
-  }
+  for (int r = 0; r < R; ++r)
+    #pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      float* rw = red + (size_t(warp) * ROWS + 16 * r + g) * RC + nb * 8 + 2 * t;
+      rw[0] = acc[r][nb][0];
+      rw[1] = acc[r][nb][1];
+      rw[8 * RC] = acc[r][nb][2];
+      rw[8 * RC + 1] = acc[r][nb][3];
+    }
   __syncthreads();
-  for (int i = threadIdx.x; i < 16 * M; i += blockDim.x) {
-    const int r = i & 15, m = i >> 4;
+  for (int i = threadIdx.x; i < ROWS * M; i += blockDim.x) {
+    const int r = i % ROWS, m = i / ROWS;
     if (row0 + r >= N) continue;
     float sum = 0.0f;
     #pragma unroll
-    for (int w = 0; w < WARPS; ++w) sum += red[w][r][m];
+    for (int w = 0; w < WARPS; ++w) sum += red[(size_t(w) * ROWS + r) * RC + m];
     if constexpr (F == NVFP4) sum *= glob;
     const int64_t o = int64_t(m) * N + row0 + r;
     if (out_f32) static_cast<float*>(out)[o] = sum;
@@ -371,37 +430,59 @@ inline int stage_k(int M, int K) {
   return k64 < cap ? k64 : cap;
 }
 
-inline size_t smem_bytes(int F, int M, int KS) {
-  return size_t(M) * (KS + 8) * 2 + size_t(M) * (KS / 64) * 4 * (F == INT4_AFFINE ? 2 : 1);
+inline size_t smem_bytes(int F, int M, int KS, int R, int NB) {
+  return size_t(M) * (KS + 8) * 2 + size_t(M) * (KS / 64) * 4 * (F == INT4_AFFINE ? 2 : 1) +
+         size_t(WARPS) * 16 * R * 8 * NB * 4;
 }
 
-template <int F, int NB>
+// Launch with programmatic stream serialization: the kernel may start while
+// the preceding kernel in the stream finishes (it waits before touching X).
+template <typename Kern, typename... Args>
+static cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kern, args...);
+}
+
+template <int F, int NB, int R>
 static cudaError_t launch_nb(const uint8_t* c, const uint8_t* s, float glob, const uint16_t* x, void* out,
                              bool out_f32, int M, int N, int K, cudaStream_t st) {
   static std::atomic<int> attr_done[64];
   const int KS = stage_k(M, K);
-  const size_t sm = smem_bytes(F, M, KS);
+  const size_t sm = smem_bytes(F, M, KS, R, NB);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
-    const size_t cap = NB == 1 ? smem_bytes(F, 8, 4096) : smem_bytes(F, 16, 2048);
-    e = cudaFuncSetAttribute(qgemv_kernel<F, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(cap));
+    const size_t cap = NB == 1 ? smem_bytes(F, 8, 4096, R, NB) : smem_bytes(F, 16, 2048, R, NB);
+    e = cudaFuncSetAttribute(qgemv_kernel<F, NB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(cap));
     if (e != cudaSuccess) return e;
     attr_done[dev].store(1);
   }
-  qgemv_kernel<F, NB><<<dim3((N + 15) / 16), dim3(WARPS * 32), sm, st>>>(c, s, glob, x, out, out_f32, M, N, K, KS);
-  return cudaGetLastError();
+  e = launch_pdl(qgemv_kernel<F, NB, R>, dim3((N + 16 * R - 1) / (16 * R)), dim3(WARPS * 32), sm, st, c, s, glob, x,
+                 out, int(out_f32), M, N, K, KS);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Rows per warp: 16 for M <= 2, 32 beyond (each staged activation then serves
+// two weight tiles, which keeps staging small next to the weight stream).
 template <int F>
 static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
                               bool out_f32, int M, int N, int K, cudaStream_t st) {
   auto c = static_cast<const uint8_t*>(codes);
   auto s = static_cast<const uint8_t*>(scales);
   auto xx = static_cast<const uint16_t*>(x);
-  if (M <= 8) return launch_nb<F, 1>(c, s, glob, xx, out, out_f32, M, N, K, st);
-  return launch_nb<F, 2>(c, s, glob, xx, out, out_f32, M, N, K, st);
+  if (M <= 2) return launch_nb<F, 1, 1>(c, s, glob, xx, out, out_f32, M, N, K, st);
+  if (M <= 8) return launch_nb<F, 1, 2>(c, s, glob, xx, out, out_f32, M, N, K, st);
+  return launch_nb<F, 2, 2>(c, s, glob, xx, out, out_f32, M, N, K, st);
 }
 
 }  // namespace gemv

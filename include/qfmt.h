@@ -31,7 +31,12 @@
  * buffer.  qfmt_pack works on host memory and is synchronous.  qfmt_dequant,
  * qmm and qmm_ex take device pointers, enqueue work on `stream` (a
  * cudaStream_t; NULL = the legacy default stream) and return without
- * waiting; their status reports argument and launch errors only.  The
+ * waiting; their status reports argument and launch errors only.  They
+ * launch with programmatic dependent launch: X is read and `out` written only
+ * after every preceding kernel in the stream has completed, but the weight
+ * codes and scales may be read while a preceding kernel that signals early
+ * completion (griddepcontrol.launch_dependents, as this library's kernels do)
+ * is still running, so such a kernel must not write them.  The
  * library keeps no handle and allocates no device memory.  Its global state
  * is a per-thread error message, one status word per device (written only
  * when a kernel's bounded wait expires; see qfmt_device_status) and the

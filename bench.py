@@ -232,30 +232,40 @@ def copies_for(nbytes, m):
 
 
 def measure_e2e(prob, steps, warmup):
-    """Same metric through the public call with host buffers: per step, H2D of each
-    layer's activations from pinned memory, the qmm launches, D2H of each output."""
+    """Same metric through the public call with host buffers: per step, one H2D copy
+    of every layer's activations from pinned memory, the qmm launches, and one D2H
+    copy of every layer's output (weights stay resident, as in a decode step)."""
     import torch
     import block_scaled_quantized_spec_gb300 as q
-    xh = [prob.x_host.pin_memory() for _ in range(prob.copies)]
-    oh = [torch.empty((prob.m, prob.n), dtype=torch.bfloat16).pin_memory() for _ in range(prob.copies)]
+    L, m, n, k = prob.copies, prob.m, prob.n, prob.k
+    xh = prob.x_host.repeat(L, 1).pin_memory()                       # [L*M, K] bf16, pinned
+    oh = torch.empty((L * m, n), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty((L * m, k), dtype=torch.bfloat16, device="cuda")
+    od = torch.empty((L * m, n), dtype=torch.bfloat16, device="cuda")
 
     def one():
-        for i in range(prob.copies):
-            prob.x[i].copy_(xh[i], non_blocking=True)
-            q.qmm(prob.fmt, prob.codes[i], prob.scales[i], prob.g, prob.x[i], prob.n, out=prob.out[i])
-            oh[i].copy_(prob.out[i], non_blocking=True)
-    for _ in range(warmup):
+        xd.copy_(xh, non_blocking=True)
+        for i in range(L):
+            q.qmm(prob.fmt, prob.codes[i], prob.scales[i], prob.g, xd[i * m:(i + 1) * m], n,
+                  out=od[i * m:(i + 1) * m])
+        oh.copy_(od, non_blocking=True)
+    one()                                                             # warm the library's caches
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()                                    # the step's copies and launches
+    with torch.cuda.graph(graph):
         one()
+    for _ in range(warmup):
+        graph.replay()
     torch.cuda.synchronize()
     st = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
     for _ in range(steps):
-        one()
+        graph.replay()
     e1.record(st)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    return ms, prob.copies * prob.m * prob.k * 2, prob.copies * prob.m * prob.n * 2
+    return ms, xh.numel() * 2, oh.numel() * 2
 
 
 class OracleSample:
@@ -415,7 +425,7 @@ def main():
         "roofline": roofline_gemv(prob, ms, hbm, kind),
         "e2e": {"value": round(world * copies * nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "pinned-host X in, out back, per layer; weights resident"},
+                "note": "per step (one CUDA graph): one pinned H2D of all layers' X, L qmm calls, one D2H of all outputs; weights resident"},
         "gpu_launches": copies * args.steps,
         "clocks": clk,
     }

@@ -30,5 +30,7 @@ cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, floa
 void set_wait_limit_ns(uint64_t ns);
 void set_drop_arrivals(int on);
 cudaError_t read_and_clear_device_status(unsigned int* status);
+cudaError_t read_and_clear_gemv_status(unsigned int* status);
+uint64_t wait_limit_ns();
 
 }  // namespace qfmt_dev

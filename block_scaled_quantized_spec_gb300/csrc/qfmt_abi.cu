@@ -113,9 +113,11 @@ int qfmt_device_status(void* stream) {
   clear_error();
   int st = cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream sync");
   if (st) return st;
-  unsigned int word = 0;
+  unsigned int word = 0, gw = 0;
   if ((st = cuda_status(qfmt_dev::read_and_clear_device_status(&word), "device status"))) return st;
+  if ((st = cuda_status(qfmt_dev::read_and_clear_gemv_status(&gw), "device status"))) return st;
   if (word) return fail(QFMT_ETIMEOUT, "a tensor-core GEMM pipeline wait expired (status 0x%x)", word);
+  if (gw) return fail(QFMT_ETIMEOUT, "a GEMV weight-copy wait expired (status 0x%x)", gw);
   return QFMT_OK;
 }
 

@@ -10,13 +10,15 @@
 // code; they note it reads at a low fraction of bandwidth.  On GB300 the HBM
 // delivers about 46 four-bit codes per SM per clock, so everything per code
 // has to fit in a couple of issue slots.  The design:
-//  * a CTA owns 16 (M <= 2) or 32 weight rows; its 8 warps split K in
-//    64-code units, every lane loading word t of each 16-byte row segment (the
-//    four lanes of a quad share each scale block);
-//  * the launch is programmatic-dependent: a CTA prefetches its weight rows
-//    into L2, loads its first units of codes into registers and stages its
-//    block scales (as float32, or f16 for nvfp4) in shared memory while the
-//    preceding kernel drains, and only then waits for the activations;
+//  * a CTA owns 16 (M <= 2) or 32 weight rows; one thread bulk-copies the
+//    CTA's code rows (up to 64 KiB per pass) into shared memory with
+//    cp.async.bulk on an mbarrier, rows padded by 16 bytes so that the reads
+//    below are bank-conflict free;
+//  * the launch is programmatic-dependent: the weight copies and the staging
+//    of the block scales (float32, or f16 for nvfp4) run while the preceding
+//    kernel drains; the CTA waits for that kernel only before its activations;
+//  * the 8 warps split K in 64-code units; every lane reads word t of each
+//    16-byte row segment (the four lanes of a quad share each scale block);
 //  * element codes go to f16 with the hardware conversions (E2M1, E4M3, E5M2 ->
 //    f16x2 are exact; int4 becomes the exact f16 1024 + q), and the weights
 //    are the 16-row A operand of mma.sync m16n8k16 (f16 in, float32 out);
@@ -48,16 +50,6 @@ __device__ __forceinline__ void mma_f16(float c[4], uint32_t a0, uint32_t a1, ui
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t ldg32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // 8 E2M1 codes -> f16x2 in natural order (c0,c1) (c2,c3) (c4,c5) (c6,c7).
@@ -112,8 +104,6 @@ struct Cfg {
   static constexpr bool four = FmtTraits<F>::four;
   static constexpr int BLK = FmtTraits<F>::block;
   static constexpr int SEGS = four ? 2 : 4;        // 16-byte row segments per 64-code unit
-  // units in flight per lane (with R = 1 and K <= 4096: a warp's whole share)
-  static constexpr int UNROLL = four ? (R == 1 ? 8 : 2) : (R == 1 ? 4 : 1);
   // staged scale words per row per 64-code unit (int4 affine: s and b - 1024 s)
   static constexpr int SPU = F == INT4_AFFINE ? 2 : 64 / BLK;
 };
@@ -125,14 +115,41 @@ __host__ __device__ constexpr int sc_stride(int KS) {
   return ((KS / 64) * Cfg<F, R>::SPU + 3) / 4 * 4 + 4;
 }
 
+// Staged code-row stride in bytes: the row's bytes plus 16, so that word t of
+// a 16-byte segment in eight consecutive rows falls in distinct banks.
+template <int F>
+__host__ __device__ constexpr int code_stride(int KS) {
+  return (FmtTraits<F>::four ? KS / 2 : KS) + 16;
+}
+
+__device__ unsigned int g_gemv_status;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 template <int F, int NB, int R>
 __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restrict__ codes,
                                                         const uint8_t* __restrict__ scales, float glob,
                                                         const uint16_t* __restrict__ x, void* __restrict__ out,
-                                                        int out_f32, int M, int N, int K, int KS) {
+                                                        int out_f32, int M, int N, int K, int KS, uint64_t limit_ns) {
   using C = Cfg<F, R>;
   constexpr bool FOUR = C::four;
-  constexpr int SEGS = C::SEGS, U = C::UNROLL, SPU = C::SPU, BLK = C::BLK;
+  constexpr int SEGS = C::SEGS, SPU = C::SPU, BLK = C::BLK;
   constexpr bool I4 = F == INT4_AFFINE;
   constexpr int ROWS = 16 * R;
   constexpr int RC = 8 * NB;
@@ -140,11 +157,14 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
   const int xstride = KS + 8;                                          // f16 per staged activation row
   const int units_max = KS / 64;
   const int sst = sc_stride<F, R>(KS);
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                    // [M][KS + 8] f16
-  float* xsc = reinterpret_cast<float*>(smem + size_t(M) * xstride * 2);   // [M][KS/64] 2^-shift
+  const int cst = code_stride<F>(KS);
+  uint8_t* wsm = smem;                                                 // [ROWS][cst] staged codes
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + size_t(ROWS) * cst);   // [M][KS + 8] f16
+  float* xsc = reinterpret_cast<float*>(xs + size_t(M) * xstride);     // [M][KS/64] 2^-shift
   float* xsum = xsc + M * units_max;                                   // [M][KS/64] (int4 affine)
   float* wsc = xsum + (I4 ? M * units_max : 0);                        // [ROWS][sst] staged scales
   float* red = wsc + ROWS * sst;                                       // [WARPS][ROWS][RC]
+  __shared__ __align__(8) uint64_t wbar;
 
   // The next kernel in the stream may launch now.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -154,25 +174,13 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
   const int row0 = blockIdx.x * ROWS;
   const int64_t row_bytes = FOUR ? K / 2 : K;
   const int64_t nblk = K / BLK;
-
-  // Weights do not come from the preceding kernel: pull this CTA's code rows into L2.
-  if (lane == 0) {
-    #pragma unroll 1
-    for (int rr = warp * (ROWS / WARPS); rr < (warp + 1) * (ROWS / WARPS); ++rr)
-      if (row0 + rr < N) prefetch_l2(codes + int64_t(row0 + rr) * row_bytes, uint32_t(row_bytes));
+  const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(&wbar));
+  const int nrows = N - row0 < ROWS ? N - row0 : ROWS;
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-
-  const uint8_t* pA[R];
-  const uint8_t* pB[R];
-  bool okA[R], okB[R];
-  #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int ra = row0 + 16 * r + g, rb = ra + 8;
-    okA[r] = ra < N;
-    okB[r] = rb < N;
-    pA[r] = codes + int64_t(okA[r] ? ra : 0) * row_bytes + 4 * t;
-    pB[r] = codes + int64_t(okB[r] ? rb : 0) * row_bytes + 4 * t;
-  }
+  __syncthreads();
 
   float acc[R][NB][4];
   #pragma unroll
@@ -180,31 +188,29 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
     #pragma unroll
     for (int nb = 0; nb < NB; ++nb) acc[r][nb][0] = acc[r][nb][1] = acc[r][nb][2] = acc[r][nb][3] = 0.0f;
 
-  uint32_t wa[U][R][SEGS], wb[U][R][SEGS];
-
-  for (int ks = 0; ks < K; ks += KS) {
+  bool ok_all = true;
+  int pass = 0;
+  for (int ks = 0; ks < K; ks += KS, ++pass) {
     const int kn = K - ks < KS ? K - ks : KS;
     const int units = (kn + 63) / 64;
-    // lane's words of unit u (relative to this pass) for every row it owns
-    auto issue = [&](int i, int slot) {
-      const int u = warp + i * WARPS;
-      const int kb = ks + u * 64;
-      #pragma unroll
-      for (int sgm = 0; sgm < SEGS; ++sgm) {
-        const int ksg = kb + sgm * (FOUR ? 32 : 16);
-        const bool v = u < units && ksg < K;
-        const int off = FOUR ? ksg / 2 : ksg;
-        #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          wa[slot][r][sgm] = v && okA[r] ? ldg32(pA[r] + off) : 0u;
-          wb[slot][r][sgm] = v && okB[r] ? ldg32(pB[r] + off) : 0u;
-        }
-      }
-    };
-    #pragma unroll
-    for (int i = 0; i < U; ++i) issue(i, i);
+    const uint32_t pbytes = uint32_t(FOUR ? kn / 2 : kn);             // code bytes per row this pass
 
-    // ---- stage this pass's block scales (weights: no wait needed) ---------
+    // ---- weights of this pass: one bulk copy per row into shared memory ----
+    // (they do not come from the preceding kernel, so no wait is needed)
+    if (tid == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier generic reads before the overwrite
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(pbytes * uint32_t(nrows))
+                   : "memory");
+      for (int rr = 0; rr < nrows; ++rr) {
+        const uint8_t* src = codes + int64_t(row0 + rr) * row_bytes + (FOUR ? ks / 2 : ks);
+        const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(wsm + size_t(rr) * cst));
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(dst), "l"(src), "r"(pbytes), "r"(bar)
+                     : "memory");
+      }
+    }
+
+    // ---- block scales of this pass (float32, f16 pairs for nvfp4) ---------
     {
       const int per_row = units * 64 / BLK;                            // scale entries per row
       const int ntask = ROWS * per_row;
@@ -233,7 +239,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
     // The activations may be the preceding kernel's output: wait for it (once).
     if (ks == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // ---- stage the activations of this pass as scaled f16 -----------------
+    // ---- activations of this pass as scaled f16 ---------------------------
     // 8 lanes per (row, 64-code unit), 8 values each; the shift puts the
     // unit's max |x| in [2^14, 2^15).  Four tasks' loads are in flight at once.
     {
@@ -300,31 +306,58 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
     }
     __syncthreads();
 
-    // ---- stream the weights -------------------------------------------------
-    #pragma unroll 1
-    for (int i0 = 0; warp + i0 * WARPS < units; i0 += U) {
-      #pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const int i = i0 + j;
-        const int u = warp + i * WARPS;
-        if (u >= units) break;
+    // ---- the weights must have landed (bounded wait) ------------------------
+    {
+      int ok = 1;
+      if (lane == 0) {
+        if (!mbar_try_wait(bar, uint32_t(pass & 1))) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar, uint32_t(pass & 1)))
+            if (globaltimer_ns() - t0 > limit_ns) { ok = 0; break; }
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          atomicOr(&g_gemv_status, 1u);
+          // let the copies finish before this CTA's shared memory can be released
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar, uint32_t(pass & 1)) && globaltimer_ns() - t0 < limit_ns) {
+          }
+        }
+        ok_all = false;
+      }
+    }
+
+    // ---- multiply: each warp takes 64-code units warp, warp + 8, ... ------
+    if (ok_all) {
+      const uint8_t* wlane = wsm + g * cst + 4 * t;                    // row g of tile 0, lane's word
+      const float* scl = wsc + g * sst;
+      #pragma unroll 1
+      for (int u = warp; u < units; u += WARPS) {
         #pragma unroll
         for (int r = 0; r < R; ++r) {
-          const float* sca = wsc + (16 * r + g) * sst + u * SPU;      // row A's scales of this unit
-          const float* scb = sca + 8 * sst;                            // row B
+          const uint8_t* wra = wlane + (16 * r) * cst + (FOUR ? u * 32 : u * 64);
+          const uint8_t* wrb = wra + 8 * cst;
+          const float* sca = scl + (16 * r) * sst + u * SPU;
+          const float* scb = sca + 8 * sst;
           float d64[NB][4];
           #pragma unroll
           for (int nb = 0; nb < NB; ++nb) d64[nb][0] = d64[nb][1] = d64[nb][2] = d64[nb][3] = 0.0f;
           #pragma unroll
           for (int sgm = 0; sgm < SEGS; ++sgm) {
+            // a K that ends mid-unit leaves the tail segments unstaged: use zero codes
+            const bool in = ks + u * 64 + sgm * (FOUR ? 32 : 16) < K;
+            const uint32_t wa = in ? *reinterpret_cast<const uint32_t*>(wra + 16 * sgm) : 0u;
+            const uint32_t wb = in ? *reinterpret_cast<const uint32_t*>(wrb + 16 * sgm) : 0u;
             if constexpr (FOUR) {
               uint32_t fa[4], fb[4];
               if constexpr (I4) {
-                int4x8_f16_biased(wa[j][r][sgm], fa);
-                int4x8_f16_biased(wb[j][r][sgm], fb);
+                int4x8_f16_biased(wa, fa);
+                int4x8_f16_biased(wb, fb);
               } else {
-                e2m1x8_f16(wa[j][r][sgm], fa);
-                e2m1x8_f16(wb[j][r][sgm], fb);
+                e2m1x8_f16(wa, fa);
+                e2m1x8_f16(wb, fb);
                 if constexpr (F == NVFP4) {
                   // the lane's word of this segment lies in micro-block 2 sgm + t/2 of the unit
                   const uint32_t ca = __float_as_uint(sca[2 * sgm + (t >> 1)]);
@@ -356,8 +389,8 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
               }
             } else {
               uint32_t fa[2], fb[2];
-              f8x4_f16<F == MXFP8_E5M2>(wa[j][r][sgm], fa);
-              f8x4_f16<F == MXFP8_E5M2>(wb[j][r][sgm], fb);
+              f8x4_f16<F == MXFP8_E5M2>(wa, fa);
+              f8x4_f16<F == MXFP8_E5M2>(wb, fb);
               const float swa = F == NVFP8 ? sca[sgm] : sca[sgm >> 1];
               const float swb = F == NVFP8 ? scb[sgm] : scb[sgm >> 1];
               #pragma unroll
@@ -391,10 +424,9 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
             acc[r][nb][3] = __fmaf_rn(x1, d64[nb][3], acc[r][nb][3]);
           }
         }
-        issue(i + U, j);   // refill this slot with the unit U ahead
       }
     }
-    __syncthreads();
+    __syncthreads();   // the next pass overwrites the staged codes, scales and activations
   }
 
   // acc[r][nb]: c0 = (row 16r+g, col 2t), c1 = (16r+g, 2t+1), c2 = (16r+g+8, 2t), c3 = (16r+g+8, 2t+1).
@@ -409,6 +441,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
       rw[8 * RC + 1] = acc[r][nb][3];
     }
   __syncthreads();
+  if (!ok_all) return;   // an expired wait leaves this CTA's outputs unwritten (status word set)
   for (int i = tid; i < ROWS * M; i += THREADS) {
     const int r = i % ROWS, m = i / ROWS;
     if (row0 + r >= N) continue;
@@ -422,9 +455,12 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
   }
 }
 
-// Activations staged per pass: all of K up to 4096 (M <= 8) or 2048 (M > 8).
-inline int stage_k(int M, int K) {
-  const int cap = M <= 8 ? 4096 : 2048;
+// Codes per pass: the whole K when the CTA's code slab fits 64 KiB, else the
+// largest multiple of 64 codes that does.
+template <int F, int R>
+inline int stage_k(int K) {
+  const int bytes_per_code_row = FmtTraits<F>::four ? 1 : 2;          // 2 x bytes per code
+  const int cap = (65536 * 2 / (16 * R * bytes_per_code_row)) / 64 * 64;
   const int k64 = (K + 63) / 64 * 64;
   return k64 < cap ? k64 : cap;
 }
@@ -432,8 +468,9 @@ inline int stage_k(int M, int K) {
 template <int F, int NB, int R>
 inline size_t smem_bytes(int M, int KS) {
   const int units = KS / 64;
-  return size_t(M) * (KS + 8) * 2 + size_t(M) * units * 4 * (F == INT4_AFFINE ? 2 : 1) +
-         size_t(16 * R) * sc_stride<F, R>(KS) * 4 + size_t(WARPS) * 16 * R * 8 * NB * 4;
+  return size_t(16 * R) * code_stride<F>(KS) + size_t(M) * (KS + 8) * 2 +
+         size_t(M) * units * 4 * (F == INT4_AFFINE ? 2 : 1) + size_t(16 * R) * sc_stride<F, R>(KS) * 4 +
+         size_t(WARPS) * 16 * R * 8 * NB * 4;
 }
 
 // Launch with programmatic stream serialization: the kernel may start while
@@ -457,19 +494,20 @@ template <int F, int NB, int R>
 static cudaError_t launch_nb(const uint8_t* c, const uint8_t* s, float glob, const uint16_t* x, void* out,
                              bool out_f32, int M, int N, int K, cudaStream_t st) {
   static std::atomic<int> attr_done[64];
-  const int KS = stage_k(M, K);
+  const int KS = stage_k<F, R>(K);
   const size_t sm = smem_bytes<F, NB, R>(M, KS);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
-    const size_t cap = NB == 1 ? smem_bytes<F, NB, R>(8, 4096) : smem_bytes<F, NB, R>(16, 2048);
-    e = cudaFuncSetAttribute(qgemv_kernel<F, NB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(cap));
+    const int kcap = stage_k<F, R>(1 << 30);
+    e = cudaFuncSetAttribute(qgemv_kernel<F, NB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(smem_bytes<F, NB, R>(8 * NB, kcap)));
     if (e != cudaSuccess) return e;
     attr_done[dev].store(1);
   }
   e = launch_pdl(qgemv_kernel<F, NB, R>, dim3((N + 16 * R - 1) / (16 * R)), dim3(THREADS), sm, st, c, s, glob, x,
-                 out, int(out_f32), M, N, K, KS);
+                 out, int(out_f32), M, N, K, KS, wait_limit_ns());
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -487,6 +525,13 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, float glob,
 }
 
 }  // namespace gemv
+
+cudaError_t read_and_clear_gemv_status(unsigned int* status) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, gemv::g_gemv_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(gemv::g_gemv_status, &zero, sizeof(unsigned int));
+}
 
 cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float glob, const void* x, void* out,
                          bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms) {

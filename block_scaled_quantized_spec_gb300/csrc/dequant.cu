@@ -111,9 +111,8 @@ static cudaError_t launch_dequant_fmt(const void* codes, const void* scales, flo
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 1;
-  cudaError_t e = bf16 ? cudaLaunchKernelEx(&lc, dequant_kernel<F, true>, c, s, glob, out, N, K)
-                       : cudaLaunchKernelEx(&lc, dequant_kernel<F, false>, c, s, glob, out, N, K);
-  return e != cudaSuccess ? e : cudaGetLastError();
+  return bf16 ? cudaLaunchKernelEx(&lc, dequant_kernel<F, true>, c, s, glob, out, N, K)
+              : cudaLaunchKernelEx(&lc, dequant_kernel<F, false>, c, s, glob, out, N, K);
 }
 
 cudaError_t launch_dequant(int fmt, const void* codes, const void* scales, float glob, void* out,

@@ -503,8 +503,7 @@ static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* s
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 1;
-  e = cudaLaunchKernelEx(&lc, qgemm_tc_kernel<F, MT>, map, prm);
-  return e != cudaSuccess ? e : cudaGetLastError();
+  return cudaLaunchKernelEx(&lc, qgemm_tc_kernel<F, MT>, map, prm);
 }
 
 // 256-row tiles once M exceeds one 128-row tile.

@@ -455,22 +455,25 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
   }
 }
 
-// Codes per pass: the whole K when the CTA's code slab fits 64 KiB, else the
-// largest multiple of 64 codes that does.
-template <int F, int R>
-inline int stage_k(int K) {
-  const int bytes_per_code_row = FmtTraits<F>::four ? 1 : 2;          // 2 x bytes per code
-  const int cap = (65536 * 2 / (16 * R * bytes_per_code_row)) / 64 * 64;
-  const int k64 = (K + 63) / 64 * 64;
-  return k64 < cap ? k64 : cap;
-}
-
 template <int F, int NB, int R>
 inline size_t smem_bytes(int M, int KS) {
   const int units = KS / 64;
   return size_t(16 * R) * code_stride<F>(KS) + size_t(M) * (KS + 8) * 2 +
          size_t(M) * units * 4 * (F == INT4_AFFINE ? 2 : 1) + size_t(16 * R) * sc_stride<F, R>(KS) * 4 +
          size_t(WARPS) * 16 * R * 8 * NB * 4;
+}
+
+// Shared memory per CTA is held under this budget (two or more CTAs per SM).
+constexpr size_t SMEM_BUDGET = 112 * 1024;
+
+// Codes per pass: the largest multiple of 64 (at most 8192, at most K
+// rounded up) whose staged codes, activations and scales fit the budget.
+template <int F, int NB, int R>
+inline int stage_k(int M, int K) {
+  int ks = (K + 63) / 64 * 64;
+  ks = ks < 8192 ? ks : 8192;
+  while (ks > 64 && smem_bytes<F, NB, R>(M, ks) > SMEM_BUDGET) ks -= 64;
+  return ks;
 }
 
 // Launch with programmatic stream serialization: the kernel may start while
@@ -494,21 +497,18 @@ template <int F, int NB, int R>
 static cudaError_t launch_nb(const uint8_t* c, const uint8_t* s, float glob, const uint16_t* x, void* out,
                              bool out_f32, int M, int N, int K, cudaStream_t st) {
   static std::atomic<int> attr_done[64];
-  const int KS = stage_k<F, R>(K);
+  const int KS = stage_k<F, NB, R>(M, K);
   const size_t sm = smem_bytes<F, NB, R>(M, KS);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
-    const int kcap = stage_k<F, R>(1 << 30);
-    e = cudaFuncSetAttribute(qgemv_kernel<F, NB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(smem_bytes<F, NB, R>(8 * NB, kcap)));
+    e = cudaFuncSetAttribute(qgemv_kernel<F, NB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BUDGET));
     if (e != cudaSuccess) return e;
     attr_done[dev].store(1);
   }
-  e = launch_pdl(qgemv_kernel<F, NB, R>, dim3((N + 16 * R - 1) / (16 * R)), dim3(THREADS), sm, st, c, s, glob, x,
-                 out, int(out_f32), M, N, K, KS, wait_limit_ns());
-  return e != cudaSuccess ? e : cudaGetLastError();
+  return launch_pdl(qgemv_kernel<F, NB, R>, dim3((N + 16 * R - 1) / (16 * R)), dim3(THREADS), sm, st, c, s, glob, x,
+                    out, int(out_f32), M, N, K, KS, wait_limit_ns());
 }
 
 // Rows per CTA: 16 for M <= 2, 32 beyond (each staged activation then serves

@@ -15,6 +15,11 @@ cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float g
                          void* out, bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st,
                          int sms);
 
+// Register-direct decode GEMV for M <= 2 (when its staged activations fit).
+bool qgemv_m2_fits(int fmt, int64_t M, int64_t K);
+cudaError_t launch_qgemv_m2(int fmt, const void* codes, const void* scales, float glob, const void* x,
+                            void* out, bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st);
+
 // Float32-activation path (CUDA cores, exact products), any M.
 cudaError_t launch_qmm_f32x(int fmt, const void* codes, const void* scales, float glob,
                             const float* x, void* out, bool out_f32, int64_t M, int64_t N,

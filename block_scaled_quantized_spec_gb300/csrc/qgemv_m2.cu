@@ -1,0 +1,479 @@
+// Decode GEMV for one or two activation rows (M <= 2):
+//   out[m, n] = sum_k x[m, k] * dequant(W)[n, k]
+// (metaltile PR #250 qgemv commits: output[row] = sum_k dequant(weight[row,k])
+// * input[k]; rlx-cpu thunk/ops/quant.rs dequant_matmul_nvfp4, whose m == 1
+// loop streams the packed codes once and applies each block scale to that
+// block's partial sum).
+//
+// At M = 1 a launch moves a few MB and its time is set by how soon the weight
+// bytes are requested and how little work is left once the activations exist.
+// So:
+//  * every lane loads its weight spans straight into registers with 16-byte
+//    loads at the top of the kernel (a CTA owns 16 weight rows; its 8 warps
+//    take 64-byte column chunks of those rows in turn), together with the
+//    block scales it will need, before waiting on the preceding kernel (the
+//    launch is programmatic-dependent; the weights are not that kernel's
+//    output).  Chunks past the first round are prefetched into L2;
+//  * the activations are staged once per CTA in shared memory as f16 with a
+//    power-of-two scale per 32 values (the span's largest |x| goes to
+//    [2^14, 2^15): exact for every bf16 value within 2^29 of that maximum);
+//  * a lane's 16-byte span (32 four-bit or 16 eight-bit codes) is converted to
+//    f16 with the hardware conversions (E2M1/E4M3/E5M2 -> f16x2 are exact,
+//    int4 becomes the exact f16 1024 + q) and is the lane's share of the A
+//    operand of mma.sync m16n8k16.  The B operand is zero except in column t
+//    (activation row 0) and t + 4 (row 1) of the lanes that supply quad lane
+//    t's k positions, so D column t collects exactly quad lane t's span: one
+//    scale block per column, scaled once per chunk in float32 (nvfp4 applies
+//    its E4M3 micro-scales to the f16 weights instead: E2M1 x E4M3 is exact in
+//    f16; its FP32 global scale is applied at the end);
+//  * per-warp sums meet in shared memory; one thread per output stores it.
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "decode.cuh"
+#include "kernels.h"
+
+namespace qfmt_dev {
+namespace gemv_m2 {
+
+constexpr int WARPS = 8;
+constexpr int THREADS = WARPS * 32;
+constexpr int P = 4;              // chunks per warp held in registers at a time
+constexpr size_t SMEM_LIMIT = 96 * 1024;
+
+template <int F>
+struct Shape {
+  static constexpr bool four = FmtTraits<F>::four;
+  static constexpr int CODES = four ? 128 : 64;   // codes per row in one 64-byte chunk
+  static constexpr int LANE = CODES / 4;           // codes in a lane's 16-byte span
+};
+
+__device__ __forceinline__ void mma_f16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 8 E2M1 codes -> f16x2 (c0,c1) (c2,c3) (c4,c5) (c6,c7) (low code in the low half).
+__device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t r[4]) {
+  asm("{.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
+}
+
+// 4 E4M3 (or E5M2) codes -> f16x2 (c0,c1) (c2,c3).
+template <bool E5>
+__device__ __forceinline__ void f8x4_f16(uint32_t w, uint32_t* r) {
+  if constexpr (E5)
+    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.f16x2.e5m2x2 %0, h0;\n\tcvt.rn.f16x2.e5m2x2 %1, h1;}"
+        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
+  else
+    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;}"
+        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int j) {
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+// The four f16x2 fragments of activations 8q .. 8q+7 of a lane's span, in the
+// order the staged activations use: E2M1 and 8-bit codes (8q, 8q+1) ..
+// (8q+6, 8q+7); int4 the biased pairs (q_{8q+b}, q_{8q+b+4}), b = 0..3.
+template <int F>
+__device__ __forceinline__ void frags8(const uint4& v, int q, uint32_t r[4]) {
+  if constexpr (F == MXFP4 || F == NVFP4) {
+    e2m1x8_f16(word(v, q), r);
+  } else if constexpr (F == INT4_AFFINE) {
+    const uint32_t w = word(v, q);
+    #pragma unroll
+    for (int b = 0; b < 4; ++b) r[b] = ((w >> (4 * b)) & 0x000F000Fu) | 0x64006400u;
+  } else {
+    f8x4_f16<F == MXFP8_E5M2>(word(v, 2 * q), r);
+    f8x4_f16<F == MXFP8_E5M2>(word(v, 2 * q + 1), r + 2);
+  }
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Halfword offset of activation k in a staged row: 8 halfwords of padding
+// after every 32 values keep the B-operand reads of a warp in distinct banks.
+__host__ __device__ constexpr int xoff(int k) { return k + (k >> 5) * 8; }
+
+// Staged activation row stride in halfwords: the padded row rounded so that
+// consecutive rows start 64 bytes apart modulo 128 (rows 0 and 1 then use
+// disjoint banks).
+__host__ __device__ constexpr int xstride(int K) {
+  const int h = xoff(K);
+  const int bytes = 2 * h;
+  const int pad = ((64 - bytes % 128) + 128) % 128;
+  return h + pad / 2;
+}
+
+inline size_t smem_bytes(int F, int M, int K) {
+  const int spans = K / 32;
+  return size_t(M) * xstride(K) * 2 + 64 + size_t(M) * spans * 4 * (F == INT4_AFFINE ? 2 : 1) +
+         size_t(WARPS) * 2 * 16 * 4;
+}
+
+// Per-chunk scale words a D-holding lane keeps: the weight block scales of
+// the two columns it holds, for rows g and g + 8 (raw encodings).
+struct ChunkScales {
+  uint32_t a0, a1, b0, b1;
+};
+
+template <int F>
+__global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __restrict__ codes,
+                                                           const uint8_t* __restrict__ scales, float glob,
+                                                           const uint16_t* __restrict__ x, void* __restrict__ out,
+                                                           int out_f32, int M, int N, int K) {
+  using S = Shape<F>;
+  constexpr bool FOUR = S::four, I4 = F == INT4_AFFINE;
+  constexpr int CODES = S::CODES, LANE = S::LANE;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int xst = xstride(K);
+  const int spans = K / 32;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                         // [M][xst] f16
+  uint16_t* xzero = xs + size_t(M) * xst;                                   // 32 zero halfwords
+  float* xsc = reinterpret_cast<float*>(xzero + 32);                        // [M][spans] 2^-shift
+  float* xsum = xsc + M * spans;                                            // [M][spans] (int4 affine)
+  float* red = xsum + (I4 ? M * spans : 0);                                 // [WARPS][2][16]
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int row0 = blockIdx.x * 16;
+  const int ra = row0 + g, rb = row0 + g + 8;
+  const bool va = ra < N, vb = rb < N;
+  const int64_t rowbytes = FOUR ? K / 2 : K;
+  const uint8_t* pa = codes + int64_t(va ? ra : 0) * rowbytes + 16 * t;
+  const uint8_t* pb = codes + int64_t(vb ? rb : 0) * rowbytes + 16 * t;
+  const int nchunk = (K + CODES - 1) / CODES;
+  const int mine = nchunk > warp ? (nchunk - warp + WARPS - 1) / WARPS : 0;   // chunks of this warp
+  const int a0 = (2 * t) & 3;                                                 // first column's quad lane
+  const int64_t nblk = K / FmtTraits<F>::block;
+
+  uint4 wa[P], wb[P];
+  ChunkScales cs[P];
+  uint32_t ms[P];      // nvfp4: this lane's two E4M3 micro-scales, row g (low half) and row g + 8
+
+  auto load_round = [&](int r) {
+    #pragma unroll
+    for (int i = 0; i < P; ++i) {
+      const int c = warp + WARPS * (r * P + i);
+      const bool live = r * P + i < mine;
+      const int ks = c * CODES + LANE * t;                                   // this lane's first k
+      const bool kin = live && ks < K;
+      wa[i] = (kin && va) ? ldg_stream(pa + int64_t(c) * 64) : make_uint4(0, 0, 0, 0);
+      wb[i] = (kin && vb) ? ldg_stream(pb + int64_t(c) * 64) : make_uint4(0, 0, 0, 0);
+      // the block (or pair of blocks) of quad lanes a0 and a0 + 1 in this chunk
+      const int k0 = c * CODES + LANE * a0;
+      const bool c0 = live && k0 < K, c1 = live && k0 + LANE < K;
+      const int64_t ia = int64_t(va ? ra : 0) * nblk, ib = int64_t(vb ? rb : 0) * nblk;
+      if constexpr (F == MXFP4) {
+        const int64_t e = k0 / 32;
+        const uint32_t x0 = (c0 && va) ? __ldg(scales + ia + e) : 0u;
+        const uint32_t x1 = (c1 && va) ? __ldg(scales + ia + e + 1) : 0u;
+        const uint32_t x2 = (c0 && vb) ? __ldg(scales + ib + e) : 0u;
+        const uint32_t x3 = (c1 && vb) ? __ldg(scales + ib + e + 1) : 0u;
+        cs[i].a0 = x0 | (x1 << 8) | (x2 << 16) | (x3 << 24);                   // four E8M0 bytes
+        cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
+      } else if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+        const int64_t e = k0 / 32;                                            // a0, a0 + 1 share it
+        cs[i].a0 = (c0 && va) ? __ldg(scales + ia + e) : 0u;
+        cs[i].b0 = (c0 && vb) ? __ldg(scales + ib + e) : 0u;
+        cs[i].a1 = cs[i].b1 = 0u;
+      } else if constexpr (F == NVFP8) {
+        const float* sf = reinterpret_cast<const float*>(scales);
+        const int64_t e = k0 / 16;
+        cs[i].a0 = (c0 && va) ? __float_as_uint(__ldg(sf + ia + e)) : 0u;
+        cs[i].a1 = (c1 && va) ? __float_as_uint(__ldg(sf + ia + e + 1)) : 0u;
+        cs[i].b0 = (c0 && vb) ? __float_as_uint(__ldg(sf + ib + e)) : 0u;
+        cs[i].b1 = (c1 && vb) ? __float_as_uint(__ldg(sf + ib + e + 1)) : 0u;
+      } else if constexpr (F == INT4_AFFINE) {
+        const uint32_t* sp = reinterpret_cast<const uint32_t*>(scales);
+        const int64_t e = k0 / 64;                                            // a0, a0 + 1 share it
+        cs[i].a0 = (c0 && va) ? __ldg(sp + ia + e) : 0u;
+        cs[i].b0 = (c0 && vb) ? __ldg(sp + ib + e) : 0u;
+        cs[i].a1 = cs[i].b1 = 0u;
+      } else {   // NVFP4: the lane's own two micro-blocks, one 16-bit pair per row
+        const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales);
+        const int64_t e = ks / 32;                                            // pair index (16-code blocks / 2)
+        const uint32_t ma = (kin && va) ? __ldg(sp + ia / 2 + e) : 0u;
+        const uint32_t mb2 = (kin && vb) ? __ldg(sp + ib / 2 + e) : 0u;
+        ms[i] = ma | (mb2 << 16);
+        cs[i].a0 = cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
+      }
+    }
+  };
+
+  const int rounds = (mine + P - 1) / P;
+  load_round(0);
+  // chunks past the first round: start them towards L2 now
+  if (rounds > 1 && tid < 16 && row0 + tid < N) {
+    const int64_t first = int64_t(WARPS) * P * 64;
+    if (rowbytes > first) {
+      const uint8_t* p = codes + int64_t(row0 + tid) * rowbytes + first;
+      const uint32_t n = uint32_t(rowbytes - first);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+    }
+  }
+
+  // The activations may be the preceding kernel's output.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // ---- stage the activations: 16 values per task, two tasks per 32-span ---
+  {
+    const int per_m = K / 16;
+    const int tasks = M * per_m;
+    for (int i0 = 0; i0 < tasks; i0 += 2 * THREADS) {
+      uint4 v[2][2];
+      #pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int i = i0 + tid + j * THREADS;
+        const int m = i / per_m, k = (i - m * per_m) * 16;
+        const uint4* src = reinterpret_cast<const uint4*>(x + int64_t(m) * K + k);
+        v[j][0] = i < tasks ? __ldg(src) : make_uint4(0, 0, 0, 0);
+        v[j][1] = i < tasks ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
+      }
+      #pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (i0 + j * THREADS >= tasks) break;                                  // uniform over the CTA
+        const int i = i0 + tid + j * THREADS;
+        const bool live = i < tasks;
+        const int m = live ? i / per_m : 0;
+        const int k = live ? (i - m * per_m) * 16 : 0;
+        const uint32_t h[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w, v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
+        uint32_t mx = 0;
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) mx = max(mx, max(h[q] & 0x7FFFu, (h[q] >> 16) & 0x7FFFu));
+        mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));                     // the other half of the span
+        const int E = int(mx >> 7);
+        int sh = (mx == 0u || E == 255) ? 0 : 141 - E;                         // 14 - (E - 127)
+        sh = sh > 126 ? 126 : sh;
+        const float up = __uint_as_float(uint32_t(sh + 127) << 23);
+        float f[16];
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          f[2 * q] = __fmul_rn(__uint_as_float(h[q] << 16), up);
+          f[2 * q + 1] = __fmul_rn(__uint_as_float(h[q] & 0xFFFF0000u), up);
+        }
+        uint32_t o[8];
+        if constexpr (I4) {   // per 8 values: (x0,x4) (x1,x5) (x2,x6) (x3,x7), the int4 pairing
+          #pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            o[q] = pack_f16x2(f[q], f[q + 4]);
+            o[4 + q] = pack_f16x2(f[8 + q], f[12 + q]);
+          }
+        } else {
+          #pragma unroll
+          for (int q = 0; q < 8; ++q) o[q] = pack_f16x2(f[2 * q], f[2 * q + 1]);
+        }
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(xs + size_t(m) * xst + xoff(k));
+          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        if constexpr (I4) {   // span sum of the staged (rounded) values
+          float sm = 0.0f;
+          #pragma unroll
+          for (int q = 0; q < 8; ++q) sm += f16x2_lo(o[q]) + f16x2_hi(o[q]);
+          sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
+          if (live && (k & 16) == 0) xsum[m * spans + k / 32] = sm;
+        }
+        if (live && (k & 16) == 0) xsc[m * spans + k / 32] = __uint_as_float(uint32_t(127 - sh) << 23);
+      }
+    }
+    if (tid < 16) reinterpret_cast<uint32_t*>(xzero)[tid] = 0u;
+  }
+  __syncthreads();
+
+  // B-operand lanes: (g == t) supplies activation row 0, (g == t + 4) row 1.
+  const int mb = g == t ? 0 : (g == t + 4 ? 1 : -1);
+  const bool bl = mb >= 0 && mb < M;
+  const int md = (t >> 1) < M ? (t >> 1) : M - 1;   // the activation row of this lane's D columns
+
+  float acc_a = 0.0f, acc_b = 0.0f;
+  for (int r = 0; r < rounds; ++r) {
+    if (r > 0) load_round(r);
+    // Chunks advance in pairs (two independent accumulator chains per warp);
+    // a chunk past the end of this warp's share has zero codes, zero
+    // activations and zero scales and adds nothing.
+    #pragma unroll
+    for (int ip = 0; ip < P; ip += 2) {
+    int xo[2];
+    float d[2][4];
+    uint32_t sa0[2], sa1[2], sb0[2], sb1[2];
+    #pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+      const int i = ip + ii;
+      const int c = warp + WARPS * (r * P + i);
+      const int ks = c * CODES + LANE * t;
+      xo[ii] = (bl && r * P + i < mine && ks < K) ? mb * xst + xoff(ks) : M * xst;   // M * xst: the zero block
+      d[ii][0] = d[ii][1] = d[ii][2] = d[ii][3] = 0.0f;
+      if constexpr (F == NVFP4) {
+        // E4M3 pair -> f16x2 (s0, s1), then splat each
+        uint32_t pa2, pb2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(pa2) : "h"(uint16_t(ms[i] & 0xFFFFu)));
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(pb2) : "h"(uint16_t(ms[i] >> 16)));
+        sa0[ii] = prmt(pa2, 0u, 0x1010u);
+        sa1[ii] = prmt(pa2, 0u, 0x3232u);
+        sb0[ii] = prmt(pb2, 0u, 0x1010u);
+        sb1[ii] = prmt(pb2, 0u, 0x3232u);
+      }
+    }
+    #pragma unroll
+    for (int q = 0; q < LANE / 8; ++q) {                                       // 8 activations, two MMAs
+      #pragma unroll
+      for (int ii = 0; ii < 2; ++ii) {
+        const int i = ip + ii;
+        const uint4 xv = *reinterpret_cast<const uint4*>(xs + xo[ii] + 8 * q);
+        uint32_t fa[4], fb[4];
+        frags8<F>(wa[i], q, fa);
+        frags8<F>(wb[i], q, fb);
+        if constexpr (F == NVFP4) {                                            // codes 0-15 / 16-31 of the span
+          const uint32_t ca = q < 2 ? sa0[ii] : sa1[ii], cb = q < 2 ? sb0[ii] : sb1[ii];
+          #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            fa[e] = hmul2_f16(fa[e], ca);
+            fb[e] = hmul2_f16(fb[e], cb);
+          }
+        }
+        mma_f16(d[ii], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+        mma_f16(d[ii], fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
+      }
+    }
+    #pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+      const int i = ip + ii;
+      // D columns 2t, 2t+1 hold quad lanes a0, a0 + 1 of activation row md
+      const int c = warp + WARPS * (r * P + i);
+      const int k0 = c * CODES + LANE * a0;
+      const int s0 = min(k0 / 32, spans - 1), s1 = min((k0 + LANE) / 32, spans - 1);
+      const float x0s = xsc[md * spans + s0], x1s = xsc[md * spans + s1];
+      if constexpr (F == MXFP4) {
+        const uint32_t w4 = cs[i].a0;
+        acc_a = __fmaf_rn(__fmul_rn(e8m0_f32(w4 & 0xFFu), x0s), d[ii][0], acc_a);
+        acc_a = __fmaf_rn(__fmul_rn(e8m0_f32((w4 >> 8) & 0xFFu), x1s), d[ii][1], acc_a);
+        acc_b = __fmaf_rn(__fmul_rn(e8m0_f32((w4 >> 16) & 0xFFu), x0s), d[ii][2], acc_b);
+        acc_b = __fmaf_rn(__fmul_rn(e8m0_f32(w4 >> 24), x1s), d[ii][3], acc_b);
+      } else if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+        const float ca = __fmul_rn(e8m0_f32(cs[i].a0), x0s), cb = __fmul_rn(e8m0_f32(cs[i].b0), x0s);
+        acc_a = __fmaf_rn(ca, d[ii][0] + d[ii][1], acc_a);
+        acc_b = __fmaf_rn(cb, d[ii][2] + d[ii][3], acc_b);
+      } else if constexpr (F == NVFP8) {
+        acc_a = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].a0), x0s), d[ii][0], acc_a);
+        acc_a = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].a1), x1s), d[ii][1], acc_a);
+        acc_b = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].b0), x0s), d[ii][2], acc_b);
+        acc_b = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].b1), x1s), d[ii][3], acc_b);
+      } else if constexpr (F == INT4_AFFINE) {
+        // sum_k x~ (1024 + q): s * D + (b - 1024 s) * sum(x~), then the span's 2^-shift
+        const float m0 = xsum[md * spans + s0], m1 = xsum[md * spans + s1];
+        const float sa = bf16bits_f32(cs[i].a0 & 0xFFFFu), ba = __fmaf_rn(-1024.0f, sa, bf16bits_f32(cs[i].a0 >> 16));
+        const float sb = bf16bits_f32(cs[i].b0 & 0xFFFFu), bb = __fmaf_rn(-1024.0f, sb, bf16bits_f32(cs[i].b0 >> 16));
+        acc_a = __fmaf_rn(x0s, __fmaf_rn(sa, d[ii][0], ba * m0), acc_a);
+        acc_a = __fmaf_rn(x1s, __fmaf_rn(sa, d[ii][1], ba * m1), acc_a);
+        acc_b = __fmaf_rn(x0s, __fmaf_rn(sb, d[ii][2], bb * m0), acc_b);
+        acc_b = __fmaf_rn(x1s, __fmaf_rn(sb, d[ii][3], bb * m1), acc_b);
+      } else {   // NVFP4: micro-scales already applied; the span shifts remain
+        acc_a = __fmaf_rn(x0s, d[ii][0], acc_a);
+        acc_a = __fmaf_rn(x1s, d[ii][1], acc_a);
+        acc_b = __fmaf_rn(x0s, d[ii][2], acc_b);
+        acc_b = __fmaf_rn(x1s, d[ii][3], acc_b);
+      }
+    }
+    }
+  }
+
+  // lanes t and t ^ 1 hold the two column pairs of the same activation row
+  acc_a += __shfl_xor_sync(0xFFFFFFFFu, acc_a, 1);
+  acc_b += __shfl_xor_sync(0xFFFFFFFFu, acc_b, 1);
+  if ((t & 1) == 0) {
+    red[(warp * 2 + (t >> 1)) * 16 + g] = acc_a;
+    red[(warp * 2 + (t >> 1)) * 16 + g + 8] = acc_b;
+  }
+  __syncthreads();
+  if (tid < 16 * M) {
+    const int m = tid >> 4, rr = tid & 15;
+    if (row0 + rr < N) {
+      float sum = 0.0f;
+      #pragma unroll
+      for (int w = 0; w < WARPS; ++w) sum += red[(w * 2 + m) * 16 + rr];
+      if constexpr (F == NVFP4) sum *= glob;
+      const int64_t o = int64_t(m) * N + row0 + rr;
+      if (out_f32) static_cast<float*>(out)[o] = sum;
+      else static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(sum);
+    }
+  }
+}
+
+template <int F>
+static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
+                              bool out_f32, int M, int N, int K, cudaStream_t st) {
+  static std::atomic<int> attr_done[64];
+  const size_t sm = smem_bytes(F, M, K);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
+    e = cudaFuncSetAttribute(qgemv_m2_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
+    if (e != cudaSuccess) return e;
+    attr_done[dev].store(1);
+  }
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.gridDim = dim3((N + 15) / 16);
+  lc.blockDim = dim3(THREADS);
+  lc.dynamicSmemBytes = sm;
+  lc.stream = st;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F>, static_cast<const uint8_t*>(codes),
+                            static_cast<const uint8_t*>(scales), glob, static_cast<const uint16_t*>(x), out,
+                            int(out_f32), M, N, K);
+}
+
+}  // namespace gemv_m2
+
+bool qgemv_m2_fits(int fmt, int64_t M, int64_t K) {
+  return M >= 1 && M <= 2 && K <= (int64_t(1) << 20) && gemv_m2::smem_bytes(fmt, int(M), int(K)) <= gemv_m2::SMEM_LIMIT;
+}
+
+cudaError_t launch_qgemv_m2(int fmt, const void* codes, const void* scales, float glob, const void* x, void* out,
+                            bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+  const int m = int(M), n = int(N), k = int(K);
+  switch (fmt) {
+    case MXFP4: return gemv_m2::launch_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case NVFP4: return gemv_m2::launch_fmt<NVFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP8_E4M3: return gemv_m2::launch_fmt<MXFP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP8_E5M2: return gemv_m2::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case NVFP8: return gemv_m2::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    default: return gemv_m2::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+  }
+}
+
+}  // namespace qfmt_dev

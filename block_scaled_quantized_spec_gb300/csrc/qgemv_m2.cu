@@ -109,6 +109,25 @@ __device__ __forceinline__ void frags8(const uint4& v, int q, uint32_t r[4]) {
   }
 }
 
+// E8M0 byte j of w as float32 when 1 <= byte <= 254 (the biased exponent
+// moved into place); bytes 0 and 255 take e8m0_f32.
+template <int J>
+__device__ __forceinline__ float e8m0_fast(uint32_t w) {
+  return __uint_as_float(J == 3 ? (w >> 1) & 0x7F800000u : (w << (23 - 8 * J)) & 0x7F800000u);
+}
+
+__device__ __forceinline__ bool has_byte_00_or_ff(uint32_t w) {
+  const uint32_t z = (w - 0x01010101u) & ~w & 0x80808080u;
+  const uint32_t f = (~w - 0x01010101u) & w & 0x80808080u;
+  return (z | f) != 0u;
+}
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 __device__ __forceinline__ uint4 ldg_stream(const uint8_t* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -143,7 +162,7 @@ struct ChunkScales {
   uint32_t a0, a1, b0, b1;
 };
 
-template <int F>
+template <int F, int MR>
 __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __restrict__ codes,
                                                            const uint8_t* __restrict__ scales, float glob,
                                                            const uint16_t* __restrict__ x, void* __restrict__ out,
@@ -179,9 +198,9 @@ __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __r
   ChunkScales cs[P];
   uint32_t ms[P];      // nvfp4: this lane's two E4M3 micro-scales, row g (low half) and row g + 8
 
-  auto load_round = [&](int r) {
-    #pragma unroll
-    for (int i = 0; i < P; ++i) {
+  // chunk slot i of round r: codes of rows g and g + 8 and their scales
+  auto load_chunk = [&](int r, int i) {
+    {
       const int c = warp + WARPS * (r * P + i);
       const bool live = r * P + i < mine;
       const int ks = c * CODES + LANE * t;                                   // this lane's first k
@@ -194,17 +213,19 @@ __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __r
       const int64_t ia = int64_t(va ? ra : 0) * nblk, ib = int64_t(vb ? rb : 0) * nblk;
       if constexpr (F == MXFP4) {
         const int64_t e = k0 / 32;
-        const uint32_t x0 = (c0 && va) ? __ldg(scales + ia + e) : 0u;
-        const uint32_t x1 = (c1 && va) ? __ldg(scales + ia + e + 1) : 0u;
-        const uint32_t x2 = (c0 && vb) ? __ldg(scales + ib + e) : 0u;
-        const uint32_t x3 = (c1 && vb) ? __ldg(scales + ib + e + 1) : 0u;
-        cs[i].a0 = x0 | (x1 << 8) | (x2 << 16) | (x3 << 24);                   // four E8M0 bytes
+        // four E8M0 bytes; a block outside the matrix reads as 127 (its D column is zero)
+        const uint32_t x0 = (c0 && va) ? __ldg(scales + ia + e) : 127u;
+        const uint32_t x1 = (c1 && va) ? __ldg(scales + ia + e + 1) : 127u;
+        const uint32_t x2 = (c0 && vb) ? __ldg(scales + ib + e) : 127u;
+        const uint32_t x3 = (c1 && vb) ? __ldg(scales + ib + e + 1) : 127u;
+        cs[i].a0 = x0 | (x1 << 8) | (x2 << 16) | (x3 << 24);
         cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
       } else if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {
         const int64_t e = k0 / 32;                                            // a0, a0 + 1 share it
-        cs[i].a0 = (c0 && va) ? __ldg(scales + ia + e) : 0u;
-        cs[i].b0 = (c0 && vb) ? __ldg(scales + ib + e) : 0u;
-        cs[i].a1 = cs[i].b1 = 0u;
+        const uint32_t x0 = (c0 && va) ? __ldg(scales + ia + e) : 127u;
+        const uint32_t x2 = (c0 && vb) ? __ldg(scales + ib + e) : 127u;
+        cs[i].a0 = x0 | (127u << 8) | (x2 << 16) | (127u << 24);               // bytes 0 and 2 used
+        cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
       } else if constexpr (F == NVFP8) {
         const float* sf = reinterpret_cast<const float*>(scales);
         const int64_t e = k0 / 16;
@@ -228,6 +249,10 @@ __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __r
       }
     }
   };
+  auto load_round = [&](int r) {
+    #pragma unroll
+    for (int i = 0; i < P; ++i) load_chunk(r, i);
+  };
 
   const int rounds = (mine + P - 1) / P;
   load_round(0);
@@ -241,34 +266,56 @@ __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __r
     }
   }
 
+  // Any E8M0 scale byte of this round equal to 0 or 255 sends the warp down the exact decode.
+  bool exact = false;
+  if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+    bool sp = false;
+    #pragma unroll
+    for (int i = 0; i < P; ++i) sp |= has_byte_00_or_ff(cs[i].a0);
+    exact = __any_sync(0xFFFFFFFFu, sp);
+  }
+  if (tid < 16) reinterpret_cast<uint32_t*>(xzero)[tid] = 0u;
+  __syncthreads();
+
   // The activations may be the preceding kernel's output.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- stage the activations: 16 values per task, two tasks per 32-span ---
+  // ---- stage this warp's activations: the k ranges of its own chunks --------
+  // 16 values per task, tasks 2s and 2s+1 (lanes l and l^1) share a 32-span;
+  // the span's shift puts its largest |x| in [2^14, 2^15).
   {
-    const int per_m = K / 16;
+    constexpr int TPC = CODES / 16;                                            // tasks per chunk and row
+    const int per_m = mine * TPC;
     const int tasks = M * per_m;
-    for (int i0 = 0; i0 < tasks; i0 += 2 * THREADS) {
-      uint4 v[2][2];
+    // MR tasks per lane and pass are in flight together (one per activation row)
+    for (int j0 = 0; j0 < tasks; j0 += 32 * MR) {
+      uint4 v[MR][2];
+      int kk[MR], mm[MR];
+      bool lv[MR];
       #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int i = i0 + tid + j * THREADS;
-        const int m = i / per_m, k = (i - m * per_m) * 16;
+      for (int u = 0; u < MR; ++u) {
+        const int j = j0 + lane + 32 * u;
+        const int m = j >= per_m ? 1 : 0;
+        const int rem = j - m * per_m;
+        const int c = warp + WARPS * (rem / TPC);
+        const int k = c * CODES + (rem % TPC) * 16;
+        lv[u] = j < tasks && k < K;
+        kk[u] = k;
+        mm[u] = m;
         const uint4* src = reinterpret_cast<const uint4*>(x + int64_t(m) * K + k);
-        v[j][0] = i < tasks ? __ldg(src) : make_uint4(0, 0, 0, 0);
-        v[j][1] = i < tasks ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
+        v[u][0] = lv[u] ? __ldg(src) : make_uint4(0, 0, 0, 0);
+        v[u][1] = lv[u] ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
       }
       #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        if (i0 + j * THREADS >= tasks) break;                                  // uniform over the CTA
-        const int i = i0 + tid + j * THREADS;
-        const bool live = i < tasks;
-        const int m = live ? i / per_m : 0;
-        const int k = live ? (i - m * per_m) * 16 : 0;
-        const uint32_t h[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w, v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
-        uint32_t mx = 0;
+      for (int u = 0; u < MR; ++u) {
+        if (j0 + 32 * u >= tasks) break;                                       // uniform over the warp
+        const bool live = lv[u];
+        const int m = mm[u], k = kk[u];
+        const uint32_t h[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+        uint32_t m2 = 0;
         #pragma unroll
-        for (int q = 0; q < 8; ++q) mx = max(mx, max(h[q] & 0x7FFFu, (h[q] >> 16) & 0x7FFFu));
+        for (int q = 0; q < 8; ++q) m2 = max_u16x2(m2, h[q] & 0x7FFF7FFFu);
+        uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
         mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));                     // the other half of the span
         const int E = int(mx >> 7);
         int sh = (mx == 0u || E == 255) ? 0 : 141 - E;                         // 14 - (E - 127)
@@ -306,9 +353,8 @@ __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __r
         if (live && (k & 16) == 0) xsc[m * spans + k / 32] = __uint_as_float(uint32_t(127 - sh) << 23);
       }
     }
-    if (tid < 16) reinterpret_cast<uint32_t*>(xzero)[tid] = 0u;
   }
-  __syncthreads();
+  __syncwarp();
 
   // B-operand lanes: (g == t) supplies activation row 0, (g == t + 4) row 1.
   const int mb = g == t ? 0 : (g == t + 4 ? 1 : -1);
@@ -317,7 +363,14 @@ __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __r
 
   float acc_a = 0.0f, acc_b = 0.0f;
   for (int r = 0; r < rounds; ++r) {
-    if (r > 0) load_round(r);
+    if (r > 0) {   // this round's chunks were requested while the previous round computed
+      if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+        bool sp = false;
+        #pragma unroll
+        for (int i = 0; i < P; ++i) sp |= has_byte_00_or_ff(cs[i].a0);
+        exact = __any_sync(0xFFFFFFFFu, sp);
+      }
+    }
     // Chunks advance in pairs (two independent accumulator chains per warp);
     // a chunk past the end of this warp's share has zero codes, zero
     // activations and zero scales and adds nothing.
@@ -375,12 +428,22 @@ __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __r
       const float x0s = xsc[md * spans + s0], x1s = xsc[md * spans + s1];
       if constexpr (F == MXFP4) {
         const uint32_t w4 = cs[i].a0;
-        acc_a = __fmaf_rn(__fmul_rn(e8m0_f32(w4 & 0xFFu), x0s), d[ii][0], acc_a);
-        acc_a = __fmaf_rn(__fmul_rn(e8m0_f32((w4 >> 8) & 0xFFu), x1s), d[ii][1], acc_a);
-        acc_b = __fmaf_rn(__fmul_rn(e8m0_f32((w4 >> 16) & 0xFFu), x0s), d[ii][2], acc_b);
-        acc_b = __fmaf_rn(__fmul_rn(e8m0_f32(w4 >> 24), x1s), d[ii][3], acc_b);
+        float q0, q1, q2, q3;
+        if (exact) {
+          q0 = e8m0_f32(w4 & 0xFFu); q1 = e8m0_f32((w4 >> 8) & 0xFFu);
+          q2 = e8m0_f32((w4 >> 16) & 0xFFu); q3 = e8m0_f32(w4 >> 24);
+        } else {
+          q0 = e8m0_fast<0>(w4); q1 = e8m0_fast<1>(w4); q2 = e8m0_fast<2>(w4); q3 = e8m0_fast<3>(w4);
+        }
+        acc_a = __fmaf_rn(__fmul_rn(q0, x0s), d[ii][0], acc_a);
+        acc_a = __fmaf_rn(__fmul_rn(q1, x1s), d[ii][1], acc_a);
+        acc_b = __fmaf_rn(__fmul_rn(q2, x0s), d[ii][2], acc_b);
+        acc_b = __fmaf_rn(__fmul_rn(q3, x1s), d[ii][3], acc_b);
       } else if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {
-        const float ca = __fmul_rn(e8m0_f32(cs[i].a0), x0s), cb = __fmul_rn(e8m0_f32(cs[i].b0), x0s);
+        const uint32_t w4 = cs[i].a0;
+        const float qa = exact ? e8m0_f32(w4 & 0xFFu) : e8m0_fast<0>(w4);
+        const float qb = exact ? e8m0_f32((w4 >> 16) & 0xFFu) : e8m0_fast<2>(w4);
+        const float ca = __fmul_rn(qa, x0s), cb = __fmul_rn(qb, x0s);
         acc_a = __fmaf_rn(ca, d[ii][0] + d[ii][1], acc_a);
         acc_b = __fmaf_rn(cb, d[ii][2] + d[ii][3], acc_b);
       } else if constexpr (F == NVFP8) {
@@ -403,6 +466,11 @@ __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __r
         acc_b = __fmaf_rn(x0s, d[ii][2], acc_b);
         acc_b = __fmaf_rn(x1s, d[ii][3], acc_b);
       }
+    }
+    // the pair's registers are free: request the same slots of the next round
+    if (r + 1 < rounds) {
+      load_chunk(r + 1, ip);
+      load_chunk(r + 1, ip + 1);
     }
     }
   }
@@ -429,8 +497,8 @@ __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __r
   }
 }
 
-template <int F>
-static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
+template <int F, int MR>
+static cudaError_t launch_mr(const void* codes, const void* scales, float glob, const void* x, void* out,
                               bool out_f32, int M, int N, int K, cudaStream_t st) {
   static std::atomic<int> attr_done[64];
   const size_t sm = smem_bytes(F, M, K);
@@ -438,7 +506,7 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, float glob,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
-    e = cudaFuncSetAttribute(qgemv_m2_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
+    e = cudaFuncSetAttribute(qgemv_m2_kernel<F, MR>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
     if (e != cudaSuccess) return e;
     attr_done[dev].store(1);
   }
@@ -452,9 +520,16 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, float glob,
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F>, static_cast<const uint8_t*>(codes),
+  return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F, MR>, static_cast<const uint8_t*>(codes),
                             static_cast<const uint8_t*>(scales), glob, static_cast<const uint16_t*>(x), out,
                             int(out_f32), M, N, K);
+}
+
+template <int F>
+static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
+                              bool out_f32, int M, int N, int K, cudaStream_t st) {
+  if (M == 1) return launch_mr<F, 1>(codes, scales, glob, x, out, out_f32, M, N, K, st);
+  return launch_mr<F, 2>(codes, scales, glob, x, out, out_f32, M, N, K, st);
 }
 
 }  // namespace gemv_m2

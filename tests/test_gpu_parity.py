@@ -258,3 +258,29 @@ def test_full_size_sampled(fmt, m, n, k, outl):
     got = out[rows, cols].astype(np.float64)
     err = np.abs(got - ref)
     assert (err <= bound + np.abs(got) * 2.0 ** -9).all(), float((err / bound).max())
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8_e4m3", "mxfp8_e5m2"])
+@pytest.mark.parametrize("m", [1, 2, 5])
+def test_gemv_e8m0_special_scales(fmt, m):
+    # E8M0 code 0 (2^-127, a float32 subnormal) among ordinary scales, then a
+    # 255 (NaN) scale: the NaN reaches exactly the outputs of its weight row
+    # (rlx-cpu lowp_scaled_matmul multiplies every block sum by its scale)
+    n, k = 48, 256
+    c, s, g = _packed(fmt, n, k, seed=31)
+    rng = np.random.default_rng(32)
+    s = s.copy()
+    s[rng.random(s.shape) < 0.2] = 0
+    s[3, :] = 0
+    xb, xt = _x(m, k, seed=33)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, m, "zero scales"))
+    s[5, 2] = 255
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n).float().cpu().numpy()
+    assert np.isnan(out[:, 5]).all()
+    keep = np.ones(n, bool)
+    keep[5] = False
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    err = np.abs(out[:, keep] - ref[:, keep])
+    assert (err <= bound[:, keep] + np.abs(out[:, keep]) * 2.0 ** -9).all()

@@ -39,7 +39,10 @@ namespace gemv_m2 {
 
 constexpr int WARPS = 8;
 constexpr int THREADS = WARPS * 32;
-constexpr int P = 4;              // chunks per warp held in registers at a time
+// chunks per warp held in registers at a time: four 64-byte chunks (the whole
+// of a 4096-wide fp4 row share); the E8M0 8-bit formats hold eight
+template <int F>
+constexpr int chunks_in_flight() { return (F == MXFP8_E4M3 || F == MXFP8_E5M2) ? 8 : 4; }
 constexpr size_t SMEM_LIMIT = 96 * 1024;
 
 template <int F>
@@ -162,12 +165,13 @@ struct ChunkScales {
   uint32_t a0, a1, b0, b1;
 };
 
-template <int F, int MR>
-__global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __restrict__ codes,
+template <int F, int MR, bool UNI>
+__global__ void __launch_bounds__(THREADS, 2) qgemv_m2_kernel(const uint8_t* __restrict__ codes,
                                                            const uint8_t* __restrict__ scales, float glob,
                                                            const uint16_t* __restrict__ x, void* __restrict__ out,
                                                            int out_f32, int M, int N, int K) {
   using S = Shape<F>;
+  constexpr int P = chunks_in_flight<F>();
   constexpr bool FOUR = S::four, I4 = F == INT4_AFFINE;
   constexpr int CODES = S::CODES, LANE = S::LANE;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -198,55 +202,66 @@ __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __r
   ChunkScales cs[P];
   uint32_t ms[P];      // nvfp4: this lane's two E4M3 micro-scales, row g (low half) and row g + 8
 
+  // Rows past N read row 0 (their outputs are never stored).  UNI: every
+  // warp's chunks are whole and in range (K a multiple of 8 chunks, the chunk
+  // count per warp a multiple of P), so the loads carry no predicates and
+  // paired E8M0 bytes come in one 16-bit load.
+  constexpr bool uni = UNI;
+  constexpr int SB = FmtTraits<F>::sbytes;
+  const uint8_t* sra = scales + int64_t(va ? ra : 0) * nblk * SB;           // row g's scales
+  const uint8_t* srb = scales + int64_t(vb ? rb : 0) * nblk * SB;           // row g + 8's scales
+
   // chunk slot i of round r: codes of rows g and g + 8 and their scales
   auto load_chunk = [&](int r, int i) {
-    {
-      const int c = warp + WARPS * (r * P + i);
-      const bool live = r * P + i < mine;
-      const int ks = c * CODES + LANE * t;                                   // this lane's first k
-      const bool kin = live && ks < K;
-      wa[i] = (kin && va) ? ldg_stream(pa + int64_t(c) * 64) : make_uint4(0, 0, 0, 0);
-      wb[i] = (kin && vb) ? ldg_stream(pb + int64_t(c) * 64) : make_uint4(0, 0, 0, 0);
-      // the block (or pair of blocks) of quad lanes a0 and a0 + 1 in this chunk
-      const int k0 = c * CODES + LANE * a0;
-      const bool c0 = live && k0 < K, c1 = live && k0 + LANE < K;
-      const int64_t ia = int64_t(va ? ra : 0) * nblk, ib = int64_t(vb ? rb : 0) * nblk;
-      if constexpr (F == MXFP4) {
-        const int64_t e = k0 / 32;
-        // four E8M0 bytes; a block outside the matrix reads as 127 (its D column is zero)
-        const uint32_t x0 = (c0 && va) ? __ldg(scales + ia + e) : 127u;
-        const uint32_t x1 = (c1 && va) ? __ldg(scales + ia + e + 1) : 127u;
-        const uint32_t x2 = (c0 && vb) ? __ldg(scales + ib + e) : 127u;
-        const uint32_t x3 = (c1 && vb) ? __ldg(scales + ib + e + 1) : 127u;
+    const int c = warp + WARPS * (r * P + i);
+    const int ks = c * CODES + LANE * t;                                     // this lane's first k
+    const int k0 = c * CODES + LANE * a0;                                    // quad lane a0's first k
+    const bool live = uni || r * P + i < mine;
+    const bool kin = uni || (live && ks < K);
+    const bool c0 = uni || (live && k0 < K), c1 = uni || (live && k0 + LANE < K);
+    wa[i] = kin ? ldg_stream(pa + int64_t(c) * 64) : make_uint4(0, 0, 0, 0);
+    wb[i] = kin ? ldg_stream(pb + int64_t(c) * 64) : make_uint4(0, 0, 0, 0);
+    // the block (or pair of blocks) of quad lanes a0 and a0 + 1 in this chunk;
+    // a block outside the matrix reads as E8M0 127 / zero (its D column is zero)
+    if constexpr (F == MXFP4) {
+      const int e = k0 / 32;                                                  // even
+      if (uni) {
+        const uint32_t pa2 = __ldg(reinterpret_cast<const uint16_t*>(sra) + e / 2);
+        const uint32_t pb2 = __ldg(reinterpret_cast<const uint16_t*>(srb) + e / 2);
+        cs[i].a0 = prmt(pa2, pb2, 0x5410u);                                   // four E8M0 bytes
+      } else {
+        const uint32_t x0 = c0 ? __ldg(sra + e) : 127u;
+        const uint32_t x1 = c1 ? __ldg(sra + e + 1) : 127u;
+        const uint32_t x2 = c0 ? __ldg(srb + e) : 127u;
+        const uint32_t x3 = c1 ? __ldg(srb + e + 1) : 127u;
         cs[i].a0 = x0 | (x1 << 8) | (x2 << 16) | (x3 << 24);
-        cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
-      } else if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {
-        const int64_t e = k0 / 32;                                            // a0, a0 + 1 share it
-        const uint32_t x0 = (c0 && va) ? __ldg(scales + ia + e) : 127u;
-        const uint32_t x2 = (c0 && vb) ? __ldg(scales + ib + e) : 127u;
-        cs[i].a0 = x0 | (127u << 8) | (x2 << 16) | (127u << 24);               // bytes 0 and 2 used
-        cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
-      } else if constexpr (F == NVFP8) {
-        const float* sf = reinterpret_cast<const float*>(scales);
-        const int64_t e = k0 / 16;
-        cs[i].a0 = (c0 && va) ? __float_as_uint(__ldg(sf + ia + e)) : 0u;
-        cs[i].a1 = (c1 && va) ? __float_as_uint(__ldg(sf + ia + e + 1)) : 0u;
-        cs[i].b0 = (c0 && vb) ? __float_as_uint(__ldg(sf + ib + e)) : 0u;
-        cs[i].b1 = (c1 && vb) ? __float_as_uint(__ldg(sf + ib + e + 1)) : 0u;
-      } else if constexpr (F == INT4_AFFINE) {
-        const uint32_t* sp = reinterpret_cast<const uint32_t*>(scales);
-        const int64_t e = k0 / 64;                                            // a0, a0 + 1 share it
-        cs[i].a0 = (c0 && va) ? __ldg(sp + ia + e) : 0u;
-        cs[i].b0 = (c0 && vb) ? __ldg(sp + ib + e) : 0u;
-        cs[i].a1 = cs[i].b1 = 0u;
-      } else {   // NVFP4: the lane's own two micro-blocks, one 16-bit pair per row
-        const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales);
-        const int64_t e = ks / 32;                                            // pair index (16-code blocks / 2)
-        const uint32_t ma = (kin && va) ? __ldg(sp + ia / 2 + e) : 0u;
-        const uint32_t mb2 = (kin && vb) ? __ldg(sp + ib / 2 + e) : 0u;
-        ms[i] = ma | (mb2 << 16);
-        cs[i].a0 = cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
       }
+      cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
+    } else if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+      const int e = k0 / 32;                                                  // a0, a0 + 1 share it
+      const uint32_t x0 = c0 ? __ldg(sra + e) : 127u;
+      const uint32_t x2 = c0 ? __ldg(srb + e) : 127u;
+      cs[i].a0 = prmt(x0, x2, 0x1410u) | 0x7F007F00u;                         // bytes 0 and 2 used, 1 and 3 = 127
+      cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
+    } else if constexpr (F == NVFP8) {
+      const float* sfa = reinterpret_cast<const float*>(sra);
+      const float* sfb = reinterpret_cast<const float*>(srb);
+      const int e = k0 / 16;
+      cs[i].a0 = c0 ? __float_as_uint(__ldg(sfa + e)) : 0u;
+      cs[i].a1 = c1 ? __float_as_uint(__ldg(sfa + e + 1)) : 0u;
+      cs[i].b0 = c0 ? __float_as_uint(__ldg(sfb + e)) : 0u;
+      cs[i].b1 = c1 ? __float_as_uint(__ldg(sfb + e + 1)) : 0u;
+    } else if constexpr (F == INT4_AFFINE) {
+      const int e = k0 / 64;                                                  // a0, a0 + 1 share it
+      cs[i].a0 = c0 ? __ldg(reinterpret_cast<const uint32_t*>(sra) + e) : 0u;
+      cs[i].b0 = c0 ? __ldg(reinterpret_cast<const uint32_t*>(srb) + e) : 0u;
+      cs[i].a1 = cs[i].b1 = 0u;
+    } else {   // NVFP4: the lane's own two micro-blocks, one 16-bit pair per row
+      const int e = ks / 32;                                                  // pair index (16-code blocks / 2)
+      const uint32_t ma = kin ? __ldg(reinterpret_cast<const uint16_t*>(sra) + e) : 0u;
+      const uint32_t mb2 = kin ? __ldg(reinterpret_cast<const uint16_t*>(srb) + e) : 0u;
+      ms[i] = prmt(ma, mb2, 0x5410u);
+      cs[i].a0 = cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
     }
   };
   auto load_round = [&](int r) {
@@ -497,7 +512,7 @@ __global__ void __launch_bounds__(THREADS, 3) qgemv_m2_kernel(const uint8_t* __r
   }
 }
 
-template <int F, int MR>
+template <int F, int MR, bool UNI>
 static cudaError_t launch_mr(const void* codes, const void* scales, float glob, const void* x, void* out,
                               bool out_f32, int M, int N, int K, cudaStream_t st) {
   static std::atomic<int> attr_done[64];
@@ -506,7 +521,7 @@ static cudaError_t launch_mr(const void* codes, const void* scales, float glob, 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
-    e = cudaFuncSetAttribute(qgemv_m2_kernel<F, MR>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
+    e = cudaFuncSetAttribute(qgemv_m2_kernel<F, MR, UNI>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
     if (e != cudaSuccess) return e;
     attr_done[dev].store(1);
   }
@@ -520,7 +535,7 @@ static cudaError_t launch_mr(const void* codes, const void* scales, float glob, 
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F, MR>, static_cast<const uint8_t*>(codes),
+  return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F, MR, UNI>, static_cast<const uint8_t*>(codes),
                             static_cast<const uint8_t*>(scales), glob, static_cast<const uint16_t*>(x), out,
                             int(out_f32), M, N, K);
 }
@@ -528,8 +543,14 @@ static cudaError_t launch_mr(const void* codes, const void* scales, float glob, 
 template <int F>
 static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
                               bool out_f32, int M, int N, int K, cudaStream_t st) {
-  if (M == 1) return launch_mr<F, 1>(codes, scales, glob, x, out, out_f32, M, N, K, st);
-  return launch_mr<F, 2>(codes, scales, glob, x, out, out_f32, M, N, K, st);
+  constexpr int CODES = Shape<F>::CODES;
+  const int nchunk = (K + CODES - 1) / CODES;
+  const bool uni = K % (WARPS * CODES) == 0 && (nchunk / WARPS) % chunks_in_flight<F>() == 0;
+  if (M == 1)
+    return uni ? launch_mr<F, 1, true>(codes, scales, glob, x, out, out_f32, M, N, K, st)
+               : launch_mr<F, 1, false>(codes, scales, glob, x, out, out_f32, M, N, K, st);
+  return uni ? launch_mr<F, 2, true>(codes, scales, glob, x, out, out_f32, M, N, K, st)
+             : launch_mr<F, 2, false>(codes, scales, glob, x, out, out_f32, M, N, K, st);
 }
 
 }  // namespace gemv_m2

@@ -537,6 +537,8 @@ cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float g
                          bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms) {
   (void)sms;
   if (qgemv_m2_fits(fmt, M, K)) return launch_qgemv_m2(fmt, codes, scales, glob, x, out, out_f32, M, N, K, st);
+  if (M >= 3 && qgemv_mb_fits(fmt, M, K))
+    return launch_qgemv_mb(fmt, codes, scales, glob, x, out, out_f32, M, N, K, st);
   const int m = int(M), n = int(N), k = int(K);
   switch (fmt) {
     case MXFP4: return gemv::launch_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);

@@ -284,3 +284,17 @@ def test_gemv_e8m0_special_scales(fmt, m):
     ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
     err = np.abs(out[:, keep] - ref[:, keep])
     assert (err <= bound[:, keep] + np.abs(out[:, keep]) * 2.0 ** -9).all()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("m", [3, 12, 16])
+def test_batch_gemv_split_k_ragged(fmt, m):
+    # K not a multiple of 128 and large enough that 3 <= M <= 16 splits it over
+    # a cluster of CTAs: the last K part ends inside a chunk; N ends inside a
+    # 64-row CTA tile
+    n, k = 100, (2112 if fmt == "int4_affine" else 2080)
+    c, s, g = _packed(fmt, n, k, seed=40 + m)
+    xb, xt = _x(m, k, seed=41 + m)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, m, k))

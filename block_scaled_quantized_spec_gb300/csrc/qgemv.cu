@@ -538,7 +538,7 @@ cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float g
   (void)sms;
   if (qgemv_m2_fits(fmt, M, K)) return launch_qgemv_m2(fmt, codes, scales, glob, x, out, out_f32, M, N, K, st);
   if (M >= 3 && qgemv_mb_fits(fmt, M, K))
-    return launch_qgemv_mb(fmt, codes, scales, glob, x, out, out_f32, M, N, K, st);
+    return launch_qgemv_mb(fmt, codes, scales, glob, x, out, out_f32, M, N, K, st, sms);
   const int m = int(M), n = int(N), k = int(K);
   switch (fmt) {
     case MXFP4: return gemv::launch_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);

@@ -37,9 +37,13 @@ namespace gemv_mb {
 constexpr int WARPS = 4;
 constexpr int THREADS = WARPS * 32;
 constexpr int ROWS = 16 * WARPS;        // weight rows per CTA
-constexpr int P = 4;                    // 64-byte chunks per lane in flight
 constexpr int XSPAN = 128;              // activations sharing one power-of-two scale
-constexpr size_t X_BUDGET = 32 * 1024;  // staged f16 activations per CTA
+constexpr size_t X_BUDGET = 40 * 1024;  // staged f16 activations per CTA (five CTAs per SM)
+
+// 64-byte chunks per lane in flight: four; two for nvfp8 and int4 affine,
+// whose per-chunk scales (eight float32, four scale/bias pairs) stay in registers
+template <int F>
+constexpr int chunks_in_flight() { return (F == NVFP8 || F == INT4_AFFINE) ? 2 : 4; }
 
 template <int F>
 struct Shape {
@@ -150,8 +154,8 @@ inline size_t smem_bytes(int F, int M, int kr) {
 template <int F>
 constexpr int scale_words() { return F == NVFP8 ? 8 : (F == INT4_AFFINE ? 4 : 2); }
 
-template <int F, int NB>
-__global__ void __launch_bounds__(THREADS) qgemv_mb_kernel(const uint8_t* __restrict__ codes,
+template <int F, int NB, bool UNI>
+__global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __restrict__ codes,
                                                            const uint8_t* __restrict__ scales, float glob,
                                                            const uint16_t* __restrict__ x, void* __restrict__ out,
                                                            int out_f32, int M, int N, int K, int KR) {
@@ -160,6 +164,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_mb_kernel(const uint8_t* __rest
   constexpr int CODES = S::CODES, SEG = S::SEG;
   constexpr int BLK = FmtTraits<F>::block, SB = FmtTraits<F>::sbytes;
   constexpr int SW = scale_words<F>();
+  constexpr int P = chunks_in_flight<F>();
   extern __shared__ __align__(16) uint8_t smem[];
   const int xst = xstride(KR, read_bytes<F>());
   const int nsp = KR / XSPAN;
@@ -198,12 +203,13 @@ __global__ void __launch_bounds__(THREADS) qgemv_mb_kernel(const uint8_t* __rest
   auto load_chunk = [&](int c, int i) {
     #pragma unroll
     for (int sg = 0; sg < 4; ++sg) {
-      const bool ok = c < nch && k0 + c * CODES + sg * SEG < k1;
+      // UNI: every CTA's K range is whole and a multiple of P chunks
+      const bool ok = UNI || (c < nch && k0 + c * CODES + sg * SEG < k1);
       wa[i][sg] = ok ? ldg_word(pa + int64_t(c) * 64 + 16 * sg) : 0u;
       wb[i][sg] = ok ? ldg_word(pb + int64_t(c) * 64 + 16 * sg) : 0u;
     }
     const int kc = k0 + c * CODES;                                          // first k of the chunk
-    auto live = [&](int k) { return c < nch && k < k1; };
+    auto live = [&](int k) { return UNI || (c < nch && k < k1); };
     if constexpr (F == MXFP4) {                                             // one E8M0 block per segment
       uint32_t a = 0, b = 0;
       #pragma unroll
@@ -496,12 +502,15 @@ __global__ void __launch_bounds__(THREADS) qgemv_mb_kernel(const uint8_t* __rest
 }
 
 // The K split: the smallest cluster size S in {1, 2, 4, 8} whose per-CTA K
-// range (rounded up to 128) keeps the staged activations within X_BUDGET.
-inline bool plan(int F, int M, int K, int* S, int* KR) {
+// range (rounded up to 128) keeps the staged activations within X_BUDGET and
+// gives at least four CTAs per SM (shorter K ranges per warp, fewer rounds).
+inline bool plan(int F, int M, int N, int K, int sms, int* S, int* KR) {
   const int rb = (F == MXFP4 || F == NVFP4 || F == INT4_AFFINE) ? 64 : 32;
+  const int row_ctas = (N + ROWS - 1) / ROWS;
   for (int s = 1; s <= 8; s *= 2) {
     const int kr = ((K + s - 1) / s + XSPAN - 1) / XSPAN * XSPAN;
-    if (size_t(M) * xstride(kr, rb) * 2 <= X_BUDGET) {
+    const bool fits = size_t(M) * xstride(kr, rb) * 2 <= X_BUDGET;
+    if (fits && (row_ctas * s >= 4 * sms || s == 8 || kr == XSPAN)) {
       *S = s;
       *KR = kr;
       return true;
@@ -510,11 +519,9 @@ inline bool plan(int F, int M, int K, int* S, int* KR) {
   return false;
 }
 
-template <int F, int NB>
+template <int F, int NB, bool UNI>
 static cudaError_t launch_nb(const void* codes, const void* scales, float glob, const void* x, void* out,
-                             bool out_f32, int M, int N, int K, cudaStream_t st) {
-  int S = 1, KR = 0;
-  if (!plan(F, M, K, &S, &KR)) return cudaErrorInvalidValue;
+                             bool out_f32, int M, int N, int K, int S, int KR, cudaStream_t st) {
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -529,35 +536,41 @@ static cudaError_t launch_nb(const void* codes, const void* scales, float glob, 
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 2;
-  return cudaLaunchKernelEx(&lc, qgemv_mb_kernel<F, NB>, static_cast<const uint8_t*>(codes),
+  return cudaLaunchKernelEx(&lc, qgemv_mb_kernel<F, NB, UNI>, static_cast<const uint8_t*>(codes),
                             static_cast<const uint8_t*>(scales), glob, static_cast<const uint16_t*>(x), out,
                             int(out_f32), M, N, K, KR);
 }
 
 template <int F>
 static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
-                              bool out_f32, int M, int N, int K, cudaStream_t st) {
-  if (M <= 8) return launch_nb<F, 1>(codes, scales, glob, x, out, out_f32, M, N, K, st);
-  return launch_nb<F, 2>(codes, scales, glob, x, out, out_f32, M, N, K, st);
+                              bool out_f32, int M, int N, int K, cudaStream_t st, int sms) {
+  int S = 1, KR = 0;
+  if (!plan(F, M, N, K, sms, &S, &KR)) return cudaErrorInvalidValue;
+  const bool uni = S * KR == K && (KR / Shape<F>::CODES) % chunks_in_flight<F>() == 0;
+  if (M <= 8)
+    return uni ? launch_nb<F, 1, true>(codes, scales, glob, x, out, out_f32, M, N, K, S, KR, st)
+               : launch_nb<F, 1, false>(codes, scales, glob, x, out, out_f32, M, N, K, S, KR, st);
+  return uni ? launch_nb<F, 2, true>(codes, scales, glob, x, out, out_f32, M, N, K, S, KR, st)
+             : launch_nb<F, 2, false>(codes, scales, glob, x, out, out_f32, M, N, K, S, KR, st);
 }
 
 }  // namespace gemv_mb
 
 bool qgemv_mb_fits(int fmt, int64_t M, int64_t K) {
   int S = 0, KR = 0;
-  return M >= 1 && M <= 16 && K <= (int64_t(1) << 24) && gemv_mb::plan(fmt, int(M), int(K), &S, &KR);
+  return M >= 1 && M <= 16 && K <= (int64_t(1) << 24) && gemv_mb::plan(fmt, int(M), 1, int(K), 1, &S, &KR);
 }
 
 cudaError_t launch_qgemv_mb(int fmt, const void* codes, const void* scales, float glob, const void* x, void* out,
-                            bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+                            bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms) {
   const int m = int(M), n = int(N), k = int(K);
   switch (fmt) {
-    case MXFP4: return gemv_mb::launch_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case NVFP4: return gemv_mb::launch_fmt<NVFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case MXFP8_E4M3: return gemv_mb::launch_fmt<MXFP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case MXFP8_E5M2: return gemv_mb::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case NVFP8: return gemv_mb::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    default: return gemv_mb::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP4: return gemv_mb::launch_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case NVFP4: return gemv_mb::launch_fmt<NVFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXFP8_E4M3: return gemv_mb::launch_fmt<MXFP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXFP8_E5M2: return gemv_mb::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case NVFP8: return gemv_mb::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    default: return gemv_mb::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }
 

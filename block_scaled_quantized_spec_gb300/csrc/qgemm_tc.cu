@@ -122,6 +122,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// four floats at the same shared-memory offset in cluster CTA `rank`
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  float4 v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(r)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -200,6 +214,7 @@ struct Params {
   float glob;
   int M, N, K;
   int out_f32;
+  int kb_per;          // K steps per split (grid z = the splits of one cluster)
   uint64_t limit_ns;   // bound on every wait
   int drop_arrivals;   // test hook: decoders never signal a stage (the waits must expire)
 };
@@ -218,6 +233,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
   constexpr int ROWS_PER_PASS = DEC_THREADS / PIECES_PER_ROW;            // 128 or 64
   constexpr int NREG = T::four ? 16 : 8;
   constexpr uint32_t LO_OFF = uint32_t(BN) * BK * 2;       // lo rows follow the hi rows
+  constexpr int PSTRIDE = BN + 4;                          // floats per partial-tile row (K split)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -229,6 +245,11 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM * MT;
   const int nkb = (p.K + BK - 1) / BK;
+  // K split: this CTA accumulates K steps [kb0, kb1) (one split per cluster rank along z)
+  const int kb0 = blockIdx.z * p.kb_per;
+  const int kb1 = min(nkb, kb0 + p.kb_per);
+  const int nloc = kb1 - kb0;
+  const bool split_k = gridDim.z > 1;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
   auto a_full = [&](int s) { return bar0 + 8u * s; };
@@ -273,25 +294,25 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
     if (lane == 0) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
       int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
+      for (int j = 0; j < nloc; ++j) {
+        const int s = j % STAGES;
+        const uint32_t ph = (j / STAGES) & 1;
         if (*abort_flag) break;
         if (!mbar_wait(empty(s), ph ^ 1u, p.limit_ns)) { fail(); break; }
         mbar_arrive_expect_tx(a_full(s), A_BYTES);
-        tma_load_2d(stage_a(s), &xmap, kb * BK, m0, a_full(s));
-        issued = kb + 1;
+        tma_load_2d(stage_a(s), &xmap, (kb0 + j) * BK, m0, a_full(s));
+        issued = j + 1;
       }
       // every issued copy must land before the CTA may exit
-      for (int kb = issued > STAGES ? issued - STAGES : 0; kb < issued; ++kb)
-        if (!mbar_wait(a_full(kb % STAGES), (kb / STAGES) & 1, p.limit_ns)) fail();
+      for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+        if (!mbar_wait(a_full(j % STAGES), (j / STAGES) & 1, p.limit_ns)) fail();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
+      for (int j = 0; j < nloc; ++j) {
+        const int s = j % STAGES;
+        const uint32_t ph = (j / STAGES) & 1;
         if (*abort_flag) break;
         if (!mbar_wait(a_full(s), ph, p.limit_ns) || !mbar_wait(b_full(s), ph, p.limit_ns)) { fail(); break; }
         tc_fence_after();
@@ -302,7 +323,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
           for (int mt = 0; mt < MT; ++mt) {
             const uint64_t ad = desc_sw128(stage_a(s) + uint32_t(mt * BM * BK * 2));
             const uint32_t d = tmem + uint32_t(mt * BN);
-            mma_f16(d, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), IDESC, (kb | kk) != 0);
+            mma_f16(d, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), IDESC, (j | kk) != 0);
             if constexpr (SPLIT) mma_f16(d, ad + uint64_t(2 * kk), ld + uint64_t(2 * kk), IDESC, 1u);
           }
         }
@@ -325,17 +346,26 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
         const int r = rbase + i * ROWS_PER_PASS;
         const int n = n0 + r;
         const int64_t k0 = int64_t(kb) * BK + sub * PIECE;
-        const bool ok = kb < nkb && n < p.N && k0 < p.K;
+        const bool ok = kb < kb1 && n < p.N && k0 < p.K;
         v[i] = ok ? ldg_stream(p.codes + int64_t(n) * row_bytes + (T::four ? k0 / 2 : k0)) : make_uint4(0, 0, 0, 0);
         sc[i] = load_piece_scale<F>(p.scales, n, nblk, k0, ok);
       }
     };
-    load(0, cur, cs);
-    load(1, nxt, ns);
+    // a single 128-row tile: this CTA's weight slab [kb0, kb1) towards L2 now
+    // (one row per thread); with more M tiles the other tiles' CTAs share it
+    if (gridDim.y == 1 && dt < BN && n0 + dt < p.N && nloc > 0) {
+      const int64_t kbeg = int64_t(kb0) * BK, kend = min(int64_t(kb1) * BK, int64_t(p.K));
+      const uint8_t* src = p.codes + int64_t(n0 + dt) * row_bytes + (T::four ? kbeg / 2 : kbeg);
+      const uint32_t bytes = uint32_t(T::four ? (kend - kbeg) / 2 : (kend - kbeg)) & ~15u;
+      if (bytes) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+    }
+    load(kb0, cur, cs);
+    load(kb0 + 1, nxt, ns);
     bool aborted = false;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = (kb / STAGES) & 1;
+    for (int j = 0; j < nloc; ++j) {
+      const int kb = kb0 + j;
+      const int s = j % STAGES;
+      const uint32_t ph = (j / STAGES) & 1;
       int ok = 1;
       if (lane == 0) ok = (*abort_flag == 0u) && mbar_wait(empty(s), ph ^ 1u, p.limit_ns);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -393,6 +423,14 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
       for (int cb = 0; cb < BN / 32; ++cb) {
         uint32_t r[32];
         tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(mt * BN + cb * 32), r);
+        if (split_k) {   // this split's partial tile into the (drained) stage memory
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(smem) + (q * 32 + lane) * PSTRIDE + cb * 32);
+          #pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                                 __uint_as_float(r[4 * j + 3]));
+          continue;
+        }
         const int nb = n0 + cb * 32;
         if (!live || m >= p.M || nb >= p.N) continue;
         float v[32];
@@ -430,6 +468,46 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_const
     }
   }
 
+  if (split_k) {
+    // The splits of one tile form a cluster: each CTA sums a slice of the
+    // tile over the cluster's partial tiles (rank order) and stores it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    cluster_sync();
+    uint32_t rank, csize;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
+    constexpr int E = BM * (BN / 4);                       // float4 elements of the tile
+    const int e0 = int(rank) * E / int(csize), e1 = (int(rank) + 1) * E / int(csize);
+    for (int e = e0 + int(threadIdx.x); e < e1; e += THREADS) {
+      const int row = e / (BN / 4), c4 = e - row * (BN / 4);
+      const int m = m0 + row, n = n0 + 4 * c4;
+      if (m >= p.M || n >= p.N) continue;
+      const uint32_t sa = sbase + uint32_t((row * PSTRIDE + 4 * c4) * 4);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (uint32_t q = 0; q < csize; ++q) {
+        const float4 w = ld_cluster_f32x4(sa, q);
+        v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+      }
+      if constexpr (F == NVFP4) { v.x *= p.glob; v.y *= p.glob; v.z *= p.glob; v.w *= p.glob; }
+      const float f4[4] = {v.x, v.y, v.z, v.w};
+      const bool vec = n + 4 <= p.N && (p.N & 3) == 0;
+      if (p.out_f32) {
+        float* o = static_cast<float*>(p.out) + int64_t(m) * p.N + n;
+        if (vec) *reinterpret_cast<float4*>(o) = v;
+        else for (int j = 0; j < 4 && n + j < p.N; ++j) o[j] = f4[j];
+      } else {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + int64_t(m) * p.N + n;
+        if (vec) {
+          *reinterpret_cast<uint2*>(o) = make_uint2(f32_to_bf16bits(v.x) | (f32_to_bf16bits(v.y) << 16),
+                                                    f32_to_bf16bits(v.z) | (f32_to_bf16bits(v.w) << 16));
+        } else {
+          for (int j = 0; j < 4 && n + j < p.N; ++j) o[j] = __float2bfloat16_rn(f4[j]);
+        }
+      }
+    }
+    cluster_sync();   // no CTA leaves while the others still read its partial tile
+  }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -462,7 +540,7 @@ static std::atomic<int> g_drop{0};
 
 template <int F, int MT>
 static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* scales, float glob, const void* x,
-                             void* out, bool out_f32, int M, int N, int K, cudaStream_t st) {
+                             void* out, bool out_f32, int M, int N, int K, cudaStream_t st, int sms) {
   static std::atomic<int> attr_done[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -493,42 +571,61 @@ static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* s
   prm.out_f32 = out_f32 ? 1 : 0;
   prm.limit_ns = g_limit_ns.load();
   prm.drop_arrivals = g_drop.load();
+  // K split (one 128-row tile only, whose partial tile fits the stage memory):
+  // S splits of every tile form a cluster; S in 1..4 minimises the waves of
+  // one-CTA-per-SM work, ceil(tiles * S / SMs) / S, with no split left empty.
+  const int tiles = ((N + Tile<F>::BN - 1) / Tile<F>::BN) * ((M + BM * MT - 1) / (BM * MT));
+  const int nkb = (K + BK - 1) / BK;
+  int S = 1;
+  if (MT == 1) {
+    double best = 1.0;
+    for (int s = 2; s <= 4; ++s) {
+      const int per = (nkb + s - 1) / s;
+      if ((s - 1) * per >= nkb) continue;
+      const double cost = double((tiles * s + sms - 1) / sms) / s;
+      if (cost < best - 1e-9) { best = cost; S = s; }
+    }
+  }
+  prm.kb_per = (nkb + S - 1) / S;
   cudaLaunchConfig_t lc = {};
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.gridDim = dim3((N + Tile<F>::BN - 1) / Tile<F>::BN, (M + BM * MT - 1) / (BM * MT));
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = 1;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = unsigned(S);
+  lc.gridDim = dim3((N + Tile<F>::BN - 1) / Tile<F>::BN, (M + BM * MT - 1) / (BM * MT), S);
   lc.blockDim = dim3(THREADS);
   lc.dynamicSmemBytes = Pipe<MT>::SMEM_BYTES;
   lc.stream = st;
   lc.attrs = at;
-  lc.numAttrs = 1;
+  lc.numAttrs = 2;
   return cudaLaunchKernelEx(&lc, qgemm_tc_kernel<F, MT>, map, prm);
 }
 
 // 256-row tiles once M exceeds one 128-row tile.
 template <int F>
 static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
-                              bool out_f32, int M, int N, int K, cudaStream_t st) {
+                              bool out_f32, int M, int N, int K, cudaStream_t st, int sms) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  if (M > BM) return launch_mt<F, 2>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st);
-  return launch_mt<F, 1>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st);
+  if (M > BM) return launch_mt<F, 2>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st, sms);
+  return launch_mt<F, 1>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st, sms);
 }
 
 }  // namespace tc
 
 cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, float glob, const void* x, void* out,
                             bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms) {
-  (void)sms;
   const int m = int(M), n = int(N), k = int(K);
   switch (fmt) {
-    case MXFP4: return tc::launch_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case NVFP4: return tc::launch_fmt<NVFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case MXFP8_E4M3: return tc::launch_fmt<MXFP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case MXFP8_E5M2: return tc::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case NVFP8: return tc::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    default: return tc::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP4: return tc::launch_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case NVFP4: return tc::launch_fmt<NVFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXFP8_E4M3: return tc::launch_fmt<MXFP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXFP8_E5M2: return tc::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case NVFP8: return tc::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    default: return tc::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }
 

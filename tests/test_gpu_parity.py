@@ -298,3 +298,16 @@ def test_batch_gemv_split_k_ragged(fmt, m):
     out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
     ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
     _check_qmm(out, ref, bound, (fmt, m, k))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("m", [2, 16])
+def test_gemv_fallback_long_k(fmt, m):
+    # K too long for the activation slices of the register-direct GEMVs: the
+    # bulk-copy GEMV takes it in several K passes
+    n, k = 48, 24576
+    c, s, g = _packed(fmt, n, k, seed=50 + m)
+    xb, xt = _x(m, k, seed=51 + m)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, m, k))

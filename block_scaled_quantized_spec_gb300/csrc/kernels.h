@@ -18,7 +18,8 @@ cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float g
 // Register-direct decode GEMV for M <= 2 (when its staged activations fit).
 bool qgemv_m2_fits(int fmt, int64_t M, int64_t K);
 cudaError_t launch_qgemv_m2(int fmt, const void* codes, const void* scales, float glob, const void* x,
-                            void* out, bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st);
+                            void* out, bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st,
+                            int sms);
 
 // Batch decode GEMV for 3 <= M <= 16, K split over a thread-block cluster.
 bool qgemv_mb_fits(int fmt, int64_t M, int64_t K);

@@ -43,6 +43,9 @@ constexpr int THREADS = WARPS * 32;
 // of a 4096-wide fp4 row share); the E8M0 8-bit formats hold eight
 template <int F>
 constexpr int chunks_in_flight() { return (F == MXFP8_E4M3 || F == MXFP8_E5M2) ? 8 : 4; }
+// with W warps per CTA: 4-warp CTAs hold twice the 4-bit chunks per warp
+template <int F, int W>
+constexpr int chunks_per_warp() { return (W == 4 && FmtTraits<F>::four) ? 2 * chunks_in_flight<F>() : chunks_in_flight<F>(); }
 constexpr size_t SMEM_LIMIT = 96 * 1024;
 
 template <int F>
@@ -153,10 +156,10 @@ __host__ __device__ constexpr int xstride(int K) {
   return h + pad / 2;
 }
 
-inline size_t smem_bytes(int F, int M, int K) {
+inline size_t smem_bytes(int F, int M, int K, int warps = WARPS) {
   const int spans = K / 32;
   return size_t(M) * xstride(K) * 2 + 64 + size_t(M) * spans * 4 * (F == INT4_AFFINE ? 2 : 1) +
-         size_t(WARPS) * 2 * 16 * 4;
+         size_t(warps) * 2 * 16 * 4;
 }
 
 // Per-chunk scale words a D-holding lane keeps: the weight block scales of
@@ -165,13 +168,14 @@ struct ChunkScales {
   uint32_t a0, a1, b0, b1;
 };
 
-template <int F, int MR, bool UNI>
-__global__ void __launch_bounds__(THREADS, 2) qgemv_m2_kernel(const uint8_t* __restrict__ codes,
+template <int F, int MR, bool UNI, int W>
+__global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const uint8_t* __restrict__ codes,
                                                            const uint8_t* __restrict__ scales, float glob,
                                                            const uint16_t* __restrict__ x, void* __restrict__ out,
                                                            int out_f32, int M, int N, int K) {
   using S = Shape<F>;
-  constexpr int P = chunks_in_flight<F>();
+  constexpr int P = chunks_per_warp<F, W>();
+  constexpr int WARPS = W, THREADS = 32 * W;
   constexpr bool FOUR = S::four, I4 = F == INT4_AFFINE;
   constexpr int CODES = S::CODES, LANE = S::LANE;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -302,13 +306,14 @@ __global__ void __launch_bounds__(THREADS, 2) qgemv_m2_kernel(const uint8_t* __r
     constexpr int TPC = CODES / 16;                                            // tasks per chunk and row
     const int per_m = mine * TPC;
     const int tasks = M * per_m;
-    // MR tasks per lane and pass are in flight together (one per activation row)
-    for (int j0 = 0; j0 < tasks; j0 += 32 * MR) {
-      uint4 v[MR][2];
-      int kk[MR], mm[MR];
-      bool lv[MR];
+    // TIF tasks per lane and pass are in flight together (a round's worth)
+    constexpr int TIF = (MR * P * TPC + 31) / 32;
+    for (int j0 = 0; j0 < tasks; j0 += 32 * TIF) {
+      uint4 v[TIF][2];
+      int kk[TIF], mm[TIF];
+      bool lv[TIF];
       #pragma unroll
-      for (int u = 0; u < MR; ++u) {
+      for (int u = 0; u < TIF; ++u) {
         const int j = j0 + lane + 32 * u;
         const int m = j >= per_m ? 1 : 0;
         const int rem = j - m * per_m;
@@ -322,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 2) qgemv_m2_kernel(const uint8_t* __r
         v[u][1] = lv[u] ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
       }
       #pragma unroll
-      for (int u = 0; u < MR; ++u) {
+      for (int u = 0; u < TIF; ++u) {
         if (j0 + 32 * u >= tasks) break;                                       // uniform over the warp
         const bool live = lv[u];
         const int m = mm[u], k = kk[u];
@@ -512,16 +517,16 @@ __global__ void __launch_bounds__(THREADS, 2) qgemv_m2_kernel(const uint8_t* __r
   }
 }
 
-template <int F, int MR, bool UNI>
+template <int F, int MR, bool UNI, int W = 8>
 static cudaError_t launch_mr(const void* codes, const void* scales, float glob, const void* x, void* out,
                               bool out_f32, int M, int N, int K, cudaStream_t st) {
   static std::atomic<int> attr_done[64];
-  const size_t sm = smem_bytes(F, M, K);
+  const size_t sm = smem_bytes(F, M, K, W);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
-    e = cudaFuncSetAttribute(qgemv_m2_kernel<F, MR, UNI>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
+    e = cudaFuncSetAttribute(qgemv_m2_kernel<F, MR, UNI, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
     if (e != cudaSuccess) return e;
     attr_done[dev].store(1);
   }
@@ -530,21 +535,34 @@ static cudaError_t launch_mr(const void* codes, const void* scales, float glob, 
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   lc.gridDim = dim3((N + 15) / 16);
-  lc.blockDim = dim3(THREADS);
+  lc.blockDim = dim3(32 * W);
   lc.dynamicSmemBytes = sm;
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F, MR, UNI>, static_cast<const uint8_t*>(codes),
+  return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F, MR, UNI, W>, static_cast<const uint8_t*>(codes),
                             static_cast<const uint8_t*>(scales), glob, static_cast<const uint16_t*>(x), out,
                             int(out_f32), M, N, K);
 }
 
+// 8-warp CTAs (two per SM); E2M1 formats whose grid exceeds two CTAs per SM
+// use 4-warp CTAs holding all eight chunks of a 4096-wide row share (three
+// per SM: fewer, longer warps; measured faster for nvfp4 at N = 14336, not for
+// int4 affine).
 template <int F>
 static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
-                              bool out_f32, int M, int N, int K, cudaStream_t st) {
+                              bool out_f32, int M, int N, int K, cudaStream_t st, int sms) {
   constexpr int CODES = Shape<F>::CODES;
   const int nchunk = (K + CODES - 1) / CODES;
+  const bool wide = (F == MXFP4 || F == NVFP4) && (N + 15) / 16 > 2 * sms;
+  if (wide) {
+    const bool uni = K % (4 * CODES) == 0 && (nchunk / 4) % chunks_per_warp<F, 4>() == 0;
+    if (M == 1)
+      return uni ? launch_mr<F, 1, true, 4>(codes, scales, glob, x, out, out_f32, M, N, K, st)
+                 : launch_mr<F, 1, false, 4>(codes, scales, glob, x, out, out_f32, M, N, K, st);
+    return uni ? launch_mr<F, 2, true, 4>(codes, scales, glob, x, out, out_f32, M, N, K, st)
+               : launch_mr<F, 2, false, 4>(codes, scales, glob, x, out, out_f32, M, N, K, st);
+  }
   const bool uni = K % (WARPS * CODES) == 0 && (nchunk / WARPS) % chunks_in_flight<F>() == 0;
   if (M == 1)
     return uni ? launch_mr<F, 1, true>(codes, scales, glob, x, out, out_f32, M, N, K, st)
@@ -560,15 +578,15 @@ bool qgemv_m2_fits(int fmt, int64_t M, int64_t K) {
 }
 
 cudaError_t launch_qgemv_m2(int fmt, const void* codes, const void* scales, float glob, const void* x, void* out,
-                            bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+                            bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms) {
   const int m = int(M), n = int(N), k = int(K);
   switch (fmt) {
-    case MXFP4: return gemv_m2::launch_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case NVFP4: return gemv_m2::launch_fmt<NVFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case MXFP8_E4M3: return gemv_m2::launch_fmt<MXFP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case MXFP8_E5M2: return gemv_m2::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    case NVFP8: return gemv_m2::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
-    default: return gemv_m2::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP4: return gemv_m2::launch_fmt<MXFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case NVFP4: return gemv_m2::launch_fmt<NVFP4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXFP8_E4M3: return gemv_m2::launch_fmt<MXFP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXFP8_E5M2: return gemv_m2::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case NVFP8: return gemv_m2::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    default: return gemv_m2::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }
 

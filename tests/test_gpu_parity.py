@@ -311,3 +311,16 @@ def test_gemv_fallback_long_k(fmt, m):
     out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
     ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
     _check_qmm(out, ref, bound, (fmt, m, k))
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "int4_affine"])
+@pytest.mark.parametrize("m", [1, 2])
+def test_wide_gemv_four_warp_ctas(fmt, m):
+    # more 16-row tiles than two per SM: the 4-bit GEMV runs 4-warp CTAs; N
+    # ends inside a tile and K leaves a partial round
+    n, k = 6000, 1152
+    c, s, g = _packed(fmt, n, k, seed=60 + m)
+    xb, xt = _x(m, k, seed=61 + m)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, m))

@@ -276,10 +276,12 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
     const int per_m = KR / 16;
     const int tasks = M * per_m;
     const int iters = (tasks + THREADS - 1) / THREADS;
+    // i / per_m as a multiply-high: exact for i < 16 per_m < 2^32 / per_m
+    const uint32_t pm_magic = 0xFFFFFFFFu / uint32_t(per_m) + 1u;
     for (int j = 0; j < iters; ++j) {
       const int i = tid + j * THREADS;
       if (i < tasks) {
-        const int m = i / per_m, kk = (i - m * per_m) * 16;
+        const int m = int(__umulhi(uint32_t(i), pm_magic)), kk = (i - m * per_m) * 16;
         const bool ok = k0 + kk < k1;
         const uint16_t* src = ok ? x + int64_t(m) * K + k0 + kk : x;
         const uint32_t dst = xsa + uint32_t((m * xst + kk) * 2);
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
     for (int j = 0; j < iters; ++j) {
       const int i = tid + j * THREADS;
       const bool live = i < tasks;                                          // whole 8-lane groups
-      const int m = live ? i / per_m : 0;
+      const int m = live ? int(__umulhi(uint32_t(i), pm_magic)) : 0;
       const int kk = live ? (i - m * per_m) * 16 : 0;
       uint4* p16 = reinterpret_cast<uint4*>(xs + m * xst + kk);
       const uint4 v0 = live ? p16[0] : make_uint4(0, 0, 0, 0);
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
         for (int q = 0; q < 8; ++q) sm += f16x2_lo(o[q]) + f16x2_hi(o[q]);
         sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
         sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 2);
-        if (live && (kk & 63) == 0) xsum[m * (KR / 64) + kk / 64] = sm;
+        if (live && (kk & 63) == 0) xsum[m * (KR >> 6) + (kk >> 6)] = sm;
       }
       if (live && (kk & (XSPAN - 1)) == 0) xsc[m * nsp + kk / XSPAN] = __uint_as_float(uint32_t(127 - sh) << 23);
     }
@@ -427,8 +429,8 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
               const int blk = (c * CODES) / 64 + h;
               #pragma unroll
               for (int nb = 0; nb < NB; ++nb) {
-                xm0[nb] = xsum[mc0[nb] * (KR / 64) + blk];
-                xm1[nb] = xsum[mc1[nb] * (KR / 64) + blk];
+                xm0[nb] = xsum[mc0[nb] * (KR >> 6) + blk];
+                xm1[nb] = xsum[mc1[nb] * (KR >> 6) + blk];
               }
             } else {
               sa = e8m0_f32((sc[i][0] >> (8 * (sg >> 1))) & 0xFFu);
@@ -487,8 +489,10 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
     const int rpr = ROWS / int(csize);                                      // rows reduced by this CTA
+    const uint32_t m_magic = 0xFFFFFFFFu / uint32_t(M) + 1u;                // i / M, exact for i < 2^16
     for (int i = tid; i < rpr * M; i += THREADS) {
-      const int rr = int(rank) * rpr + i / M, m = i - (i / M) * M;
+      const int iq = int(__umulhi(uint32_t(i), m_magic));
+      const int rr = int(rank) * rpr + iq, m = i - iq * M;
       if (row0 + rr >= N) continue;
       float sum = 0.0f;
       for (uint32_t q = 0; q < csize; ++q) sum += ld_cluster_f32(red + rr * 16 + m, q);

@@ -48,9 +48,14 @@ namespace tc {
 
 constexpr int BM = 128, BK = 64;          // one MMA covers 128 rows of X
 constexpr int B_BYTES = 256 * BK * 2;     // 32 KiB: 256 bf16 rows, or 128 hi rows + 128 lo rows
-constexpr int DEC_WARPS = 8;
-constexpr int DEC_THREADS = DEC_WARPS * 32;
-constexpr int THREADS = (2 + DEC_WARPS) * 32;
+// Decoder warps per CTA: 16 (two pieces or one per thread and K step) for the
+// formats exact in bf16; 8 for nvfp8 and int4 affine, whose hi + lo tiles were
+// measured faster with eight.
+template <int F> struct Dec {
+  static constexpr int WARPS = (F == INT4_AFFINE || F == NVFP8) ? 8 : 16;
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int CTA_THREADS = (2 + WARPS) * 32;
+};
 
 // MT 128-row sub-tiles of X share each decoded weight tile: MT = 2 halves the
 // decode work per FLOP (two accumulators, all 512 TMEM columns at BN = 256).
@@ -220,7 +225,9 @@ struct Params {
 };
 
 template <int F, int MT>
-__global__ void __launch_bounds__(THREADS, 1) qgemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
+__global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                          const Params p) {
+  constexpr int DEC_WARPS = Dec<F>::WARPS, DEC_THREADS = Dec<F>::THREADS, THREADS = Dec<F>::CTA_THREADS;
   using T = FmtTraits<F>;
   constexpr bool SPLIT = Tile<F>::split;
   constexpr int BN = Tile<F>::BN;
@@ -596,7 +603,7 @@ static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* s
   at[1].val.clusterDim.y = 1;
   at[1].val.clusterDim.z = unsigned(S);
   lc.gridDim = dim3((N + Tile<F>::BN - 1) / Tile<F>::BN, (M + BM * MT - 1) / (BM * MT), S);
-  lc.blockDim = dim3(THREADS);
+  lc.blockDim = dim3(Dec<F>::CTA_THREADS);
   lc.dynamicSmemBytes = Pipe<MT>::SMEM_BYTES;
   lc.stream = st;
   lc.attrs = at;

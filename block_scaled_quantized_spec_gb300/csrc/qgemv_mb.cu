@@ -61,6 +61,14 @@ __device__ __forceinline__ void mma_f16(float c[4], uint32_t a0, uint32_t a1, ui
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // 8 E2M1 codes -> f16x2 (c0,c1) (c2,c3) (c4,c5) (c6,c7).
 __device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t r[4]) {
   asm("{.reg .b8 b0, b1, b2, b3;\n\t"
@@ -290,6 +298,32 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       }
     }
     cp_async_wait_all();
+    if constexpr (I4) {
+      // int4 affine multiplies bf16 activations as given: only the pairing
+      // (x0,x4) (x1,x5) (x2,x6) (x3,x7) per 8 values, and float32 sums per 64
+      for (int j = 0; j < iters; ++j) {
+        const int i = tid + j * THREADS;
+        const bool live = i < tasks;                                        // whole 4-lane groups
+        const int m = live ? int(__umulhi(uint32_t(i), pm_magic)) : 0;
+        const int kk = live ? (i - m * per_m) * 16 : 0;
+        uint4* p16 = reinterpret_cast<uint4*>(xs + m * xst + kk);
+        const uint4 v0 = live ? p16[0] : make_uint4(0, 0, 0, 0);
+        const uint4 v1 = live ? p16[1] : make_uint4(0, 0, 0, 0);
+        float sm = 0.0f;
+        const uint32_t h[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) sm += bf16bits_f32(h[q] & 0xFFFFu) + bf16bits_f32(h[q] >> 16);
+        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
+        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 2);
+        if (live) {
+          p16[0] = make_uint4(prmt(v0.x, v0.z, 0x5410u), prmt(v0.x, v0.z, 0x7632u), prmt(v0.y, v0.w, 0x5410u),
+                              prmt(v0.y, v0.w, 0x7632u));
+          p16[1] = make_uint4(prmt(v1.x, v1.z, 0x5410u), prmt(v1.x, v1.z, 0x7632u), prmt(v1.y, v1.w, 0x5410u),
+                              prmt(v1.y, v1.w, 0x7632u));
+          if ((kk & 63) == 0) xsum[m * (KR >> 6) + (kk >> 6)] = sm;
+        }
+      }
+    } else {
     for (int j = 0; j < iters; ++j) {
       const int i = tid + j * THREADS;
       const bool live = i < tasks;                                          // whole 8-lane groups
@@ -317,29 +351,14 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
         f[2 * q + 1] = __fmul_rn(__uint_as_float(h[q] & 0xFFFF0000u), up);
       }
       uint32_t o[8];
-      if constexpr (I4) {   // per 8 values: (x0,x4) (x1,x5) (x2,x6) (x3,x7), the int4 pairing
-        #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          o[q] = pack_f16x2(f[q], f[q + 4]);
-          o[4 + q] = pack_f16x2(f[8 + q], f[12 + q]);
-        }
-      } else {
-        #pragma unroll
-        for (int q = 0; q < 8; ++q) o[q] = pack_f16x2(f[2 * q], f[2 * q + 1]);
-      }
+      #pragma unroll
+      for (int q = 0; q < 8; ++q) o[q] = pack_f16x2(f[2 * q], f[2 * q + 1]);
       if (live) {
         p16[0] = make_uint4(o[0], o[1], o[2], o[3]);
         p16[1] = make_uint4(o[4], o[5], o[6], o[7]);
       }
-      if constexpr (I4) {   // sums of the staged (rounded) values per 64
-        float sm = 0.0f;
-        #pragma unroll
-        for (int q = 0; q < 8; ++q) sm += f16x2_lo(o[q]) + f16x2_hi(o[q]);
-        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
-        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 2);
-        if (live && (kk & 63) == 0) xsum[m * (KR >> 6) + (kk >> 6)] = sm;
-      }
       if (live && (kk & (XSPAN - 1)) == 0) xsc[m * nsp + kk / XSPAN] = __uint_as_float(uint32_t(127 - sh) << 23);
+    }
     }
   }
   __syncthreads();
@@ -375,8 +394,8 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             if constexpr (I4) {
               #pragma unroll
               for (int b = 0; b < 4; ++b) {
-                fa[b] = ((wa[i][sg] >> (4 * b)) & 0x000F000Fu) | 0x64006400u;
-                fb[b] = ((wb[i][sg] >> (4 * b)) & 0x000F000Fu) | 0x64006400u;
+                fa[b] = ((wa[i][sg] >> (4 * b)) & 0x000F000Fu) | 0x43004300u;   // bf16 128 + q
+                fb[b] = ((wb[i][sg] >> (4 * b)) & 0x000F000Fu) | 0x43004300u;
               }
             } else {
               e2m1x8_f16(wa[i][sg], fa);
@@ -396,8 +415,13 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
               const uint4 xv = *reinterpret_cast<const uint4*>(xs + mrow[nb] * xst + kx);
-              mma_f16(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
-              mma_f16(d[nb], fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
+              if constexpr (I4) {   // bf16 activations as given, bf16 weights 128 + q (both exact)
+                mma_bf16(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+                mma_bf16(d[nb], fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
+              } else {
+                mma_f16(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+                mma_f16(d[nb], fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
+              }
             }
           } else {
             uint32_t fa[2], fb[2];
@@ -420,12 +444,12 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             } else if constexpr (F == NVFP8) {
               sa = __uint_as_float(sc[i][sg]);
               sb = __uint_as_float(sc[i][4 + sg]);
-            } else if constexpr (I4) {                                      // s * D + (b - 1024 s) * sum(x~)
+            } else if constexpr (I4) {                                      // s * D + (b - 128 s) * sum(x)
               const int h = sg >> 1;
               sa = bf16bits_f32(sc[i][h] & 0xFFFFu);
               sb = bf16bits_f32(sc[i][2 + h] & 0xFFFFu);
-              ba = __fmaf_rn(-1024.0f, sa, bf16bits_f32(sc[i][h] >> 16));
-              bb = __fmaf_rn(-1024.0f, sb, bf16bits_f32(sc[i][2 + h] >> 16));
+              ba = __fmaf_rn(-128.0f, sa, bf16bits_f32(sc[i][h] >> 16));
+              bb = __fmaf_rn(-128.0f, sb, bf16bits_f32(sc[i][2 + h] >> 16));
               const int blk = (c * CODES) / 64 + h;
               #pragma unroll
               for (int nb = 0; nb < NB; ++nb) {
@@ -457,6 +481,13 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
         const int span = (c * CODES) / XSPAN;
         #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
+          if constexpr (I4) {                                               // activations unscaled
+            acc[nb][0] += ac[nb][0];
+            acc[nb][1] += ac[nb][1];
+            acc[nb][2] += ac[nb][2];
+            acc[nb][3] += ac[nb][3];
+            continue;
+          }
           const float x0 = xsc[mc0[nb] * nsp + span], x1 = xsc[mc1[nb] * nsp + span];
           if constexpr (F == NVFP4) {                                       // micro-scales already applied
             acc[nb][0] = __fmaf_rn(x0, d[nb][0], acc[nb][0]);

@@ -69,6 +69,22 @@ __device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, u
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// As above with a zero accumulator input (the first MMA of a scale block).
+__device__ __forceinline__ void mma_f16_z(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+__device__ __forceinline__ void mma_bf16_z(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                           uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 // 8 E2M1 codes -> f16x2 (c0,c1) (c2,c3) (c4,c5) (c6,c7).
 __device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t r[4]) {
   asm("{.reg .b8 b0, b1, b2, b3;\n\t"
@@ -382,12 +398,12 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       const int c = r * P + i;
       if (c < nch) {                                                        // uniform over the CTA
         float ac[NB][4], d[NB][4];
-        #pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-          #pragma unroll
-          for (int e = 0; e < 4; ++e) ac[nb][e] = d[nb][e] = 0.0f;
+        constexpr bool per_seg = F == MXFP4 || F == NVFP8;                   // a block per segment
+        constexpr bool per_pair = F == MXFP8_E4M3 || F == MXFP8_E5M2 || I4;  // a block per two segments
         #pragma unroll
         for (int sg = 0; sg < 4; ++sg) {
+          // this segment starts a scale block: its first MMA takes a zero accumulator
+          const bool fresh = per_seg || (per_pair && (sg & 1) == 0) || sg == 0;
           const int kx = c * CODES + sg * SEG + WORD * t;                   // this lane's first staged k
           if constexpr (FOUR) {
             uint32_t fa[4], fb[4];
@@ -416,10 +432,12 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             for (int nb = 0; nb < NB; ++nb) {
               const uint4 xv = *reinterpret_cast<const uint4*>(xs + mrow[nb] * xst + kx);
               if constexpr (I4) {   // bf16 activations as given, bf16 weights 128 + q (both exact)
-                mma_bf16(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+                if (fresh) mma_bf16_z(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+                else mma_bf16(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
                 mma_bf16(d[nb], fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
               } else {
-                mma_f16(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+                if (fresh) mma_f16_z(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+                else mma_f16(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
                 mma_f16(d[nb], fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
               }
             }
@@ -430,13 +448,15 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
               const uint2 xv = *reinterpret_cast<const uint2*>(xs + mrow[nb] * xst + kx);
-              mma_f16(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+              if (fresh) mma_f16_z(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
+              else mma_f16(d[nb], fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
             }
           }
           // block scales on the float32 MMA results (d rows g: e = 0, 1; g + 8: e = 2, 3)
           constexpr bool per_seg = F == MXFP4 || F == NVFP8;                   // a block per segment
           constexpr bool per_pair = F == MXFP8_E4M3 || F == MXFP8_E5M2 || I4;  // a block per two segments
           if (per_seg || (per_pair && (sg & 1))) {
+            const bool first = sg < (per_seg ? 1 : 2);                      // the chunk's first block
             float sa, sb, ba = 0.0f, bb = 0.0f, xm0[NB], xm1[NB];
             if constexpr (F == MXFP4) {
               sa = e8m0_f32((sc[i][0] >> (8 * sg)) & 0xFFu);
@@ -463,17 +483,16 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
               if constexpr (I4) {
-                ac[nb][0] = __fmaf_rn(sa, d[nb][0], __fmaf_rn(ba, xm0[nb], ac[nb][0]));
-                ac[nb][1] = __fmaf_rn(sa, d[nb][1], __fmaf_rn(ba, xm1[nb], ac[nb][1]));
-                ac[nb][2] = __fmaf_rn(sb, d[nb][2], __fmaf_rn(bb, xm0[nb], ac[nb][2]));
-                ac[nb][3] = __fmaf_rn(sb, d[nb][3], __fmaf_rn(bb, xm1[nb], ac[nb][3]));
+                ac[nb][0] = __fmaf_rn(sa, d[nb][0], first ? ba * xm0[nb] : __fmaf_rn(ba, xm0[nb], ac[nb][0]));
+                ac[nb][1] = __fmaf_rn(sa, d[nb][1], first ? ba * xm1[nb] : __fmaf_rn(ba, xm1[nb], ac[nb][1]));
+                ac[nb][2] = __fmaf_rn(sb, d[nb][2], first ? bb * xm0[nb] : __fmaf_rn(bb, xm0[nb], ac[nb][2]));
+                ac[nb][3] = __fmaf_rn(sb, d[nb][3], first ? bb * xm1[nb] : __fmaf_rn(bb, xm1[nb], ac[nb][3]));
               } else {
-                ac[nb][0] = __fmaf_rn(sa, d[nb][0], ac[nb][0]);
-                ac[nb][1] = __fmaf_rn(sa, d[nb][1], ac[nb][1]);
-                ac[nb][2] = __fmaf_rn(sb, d[nb][2], ac[nb][2]);
-                ac[nb][3] = __fmaf_rn(sb, d[nb][3], ac[nb][3]);
+                ac[nb][0] = first ? sa * d[nb][0] : __fmaf_rn(sa, d[nb][0], ac[nb][0]);
+                ac[nb][1] = first ? sa * d[nb][1] : __fmaf_rn(sa, d[nb][1], ac[nb][1]);
+                ac[nb][2] = first ? sb * d[nb][2] : __fmaf_rn(sb, d[nb][2], ac[nb][2]);
+                ac[nb][3] = first ? sb * d[nb][3] : __fmaf_rn(sb, d[nb][3], ac[nb][3]);
               }
-              d[nb][0] = d[nb][1] = d[nb][2] = d[nb][3] = 0.0f;
             }
           }
         }

@@ -346,8 +346,8 @@ def run_reference(args):
 # kernel reports null until it is captured again).
 TRAFFIC = {
     "kernel_source": "block_scaled_quantized_spec_gb300/csrc/qgemv_m2.cu",
-    "sha256_16": "71a78efde73e59a6",
-    "bytes": 8940288,
+    "sha256_16": "851d7979253b1909",
+    "bytes": 8940032,
     "profile": "profiles/qgemv_m2_mxfp4_M1_N4096_K4096.md",
 }
 

@@ -16,14 +16,17 @@
 //  * warp 1: one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> float32 in
 //    TMEM, 128 x 256 x 16 per instruction) and commits each stage back to the
 //    producers through an mbarrier;
-//  * warps 2-9: decoders.  Each streams 16-byte pieces of codes (plus their
-//    block scales) from global memory with 128-bit loads one K step ahead,
+//  * warps 2 and up: decoders (16 warps; 8 for nvfp8 and int4 affine).  Each
+//    streams 16-byte pieces of codes (plus their block scales) from global
+//    memory with 128-bit loads three K steps ahead,
 //    decodes them in registers to bf16 with the block scale applied (exact for
 //    power-of-two and E4M3 scales; nvfp8 and int4-affine weights become
 //    float32 then a hi + lo bf16 pair, two MMAs per K slice) and writes the
 //    canonical 128B-swizzled K-major layout the MMA reads;
-//  * warps 2-5 (one per TMEM lane quadrant) then drain the accumulator with
-//    tcgen05.ld, apply the nvfp4 global scale and store bf16/float32 rows;
+//  * warps 2-5 (one per TMEM lane quadrant, per 128-row accumulator) then drain
+//    the accumulator with tcgen05.ld, apply the nvfp4 global scale and store
+//    bf16/float32 rows; a single 128-row tile may split K over a cluster, the
+//    partial tiles then summed through distributed shared memory;
 //  * the launch is programmatic-dependent: weight codes stream in while the
 //    preceding kernel finishes, X is read and `out` written only after
 //    griddepcontrol.wait.
@@ -366,8 +369,12 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
       const uint32_t bytes = uint32_t(T::four ? (kend - kbeg) / 2 : (kend - kbeg)) & ~15u;
       if (bytes) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
     }
+    // codes three K steps ahead in flight (cur, nxt, nx2 loaded; nx3 issued per step)
+    uint4 nx2[PIECES_PER_THREAD];
+    PieceScale ns2[PIECES_PER_THREAD];
     load(kb0, cur, cs);
     load(kb0 + 1, nxt, ns);
+    load(kb0 + 2, nx2, ns2);
     bool aborted = false;
     for (int j = 0; j < nloc; ++j) {
       const int kb = kb0 + j;
@@ -381,9 +388,9 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
         aborted = true;
         break;
       }
-      uint4 nx2[PIECES_PER_THREAD];
-      PieceScale ns2[PIECES_PER_THREAD];
-      load(kb + 2, nx2, ns2);                              // codes two K steps ahead in flight
+      uint4 nx3[PIECES_PER_THREAD];
+      PieceScale ns3[PIECES_PER_THREAD];
+      load(kb + 3, nx3, ns3);
       const uint32_t bs = stage_b(s);
       #pragma unroll
       for (int i = 0; i < PIECES_PER_THREAD; ++i) {
@@ -408,6 +415,8 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
         cs[i] = ns[i];
         nxt[i] = nx2[i];
         ns[i] = ns2[i];
+        nx2[i] = nx3[i];
+        ns2[i] = ns3[i];
       }
       fence_proxy_async();                                 // generic-proxy stores -> tensor core reads
       __syncwarp();

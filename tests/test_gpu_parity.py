@@ -324,3 +324,27 @@ def test_wide_gemv_four_warp_ctas(fmt, m):
     out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
     ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
     _check_qmm(out, ref, bound, (fmt, m))
+
+
+@pytest.mark.parametrize("fmt,m", [("mxfp4", 1), ("nvfp8", 2), ("nvfp4", 8), ("int4_affine", 16),
+                                   ("mxfp8_e4m3", 64), ("mxfp8_e5m2", 200)])
+def test_chained_layers_read_the_previous_output(fmt, m):
+    # Every kernel lets the next launch start early (programmatic dependent
+    # launch) and reads X only after waiting for the preceding kernel.  A chain
+    # of square layers, X(i+1) = out(i), launched back to back on one stream:
+    # each layer must match the oracle on the input it was actually given.
+    n = k = 512
+    layers = 6
+    packed = [_packed(fmt, n, k, seed=70 + i) for i in range(layers)]
+    dev = [(_dev(c), _dev(s), g) for c, s, g in packed]
+    xb, xt = _x(m, k, seed=80)
+    outs = [xt]
+    for i in range(layers):
+        dc, ds, g = dev[i]
+        outs.append(q.qmm(fmt, dc, ds, g, outs[-1], n))
+    torch.cuda.synchronize()
+    for i in range(layers):
+        xin = outs[i].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        c, s, g = packed[i]
+        ref, bound = oref.qmm_ref(fmt, c, s, g, xin, "bf16", m, n, k)
+        _check_qmm(outs[i + 1], ref, bound, (fmt, m, "layer", i))

@@ -1,4 +1,6 @@
-// Decode-phase dequantizing GEMV, 1 <= M <= 16:
+// Decode GEMV dispatch for 1 <= M <= 16, and the bulk-copy GEMV that serves
+// the shapes the two register-direct kernels do not plan for (activations of a
+// very long K that exceed their shared-memory slices):
 //   out[m, n] = sum_k x[m, k] * dequant(W)[n, k]
 // (metaltile PR #250 qgemv commits: output[row] = sum_k dequant(weight[row,k])
 // * input[k], and the multi-row qmm; rlx-cpu thunk/ops/quant.rs
@@ -6,14 +8,12 @@
 // folds each block scale into a per-block partial sum, and lowp_scaled_matmul,
 // which factors both operands' block scales out of each block's sum).
 //
-// The pages' Metal GEMVs give each row one threadgroup and reduce with scalar
-// code; they note it reads at a low fraction of bandwidth.  On GB300 the HBM
-// delivers about 46 four-bit codes per SM per clock, so everything per code
-// has to fit in a couple of issue slots.  The design:
+// Dispatch: M <= 2 -> qgemv_m2.cu; 3 <= M <= 16 -> qgemv_mb.cu; otherwise the
+// kernel below, which takes K in passes:
 //  * a CTA owns 16 (M <= 2) or 32 weight rows; one thread bulk-copies the
-//    CTA's code rows (up to 64 KiB per pass) into shared memory with
-//    cp.async.bulk on an mbarrier, rows padded by 16 bytes so that the reads
-//    below are bank-conflict free;
+//    CTA's code rows for a pass into shared memory with cp.async.bulk on an
+//    mbarrier, rows padded by 16 bytes so that the reads below are
+//    bank-conflict free;
 //  * the launch is programmatic-dependent: the weight copies and the staging
 //    of the block scales (float32, or f16 for nvfp4) run while the preceding
 //    kernel drains; the CTA waits for that kernel only before its activations;
@@ -22,7 +22,7 @@
 //  * element codes go to f16 with the hardware conversions (E2M1, E4M3, E5M2 ->
 //    f16x2 are exact; int4 becomes the exact f16 1024 + q), and the weights
 //    are the 16-row A operand of mma.sync m16n8k16 (f16 in, float32 out);
-//  * the activations are staged once per CTA in shared memory as f16 with a
+//  * the activations are staged once per pass in shared memory as f16 with a
 //    power-of-two scale per (row, 64-code unit) that puts the unit's largest
 //    |x| in [2^14, 2^15): exact for every bf16 value within 2^28 of that
 //    maximum;
@@ -30,7 +30,8 @@
 //    slice), except nvfp4 whose E4M3 micro-scale times the E2M1 value is exact
 //    in f16 and is applied before the MMA; the activation scale and the nvfp4
 //    global scale follow in float32;
-//  * per-warp partial tiles are summed through shared memory.
+//  * per-warp partial tiles are summed through shared memory; the mbarrier
+//    wait is bounded and records an expired wait in a device status word.
 #include <cuda_runtime.h>
 
 #include <atomic>

@@ -64,6 +64,15 @@ __device__ __forceinline__ float bf16bits_f32(uint32_t h) { return __uint_as_flo
 
 // ------------------------------------------------------------ bf16 pairs ---
 
+// Start [p, p + bytes) towards L2, trimmed to the whole 16-byte units inside
+// the range: the bulk prefetch takes 16-byte aligned addresses and sizes (code
+// rows always are; a row of block scales need not be).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint64_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uintptr_t s = (a + 15) & ~uintptr_t(15), e = (a + bytes) & ~uintptr_t(15);
+  if (e > s) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s), "r"(uint32_t(e - s)) : "memory");
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));

@@ -366,8 +366,7 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
     if (gridDim.y == 1 && dt < BN && n0 + dt < p.N && nloc > 0) {
       const int64_t kbeg = int64_t(kb0) * BK, kend = min(int64_t(kb1) * BK, int64_t(p.K));
       const uint8_t* src = p.codes + int64_t(n0 + dt) * row_bytes + (T::four ? kbeg / 2 : kbeg);
-      const uint32_t bytes = uint32_t(T::four ? (kend - kbeg) / 2 : (kend - kbeg)) & ~15u;
-      if (bytes) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+      prefetch_l2(src, uint64_t(T::four ? (kend - kbeg) / 2 : (kend - kbeg)));
     }
     // codes three K steps ahead in flight (cur, nxt, nx2 loaded; nx3 issued per step)
     uint4 nx2[PIECES_PER_THREAD];

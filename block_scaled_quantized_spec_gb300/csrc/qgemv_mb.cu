@@ -217,8 +217,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
   // This CTA's weight rows towards L2 now (rounds after the first read them there).
   if (tid < ROWS && row0 + tid < N && k1 > k0) {
     const uint8_t* p = codes + int64_t(row0 + tid) * rowbytes + (FOUR ? k0 / 2 : k0);
-    const uint32_t n = uint32_t(FOUR ? (k1 - k0) / 2 : (k1 - k0)) & ~15u;
-    if (n) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+    prefetch_l2(p, uint64_t(FOUR ? (k1 - k0) / 2 : (k1 - k0)));
   }
 
   uint32_t wa[P][4], wb[P][4];     // word t of the chunk's four segments, rows g and g + 8

@@ -166,11 +166,11 @@ __device__ __forceinline__ float ld_cluster_f32(const float* p, uint32_t rank) {
 }
 
 // Shared memory of one CTA: staged activations [M][xst] f16, their scales
-// [M][kr/128] (and int4-affine span sums [M][kr/64]), the partial tile [64][16].
+// [M][kr/128 + 1] (and int4-affine span sums [M][kr/64 + 1]), the partial tile [64][16].
 inline size_t smem_bytes(int F, int M, int kr) {
   const int rb = (F == MXFP4 || F == NVFP4 || F == INT4_AFFINE) ? 64 : 32;
-  return size_t(M) * xstride(kr, rb) * 2 + size_t(M) * (kr / XSPAN) * 4 +
-         (F == INT4_AFFINE ? size_t(M) * (kr / 64) * 4 : 0) + size_t(ROWS) * 16 * 4;
+  return size_t(M) * xstride(kr, rb) * 2 + size_t(M) * (kr / XSPAN + 1) * 4 +
+         (F == INT4_AFFINE ? size_t(M) * (kr / 64 + 1) * 4 : 0) + size_t(ROWS) * 16 * 4;
 }
 
 // Raw scale words a lane keeps per chunk: 2 (rows g, g + 8) for the byte
@@ -191,11 +191,14 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
   constexpr int P = chunks_in_flight<F>();
   extern __shared__ __align__(16) uint8_t smem[];
   const int xst = xstride(KR, read_bytes<F>());
-  const int nsp = KR / XSPAN;
+  // Row strides of the activation scales and span sums, one float longer than
+  // the row: the lanes of a quad read rows 2t and 2t + 1, which then fall in
+  // different banks.
+  const int nsp = KR / XSPAN + 1, nsm = KR / 64 + 1;
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                         // [M][xst] f16
   float* xsc = reinterpret_cast<float*>(xs + size_t(M) * xst);              // [M][nsp] 2^-shift
-  float* xsum = xsc + M * nsp;                                              // [M][KR/64] (int4 affine)
-  float* red = xsum + (I4 ? M * (KR / 64) : 0);                             // [ROWS][16] partial tile
+  float* xsum = xsc + M * nsp;                                              // [M][nsm] (int4 affine)
+  float* red = xsum + (I4 ? M * nsm : 0);                                   // [ROWS][16] partial tile
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -301,9 +304,14 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
     const int iters = (tasks + THREADS - 1) / THREADS;
     // i / per_m as a multiply-high: exact for i < 16 per_m < 2^32 / per_m
     const uint32_t pm_magic = 0xFFFFFFFFu / uint32_t(per_m) + 1u;
+    // Every row group reads the same activation lines: each CTA starts at its
+    // own place in the slice (a whole 128-value span, so the groups of 8
+    // lanes below stay aligned), spreading the requests over the L2 slices.
+    const int rot = 8 * int((blockIdx.x * 37u) % uint32_t(tasks / 8));
+    auto task = [&](int i) { return i + rot < tasks ? i + rot : i + rot - tasks; };
     for (int j = 0; j < iters; ++j) {
-      const int i = tid + j * THREADS;
-      if (i < tasks) {
+      const int i = task(tid + j * THREADS);
+      if (tid + j * THREADS < tasks) {
         const int m = int(__umulhi(uint32_t(i), pm_magic)), kk = (i - m * per_m) * 16;
         const bool ok = k0 + kk < k1;
         const uint16_t* src = ok ? x + int64_t(m) * K + k0 + kk : x;
@@ -317,8 +325,8 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       // int4 affine multiplies bf16 activations as given: only the pairing
       // (x0,x4) (x1,x5) (x2,x6) (x3,x7) per 8 values, and float32 sums per 64
       for (int j = 0; j < iters; ++j) {
-        const int i = tid + j * THREADS;
-        const bool live = i < tasks;                                        // whole 4-lane groups
+        const bool live = tid + j * THREADS < tasks;                        // whole 4-lane groups
+        const int i = task(tid + j * THREADS);
         const int m = live ? int(__umulhi(uint32_t(i), pm_magic)) : 0;
         const int kk = live ? (i - m * per_m) * 16 : 0;
         uint4* p16 = reinterpret_cast<uint4*>(xs + m * xst + kk);
@@ -335,13 +343,13 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
                               prmt(v0.y, v0.w, 0x7632u));
           p16[1] = make_uint4(prmt(v1.x, v1.z, 0x5410u), prmt(v1.x, v1.z, 0x7632u), prmt(v1.y, v1.w, 0x5410u),
                               prmt(v1.y, v1.w, 0x7632u));
-          if ((kk & 63) == 0) xsum[m * (KR >> 6) + (kk >> 6)] = sm;
+          if ((kk & 63) == 0) xsum[m * nsm + (kk >> 6)] = sm;
         }
       }
     } else {
     for (int j = 0; j < iters; ++j) {
-      const int i = tid + j * THREADS;
-      const bool live = i < tasks;                                          // whole 8-lane groups
+      const bool live = tid + j * THREADS < tasks;                          // whole 8-lane groups
+      const int i = task(tid + j * THREADS);
       const int m = live ? int(__umulhi(uint32_t(i), pm_magic)) : 0;
       const int kk = live ? (i - m * per_m) * 16 : 0;
       uint4* p16 = reinterpret_cast<uint4*>(xs + m * xst + kk);
@@ -472,8 +480,8 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
               const int blk = (c * CODES) / 64 + h;
               #pragma unroll
               for (int nb = 0; nb < NB; ++nb) {
-                xm0[nb] = xsum[mc0[nb] * (KR >> 6) + blk];
-                xm1[nb] = xsum[mc1[nb] * (KR >> 6) + blk];
+                xm0[nb] = xsum[mc0[nb] * nsm + blk];
+                xm1[nb] = xsum[mc1[nb] * nsm + blk];
               }
             } else {
               sa = e8m0_f32((sc[i][0] >> (8 * (sg >> 1))) & 0xFFu);

@@ -295,6 +295,7 @@ class OracleSample:
     def summary(self, times):
         t = statistics.median(times)
         return {"value": self.nbytes / t / 1e9, "unit": "GB/s", "cores": _blas_threads(), "kind": "oracle",
+                "host_cpus": os.cpu_count(), "cpu_model": _cpu_model(),
                 "sample": f"{len(times)} whole oracle calls {self.fmt} M={self.m} N={self.n} K={self.k} "
                           f"(median {t * 1e3:.1f} ms each; numpy decode single-threaded, float64 matmul on "
                           f"the BLAS threads)"}
@@ -303,6 +304,24 @@ class OracleSample:
 def cpu_baseline(fmt, m, n, k, budget_s=12.0):
     o = OracleSample(fmt, m, n, k)
     return o.summary(o.run(budget_s, min_calls=2))
+
+
+def _cpu_model():
+    """The host CPU's model string (x86 'model name'; on Arm the implementer/part codes)."""
+    import platform
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+        for key in ("model name", "Model"):
+            for line in info:
+                if line.split(":")[0].strip() == key:
+                    return line.split(":", 1)[1].strip()
+        imp = [ln.split(":", 1)[1].strip() for ln in info if ln.startswith("CPU implementer")]
+        part = [ln.split(":", 1)[1].strip() for ln in info if ln.startswith("CPU part")]
+        if imp and part:
+            return f"{platform.machine()} implementer {imp[0]} part {part[0]}"
+    except OSError:
+        pass
+    return platform.machine()
 
 
 def _blas_threads():
@@ -336,7 +355,7 @@ def run_reference(args):
             "data": "synthetic",
             "config": {"workload": "mxfp4 decode qGEMV M=1 N=4096 K=4096 (CPU oracle; a step = 3 whole calls)"},
             "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": v,
-                             "unit": "GB/s"},
+                             "unit": "GB/s", "host_cpus": cb["host_cpus"], "cpu_model": cb["cpu_model"]},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -555,7 +555,7 @@ static std::atomic<int> g_drop{0};
 
 template <int F, int MT>
 static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* scales, float glob, const void* x,
-                             void* out, bool out_f32, int M, int N, int K, cudaStream_t st, int sms) {
+                             void* out, bool out_f32, int M, int N, int K, cudaStream_t st, int S) {
   static std::atomic<int> attr_done[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -586,21 +586,9 @@ static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* s
   prm.out_f32 = out_f32 ? 1 : 0;
   prm.limit_ns = g_limit_ns.load();
   prm.drop_arrivals = g_drop.load();
-  // K split (one 128-row tile only, whose partial tile fits the stage memory):
-  // S splits of every tile form a cluster; S in 1..4 minimises the waves of
-  // one-CTA-per-SM work, ceil(tiles * S / SMs) / S, with no split left empty.
-  const int tiles = ((N + Tile<F>::BN - 1) / Tile<F>::BN) * ((M + BM * MT - 1) / (BM * MT));
+  // K split: the S splits of every tile form a cluster (MT = 1 only, whose
+  // float32 partial tile fits the drained stage memory)
   const int nkb = (K + BK - 1) / BK;
-  int S = 1;
-  if (MT == 1) {
-    double best = 1.0;
-    for (int s = 2; s <= 4; ++s) {
-      const int per = (nkb + s - 1) / s;
-      if ((s - 1) * per >= nkb) continue;
-      const double cost = double((tiles * s + sms - 1) / sms) / s;
-      if (cost < best - 1e-9) { best = cost; S = s; }
-    }
-  }
   prm.kb_per = (nkb + S - 1) / S;
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute at[2];
@@ -619,14 +607,45 @@ static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* s
   return cudaLaunchKernelEx(&lc, qgemm_tc_kernel<F, MT>, map, prm);
 }
 
-// 256-row tiles once M exceeds one 128-row tile.
+// Tile shape (MT 128-row accumulators per CTA) and K split S, by the estimated
+// time in K steps of one CTA: the decoders set the pace, so a K step costs
+// about the same with one accumulator or two (two measured ~10 % longer), times
+// the waves of one-CTA-per-SM work, plus ~8 K steps for a split's partial-tile
+// reduction.  No split may be left empty.
+struct GemmPlan {
+  int MT, S;
+};
+inline GemmPlan plan_gemm(int BN, int M, int N, int K, int sms) {
+  const int ntiles = (N + BN - 1) / BN;
+  const int nkb = (K + BK - 1) / BK;
+  GemmPlan best{1, 1};
+  double best_cost = 1e300;
+  for (int mt = 1; mt <= 2; ++mt) {
+    if (mt == 2 && M <= BM) continue;
+    const int64_t mtiles = (M + int64_t(BM) * mt - 1) / (int64_t(BM) * mt);
+    for (int s = 1; s <= (mt == 1 ? 4 : 1); ++s) {
+      const int per = (nkb + s - 1) / s;
+      if (s > 1 && (s - 1) * per >= nkb) continue;
+      const int64_t ctas = int64_t(ntiles) * mtiles * s;
+      const int64_t waves = (ctas + sms - 1) / sms;
+      const double cost = double(waves) * per * (mt == 2 ? 1.1 : 1.0) + (s > 1 ? 8.0 : 0.0);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = {mt, s};
+      }
+    }
+  }
+  return best;
+}
+
 template <int F>
 static cudaError_t launch_fmt(const void* codes, const void* scales, float glob, const void* x, void* out,
                               bool out_f32, int M, int N, int K, cudaStream_t st, int sms) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  if (M > BM) return launch_mt<F, 2>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st, sms);
-  return launch_mt<F, 1>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st, sms);
+  const GemmPlan pl = plan_gemm(Tile<F>::BN, M, N, K, sms > 0 ? sms : 1);
+  if (pl.MT == 2) return launch_mt<F, 2>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st, 1);
+  return launch_mt<F, 1>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st, pl.S);
 }
 
 }  // namespace tc

@@ -25,8 +25,9 @@
 //    canonical 128B-swizzled K-major layout the MMA reads;
 //  * warps 2-5 (one per TMEM lane quadrant, per 128-row accumulator) then drain
 //    the accumulator with tcgen05.ld, apply the nvfp4 global scale and store
-//    bf16/float32 rows; a single 128-row tile may split K over a cluster, the
-//    partial tiles then summed through distributed shared memory;
+//    bf16/float32 rows; 128-row tiles may split K over a cluster (when the
+//    tiles alone leave SMs idle), the partial tiles then summed through
+//    distributed shared memory;
 //  * the launch is programmatic-dependent: weight codes stream in while the
 //    preceding kernel finishes, X is read and `out` written only after
 //    griddepcontrol.wait.
@@ -361,8 +362,8 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
         sc[i] = load_piece_scale<F>(p.scales, n, nblk, k0, ok);
       }
     };
-    // a single 128-row tile: this CTA's weight slab [kb0, kb1) towards L2 now
-    // (one row per thread); with more M tiles the other tiles' CTAs share it
+    // one M tile: this CTA's weight slab [kb0, kb1) towards L2 now (one row
+    // per thread); with more M tiles the other tiles' CTAs share it
     if (gridDim.y == 1 && dt < BN && n0 + dt < p.N && nloc > 0) {
       const int64_t kbeg = int64_t(kb0) * BK, kend = min(int64_t(kb1) * BK, int64_t(p.K));
       const uint8_t* src = p.codes + int64_t(n0 + dt) * row_bytes + (T::four ? kbeg / 2 : kbeg);

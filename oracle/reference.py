@@ -24,6 +24,11 @@ Value definitions (page title, then the section):
 * qmm: "dequant-then-dot" -- PR #250 qgemv/qmm commits (the oracle the GPU
   kernels are checked against) and rlx-cpu ``lowp_scaled_matmul`` (a
   decode-and-accumulate reference kept for correctness, not speed).
+* qmm_gather: expert-routed rows over one stacked [E * N, K] weight, row m
+  against rows [e N, e N + N) with e = expert_idx[m] -- PR #250, the MoE
+  gather-qmm commit (weight row expert_ids[m] * out_dim + n, one stacked
+  packed tensor, one nvfp4 global), and rlx-cpu ``lowp_scaled_grouped_matmul``
+  (one row per token against its routed expert).
 """
 from __future__ import annotations
 
@@ -130,3 +135,24 @@ def qmm_ref_sampled(fmt, codes, scales, global_scale, x, x_dtype, m, n, k, rows,
     ref = np.einsum("ik,ik->i", xv, w)
     bound = BOUND_REL * np.einsum("ik,ik->i", np.abs(xv), np.abs(w)) + BOUND_ABS
     return ref, bound
+
+
+def qmm_gather_ref(fmt, codes, scales, global_scale, x, x_dtype, expert_idx, m, n, k, e):
+    """(ref, bound) for the expert-routed product, both [M, N] float64.
+
+    ``codes``/``scales`` hold the stacked [E * N, K] weight; ``expert_idx`` the
+    M expert numbers, each in [0, E) (anything else raises ValueError).
+    """
+    idx = np.asarray(expert_idx).reshape(m)
+    if m and (idx.min() < 0 or idx.max() >= e):
+        raise ValueError("expert index outside [0, E)")
+    w = dequant_exact(fmt, codes, scales, global_scale, e * n, k).reshape(e, n, k)
+    xv = x_values(x, x_dtype).reshape(m, k)
+    ref = np.empty((m, n))
+    bound = np.empty((m, n))
+    for i in range(m):
+        we = w[idx[i]]
+        ref[i] = we @ xv[i]
+        bound[i] = BOUND_REL * (np.abs(we) @ np.abs(xv[i])) + BOUND_ABS
+    return ref, bound
+

@@ -6,6 +6,8 @@
 * the int4-affine algebraic split (scale * sum q x + bias * sum x) that the
   metaltile qmm correctness test uses, on that test's deterministic pattern;
 * batch rows equal stacked single-row results;
+* the expert-routed product: exact rational brute force over a stacked
+  weight, E = 1 reduces to qmm, and relabelling the experts changes nothing;
 * planted mistakes (applied to the oracle on the CPU) are caught by these pins.
 """
 from fractions import Fraction
@@ -250,3 +252,80 @@ def test_planted_mistakes_are_caught(monkeypatch):
         mp.setattr(reference, "qmm_ref", transposed_ref)
         with pytest.raises(AssertionError):
             _check_brute("mxfp8_e4m3")
+
+
+# ----- expert-routed rows (MoE gather-qmm) -----
+
+def _gather_case(fmt, m, n, k, e, seed):
+    w = synth.weights(e * n, k, seed=seed, outliers=(fmt == "nvfp4"))
+    c, s, g = pack.pack(fmt, w)
+    x = synth.activations_bf16(m, k, seed=seed + 1)
+    idx = np.random.default_rng(seed + 2).integers(0, e, size=m).astype(np.int32)
+    return c, s, g, x, idx
+
+
+def _check_gather_brute(fmt):
+    # Row m against expert idx[m]'s N rows of the stack, summed exactly (the
+    # explicit decode loops above over the whole [E * N, K] stack).
+    m, n, k, e = 4, 3, 64, 3
+    c, s, g, x, idx = _gather_case(fmt, m, n, k, e, seed=21)
+    idx[:] = [2, 0, 2, 1]
+    ref, _ = reference.qmm_gather_ref(fmt, c, s, g, x, "bf16", idx, m, n, k, e)
+    x64 = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    exact = _brute_qmm(fmt, c, s, g, x64, m, e * n, k)        # every row against every stacked row
+    for i in range(m):
+        for j in range(n):
+            want = exact[i][idx[i] * n + j]
+            scale = sum(abs(Fraction(float(x64[i][kk]))) for kk in range(k)) + 1
+            assert abs(Fraction(ref[i, j]) - want) <= Fraction(1, 2 ** 40) * scale, (fmt, i, j)
+    return True
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gather_ref_matches_exact_rational_brute_force(fmt):
+    assert _check_gather_brute(fmt)
+
+
+def test_planted_gather_mistake_is_caught(monkeypatch):
+    """An expert-minor reading of the stack ([N, E, K] instead of [E, N, K])
+    must fail the brute-force pin."""
+    orig_exact = reference.dequant_exact
+
+    def expert_minor(fmt, codes, scales, g, rows, k):
+        w = orig_exact(fmt, codes, scales, g, rows, k)
+        e = 3                                            # the pin's expert count
+        return w.reshape(rows // e, e, k).transpose(1, 0, 2).reshape(rows, k)
+
+    with monkeypatch.context() as mp:
+        mp.setattr(reference, "dequant_exact", expert_minor)
+        with pytest.raises(AssertionError):
+            _check_gather_brute("mxfp4")
+
+
+def test_gather_ref_with_one_expert_is_qmm():
+    fmt, m, n, k = "mxfp4", 5, 24, 256
+    c, s, g, x, _ = _gather_case(fmt, m, n, k, 1, seed=22)
+    ref, bound = reference.qmm_gather_ref(fmt, c, s, g, x, "bf16", np.zeros(m, np.int32), m, n, k, 1)
+    r2, b2 = reference.qmm_ref(fmt, c, s, g, x, "bf16", m, n, k)
+    assert np.allclose(ref, r2, rtol=1e-13, atol=1e-13) and np.allclose(bound, b2, rtol=1e-13, atol=1e-13)
+
+
+def test_gather_ref_invariant_under_expert_relabelling():
+    # Permute the experts' slabs in the stack and remap the indices: same result.
+    fmt, m, n, k, e = "mxfp8_e5m2", 6, 8, 128, 4
+    c, s, g, x, idx = _gather_case(fmt, m, n, k, e, seed=23)
+    perm = np.array([2, 0, 3, 1])                  # new slab j holds old expert perm[j]
+    inv = np.argsort(perm)
+    c2 = np.asarray(c).reshape(e, n, -1)[perm].reshape(e * n, -1)
+    s2 = np.asarray(s).reshape(e, n, -1)[perm].reshape(e * n, -1)
+    r1, _ = reference.qmm_gather_ref(fmt, c, s, g, x, "bf16", idx, m, n, k, e)
+    r2, _ = reference.qmm_gather_ref(fmt, c2, s2, g, x, "bf16", inv[idx], m, n, k, e)
+    assert np.array_equal(r1, r2)
+
+
+def test_gather_ref_rejects_out_of_range_index():
+    fmt, m, n, k, e = "nvfp8", 2, 4, 64, 2
+    c, s, g, x, idx = _gather_case(fmt, m, n, k, e, seed=24)
+    with pytest.raises(ValueError):
+        reference.qmm_gather_ref(fmt, c, s, g, x, "bf16", np.array([0, 2], np.int32), m, n, k, e)
+

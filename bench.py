@@ -42,7 +42,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-breakdown", action="store_true")
-    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K")
+    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K or gather:fmt:M:N:K:E")
     return p.parse_args()
 
 
@@ -365,8 +365,8 @@ def run_reference(args):
 # kernel reports null until it is captured again).
 TRAFFIC = {
     "kernel_source": "block_scaled_quantized_spec_gb300/csrc/qgemv_m2.cu",
-    "sha256_16": "851d7979253b1909",
-    "bytes": 8940032,
+    "sha256_16": "486a4f593ff9632d",
+    "bytes": 8940288,
     "profile": "profiles/qgemv_m2_mxfp4_M1_N4096_K4096.md",
 }
 
@@ -401,6 +401,60 @@ BREAKDOWN = [
     ("nvfp8", 1, 11008, 4096), ("nvfp8", 16, 11008, 4096),
     ("nvfp8", 128, 11008, 4096), ("nvfp8", 4096, 11008, 4096),
 ]
+
+
+# Expert-routed rows (MoE gather-qmm): one token's top-8 routing over 8 experts
+# of [4096, 4096] mxfp4 weights, each row to a different expert.
+GATHER = [("mxfp4", 8, 4096, 4096, 8)]
+
+
+class GatherProblem:
+    """L copies of one stacked [E * N, K] expert weight, the routed rows and their outputs."""
+
+    def __init__(self, fmt, m, n, k, e, copies, seed=0):
+        import numpy as np
+        import torch
+        import block_scaled_quantized_spec_gb300 as q
+        from block_scaled_quantized_spec_gb300 import synth
+        self.fmt, self.m, self.n, self.k, self.e = fmt, m, n, k, e
+        rng = np.random.default_rng(seed)
+        c, s, g = q.qfmt_pack(fmt, synth.weights(e * n, k, rng=rng))
+        self.g = g
+        dc, ds = torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda()
+        self.codes = [dc] + [dc.clone() for _ in range(copies - 1)]
+        self.scales = [ds] + [ds.clone() for _ in range(copies - 1)]
+        xb = synth.activations_bf16(m, k, rng=rng)
+        self.x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+        self.idx = [torch.from_numpy(rng.permutation(e)[:m].astype(np.int32)).cuda() for _ in range(copies)]
+        self.out = [torch.empty((m, n), dtype=torch.bfloat16, device="cuda") for _ in range(copies)]
+        self.copies = copies
+        experts = len(set(int(v) for v in self.idx[0].cpu()))
+        self.bytes = experts * (sizes(fmt, 0, n, k) - (4 if fmt == "nvfp4" else 0)) + 2 * m * k + 2 * m * n + \
+            4 * m + (4 if fmt == "nvfp4" else 0)
+
+    def step(self):
+        import block_scaled_quantized_spec_gb300 as q
+        for i in range(self.copies):
+            q.qmm_gather(self.fmt, self.codes[i], self.scales[i], self.g, self.x, self.idx[i], self.n, self.e,
+                         out=self.out[i])
+
+    graph = Problem.graph
+
+
+def gather_row(fmt, m, n, k, e, hbm, steps=10, warmup=3):
+    import torch
+    per_call = sizes(fmt, 0, n, k) * min(m, e)
+    prob = GatherProblem(fmt, m, n, k, e, max(2, -(-3 * L2_BYTES // per_call)))
+    g = prob.graph()
+    ms, _ = time_graph(g, steps, warmup, 1)
+    per = ms / prob.copies
+    gbs = prob.bytes / (per * 1e-3) / 1e9
+    row = {"op": "qmm_gather", "fmt": fmt, "M": m, "N": n, "K": k, "E": e, "us": round(per * 1e3, 2),
+           "copies": prob.copies, "GB/s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
+           "bytes": prob.bytes}
+    del prob, g
+    torch.cuda.empty_cache()
+    return row
 
 
 def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3):
@@ -443,7 +497,12 @@ def main():
     nbytes = sizes(fmt, m, n, k)
     copies = copies_for(nbytes, m) if args.only is None else 4
     if args.only:
-        f, mm, nn, kk = args.only.split(":")
+        parts = args.only.split(":")
+        if parts[0] == "gather":          # gather:fmt:M:N:K:E
+            f, mm, nn, kk, ee = parts[1:]
+            print(json.dumps(gather_row(f, int(mm), int(nn), int(kk), int(ee), hbm, args.steps, args.warmup)))
+            return
+        f, mm, nn, kk = parts
         print(json.dumps(breakdown_row(f, int(mm), int(nn), int(kk), hbm, bf16, kind, args.steps,
                                        args.warmup)))
         return
@@ -476,6 +535,8 @@ def main():
         rows = []
         for (f, mm, nn, kk) in BREAKDOWN:
             rows.append(breakdown_row(f, mm, nn, kk, hbm, bf16, kind))
+        for (f, mm, nn, kk, ee) in GATHER:
+            rows.append(gather_row(f, mm, nn, kk, ee, hbm))
         line["breakdown"] = rows
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(fmt, m, n, k)

@@ -19,14 +19,14 @@ import numpy as np
 __all__ = [
     "FORMATS", "QfmtError", "load", "lib_path",
     "qfmt_block_size", "qfmt_codes_bytes", "qfmt_scales_bytes",
-    "qfmt_pack", "qfmt_dequant", "qmm", "qmm_ex", "qmm_workspace_bytes", "qfmt_last_error",
+    "qfmt_pack", "qfmt_dequant", "qmm", "qmm_ex", "qmm_workspace_bytes", "qmm_gather", "qfmt_last_error",
     "qfmt_version", "qfmt_device_status", "qfmt_debug_set",
 ]
 
 FORMATS = {"mxfp4": 1, "nvfp4": 2, "mxfp8_e4m3": 3, "mxfp8_e5m2": 4, "nvfp8": 5, "int4_affine": 6}
 F32, BF16 = 0, 1
 STATUS = {0: "QFMT_OK", -1: "QFMT_EINVAL", -2: "QFMT_ESHAPE", -3: "QFMT_EALIGN", -4: "QFMT_EUNSUPPORTED",
-          -5: "QFMT_ECUDA", -6: "QFMT_ETIMEOUT", -7: "QFMT_ENONFINITE", -8: "QFMT_ENOSPACE"}
+          -5: "QFMT_ECUDA", -6: "QFMT_ETIMEOUT", -7: "QFMT_ENONFINITE", -8: "QFMT_ENOSPACE", -9: "QFMT_EINDEX"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -60,6 +60,9 @@ _SIGS = {
                               ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                               ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "qmm_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]),
+    "qmm_gather": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                  ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]),
     "qfmt_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "qfmt_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_int64]),
 }
@@ -120,9 +123,9 @@ def qfmt_last_error() -> str:
 
 
 def qfmt_device_status(stream=None) -> int:
-    """Wait for the stream; return (and clear) the device status: 0 or QFMT_ETIMEOUT (-6)."""
+    """Wait for the stream; return (and clear) the device status: 0, QFMT_ETIMEOUT (-6) or QFMT_EINDEX (-9)."""
     st = load().qfmt_device_status(_stream(stream))
-    if st not in (0, -6):
+    if st not in (0, -6, -9):
         _check(st, "qfmt_device_status")
     return st
 
@@ -198,4 +201,21 @@ def qmm_ex(fmt, codes, scales, global_scale: float, x, N: int, out=None, out_dty
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().qmm_ex(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), xd, _ptr(out), od,
                          M, N, K, group, _ptr(workspace), ws_bytes, _stream(stream)), "qmm_ex")
+    return out
+
+
+def qmm_gather(fmt, codes, scales, global_scale: float, x, expert_idx, N: int, E: int, out=None, group: int = 0,
+               stream=None):
+    """out [M, N] bf16: row m = x[m] . dequant(W[expert_idx[m] * N : + N])^T over a stacked [E * N, K] weight.
+
+    ``expert_idx`` is a device int32 tensor [M].
+    """
+    import torch
+    M, K = x.shape
+    if expert_idx.dtype != torch.int32 or expert_idx.numel() != M:
+        raise QfmtError(-1, "qmm_gather", "expert_idx must be an int32 tensor of M entries")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(load().qmm_gather(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), _ptr(expert_idx),
+                             _ptr(out), M, N, K, E, group, _stream(stream)), "qmm_gather")
     return out

@@ -43,6 +43,13 @@ void set_wait_limit_ns(uint64_t ns);
 void set_drop_arrivals(int on);
 cudaError_t read_and_clear_device_status(unsigned int* status);
 cudaError_t read_and_clear_gemv_status(unsigned int* status);
+
+// Expert-routed decode GEMV: out[m, :] = x[m, :] . dequant(W[eidx[m] N .. + N))^T
+// for a stacked [E N, K] weight (one single-row GEMV per row m).
+cudaError_t launch_qgemv_gather(int fmt, const void* codes, const void* scales, float glob, const void* x,
+                                const int32_t* eidx, void* out, bool out_f32, int64_t M, int64_t N, int64_t K,
+                                int64_t E, cudaStream_t st);
+cudaError_t read_and_clear_gather_status(unsigned int* status);
 uint64_t wait_limit_ns();
 
 }  // namespace qfmt_dev

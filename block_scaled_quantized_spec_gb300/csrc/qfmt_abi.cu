@@ -109,6 +109,30 @@ int qmm(int fmt, const void* codes, const void* scales, float global_scale, cons
                 stream);
 }
 
+int qmm_gather(int fmt, const void* codes, const void* scales, float global_scale, const void* x,
+               const int32_t* expert_idx, void* out, int64_t M, int64_t N, int64_t K, int64_t E, int group,
+               void* stream) {
+  clear_error();
+  int st = check_group(fmt, group);
+  if (st) return st;
+  if ((st = check_shape(fmt, M, N, K))) return st;
+  if (E < 1) return fail(QFMT_EINVAL, "expert count E=%lld must be >= 1", (long long)E);
+  if (E * N > (int64_t(1) << 31)) return fail(QFMT_ESHAPE, "E*N above 2^31");
+  if (M > 65535) return fail(QFMT_ESHAPE, "M=%lld above 65535 rows", (long long)M);
+  if (M == 0 || N == 0) return QFMT_OK;
+  if ((st = check_ptr(out, 16, "out"))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return cuda_status(cudaMemsetAsync(out, 0, size_t(M) * size_t(N) * 2, s), "memset");
+  if ((st = check_common(fmt, codes, scales, global_scale, group))) return st;
+  if ((st = check_ptr(x, 16, "x"))) return st;
+  if ((st = check_ptr(expert_idx, 4, "expert_idx"))) return st;
+  if (!qfmt_dev::qgemv_m2_fits(fmt, 1, K))
+    return fail(QFMT_EUNSUPPORTED, "K=%lld too long for the expert-routed GEMV", (long long)K);
+  return cuda_status(qfmt_dev::launch_qgemv_gather(fmt, codes, scales, global_scale, x, expert_idx, out, false, M,
+                                                    N, K, E, s),
+                     "qmm_gather launch");
+}
+
 int qfmt_device_status(void* stream) {
   clear_error();
   int st = cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream sync");
@@ -116,8 +140,11 @@ int qfmt_device_status(void* stream) {
   unsigned int word = 0, gw = 0;
   if ((st = cuda_status(qfmt_dev::read_and_clear_device_status(&word), "device status"))) return st;
   if ((st = cuda_status(qfmt_dev::read_and_clear_gemv_status(&gw), "device status"))) return st;
+  unsigned int gx = 0;
+  if ((st = cuda_status(qfmt_dev::read_and_clear_gather_status(&gx), "device status"))) return st;
   if (word) return fail(QFMT_ETIMEOUT, "a tensor-core GEMM pipeline wait expired (status 0x%x)", word);
   if (gw) return fail(QFMT_ETIMEOUT, "a GEMV weight-copy wait expired (status 0x%x)", gw);
+  if (gx) return fail(QFMT_EINDEX, "qmm_gather: an expert index outside [0, E) (its output row was zeroed)");
   return QFMT_OK;
 }
 

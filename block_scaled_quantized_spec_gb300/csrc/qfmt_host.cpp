@@ -177,7 +177,7 @@ using namespace qfmt;
 
 extern "C" {
 
-int qfmt_version(void) { return 100; }
+int qfmt_version(void) { return 101; }
 
 const char* qfmt_last_error(void) { return qfmt::g_err; }
 

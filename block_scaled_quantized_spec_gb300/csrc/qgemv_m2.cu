@@ -168,11 +168,19 @@ struct ChunkScales {
   uint32_t a0, a1, b0, b1;
 };
 
-template <int F, int MR, bool UNI, int W>
+// Rows whose expert index lies outside [0, E) in an expert-routed launch.
+__device__ unsigned int g_gather_status;
+
+// GATHER: the expert-routed form (one activation row per blockIdx.y, M = 1):
+// the row's weights are rows [e N, e N + N) of the stacked matrix, e =
+// eidx[blockIdx.y], read once the preceding kernel has completed (it may be
+// the router that wrote them), so the weight requests wait for it too.
+template <int F, int MR, bool UNI, int W, bool GATHER = false>
 __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const uint8_t* __restrict__ codes,
                                                            const uint8_t* __restrict__ scales, float glob,
                                                            const uint16_t* __restrict__ x, void* __restrict__ out,
-                                                           int out_f32, int M, int N, int K) {
+                                                           int out_f32, int M, int N, int K,
+                                                           const int32_t* __restrict__ eidx, int E) {
   using S = Shape<F>;
   constexpr int P = chunks_per_warp<F, W>();
   constexpr int WARPS = W, THREADS = 32 * W;
@@ -192,6 +200,23 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int row0 = blockIdx.x * 16;
+  if constexpr (GATHER) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t m = blockIdx.y;
+    const int e = __ldg(eidx + m);
+    x += m * K;
+    out = static_cast<uint8_t*>(out) + m * N * (out_f32 ? 4 : 2);
+    if (e < 0 || e >= E) {                                                  // a zero row, and the status bit
+      if (tid < 16 && row0 + tid < N) {
+        if (out_f32) static_cast<float*>(out)[row0 + tid] = 0.0f;
+        else static_cast<__nv_bfloat16*>(out)[row0 + tid] = __float2bfloat16_rn(0.0f);
+      }
+      if (tid == 0) atomicOr(&g_gather_status, 1u);
+      return;
+    }
+    codes += int64_t(e) * N * (FmtTraits<F>::four ? K / 2 : K);
+    scales += int64_t(e) * N * (K / FmtTraits<F>::block) * FmtTraits<F>::sbytes;
+  }
   const int ra = row0 + g, rb = row0 + g + 8;
   const bool va = ra < N, vb = rb < N;
   const int64_t rowbytes = FOUR ? K / 2 : K;
@@ -517,16 +542,18 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   }
 }
 
-template <int F, int MR, bool UNI, int W = 8>
+template <int F, int MR, bool UNI, int W = 8, bool GATHER = false>
 static cudaError_t launch_mr(const void* codes, const void* scales, float glob, const void* x, void* out,
-                              bool out_f32, int M, int N, int K, cudaStream_t st) {
+                              bool out_f32, int M, int N, int K, cudaStream_t st, const int32_t* eidx = nullptr,
+                              int E = 0, int rows = 1) {
   static std::atomic<int> attr_done[64];
   const size_t sm = smem_bytes(F, M, K, W);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
-    e = cudaFuncSetAttribute(qgemv_m2_kernel<F, MR, UNI, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
+    e = cudaFuncSetAttribute(qgemv_m2_kernel<F, MR, UNI, W, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(SMEM_LIMIT));
     if (e != cudaSuccess) return e;
     attr_done[dev].store(1);
   }
@@ -534,15 +561,15 @@ static cudaError_t launch_mr(const void* codes, const void* scales, float glob, 
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.gridDim = dim3((N + 15) / 16);
+  lc.gridDim = dim3((N + 15) / 16, rows);
   lc.blockDim = dim3(32 * W);
   lc.dynamicSmemBytes = sm;
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F, MR, UNI, W>, static_cast<const uint8_t*>(codes),
+  return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F, MR, UNI, W, GATHER>, static_cast<const uint8_t*>(codes),
                             static_cast<const uint8_t*>(scales), glob, static_cast<const uint16_t*>(x), out,
-                            int(out_f32), M, N, K);
+                            int(out_f32), M, N, K, eidx, E);
 }
 
 // 8-warp CTAs (two per SM); E2M1 formats whose grid exceeds two CTAs per SM
@@ -571,6 +598,18 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, float glob,
              : launch_mr<F, 2, false>(codes, scales, glob, x, out, out_f32, M, N, K, st);
 }
 
+// Expert-routed rows: one single-row GEMV per activation row (blockIdx.y).
+template <int F>
+static cudaError_t launch_gather_fmt(const void* codes, const void* scales, float glob, const void* x,
+                                     const int32_t* eidx, void* out, bool out_f32, int M, int N, int K, int E,
+                                     cudaStream_t st) {
+  constexpr int CODES = Shape<F>::CODES;
+  const int nchunk = (K + CODES - 1) / CODES;
+  const bool uni = K % (WARPS * CODES) == 0 && (nchunk / WARPS) % chunks_in_flight<F>() == 0;
+  return uni ? launch_mr<F, 1, true, 8, true>(codes, scales, glob, x, out, out_f32, 1, N, K, st, eidx, E, M)
+             : launch_mr<F, 1, false, 8, true>(codes, scales, glob, x, out, out_f32, 1, N, K, st, eidx, E, M);
+}
+
 }  // namespace gemv_m2
 
 bool qgemv_m2_fits(int fmt, int64_t M, int64_t K) {
@@ -588,6 +627,30 @@ cudaError_t launch_qgemv_m2(int fmt, const void* codes, const void* scales, floa
     case NVFP8: return gemv_m2::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_m2::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
+}
+
+cudaError_t launch_qgemv_gather(int fmt, const void* codes, const void* scales, float glob, const void* x,
+                                const int32_t* eidx, void* out, bool out_f32, int64_t M, int64_t N, int64_t K,
+                                int64_t E, cudaStream_t st) {
+  const int m = int(M), n = int(N), k = int(K), e = int(E);
+  switch (fmt) {
+    case MXFP4: return gemv_m2::launch_gather_fmt<MXFP4>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    case NVFP4: return gemv_m2::launch_gather_fmt<NVFP4>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    case MXFP8_E4M3:
+      return gemv_m2::launch_gather_fmt<MXFP8_E4M3>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    case MXFP8_E5M2:
+      return gemv_m2::launch_gather_fmt<MXFP8_E5M2>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    case NVFP8: return gemv_m2::launch_gather_fmt<NVFP8>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    default:
+      return gemv_m2::launch_gather_fmt<INT4_AFFINE>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+  }
+}
+
+cudaError_t read_and_clear_gather_status(unsigned int* status) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, gemv_m2::g_gather_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(gemv_m2::g_gather_status, &zero, sizeof(unsigned int));
 }
 
 }  // namespace qfmt_dev

@@ -76,7 +76,8 @@ typedef enum {
   QFMT_ECUDA = -5,         /* a CUDA launch or device query failed */
   QFMT_ETIMEOUT = -6,      /* a kernel's bounded pipeline wait expired (see qfmt_device_status) */
   QFMT_ENONFINITE = -7,    /* qfmt_pack: NaN/Inf weight, or a block scale overflowing float32 */
-  QFMT_ENOSPACE = -8       /* a caller workspace smaller than qmm_workspace_bytes() */
+  QFMT_ENOSPACE = -8,      /* a caller workspace smaller than qmm_workspace_bytes() */
+  QFMT_EINDEX = -9         /* qmm_gather met an expert index outside [0, E) (see qfmt_device_status) */
 } qfmt_status;
 
 /* Block (group) size of a format along K: 32, 16, 32, 32, 16, 64; 0 for an
@@ -147,12 +148,36 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale,
 size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
 
 /*
+ * qmm_gather -- device, expert-routed rows (mixture of experts):
+ *   out[m, n] (bf16) = sum_k X[m, k] (bf16) . dequant(W)[expert_idx[m] * N + n, k]
+ * where the E experts' [N, K] weights are stacked row-wise into one packed
+ * matrix W [E*N, K] (codes and scales laid out as for qmm with E*N rows; one
+ * nvfp4 global scale for all experts).  (metaltile PR #250, the MoE
+ * gather-qmm commit: the qmm with one indirection, weight row
+ * expert_ids[m] * out_dim + n over one stacked packed tensor; rlx-cpu
+ * thunk/ops/quant.rs lowp_scaled_grouped_matmul: one row per token against
+ * its routed expert.)
+ * expert_idx: device int32 [M], 4-byte aligned.  It is read only after every
+ * preceding kernel in the stream has completed (it may be the router's
+ * output), so this call's weight reads wait for that kernel too.  Each row
+ * runs as its own decode GEMV: rows that share an expert are not grouped, so
+ * the call suits decode batches.  Bounds: 1 <= E, E*N <= 2^31, M <= 65535, K
+ * within the single-row GEMV's shared-memory plan (QFMT_EUNSUPPORTED
+ * beyond).  An index outside [0, E) makes that row's output zero and is
+ * reported by the next qfmt_device_status (QFMT_EINDEX).  Tolerance as qmm.
+ */
+int qmm_gather(int fmt, const void* codes, const void* scales, float global_scale,
+               const void* x, const int32_t* expert_idx, void* out,
+               int64_t M, int64_t N, int64_t K, int64_t E, int group, void* stream);
+
+/*
  * qfmt_device_status -- waits for `stream`, then reads and clears the
  * library's device status word for the current device.  Every pipeline wait
  * inside the tensor-core GEMM is bounded in time; when one expires the kernel
  * records it there, drains its in-flight copies and MMAs, frees its tensor
  * memory and exits without writing its output tile.  Returns QFMT_OK, or
- * QFMT_ETIMEOUT if any such kernel since the last call gave up, or QFMT_ECUDA.
+ * QFMT_ETIMEOUT if any such kernel since the last call gave up, QFMT_EINDEX
+ * if a qmm_gather row met an expert index outside [0, E), or QFMT_ECUDA.
  */
 int qfmt_device_status(void* stream);
 

@@ -160,3 +160,26 @@ def test_device_entry_validation_without_gpu(lib):
     assert lib.qfmt_dequant(1, 0x1000, 0x1000, 1.0, 0x1000, 3, 4, 64, 0, None) == -1
     assert lib.qfmt_dequant(1, 0x1000, 0x1000, 1.0, 0x1004, 0, 4, 64, 0, None) == -3
     assert lib.qmm_workspace_bytes(1, 16, 16, 64) == 0
+
+
+def _call_gather(lib, **kw):
+    a = dict(fmt=1, codes=0x1000, scales=0x1000, g=1.0, x=0x1000, idx=0x2000, out=0x1000,
+             M=4, N=4, K=64, E=2, group=0)
+    a.update(kw)
+    return lib.qmm_gather(a["fmt"], a["codes"], a["scales"], a["g"], a["x"], a["idx"], a["out"],
+                          a["M"], a["N"], a["K"], a["E"], a["group"], None)
+
+
+def test_gather_entry_validation_without_gpu(lib):
+    # each fails in host-side validation, before any CUDA call
+    assert _call_gather(lib, E=0) == -1
+    assert _call_gather(lib, M=70000) == -2
+    assert _call_gather(lib, E=1 << 20, N=1 << 12) == -2          # E * N above 2^31
+    assert _call_gather(lib, K=48) == -2
+    assert _call_gather(lib, idx=None) == -1
+    assert _call_gather(lib, idx=0x2002) == -3
+    assert _call_gather(lib, x=0x1004) == -3
+    assert _call_gather(lib, fmt=2, g=0.0) == -1
+    assert _call_gather(lib, group=32, fmt=6) == -4
+    assert b"expert" in lib.qfmt_last_error() or _call_gather(lib, E=0) == -1
+    assert _call_gather(lib, M=0) == 0 and _call_gather(lib, N=0) == 0

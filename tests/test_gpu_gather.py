@@ -1,0 +1,116 @@
+"""GPU parity of the expert-routed product (MoE gather-qmm) against the oracle.
+
+Row m of the output is x[m] against rows [e N, e N + N) of one stacked
+[E * N, K] packed weight, e = expert_idx[m] (metaltile PR #250, the MoE
+gather-qmm commit).  Tolerance as qmm: |out - ref| <= 2e-3 sum_k |x||w| + 1e-6
+plus half an ulp of the bf16 output.  Inputs: weights packed by the oracle's
+packer, activations and expert numbers from seeded generators.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import block_scaled_quantized_spec_gb300 as q  # noqa: E402
+from block_scaled_quantized_spec_gb300 import synth  # noqa: E402
+from oracle import pack as opack  # noqa: E402
+from oracle import reference as oref  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+FMTS = list(q.FORMATS)
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_scaled_quantized_spec_gb300 import build
+    build.build()
+    q.load()
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _case(fmt, m, n, k, e, seed):
+    w = synth.weights(e * n, k, seed=seed, outliers=(fmt == "nvfp4"))
+    c, s, g = opack.pack(fmt, w)
+    xb = synth.activations_bf16(m, k, seed=seed + 1)
+    xt = _dev(xb.view(np.int16)).view(torch.bfloat16)
+    idx = np.random.default_rng(seed + 2).integers(0, e, size=m).astype(np.int32)
+    return c, s, g, xb, xt, idx
+
+
+def _check(out_t, ref, bound, what):
+    out = out_t.float().cpu().numpy().astype(np.float64)
+    err = np.abs(out - ref)
+    ok = err <= bound + np.abs(out) * 2.0 ** -9
+    assert np.isfinite(out).all(), what
+    assert ok.all(), (what, float((err / bound).max()), np.argwhere(~ok)[:5].tolist())
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("m", [1, 5, 9])
+def test_gather_parity(fmt, m):
+    n, k, e = 200, 1024, 3                 # ragged row tiles, several chunks per warp
+    c, s, g, xb, xt, idx = _case(fmt, m, n, k, e, seed=30 + m)
+    idx[0] = e - 1                         # the last slab is reached
+    out = q.qmm_gather(fmt, _dev(c), _dev(s), g, xt, _dev(idx), n, e)
+    ref, bound = oref.qmm_gather_ref(fmt, c, s, g, xb, "bf16", idx, m, n, k, e)
+    _check(out, ref, bound, (fmt, m))
+    assert q.qfmt_device_status() == 0
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "int4_affine", "mxfp8_e5m2"])
+def test_gather_wider_shape_and_repeated_experts(fmt):
+    # eight rows over four experts (each twice), N = 1024, K = 2048
+    m, n, k, e = 8, 1024, 2048, 4
+    c, s, g, xb, xt, idx = _case(fmt, m, n, k, e, seed=40)
+    idx[:] = [3, 1, 0, 2, 1, 3, 0, 2]
+    out = q.qmm_gather(fmt, _dev(c), _dev(s), g, xt, _dev(idx), n, e)
+    ref, bound = oref.qmm_gather_ref(fmt, c, s, g, xb, "bf16", idx, m, n, k, e)
+    _check(out, ref, bound, fmt)
+
+
+def test_gather_one_expert_equals_qmm():
+    fmt, m, n, k = "nvfp8", 4, 96, 512
+    c, s, g, xb, xt, _ = _case(fmt, m, n, k, 1, seed=41)
+    idx = _dev(np.zeros(m, np.int32))
+    a = q.qmm_gather(fmt, _dev(c), _dev(s), g, xt, idx, n, 1)
+    b = torch.cat([q.qmm(fmt, _dev(c), _dev(s), g, xt[i:i + 1], n) for i in range(m)])
+    assert torch.equal(a, b)               # the same single-row GEMV on the same weights
+
+
+def test_gather_out_of_range_index_zeroes_the_row():
+    fmt, m, n, k, e = "mxfp8_e4m3", 4, 64, 256, 2
+    c, s, g, xb, xt, idx = _case(fmt, m, n, k, e, seed=42)
+    bad = idx.copy()
+    bad[1], bad[3] = 2, -1
+    q.qfmt_device_status()                 # start clean
+    out = q.qmm_gather(fmt, _dev(c), _dev(s), g, xt, _dev(bad), n, e)
+    assert q.qfmt_device_status() == -9    # QFMT_EINDEX, then cleared
+    assert q.qfmt_device_status() == 0
+    o = out.float().cpu().numpy()
+    assert (o[1] == 0).all() and (o[3] == 0).all()
+    good = [0, 2]
+    ref, bound = oref.qmm_gather_ref(fmt, c, s, g, xb[good], "bf16", bad[good], 2, n, k, e)
+    _check(out[good], ref, bound, "good rows")
+
+
+def test_gather_reads_indices_written_by_the_preceding_kernel():
+    # The router's output (here a device op enqueued right before) must be
+    # read only after it completes: the call waits on the preceding kernel.
+    fmt, m, n, k, e = "mxfp4", 6, 512, 4096, 5
+    c, s, g, xb, xt, _ = _case(fmt, m, n, k, e, seed=43)
+    dc, ds = _dev(c), _dev(s)
+    idx_t = torch.full((m,), 0, dtype=torch.int32, device=DEV)
+    outs = []
+    for r in range(4):
+        seq = torch.arange(m, device=DEV, dtype=torch.int32)
+        idx_t.copy_((seq * 3 + r) % e)     # written on the stream just before the call
+        outs.append((q.qmm_gather(fmt, dc, ds, g, xt, idx_t, n, e), ((np.arange(m) * 3 + r) % e).astype(np.int32)))
+    for out, want_idx in outs:
+        ref, bound = oref.qmm_gather_ref(fmt, c, s, g, xb, "bf16", want_idx, m, n, k, e)
+        _check(out, ref, bound, "chained")

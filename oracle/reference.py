@@ -24,6 +24,12 @@ Value definitions (page title, then the section):
 * qmm: "dequant-then-dot" -- PR #250 qgemv/qmm commits (the oracle the GPU
   kernels are checked against) and rlx-cpu ``lowp_scaled_matmul`` (a
   decode-and-accumulate reference kept for correctness, not speed).
+* qmm_batched: up to four products sharing one activation, each the qmm
+  value -- PR #250, the batched Q/K/V and batched-4 GEMV commits.
+* qmm_rmsnorm: the qmm value of the RMS-normalised activation x * gamma /
+  sqrt(mean(x^2) + eps) -- PR #250, the fused RMSNorm + GEMV commit (phase 1
+  the sum of squares and its inverse root, phase 2 the GEMV over
+  x * norm_weight * inv_rms).
 * qmm_gather: expert-routed rows over one stacked [E * N, K] weight, row m
   against rows [e N, e N + N) with e = expert_idx[m] -- PR #250, the MoE
   gather-qmm commit (weight row expert_ids[m] * out_dim + n, one stacked
@@ -154,5 +160,27 @@ def qmm_gather_ref(fmt, codes, scales, global_scale, x, x_dtype, expert_idx, m, 
         we = w[idx[i]]
         ref[i] = we @ xv[i]
         bound[i] = BOUND_REL * (np.abs(we) @ np.abs(xv[i])) + BOUND_ABS
+    return ref, bound
+
+
+def qmm_batched_ref(fmt, mats, x, x_dtype, m, k):
+    """[(ref, bound)] of each matrix in ``mats`` = [(codes, scales, global_scale, n), ...] against x."""
+    return [qmm_ref(fmt, c, s, g, x, x_dtype, m, n, k) for (c, s, g, n) in mats]
+
+
+def rmsnorm_values(x, x_dtype, gamma_bits, eps, m, k):
+    """x * gamma / sqrt(mean_k x^2 + eps), float64 [M, K]; gamma as bf16 bit patterns [K]."""
+    xv = x_values(x, x_dtype).reshape(m, k)
+    g = codec.decode_bf16(np.asarray(gamma_bits, dtype=np.uint16)).reshape(k)
+    inv = 1.0 / np.sqrt(np.mean(xv * xv, axis=1) + eps)
+    return xv * g[None, :] * inv[:, None]
+
+
+def qmm_rmsnorm_ref(fmt, codes, scales, global_scale, x, x_dtype, gamma_bits, eps, m, n, k):
+    """(ref, bound) for out = rmsnorm(x) . dequant(W)^T, bound on the normalised activation."""
+    w = dequant_exact(fmt, codes, scales, global_scale, n, k)
+    xt = rmsnorm_values(x, x_dtype, gamma_bits, eps, m, k)
+    ref = xt @ w.T
+    bound = BOUND_REL * (np.abs(xt) @ np.abs(w).T) + BOUND_ABS
     return ref, bound
 

@@ -8,6 +8,10 @@
 * batch rows equal stacked single-row results;
 * the expert-routed product: exact rational brute force over a stacked
   weight, E = 1 reduces to qmm, and relabelling the experts changes nothing;
+* the batched products: exact rational brute force per matrix;
+* the RMSNorm-fused product: 60-digit decimal brute force, the closed form of
+  a constant row, and invariance of the normalisation under power-of-two
+  scaling of x (eps = 0);
 * planted mistakes (applied to the oracle on the CPU) are caught by these pins.
 """
 from fractions import Fraction
@@ -329,3 +333,94 @@ def test_gather_ref_rejects_out_of_range_index():
     with pytest.raises(ValueError):
         reference.qmm_gather_ref(fmt, c, s, g, x, "bf16", np.array([0, 2], np.int32), m, n, k, e)
 
+
+# ----- batched products and the RMSNorm-fused product -----
+
+def test_batched_ref_matches_exact_rational_brute_force():
+    fmt, m, k = "nvfp4", 2, 64
+    mats, brute = [], []
+    x = synth.activations_bf16(m, k, seed=51)
+    x64 = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for i, n in enumerate((3, 5)):
+        w = synth.weights(n, k, seed=52 + i, outliers=True)
+        c, s_, g = pack.pack(fmt, w)
+        mats.append((c, s_, g, n))
+        brute.append(_brute_qmm(fmt, c, s_, g, x64, m, n, k))
+    refs = reference.qmm_batched_ref(fmt, mats, x, "bf16", m, k)
+    assert len(refs) == 2
+    for (ref, _), exact, (_, _, _, n) in zip(refs, brute, mats):
+        for i in range(m):
+            for j in range(n):
+                scale = sum(abs(Fraction(float(x64[i][kk]))) for kk in range(k)) + 1
+                assert abs(Fraction(ref[i, j]) - exact[i][j]) <= Fraction(1, 2 ** 40) * scale
+
+
+def _gamma_bits(k, seed):
+    g = 1.0 + 0.25 * np.random.default_rng(seed).standard_normal(k)
+    return (torch.from_numpy(g.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()).view(np.uint16)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "int4_affine", "nvfp8"])
+def test_rmsnorm_ref_matches_decimal_brute_force(fmt):
+    from decimal import Decimal, getcontext
+    getcontext().prec = 60
+    m, n, k, eps = 2, 3, 64, 1e-5
+    c, s_, g, x = _tiny_case(fmt, m, n, k, seed=55)
+    gb = _gamma_bits(k, 56)
+    ref, _ = reference.qmm_rmsnorm_ref(fmt, c, s_, g, x, "bf16", gb, eps, m, n, k)
+    x64 = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    g64 = (gb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    codes = [[int(v) for v in r] for r in np.asarray(c).reshape(n, -1)]
+    scales = [[int(v) for v in r] for r in np.asarray(s_).reshape(n, -1)]
+    blk = pack.BLOCK[fmt]
+    D = lambda fr: Decimal(fr.numerator) / Decimal(fr.denominator)  # noqa: E731
+    for i in range(m):
+        ms = sum(Decimal(float(v)) ** 2 for v in x64[i]) / k + Decimal(eps)
+        inv = 1 / ms.sqrt()
+        for j in range(n):
+            acc = Decimal(0)
+            for kk in range(k):
+                byte = codes[j][kk // 2] if fmt in ("mxfp4", "nvfp4", "int4_affine") else codes[j][kk]
+                cc = (byte >> (4 * (kk % 2))) & 0xF if fmt in ("mxfp4", "nvfp4", "int4_affine") else byte
+                mul, add = _lib_scale(fmt, scales, j, kk // blk)
+                w = _lib_elem(fmt, cc) * mul + add
+                acc += Decimal(float(x64[i][kk])) * Decimal(float(g64[kk])) * inv * D(w)
+            assert abs(Decimal(float(ref[i, j])) - acc) <= Decimal(2) ** -40 * (abs(acc) + 1), (fmt, i, j)
+
+
+def test_rmsnorm_ref_constant_row_closed_form():
+    # x[m, :] = c, gamma = 1: every normalised value is c / sqrt(c^2 + eps).
+    fmt, n, k, eps = "mxfp8_e4m3", 6, 128, 0.01
+    c_, s_, g, _ = _tiny_case(fmt, 1, n, k, seed=57)
+    c = 0.75                                              # exact in bf16
+    x = np.full((1, k), np.float32(c)).view(np.uint32) >> 16
+    ones = np.full(k, 0x3F80, np.uint16)
+    ref, _ = reference.qmm_rmsnorm_ref(fmt, c_, s_, g, x.astype(np.uint16), "bf16", ones, eps, 1, n, k)
+    w = reference.dequant_exact(fmt, c_, s_, g, n, k)
+    want = (c / np.sqrt(c * c + eps)) * w.sum(axis=1)
+    assert np.allclose(ref[0], want, rtol=1e-13, atol=1e-15)
+
+
+def test_rmsnorm_values_invariant_under_power_of_two_scaling():
+    m, k = 3, 256
+    x = synth.activations_bf16(m, k, seed=58)
+    gb = _gamma_bits(k, 59)
+    a = reference.rmsnorm_values(x, "bf16", gb, 0.0, m, k)
+    x4 = ((x.astype(np.uint32) + (2 << 7)) & 0xFFFF).astype(np.uint16)   # exponent + 2: x * 4 (no zeros here)
+    assert (x & 0x7F80).min() > 0 and (x & 0x7F80).max() < 0x7E00
+    b = reference.rmsnorm_values(x4, "bf16", gb, 0.0, m, k)
+    assert np.array_equal(a, b)
+
+
+
+def test_planted_rmsnorm_mistake_is_caught(monkeypatch):
+    """A normalisation by the root of the sum (not the mean) of squares must fail the decimal pin."""
+    def sum_not_mean(x, x_dtype, gamma_bits, eps, m, k):
+        xv = reference.x_values(x, x_dtype).reshape(m, k)
+        g = reference.codec.decode_bf16(np.asarray(gamma_bits, dtype=np.uint16)).reshape(k)
+        return xv * g[None, :] / np.sqrt(np.sum(xv * xv, axis=1) + eps)[:, None]
+
+    with monkeypatch.context() as mp:
+        mp.setattr(reference, "rmsnorm_values", sum_not_mean)
+        with pytest.raises(AssertionError):
+            test_rmsnorm_ref_matches_decimal_brute_force("mxfp4")

@@ -42,7 +42,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-breakdown", action="store_true")
-    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K or gather:fmt:M:N:K:E")
+    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K, gather:fmt:M:N:K:E, batched:fmt:M:N1,N2:K or rmsnorm:fmt:M:N:K")
     return p.parse_args()
 
 
@@ -365,8 +365,8 @@ def run_reference(args):
 # kernel reports null until it is captured again).
 TRAFFIC = {
     "kernel_source": "block_scaled_quantized_spec_gb300/csrc/qgemv_m2.cu",
-    "sha256_16": "486a4f593ff9632d",
-    "bytes": 8940288,
+    "sha256_16": "d335d6e7c41ff0dc",
+    "bytes": 8939776,
     "profile": "profiles/qgemv_m2_mxfp4_M1_N4096_K4096.md",
 }
 
@@ -441,6 +441,68 @@ class GatherProblem:
     graph = Problem.graph
 
 
+# Fused decode forms: the Q/K/V projections of a grouped-query layer in one
+# launch, and RMSNorm in front of one mxfp4 [4096, 4096] GEMV.
+FUSED = [("batched", "mxfp4", 1, (4096, 1024, 1024), 4096), ("rmsnorm", "mxfp4", 1, (4096,), 4096)]
+
+
+class FusedProblem:
+    """L copies of the weights of one fused call (1..4 matrices), their activations and outputs."""
+
+    def __init__(self, kind, fmt, m, ns, k, copies, seed=0):
+        import numpy as np
+        import torch
+        import block_scaled_quantized_spec_gb300 as q
+        from block_scaled_quantized_spec_gb300 import synth
+        self.kind, self.fmt, self.m, self.ns, self.k = kind, fmt, m, tuple(ns), k
+        rng = np.random.default_rng(seed)
+        packed = [q.qfmt_pack(fmt, synth.weights(n, k, rng=rng)) for n in ns]
+        self.g = [p[2] for p in packed]
+        base = [(torch.from_numpy(p[0]).cuda(), torch.from_numpy(p[1]).cuda()) for p in packed]
+        self.w = [base] + [[(c.clone(), s.clone()) for (c, s) in base] for _ in range(copies - 1)]
+        xb = synth.activations_bf16(m, k, rng=rng)
+        self.x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+        self.gamma = (1.0 + 0.1 * torch.randn(k, generator=torch.Generator().manual_seed(seed))).to(torch.bfloat16).cuda()
+        self.outs = [[torch.empty((m, n), dtype=torch.bfloat16, device="cuda") for n in ns] for _ in range(copies)]
+        self.copies = copies
+        self.bytes = sum(sizes(fmt, m, n, k) - 2 * m * k for n in ns) + 2 * m * k + (2 * k if kind == "rmsnorm" else 0)
+
+    def step(self, separate=False):
+        import block_scaled_quantized_spec_gb300 as q
+        for i in range(self.copies):
+            w, o = self.w[i], self.outs[i]
+            if self.kind == "rmsnorm":
+                q.qmm_rmsnorm(self.fmt, w[0][0], w[0][1], self.g[0], self.x, self.gamma, 1e-5, self.ns[0], out=o[0])
+            elif separate:
+                for j, n in enumerate(self.ns):
+                    q.qmm(self.fmt, w[j][0], w[j][1], self.g[j], self.x, n, out=o[j])
+            else:
+                q.qmm_batched(self.fmt, [c for c, _ in w], [s for _, s in w], self.g, self.x, list(self.ns), outs=o)
+
+    graph = Problem.graph
+
+
+def fused_row(kind, fmt, m, ns, k, hbm, steps=10, warmup=3):
+    import torch
+    per_call = sum(sizes(fmt, m, n, k) for n in ns)
+    prob = FusedProblem(kind, fmt, m, ns, k, max(4, min(64, -(-3 * L2_BYTES // per_call))))
+    g = prob.graph()
+    ms, _ = time_graph(g, steps, warmup, 1)
+    per = ms / prob.copies
+    gbs = prob.bytes / (per * 1e-3) / 1e9
+    row = {"op": f"qmm_{kind}", "fmt": fmt, "M": m, "N": list(ns), "K": k, "us": round(per * 1e3, 2),
+           "copies": prob.copies, "GB/s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
+    if kind == "batched":     # the same products as one qmm launch per matrix
+        prob.step = lambda: FusedProblem.step(prob, separate=True)
+        g2 = Problem.graph(prob)
+        ms2, _ = time_graph(g2, steps, warmup, 1)
+        row["us_separate_qmm"] = round(ms2 / prob.copies * 1e3, 2)
+        del g2
+    del prob, g
+    torch.cuda.empty_cache()
+    return row
+
+
 def gather_row(fmt, m, n, k, e, hbm, steps=10, warmup=3):
     import torch
     per_call = sizes(fmt, 0, n, k) * min(m, e)
@@ -502,6 +564,11 @@ def main():
             f, mm, nn, kk, ee = parts[1:]
             print(json.dumps(gather_row(f, int(mm), int(nn), int(kk), int(ee), hbm, args.steps, args.warmup)))
             return
+        if parts[0] in ("batched", "rmsnorm"):   # batched:fmt:M:N1,N2,..:K  /  rmsnorm:fmt:M:N:K
+            f, mm, nn, kk = parts[1:]
+            ns = tuple(int(v) for v in nn.split(","))
+            print(json.dumps(fused_row(parts[0], f, int(mm), ns, int(kk), hbm, args.steps, args.warmup)))
+            return
         f, mm, nn, kk = parts
         print(json.dumps(breakdown_row(f, int(mm), int(nn), int(kk), hbm, bf16, kind, args.steps,
                                        args.warmup)))
@@ -537,6 +604,8 @@ def main():
             rows.append(breakdown_row(f, mm, nn, kk, hbm, bf16, kind))
         for (f, mm, nn, kk, ee) in GATHER:
             rows.append(gather_row(f, mm, nn, kk, ee, hbm))
+        for (kind, f, mm, ns, kk) in FUSED:
+            rows.append(fused_row(kind, f, mm, ns, kk, hbm))
         line["breakdown"] = rows
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(fmt, m, n, k)

@@ -19,7 +19,8 @@ import numpy as np
 __all__ = [
     "FORMATS", "QfmtError", "load", "lib_path",
     "qfmt_block_size", "qfmt_codes_bytes", "qfmt_scales_bytes",
-    "qfmt_pack", "qfmt_dequant", "qmm", "qmm_ex", "qmm_workspace_bytes", "qmm_gather", "qfmt_last_error",
+    "qfmt_pack", "qfmt_dequant", "qmm", "qmm_ex", "qmm_workspace_bytes", "qmm_gather", "qmm_batched", "qmm_rmsnorm",
+    "qfmt_last_error",
     "qfmt_version", "qfmt_device_status", "qfmt_debug_set",
 ]
 
@@ -63,6 +64,13 @@ _SIGS = {
     "qmm_gather": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                   ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]),
+    "qmm_batched": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_void_p),
+                                   ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_float),
+                                   ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
+                                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]),
+    "qmm_rmsnorm": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                   ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]),
     "qfmt_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "qfmt_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_int64]),
 }
@@ -219,3 +227,33 @@ def qmm_gather(fmt, codes, scales, global_scale: float, x, expert_idx, N: int, E
     _check(load().qmm_gather(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), _ptr(expert_idx),
                              _ptr(out), M, N, K, E, group, _stream(stream)), "qmm_gather")
     return out
+
+
+def qmm_batched(fmt, codes, scales, global_scales, x, Ns, outs=None, group: int = 0, stream=None):
+    """Products of up to four weights with one activation: outs[i] [M, Ns[i]] bf16 = x . dequant(W_i)^T."""
+    import torch
+    M, K = x.shape
+    count = len(codes)
+    if not (len(scales) == len(global_scales) == len(Ns) == count):
+        raise QfmtError(-1, "qmm_batched", "codes, scales, global_scales and Ns differ in length")
+    if outs is None:
+        outs = [torch.empty((M, n), dtype=torch.bfloat16, device=x.device) for n in Ns]
+    arr = lambda ts: (ctypes.c_void_p * count)(*[t.data_ptr() for t in ts])  # noqa: E731
+    _check(load().qmm_batched(_fmt(fmt), count, arr(codes), arr(scales),
+                              (ctypes.c_float * count)(*[float(g) for g in global_scales]),
+                              (ctypes.c_int64 * count)(*[int(n) for n in Ns]), _ptr(x), arr(outs), M, K, group,
+                              _stream(stream)), "qmm_batched")
+    return outs
+
+
+def qmm_rmsnorm(fmt, codes, scales, global_scale: float, x, norm_weight, eps: float, N: int, out=None,
+                group: int = 0, stream=None):
+    """out [M, N] bf16 = rmsnorm(x; norm_weight, eps) . dequant(W)^T, M <= 2 (x and norm_weight bf16)."""
+    import torch
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(load().qmm_rmsnorm(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), _ptr(norm_weight),
+                              float(eps), _ptr(out), M, N, K, group, _stream(stream)), "qmm_rmsnorm")
+    return out
+

@@ -50,6 +50,13 @@ cudaError_t launch_qgemv_gather(int fmt, const void* codes, const void* scales, 
                                 const int32_t* eidx, void* out, bool out_f32, int64_t M, int64_t N, int64_t K,
                                 int64_t E, cudaStream_t st);
 cudaError_t read_and_clear_gather_status(unsigned int* status);
+
+// Decode GEMV (M <= 2) over `count` (1..4) weight matrices sharing the
+// activations, one launch; with gamma != nullptr the activations are
+// RMS-normalised first (x * gamma / sqrt(mean(x^2) + eps)).
+cudaError_t launch_qgemv_multi(int fmt, int count, const void* const* codes, const void* const* scales,
+                               const float* globs, const int64_t* Ns, const void* x, const void* gamma, float eps,
+                               void* const* outs, bool out_f32, int64_t M, int64_t K, cudaStream_t st);
 uint64_t wait_limit_ns();
 
 }  // namespace qfmt_dev

@@ -133,6 +133,80 @@ int qmm_gather(int fmt, const void* codes, const void* scales, float global_scal
                      "qmm_gather launch");
 }
 
+int qmm_batched(int fmt, int count, const void* const* codes, const void* const* scales,
+                const float* global_scales, const int64_t* N, const void* x, void* const* out, int64_t M,
+                int64_t K, int group, void* stream) {
+  clear_error();
+  int st = check_group(fmt, group);
+  if (st) return st;
+  if (count < 1 || count > 4) return fail(QFMT_EINVAL, "count=%d must be 1..4", count);
+  if (!codes || !scales || !global_scales || !N || !out) return fail(QFMT_EINVAL, "NULL pointer array");
+  for (int i = 0; i < count; ++i) {
+    if ((st = check_shape(fmt, M, N[i], K))) return st;
+    if ((st = check_ptr(out[i], 16, "out"))) return st;
+  }
+  if (M == 0) return QFMT_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    for (int i = 0; i < count; ++i)
+      if ((st = cuda_status(cudaMemsetAsync(out[i], 0, size_t(M) * size_t(N[i]) * 2, s), "memset"))) return st;
+    return QFMT_OK;
+  }
+  for (int i = 0; i < count; ++i)
+    if ((st = check_common(fmt, codes[i], scales[i], global_scales[i], group))) return st;
+  if ((st = check_ptr(x, 16, "x"))) return st;
+  bool any = false;
+  for (int i = 0; i < count; ++i) any |= N[i] > 0;
+  if (!any) return QFMT_OK;
+  if (M <= 2 && qfmt_dev::qgemv_m2_fits(fmt, M, K)) {
+    // one launch over every matrix's row tiles (a matrix with N = 0 has none)
+    const void* c[4];
+    const void* sc[4];
+    float g[4];
+    int64_t n[4];
+    void* o[4];
+    int live = 0;
+    for (int i = 0; i < count; ++i) {
+      if (N[i] == 0) continue;
+      c[live] = codes[i];
+      sc[live] = scales[i];
+      g[live] = global_scales[i];
+      n[live] = N[i];
+      o[live] = out[i];
+      ++live;
+    }
+    return cuda_status(qfmt_dev::launch_qgemv_multi(fmt, live, c, sc, g, n, x, nullptr, 0.0f, o, false, M, K, s),
+                       "qmm_batched launch");
+  }
+  for (int i = 0; i < count; ++i)   // larger batches: one qmm per matrix
+    if ((st = qmm(fmt, codes[i], scales[i], global_scales[i], x, out[i], M, N[i], K, group, stream))) return st;
+  return QFMT_OK;
+}
+
+int qmm_rmsnorm(int fmt, const void* codes, const void* scales, float global_scale, const void* x,
+                const void* norm_weight, float eps, void* out, int64_t M, int64_t N, int64_t K, int group,
+                void* stream) {
+  clear_error();
+  int st = check_group(fmt, group);
+  if (st) return st;
+  if ((st = check_shape(fmt, M, N, K))) return st;
+  if (M > 2) return fail(QFMT_EUNSUPPORTED, "qmm_rmsnorm is the decode form: M=%lld above 2", (long long)M);
+  if (!(std::isfinite(eps) && eps >= 0.0f)) return fail(QFMT_EINVAL, "eps must be finite and >= 0");
+  if (M == 0 || N == 0) return QFMT_OK;
+  if (K == 0) return fail(QFMT_ESHAPE, "the RMS of an empty row is undefined (K = 0)");
+  if ((st = check_ptr(out, 16, "out"))) return st;
+  if ((st = check_common(fmt, codes, scales, global_scale, group))) return st;
+  if ((st = check_ptr(x, 16, "x"))) return st;
+  if ((st = check_ptr(norm_weight, 16, "norm_weight"))) return st;
+  if (!qfmt_dev::qgemv_m2_fits(fmt, M, K))
+    return fail(QFMT_EUNSUPPORTED, "K=%lld too long for the fused decode GEMV", (long long)K);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float g = global_scale;
+  return cuda_status(qfmt_dev::launch_qgemv_multi(fmt, 1, &codes, &scales, &g, &N, x, norm_weight, eps, &out, false,
+                                                   M, K, s),
+                     "qmm_rmsnorm launch");
+}
+
 int qfmt_device_status(void* stream) {
   clear_error();
   int st = cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream sync");

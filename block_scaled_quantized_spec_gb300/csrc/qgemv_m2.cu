@@ -159,7 +159,7 @@ __host__ __device__ constexpr int xstride(int K) {
 inline size_t smem_bytes(int F, int M, int K, int warps = WARPS) {
   const int spans = K / 32;
   return size_t(M) * xstride(K) * 2 + 64 + size_t(M) * spans * 4 * (F == INT4_AFFINE ? 2 : 1) +
-         size_t(warps) * 2 * 16 * 4;
+         size_t(warps) * 2 * 16 * 4 + size_t(warps) * 2 * 4;
 }
 
 // Per-chunk scale words a D-holding lane keeps: the weight block scales of
@@ -171,16 +171,36 @@ struct ChunkScales {
 // Rows whose expert index lies outside [0, E) in an expert-routed launch.
 __device__ unsigned int g_gather_status;
 
-// GATHER: the expert-routed form (one activation row per blockIdx.y, M = 1):
-// the row's weights are rows [e N, e N + N) of the stacked matrix, e =
-// eidx[blockIdx.y], read once the preceding kernel has completed (it may be
-// the router that wrote them), so the weight requests wait for it too.
-template <int F, int MR, bool UNI, int W, bool GATHER = false>
+// Launch forms beyond the plain product (bits of MODE):
+//  * GATHER, the expert-routed form (one activation row per blockIdx.y, M =
+//    1): the row's weights are rows [e N, e N + N) of the stacked matrix, e =
+//    eidx[blockIdx.y], read once the preceding kernel has completed (it may be
+//    the router that wrote them), so the weight requests wait for it too;
+//  * BATCH: up to four weight matrices share the activations (the Q/K/V and
+//    4-way projections); the CTAs of matrix i are [tile0[i], tile0[i + 1]);
+//  * RMS: the activations are RMS-normalised on the way in: x * gamma is
+//    staged, sum(x^2) is gathered over the CTA (whose warps cover all of K),
+//    and 1 / sqrt(mean(x^2) + eps) multiplies each output.
+constexpr int GATHER = 1, BATCH = 2, RMS = 4;
+struct Extra {
+  const int32_t* eidx;          // GATHER
+  int E;
+  int count;                    // BATCH
+  const uint8_t* codes[4];
+  const uint8_t* scales[4];
+  float glob[4];
+  void* out[4];
+  int n[4];
+  int tile0[5];
+  const uint16_t* gamma;        // RMS: bf16 [K]
+  float eps;
+};
+
+template <int F, int MR, bool UNI, int W, int MODE = 0>
 __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const uint8_t* __restrict__ codes,
                                                            const uint8_t* __restrict__ scales, float glob,
                                                            const uint16_t* __restrict__ x, void* __restrict__ out,
-                                                           int out_f32, int M, int N, int K,
-                                                           const int32_t* __restrict__ eidx, int E) {
+                                                           int out_f32, int M, int N, int K, const Extra ex) {
   using S = Shape<F>;
   constexpr int P = chunks_per_warp<F, W>();
   constexpr int WARPS = W, THREADS = 32 * W;
@@ -194,19 +214,36 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   float* xsc = reinterpret_cast<float*>(xzero + 32);                        // [M][spans] 2^-shift
   float* xsum = xsc + M * spans;                                            // [M][spans] (int4 affine)
   float* red = xsum + (I4 ? M * spans : 0);                                 // [WARPS][2][16]
+  float* rss = red + WARPS * 2 * 16;                                        // [WARPS][2] (RMS)
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
-  const int row0 = blockIdx.x * 16;
-  if constexpr (GATHER) {
+  int row0 = blockIdx.x * 16;
+  if constexpr ((MODE & BATCH) != 0) {    // this CTA's matrix: unrolled selects, no indexed parameters
+    int i = 0;
+    #pragma unroll
+    for (int j = 1; j < 4; ++j) i += (j < ex.count && int(blockIdx.x) >= ex.tile0[j]) ? 1 : 0;
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j == i) {
+        codes = ex.codes[j];
+        scales = ex.scales[j];
+        glob = ex.glob[j];
+        out = ex.out[j];
+        N = ex.n[j];
+        row0 = (int(blockIdx.x) - ex.tile0[j]) * 16;
+      }
+    }
+  }
+  if constexpr ((MODE & GATHER) != 0) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t m = blockIdx.y;
-    const int e = __ldg(eidx + m);
+    const int e = __ldg(ex.eidx + m);
     x += m * K;
     out = static_cast<uint8_t*>(out) + m * N * (out_f32 ? 4 : 2);
-    if (e < 0 || e >= E) {                                                  // a zero row, and the status bit
+    if (e < 0 || e >= ex.E) {                                               // a zero row, and the status bit
       if (tid < 16 && row0 + tid < N) {
         if (out_f32) static_cast<float*>(out)[row0 + tid] = 0.0f;
         else static_cast<__nv_bfloat16*>(out)[row0 + tid] = __float2bfloat16_rn(0.0f);
@@ -327,6 +364,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   // ---- stage this warp's activations: the k ranges of its own chunks --------
   // 16 values per task, tasks 2s and 2s+1 (lanes l and l^1) share a 32-span;
   // the span's shift puts its largest |x| in [2^14, 2^15).
+  float ssq[2] = {0.0f, 0.0f};                                               // RMS: this lane's sum of x^2 per row
   {
     constexpr int TPC = CODES / 16;                                            // tasks per chunk and row
     const int per_m = mine * TPC;
@@ -357,21 +395,49 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
         const bool live = lv[u];
         const int m = mm[u], k = kk[u];
         const uint32_t h[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
-        uint32_t m2 = 0;
-        #pragma unroll
-        for (int q = 0; q < 8; ++q) m2 = max_u16x2(m2, h[q] & 0x7FFF7FFFu);
-        uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
-        mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));                     // the other half of the span
-        const int E = int(mx >> 7);
-        int sh = (mx == 0u || E == 255) ? 0 : 141 - E;                         // 14 - (E - 127)
-        sh = sh > 126 ? 126 : sh;
-        const float up = __uint_as_float(uint32_t(sh + 127) << 23);
         float f[16];
-        #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          f[2 * q] = __fmul_rn(__uint_as_float(h[q] << 16), up);
-          f[2 * q + 1] = __fmul_rn(__uint_as_float(h[q] & 0xFFFF0000u), up);
+        int sh;
+        if constexpr ((MODE & RMS) != 0) {
+          // x * gamma (exact in float32), its span maximum, and this row's sum of x^2
+          const uint4* gp = reinterpret_cast<const uint4*>(ex.gamma + k);
+          const uint4 g0 = live ? __ldg(gp) : make_uint4(0, 0, 0, 0), g1 = live ? __ldg(gp + 1) : make_uint4(0, 0, 0, 0);
+          const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+          uint32_t mx = 0;
+          float sq = 0.0f;
+          #pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float x0 = __uint_as_float(h[q] << 16), x1 = __uint_as_float(h[q] & 0xFFFF0000u);
+            f[2 * q] = __fmul_rn(x0, __uint_as_float(gw[q] << 16));
+            f[2 * q + 1] = __fmul_rn(x1, __uint_as_float(gw[q] & 0xFFFF0000u));
+            sq = __fmaf_rn(x0, x0, sq);
+            sq = __fmaf_rn(x1, x1, sq);
+            mx = max(mx, __float_as_uint(f[2 * q]) & 0x7FFFFFFFu);
+            mx = max(mx, __float_as_uint(f[2 * q + 1]) & 0x7FFFFFFFu);
+          }
+          if (m == 0) ssq[0] += sq;
+          else ssq[1] += sq;
+          mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));                   // the other half of the span
+          const int E = int(mx >> 23);
+          sh = (mx == 0u || E == 255) ? 0 : 141 - E;                           // 14 - (E - 127)
+          sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
+        } else {
+          uint32_t m2 = 0;
+          #pragma unroll
+          for (int q = 0; q < 8; ++q) m2 = max_u16x2(m2, h[q] & 0x7FFF7FFFu);
+          uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+          mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));                   // the other half of the span
+          const int E = int(mx >> 7);
+          sh = (mx == 0u || E == 255) ? 0 : 141 - E;                           // 14 - (E - 127)
+          sh = sh > 126 ? 126 : sh;
+          #pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            f[2 * q] = __uint_as_float(h[q] << 16);
+            f[2 * q + 1] = __uint_as_float(h[q] & 0xFFFF0000u);
+          }
         }
+        const float up = __uint_as_float(uint32_t(sh + 127) << 23);
+        #pragma unroll
+        for (int q = 0; q < 16; ++q) f[q] = __fmul_rn(f[q], up);
         uint32_t o[8];
         if constexpr (I4) {   // per 8 values: (x0,x4) (x1,x5) (x2,x6) (x3,x7), the int4 pairing
           #pragma unroll
@@ -527,6 +593,15 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
     red[(warp * 2 + (t >> 1)) * 16 + g] = acc_a;
     red[(warp * 2 + (t >> 1)) * 16 + g + 8] = acc_b;
   }
+  if constexpr ((MODE & RMS) != 0) {
+    #pragma unroll
+    for (int mm = 0; mm < 2; ++mm) {
+      float v = ssq[mm];
+      #pragma unroll
+      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+      if (lane == 0) rss[warp * 2 + mm] = v;
+    }
+  }
   __syncthreads();
   if (tid < 16 * M) {
     const int m = tid >> 4, rr = tid & 15;
@@ -535,6 +610,12 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
       #pragma unroll
       for (int w = 0; w < WARPS; ++w) sum += red[(w * 2 + m) * 16 + rr];
       if constexpr (F == NVFP4) sum *= glob;
+      if constexpr ((MODE & RMS) != 0) {
+        float ss = 0.0f;
+        #pragma unroll
+        for (int w = 0; w < WARPS; ++w) ss += rss[w * 2 + m];
+        sum *= rsqrtf(__fadd_rn(__fdiv_rn(ss, float(K)), ex.eps));
+      }
       const int64_t o = int64_t(m) * N + row0 + rr;
       if (out_f32) static_cast<float*>(out)[o] = sum;
       else static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(sum);
@@ -542,17 +623,17 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   }
 }
 
-template <int F, int MR, bool UNI, int W = 8, bool GATHER = false>
+template <int F, int MR, bool UNI, int W = 8, int MODE = 0>
 static cudaError_t launch_mr(const void* codes, const void* scales, float glob, const void* x, void* out,
-                              bool out_f32, int M, int N, int K, cudaStream_t st, const int32_t* eidx = nullptr,
-                              int E = 0, int rows = 1) {
+                              bool out_f32, int M, int N, int K, cudaStream_t st, const Extra& ex = Extra{},
+                              int tiles = 0, int rows = 1) {
   static std::atomic<int> attr_done[64];
   const size_t sm = smem_bytes(F, M, K, W);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
-    e = cudaFuncSetAttribute(qgemv_m2_kernel<F, MR, UNI, W, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(qgemv_m2_kernel<F, MR, UNI, W, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(SMEM_LIMIT));
     if (e != cudaSuccess) return e;
     attr_done[dev].store(1);
@@ -561,15 +642,15 @@ static cudaError_t launch_mr(const void* codes, const void* scales, float glob, 
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.gridDim = dim3((N + 15) / 16, rows);
+  lc.gridDim = dim3(tiles > 0 ? tiles : (N + 15) / 16, rows);
   lc.blockDim = dim3(32 * W);
   lc.dynamicSmemBytes = sm;
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F, MR, UNI, W, GATHER>, static_cast<const uint8_t*>(codes),
+  return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F, MR, UNI, W, MODE>, static_cast<const uint8_t*>(codes),
                             static_cast<const uint8_t*>(scales), glob, static_cast<const uint16_t*>(x), out,
-                            int(out_f32), M, N, K, eidx, E);
+                            int(out_f32), M, N, K, ex);
 }
 
 // 8-warp CTAs (two per SM); E2M1 formats whose grid exceeds two CTAs per SM
@@ -606,8 +687,28 @@ static cudaError_t launch_gather_fmt(const void* codes, const void* scales, floa
   constexpr int CODES = Shape<F>::CODES;
   const int nchunk = (K + CODES - 1) / CODES;
   const bool uni = K % (WARPS * CODES) == 0 && (nchunk / WARPS) % chunks_in_flight<F>() == 0;
-  return uni ? launch_mr<F, 1, true, 8, true>(codes, scales, glob, x, out, out_f32, 1, N, K, st, eidx, E, M)
-             : launch_mr<F, 1, false, 8, true>(codes, scales, glob, x, out, out_f32, 1, N, K, st, eidx, E, M);
+  Extra ex{};
+  ex.eidx = eidx;
+  ex.E = E;
+  return uni ? launch_mr<F, 1, true, 8, GATHER>(codes, scales, glob, x, out, out_f32, 1, N, K, st, ex, 0, M)
+             : launch_mr<F, 1, false, 8, GATHER>(codes, scales, glob, x, out, out_f32, 1, N, K, st, ex, 0, M);
+}
+
+// Up to four weight matrices sharing the activations (BATCH), optionally
+// behind a fused RMSNorm (RMS), or one matrix behind the RMSNorm.
+template <int F, int MODE>
+static cudaError_t launch_multi_fmt(const Extra& ex, const void* x, bool out_f32, int M, int K, int tiles,
+                                    cudaStream_t st) {
+  constexpr int CODES = Shape<F>::CODES;
+  const int nchunk = (K + CODES - 1) / CODES;
+  const bool uni = K % (WARPS * CODES) == 0 && (nchunk / WARPS) % chunks_in_flight<F>() == 0;
+  const void* c0 = ex.codes[0];
+  const void* s0 = ex.scales[0];
+  if (M == 1)
+    return uni ? launch_mr<F, 1, true, 8, MODE>(c0, s0, ex.glob[0], x, ex.out[0], out_f32, M, ex.n[0], K, st, ex, tiles)
+               : launch_mr<F, 1, false, 8, MODE>(c0, s0, ex.glob[0], x, ex.out[0], out_f32, M, ex.n[0], K, st, ex, tiles);
+  return uni ? launch_mr<F, 2, true, 8, MODE>(c0, s0, ex.glob[0], x, ex.out[0], out_f32, M, ex.n[0], K, st, ex, tiles)
+             : launch_mr<F, 2, false, 8, MODE>(c0, s0, ex.glob[0], x, ex.out[0], out_f32, M, ex.n[0], K, st, ex, tiles);
 }
 
 }  // namespace gemv_m2
@@ -651,6 +752,43 @@ cudaError_t read_and_clear_gather_status(unsigned int* status) {
   if (e != cudaSuccess) return e;
   const unsigned int zero = 0;
   return cudaMemcpyToSymbol(gemv_m2::g_gather_status, &zero, sizeof(unsigned int));
+}
+
+cudaError_t launch_qgemv_multi(int fmt, int count, const void* const* codes, const void* const* scales,
+                               const float* globs, const int64_t* Ns, const void* x, const void* gamma, float eps,
+                               void* const* outs, bool out_f32, int64_t M, int64_t K, cudaStream_t st) {
+  using namespace gemv_m2;
+  Extra ex{};
+  ex.count = count;
+  int tiles = 0;
+  for (int i = 0; i < 4; ++i) {
+    const int j = i < count ? i : count - 1;   // unused slots repeat the last matrix
+    ex.codes[i] = static_cast<const uint8_t*>(codes[j]);
+    ex.scales[i] = static_cast<const uint8_t*>(scales[j]);
+    ex.glob[i] = globs[j];
+    ex.out[i] = outs[j];
+    ex.n[i] = int(Ns[j]);
+    ex.tile0[i] = tiles;
+    if (i < count) tiles += int((Ns[i] + 15) / 16);
+  }
+  ex.tile0[4] = tiles;
+  ex.gamma = static_cast<const uint16_t*>(gamma);
+  ex.eps = eps;
+  const int m = int(M), k = int(K);
+  const bool rms = gamma != nullptr, batch = count > 1;
+#define QFMT_MULTI(FMT)                                                                             \
+  return rms ? (batch ? launch_multi_fmt<FMT, BATCH | RMS>(ex, x, out_f32, m, k, tiles, st)        \
+                      : launch_multi_fmt<FMT, RMS>(ex, x, out_f32, m, k, tiles, st))              \
+             : launch_multi_fmt<FMT, BATCH>(ex, x, out_f32, m, k, tiles, st)
+  switch (fmt) {
+    case MXFP4: QFMT_MULTI(MXFP4);
+    case NVFP4: QFMT_MULTI(NVFP4);
+    case MXFP8_E4M3: QFMT_MULTI(MXFP8_E4M3);
+    case MXFP8_E5M2: QFMT_MULTI(MXFP8_E5M2);
+    case NVFP8: QFMT_MULTI(NVFP8);
+    default: QFMT_MULTI(INT4_AFFINE);
+  }
+#undef QFMT_MULTI
 }
 
 }  // namespace qfmt_dev

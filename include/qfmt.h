@@ -171,6 +171,38 @@ int qmm_gather(int fmt, const void* codes, const void* scales, float global_scal
                int64_t M, int64_t N, int64_t K, int64_t E, int group, void* stream);
 
 /*
+ * qmm_batched -- device: `count` (1..4) products sharing one activation:
+ *   out[i][M, N[i]] (bf16) = X[M, K] (bf16) . dequant(W_i[N[i], K])^T
+ * (metaltile PR #250, the batched Q/K/V and batched-4 dequantizing GEMV
+ * commits: one dispatch projects [Wq x | Wk x | Wv x] over a shared
+ * activation, each matrix into its own output).  codes, scales,
+ * global_scales, N and out are HOST arrays of `count` entries (device
+ * pointers inside, each laid out as for qmm; the matrices may differ in N but
+ * not in format, K or group).  M <= 2 runs one launch over every matrix's row
+ * tiles; larger M runs one qmm per matrix.  Errors as qmm, per matrix;
+ * QFMT_EINVAL for count outside 1..4 or a NULL array.  Tolerance as qmm.
+ */
+int qmm_batched(int fmt, int count, const void* const* codes, const void* const* scales,
+                const float* global_scales, const int64_t* N, const void* x, void* const* out,
+                int64_t M, int64_t K, int group, void* stream);
+
+/*
+ * qmm_rmsnorm -- device, RMSNorm fused in front of the decode GEMV:
+ *   out[m, n] (bf16) = sum_k (x[m,k] * gamma[k] / sqrt(mean_k x[m,k]^2 + eps))
+ *                      * dequant(W)[n, k]
+ * (metaltile PR #250, the fused RMSNorm + dequantizing GEMV commit: phase 1
+ * the sum of x^2 and its inverse root, phase 2 the GEMV over the normalised
+ * activation x * norm_weight * inv_rms).  x bf16 [M, K], norm_weight (gamma)
+ * bf16 [K], both 16-byte aligned; eps finite and >= 0.  M <= 2 (the decode
+ * form; QFMT_EUNSUPPORTED beyond); K = 0 is QFMT_ESHAPE.  Result within
+ * 2e-3 * sum_k |x~||w| + 1e-6 of the exact value, x~ the exactly normalised
+ * activation.
+ */
+int qmm_rmsnorm(int fmt, const void* codes, const void* scales, float global_scale,
+                const void* x, const void* norm_weight, float eps, void* out,
+                int64_t M, int64_t N, int64_t K, int group, void* stream);
+
+/*
  * qfmt_device_status -- waits for `stream`, then reads and clears the
  * library's device status word for the current device.  Every pipeline wait
  * inside the tensor-core GEMM is bounded in time; when one expires the kernel

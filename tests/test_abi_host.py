@@ -183,3 +183,36 @@ def test_gather_entry_validation_without_gpu(lib):
     assert _call_gather(lib, group=32, fmt=6) == -4
     assert b"expert" in lib.qfmt_last_error() or _call_gather(lib, E=0) == -1
     assert _call_gather(lib, M=0) == 0 and _call_gather(lib, N=0) == 0
+
+
+def test_batched_and_rmsnorm_validation_without_gpu(lib):
+    P = ctypes.c_void_p
+    arr = lambda *v: (P * len(v))(*v)  # noqa: E731
+    f = lambda *v: (ctypes.c_float * len(v))(*v)  # noqa: E731
+    n = lambda *v: (ctypes.c_int64 * len(v))(*v)  # noqa: E731
+    ok = dict(codes=arr(0x1000, 0x1000), scales=arr(0x1000, 0x1000), g=f(1.0, 1.0), N=n(4, 4),
+              out=arr(0x1000, 0x1000))
+
+    def batched(count=2, x=0x1000, M=1, K=64, **kw):
+        a = dict(ok)
+        a.update(kw)
+        return lib.qmm_batched(1, count, a["codes"], a["scales"], a["g"], a["N"], x, a["out"], M, K, 0, None)
+
+    assert batched(count=0) == -1
+    assert batched(count=5) == -1
+    assert batched(K=48) == -2
+    assert batched(out=arr(0x1000, 0x1004)) == -3
+    assert batched(codes=arr(0x1000, 0x1008)) == -3
+    assert batched(x=0x1002) == -3
+    assert batched(M=0) == 0
+
+    def rms(M=1, eps=1e-5, gamma=0x1000, K=64, N=4):
+        return lib.qmm_rmsnorm(1, 0x1000, 0x1000, 1.0, 0x1000, gamma, eps, 0x1000, M, N, K, 0, None)
+
+    assert rms(M=3) == -4
+    assert rms(eps=-1.0) == -1
+    assert rms(eps=float("inf")) == -1
+    assert rms(K=0) == -2
+    assert rms(gamma=0x1008) == -3
+    assert rms(gamma=None) == -1
+    assert rms(M=0) == 0 and rms(N=0) == 0

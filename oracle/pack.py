@@ -27,7 +27,12 @@ Readings taken where the pages are silent (each is listed in the design doc):
 * Element encoders round to nearest, ties to the even code, saturating.
 * int4 affine (MLX style, group 64): s = (max - min) / 15 (1.0 when 0), stored
   as bf16 (RNE); bias = bf16(min); q = clamp(round_half_away((w - b) / s), 0, 15);
-  scale and bias are interleaved per group as bf16 pairs [N, K/64, 2].
+  scale and bias are interleaved per group as bf16 pairs [N, ceil(K/64), 2].
+* K is a multiple of 32.  A K that 64 does not divide leaves int4 affine a
+  ragged trailing group of 32 values with its own statistics (metaltile PR
+  #250 body: a group size that does not divide the dimension tiles with a
+  ragged trailing block, n_blocks = ceil(dim / block_size), packer and kernel
+  rounding up alike).
 """
 from __future__ import annotations
 
@@ -51,8 +56,13 @@ def codes_nbytes(fmt: str, n: int, k: int) -> int:
     return n * k * ELEM_BITS[fmt] // 8
 
 
+def n_blocks(fmt: str, k: int) -> int:
+    """Blocks per row: ceil(K / block) (only int4 affine can have a ragged last one)."""
+    return -(-k // BLOCK[fmt])
+
+
 def scales_nbytes(fmt: str, n: int, k: int) -> int:
-    return n * (k // BLOCK[fmt]) * SCALE_BYTES[fmt]
+    return n * n_blocks(fmt, k) * SCALE_BYTES[fmt]
 
 
 def _pack_nibbles(codes: np.ndarray) -> np.ndarray:
@@ -72,18 +82,26 @@ def _quantize(w_blocks: np.ndarray, eff: np.ndarray, elem: str) -> np.ndarray:
 def pack(fmt: str, w: np.ndarray):
     """Pack float32 W [N, K].  Returns (codes bytes, scales bytes, global_scale float32).
 
-    Raises ValueError on non-finite weights, K not a multiple of the block, or a
-    scale that overflows float32.
+    Raises ValueError on non-finite weights, K not a multiple of 32 (and of the
+    block, except int4 affine's ragged last group), or a scale that overflows
+    float32.
     """
     if fmt not in FORMATS:
         raise ValueError(f"unknown format {fmt!r}")
     w = np.ascontiguousarray(w, dtype=F32)
     n, k = w.shape
     blk = BLOCK[fmt]
-    if k % blk or k % 8:
-        raise ValueError("K must be a multiple of the block size and of 8")
+    if k % 32 or (k % blk and fmt != "int4_affine"):
+        raise ValueError("K must be a multiple of 32 and of the block size (int4 affine: of 32)")
     if not np.all(np.isfinite(w)):
         raise ValueError("non-finite weight")
+    if fmt == "int4_affine" and k % blk:
+        # the ragged last group, padded with copies of its own first value:
+        # its min and max, hence its scale, bias and codes, are unchanged
+        kp = n_blocks(fmt, k) * blk
+        wp = np.concatenate([w, np.repeat(w[:, (kp - blk):(kp - blk) + 1], kp - k, axis=1)], axis=1)
+        c, s, g = _pack_int4_affine(wp.reshape(n, kp // blk, blk), n, kp)
+        return np.ascontiguousarray(c[:, : k // 2]), s, g
     wb = w.reshape(n, k // blk, blk)
     amax = np.max(np.abs(wb), axis=2).astype(F32)          # step 1
     glob = F32(1.0)

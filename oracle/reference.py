@@ -59,13 +59,13 @@ def unpack_codes(fmt: str, codes: np.ndarray, n: int, k: int) -> np.ndarray:
 
 
 def block_scales(fmt: str, scales: np.ndarray, global_scale: float, n: int, k: int):
-    """Decoded per-block scale terms, each [N, K/block] float64.
+    """Decoded per-block scale terms, each [N, ceil(K/block)] float64.
 
     Returns (mult, add): w = elem * mult (+ add for int4 affine).  For nvfp4
     ``mult`` is the E4M3 micro-scale only; the global is applied separately so
     that the product order (e2m1 * e4m3) * global is kept.
     """
-    nb = k // BLOCK[fmt]
+    nb = -(-k // BLOCK[fmt])
     s = np.asarray(scales, dtype=np.uint8).reshape(n, -1)
     if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2"):
         return codec.E8M0_TABLE[s.reshape(n, nb)], None
@@ -92,15 +92,16 @@ def dequant_exact(fmt: str, codes, scales, global_scale, n: int, k: int) -> np.n
     if fmt not in FORMATS:
         raise ValueError(fmt)
     blk = BLOCK[fmt]
-    e = element_values(fmt, unpack_codes(fmt, codes, n, k)).reshape(n, k // blk, blk)
+    e = element_values(fmt, unpack_codes(fmt, codes, n, k))
     mult, add = block_scales(fmt, scales, global_scale, n, k)
+    col = np.arange(k) // blk                            # the block of every column (a ragged last one too)
     with np.errstate(invalid="ignore", over="ignore"):
-        w = e * mult[..., None]
+        w = e * mult[:, col]
         if add is not None:
-            w = w + add[..., None]
+            w = w + add[:, col]
         if fmt == "nvfp4":
             w = w * np.float64(np.float32(global_scale))
-    return w.reshape(n, k)
+    return w
 
 
 def dequant_f32(fmt: str, codes, scales, global_scale, n: int, k: int) -> np.ndarray:
@@ -133,7 +134,7 @@ def qmm_ref_sampled(fmt, codes, scales, global_scale, x, x_dtype, m, n, k, rows,
     cols = np.asarray(cols)
     uniq, inv = np.unique(cols, return_inverse=True)
     per_row_codes = ELEM_BITS[fmt] * k // 8
-    per_row_scales = (k // BLOCK[fmt]) * (4 if fmt in ("nvfp8", "int4_affine") else 1)
+    per_row_scales = -(-k // BLOCK[fmt]) * (4 if fmt in ("nvfp8", "int4_affine") else 1)
     c = np.asarray(codes, dtype=np.uint8).reshape(n, per_row_codes)[uniq]
     s = np.asarray(scales, dtype=np.uint8).reshape(n, per_row_scales)[uniq]
     w = dequant_exact(fmt, c, s, global_scale, len(uniq), k)[inv]

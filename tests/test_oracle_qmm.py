@@ -424,3 +424,29 @@ def test_planted_rmsnorm_mistake_is_caught(monkeypatch):
         mp.setattr(reference, "rmsnorm_values", sum_not_mean)
         with pytest.raises(AssertionError):
             test_rmsnorm_ref_matches_decimal_brute_force("mxfp4")
+
+
+# ----- int4 affine with a ragged last group (K a multiple of 32, not of 64) -----
+
+@pytest.mark.parametrize("k", [32, 96, 160])
+def test_ragged_int4_matches_exact_rational_brute_force(k):
+    assert _check_brute("int4_affine", m=2, n=4, k=k, seed=k)
+
+
+def test_ragged_int4_group_round_trips_exactly():
+    # Every group (the 32-wide last one too) holds b + s q with q spanning 0..15,
+    # s and b exact in bf16: the packer must find exactly s and b and the codes.
+    n, k = 3, 96
+    rng = np.random.default_rng(61)
+    w = np.empty((n, k), np.float32)
+    for r in range(n):
+        for g0 in range(0, k, 64):
+            width = min(64, k - g0)
+            s = np.float32(2.0 ** rng.integers(-6, 2)) * np.float32(1.5)
+            b = np.float32(rng.integers(-40, 40)) * np.float32(0.125)
+            q = rng.integers(0, 16, size=width)
+            q[0], q[-1] = 0, 15
+            w[r, g0:g0 + width] = b + s * q.astype(np.float32)
+    c, s_, g = pack.pack("int4_affine", w)
+    assert c.shape == (n, k // 2) and s_.shape == (n, 2 * 4)
+    assert np.array_equal(reference.dequant_exact("int4_affine", c, s_, g, n, k), w.astype(np.float64))

@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
   constexpr int PIECE = T::four ? 32 : 16;     // codes per 16-byte piece
   const int64_t pieces_per_row = K / PIECE;
   const int64_t total = N * pieces_per_row;
-  const int64_t nblk = K / T::block;
+  const int64_t nblk = (K + T::block - 1) / T::block;   // int4 affine: a ragged last group
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int64_t p = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; p < total;

@@ -61,8 +61,8 @@ int check_group(int fmt, int group) {
 int check_shape(int fmt, int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0) return fail(QFMT_ESHAPE, "negative size M=%lld N=%lld K=%lld",
                                            (long long)M, (long long)N, (long long)K);
-  const int kq = fmt == QFMT_INT4_AFFINE ? 64 : 32;
-  if (K % kq) return fail(QFMT_ESHAPE, "K=%lld must be a multiple of %d", (long long)K, kq);
+  // int4 affine (group 64) may end in a ragged group of 32 (ceil(K/64) groups)
+  if (K % 32) return fail(QFMT_ESHAPE, "K=%lld must be a multiple of 32", (long long)K);
   if (N > (int64_t(1) << 31) || M > (int64_t(1) << 31) || K > (int64_t(1) << 31))
     return fail(QFMT_ESHAPE, "size above 2^31");
   return QFMT_OK;
@@ -190,7 +190,7 @@ int64_t qfmt_codes_bytes(int fmt, int64_t N, int64_t K) {
 
 int64_t qfmt_scales_bytes(int fmt, int64_t N, int64_t K) {
   if (!valid_format(fmt) || check_shape(fmt, 0, N, K) != QFMT_OK) return -1;
-  return N * (K / block_of(fmt)) * scale_entry_bytes(fmt);
+  return N * ((K + block_of(fmt) - 1) / block_of(fmt)) * scale_entry_bytes(fmt);
 }
 
 int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* codes,
@@ -206,7 +206,7 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
   if (N == 0 || K == 0) return QFMT_OK;
 
   const int blk = block_of(fmt);
-  const int64_t nb = K / blk;
+  const int64_t nb = (K + blk - 1) / blk;   // int4 affine: a ragged last group of K - 64 (nb - 1) values
   const bool four = is_4bit(fmt);
   const int64_t row_bytes = four ? K / 2 : K;
   uint8_t* cb = static_cast<uint8_t*>(codes);
@@ -240,9 +240,10 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
       uint8_t* crow = cb + n * row_bytes;
       for (int64_t b = 0; b < nb; ++b) {
         const float* wb = w + b * blk;
+        const int len = int(std::min<int64_t>(blk, K - b * blk));
         if (fmt == QFMT_INT4_AFFINE) {
           float mn = wb[0], mx = wb[0];
-          for (int j = 1; j < blk; ++j) { mn = std::min(mn, wb[j]); mx = std::max(mx, wb[j]); }
+          for (int j = 1; j < len; ++j) { mn = std::min(mn, wb[j]); mx = std::max(mx, wb[j]); }
           float s = (mx - mn) / 15.0f;
           if (s == 0.0f) s = 1.0f;
           if (!std::isfinite(s)) { bad = true; continue; }
@@ -251,7 +252,7 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
           uint16_t* pr = reinterpret_cast<uint16_t*>(sb + (n * nb + b) * 4);
           pr[0] = sh;
           pr[1] = bh;
-          for (int j = 0; j < blk; ++j) {
+          for (int j = 0; j < len; ++j) {
             uint32_t q = 0;
             if (sf != 0.0f) {
               float v = std::round((wb[j] - bfv) / sf);

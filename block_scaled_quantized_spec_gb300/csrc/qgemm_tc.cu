@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
     // -------------------------------------------------------------- decoders
     const int dt = threadIdx.x - 64;                       // 0 .. DEC_THREADS-1
     const int64_t row_bytes = T::four ? p.K / 2 : p.K;
-    const int64_t nblk = p.K / T::block;
+    const int64_t nblk = (p.K + T::block - 1) / T::block;   // int4 affine: a ragged last group
     const int sub = dt % PIECES_PER_ROW;                   // piece index within the row's K step
     const int rbase = dt / PIECES_PER_ROW;
     uint4 cur[PIECES_PER_THREAD], nxt[PIECES_PER_THREAD];

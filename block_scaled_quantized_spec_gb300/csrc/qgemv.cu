@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
   const int g = lane >> 2, t = lane & 3;
   const int row0 = blockIdx.x * ROWS;
   const int64_t row_bytes = FOUR ? K / 2 : K;
-  const int64_t nblk = K / BLK;
+  const int64_t nblk = (K + BLK - 1) / BLK;   // int4 affine: a ragged last group
   const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(&wbar));
   const int nrows = N - row0 < ROWS ? N - row0 : ROWS;
   if (tid == 0) {

@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
       return;
     }
     codes += int64_t(e) * N * (FmtTraits<F>::four ? K / 2 : K);
-    scales += int64_t(e) * N * (K / FmtTraits<F>::block) * FmtTraits<F>::sbytes;
+    scales += int64_t(e) * N * ((K + FmtTraits<F>::block - 1) / FmtTraits<F>::block) * FmtTraits<F>::sbytes;
   }
   const int ra = row0 + g, rb = row0 + g + 8;
   const bool va = ra < N, vb = rb < N;
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   const int nchunk = (K + CODES - 1) / CODES;
   const int mine = nchunk > warp ? (nchunk - warp + WARPS - 1) / WARPS : 0;   // chunks of this warp
   const int a0 = (2 * t) & 3;                                                 // first column's quad lane
-  const int64_t nblk = K / FmtTraits<F>::block;
+  const int64_t nblk = (K + FmtTraits<F>::block - 1) / FmtTraits<F>::block;   // int4 affine: a ragged last group
 
   uint4 wa[P], wb[P];
   ChunkScales cs[P];
@@ -564,7 +564,8 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
         acc_b = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].b1), x1s), d[ii][3], acc_b);
       } else if constexpr (F == INT4_AFFINE) {
         // sum_k x~ (1024 + q): s * D + (b - 1024 s) * sum(x~), then the span's 2^-shift
-        const float m0 = xsum[md * spans + s0], m1 = xsum[md * spans + s1];
+        // a second span past K (a ragged last group of 32) adds no bias term
+        const float m0 = xsum[md * spans + s0], m1 = k0 + LANE < K ? xsum[md * spans + s1] : 0.0f;
         const float sa = bf16bits_f32(cs[i].a0 & 0xFFFFu), ba = __fmaf_rn(-1024.0f, sa, bf16bits_f32(cs[i].a0 >> 16));
         const float sb = bf16bits_f32(cs[i].b0 & 0xFFFFu), bb = __fmaf_rn(-1024.0f, sb, bf16bits_f32(cs[i].b0 >> 16));
         acc_a = __fmaf_rn(x0s, __fmaf_rn(sa, d[ii][0], ba * m0), acc_a);

@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
   const int ra = row0 + 16 * warp + g, rb = ra + 8;
   const bool va = ra < N, vb = rb < N;                                      // rows past N read row 0, never stored
   const int64_t rowbytes = FOUR ? K / 2 : K;
-  const int64_t nblk = K / BLK;
+  const int64_t nblk = (K + BLK - 1) / BLK;   // int4 affine: a ragged last group
   const uint8_t* pa = codes + int64_t(va ? ra : 0) * rowbytes + (FOUR ? k0 / 2 : k0) + 4 * t;
   const uint8_t* pb = codes + int64_t(vb ? rb : 0) * rowbytes + (FOUR ? k0 / 2 : k0) + 4 * t;
   const uint8_t* sra = scales + int64_t(va ? ra : 0) * nblk * SB;

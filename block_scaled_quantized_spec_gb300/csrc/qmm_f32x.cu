@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(256) qmm_f32x_kernel(const uint8_t* __restrict
   if (wid >= int64_t(N) * mgroups) return;
   const int n = int(wid / mgroups), m0 = int(wid % mgroups) * 8;
   const int64_t row_bytes = T::four ? K / 2 : K;
-  const int64_t nblk = K / T::block;
+  const int64_t nblk = (K + T::block - 1) / T::block;   // int4 affine: a ragged last group
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int k0 = lane * PIECE; k0 < K; k0 += 32 * PIECE) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(codes + n * row_bytes + (T::four ? k0 / 2 : k0)));

@@ -18,8 +18,12 @@
  *   codes   [N, K/2] bytes for 4-bit formats: element k of a row sits in byte
  *           k/2, low nibble for even k (LSB-first; 8 codes per u32 word);
  *           [N, K] bytes for 8-bit formats.
- *   scales  [N, K/block] entries of the sizes above; int4 affine stores the
- *           (scale, bias) bf16 pair of each group adjacently: [N, K/64, 2].
+ *   scales  [N, ceil(K/block)] entries of the sizes above; int4 affine stores
+ *           the (scale, bias) bf16 pair of each group adjacently:
+ *           [N, ceil(K/64), 2].  K is a multiple of 32 for every format, so
+ *           only int4 affine can end in a ragged group (of 32 values, with its
+ *           own scale and bias; PR #250: a ragged trailing block, the block
+ *           count rounded up).
  *   X       [M, K] bf16 (or f32 through qmm_ex), out [M, N] bf16 (or f32).
  *
  * Element values: E2M1 {0,.5,1,1.5,2,3,4,6} with sign bit 3; E4M3 bias 7,
@@ -70,7 +74,7 @@ typedef enum { QFMT_F32 = 0, QFMT_BF16 = 1 } qfmt_dtype;
 typedef enum {
   QFMT_OK = 0,
   QFMT_EINVAL = -1,        /* unknown format/dtype, NULL pointer, bad global scale */
-  QFMT_ESHAPE = -2,        /* negative size, or K not a multiple of 32 (64 for int4 affine) */
+  QFMT_ESHAPE = -2,        /* negative size, or K not a multiple of 32 */
   QFMT_EALIGN = -3,        /* a device pointer not 16-byte aligned (scales: 4-byte) */
   QFMT_EUNSUPPORTED = -4,  /* a group size other than the format's block */
   QFMT_ECUDA = -5,         /* a CUDA launch or device query failed */

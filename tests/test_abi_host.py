@@ -51,7 +51,8 @@ def test_sizes_and_blocks(lib):
         assert q.qfmt_scales_bytes(name, 7, 256) == opack.scales_nbytes(name, 7, 256)
     assert q.qfmt_block_size(99) == 0
     assert q.qfmt_codes_bytes("mxfp4", 4, 48) == -1           # K not a multiple of 32
-    assert q.qfmt_codes_bytes("int4_affine", 4, 96) == -1     # K not a multiple of 64
+    assert q.qfmt_codes_bytes("int4_affine", 4, 80) == -1     # K not a multiple of 32
+    assert q.qfmt_scales_bytes("int4_affine", 4, 96) == 4 * 2 * 4   # a ragged last group of 32
 
 
 CASES = [
@@ -60,6 +61,8 @@ CASES = [
     (8, 256, 2, 1e-20, False),      # tiny weights: subnormal scales / codes
     (8, 256, 3, 3e3, False),        # large weights
     (4, 2048, 4, 0.02, True),
+    (5, 96, 5, 0.02, False),        # K = 96: int4 affine's ragged last group of 32
+    (3, 4128, 6, 0.02, True),       # K = 64 * 64 + 32
 ]
 
 
@@ -151,7 +154,7 @@ def test_device_entry_validation_without_gpu(lib):
     assert _call_qmm(lib, codes=None) == -1
     assert _call_qmm(lib, fmt=2, g=0.0) == -1
     assert _call_qmm(lib, fmt=2, g=float("nan")) == -1
-    assert _call_qmm(lib, fmt=6, K=96) == -2
+    assert _call_qmm(lib, fmt=6, K=80) == -2
     assert b"multiple" in lib.qfmt_last_error()
     # empty problems are legal no-ops
     assert _call_qmm(lib, M=0) == 0

@@ -131,7 +131,7 @@ def test_qgemm_parity(fmt, m):
 def test_short_and_odd_k(fmt, m):
     # K of one block quantum and K that leave partial chunks / K steps; few terms
     # per output, so a per-weight rounding above the bound would show
-    for k in ((64, 192) if fmt == "int4_affine" else (32, 96, 160)):
+    for k in (32, 64, 96, 160, 192) if fmt == "int4_affine" else (32, 96, 160):   # int4: ragged last groups too
         n = 33 if m < 17 else 300
         c, s, g = _packed(fmt, n, k, seed=k)
         xb, xt = _x(m, k, seed=k + 1)
@@ -348,3 +348,34 @@ def test_chained_layers_read_the_previous_output(fmt, m):
         c, s, g = packed[i]
         ref, bound = oref.qmm_ref(fmt, c, s, g, xin, "bf16", m, n, k)
         _check_qmm(outs[i + 1], ref, bound, (fmt, m, "layer", i))
+
+
+@pytest.mark.parametrize("m", [1, 2, 5, 16, 40, 300])
+def test_int4_ragged_last_group_every_path(m):
+    # K = 64 * 32 + 32: the last int4-affine group holds 32 values (its own scale and bias)
+    fmt, n, k = "int4_affine", 136, 2080
+    c, s, g = _packed(fmt, n, k, seed=90 + m)
+    xb, xt = _x(m, k, seed=91 + m)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, m, k))
+    if m == 2:   # the float32-activation path over the same weights
+        xf = synth.activations_f32(m, k, seed=92)
+        out_f = q.qmm_ex(fmt, _dev(c), _dev(s), g, _dev(xf), n)
+        ref_f, bound_f = oref.qmm_ref(fmt, c, s, g, xf, "f32", m, n, k)
+        _check_qmm(out_f, ref_f, bound_f, (fmt, "f32", k))
+    if m == 1:
+        want = oref.dequant_f32(fmt, c, s, g, n, k)
+        got = q.qfmt_dequant(fmt, _dev(c), _dev(s), g, n, k).cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+
+def test_int4_ragged_last_group_long_k_fallback():
+    # two rows of K = 64 * 384 + 32: past the single-pass GEMVs' shared-memory plans
+    fmt, m, n, k = "int4_affine", 2, 48, 24608
+    c, s, g = _packed(fmt, n, k, seed=95)
+    xb, xt = _x(m, k, seed=96)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, m, k))

@@ -365,8 +365,8 @@ def run_reference(args):
 # kernel reports null until it is captured again).
 TRAFFIC = {
     "kernel_source": "block_scaled_quantized_spec_gb300/csrc/qgemv_m2.cu",
-    "sha256_16": "d335d6e7c41ff0dc",
-    "bytes": 8939776,
+    "sha256_16": "99b7609ee8f3e385",
+    "bytes": 8940032,
     "profile": "profiles/qgemv_m2_mxfp4_M1_N4096_K4096.md",
 }
 

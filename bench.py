@@ -225,6 +225,23 @@ def time_graph(graph, steps, warmup, world, clocks_index=None):
     return max_over_ranks(ms, world), (clk.summary() if clk else None)
 
 
+def step_spread(graph, steps):
+    """Per-step device times of a second pass (events around each replay): p10 / p50 / p90 in ms."""
+    import statistics
+    import torch
+    st = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(st)
+    for i in range(steps):
+        graph.replay()
+        ev[i + 1].record(st)
+    torch.cuda.synchronize()
+    t = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+    q = statistics.quantiles(t, n=10, method="inclusive") if len(t) > 1 else [t[0]] * 9
+    return {"p10": round(q[0], 4), "p50": round(statistics.median(t), 4), "p90": round(q[8], 4), "steps": steps}
+
+
 def copies_for(nbytes, m):
     if m >= 128:
         return 2
@@ -527,6 +544,7 @@ def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3):
     g = prob.graph()
     ms, _ = time_graph(g, steps, warmup, 1)
     per = ms / copies
+    prob_flops_per_byte = prob.flops / nbytes
     row = {"fmt": fmt, "M": m, "N": n, "K": k, "us": round(per * 1e3, 2), "copies": copies}
     gbs = nbytes / (per * 1e-3) / 1e9
     tfl = prob.flops / (per * 1e-3) / 1e12
@@ -537,6 +555,9 @@ def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3):
         fp_peak = {"mxfp8_e4m3": 2 * bf16, "mxfp8_e5m2": 2 * bf16, "nvfp8": 2 * bf16}.get(fmt, 6 * bf16)
         row["bf16_frac"] = round(tfl / bf16, 4)
         row["native_peak_frac"] = round(tfl / fp_peak, 4)
+        # against the roofline at this arithmetic intensity: min(bf16 peak, FLOP/byte x HBM)
+        ridge = min(bf16, prob_flops_per_byte * hbm / 1e3)
+        row["roofline_frac"] = round(tfl / ridge, 4)
     del prob, g
     torch.cuda.empty_cache()
     return row
@@ -576,6 +597,7 @@ def main():
     prob = Problem(fmt, m, n, k, copies, seed=rank)
     graph = prob.graph()
     ms, clk = time_graph(graph, args.steps, args.warmup, world, clocks_index=local)
+    spread = step_spread(graph, max(args.steps, 10))
     total_bytes = world * copies * nbytes
     value = total_bytes / (ms * 1e-3) / 1e9
     e2e_ms, h2d, d2h = measure_e2e(prob, max(3, args.steps // 2), 2)
@@ -593,6 +615,7 @@ def main():
         "e2e": {"value": round(world * copies * nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "per step (one CUDA graph): one pinned H2D of all layers' X, L qmm calls, one D2H of all outputs; weights resident"},
+        "step_ms_spread": spread,
         "gpu_launches": copies * args.steps,
         "clocks": clk,
     }

@@ -25,6 +25,9 @@ Readings taken where the pages are silent (each is listed in the design doc):
   largest micro-scale lands at 448; micro-scale u = E4M3_RNE((amax_b / 6) /
   global); an all-zero block stores u = E4M3(1.0) = 0x38.
 * Element encoders round to nearest, ties to the even code, saturating.
+* nvfp8_f16, the fp16-scale twin of nvfp8 (PR #250, "fp16-scale axis": the
+  same element and block, the per-block scale stored as a 2-byte IEEE half,
+  rounded to nearest even with subnormals kept): scale = half(amax / 448).
 * int4 affine (MLX style, group 64): s = (max - min) / 15 (1.0 when 0), stored
   as bf16 (RNE); bias = bf16(min); q = clamp(round_half_away((w - b) / s), 0, 15);
   scale and bias are interleaved per group as bf16 pairs [N, ceil(K/64), 2].
@@ -40,14 +43,16 @@ import numpy as np
 
 from . import codec
 
-FORMATS = ("mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8", "int4_affine")
+FORMATS = ("mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8", "int4_affine", "nvfp8_f16")
 
-BLOCK = {"mxfp4": 32, "nvfp4": 16, "mxfp8_e4m3": 32, "mxfp8_e5m2": 32, "nvfp8": 16, "int4_affine": 64}
-ELEM_BITS = {"mxfp4": 4, "nvfp4": 4, "mxfp8_e4m3": 8, "mxfp8_e5m2": 8, "nvfp8": 8, "int4_affine": 4}
-SCALE_BYTES = {"mxfp4": 1, "nvfp4": 1, "mxfp8_e4m3": 1, "mxfp8_e5m2": 1, "nvfp8": 4, "int4_affine": 4}
+BLOCK = {"mxfp4": 32, "nvfp4": 16, "mxfp8_e4m3": 32, "mxfp8_e5m2": 32, "nvfp8": 16, "int4_affine": 64,
+         "nvfp8_f16": 16}
+ELEM_BITS = {"mxfp4": 4, "nvfp4": 4, "mxfp8_e4m3": 8, "mxfp8_e5m2": 8, "nvfp8": 8, "int4_affine": 4, "nvfp8_f16": 8}
+SCALE_BYTES = {"mxfp4": 1, "nvfp4": 1, "mxfp8_e4m3": 1, "mxfp8_e5m2": 1, "nvfp8": 4, "int4_affine": 4,
+               "nvfp8_f16": 2}
 _ELEM = {"mxfp4": ("e2m1", codec.E2M1_MAX), "nvfp4": ("e2m1", codec.E2M1_MAX),
          "mxfp8_e4m3": ("e4m3", codec.E4M3_MAX), "mxfp8_e5m2": ("e5m2", codec.E5M2_MAX),
-         "nvfp8": ("e4m3", codec.E4M3_MAX)}
+         "nvfp8": ("e4m3", codec.E4M3_MAX), "nvfp8_f16": ("e4m3", codec.E4M3_MAX)}
 
 F32 = np.float32
 
@@ -123,6 +128,14 @@ def pack(fmt: str, w: np.ndarray):
         ucode = np.where(amax > 0, ucode, np.uint8(0x38)).astype(np.uint8)
         eff = (codec.E4M3_TABLE[ucode].astype(F32) * glob).astype(F32)
         scales = ucode
+    elif fmt == "nvfp8_f16":
+        # the fp16-scale twin: amax / 448 rounded once to an IEEE half (nearest
+        # even, subnormals kept, overflow to inf, rejected below)
+        s = np.where(amax > 0, amax / F32(maxf), F32(1.0)).astype(F32)
+        with np.errstate(over="ignore"):
+            h = s.astype(np.float16)
+        eff = h.astype(F32)
+        scales = h
     else:  # nvfp8: float32 scale stored raw
         s = np.where(amax > 0, amax / F32(maxf), F32(1.0)).astype(F32)
         eff = s

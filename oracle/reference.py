@@ -15,7 +15,9 @@ Value definitions (page title, then the section):
   ``thunk/ops/quant.rs`` ``dequant_matmul_nvfp4`` (E2M1 nibble times the E4M3
   block scale times the global FP32 scale, block 16 along K).  The inner
   product is exact, so the single float32 rounding is well defined.
-* nvfp8: w = e4m3(code) * scale_f32 (block 16) -- PR #250 format list.
+* nvfp8: w = e4m3(code) * scale_f32 (block 16) -- PR #250 format list; its
+  fp16-scale twin nvfp8_f16 the same with the scale an IEEE half -- PR #250,
+  the fp16-scale axis.
 * int4 affine: w = scale * q + bias with q the LSB-first nibble, group 64 --
   metaltile-std ``tests/qmm_gpu_correctness.rs``, ``cpu_qmm_reference``;
   scale and bias are bf16.  float64 evaluation of s*q + b is exact or, when
@@ -41,7 +43,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import codec
-from .pack import BLOCK, ELEM_BITS, FORMATS
+from .pack import BLOCK, ELEM_BITS, FORMATS, SCALE_BYTES
 
 BOUND_REL = 2e-3
 BOUND_ABS = 1e-6
@@ -73,6 +75,8 @@ def block_scales(fmt: str, scales: np.ndarray, global_scale: float, n: int, k: i
         return codec.E4M3_TABLE[s.reshape(n, nb)], None
     if fmt == "nvfp8":
         return np.ascontiguousarray(s).view(np.float32).reshape(n, nb).astype(np.float64), None
+    if fmt == "nvfp8_f16":
+        return np.ascontiguousarray(s).view(np.float16).reshape(n, nb).astype(np.float64), None
     pair = np.ascontiguousarray(s).view(np.uint16).reshape(n, nb, 2)
     return codec.decode_bf16(pair[..., 0]), codec.decode_bf16(pair[..., 1])
 
@@ -80,7 +84,7 @@ def block_scales(fmt: str, scales: np.ndarray, global_scale: float, n: int, k: i
 def element_values(fmt: str, codes: np.ndarray) -> np.ndarray:
     if fmt in ("mxfp4", "nvfp4"):
         return codec.E2M1_TABLE[codes]
-    if fmt in ("mxfp8_e4m3", "nvfp8"):
+    if fmt in ("mxfp8_e4m3", "nvfp8", "nvfp8_f16"):
         return codec.E4M3_TABLE[codes]
     if fmt == "mxfp8_e5m2":
         return codec.E5M2_TABLE[codes]
@@ -134,7 +138,7 @@ def qmm_ref_sampled(fmt, codes, scales, global_scale, x, x_dtype, m, n, k, rows,
     cols = np.asarray(cols)
     uniq, inv = np.unique(cols, return_inverse=True)
     per_row_codes = ELEM_BITS[fmt] * k // 8
-    per_row_scales = -(-k // BLOCK[fmt]) * (4 if fmt in ("nvfp8", "int4_affine") else 1)
+    per_row_scales = -(-k // BLOCK[fmt]) * SCALE_BYTES[fmt]
     c = np.asarray(codes, dtype=np.uint8).reshape(n, per_row_codes)[uniq]
     s = np.asarray(scales, dtype=np.uint8).reshape(n, per_row_scales)[uniq]
     w = dequant_exact(fmt, c, s, global_scale, len(uniq), k)[inv]

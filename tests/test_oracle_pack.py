@@ -21,7 +21,7 @@ def _elem_values_lib(fmt, codes_nk):
         e, m = c3 >> 1, c3 & 1
         two_m = np.where(e == 0, m, (m + 2) * (2 ** np.maximum(e - 1, 0)))
         return (1 - 2 * (c >> 3)) * two_m / 2.0
-    if fmt in ("mxfp8_e4m3", "nvfp8"):
+    if fmt in ("mxfp8_e4m3", "nvfp8", "nvfp8_f16"):
         return torch.from_numpy(codes_nk.astype(np.uint8)).view(torch.float8_e4m3fn).double().numpy()
     if fmt == "mxfp8_e5m2":
         return (codes_nk.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
@@ -37,7 +37,7 @@ def test_byte_sizes():
         c, s, g = pack.pack(fmt, w)
         bits = 4 if fmt in ("mxfp4", "nvfp4", "int4_affine") else 8
         assert c.nbytes == n * k * bits // 8 == pack.codes_nbytes(fmt, n, k)
-        per_scale = {"nvfp8": 4, "int4_affine": 4}.get(fmt, 1)
+        per_scale = {"nvfp8": 4, "int4_affine": 4, "nvfp8_f16": 2}.get(fmt, 1)
         assert s.nbytes == n * (k // pack.BLOCK[fmt]) * per_scale == pack.scales_nbytes(fmt, n, k)
         assert c.dtype == np.uint8 and s.dtype == np.uint8 and isinstance(g, np.float32)
 
@@ -68,6 +68,8 @@ def test_zero_blocks():
             assert (s == 0x38).all() and g == 1.0
         elif fmt == "nvfp8":
             assert (s.view(np.float32) == 1.0).all()
+        elif fmt == "nvfp8_f16":
+            assert (s.view(np.float16) == 1.0).all()
         else:
             pair = s.view(np.uint16).reshape(n, -1, 2)
             assert (pair[..., 0] == 0x3F80).all() and (pair[..., 1] == 0).all()
@@ -120,7 +122,7 @@ def test_value_idempotence(fmt):
 
 
 FLOORS = {"mxfp4": 0.98, "nvfp4": 0.98, "int4_affine": 0.99,
-          "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999}
+          "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999, "nvfp8_f16": 0.999}
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -135,7 +137,7 @@ def test_cosine_floor(fmt):
     assert cos >= FLOORS[fmt], (fmt, cos)
 
 
-@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8"])
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8", "nvfp8_f16"])
 def test_elements_are_nearest_grid_points(fmt):
     # Brute force over every code: each dequantized element is a closest point
     # of {value(code) * eff} to w (ties allowed either way), eff the block's effective scale.
@@ -176,7 +178,7 @@ def test_nvfp4_two_level_global():
 
 def test_no_special_codes_emitted():
     n, k = 64, 512
-    for fmt in ("mxfp8_e4m3", "nvfp8", "mxfp8_e5m2"):
+    for fmt in ("mxfp8_e4m3", "nvfp8", "mxfp8_e5m2", "nvfp8_f16"):
         w = synth.weights(n, k, seed=23) * np.float32(1e3)
         c, s, g = pack.pack(fmt, w)
         if fmt == "mxfp8_e5m2":
@@ -211,3 +213,24 @@ def test_pack_rejects_bad_input():
         pack.pack("mxfp4", np.zeros((1, 48), np.float32))
     with pytest.raises(ValueError):
         pack.pack("bogus", np.zeros((1, 64), np.float32))
+
+
+def test_nvfp8_f16_scales_are_rounded_halves_with_subnormals():
+    # PR #250 fp16-scale axis: the scale is amax / 448 rounded to nearest even as
+    # an IEEE half, subnormals kept (tiny blocks must not flush to zero).
+    n, k = 4, 64
+    w = synth.weights(n, k, seed=31)
+    w[1] *= np.float32(1e-2)                      # amax / 448 in the half subnormal range
+    w[2] *= np.float32(1e3)
+    c, s, g = pack.pack("nvfp8_f16", w)
+    amax = np.abs(w).reshape(n, k // 16, 16).max(axis=2)
+    want = (amax / np.float32(448.0)).astype(np.float32).astype(np.float16)
+    got = s.view(np.float16).reshape(n, k // 16)
+    assert np.array_equal(got, want)
+    assert (np.abs(got[1].astype(np.float64)) < 2.0 ** -14).all() and (got[1] > 0).all()
+    # and a row of the twin dequantizes like nvfp8 given the same (half-exact) scales
+    ref = reference.dequant_exact("nvfp8_f16", c, s, g, n, k)
+    s32 = got.astype(np.float32)
+    again = reference.dequant_exact("nvfp8", c, s32.view(np.uint8).reshape(n, -1), 1.0, n, k)
+    assert np.array_equal(ref, again)
+

@@ -35,7 +35,7 @@ def _lib_elem(fmt, c):
         e, m = c3 >> 1, c3 & 1
         two_m = m if e == 0 else (m + 2) * 2 ** (e - 1)
         return Fraction(s * two_m, 2)
-    if fmt in ("mxfp8_e4m3", "nvfp8"):
+    if fmt in ("mxfp8_e4m3", "nvfp8", "nvfp8_f16"):
         v = torch.tensor([c], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()
         return Fraction(v)
     if fmt == "mxfp8_e5m2":
@@ -51,6 +51,8 @@ def _lib_scale(fmt, sbytes, n, b):
         return Fraction(v), Fraction(0)
     if fmt == "nvfp8":
         return Fraction(float(np.frombuffer(bytes(sbytes[n][4 * b:4 * b + 4]), "<f4")[0])), Fraction(0)
+    if fmt == "nvfp8_f16":
+        return Fraction(float(np.frombuffer(bytes(sbytes[n][2 * b:2 * b + 2]), "<f2")[0])), Fraction(0)
     raw = bytes(sbytes[n][4 * b:4 * b + 4])
     s_bits, b_bits = np.frombuffer(raw, "<u2")
     f = lambda h: Fraction(float((np.array([h], np.uint32) << 16).view(np.float32)[0]))  # noqa: E731

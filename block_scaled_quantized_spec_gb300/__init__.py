@@ -24,7 +24,8 @@ __all__ = [
     "qfmt_version", "qfmt_device_status", "qfmt_debug_set",
 ]
 
-FORMATS = {"mxfp4": 1, "nvfp4": 2, "mxfp8_e4m3": 3, "mxfp8_e5m2": 4, "nvfp8": 5, "int4_affine": 6}
+FORMATS = {"mxfp4": 1, "nvfp4": 2, "mxfp8_e4m3": 3, "mxfp8_e5m2": 4, "nvfp8": 5, "int4_affine": 6,
+           "nvfp8_f16": 7}
 F32, BF16 = 0, 1
 STATUS = {0: "QFMT_OK", -1: "QFMT_EINVAL", -2: "QFMT_ESHAPE", -3: "QFMT_EALIGN", -4: "QFMT_EUNSUPPORTED",
           -5: "QFMT_ECUDA", -6: "QFMT_ETIMEOUT", -7: "QFMT_ENONFINITE", -8: "QFMT_ENOSPACE", -9: "QFMT_EINDEX"}

@@ -22,7 +22,7 @@
 
 namespace qfmt_dev {
 
-enum Fmt { MXFP4 = 1, NVFP4 = 2, MXFP8_E4M3 = 3, MXFP8_E5M2 = 4, NVFP8 = 5, INT4_AFFINE = 6 };
+enum Fmt { MXFP4 = 1, NVFP4 = 2, MXFP8_E4M3 = 3, MXFP8_E5M2 = 4, NVFP8 = 5, INT4_AFFINE = 6, NVFP8_F16 = 7 };
 
 template <int F> struct FmtTraits;
 template <> struct FmtTraits<MXFP4> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 1; };
@@ -31,6 +31,19 @@ template <> struct FmtTraits<MXFP8_E4M3> { static constexpr bool four = false; s
 template <> struct FmtTraits<MXFP8_E5M2> { static constexpr bool four = false; static constexpr int block = 32; static constexpr int sbytes = 1; };
 template <> struct FmtTraits<NVFP8> { static constexpr bool four = false; static constexpr int block = 16; static constexpr int sbytes = 4; };
 template <> struct FmtTraits<INT4_AFFINE> { static constexpr bool four = true; static constexpr int block = 64; static constexpr int sbytes = 4; };
+template <> struct FmtTraits<NVFP8_F16> { static constexpr bool four = false; static constexpr int block = 16; static constexpr int sbytes = 2; };
+
+// nvfp8 and its fp16-scale twin: E4M3 elements, one scale per 16 along K
+template <int F>
+constexpr bool is_nv8() { return F == NVFP8 || F == NVFP8_F16; }
+
+// Block scale idx of an nvfp8 scale array as float32: the stored float32, or
+// the (exact) float32 of the stored IEEE half.
+template <int F>
+__device__ __forceinline__ float nv8_scale(const uint8_t* scales, int64_t idx) {
+  if constexpr (F == NVFP8) return __ldg(reinterpret_cast<const float*>(scales) + idx);
+  else return __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(scales) + idx)));
+}
 
 // ------------------------------------------------------------------ exact ---
 
@@ -194,8 +207,8 @@ __device__ __forceinline__ PieceScale load_piece_scale(const uint8_t* scales, in
     s.a = __ldg(scales + base + k0 / 32);
   } else if constexpr (F == NVFP4) {
     s.a = __ldg(reinterpret_cast<const unsigned short*>(scales + base + k0 / 16));
-  } else if constexpr (F == NVFP8) {
-    s.a = __ldg(reinterpret_cast<const uint32_t*>(scales) + base + k0 / 16);
+  } else if constexpr (is_nv8<F>()) {
+    s.a = __float_as_uint(nv8_scale<F>(scales, base + k0 / 16));
   } else {
     s.a = __ldg(reinterpret_cast<const uint32_t*>(scales) + base + k0 / 64);
   }
@@ -255,7 +268,7 @@ __device__ __forceinline__ void decode_piece(const uint4& v, const PieceScale& p
         m2 = bf16x2_splat(pow2_bf16(b - 127));
         two = true;
       }
-    } else {  // NVFP8: float32 scale rounded once to bf16
+    } else {  // nvfp8 (either scale storage): the float32 scale rounded once to bf16
       const float s = __uint_as_float(ps.a);
       if (fabsf(s) < 128.0f) {
         m1 = bf16x2_splat(f32_to_bf16bits(s * 0x1p120f));
@@ -326,7 +339,7 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
 template <int F>
 __device__ __forceinline__ void decode_piece_hilo(const uint4& v, const PieceScale& ps, uint32_t* hi, uint32_t* lo) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  if constexpr (F == NVFP8) {
+  if constexpr (is_nv8<F>()) {
     const float s = __uint_as_float(ps.a);
     #pragma unroll
     for (int j = 0; j < 4; ++j) {

@@ -26,7 +26,7 @@ __device__ __forceinline__ float dq_value(uint32_t code, float s, float b, float
   if constexpr (F == NVFP4) return __fmul_rn(__fmul_rn(e2m1_f32(code), s), glob);   // (e2m1 * e4m3) exact
   if constexpr (F == MXFP8_E4M3) return __fmul_rn(e4m3_f32(code), s);
   if constexpr (F == MXFP8_E5M2) return __fmul_rn(e5m2_f32(code), s);
-  if constexpr (F == NVFP8) return __fmul_rn(e4m3_f32(code), s);
+  if constexpr (is_nv8<F>()) return __fmul_rn(e4m3_f32(code), s);
   return __fmaf_rn(s, float(code), b);                                               // INT4_AFFINE
 }
 
@@ -36,7 +36,7 @@ __device__ __forceinline__ void dq_scale(const uint8_t* scales, int64_t idx, flo
   b = 0.0f;
   if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) s = e8m0_f32(scales[idx]);
   else if constexpr (F == NVFP4) s = e4m3_f32(scales[idx]);
-  else if constexpr (F == NVFP8) s = reinterpret_cast<const float*>(scales)[idx];
+  else if constexpr (is_nv8<F>()) s = nv8_scale<F>(scales, idx);
   else {
     const uint32_t p = reinterpret_cast<const uint32_t*>(scales)[idx];
     s = bf16bits_f32(p & 0xFFFFu);
@@ -123,6 +123,7 @@ cudaError_t launch_dequant(int fmt, const void* codes, const void* scales, float
     case MXFP8_E4M3: return launch_dequant_fmt<MXFP8_E4M3>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case MXFP8_E5M2: return launch_dequant_fmt<MXFP8_E5M2>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case NVFP8: return launch_dequant_fmt<NVFP8>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case NVFP8_F16: return launch_dequant_fmt<NVFP8_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     default: return launch_dequant_fmt<INT4_AFFINE>(codes, scales, glob, out, out_bf16, N, K, st, sms);
   }
 }

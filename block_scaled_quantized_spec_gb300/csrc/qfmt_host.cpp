@@ -35,12 +35,12 @@ int fail(int status, const char* fmt, ...) {
 
 void clear_error() { g_err[0] = '\0'; }
 
-bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_INT4_AFFINE; }
+bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_NVFP8_F16; }
 
 int block_of(int fmt) {
   switch (fmt) {
     case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: return 32;
-    case QFMT_NVFP4: case QFMT_NVFP8: return 16;
+    case QFMT_NVFP4: case QFMT_NVFP8: case QFMT_NVFP8_F16: return 16;
     case QFMT_INT4_AFFINE: return 64;
     default: return 0;
   }
@@ -48,7 +48,9 @@ int block_of(int fmt) {
 
 bool is_4bit(int fmt) { return fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4 || fmt == QFMT_INT4_AFFINE; }
 
-int scale_entry_bytes(int fmt) { return (fmt == QFMT_NVFP8 || fmt == QFMT_INT4_AFFINE) ? 4 : 1; }
+int scale_entry_bytes(int fmt) {
+  return (fmt == QFMT_NVFP8 || fmt == QFMT_INT4_AFFINE) ? 4 : (fmt == QFMT_NVFP8_F16 ? 2 : 1);
+}
 
 int check_group(int fmt, int group) {
   if (!valid_format(fmt)) return fail(QFMT_EINVAL, "unknown format %d", fmt);
@@ -278,6 +280,13 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
             const uint32_t u = amax > 0.0f ? enc_e4m3((amax / 6.0f) / glob) : 0x38u;
             sb[n * nb + b] = uint8_t(u);
             eff = dec_e4m3(u) * glob;
+            break;
+          }
+          case QFMT_NVFP8_F16: {  // the scale stored as an IEEE half, rounded to nearest even
+            const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+            const _Float16 h = static_cast<_Float16>(s);
+            std::memcpy(sb + (n * nb + b) * 2, &h, 2);
+            eff = static_cast<float>(h);
             break;
           }
           default: {  // QFMT_NVFP8

@@ -13,6 +13,11 @@
  *   QFMT_MXFP8_E5M2     E5M2 (8-bit)       32     E8M0 byte
  *   QFMT_NVFP8          E4M3 (8-bit)       16     FP32 (4 bytes)
  *   QFMT_INT4_AFFINE    unsigned 4-bit q   64     bf16 scale + bf16 bias (4 bytes)
+ *   QFMT_NVFP8_F16      E4M3 (8-bit)       16     IEEE half (2 bytes): the fp16-scale
+ *                                                 twin of nvfp8 (PR #250: the same element
+ *                                                 and block, the scale stored as a 2-byte
+ *                                                 half, rounded to nearest even with
+ *                                                 subnormals kept)
  *
  * Memory layouts (all row-major, no padding, little-endian):
  *   codes   [N, K/2] bytes for 4-bit formats: element k of a row sits in byte
@@ -66,7 +71,8 @@ typedef enum {
   QFMT_MXFP8_E4M3 = 3,
   QFMT_MXFP8_E5M2 = 4,
   QFMT_NVFP8 = 5,
-  QFMT_INT4_AFFINE = 6
+  QFMT_INT4_AFFINE = 6,
+  QFMT_NVFP8_F16 = 7
 } qfmt_format;
 
 typedef enum { QFMT_F32 = 0, QFMT_BF16 = 1 } qfmt_dtype;

@@ -83,6 +83,8 @@ def test_dequant_all_codes_and_scales(fmt):
     elif fmt == "nvfp8":
         scales = np.concatenate([rng.standard_normal(sb // 4 - 4).astype(np.float32),
                                  np.array([1e-40, 3e38, 0.0, -2.5], np.float32)]).view(np.uint8)
+    elif fmt == "nvfp8_f16":   # every 32nd half bit pattern: subnormals, +-inf, NaNs, both signs
+        scales = np.arange(0, 65536, 32, dtype=np.uint16)[:sb // 2].view(np.uint8)
     else:
         sc = synth.f32_to_bf16_bits(rng.standard_normal(sb // 2).astype(np.float32) * 1e-2)
         scales = sc.view(np.uint8)

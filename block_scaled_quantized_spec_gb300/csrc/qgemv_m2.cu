@@ -27,6 +27,12 @@
 //    its E4M3 micro-scales to the f16 weights instead: E2M1 x E4M3 is exact in
 //    f16; its FP32 global scale is applied at the end);
 //  * per-warp sums meet in shared memory; one thread per output stores it.
+//
+// The same kernel serves three more forms of the decode step (template MODE):
+// expert-routed rows over a stacked weight (PR #250, MoE gather-qmm), up to
+// four weight matrices sharing the activations (the batched Q/K/V and 4-way
+// GEMVs) and an RMSNorm of the activations fused in front (the fused
+// RMSNorm + GEMV); see the description beside `Extra` below.
 #include <cuda_runtime.h>
 
 #include <atomic>

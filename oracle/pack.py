@@ -28,6 +28,10 @@ Readings taken where the pages are silent (each is listed in the design doc):
 * nvfp8_f16, the fp16-scale twin of nvfp8 (PR #250, "fp16-scale axis": the
   same element and block, the per-block scale stored as a 2-byte IEEE half,
   rounded to nearest even with subnormals kept): scale = half(amax / 448).
+* mxint8 (PR #250's MXINT axis: a symmetric signed integer element -- sign-
+  extended from its top bit, clamped to +-(2^(N-1) - 1) -- under an E8M0 scale
+  per 32): s = amax / 127 snapped up to a power of two as for mxfp8, q =
+  clamp(round_half_away(w / s), -127, 127) stored as a two's-complement byte.
 * int4 affine (MLX style, group 64): s = (max - min) / 15 (1.0 when 0), stored
   as bf16 (RNE); bias = bf16(min); q = clamp(round_half_away((w - b) / s), 0, 15);
   scale and bias are interleaved per group as bf16 pairs [N, ceil(K/64), 2].
@@ -43,16 +47,17 @@ import numpy as np
 
 from . import codec
 
-FORMATS = ("mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8", "int4_affine", "nvfp8_f16")
+FORMATS = ("mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8", "int4_affine", "nvfp8_f16", "mxint8")
 
 BLOCK = {"mxfp4": 32, "nvfp4": 16, "mxfp8_e4m3": 32, "mxfp8_e5m2": 32, "nvfp8": 16, "int4_affine": 64,
-         "nvfp8_f16": 16}
-ELEM_BITS = {"mxfp4": 4, "nvfp4": 4, "mxfp8_e4m3": 8, "mxfp8_e5m2": 8, "nvfp8": 8, "int4_affine": 4, "nvfp8_f16": 8}
+         "nvfp8_f16": 16, "mxint8": 32}
+ELEM_BITS = {"mxfp4": 4, "nvfp4": 4, "mxfp8_e4m3": 8, "mxfp8_e5m2": 8, "nvfp8": 8, "int4_affine": 4, "nvfp8_f16": 8,
+             "mxint8": 8}
 SCALE_BYTES = {"mxfp4": 1, "nvfp4": 1, "mxfp8_e4m3": 1, "mxfp8_e5m2": 1, "nvfp8": 4, "int4_affine": 4,
-               "nvfp8_f16": 2}
+               "nvfp8_f16": 2, "mxint8": 1}
 _ELEM = {"mxfp4": ("e2m1", codec.E2M1_MAX), "nvfp4": ("e2m1", codec.E2M1_MAX),
          "mxfp8_e4m3": ("e4m3", codec.E4M3_MAX), "mxfp8_e5m2": ("e5m2", codec.E5M2_MAX),
-         "nvfp8": ("e4m3", codec.E4M3_MAX), "nvfp8_f16": ("e4m3", codec.E4M3_MAX)}
+         "nvfp8": ("e4m3", codec.E4M3_MAX), "nvfp8_f16": ("e4m3", codec.E4M3_MAX), "mxint8": ("int8", 127.0)}
 
 F32 = np.float32
 
@@ -115,7 +120,7 @@ def pack(fmt: str, w: np.ndarray):
         return _pack_int4_affine(wb, n, k)
 
     elem, maxf = _ELEM[fmt]
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8"):
         s = np.where(amax > 0, amax / F32(maxf), F32(1.0)).astype(F32)   # step 2
         scode = codec.e8m0_encode_ceil(s)                                  # step 3
         eff = codec.E8M0_TABLE[scode].astype(F32)                          # exact power of two
@@ -143,6 +148,10 @@ def pack(fmt: str, w: np.ndarray):
     if not np.all(np.isfinite(eff)):
         raise ValueError("scale overflows float32")
 
+    if elem == "int8":   # symmetric integer element: round half away from zero, clamp to +-127
+        v = (wb / eff[..., None]).astype(F32)
+        q = np.clip(_round_half_away(v), -127, 127).astype(np.int8)
+        return q.view(np.uint8).reshape(n, k), np.ascontiguousarray(scales).view(np.uint8).reshape(n, -1), F32(glob)
     codes = _quantize(wb, eff, elem).reshape(n, k)                        # step 4
     codes_b = _pack_nibbles(codes) if ELEM_BITS[fmt] == 4 else codes.astype(np.uint8)
     scales_b = np.ascontiguousarray(scales).view(np.uint8).reshape(n, -1)

@@ -8,6 +8,8 @@
 
 Value definitions (page title, then the section):
 
+* mxint8: w = q * 2^(scale_bits - 127), q the signed byte -- PR #250, the
+  MXINT axis (symmetric integer element, E8M0 block scale).
 * mxfp4 / mxfp8: w = elem(code) * 2^(scale_bits - 127) -- metaltile PR #250,
   commit "First spec-conformant block-scaled dequant kernel: mt_mxfp4_dequant"
   and the commit completing the mxfp8 dequant kernels.
@@ -69,7 +71,7 @@ def block_scales(fmt: str, scales: np.ndarray, global_scale: float, n: int, k: i
     """
     nb = -(-k // BLOCK[fmt])
     s = np.asarray(scales, dtype=np.uint8).reshape(n, -1)
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8"):
         return codec.E8M0_TABLE[s.reshape(n, nb)], None
     if fmt == "nvfp4":
         return codec.E4M3_TABLE[s.reshape(n, nb)], None
@@ -88,6 +90,8 @@ def element_values(fmt: str, codes: np.ndarray) -> np.ndarray:
         return codec.E4M3_TABLE[codes]
     if fmt == "mxfp8_e5m2":
         return codec.E5M2_TABLE[codes]
+    if fmt == "mxint8":                                  # the two's-complement byte
+        return codes.astype(np.uint8).view(np.int8).astype(np.float64)
     return codes.astype(np.float64)                      # int4 affine: q itself
 
 

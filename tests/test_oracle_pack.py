@@ -10,7 +10,7 @@ from block_scaled_quantized_spec_gb300 import synth
 from oracle import codec, pack, reference
 
 FMTS = pack.FORMATS
-MX = ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2")
+MX = ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2")          # float elements under E8M0 (mxint8 separately)
 
 
 def _elem_values_lib(fmt, codes_nk):
@@ -25,6 +25,8 @@ def _elem_values_lib(fmt, codes_nk):
         return torch.from_numpy(codes_nk.astype(np.uint8)).view(torch.float8_e4m3fn).double().numpy()
     if fmt == "mxfp8_e5m2":
         return (codes_nk.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
+    if fmt == "mxint8":
+        return torch.from_numpy(codes_nk.astype(np.uint8)).view(torch.int8).double().numpy()
     return codes_nk.astype(np.float64)
 
 
@@ -62,7 +64,7 @@ def test_zero_blocks():
     for fmt in FMTS:
         c, s, g = pack.pack(fmt, w)
         assert not c.any(), fmt
-        if fmt in MX:
+        if fmt in MX or fmt == "mxint8":
             assert (s == 127).all()
         elif fmt == "nvfp4":
             assert (s == 0x38).all() and g == 1.0
@@ -122,7 +124,7 @@ def test_value_idempotence(fmt):
 
 
 FLOORS = {"mxfp4": 0.98, "nvfp4": 0.98, "int4_affine": 0.99,
-          "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999, "nvfp8_f16": 0.999}
+          "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999, "nvfp8_f16": 0.999, "mxint8": 0.999}
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -233,4 +235,28 @@ def test_nvfp8_f16_scales_are_rounded_halves_with_subnormals():
     s32 = got.astype(np.float32)
     again = reference.dequant_exact("nvfp8", c, s32.view(np.uint8).reshape(n, -1), 1.0, n, k)
     assert np.array_equal(ref, again)
+
+
+def test_mxint8_exactly_representable_roundtrip():
+    # W = q * 2^e with q in [-127, 127] and +-127 present in every block: the
+    # packer must return exactly those bytes and scales.
+    rng = np.random.default_rng(37)
+    n, k = 6, 256
+    q = rng.integers(-127, 128, size=(n, k))
+    q[:, ::32] = 127 * rng.choice([-1, 1], size=(n, k // 32))
+    e = rng.integers(-30, 20, size=(n, k // 32))
+    w = (q * np.repeat(2.0 ** e, 32, axis=1)).astype(np.float32)
+    c, s, g = pack.pack("mxint8", w)
+    assert np.array_equal(c.view(np.int8), q.astype(np.int8))
+    assert np.array_equal(s.astype(np.int64), e + 127)
+    assert np.array_equal(reference.dequant_exact("mxint8", c, s, g, n, k), w.astype(np.float64))
+
+
+def test_mxint8_rounds_half_away_and_clamps():
+    w = np.zeros((1, 32), np.float32)
+    w[0, 0] = 127.0                          # scale 2^0
+    w[0, 1:5] = [2.5, -2.5, 126.5, -0.5]     # ties: away from zero
+    c, s, _ = pack.pack("mxint8", w)
+    assert s[0, 0] == 127
+    assert list(c.view(np.int8)[0, :5]) == [127, 3, -3, 127, -1]
 

@@ -40,11 +40,13 @@ def _lib_elem(fmt, c):
         return Fraction(v)
     if fmt == "mxfp8_e5m2":
         return Fraction(float(np.array([c << 8], np.uint16).view(np.float16)[0]))
+    if fmt == "mxint8":
+        return Fraction(c - 256 if c >= 128 else c)
     return Fraction(c)
 
 
 def _lib_scale(fmt, sbytes, n, b):
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8"):
         return Fraction(2) ** (int(sbytes[n][b]) - 127), Fraction(0)
     if fmt == "nvfp4":
         v = torch.tensor([int(sbytes[n][b])], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()

@@ -22,7 +22,7 @@
 
 namespace qfmt_dev {
 
-enum Fmt { MXFP4 = 1, NVFP4 = 2, MXFP8_E4M3 = 3, MXFP8_E5M2 = 4, NVFP8 = 5, INT4_AFFINE = 6, NVFP8_F16 = 7 };
+enum Fmt { MXFP4 = 1, NVFP4 = 2, MXFP8_E4M3 = 3, MXFP8_E5M2 = 4, NVFP8 = 5, INT4_AFFINE = 6, NVFP8_F16 = 7, MXINT8 = 8 };
 
 template <int F> struct FmtTraits;
 template <> struct FmtTraits<MXFP4> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 1; };
@@ -32,6 +32,14 @@ template <> struct FmtTraits<MXFP8_E5M2> { static constexpr bool four = false; s
 template <> struct FmtTraits<NVFP8> { static constexpr bool four = false; static constexpr int block = 16; static constexpr int sbytes = 4; };
 template <> struct FmtTraits<INT4_AFFINE> { static constexpr bool four = true; static constexpr int block = 64; static constexpr int sbytes = 4; };
 template <> struct FmtTraits<NVFP8_F16> { static constexpr bool four = false; static constexpr int block = 16; static constexpr int sbytes = 2; };
+template <> struct FmtTraits<MXINT8> { static constexpr bool four = false; static constexpr int block = 32; static constexpr int sbytes = 1; };
+
+// 8-bit elements under an E8M0 scale per 32 (mxfp8 E4M3/E5M2, mxint8), and
+// every E8M0-scaled format (those and mxfp4)
+template <int F>
+constexpr bool is_mx8() { return F == MXFP8_E4M3 || F == MXFP8_E5M2 || F == MXINT8; }
+template <int F>
+constexpr bool is_e8m0() { return F == MXFP4 || is_mx8<F>(); }
 
 // nvfp8 and its fp16-scale twin: E4M3 elements, one scale per 16 along K
 template <int F>
@@ -169,6 +177,39 @@ __device__ __forceinline__ void e5m2x4_bf16_raw(uint32_t w, uint32_t r[2]) {
   r[1] = ((w >> 3) & 0x0FE00FE0u) | (w & 0x80008000u);
 }
 
+// 4 signed-int8 codes -> bf16x2 {c0,c2} {c1,c3}, exact: each byte with its
+// sign bit flipped is 128 + q, placed under the float32 exponent of 2^23 and
+// rebased by 2^23 + 128 in float32, then packed (|q| <= 128 is exact in bf16).
+__device__ __forceinline__ void int8x4_bf16(uint32_t w, uint32_t r[2]) {
+  const uint32_t t = w ^ 0x80808080u;
+  float f[4];
+  #pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = __fsub_rn(__uint_as_float(0x4B000000u | ((t >> (8 * i)) & 0xFFu)), 8388736.0f);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r[0]) : "f"(f[2]), "f"(f[0]));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r[1]) : "f"(f[3]), "f"(f[1]));
+}
+
+// 4 8-bit codes (code i in byte i) -> f16x2 (c0,c1) (c2,c3), exact: E4M3 and
+// E5M2 by the hardware conversions; a signed int8 as the f16 1152 + q (its
+// byte with the sign bit flipped, under the exponent of 1024) less 1152.
+template <int F>
+__device__ __forceinline__ void elem8x4_f16(uint32_t w, uint32_t* r) {
+  if constexpr (F == MXINT8) {
+    const uint32_t t = w ^ 0x80808080u;
+    const uint32_t a = prmt(t, 0x64u, 0x4140u), b = prmt(t, 0x64u, 0x4342u);
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[1]) : "r"(b), "r"(0x64806480u));
+  } else if constexpr (F == MXFP8_E5M2) {
+    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.f16x2.e5m2x2 %0, h0;\n\tcvt.rn.f16x2.e5m2x2 %1, h1;}"
+        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
+  } else {
+    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;}"
+        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
+  }
+}
+
 // bf16 bits of 2^e for -133 <= e <= 127.
 __device__ __forceinline__ uint32_t pow2_bf16(int e) {
   return e >= -126 ? uint32_t(e + 127) << 7 : (0x40u >> (-127 - e));
@@ -203,7 +244,7 @@ __device__ __forceinline__ PieceScale load_piece_scale(const uint8_t* scales, in
   PieceScale s{0u, 0u};
   if (!ok) return s;
   const int64_t base = row * nblk;
-  if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+  if constexpr (is_e8m0<F>()) {
     s.a = __ldg(scales + base + k0 / 32);
   } else if constexpr (F == NVFP4) {
     s.a = __ldg(reinterpret_cast<const unsigned short*>(scales + base + k0 / 16));
@@ -256,8 +297,8 @@ __device__ __forceinline__ void decode_piece(const uint4& v, const PieceScale& p
     // applies the block scale when the combined factor fits bf16, else two.
     uint32_t m1, m2 = 0x3F803F80u;
     bool two = false;
-    if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {
-      constexpr int gap = F == MXFP8_E4M3 ? 120 : 112;
+    if constexpr (is_mx8<F>()) {
+      constexpr int gap = F == MXFP8_E4M3 ? 120 : (F == MXFP8_E5M2 ? 112 : 0);   // int8: the exact value
       const int b = int(ps.a);
       if (b == 255) {
         m1 = 0x7FC07FC0u;
@@ -282,6 +323,7 @@ __device__ __forceinline__ void decode_piece(const uint4& v, const PieceScale& p
     for (int j = 0; j < 4; ++j) {
       uint32_t r[2];
       if constexpr (F == MXFP8_E5M2) e5m2x4_bf16_raw(w[j], r);
+      else if constexpr (F == MXINT8) int8x4_bf16(w[j], r);
       else e4m3x4_bf16_raw(w[j], r);
       A[j][0] = hmul2(r[0], m1);
       A[j][1] = hmul2(r[1], m1);

@@ -26,6 +26,7 @@ __device__ __forceinline__ float dq_value(uint32_t code, float s, float b, float
   if constexpr (F == NVFP4) return __fmul_rn(__fmul_rn(e2m1_f32(code), s), glob);   // (e2m1 * e4m3) exact
   if constexpr (F == MXFP8_E4M3) return __fmul_rn(e4m3_f32(code), s);
   if constexpr (F == MXFP8_E5M2) return __fmul_rn(e5m2_f32(code), s);
+  if constexpr (F == MXINT8) return __fmul_rn(float(int8_t(uint8_t(code))), s);
   if constexpr (is_nv8<F>()) return __fmul_rn(e4m3_f32(code), s);
   return __fmaf_rn(s, float(code), b);                                               // INT4_AFFINE
 }
@@ -34,7 +35,7 @@ __device__ __forceinline__ float dq_value(uint32_t code, float s, float b, float
 template <int F>
 __device__ __forceinline__ void dq_scale(const uint8_t* scales, int64_t idx, float& s, float& b) {
   b = 0.0f;
-  if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) s = e8m0_f32(scales[idx]);
+  if constexpr (is_e8m0<F>()) s = e8m0_f32(scales[idx]);
   else if constexpr (F == NVFP4) s = e4m3_f32(scales[idx]);
   else if constexpr (is_nv8<F>()) s = nv8_scale<F>(scales, idx);
   else {
@@ -124,6 +125,7 @@ cudaError_t launch_dequant(int fmt, const void* codes, const void* scales, float
     case MXFP8_E5M2: return launch_dequant_fmt<MXFP8_E5M2>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case NVFP8: return launch_dequant_fmt<NVFP8>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case NVFP8_F16: return launch_dequant_fmt<NVFP8_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case MXINT8: return launch_dequant_fmt<MXINT8>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     default: return launch_dequant_fmt<INT4_AFFINE>(codes, scales, glob, out, out_bf16, N, K, st, sms);
   }
 }

@@ -35,11 +35,11 @@ int fail(int status, const char* fmt, ...) {
 
 void clear_error() { g_err[0] = '\0'; }
 
-bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_NVFP8_F16; }
+bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_MXINT8; }
 
 int block_of(int fmt) {
   switch (fmt) {
-    case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: return 32;
+    case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: return 32;
     case QFMT_NVFP4: case QFMT_NVFP8: case QFMT_NVFP8_F16: return 16;
     case QFMT_INT4_AFFINE: return 64;
     default: return 0;
@@ -179,7 +179,7 @@ using namespace qfmt;
 
 extern "C" {
 
-int qfmt_version(void) { return 101; }
+int qfmt_version(void) { return 102; }
 
 const char* qfmt_last_error(void) { return qfmt::g_err; }
 
@@ -268,8 +268,9 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
         for (int j = 0; j < blk; ++j) amax = std::max(amax, std::fabs(wb[j]));
         float eff;
         switch (fmt) {
-          case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: {
-            const float maxf = fmt == QFMT_MXFP4 ? 6.0f : (fmt == QFMT_MXFP8_E4M3 ? 448.0f : 57344.0f);
+          case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: {
+            const float maxf = fmt == QFMT_MXFP4 ? 6.0f
+                             : fmt == QFMT_MXFP8_E4M3 ? 448.0f : fmt == QFMT_MXINT8 ? 127.0f : 57344.0f;
             const float s = amax > 0.0f ? amax / maxf : 1.0f;
             const uint32_t code = enc_e8m0_ceil(s);
             sb[n * nb + b] = uint8_t(code);
@@ -301,6 +302,11 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
           uint32_t code = 0;
           if (eff != 0.0f) {
             const float v = wb[j] / eff;
+            if (fmt == QFMT_MXINT8) {  // symmetric: round half away from zero, clamp to +-127
+              code = uint32_t(uint8_t(int8_t(std::max(-127.0f, std::min(127.0f, std::round(v))))));
+              put_code(crow, b * blk + j, code, four);
+              continue;
+            }
             code = fmt == QFMT_MXFP8_E5M2 ? enc_e5m2(v)
                  : (fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4) ? enc_e2m1(v) : enc_e4m3(v);
           }

@@ -661,6 +661,7 @@ cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, floa
     case MXFP8_E5M2: return tc::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case NVFP8: return tc::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case NVFP8_F16: return tc::launch_fmt<NVFP8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXINT8: return tc::launch_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return tc::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }

@@ -65,19 +65,6 @@ __device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t r[4]) {
       : "r"(w));
 }
 
-// 4 E4M3 (or E5M2) codes -> f16x2 (c0,c1) (c2,c3).
-template <bool E5>
-__device__ __forceinline__ void f8x4_f16(uint32_t w, uint32_t r[2]) {
-  if constexpr (E5)
-    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
-        "cvt.rn.f16x2.e5m2x2 %0, h0;\n\tcvt.rn.f16x2.e5m2x2 %1, h1;}"
-        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
-  else
-    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;}"
-        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
-}
-
 // One E4M3 byte -> f16x2 with the value in both halves (exact).
 __device__ __forceinline__ uint32_t e4m3_f16x2_splat(uint32_t b) {
   uint32_t r;
@@ -222,7 +209,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
         const int64_t blk = int64_t(ks / BLK) + e;
         const bool ok = row < N && blk < nblk;
         const int64_t gi = int64_t(ok ? row : 0) * nblk + (ok ? blk : 0);
-        if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+        if constexpr (is_e8m0<F>()) {
           wsc[rr * sst + e] = ok ? e8m0_f32(__ldg(scales + gi)) : 0.0f;
         } else if constexpr (F == NVFP4) {
           wsc[rr * sst + e] = __uint_as_float(ok ? e4m3_f16x2_splat(__ldg(scales + gi)) : 0u);
@@ -390,8 +377,8 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
               }
             } else {
               uint32_t fa[2], fb[2];
-              f8x4_f16<F == MXFP8_E5M2>(wa, fa);
-              f8x4_f16<F == MXFP8_E5M2>(wb, fb);
+              elem8x4_f16<F>(wa, fa);
+              elem8x4_f16<F>(wb, fb);
               const float swa = is_nv8<F>() ? sca[sgm] : sca[sgm >> 1];
               const float swb = is_nv8<F>() ? scb[sgm] : scb[sgm >> 1];
               #pragma unroll
@@ -549,6 +536,7 @@ cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float g
     case MXFP8_E5M2: return gemv::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case NVFP8: return gemv::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case NVFP8_F16: return gemv::launch_fmt<NVFP8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXINT8: return gemv::launch_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     default: return gemv::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }

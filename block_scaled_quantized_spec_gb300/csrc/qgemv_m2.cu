@@ -48,7 +48,7 @@ constexpr int THREADS = WARPS * 32;
 // chunks per warp held in registers at a time: four 64-byte chunks (the whole
 // of a 4096-wide fp4 row share); the E8M0 8-bit formats hold eight
 template <int F>
-constexpr int chunks_in_flight() { return (F == MXFP8_E4M3 || F == MXFP8_E5M2) ? 8 : 4; }
+constexpr int chunks_in_flight() { return is_mx8<F>() ? 8 : 4; }
 // with W warps per CTA: 4-warp CTAs hold twice the 4-bit chunks per warp
 template <int F, int W>
 constexpr int chunks_per_warp() { return (W == 4 && FmtTraits<F>::four) ? 2 * chunks_in_flight<F>() : chunks_in_flight<F>(); }
@@ -81,19 +81,6 @@ __device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t r[4]) {
       : "r"(w));
 }
 
-// 4 E4M3 (or E5M2) codes -> f16x2 (c0,c1) (c2,c3).
-template <bool E5>
-__device__ __forceinline__ void f8x4_f16(uint32_t w, uint32_t* r) {
-  if constexpr (E5)
-    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
-        "cvt.rn.f16x2.e5m2x2 %0, h0;\n\tcvt.rn.f16x2.e5m2x2 %1, h1;}"
-        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
-  else
-    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;}"
-        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
-}
-
 __device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -116,8 +103,8 @@ __device__ __forceinline__ void frags8(const uint4& v, int q, uint32_t r[4]) {
     #pragma unroll
     for (int b = 0; b < 4; ++b) r[b] = ((w >> (4 * b)) & 0x000F000Fu) | 0x64006400u;
   } else {
-    f8x4_f16<F == MXFP8_E5M2>(word(v, 2 * q), r);
-    f8x4_f16<F == MXFP8_E5M2>(word(v, 2 * q + 1), r + 2);
+    elem8x4_f16<F>(word(v, 2 * q), r);
+    elem8x4_f16<F>(word(v, 2 * q + 1), r + 2);
   }
 }
 
@@ -309,7 +296,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
         cs[i].a0 = x0 | (x1 << 8) | (x2 << 16) | (x3 << 24);
       }
       cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
-    } else if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+    } else if constexpr (is_mx8<F>()) {
       const int e = k0 / 32;                                                  // a0, a0 + 1 share it
       const uint32_t x0 = c0 ? __ldg(sra + e) : 127u;
       const uint32_t x2 = c0 ? __ldg(srb + e) : 127u;
@@ -353,7 +340,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
 
   // Any E8M0 scale byte of this round equal to 0 or 255 sends the warp down the exact decode.
   bool exact = false;
-  if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+  if constexpr (is_e8m0<F>()) {
     bool sp = false;
     #pragma unroll
     for (int i = 0; i < P; ++i) sp |= has_byte_00_or_ff(cs[i].a0);
@@ -479,7 +466,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   float acc_a = 0.0f, acc_b = 0.0f;
   for (int r = 0; r < rounds; ++r) {
     if (r > 0) {   // this round's chunks were requested while the previous round computed
-      if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+      if constexpr (is_e8m0<F>()) {
         bool sp = false;
         #pragma unroll
         for (int i = 0; i < P; ++i) sp |= has_byte_00_or_ff(cs[i].a0);
@@ -554,7 +541,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
         acc_a = __fmaf_rn(__fmul_rn(q1, x1s), d[ii][1], acc_a);
         acc_b = __fmaf_rn(__fmul_rn(q2, x0s), d[ii][2], acc_b);
         acc_b = __fmaf_rn(__fmul_rn(q3, x1s), d[ii][3], acc_b);
-      } else if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {
+      } else if constexpr (is_mx8<F>()) {
         const uint32_t w4 = cs[i].a0;
         const float qa = exact ? e8m0_f32(w4 & 0xFFu) : e8m0_fast<0>(w4);
         const float qb = exact ? e8m0_f32((w4 >> 16) & 0xFFu) : e8m0_fast<2>(w4);
@@ -732,6 +719,7 @@ cudaError_t launch_qgemv_m2(int fmt, const void* codes, const void* scales, floa
     case MXFP8_E5M2: return gemv_m2::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case NVFP8: return gemv_m2::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case NVFP8_F16: return gemv_m2::launch_fmt<NVFP8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXINT8: return gemv_m2::launch_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_m2::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }
@@ -750,6 +738,7 @@ cudaError_t launch_qgemv_gather(int fmt, const void* codes, const void* scales, 
     case NVFP8: return gemv_m2::launch_gather_fmt<NVFP8>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
     case NVFP8_F16:
       return gemv_m2::launch_gather_fmt<NVFP8_F16>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    case MXINT8: return gemv_m2::launch_gather_fmt<MXINT8>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
     default:
       return gemv_m2::launch_gather_fmt<INT4_AFFINE>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
   }
@@ -795,6 +784,7 @@ cudaError_t launch_qgemv_multi(int fmt, int count, const void* const* codes, con
     case MXFP8_E5M2: QFMT_MULTI(MXFP8_E5M2);
     case NVFP8: QFMT_MULTI(NVFP8);
     case NVFP8_F16: QFMT_MULTI(NVFP8_F16);
+    case MXINT8: QFMT_MULTI(MXINT8);
     default: QFMT_MULTI(INT4_AFFINE);
   }
 #undef QFMT_MULTI

@@ -97,19 +97,6 @@ __device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t r[4]) {
       : "r"(w));
 }
 
-// 4 E4M3 (or E5M2) codes -> f16x2 (c0,c1) (c2,c3).
-template <bool E5>
-__device__ __forceinline__ void f8x4_f16(uint32_t w, uint32_t* r) {
-  if constexpr (E5)
-    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
-        "cvt.rn.f16x2.e5m2x2 %0, h0;\n\tcvt.rn.f16x2.e5m2x2 %1, h1;}"
-        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
-  else
-    asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;}"
-        : "=r"(r[0]), "=r"(r[1]) : "r"(w));
-}
-
 __device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -256,7 +243,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       }
       sc[i][0] = a;
       sc[i][1] = b;
-    } else if constexpr (F == MXFP8_E4M3 || F == MXFP8_E5M2) {              // segments 0-1 and 2-3 share a block
+    } else if constexpr (is_mx8<F>()) {                                     // segments 0-1 and 2-3 share a block
       uint32_t a = 0, b = 0;
       #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -404,7 +391,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       if (c < nch) {                                                        // uniform over the CTA
         float ac[NB][4], d[NB][4];
         constexpr bool per_seg = F == MXFP4 || is_nv8<F>();                   // a block per segment
-        constexpr bool per_pair = F == MXFP8_E4M3 || F == MXFP8_E5M2 || I4;  // a block per two segments
+        constexpr bool per_pair = is_mx8<F>() || I4;  // a block per two segments
         #pragma unroll
         for (int sg = 0; sg < 4; ++sg) {
           // this segment starts a scale block: its first MMA takes a zero accumulator
@@ -448,8 +435,8 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             }
           } else {
             uint32_t fa[2], fb[2];
-            f8x4_f16<F == MXFP8_E5M2>(wa[i][sg], fa);
-            f8x4_f16<F == MXFP8_E5M2>(wb[i][sg], fb);
+            elem8x4_f16<F>(wa[i][sg], fa);
+            elem8x4_f16<F>(wb[i][sg], fb);
             #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
               const uint2 xv = *reinterpret_cast<const uint2*>(xs + mrow[nb] * xst + kx);
@@ -459,7 +446,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
           }
           // block scales on the float32 MMA results (d rows g: e = 0, 1; g + 8: e = 2, 3)
           constexpr bool per_seg = F == MXFP4 || is_nv8<F>();                   // a block per segment
-          constexpr bool per_pair = F == MXFP8_E4M3 || F == MXFP8_E5M2 || I4;  // a block per two segments
+          constexpr bool per_pair = is_mx8<F>() || I4;  // a block per two segments
           if (per_seg || (per_pair && (sg & 1))) {
             const bool first = sg < (per_seg ? 1 : 2);                      // the chunk's first block
             float sa, sb, ba = 0.0f, bb = 0.0f, xm0[NB], xm1[NB];
@@ -630,6 +617,7 @@ cudaError_t launch_qgemv_mb(int fmt, const void* codes, const void* scales, floa
     case MXFP8_E5M2: return gemv_mb::launch_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case NVFP8: return gemv_mb::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case NVFP8_F16: return gemv_mb::launch_fmt<NVFP8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXINT8: return gemv_mb::launch_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_mb::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }

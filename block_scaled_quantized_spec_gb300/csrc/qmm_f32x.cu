@@ -16,6 +16,7 @@ __device__ __forceinline__ float exact_weight(uint32_t code, float s, float b) {
   if constexpr (F == MXFP4 || F == NVFP4) return __fmul_rn(e2m1_f32(code), s);
   if constexpr (F == MXFP8_E4M3 || is_nv8<F>()) return __fmul_rn(e4m3_f32(code), s);
   if constexpr (F == MXFP8_E5M2) return __fmul_rn(e5m2_f32(code), s);
+  if constexpr (F == MXINT8) return __fmul_rn(float(int8_t(uint8_t(code))), s);
   return __fmaf_rn(s, float(code), b);
 }
 
@@ -42,7 +43,7 @@ __global__ void __launch_bounds__(256) qmm_f32x_kernel(const uint8_t* __restrict
       const int k = k0 + i;
       const int64_t bi = n * nblk + k / T::block;
       float s, b = 0.0f;
-      if constexpr (F == MXFP4 || F == MXFP8_E4M3 || F == MXFP8_E5M2) s = e8m0_f32(scales[bi]);
+      if constexpr (is_e8m0<F>()) s = e8m0_f32(scales[bi]);
       else if constexpr (F == NVFP4) s = e4m3_f32(scales[bi]);
       else if constexpr (is_nv8<F>()) s = nv8_scale<F>(scales, bi);
       else {
@@ -93,6 +94,7 @@ cudaError_t launch_qmm_f32x(int fmt, const void* codes, const void* scales, floa
     case MXFP8_E5M2: return launch_f32x_fmt<MXFP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case NVFP8: return launch_f32x_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case NVFP8_F16: return launch_f32x_fmt<NVFP8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXINT8: return launch_f32x_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     default: return launch_f32x_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }

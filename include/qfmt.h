@@ -18,6 +18,12 @@
  *                                                 and block, the scale stored as a 2-byte
  *                                                 half, rounded to nearest even with
  *                                                 subnormals kept)
+ *   QFMT_MXINT8         signed int8 q      32     E8M0 byte: w = q * 2^(b-127), q the
+ *                                                 two's-complement byte (PR #250, the MXINT
+ *                                                 axis: a symmetric integer element; the
+ *                                                 packer clamps q to +-127 and rounds half
+ *                                                 away from zero; a stored -128 decodes as
+ *                                                 -128)
  *
  * Memory layouts (all row-major, no padding, little-endian):
  *   codes   [N, K/2] bytes for 4-bit formats: element k of a row sits in byte
@@ -72,7 +78,8 @@ typedef enum {
   QFMT_MXFP8_E5M2 = 4,
   QFMT_NVFP8 = 5,
   QFMT_INT4_AFFINE = 6,
-  QFMT_NVFP8_F16 = 7
+  QFMT_NVFP8_F16 = 7,
+  QFMT_MXINT8 = 8
 } qfmt_format;
 
 typedef enum { QFMT_F32 = 0, QFMT_BF16 = 1 } qfmt_dtype;

@@ -78,7 +78,7 @@ def test_dequant_all_codes_and_scales(fmt):
     cb = opack.codes_nbytes(fmt, n, k)
     codes = np.tile(np.arange(256, dtype=np.uint8), cb // 256 + 1)[:cb].reshape(n, -1)
     sb = opack.scales_nbytes(fmt, n, k)
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp4"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "nvfp4"):
         scales = np.tile(np.arange(256, dtype=np.uint8), sb // 256 + 1)[:sb]
     elif fmt == "nvfp8":
         scales = np.concatenate([rng.standard_normal(sb // 4 - 4).astype(np.float32),
@@ -262,7 +262,7 @@ def test_full_size_sampled(fmt, m, n, k, outl):
     assert (err <= bound + np.abs(got) * 2.0 ** -9).all(), float((err / bound).max())
 
 
-@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8_e4m3", "mxfp8_e5m2"])
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8"])
 @pytest.mark.parametrize("m", [1, 2, 5])
 def test_gemv_e8m0_special_scales(fmt, m):
     # E8M0 code 0 (2^-127, a float32 subnormal) among ordinary scales, then a

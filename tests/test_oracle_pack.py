@@ -25,7 +25,7 @@ def _elem_values_lib(fmt, codes_nk):
         return torch.from_numpy(codes_nk.astype(np.uint8)).view(torch.float8_e4m3fn).double().numpy()
     if fmt == "mxfp8_e5m2":
         return (codes_nk.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
-    if fmt == "mxint8":
+    if fmt in ("mxint8", "int8", "int8_f16"):
         return torch.from_numpy(codes_nk.astype(np.uint8)).view(torch.int8).double().numpy()
     return codes_nk.astype(np.float64)
 
@@ -39,7 +39,7 @@ def test_byte_sizes():
         c, s, g = pack.pack(fmt, w)
         bits = 4 if fmt in ("mxfp4", "nvfp4", "int4_affine") else 8
         assert c.nbytes == n * k * bits // 8 == pack.codes_nbytes(fmt, n, k)
-        per_scale = {"nvfp8": 4, "int4_affine": 4, "nvfp8_f16": 2}.get(fmt, 1)
+        per_scale = {"nvfp8": 4, "int4_affine": 4, "nvfp8_f16": 2, "int8": 4, "int8_f16": 2}.get(fmt, 1)
         assert s.nbytes == n * (k // pack.BLOCK[fmt]) * per_scale == pack.scales_nbytes(fmt, n, k)
         assert c.dtype == np.uint8 and s.dtype == np.uint8 and isinstance(g, np.float32)
 
@@ -68,9 +68,9 @@ def test_zero_blocks():
             assert (s == 127).all()
         elif fmt == "nvfp4":
             assert (s == 0x38).all() and g == 1.0
-        elif fmt == "nvfp8":
+        elif fmt in ("nvfp8", "int8"):
             assert (s.view(np.float32) == 1.0).all()
-        elif fmt == "nvfp8_f16":
+        elif fmt in ("nvfp8_f16", "int8_f16"):
             assert (s.view(np.float16) == 1.0).all()
         else:
             pair = s.view(np.uint16).reshape(n, -1, 2)
@@ -124,7 +124,8 @@ def test_value_idempotence(fmt):
 
 
 FLOORS = {"mxfp4": 0.98, "nvfp4": 0.98, "int4_affine": 0.99,
-          "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999, "nvfp8_f16": 0.999, "mxint8": 0.999}
+          "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999, "nvfp8_f16": 0.999, "mxint8": 0.999,
+          "int8": 0.9999, "int8_f16": 0.9999}
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -260,3 +261,62 @@ def test_mxint8_rounds_half_away_and_clamps():
     assert s[0, 0] == 127
     assert list(c.view(np.int8)[0, :5]) == [127, 3, -3, 127, -1]
 
+
+
+def _int8_exact_case(rng, n, k, half):
+    """W = q * s per group of 64 (a last group of 32 when 64 does not divide K),
+    +-127 in every group, s with few enough significant bits that 127 s / 127
+    is exact in float32 (and s is a half for the fp16-scale twin)."""
+    nb = -(-k // 64)
+    q = rng.integers(-127, 128, size=(n, k))
+    q[:, ::64] = 127 * rng.choice([-1, 1], size=(n, nb))
+    if half:   # 11 significant bits, exponents down into the half subnormals
+        m = rng.integers(2 ** 10, 2 ** 11, size=(n, nb)).astype(np.float64)
+        e = rng.integers(-34, 4, size=(n, nb))
+        e = np.maximum(e, -24 - 10)            # m 2^e stays a (possibly subnormal) half
+        s = (m * 2.0 ** e).astype(np.float16).astype(np.float64)
+    else:      # 16 significant bits
+        m = rng.integers(2 ** 15, 2 ** 16, size=(n, nb)).astype(np.float64)
+        s = m * 2.0 ** rng.integers(-60, 20, size=(n, nb))
+    w = (q * np.repeat(s, 64, axis=1)[:, :k]).astype(np.float32)
+    return q, s, w
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int8_f16"])
+@pytest.mark.parametrize("k", [256, 96, 160])
+def test_int8_exactly_representable_roundtrip(fmt, k):
+    # PR #250 symmetric int8 (scale-only, +-127, group 64; the pages' ragged
+    # example is this group over a dimension of 96): the packer must give back
+    # exactly q and s, and the dequant exactly W -- a wrong group boundary, a
+    # scale from the wrong columns or a dropped ragged group breaks it.
+    rng = np.random.default_rng(41 + k)
+    n = 6
+    q, s, w = _int8_exact_case(rng, n, k, fmt == "int8_f16")
+    assert np.array_equal(w.astype(np.float64), q * np.repeat(s, 64, axis=1)[:, :k])
+    c, sc, g = pack.pack(fmt, w)
+    assert c.shape == (n, k) and sc.nbytes == n * -(-k // 64) * (4 if fmt == "int8" else 2)
+    assert np.array_equal(c.view(np.int8), q.astype(np.int8))
+    got_s = sc.view(np.float32 if fmt == "int8" else np.float16).reshape(n, -1).astype(np.float64)
+    assert np.array_equal(got_s, s)
+    assert np.array_equal(reference.dequant_exact(fmt, c, sc, g, n, k), w.astype(np.float64))
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int8_f16"])
+def test_int8_rounds_half_away_and_clamps(fmt):
+    w = np.zeros((1, 64), np.float32)
+    w[0, 0] = -127.0                         # scale exactly 1
+    w[0, 1:5] = [2.5, -2.5, 126.5, -0.5]     # ties: away from zero
+    c, s, _ = pack.pack(fmt, w)
+    assert s.view(np.float32 if fmt == "int8" else np.float16)[0] == 1.0
+    assert list(c.view(np.int8)[0, :5]) == [-127, 3, -3, 127, -1]
+
+
+def test_int8_f16_scale_underflow_quantizes_to_zero():
+    # a group whose amax / 127 rounds to a zero half stores scale 0 and zero codes
+    w = np.zeros((2, 64), np.float32)
+    w[0, :] = np.float32(1e-9)
+    w[1, 0] = np.float32(0.5)
+    c, s, g = pack.pack("int8_f16", w)
+    assert s.view(np.float16)[0] == 0 and not c[0].any()
+    assert not reference.dequant_exact("int8_f16", c, s, g, 2, 64)[0].any()
+    assert c.view(np.int8)[1, 0] == 127

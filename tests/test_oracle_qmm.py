@@ -40,7 +40,7 @@ def _lib_elem(fmt, c):
         return Fraction(v)
     if fmt == "mxfp8_e5m2":
         return Fraction(float(np.array([c << 8], np.uint16).view(np.float16)[0]))
-    if fmt == "mxint8":
+    if fmt in ("mxint8", "int8", "int8_f16"):
         return Fraction(c - 256 if c >= 128 else c)
     return Fraction(c)
 
@@ -51,9 +51,9 @@ def _lib_scale(fmt, sbytes, n, b):
     if fmt == "nvfp4":
         v = torch.tensor([int(sbytes[n][b])], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()
         return Fraction(v), Fraction(0)
-    if fmt == "nvfp8":
+    if fmt in ("nvfp8", "int8"):
         return Fraction(float(np.frombuffer(bytes(sbytes[n][4 * b:4 * b + 4]), "<f4")[0])), Fraction(0)
-    if fmt == "nvfp8_f16":
+    if fmt in ("nvfp8_f16", "int8_f16"):
         return Fraction(float(np.frombuffer(bytes(sbytes[n][2 * b:2 * b + 2]), "<f2")[0])), Fraction(0)
     raw = bytes(sbytes[n][4 * b:4 * b + 4])
     s_bits, b_bits = np.frombuffer(raw, "<u2")

@@ -22,7 +22,10 @@
 
 namespace qfmt_dev {
 
-enum Fmt { MXFP4 = 1, NVFP4 = 2, MXFP8_E4M3 = 3, MXFP8_E5M2 = 4, NVFP8 = 5, INT4_AFFINE = 6, NVFP8_F16 = 7, MXINT8 = 8 };
+enum Fmt {
+  MXFP4 = 1, NVFP4 = 2, MXFP8_E4M3 = 3, MXFP8_E5M2 = 4, NVFP8 = 5, INT4_AFFINE = 6, NVFP8_F16 = 7, MXINT8 = 8,
+  INT8 = 9, INT8_F16 = 10
+};
 
 template <int F> struct FmtTraits;
 template <> struct FmtTraits<MXFP4> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 1; };
@@ -33,6 +36,8 @@ template <> struct FmtTraits<NVFP8> { static constexpr bool four = false; static
 template <> struct FmtTraits<INT4_AFFINE> { static constexpr bool four = true; static constexpr int block = 64; static constexpr int sbytes = 4; };
 template <> struct FmtTraits<NVFP8_F16> { static constexpr bool four = false; static constexpr int block = 16; static constexpr int sbytes = 2; };
 template <> struct FmtTraits<MXINT8> { static constexpr bool four = false; static constexpr int block = 32; static constexpr int sbytes = 1; };
+template <> struct FmtTraits<INT8> { static constexpr bool four = false; static constexpr int block = 64; static constexpr int sbytes = 4; };
+template <> struct FmtTraits<INT8_F16> { static constexpr bool four = false; static constexpr int block = 64; static constexpr int sbytes = 2; };
 
 // 8-bit elements under an E8M0 scale per 32 (mxfp8 E4M3/E5M2, mxint8), and
 // every E8M0-scaled format (those and mxfp4)
@@ -41,15 +46,20 @@ constexpr bool is_mx8() { return F == MXFP8_E4M3 || F == MXFP8_E5M2 || F == MXIN
 template <int F>
 constexpr bool is_e8m0() { return F == MXFP4 || is_mx8<F>(); }
 
-// nvfp8 and its fp16-scale twin: E4M3 elements, one scale per 16 along K
+// 8-bit elements under a float block scale (float32 or IEEE half): nvfp8 and
+// its twin (E4M3, per 16), symmetric int8 and its twin (per 64)
 template <int F>
-constexpr bool is_nv8() { return F == NVFP8 || F == NVFP8_F16; }
+constexpr bool is_fs8() { return F == NVFP8 || F == NVFP8_F16 || F == INT8 || F == INT8_F16; }
 
-// Block scale idx of an nvfp8 scale array as float32: the stored float32, or
+// signed-int8 elements (under an E8M0 or a float scale)
+template <int F>
+constexpr bool is_int8() { return F == MXINT8 || F == INT8 || F == INT8_F16; }
+
+// Block scale idx of a float-scaled array as float32: the stored float32, or
 // the (exact) float32 of the stored IEEE half.
 template <int F>
-__device__ __forceinline__ float nv8_scale(const uint8_t* scales, int64_t idx) {
-  if constexpr (F == NVFP8) return __ldg(reinterpret_cast<const float*>(scales) + idx);
+__device__ __forceinline__ float fs8_scale(const uint8_t* scales, int64_t idx) {
+  if constexpr (FmtTraits<F>::sbytes == 4) return __ldg(reinterpret_cast<const float*>(scales) + idx);
   else return __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(scales) + idx)));
 }
 
@@ -194,7 +204,7 @@ __device__ __forceinline__ void int8x4_bf16(uint32_t w, uint32_t r[2]) {
 // byte with the sign bit flipped, under the exponent of 1024) less 1152.
 template <int F>
 __device__ __forceinline__ void elem8x4_f16(uint32_t w, uint32_t* r) {
-  if constexpr (F == MXINT8) {
+  if constexpr (is_int8<F>()) {
     const uint32_t t = w ^ 0x80808080u;
     const uint32_t a = prmt(t, 0x64u, 0x4140u), b = prmt(t, 0x64u, 0x4342u);
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(a), "r"(0x64806480u));
@@ -248,8 +258,8 @@ __device__ __forceinline__ PieceScale load_piece_scale(const uint8_t* scales, in
     s.a = __ldg(scales + base + k0 / 32);
   } else if constexpr (F == NVFP4) {
     s.a = __ldg(reinterpret_cast<const unsigned short*>(scales + base + k0 / 16));
-  } else if constexpr (is_nv8<F>()) {
-    s.a = __float_as_uint(nv8_scale<F>(scales, base + k0 / 16));
+  } else if constexpr (is_fs8<F>()) {
+    s.a = __float_as_uint(fs8_scale<F>(scales, base + k0 / FmtTraits<F>::block));
   } else {
     s.a = __ldg(reinterpret_cast<const uint32_t*>(scales) + base + k0 / 64);
   }
@@ -310,6 +320,7 @@ __device__ __forceinline__ void decode_piece(const uint4& v, const PieceScale& p
         two = true;
       }
     } else {  // nvfp8 (either scale storage): the float32 scale rounded once to bf16
+      static_assert(!is_int8<F>(), "float-scaled int8 decodes through decode_piece_hilo");
       const float s = __uint_as_float(ps.a);
       if (fabsf(s) < 128.0f) {
         m1 = bf16x2_splat(f32_to_bf16bits(s * 0x1p120f));
@@ -376,18 +387,25 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
   lo = pack_bf16x2(__fsub_rn(a, __uint_as_float(hi << 16)), __fsub_rn(b, __uint_as_float(hi & 0xFFFF0000u)));
 }
 
-// One 16-byte piece of an nvfp8 (16 codes) or int4-affine (32 codes) row as
-// hi/lo bf16 pairs in natural k order (8 or 16 registers each).
+// One 16-byte piece of a float-scaled 8-bit (16 codes) or int4-affine (32
+// codes) row as hi/lo bf16 pairs in natural k order (8 or 16 registers each).
 template <int F>
 __device__ __forceinline__ void decode_piece_hilo(const uint4& v, const PieceScale& ps, uint32_t* hi, uint32_t* lo) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  if constexpr (is_nv8<F>()) {
+  if constexpr (is_fs8<F>()) {
     const float s = __uint_as_float(ps.a);
     #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      uint32_t r[2];
-      e4m3x4_bf16_raw(w[j], r);
-      const uint32_t e02 = hmul2(r[0], 0x7B807B80u), e13 = hmul2(r[1], 0x7B807B80u);   // x 2^120: exact values
+      uint32_t r[2], e02, e13;
+      if constexpr (is_int8<F>()) {
+        int8x4_bf16(w[j], r);                                                       // exact values
+        e02 = r[0];
+        e13 = r[1];
+      } else {
+        e4m3x4_bf16_raw(w[j], r);
+        e02 = hmul2(r[0], 0x7B807B80u);                                             // x 2^120: exact values
+        e13 = hmul2(r[1], 0x7B807B80u);
+      }
       const float v0 = __fmul_rn(__uint_as_float(e02 << 16), s), v2 = __fmul_rn(__uint_as_float(e02 & 0xFFFF0000u), s);
       const float v1 = __fmul_rn(__uint_as_float(e13 << 16), s), v3 = __fmul_rn(__uint_as_float(e13 & 0xFFFF0000u), s);
       split_bf16x2(v0, v1, hi[2 * j], lo[2 * j]);

@@ -26,8 +26,8 @@ __device__ __forceinline__ float dq_value(uint32_t code, float s, float b, float
   if constexpr (F == NVFP4) return __fmul_rn(__fmul_rn(e2m1_f32(code), s), glob);   // (e2m1 * e4m3) exact
   if constexpr (F == MXFP8_E4M3) return __fmul_rn(e4m3_f32(code), s);
   if constexpr (F == MXFP8_E5M2) return __fmul_rn(e5m2_f32(code), s);
-  if constexpr (F == MXINT8) return __fmul_rn(float(int8_t(uint8_t(code))), s);
-  if constexpr (is_nv8<F>()) return __fmul_rn(e4m3_f32(code), s);
+  if constexpr (is_int8<F>()) return __fmul_rn(float(int8_t(uint8_t(code))), s);
+  if constexpr (is_fs8<F>()) return __fmul_rn(e4m3_f32(code), s);
   return __fmaf_rn(s, float(code), b);                                               // INT4_AFFINE
 }
 
@@ -37,7 +37,7 @@ __device__ __forceinline__ void dq_scale(const uint8_t* scales, int64_t idx, flo
   b = 0.0f;
   if constexpr (is_e8m0<F>()) s = e8m0_f32(scales[idx]);
   else if constexpr (F == NVFP4) s = e4m3_f32(scales[idx]);
-  else if constexpr (is_nv8<F>()) s = nv8_scale<F>(scales, idx);
+  else if constexpr (is_fs8<F>()) s = fs8_scale<F>(scales, idx);
   else {
     const uint32_t p = reinterpret_cast<const uint32_t*>(scales)[idx];
     s = bf16bits_f32(p & 0xFFFFu);
@@ -126,6 +126,8 @@ cudaError_t launch_dequant(int fmt, const void* codes, const void* scales, float
     case NVFP8: return launch_dequant_fmt<NVFP8>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case NVFP8_F16: return launch_dequant_fmt<NVFP8_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case MXINT8: return launch_dequant_fmt<MXINT8>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case INT8: return launch_dequant_fmt<INT8>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case INT8_F16: return launch_dequant_fmt<INT8_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     default: return launch_dequant_fmt<INT4_AFFINE>(codes, scales, glob, out, out_bf16, N, K, st, sms);
   }
 }

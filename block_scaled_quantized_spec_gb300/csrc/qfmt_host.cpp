@@ -35,13 +35,13 @@ int fail(int status, const char* fmt, ...) {
 
 void clear_error() { g_err[0] = '\0'; }
 
-bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_MXINT8; }
+bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_INT8_F16; }
 
 int block_of(int fmt) {
   switch (fmt) {
     case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: return 32;
     case QFMT_NVFP4: case QFMT_NVFP8: case QFMT_NVFP8_F16: return 16;
-    case QFMT_INT4_AFFINE: return 64;
+    case QFMT_INT4_AFFINE: case QFMT_INT8: case QFMT_INT8_F16: return 64;
     default: return 0;
   }
 }
@@ -49,7 +49,8 @@ int block_of(int fmt) {
 bool is_4bit(int fmt) { return fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4 || fmt == QFMT_INT4_AFFINE; }
 
 int scale_entry_bytes(int fmt) {
-  return (fmt == QFMT_NVFP8 || fmt == QFMT_INT4_AFFINE) ? 4 : (fmt == QFMT_NVFP8_F16 ? 2 : 1);
+  if (fmt == QFMT_NVFP8 || fmt == QFMT_INT4_AFFINE || fmt == QFMT_INT8) return 4;
+  return (fmt == QFMT_NVFP8_F16 || fmt == QFMT_INT8_F16) ? 2 : 1;
 }
 
 int check_group(int fmt, int group) {
@@ -179,7 +180,7 @@ using namespace qfmt;
 
 extern "C" {
 
-int qfmt_version(void) { return 102; }
+int qfmt_version(void) { return 103; }
 
 const char* qfmt_last_error(void) { return qfmt::g_err; }
 
@@ -265,7 +266,7 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
           continue;
         }
         float amax = 0.0f;
-        for (int j = 0; j < blk; ++j) amax = std::max(amax, std::fabs(wb[j]));
+        for (int j = 0; j < len; ++j) amax = std::max(amax, std::fabs(wb[j]));
         float eff;
         switch (fmt) {
           case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: {
@@ -283,26 +284,26 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
             eff = dec_e4m3(u) * glob;
             break;
           }
-          case QFMT_NVFP8_F16: {  // the scale stored as an IEEE half, rounded to nearest even
-            const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+          case QFMT_NVFP8_F16: case QFMT_INT8_F16: {  // the scale stored as an IEEE half, rounded to nearest even
+            const float s = amax > 0.0f ? amax / (fmt == QFMT_INT8_F16 ? 127.0f : 448.0f) : 1.0f;
             const _Float16 h = static_cast<_Float16>(s);
             std::memcpy(sb + (n * nb + b) * 2, &h, 2);
             eff = static_cast<float>(h);
             break;
           }
-          default: {  // QFMT_NVFP8
-            const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+          default: {  // QFMT_NVFP8, QFMT_INT8: the float32 scale stored raw
+            const float s = amax > 0.0f ? amax / (fmt == QFMT_INT8 ? 127.0f : 448.0f) : 1.0f;
             std::memcpy(sb + (n * nb + b) * 4, &s, 4);
             eff = s;
             break;
           }
         }
         if (!std::isfinite(eff)) { bad = true; continue; }
-        for (int j = 0; j < blk; ++j) {
+        for (int j = 0; j < len; ++j) {
           uint32_t code = 0;
           if (eff != 0.0f) {
             const float v = wb[j] / eff;
-            if (fmt == QFMT_MXINT8) {  // symmetric: round half away from zero, clamp to +-127
+            if (fmt == QFMT_MXINT8 || fmt == QFMT_INT8 || fmt == QFMT_INT8_F16) {  // symmetric: round half away from zero, clamp to +-127
               code = uint32_t(uint8_t(int8_t(std::max(-127.0f, std::min(127.0f, std::round(v))))));
               put_code(crow, b * blk + j, code, four);
               continue;

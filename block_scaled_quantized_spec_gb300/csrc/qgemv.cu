@@ -213,8 +213,8 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
           wsc[rr * sst + e] = ok ? e8m0_f32(__ldg(scales + gi)) : 0.0f;
         } else if constexpr (F == NVFP4) {
           wsc[rr * sst + e] = __uint_as_float(ok ? e4m3_f16x2_splat(__ldg(scales + gi)) : 0u);
-        } else if constexpr (is_nv8<F>()) {
-          wsc[rr * sst + e] = ok ? nv8_scale<F>(scales, gi) : 0.0f;
+        } else if constexpr (is_fs8<F>()) {
+          wsc[rr * sst + e] = ok ? fs8_scale<F>(scales, gi) : 0.0f;
         } else {
           const uint32_t pr = ok ? __ldg(reinterpret_cast<const uint32_t*>(scales) + gi) : 0u;
           const float sc = bf16bits_f32(pr & 0xFFFFu), bi = bf16bits_f32(pr >> 16);
@@ -379,8 +379,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
               uint32_t fa[2], fb[2];
               elem8x4_f16<F>(wa, fa);
               elem8x4_f16<F>(wb, fb);
-              const float swa = is_nv8<F>() ? sca[sgm] : sca[sgm >> 1];
-              const float swb = is_nv8<F>() ? scb[sgm] : scb[sgm >> 1];
+              const float swa = sca[16 * sgm / BLK], swb = scb[16 * sgm / BLK];   // the block of this segment
               #pragma unroll
               for (int nb = 0; nb < NB; ++nb) {
                 const int m = min(nb * 8 + g, M - 1);
@@ -537,6 +536,8 @@ cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float g
     case NVFP8: return gemv::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case NVFP8_F16: return gemv::launch_fmt<NVFP8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case MXINT8: return gemv::launch_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case INT8: return gemv::launch_fmt<INT8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case INT8_F16: return gemv::launch_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     default: return gemv::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }

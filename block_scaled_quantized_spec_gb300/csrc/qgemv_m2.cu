@@ -302,12 +302,18 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
       const uint32_t x2 = c0 ? __ldg(srb + e) : 127u;
       cs[i].a0 = prmt(x0, x2, 0x1410u) | 0x7F007F00u;                         // bytes 0 and 2 used, 1 and 3 = 127
       cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
-    } else if constexpr (is_nv8<F>()) {
-      const int e = k0 / 16;
-      cs[i].a0 = c0 ? __float_as_uint(nv8_scale<F>(sra, e)) : 0u;
-      cs[i].a1 = c1 ? __float_as_uint(nv8_scale<F>(sra, e + 1)) : 0u;
-      cs[i].b0 = c0 ? __float_as_uint(nv8_scale<F>(srb, e)) : 0u;
-      cs[i].b1 = c1 ? __float_as_uint(nv8_scale<F>(srb, e + 1)) : 0u;
+    } else if constexpr (is_fs8<F>()) {
+      constexpr int B = FmtTraits<F>::block;                                  // 16 (nvfp8) or 64 (int8)
+      const int e = k0 / B;
+      cs[i].a0 = c0 ? __float_as_uint(fs8_scale<F>(sra, e)) : 0u;
+      cs[i].b0 = c0 ? __float_as_uint(fs8_scale<F>(srb, e)) : 0u;
+      if constexpr (B == 16) {
+        cs[i].a1 = c1 ? __float_as_uint(fs8_scale<F>(sra, e + 1)) : 0u;
+        cs[i].b1 = c1 ? __float_as_uint(fs8_scale<F>(srb, e + 1)) : 0u;
+      } else {                                                                // a0, a0 + 1 share it
+        cs[i].a1 = c1 ? cs[i].a0 : 0u;
+        cs[i].b1 = c1 ? cs[i].b0 : 0u;
+      }
     } else if constexpr (F == INT4_AFFINE) {
       const int e = k0 / 64;                                                  // a0, a0 + 1 share it
       cs[i].a0 = c0 ? __ldg(reinterpret_cast<const uint32_t*>(sra) + e) : 0u;
@@ -548,7 +554,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
         const float ca = __fmul_rn(qa, x0s), cb = __fmul_rn(qb, x0s);
         acc_a = __fmaf_rn(ca, d[ii][0] + d[ii][1], acc_a);
         acc_b = __fmaf_rn(cb, d[ii][2] + d[ii][3], acc_b);
-      } else if constexpr (is_nv8<F>()) {
+      } else if constexpr (is_fs8<F>()) {
         acc_a = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].a0), x0s), d[ii][0], acc_a);
         acc_a = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].a1), x1s), d[ii][1], acc_a);
         acc_b = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].b0), x0s), d[ii][2], acc_b);
@@ -720,6 +726,8 @@ cudaError_t launch_qgemv_m2(int fmt, const void* codes, const void* scales, floa
     case NVFP8: return gemv_m2::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case NVFP8_F16: return gemv_m2::launch_fmt<NVFP8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case MXINT8: return gemv_m2::launch_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case INT8: return gemv_m2::launch_fmt<INT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case INT8_F16: return gemv_m2::launch_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_m2::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }
@@ -739,6 +747,9 @@ cudaError_t launch_qgemv_gather(int fmt, const void* codes, const void* scales, 
     case NVFP8_F16:
       return gemv_m2::launch_gather_fmt<NVFP8_F16>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
     case MXINT8: return gemv_m2::launch_gather_fmt<MXINT8>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    case INT8: return gemv_m2::launch_gather_fmt<INT8>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    case INT8_F16:
+      return gemv_m2::launch_gather_fmt<INT8_F16>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
     default:
       return gemv_m2::launch_gather_fmt<INT4_AFFINE>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
   }
@@ -785,6 +796,8 @@ cudaError_t launch_qgemv_multi(int fmt, int count, const void* const* codes, con
     case NVFP8: QFMT_MULTI(NVFP8);
     case NVFP8_F16: QFMT_MULTI(NVFP8_F16);
     case MXINT8: QFMT_MULTI(MXINT8);
+    case INT8: QFMT_MULTI(INT8);
+    case INT8_F16: QFMT_MULTI(INT8_F16);
     default: QFMT_MULTI(INT4_AFFINE);
   }
 #undef QFMT_MULTI

@@ -43,7 +43,7 @@ constexpr size_t X_BUDGET = 40 * 1024;  // staged f16 activations per CTA (five 
 // 64-byte chunks per lane in flight: four; two for nvfp8 and int4 affine,
 // whose per-chunk scales (eight float32, four scale/bias pairs) stay in registers
 template <int F>
-constexpr int chunks_in_flight() { return (is_nv8<F>() || F == INT4_AFFINE) ? 2 : 4; }
+constexpr int chunks_in_flight() { return (is_fs8<F>() || F == INT4_AFFINE) ? 2 : 4; }
 
 template <int F>
 struct Shape {
@@ -163,7 +163,7 @@ inline size_t smem_bytes(int F, int M, int kr) {
 // Raw scale words a lane keeps per chunk: 2 (rows g, g + 8) for the byte
 // scales, 4 for int4 affine (two blocks), 8 for nvfp8 (four float32 blocks).
 template <int F>
-constexpr int scale_words() { return is_nv8<F>() ? 8 : (F == INT4_AFFINE ? 4 : 2); }
+constexpr int scale_words() { return is_fs8<F>() ? 8 : (F == INT4_AFFINE ? 4 : 2); }
 
 template <int F, int NB, bool UNI>
 __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __restrict__ codes,
@@ -253,12 +253,12 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       }
       sc[i][0] = a;
       sc[i][1] = b;
-    } else if constexpr (is_nv8<F>()) {                                     // one scale block per segment
+    } else if constexpr (is_fs8<F>()) {                                     // each segment's block scale
       #pragma unroll
       for (int sg = 0; sg < 4; ++sg) {
         const int k = kc + sg * SEG;
-        sc[i][sg] = live(k) ? __float_as_uint(nv8_scale<F>(sra, k / 16)) : 0u;
-        sc[i][4 + sg] = live(k) ? __float_as_uint(nv8_scale<F>(srb, k / 16)) : 0u;
+        sc[i][sg] = live(k) ? __float_as_uint(fs8_scale<F>(sra, k / FmtTraits<F>::block)) : 0u;
+        sc[i][4 + sg] = live(k) ? __float_as_uint(fs8_scale<F>(srb, k / FmtTraits<F>::block)) : 0u;
       }
     } else {                                                                // int4 affine: (scale, bias) per 64
       const uint32_t* ua = reinterpret_cast<const uint32_t*>(sra);
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       const int c = r * P + i;
       if (c < nch) {                                                        // uniform over the CTA
         float ac[NB][4], d[NB][4];
-        constexpr bool per_seg = F == MXFP4 || is_nv8<F>();                   // a block per segment
+        constexpr bool per_seg = F == MXFP4 || is_fs8<F>();                   // a scale per segment
         constexpr bool per_pair = is_mx8<F>() || I4;  // a block per two segments
         #pragma unroll
         for (int sg = 0; sg < 4; ++sg) {
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             }
           }
           // block scales on the float32 MMA results (d rows g: e = 0, 1; g + 8: e = 2, 3)
-          constexpr bool per_seg = F == MXFP4 || is_nv8<F>();                   // a block per segment
+          constexpr bool per_seg = F == MXFP4 || is_fs8<F>();                   // a scale per segment
           constexpr bool per_pair = is_mx8<F>() || I4;  // a block per two segments
           if (per_seg || (per_pair && (sg & 1))) {
             const bool first = sg < (per_seg ? 1 : 2);                      // the chunk's first block
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             if constexpr (F == MXFP4) {
               sa = e8m0_f32((sc[i][0] >> (8 * sg)) & 0xFFu);
               sb = e8m0_f32((sc[i][1] >> (8 * sg)) & 0xFFu);
-            } else if constexpr (is_nv8<F>()) {
+            } else if constexpr (is_fs8<F>()) {
               sa = __uint_as_float(sc[i][sg]);
               sb = __uint_as_float(sc[i][4 + sg]);
             } else if constexpr (I4) {                                      // s * D + (b - 128 s) * sum(x)
@@ -618,6 +618,8 @@ cudaError_t launch_qgemv_mb(int fmt, const void* codes, const void* scales, floa
     case NVFP8: return gemv_mb::launch_fmt<NVFP8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case NVFP8_F16: return gemv_mb::launch_fmt<NVFP8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case MXINT8: return gemv_mb::launch_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case INT8: return gemv_mb::launch_fmt<INT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case INT8_F16: return gemv_mb::launch_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_mb::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }

@@ -24,6 +24,10 @@
  *                                                 packer clamps q to +-127 and rounds half
  *                                                 away from zero; a stored -128 decodes as
  *                                                 -128)
+ *   QFMT_INT8           signed int8 q      64     FP32 (4 bytes): w = q * scale (PR #250's
+ *                                                 symmetric int8, scale-only, +-127)
+ *   QFMT_INT8_F16       signed int8 q      64     IEEE half (2 bytes): the fp16-scale twin
+ *                                                 of QFMT_INT8
  *
  * Memory layouts (all row-major, no padding, little-endian):
  *   codes   [N, K/2] bytes for 4-bit formats: element k of a row sits in byte
@@ -32,9 +36,9 @@
  *   scales  [N, ceil(K/block)] entries of the sizes above; int4 affine stores
  *           the (scale, bias) bf16 pair of each group adjacently:
  *           [N, ceil(K/64), 2].  K is a multiple of 32 for every format, so
- *           only int4 affine can end in a ragged group (of 32 values, with its
- *           own scale and bias; PR #250: a ragged trailing block, the block
- *           count rounded up).
+ *           only the group-64 formats (int4 affine, int8, int8_f16) can end in
+ *           a ragged group (of 32 values, with its own scale and bias; PR
+ *           #250: a ragged trailing block, the block count rounded up).
  *   X       [M, K] bf16 (or f32 through qmm_ex), out [M, N] bf16 (or f32).
  *
  * Element values: E2M1 {0,.5,1,1.5,2,3,4,6} with sign bit 3; E4M3 bias 7,
@@ -79,7 +83,9 @@ typedef enum {
   QFMT_NVFP8 = 5,
   QFMT_INT4_AFFINE = 6,
   QFMT_NVFP8_F16 = 7,
-  QFMT_MXINT8 = 8
+  QFMT_MXINT8 = 8,
+  QFMT_INT8 = 9,
+  QFMT_INT8_F16 = 10
 } qfmt_format;
 
 typedef enum { QFMT_F32 = 0, QFMT_BF16 = 1 } qfmt_dtype;

@@ -19,6 +19,7 @@ from oracle import reference as oref  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 FMTS = list(q.FORMATS)
+GROUP64 = ["int4_affine", "int8", "int8_f16"]          # group of 64: K may end in a group of 32
 DEV = "cuda:0"
 
 
@@ -80,11 +81,11 @@ def test_dequant_all_codes_and_scales(fmt):
     sb = opack.scales_nbytes(fmt, n, k)
     if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "nvfp4"):
         scales = np.tile(np.arange(256, dtype=np.uint8), sb // 256 + 1)[:sb]
-    elif fmt == "nvfp8":
+    elif fmt in ("nvfp8", "int8"):
         scales = np.concatenate([rng.standard_normal(sb // 4 - 4).astype(np.float32),
                                  np.array([1e-40, 3e38, 0.0, -2.5], np.float32)]).view(np.uint8)
-    elif fmt == "nvfp8_f16":   # every 32nd half bit pattern: subnormals, +-inf, NaNs, both signs
-        scales = np.arange(0, 65536, 32, dtype=np.uint16)[:sb // 2].view(np.uint8)
+    elif fmt in ("nvfp8_f16", "int8_f16"):   # evenly spaced half bit patterns: subnormals, +-inf, NaNs, both signs
+        scales = np.arange(0, 65536, 65536 // (sb // 2), dtype=np.uint16)[:sb // 2].view(np.uint8)
     else:
         sc = synth.f32_to_bf16_bits(rng.standard_normal(sb // 2).astype(np.float32) * 1e-2)
         scales = sc.view(np.uint8)
@@ -133,7 +134,7 @@ def test_qgemm_parity(fmt, m):
 def test_short_and_odd_k(fmt, m):
     # K of one block quantum and K that leave partial chunks / K steps; few terms
     # per output, so a per-weight rounding above the bound would show
-    for k in (32, 64, 96, 160, 192) if fmt == "int4_affine" else (32, 96, 160):   # int4: ragged last groups too
+    for k in (32, 64, 96, 160, 192) if fmt in GROUP64 else (32, 96, 160):   # group 64: ragged last groups too
         n = 33 if m < 17 else 300
         c, s, g = _packed(fmt, n, k, seed=k)
         xb, xt = _x(m, k, seed=k + 1)
@@ -229,6 +230,10 @@ FULL = [
     ("nvfp8", 16, 11008, 4096, False),
     ("nvfp8", 128, 11008, 4096, False),
     ("nvfp8", 4096, 11008, 4096, False),
+    ("mxint8", 1, 11008, 4096, False),
+    ("mxint8", 4096, 11008, 4096, False),
+    ("int8", 1, 11008, 4096, False),
+    ("int8", 4096, 11008, 4096, False),
 ]
 
 
@@ -352,10 +357,11 @@ def test_chained_layers_read_the_previous_output(fmt, m):
         _check_qmm(outs[i + 1], ref, bound, (fmt, m, "layer", i))
 
 
+@pytest.mark.parametrize("fmt", GROUP64)
 @pytest.mark.parametrize("m", [1, 2, 5, 16, 40, 300])
-def test_int4_ragged_last_group_every_path(m):
-    # K = 64 * 32 + 32: the last int4-affine group holds 32 values (its own scale and bias)
-    fmt, n, k = "int4_affine", 136, 2080
+def test_ragged_last_group_every_path(fmt, m):
+    # K = 64 * 32 + 32: the last group of 64 holds 32 values (its own scale, and bias for int4 affine)
+    n, k = 136, 2080
     c, s, g = _packed(fmt, n, k, seed=90 + m)
     xb, xt = _x(m, k, seed=91 + m)
     out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
@@ -373,9 +379,10 @@ def test_int4_ragged_last_group_every_path(m):
 
 
 
-def test_int4_ragged_last_group_long_k_fallback():
+@pytest.mark.parametrize("fmt", GROUP64)
+def test_ragged_last_group_long_k_fallback(fmt):
     # two rows of K = 64 * 384 + 32: past the single-pass GEMVs' shared-memory plans
-    fmt, m, n, k = "int4_affine", 2, 48, 24608
+    m, n, k = 2, 48, 24608
     c, s, g = _packed(fmt, n, k, seed=95)
     xb, xt = _x(m, k, seed=96)
     out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)

@@ -41,6 +41,11 @@ Readings taken where the pages are silent (each is listed in the design doc):
   underflowed).  K that 64 does not divide leaves a ragged last group of 32
   with its own amax (the pages' own example: int8's group of 64 over a
   dimension of 96 tiles as a 64-block and a 32-block).
+* int4 / int4_f16 (PR #250's symmetric int2-6 on the FP32 group-64 scale
+  path, the intN codec sign-extending from bit N-1 and clamping to
+  +-(2^(N-1) - 1); the fp16-scale twin): as int8 with 7 in place of 127, the
+  4-bit two's-complement code stored LSB-first two per byte (the 4-bit
+  bit-stream is the nibble layout).
 * int4 affine (MLX style, group 64): s = (max - min) / 15 (1.0 when 0), stored
   as bf16 (RNE); bias = bf16(min); q = clamp(round_half_away((w - b) / s), 0, 15);
   scale and bias are interleaved per group as bf16 pairs [N, ceil(K/64), 2].
@@ -57,19 +62,20 @@ import numpy as np
 from . import codec
 
 FORMATS = ("mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8", "int4_affine", "nvfp8_f16", "mxint8",
-           "int8", "int8_f16")
-RAGGED = ("int4_affine", "int8", "int8_f16")          # block 64: K may end in a group of 32
+           "int8", "int8_f16", "int4", "int4_f16")
+RAGGED = ("int4_affine", "int8", "int8_f16", "int4", "int4_f16")   # block 64: K may end in a group of 32
+SYM_INT = ("int8", "int8_f16", "int4", "int4_f16")                 # symmetric integers, float scale per 64
 
 BLOCK = {"mxfp4": 32, "nvfp4": 16, "mxfp8_e4m3": 32, "mxfp8_e5m2": 32, "nvfp8": 16, "int4_affine": 64,
-         "nvfp8_f16": 16, "mxint8": 32, "int8": 64, "int8_f16": 64}
+         "nvfp8_f16": 16, "mxint8": 32, "int8": 64, "int8_f16": 64, "int4": 64, "int4_f16": 64}
 ELEM_BITS = {"mxfp4": 4, "nvfp4": 4, "mxfp8_e4m3": 8, "mxfp8_e5m2": 8, "nvfp8": 8, "int4_affine": 4, "nvfp8_f16": 8,
-             "mxint8": 8, "int8": 8, "int8_f16": 8}
+             "mxint8": 8, "int8": 8, "int8_f16": 8, "int4": 4, "int4_f16": 4}
 SCALE_BYTES = {"mxfp4": 1, "nvfp4": 1, "mxfp8_e4m3": 1, "mxfp8_e5m2": 1, "nvfp8": 4, "int4_affine": 4,
-               "nvfp8_f16": 2, "mxint8": 1, "int8": 4, "int8_f16": 2}
+               "nvfp8_f16": 2, "mxint8": 1, "int8": 4, "int8_f16": 2, "int4": 4, "int4_f16": 2}
 _ELEM = {"mxfp4": ("e2m1", codec.E2M1_MAX), "nvfp4": ("e2m1", codec.E2M1_MAX),
          "mxfp8_e4m3": ("e4m3", codec.E4M3_MAX), "mxfp8_e5m2": ("e5m2", codec.E5M2_MAX),
          "nvfp8": ("e4m3", codec.E4M3_MAX), "nvfp8_f16": ("e4m3", codec.E4M3_MAX), "mxint8": ("int8", 127.0),
-         "int8": ("int8", 127.0), "int8_f16": ("int8", 127.0)}
+         "int8": ("int8", 127.0), "int8_f16": ("int8", 127.0), "int4": ("int4", 7.0), "int4_f16": ("int4", 7.0)}
 
 F32 = np.float32
 
@@ -124,11 +130,11 @@ def pack(fmt: str, w: np.ndarray):
         wp = np.concatenate([w, np.repeat(w[:, (kp - blk):(kp - blk) + 1], kp - k, axis=1)], axis=1)
         c, s, g = _pack_int4_affine(wp.reshape(n, kp // blk, blk), n, kp)
         return np.ascontiguousarray(c[:, : k // 2]), s, g
-    if fmt in ("int8", "int8_f16") and k % blk:
+    if fmt in SYM_INT and k % blk:
         # the ragged last group, padded with zeros: its amax, hence its scale and codes, are unchanged
         kp = n_blocks(fmt, k) * blk
         c, s, g = pack(fmt, np.concatenate([w, np.zeros((n, kp - k), F32)], axis=1))
-        return np.ascontiguousarray(c[:, :k]), s, g
+        return np.ascontiguousarray(c[:, : codes_nbytes(fmt, 1, k)]), s, g
     wb = w.reshape(n, k // blk, blk)
     amax = np.max(np.abs(wb), axis=2).astype(F32)          # step 1
     glob = F32(1.0)
@@ -150,7 +156,7 @@ def pack(fmt: str, w: np.ndarray):
         ucode = np.where(amax > 0, ucode, np.uint8(0x38)).astype(np.uint8)
         eff = (codec.E4M3_TABLE[ucode].astype(F32) * glob).astype(F32)
         scales = ucode
-    elif fmt in ("nvfp8_f16", "int8_f16"):
+    elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):
         # the fp16-scale twin: amax / 448 rounded once to an IEEE half (nearest
         # even, subnormals kept, overflow to inf, rejected below)
         s = np.where(amax > 0, amax / F32(maxf), F32(1.0)).astype(F32)
@@ -165,12 +171,15 @@ def pack(fmt: str, w: np.ndarray):
     if not np.all(np.isfinite(eff)):
         raise ValueError("scale overflows float32")
 
-    if elem == "int8":   # symmetric integer element: round half away from zero, clamp to +-127
+    if elem in ("int8", "int4"):   # symmetric integer element: round half away from zero, clamp to +-maxf
         safe = np.where(eff == 0, F32(1.0), eff).astype(F32)
         v = (wb / safe[..., None]).astype(F32)
-        q = np.clip(_round_half_away(v), -127, 127)
-        q = np.where((eff == 0)[..., None], 0, q).astype(np.int8)
-        return q.view(np.uint8).reshape(n, k), np.ascontiguousarray(scales).view(np.uint8).reshape(n, -1), F32(glob)
+        q = np.clip(_round_half_away(v), -maxf, maxf)
+        q = np.where((eff == 0)[..., None], 0, q).astype(np.int8).reshape(n, k)
+        scales_b = np.ascontiguousarray(scales).view(np.uint8).reshape(n, -1)
+        if elem == "int4":      # 4-bit two's complement, two per byte
+            return _pack_nibbles(q.view(np.uint8) & np.uint8(0x0F)), scales_b, F32(glob)
+        return q.view(np.uint8), scales_b, F32(glob)
     codes = _quantize(wb, eff, elem).reshape(n, k)                        # step 4
     codes_b = _pack_nibbles(codes) if ELEM_BITS[fmt] == 4 else codes.astype(np.uint8)
     scales_b = np.ascontiguousarray(scales).view(np.uint8).reshape(n, -1)

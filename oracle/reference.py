@@ -23,6 +23,9 @@ Value definitions (page title, then the section):
 * int8 / int8_f16: w = q * scale, q the signed byte, one float32 (or IEEE
   half) scale per group of 64 -- PR #250, the symmetric integer formats on the
   FP32 per-group scale path and their fp16-scale twin.
+* int4 / int4_f16: the same with q the signed nibble (sign-extended from its
+  bit 3) -- PR #250, the symmetric intN formats (FP32 group 64) and the
+  fp16-scale twin.
 * int4 affine: w = scale * q + bias with q the LSB-first nibble, group 64 --
   metaltile-std ``tests/qmm_gpu_correctness.rs``, ``cpu_qmm_reference``;
   scale and bias are bf16.  float64 evaluation of s*q + b is exact or, when
@@ -78,9 +81,9 @@ def block_scales(fmt: str, scales: np.ndarray, global_scale: float, n: int, k: i
         return codec.E8M0_TABLE[s.reshape(n, nb)], None
     if fmt == "nvfp4":
         return codec.E4M3_TABLE[s.reshape(n, nb)], None
-    if fmt in ("nvfp8", "int8"):
+    if fmt in ("nvfp8", "int8", "int4"):
         return np.ascontiguousarray(s).view(np.float32).reshape(n, nb).astype(np.float64), None
-    if fmt in ("nvfp8_f16", "int8_f16"):
+    if fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):
         return np.ascontiguousarray(s).view(np.float16).reshape(n, nb).astype(np.float64), None
     pair = np.ascontiguousarray(s).view(np.uint16).reshape(n, nb, 2)
     return codec.decode_bf16(pair[..., 0]), codec.decode_bf16(pair[..., 1])
@@ -95,6 +98,9 @@ def element_values(fmt: str, codes: np.ndarray) -> np.ndarray:
         return codec.E5M2_TABLE[codes]
     if fmt in ("mxint8", "int8", "int8_f16"):            # the two's-complement byte
         return codes.astype(np.uint8).view(np.int8).astype(np.float64)
+    if fmt in ("int4", "int4_f16"):                      # the two's-complement nibble, sign-extended from bit 3
+        c = codes.astype(np.int64)
+        return np.where(c >= 8, c - 16, c).astype(np.float64)
     return codes.astype(np.float64)                      # int4 affine: q itself
 
 

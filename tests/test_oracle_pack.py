@@ -27,6 +27,8 @@ def _elem_values_lib(fmt, codes_nk):
         return (codes_nk.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
     if fmt in ("mxint8", "int8", "int8_f16"):
         return torch.from_numpy(codes_nk.astype(np.uint8)).view(torch.int8).double().numpy()
+    if fmt in ("int4", "int4_f16"):     # the nibble in the top of a byte, arithmetic shift back down
+        return torch.from_numpy((codes_nk.astype(np.uint8) << 4).astype(np.uint8)).view(torch.int8).double().numpy() / 16
     return codes_nk.astype(np.float64)
 
 
@@ -37,9 +39,10 @@ def test_byte_sizes():
     w = synth.weights(n, k, seed=5)
     for fmt in FMTS:
         c, s, g = pack.pack(fmt, w)
-        bits = 4 if fmt in ("mxfp4", "nvfp4", "int4_affine") else 8
+        bits = 4 if fmt in ("mxfp4", "nvfp4", "int4_affine", "int4", "int4_f16") else 8
         assert c.nbytes == n * k * bits // 8 == pack.codes_nbytes(fmt, n, k)
-        per_scale = {"nvfp8": 4, "int4_affine": 4, "nvfp8_f16": 2, "int8": 4, "int8_f16": 2}.get(fmt, 1)
+        per_scale = {"nvfp8": 4, "int4_affine": 4, "nvfp8_f16": 2, "int8": 4, "int8_f16": 2, "int4": 4,
+                     "int4_f16": 2}.get(fmt, 1)
         assert s.nbytes == n * (k // pack.BLOCK[fmt]) * per_scale == pack.scales_nbytes(fmt, n, k)
         assert c.dtype == np.uint8 and s.dtype == np.uint8 and isinstance(g, np.float32)
 
@@ -68,9 +71,9 @@ def test_zero_blocks():
             assert (s == 127).all()
         elif fmt == "nvfp4":
             assert (s == 0x38).all() and g == 1.0
-        elif fmt in ("nvfp8", "int8"):
+        elif fmt in ("nvfp8", "int8", "int4"):
             assert (s.view(np.float32) == 1.0).all()
-        elif fmt in ("nvfp8_f16", "int8_f16"):
+        elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):
             assert (s.view(np.float16) == 1.0).all()
         else:
             pair = s.view(np.uint16).reshape(n, -1, 2)
@@ -125,7 +128,7 @@ def test_value_idempotence(fmt):
 
 FLOORS = {"mxfp4": 0.98, "nvfp4": 0.98, "int4_affine": 0.99,
           "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999, "nvfp8_f16": 0.999, "mxint8": 0.999,
-          "int8": 0.9999, "int8_f16": 0.9999}
+          "int8": 0.9999, "int8_f16": 0.9999, "int4": 0.99, "int4_f16": 0.99}
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -263,13 +266,13 @@ def test_mxint8_rounds_half_away_and_clamps():
 
 
 
-def _int8_exact_case(rng, n, k, half):
+def _int8_exact_case(rng, n, k, half, qmax=127):
     """W = q * s per group of 64 (a last group of 32 when 64 does not divide K),
-    +-127 in every group, s with few enough significant bits that 127 s / 127
+    +-qmax in every group, s with few enough significant bits that qmax s / qmax
     is exact in float32 (and s is a half for the fp16-scale twin)."""
     nb = -(-k // 64)
-    q = rng.integers(-127, 128, size=(n, k))
-    q[:, ::64] = 127 * rng.choice([-1, 1], size=(n, nb))
+    q = rng.integers(-qmax, qmax + 1, size=(n, k))
+    q[:, ::64] = qmax * rng.choice([-1, 1], size=(n, nb))
     if half:   # 11 significant bits, exponents down into the half subnormals
         m = rng.integers(2 ** 10, 2 ** 11, size=(n, nb)).astype(np.float64)
         e = rng.integers(-34, 4, size=(n, nb))
@@ -282,7 +285,7 @@ def _int8_exact_case(rng, n, k, half):
     return q, s, w
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int8_f16"])
+@pytest.mark.parametrize("fmt", ["int8", "int8_f16", "int4", "int4_f16"])
 @pytest.mark.parametrize("k", [256, 96, 160])
 def test_int8_exactly_representable_roundtrip(fmt, k):
     # PR #250 symmetric int8 (scale-only, +-127, group 64; the pages' ragged
@@ -291,12 +294,18 @@ def test_int8_exactly_representable_roundtrip(fmt, k):
     # scale from the wrong columns or a dropped ragged group breaks it.
     rng = np.random.default_rng(41 + k)
     n = 6
-    q, s, w = _int8_exact_case(rng, n, k, fmt == "int8_f16")
+    four = fmt.startswith("int4")
+    q, s, w = _int8_exact_case(rng, n, k, fmt.endswith("_f16"), qmax=7 if four else 127)
     assert np.array_equal(w.astype(np.float64), q * np.repeat(s, 64, axis=1)[:, :k])
     c, sc, g = pack.pack(fmt, w)
-    assert c.shape == (n, k) and sc.nbytes == n * -(-k // 64) * (4 if fmt == "int8" else 2)
-    assert np.array_equal(c.view(np.int8), q.astype(np.int8))
-    got_s = sc.view(np.float32 if fmt == "int8" else np.float16).reshape(n, -1).astype(np.float64)
+    assert c.shape == (n, k // 2 if four else k)
+    assert sc.nbytes == n * -(-k // 64) * (2 if fmt.endswith("_f16") else 4)
+    if four:   # two's-complement nibbles, element 2i in the low nibble of byte i
+        assert np.array_equal(c & 0xF, (q[:, 0::2] & 0xF).astype(np.uint8))
+        assert np.array_equal(c >> 4, (q[:, 1::2] & 0xF).astype(np.uint8))
+    else:
+        assert np.array_equal(c.view(np.int8), q.astype(np.int8))
+    got_s = sc.view(np.float16 if fmt.endswith("_f16") else np.float32).reshape(n, -1).astype(np.float64)
     assert np.array_equal(got_s, s)
     assert np.array_equal(reference.dequant_exact(fmt, c, sc, g, n, k), w.astype(np.float64))
 
@@ -320,3 +329,23 @@ def test_int8_f16_scale_underflow_quantizes_to_zero():
     assert s.view(np.float16)[0] == 0 and not c[0].any()
     assert not reference.dequant_exact("int8_f16", c, s, g, 2, 64)[0].any()
     assert c.view(np.int8)[1, 0] == 127
+
+
+@pytest.mark.parametrize("fmt", ["int4", "int4_f16"])
+def test_int4_rounds_half_away_and_clamps(fmt):
+    # PR #250 intN codec: sign-extend from bit 3, clamp to +-7
+    w = np.zeros((1, 64), np.float32)
+    w[0, 0] = 7.0                            # scale exactly 1
+    w[0, 1:6] = [2.5, -2.5, 6.5, -0.5, -7.0]
+    c, s, _ = pack.pack(fmt, w)
+    assert s.view(np.float16 if fmt == "int4_f16" else np.float32)[0] == 1.0
+    q = reference.unpack_codes(fmt, c, 1, 64)[0, :6]
+    assert list(q) == [7, 3, 0xD, 7, 0xF, 0x9]           # 3, -3, 7 (6.5 away), -1, -7 as nibbles
+    assert list(reference.dequant_exact(fmt, c, s, 1.0, 1, 64)[0, :6]) == [7, 3, -3, 7, -1, -7]
+
+
+def test_int4_nibble_eight_decodes_as_minus_eight():
+    # the packer never writes 0x8, but a stored 0x8 sign-extends to -8
+    c = np.full((1, 32), 0x88, np.uint8)
+    s = np.array([1.0], np.float32).view(np.uint8).reshape(1, -1)
+    assert (reference.dequant_exact("int4", c, s, 1.0, 1, 64) == -8).all()

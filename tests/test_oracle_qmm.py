@@ -42,6 +42,8 @@ def _lib_elem(fmt, c):
         return Fraction(float(np.array([c << 8], np.uint16).view(np.float16)[0]))
     if fmt in ("mxint8", "int8", "int8_f16"):
         return Fraction(c - 256 if c >= 128 else c)
+    if fmt in ("int4", "int4_f16"):
+        return Fraction(c - 16 if c >= 8 else c)
     return Fraction(c)
 
 
@@ -51,9 +53,9 @@ def _lib_scale(fmt, sbytes, n, b):
     if fmt == "nvfp4":
         v = torch.tensor([int(sbytes[n][b])], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()
         return Fraction(v), Fraction(0)
-    if fmt in ("nvfp8", "int8"):
+    if fmt in ("nvfp8", "int8", "int4"):
         return Fraction(float(np.frombuffer(bytes(sbytes[n][4 * b:4 * b + 4]), "<f4")[0])), Fraction(0)
-    if fmt in ("nvfp8_f16", "int8_f16"):
+    if fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):
         return Fraction(float(np.frombuffer(bytes(sbytes[n][2 * b:2 * b + 2]), "<f2")[0])), Fraction(0)
     raw = bytes(sbytes[n][4 * b:4 * b + 4])
     s_bits, b_bits = np.frombuffer(raw, "<u2")
@@ -69,7 +71,7 @@ def _brute_qmm(fmt, codes, scales, g, x64, m, n, k):
     for j in range(n):
         wrow = []
         for kk in range(k):
-            if fmt in ("mxfp4", "nvfp4", "int4_affine"):
+            if fmt in ("mxfp4", "nvfp4", "int4_affine", "int4", "int4_f16"):
                 byte = codes[j][kk // 2]
                 c = (byte >> (4 * (kk % 2))) & 0xF
             else:
@@ -120,8 +122,9 @@ def test_dequant_f32_is_one_rounding_of_exact(fmt):
     blk = pack.BLOCK[fmt]
     for j in range(n):
         for kk in range(k):
-            byte = codes[j][kk // 2] if fmt in ("mxfp4", "nvfp4", "int4_affine") else codes[j][kk]
-            cc = (byte >> (4 * (kk % 2))) & 0xF if fmt in ("mxfp4", "nvfp4", "int4_affine") else byte
+            four = pack.ELEM_BITS[fmt] == 4
+            byte = codes[j][kk // 2] if four else codes[j][kk]
+            cc = (byte >> (4 * (kk % 2))) & 0xF if four else byte
             mul, add = _lib_scale(fmt, scales, j, kk // blk)
             w = _lib_elem(fmt, cc) * mul + add
             if fmt == "nvfp4":

@@ -24,7 +24,7 @@ namespace qfmt_dev {
 
 enum Fmt {
   MXFP4 = 1, NVFP4 = 2, MXFP8_E4M3 = 3, MXFP8_E5M2 = 4, NVFP8 = 5, INT4_AFFINE = 6, NVFP8_F16 = 7, MXINT8 = 8,
-  INT8 = 9, INT8_F16 = 10
+  INT8 = 9, INT8_F16 = 10, INT4 = 11, INT4_F16 = 12
 };
 
 template <int F> struct FmtTraits;
@@ -38,6 +38,8 @@ template <> struct FmtTraits<NVFP8_F16> { static constexpr bool four = false; st
 template <> struct FmtTraits<MXINT8> { static constexpr bool four = false; static constexpr int block = 32; static constexpr int sbytes = 1; };
 template <> struct FmtTraits<INT8> { static constexpr bool four = false; static constexpr int block = 64; static constexpr int sbytes = 4; };
 template <> struct FmtTraits<INT8_F16> { static constexpr bool four = false; static constexpr int block = 64; static constexpr int sbytes = 2; };
+template <> struct FmtTraits<INT4> { static constexpr bool four = true; static constexpr int block = 64; static constexpr int sbytes = 4; };
+template <> struct FmtTraits<INT4_F16> { static constexpr bool four = true; static constexpr int block = 64; static constexpr int sbytes = 2; };
 
 // 8-bit elements under an E8M0 scale per 32 (mxfp8 E4M3/E5M2, mxint8), and
 // every E8M0-scaled format (those and mxfp4)
@@ -55,12 +57,51 @@ constexpr bool is_fs8() { return F == NVFP8 || F == NVFP8_F16 || F == INT8 || F 
 template <int F>
 constexpr bool is_int8() { return F == MXINT8 || F == INT8 || F == INT8_F16; }
 
+// 4-bit integer elements with one (scale, bias) per group of 64: int4 affine
+// (stored bf16 pair), and the symmetric int4 / int4_f16 (float32 / half
+// scale, bias -8 s on the code with its sign bit flipped, see i4_u)
+template <int F>
+constexpr bool is_i4() { return F == INT4_AFFINE || F == INT4 || F == INT4_F16; }
+template <int F>
+constexpr bool is_i4sym() { return F == INT4 || F == INT4_F16; }
+inline constexpr bool fmt_is_i4(int f) { return f == INT4_AFFINE || f == INT4 || f == INT4_F16; }
+inline constexpr bool fmt_is_four(int f) { return f == MXFP4 || f == NVFP4 || fmt_is_i4(f); }
+
 // Block scale idx of a float-scaled array as float32: the stored float32, or
 // the (exact) float32 of the stored IEEE half.
 template <int F>
-__device__ __forceinline__ float fs8_scale(const uint8_t* scales, int64_t idx) {
+__device__ __forceinline__ float float_scale(const uint8_t* scales, int64_t idx) {
   if constexpr (FmtTraits<F>::sbytes == 4) return __ldg(reinterpret_cast<const float*>(scales) + idx);
   else return __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(scales) + idx)));
+}
+
+// Raw scale word of group idx of a 4-bit integer format: int4 affine's
+// (scale, bias) bf16 pair, the float32 bits, or the half bits (zero-extended).
+template <int F>
+__device__ __forceinline__ uint32_t i4_word(const uint8_t* scales, int64_t idx) {
+  if constexpr (FmtTraits<F>::sbytes == 2) return __ldg(reinterpret_cast<const unsigned short*>(scales) + idx);
+  else return __ldg(reinterpret_cast<const uint32_t*>(scales) + idx);
+}
+
+// (scale, bias) of a group from its raw word, for the unsigned u of i4_u:
+// w = s * u + b.  Symmetric: u = q + 8, so b = -8 s.
+template <int F>
+__device__ __forceinline__ void i4_scale_bias(uint32_t wd, float& s, float& b) {
+  if constexpr (F == INT4_AFFINE) {
+    s = __uint_as_float(wd << 16);
+    b = __uint_as_float(wd & 0xFFFF0000u);
+  } else {
+    s = FmtTraits<F>::sbytes == 4 ? __uint_as_float(wd) : __half2float(__ushort_as_half((unsigned short)wd));
+    b = -8.0f * s;
+  }
+}
+
+// 8 nibble codes as the unsigned u the affine decode works on: a symmetric
+// two's-complement nibble q becomes u = q + 8 by flipping its sign bit.
+template <int F>
+__device__ __forceinline__ uint32_t i4_u(uint32_t w) {
+  if constexpr (is_i4sym<F>()) return w ^ 0x88888888u;
+  else return w;
 }
 
 // ------------------------------------------------------------------ exact ---
@@ -259,9 +300,9 @@ __device__ __forceinline__ PieceScale load_piece_scale(const uint8_t* scales, in
   } else if constexpr (F == NVFP4) {
     s.a = __ldg(reinterpret_cast<const unsigned short*>(scales + base + k0 / 16));
   } else if constexpr (is_fs8<F>()) {
-    s.a = __float_as_uint(fs8_scale<F>(scales, base + k0 / FmtTraits<F>::block));
+    s.a = __float_as_uint(float_scale<F>(scales, base + k0 / FmtTraits<F>::block));
   } else {
-    s.a = __ldg(reinterpret_cast<const uint32_t*>(scales) + base + k0 / 64);
+    s.a = i4_word<F>(scales, base + k0 / 64);
   }
   return s;
 }
@@ -291,7 +332,8 @@ __device__ __forceinline__ void decode_piece(const uint4& v, const PieceScale& p
       A[2 * j + 1][0] = hmul2(r[2], sc);
       A[2 * j + 1][1] = hmul2(r[3], sc);
     }
-  } else if constexpr (F == INT4_AFFINE) {
+  } else if constexpr (is_i4<F>()) {
+    static_assert(F == INT4_AFFINE, "the symmetric int4 formats decode through decode_piece_hilo");
     const uint32_t s2 = bf16x2_splat(ps.a & 0xFFFFu), b2 = bf16x2_splat(ps.a >> 16);
     #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -411,16 +453,23 @@ __device__ __forceinline__ void decode_piece_hilo(const uint4& v, const PieceSca
       split_bf16x2(v0, v1, hi[2 * j], lo[2 * j]);
       split_bf16x2(v2, v3, hi[2 * j + 1], lo[2 * j + 1]);
     }
-  } else {
-    const float s = bf16bits_f32(ps.a & 0xFFFFu), b = bf16bits_f32(ps.a >> 16);
+  } else {   // int4 affine: fma(s, q, b); symmetric int4: s * q (one rounding either way)
+    float s, b;
+    i4_scale_bias<F>(ps.a, s, b);
     #pragma unroll
     for (int j = 0; j < 4; ++j) {
       #pragma unroll
       for (int p = 0; p < 4; ++p) {
         const uint32_t byte = (w[j] >> (8 * p)) & 0xFFu;
-        const float q0 = __fsub_rn(__uint_as_float(0x4B000000u | (byte & 0xFu)), 8388608.0f);
-        const float q1 = __fsub_rn(__uint_as_float(0x4B000000u | (byte >> 4)), 8388608.0f);
-        split_bf16x2(__fmaf_rn(s, q0, b), __fmaf_rn(s, q1, b), hi[4 * j + p], lo[4 * j + p]);
+        float q0 = __fsub_rn(__uint_as_float(0x4B000000u | (byte & 0xFu)), 8388608.0f);
+        float q1 = __fsub_rn(__uint_as_float(0x4B000000u | (byte >> 4)), 8388608.0f);
+        if constexpr (is_i4sym<F>()) {   // the sign-extended nibble
+          q0 = q0 >= 8.0f ? q0 - 16.0f : q0;
+          q1 = q1 >= 8.0f ? q1 - 16.0f : q1;
+          split_bf16x2(__fmul_rn(s, q0), __fmul_rn(s, q1), hi[4 * j + p], lo[4 * j + p]);
+        } else {
+          split_bf16x2(__fmaf_rn(s, q0, b), __fmaf_rn(s, q1, b), hi[4 * j + p], lo[4 * j + p]);
+        }
       }
     }
   }

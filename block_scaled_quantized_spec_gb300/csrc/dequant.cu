@@ -28,6 +28,7 @@ __device__ __forceinline__ float dq_value(uint32_t code, float s, float b, float
   if constexpr (F == MXFP8_E5M2) return __fmul_rn(e5m2_f32(code), s);
   if constexpr (is_int8<F>()) return __fmul_rn(float(int8_t(uint8_t(code))), s);
   if constexpr (is_fs8<F>()) return __fmul_rn(e4m3_f32(code), s);
+  if constexpr (is_i4sym<F>()) return __fmul_rn(float(int(code ^ 8u) - 8), s);         // the sign-extended nibble
   return __fmaf_rn(s, float(code), b);                                               // INT4_AFFINE
 }
 
@@ -37,7 +38,7 @@ __device__ __forceinline__ void dq_scale(const uint8_t* scales, int64_t idx, flo
   b = 0.0f;
   if constexpr (is_e8m0<F>()) s = e8m0_f32(scales[idx]);
   else if constexpr (F == NVFP4) s = e4m3_f32(scales[idx]);
-  else if constexpr (is_fs8<F>()) s = fs8_scale<F>(scales, idx);
+  else if constexpr (is_fs8<F>() || is_i4sym<F>()) s = float_scale<F>(scales, idx);
   else {
     const uint32_t p = reinterpret_cast<const uint32_t*>(scales)[idx];
     s = bf16bits_f32(p & 0xFFFFu);
@@ -128,6 +129,8 @@ cudaError_t launch_dequant(int fmt, const void* codes, const void* scales, float
     case MXINT8: return launch_dequant_fmt<MXINT8>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case INT8: return launch_dequant_fmt<INT8>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case INT8_F16: return launch_dequant_fmt<INT8_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case INT4: return launch_dequant_fmt<INT4>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case INT4_F16: return launch_dequant_fmt<INT4_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     default: return launch_dequant_fmt<INT4_AFFINE>(codes, scales, glob, out, out_bf16, N, K, st, sms);
   }
 }

@@ -35,22 +35,39 @@ int fail(int status, const char* fmt, ...) {
 
 void clear_error() { g_err[0] = '\0'; }
 
-bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_INT8_F16; }
+bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_INT4_F16; }
 
 int block_of(int fmt) {
   switch (fmt) {
     case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: return 32;
     case QFMT_NVFP4: case QFMT_NVFP8: case QFMT_NVFP8_F16: return 16;
-    case QFMT_INT4_AFFINE: case QFMT_INT8: case QFMT_INT8_F16: return 64;
+    case QFMT_INT4_AFFINE: case QFMT_INT8: case QFMT_INT8_F16: case QFMT_INT4: case QFMT_INT4_F16: return 64;
     default: return 0;
   }
 }
 
-bool is_4bit(int fmt) { return fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4 || fmt == QFMT_INT4_AFFINE; }
+bool is_4bit(int fmt) {
+  return fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4 || fmt == QFMT_INT4_AFFINE || fmt == QFMT_INT4 || fmt == QFMT_INT4_F16;
+}
+
+bool is_sym_int(int fmt) {
+  return fmt == QFMT_MXINT8 || fmt == QFMT_INT8 || fmt == QFMT_INT8_F16 || fmt == QFMT_INT4 || fmt == QFMT_INT4_F16;
+}
+
+// Largest finite element magnitude: amax / elem_max is the raw block scale.
+float elem_max(int fmt) {
+  switch (fmt) {
+    case QFMT_MXFP4: case QFMT_NVFP4: return 6.0f;
+    case QFMT_MXFP8_E5M2: return 57344.0f;
+    case QFMT_MXINT8: case QFMT_INT8: case QFMT_INT8_F16: return 127.0f;
+    case QFMT_INT4: case QFMT_INT4_F16: return 7.0f;
+    default: return 448.0f;   // E4M3
+  }
+}
 
 int scale_entry_bytes(int fmt) {
-  if (fmt == QFMT_NVFP8 || fmt == QFMT_INT4_AFFINE || fmt == QFMT_INT8) return 4;
-  return (fmt == QFMT_NVFP8_F16 || fmt == QFMT_INT8_F16) ? 2 : 1;
+  if (fmt == QFMT_NVFP8 || fmt == QFMT_INT4_AFFINE || fmt == QFMT_INT8 || fmt == QFMT_INT4) return 4;
+  return (fmt == QFMT_NVFP8_F16 || fmt == QFMT_INT8_F16 || fmt == QFMT_INT4_F16) ? 2 : 1;
 }
 
 int check_group(int fmt, int group) {
@@ -180,7 +197,7 @@ using namespace qfmt;
 
 extern "C" {
 
-int qfmt_version(void) { return 103; }
+int qfmt_version(void) { return 104; }
 
 const char* qfmt_last_error(void) { return qfmt::g_err; }
 
@@ -270,9 +287,7 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
         float eff;
         switch (fmt) {
           case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: {
-            const float maxf = fmt == QFMT_MXFP4 ? 6.0f
-                             : fmt == QFMT_MXFP8_E4M3 ? 448.0f : fmt == QFMT_MXINT8 ? 127.0f : 57344.0f;
-            const float s = amax > 0.0f ? amax / maxf : 1.0f;
+            const float s = amax > 0.0f ? amax / elem_max(fmt) : 1.0f;
             const uint32_t code = enc_e8m0_ceil(s);
             sb[n * nb + b] = uint8_t(code);
             eff = dec_e8m0(code);
@@ -284,15 +299,15 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
             eff = dec_e4m3(u) * glob;
             break;
           }
-          case QFMT_NVFP8_F16: case QFMT_INT8_F16: {  // the scale stored as an IEEE half, rounded to nearest even
-            const float s = amax > 0.0f ? amax / (fmt == QFMT_INT8_F16 ? 127.0f : 448.0f) : 1.0f;
+          case QFMT_NVFP8_F16: case QFMT_INT8_F16: case QFMT_INT4_F16: {  // an IEEE half, rounded to nearest even
+            const float s = amax > 0.0f ? amax / elem_max(fmt) : 1.0f;
             const _Float16 h = static_cast<_Float16>(s);
             std::memcpy(sb + (n * nb + b) * 2, &h, 2);
             eff = static_cast<float>(h);
             break;
           }
-          default: {  // QFMT_NVFP8, QFMT_INT8: the float32 scale stored raw
-            const float s = amax > 0.0f ? amax / (fmt == QFMT_INT8 ? 127.0f : 448.0f) : 1.0f;
+          default: {  // QFMT_NVFP8, QFMT_INT8, QFMT_INT4: the float32 scale stored raw
+            const float s = amax > 0.0f ? amax / elem_max(fmt) : 1.0f;
             std::memcpy(sb + (n * nb + b) * 4, &s, 4);
             eff = s;
             break;
@@ -303,8 +318,9 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
           uint32_t code = 0;
           if (eff != 0.0f) {
             const float v = wb[j] / eff;
-            if (fmt == QFMT_MXINT8 || fmt == QFMT_INT8 || fmt == QFMT_INT8_F16) {  // symmetric: round half away from zero, clamp to +-127
-              code = uint32_t(uint8_t(int8_t(std::max(-127.0f, std::min(127.0f, std::round(v))))));
+            if (is_sym_int(fmt)) {  // symmetric: round half away from zero, clamp to +-max, two's complement
+              const float qm = elem_max(fmt);
+              code = uint32_t(uint8_t(int8_t(std::max(-qm, std::min(qm, std::round(v)))))) & (four ? 0xFu : 0xFFu);
               put_code(crow, b * blk + j, code, four);
               continue;
             }

@@ -56,7 +56,7 @@ constexpr int B_BYTES = 256 * BK * 2;     // 32 KiB: 256 bf16 rows, or 128 hi ro
 // formats exact in bf16; 8 for nvfp8 and int4 affine, whose hi + lo tiles were
 // measured faster with eight.
 template <int F> struct Dec {
-  static constexpr int WARPS = (F == INT4_AFFINE || is_fs8<F>()) ? 8 : 16;
+  static constexpr int WARPS = (is_i4<F>() || is_fs8<F>()) ? 8 : 16;
   static constexpr int THREADS = WARPS * 32;
   static constexpr int CTA_THREADS = (2 + WARPS) * 32;
 };
@@ -74,7 +74,7 @@ template <int MT> struct Pipe {
 // affine carry each weight as a hi + lo bf16 pair (two MMAs per K slice into
 // one accumulator) on a 128 x 128 tile, so a stage holds the same bytes.
 template <int F> struct Tile {
-  static constexpr bool split = is_fs8<F>() || F == INT4_AFFINE;
+  static constexpr bool split = is_fs8<F>() || is_i4<F>();
   static constexpr int BN = split ? 128 : 256;
 };
 
@@ -664,6 +664,8 @@ cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, floa
     case MXINT8: return tc::launch_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT8: return tc::launch_fmt<INT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT8_F16: return tc::launch_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case INT4: return tc::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case INT4_F16: return tc::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return tc::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }

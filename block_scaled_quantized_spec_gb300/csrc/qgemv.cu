@@ -93,7 +93,7 @@ struct Cfg {
   static constexpr int BLK = FmtTraits<F>::block;
   static constexpr int SEGS = four ? 2 : 4;        // 16-byte row segments per 64-code unit
   // staged scale words per row per 64-code unit (int4 affine: s and b - 1024 s)
-  static constexpr int SPU = F == INT4_AFFINE ? 2 : 64 / BLK;
+  static constexpr int SPU = is_i4<F>() ? 2 : 64 / BLK;
 };
 
 // Staged scale-row stride in 32-bit words: a multiple of 4 plus 4, so the
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
   using C = Cfg<F, R>;
   constexpr bool FOUR = C::four;
   constexpr int SEGS = C::SEGS, SPU = C::SPU, BLK = C::BLK;
-  constexpr bool I4 = F == INT4_AFFINE;
+  constexpr bool I4 = is_i4<F>();
   constexpr int ROWS = 16 * R;
   constexpr int RC = 8 * NB;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -214,10 +214,10 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
         } else if constexpr (F == NVFP4) {
           wsc[rr * sst + e] = __uint_as_float(ok ? e4m3_f16x2_splat(__ldg(scales + gi)) : 0u);
         } else if constexpr (is_fs8<F>()) {
-          wsc[rr * sst + e] = ok ? fs8_scale<F>(scales, gi) : 0.0f;
+          wsc[rr * sst + e] = ok ? float_scale<F>(scales, gi) : 0.0f;
         } else {
-          const uint32_t pr = ok ? __ldg(reinterpret_cast<const uint32_t*>(scales) + gi) : 0u;
-          const float sc = bf16bits_f32(pr & 0xFFFFu), bi = bf16bits_f32(pr >> 16);
+          float sc, bi;
+          i4_scale_bias<F>(ok ? i4_word<F>(scales, gi) : 0u, sc, bi);
           wsc[rr * sst + 2 * e] = sc;
           wsc[rr * sst + 2 * e + 1] = __fmaf_rn(-1024.0f, sc, bi);
         }
@@ -341,8 +341,8 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
             if constexpr (FOUR) {
               uint32_t fa[4], fb[4];
               if constexpr (I4) {
-                int4x8_f16_biased(wa, fa);
-                int4x8_f16_biased(wb, fb);
+                int4x8_f16_biased(i4_u<F>(wa), fa);
+                int4x8_f16_biased(i4_u<F>(wb), fb);
               } else {
                 e2m1x8_f16(wa, fa);
                 e2m1x8_f16(wb, fb);
@@ -446,7 +446,7 @@ template <int F, int NB, int R>
 inline size_t smem_bytes(int M, int KS) {
   const int units = KS / 64;
   return size_t(16 * R) * code_stride<F>(KS) + size_t(M) * (KS + 8) * 2 +
-         size_t(M) * units * 4 * (F == INT4_AFFINE ? 2 : 1) + size_t(16 * R) * sc_stride<F, R>(KS) * 4 +
+         size_t(M) * units * 4 * (is_i4<F>() ? 2 : 1) + size_t(16 * R) * sc_stride<F, R>(KS) * 4 +
          size_t(WARPS) * 16 * R * 8 * NB * 4;
 }
 
@@ -538,6 +538,8 @@ cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float g
     case MXINT8: return gemv::launch_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case INT8: return gemv::launch_fmt<INT8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case INT8_F16: return gemv::launch_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case INT4: return gemv::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case INT4_F16: return gemv::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     default: return gemv::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }

@@ -98,8 +98,8 @@ template <int F>
 __device__ __forceinline__ void frags8(const uint4& v, int q, uint32_t r[4]) {
   if constexpr (F == MXFP4 || F == NVFP4) {
     e2m1x8_f16(word(v, q), r);
-  } else if constexpr (F == INT4_AFFINE) {
-    const uint32_t w = word(v, q);
+  } else if constexpr (is_i4<F>()) {
+    const uint32_t w = i4_u<F>(word(v, q));
     #pragma unroll
     for (int b = 0; b < 4; ++b) r[b] = ((w >> (4 * b)) & 0x000F000Fu) | 0x64006400u;
   } else {
@@ -151,7 +151,7 @@ __host__ __device__ constexpr int xstride(int K) {
 
 inline size_t smem_bytes(int F, int M, int K, int warps = WARPS) {
   const int spans = K / 32;
-  return size_t(M) * xstride(K) * 2 + 64 + size_t(M) * spans * 4 * (F == INT4_AFFINE ? 2 : 1) +
+  return size_t(M) * xstride(K) * 2 + 64 + size_t(M) * spans * 4 * (fmt_is_i4(F) ? 2 : 1) +
          size_t(warps) * 2 * 16 * 4 + size_t(warps) * 2 * 4;
 }
 
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   using S = Shape<F>;
   constexpr int P = chunks_per_warp<F, W>();
   constexpr int WARPS = W, THREADS = 32 * W;
-  constexpr bool FOUR = S::four, I4 = F == INT4_AFFINE;
+  constexpr bool FOUR = S::four, I4 = is_i4<F>();
   constexpr int CODES = S::CODES, LANE = S::LANE;
   extern __shared__ __align__(16) uint8_t smem[];
   const int xst = xstride(K);
@@ -305,19 +305,19 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
     } else if constexpr (is_fs8<F>()) {
       constexpr int B = FmtTraits<F>::block;                                  // 16 (nvfp8) or 64 (int8)
       const int e = k0 / B;
-      cs[i].a0 = c0 ? __float_as_uint(fs8_scale<F>(sra, e)) : 0u;
-      cs[i].b0 = c0 ? __float_as_uint(fs8_scale<F>(srb, e)) : 0u;
+      cs[i].a0 = c0 ? __float_as_uint(float_scale<F>(sra, e)) : 0u;
+      cs[i].b0 = c0 ? __float_as_uint(float_scale<F>(srb, e)) : 0u;
       if constexpr (B == 16) {
-        cs[i].a1 = c1 ? __float_as_uint(fs8_scale<F>(sra, e + 1)) : 0u;
-        cs[i].b1 = c1 ? __float_as_uint(fs8_scale<F>(srb, e + 1)) : 0u;
+        cs[i].a1 = c1 ? __float_as_uint(float_scale<F>(sra, e + 1)) : 0u;
+        cs[i].b1 = c1 ? __float_as_uint(float_scale<F>(srb, e + 1)) : 0u;
       } else {                                                                // a0, a0 + 1 share it
         cs[i].a1 = c1 ? cs[i].a0 : 0u;
         cs[i].b1 = c1 ? cs[i].b0 : 0u;
       }
-    } else if constexpr (F == INT4_AFFINE) {
+    } else if constexpr (is_i4<F>()) {
       const int e = k0 / 64;                                                  // a0, a0 + 1 share it
-      cs[i].a0 = c0 ? __ldg(reinterpret_cast<const uint32_t*>(sra) + e) : 0u;
-      cs[i].b0 = c0 ? __ldg(reinterpret_cast<const uint32_t*>(srb) + e) : 0u;
+      cs[i].a0 = c0 ? i4_word<F>(sra, e) : 0u;
+      cs[i].b0 = c0 ? i4_word<F>(srb, e) : 0u;
       cs[i].a1 = cs[i].b1 = 0u;
     } else {   // NVFP4: the lane's own two micro-blocks, one 16-bit pair per row
       const int e = ks / 32;                                                  // pair index (16-code blocks / 2)
@@ -559,12 +559,15 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
         acc_a = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].a1), x1s), d[ii][1], acc_a);
         acc_b = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].b0), x0s), d[ii][2], acc_b);
         acc_b = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].b1), x1s), d[ii][3], acc_b);
-      } else if constexpr (F == INT4_AFFINE) {
-        // sum_k x~ (1024 + q): s * D + (b - 1024 s) * sum(x~), then the span's 2^-shift
+      } else if constexpr (is_i4<F>()) {
+        // sum_k x~ (1024 + u): s * D + (b - 1024 s) * sum(x~), then the span's 2^-shift
         // a second span past K (a ragged last group of 32) adds no bias term
         const float m0 = xsum[md * spans + s0], m1 = k0 + LANE < K ? xsum[md * spans + s1] : 0.0f;
-        const float sa = bf16bits_f32(cs[i].a0 & 0xFFFFu), ba = __fmaf_rn(-1024.0f, sa, bf16bits_f32(cs[i].a0 >> 16));
-        const float sb = bf16bits_f32(cs[i].b0 & 0xFFFFu), bb = __fmaf_rn(-1024.0f, sb, bf16bits_f32(cs[i].b0 >> 16));
+        float sa, ba, sb, bb;
+        i4_scale_bias<F>(cs[i].a0, sa, ba);
+        i4_scale_bias<F>(cs[i].b0, sb, bb);
+        ba = __fmaf_rn(-1024.0f, sa, ba);
+        bb = __fmaf_rn(-1024.0f, sb, bb);
         acc_a = __fmaf_rn(x0s, __fmaf_rn(sa, d[ii][0], ba * m0), acc_a);
         acc_a = __fmaf_rn(x1s, __fmaf_rn(sa, d[ii][1], ba * m1), acc_a);
         acc_b = __fmaf_rn(x0s, __fmaf_rn(sb, d[ii][2], bb * m0), acc_b);
@@ -728,6 +731,8 @@ cudaError_t launch_qgemv_m2(int fmt, const void* codes, const void* scales, floa
     case MXINT8: return gemv_m2::launch_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT8: return gemv_m2::launch_fmt<INT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT8_F16: return gemv_m2::launch_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case INT4: return gemv_m2::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case INT4_F16: return gemv_m2::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_m2::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }
@@ -750,6 +755,9 @@ cudaError_t launch_qgemv_gather(int fmt, const void* codes, const void* scales, 
     case INT8: return gemv_m2::launch_gather_fmt<INT8>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
     case INT8_F16:
       return gemv_m2::launch_gather_fmt<INT8_F16>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    case INT4: return gemv_m2::launch_gather_fmt<INT4>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    case INT4_F16:
+      return gemv_m2::launch_gather_fmt<INT4_F16>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
     default:
       return gemv_m2::launch_gather_fmt<INT4_AFFINE>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
   }
@@ -798,6 +806,8 @@ cudaError_t launch_qgemv_multi(int fmt, int count, const void* const* codes, con
     case MXINT8: QFMT_MULTI(MXINT8);
     case INT8: QFMT_MULTI(INT8);
     case INT8_F16: QFMT_MULTI(INT8_F16);
+    case INT4: QFMT_MULTI(INT4);
+    case INT4_F16: QFMT_MULTI(INT4_F16);
     default: QFMT_MULTI(INT4_AFFINE);
   }
 #undef QFMT_MULTI

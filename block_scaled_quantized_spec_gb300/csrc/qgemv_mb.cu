@@ -43,7 +43,7 @@ constexpr size_t X_BUDGET = 40 * 1024;  // staged f16 activations per CTA (five 
 // 64-byte chunks per lane in flight: four; two for nvfp8 and int4 affine,
 // whose per-chunk scales (eight float32, four scale/bias pairs) stay in registers
 template <int F>
-constexpr int chunks_in_flight() { return (is_fs8<F>() || F == INT4_AFFINE) ? 2 : 4; }
+constexpr int chunks_in_flight() { return (is_fs8<F>() || is_i4<F>()) ? 2 : 4; }
 
 template <int F>
 struct Shape {
@@ -155,15 +155,15 @@ __device__ __forceinline__ float ld_cluster_f32(const float* p, uint32_t rank) {
 // Shared memory of one CTA: staged activations [M][xst] f16, their scales
 // [M][kr/128 + 1] (and int4-affine span sums [M][kr/64 + 1]), the partial tile [64][16].
 inline size_t smem_bytes(int F, int M, int kr) {
-  const int rb = (F == MXFP4 || F == NVFP4 || F == INT4_AFFINE) ? 64 : 32;
+  const int rb = fmt_is_four(F) ? 64 : 32;
   return size_t(M) * xstride(kr, rb) * 2 + size_t(M) * (kr / XSPAN + 1) * 4 +
-         (F == INT4_AFFINE ? size_t(M) * (kr / 64 + 1) * 4 : 0) + size_t(ROWS) * 16 * 4;
+         (fmt_is_i4(F) ? size_t(M) * (kr / 64 + 1) * 4 : 0) + size_t(ROWS) * 16 * 4;
 }
 
 // Raw scale words a lane keeps per chunk: 2 (rows g, g + 8) for the byte
 // scales, 4 for int4 affine (two blocks), 8 for nvfp8 (four float32 blocks).
 template <int F>
-constexpr int scale_words() { return is_fs8<F>() ? 8 : (F == INT4_AFFINE ? 4 : 2); }
+constexpr int scale_words() { return is_fs8<F>() ? 8 : (is_i4<F>() ? 4 : 2); }
 
 template <int F, int NB, bool UNI>
 __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __restrict__ codes,
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
                                                            const uint16_t* __restrict__ x, void* __restrict__ out,
                                                            int out_f32, int M, int N, int K, int KR) {
   using S = Shape<F>;
-  constexpr bool FOUR = S::four, I4 = F == INT4_AFFINE;
+  constexpr bool FOUR = S::four, I4 = is_i4<F>();
   constexpr int CODES = S::CODES, SEG = S::SEG;
   constexpr int BLK = FmtTraits<F>::block, SB = FmtTraits<F>::sbytes;
   constexpr int SW = scale_words<F>();
@@ -257,17 +257,15 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       #pragma unroll
       for (int sg = 0; sg < 4; ++sg) {
         const int k = kc + sg * SEG;
-        sc[i][sg] = live(k) ? __float_as_uint(fs8_scale<F>(sra, k / FmtTraits<F>::block)) : 0u;
-        sc[i][4 + sg] = live(k) ? __float_as_uint(fs8_scale<F>(srb, k / FmtTraits<F>::block)) : 0u;
+        sc[i][sg] = live(k) ? __float_as_uint(float_scale<F>(sra, k / FmtTraits<F>::block)) : 0u;
+        sc[i][4 + sg] = live(k) ? __float_as_uint(float_scale<F>(srb, k / FmtTraits<F>::block)) : 0u;
       }
     } else {                                                                // int4 affine: (scale, bias) per 64
-      const uint32_t* ua = reinterpret_cast<const uint32_t*>(sra);
-      const uint32_t* ub = reinterpret_cast<const uint32_t*>(srb);
       #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int k = kc + h * 64;
-        sc[i][h] = live(k) ? __ldg(ua + k / 64) : 0u;
-        sc[i][2 + h] = live(k) ? __ldg(ub + k / 64) : 0u;
+        sc[i][h] = live(k) ? i4_word<F>(sra, k / 64) : 0u;
+        sc[i][2 + h] = live(k) ? i4_word<F>(srb, k / 64) : 0u;
       }
     }
   };
@@ -402,8 +400,8 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             if constexpr (I4) {
               #pragma unroll
               for (int b = 0; b < 4; ++b) {
-                fa[b] = ((wa[i][sg] >> (4 * b)) & 0x000F000Fu) | 0x43004300u;   // bf16 128 + q
-                fb[b] = ((wb[i][sg] >> (4 * b)) & 0x000F000Fu) | 0x43004300u;
+                fa[b] = ((i4_u<F>(wa[i][sg]) >> (4 * b)) & 0x000F000Fu) | 0x43004300u;   // bf16 128 + u
+                fb[b] = ((i4_u<F>(wb[i][sg]) >> (4 * b)) & 0x000F000Fu) | 0x43004300u;
               }
             } else {
               e2m1x8_f16(wa[i][sg], fa);
@@ -458,10 +456,10 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
               sb = __uint_as_float(sc[i][4 + sg]);
             } else if constexpr (I4) {                                      // s * D + (b - 128 s) * sum(x)
               const int h = sg >> 1;
-              sa = bf16bits_f32(sc[i][h] & 0xFFFFu);
-              sb = bf16bits_f32(sc[i][2 + h] & 0xFFFFu);
-              ba = __fmaf_rn(-128.0f, sa, bf16bits_f32(sc[i][h] >> 16));
-              bb = __fmaf_rn(-128.0f, sb, bf16bits_f32(sc[i][2 + h] >> 16));
+              i4_scale_bias<F>(sc[i][h], sa, ba);
+              i4_scale_bias<F>(sc[i][2 + h], sb, bb);
+              ba = __fmaf_rn(-128.0f, sa, ba);
+              bb = __fmaf_rn(-128.0f, sb, bb);
               const int blk = (c * CODES) / 64 + h;
               #pragma unroll
               for (int nb = 0; nb < NB; ++nb) {
@@ -551,7 +549,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
 // range (rounded up to 128) keeps the staged activations within X_BUDGET and
 // gives at least four CTAs per SM (shorter K ranges per warp, fewer rounds).
 inline bool plan(int F, int M, int N, int K, int sms, int* S, int* KR) {
-  const int rb = (F == MXFP4 || F == NVFP4 || F == INT4_AFFINE) ? 64 : 32;
+  const int rb = fmt_is_four(F) ? 64 : 32;
   const int row_ctas = (N + ROWS - 1) / ROWS;
   for (int s = 1; s <= 8; s *= 2) {
     const int kr = ((K + s - 1) / s + XSPAN - 1) / XSPAN * XSPAN;
@@ -620,6 +618,8 @@ cudaError_t launch_qgemv_mb(int fmt, const void* codes, const void* scales, floa
     case MXINT8: return gemv_mb::launch_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT8: return gemv_mb::launch_fmt<INT8>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT8_F16: return gemv_mb::launch_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case INT4: return gemv_mb::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case INT4_F16: return gemv_mb::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_mb::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }

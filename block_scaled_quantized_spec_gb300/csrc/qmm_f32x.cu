@@ -17,6 +17,7 @@ __device__ __forceinline__ float exact_weight(uint32_t code, float s, float b) {
   if constexpr (is_int8<F>()) return __fmul_rn(float(int8_t(uint8_t(code))), s);
   if constexpr (F == MXFP8_E4M3 || is_fs8<F>()) return __fmul_rn(e4m3_f32(code), s);
   if constexpr (F == MXFP8_E5M2) return __fmul_rn(e5m2_f32(code), s);
+  if constexpr (is_i4sym<F>()) return __fmul_rn(float(int(code ^ 8u) - 8), s);
   return __fmaf_rn(s, float(code), b);
 }
 
@@ -45,7 +46,7 @@ __global__ void __launch_bounds__(256) qmm_f32x_kernel(const uint8_t* __restrict
       float s, b = 0.0f;
       if constexpr (is_e8m0<F>()) s = e8m0_f32(scales[bi]);
       else if constexpr (F == NVFP4) s = e4m3_f32(scales[bi]);
-      else if constexpr (is_fs8<F>()) s = fs8_scale<F>(scales, bi);
+      else if constexpr (is_fs8<F>() || is_i4sym<F>()) s = float_scale<F>(scales, bi);
       else {
         const uint32_t p = reinterpret_cast<const uint32_t*>(scales)[bi];
         s = bf16bits_f32(p & 0xFFFFu);
@@ -97,6 +98,8 @@ cudaError_t launch_qmm_f32x(int fmt, const void* codes, const void* scales, floa
     case MXINT8: return launch_f32x_fmt<MXINT8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case INT8: return launch_f32x_fmt<INT8>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case INT8_F16: return launch_f32x_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case INT4: return launch_f32x_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case INT4_F16: return launch_f32x_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     default: return launch_f32x_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }

@@ -28,15 +28,20 @@
  *                                                 symmetric int8, scale-only, +-127)
  *   QFMT_INT8_F16       signed int8 q      64     IEEE half (2 bytes): the fp16-scale twin
  *                                                 of QFMT_INT8
+ *   QFMT_INT4           signed 4-bit q     64     FP32 (4 bytes): w = q * scale, q the
+ *                                                 two's-complement nibble (PR #250's symmetric
+ *                                                 intN, sign-extended from bit 3, +-7)
+ *   QFMT_INT4_F16       signed 4-bit q     64     IEEE half (2 bytes): the fp16-scale twin
+ *                                                 of QFMT_INT4
  *
  * Memory layouts (all row-major, no padding, little-endian):
- *   codes   [N, K/2] bytes for 4-bit formats: element k of a row sits in byte
+ *   codes   [N, K/2] bytes for 4-bit formats (mxfp4, nvfp4, int4 affine, int4): element k of a row sits in byte
  *           k/2, low nibble for even k (LSB-first; 8 codes per u32 word);
  *           [N, K] bytes for 8-bit formats.
  *   scales  [N, ceil(K/block)] entries of the sizes above; int4 affine stores
  *           the (scale, bias) bf16 pair of each group adjacently:
  *           [N, ceil(K/64), 2].  K is a multiple of 32 for every format, so
- *           only the group-64 formats (int4 affine, int8, int8_f16) can end in
+ *           only the group-64 formats (int4 affine, int8, int4 and twins) can end in
  *           a ragged group (of 32 values, with its own scale and bias; PR
  *           #250: a ragged trailing block, the block count rounded up).
  *   X       [M, K] bf16 (or f32 through qmm_ex), out [M, N] bf16 (or f32).
@@ -85,7 +90,9 @@ typedef enum {
   QFMT_NVFP8_F16 = 7,
   QFMT_MXINT8 = 8,
   QFMT_INT8 = 9,
-  QFMT_INT8_F16 = 10
+  QFMT_INT8_F16 = 10,
+  QFMT_INT4 = 11,
+  QFMT_INT4_F16 = 12
 } qfmt_format;
 
 typedef enum { QFMT_F32 = 0, QFMT_BF16 = 1 } qfmt_dtype;

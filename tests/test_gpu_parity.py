@@ -19,7 +19,7 @@ from oracle import reference as oref  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 FMTS = list(q.FORMATS)
-GROUP64 = ["int4_affine", "int8", "int8_f16"]          # group of 64: K may end in a group of 32
+GROUP64 = ["int4_affine", "int8", "int8_f16", "int4", "int4_f16"]          # group of 64: K may end in a group of 32
 DEV = "cuda:0"
 
 
@@ -81,10 +81,10 @@ def test_dequant_all_codes_and_scales(fmt):
     sb = opack.scales_nbytes(fmt, n, k)
     if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "nvfp4"):
         scales = np.tile(np.arange(256, dtype=np.uint8), sb // 256 + 1)[:sb]
-    elif fmt in ("nvfp8", "int8"):
+    elif fmt in ("nvfp8", "int8", "int4"):
         scales = np.concatenate([rng.standard_normal(sb // 4 - 4).astype(np.float32),
                                  np.array([1e-40, 3e38, 0.0, -2.5], np.float32)]).view(np.uint8)
-    elif fmt in ("nvfp8_f16", "int8_f16"):   # evenly spaced half bit patterns: subnormals, +-inf, NaNs, both signs
+    elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):   # evenly spaced half bit patterns: subnormals, +-inf, NaNs, both signs
         scales = np.arange(0, 65536, 65536 // (sb // 2), dtype=np.uint16)[:sb // 2].view(np.uint8)
     else:
         sc = synth.f32_to_bf16_bits(rng.standard_normal(sb // 2).astype(np.float32) * 1e-2)
@@ -234,6 +234,9 @@ FULL = [
     ("mxint8", 4096, 11008, 4096, False),
     ("int8", 1, 11008, 4096, False),
     ("int8", 4096, 11008, 4096, False),
+    ("int4", 1, 11008, 4096, False),
+    ("int4", 16, 11008, 4096, False),
+    ("int4_f16", 4096, 11008, 4096, False),
 ]
 
 
@@ -320,7 +323,7 @@ def test_gemv_fallback_long_k(fmt, m):
     _check_qmm(out, ref, bound, (fmt, m, k))
 
 
-@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "int4_affine"])
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "int4_affine", "int4"])
 @pytest.mark.parametrize("m", [1, 2])
 def test_wide_gemv_four_warp_ctas(fmt, m):
     # more 16-row tiles than two per SM: the 4-bit GEMV runs 4-warp CTAs; N

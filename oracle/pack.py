@@ -46,6 +46,15 @@ Readings taken where the pages are silent (each is listed in the design doc):
   +-(2^(N-1) - 1); the fp16-scale twin): as int8 with 7 in place of 127, the
   4-bit two's-complement code stored LSB-first two per byte (the 4-bit
   bit-stream is the nibble layout).
+* mxfp4x2, the two-level residual E2M1 weight of rlx-cpu
+  ``dequant_matmul_mxfp4x2`` (w = s0 LUT[q0] + s1 LUT[q1], two E2M1 code
+  planes, a float32 scale per plane and block): the pages print the decode
+  only.  Reading of the encode: level 0 packs the block as an E2M1 block with
+  the float32 scale s0 = amax / 6; level 1 packs the float32 residual
+  r = w - s0 LUT[q0] (a float32 product, then a float32 difference) the same
+  way with s1 = amax(r) / 6 (1.0 for an all-zero residual).  Block 32 (the MX
+  block).  Layout: codes [N, 2, K/2] (a row's plane-0 nibbles, then its
+  plane-1 nibbles), scales [N, 2, K/32] float32 (s0 of every block, then s1).
 * int4 affine (MLX style, group 64): s = (max - min) / 15 (1.0 when 0), stored
   as bf16 (RNE); bias = bf16(min); q = clamp(round_half_away((w - b) / s), 0, 15);
   scale and bias are interleaved per group as bf16 pairs [N, ceil(K/64), 2].
@@ -62,16 +71,18 @@ import numpy as np
 from . import codec
 
 FORMATS = ("mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8", "int4_affine", "nvfp8_f16", "mxint8",
-           "int8", "int8_f16", "int4", "int4_f16")
+           "int8", "int8_f16", "int4", "int4_f16", "mxfp4x2")
 RAGGED = ("int4_affine", "int8", "int8_f16", "int4", "int4_f16")   # block 64: K may end in a group of 32
 SYM_INT = ("int8", "int8_f16", "int4", "int4_f16")                 # symmetric integers, float scale per 64
 
 BLOCK = {"mxfp4": 32, "nvfp4": 16, "mxfp8_e4m3": 32, "mxfp8_e5m2": 32, "nvfp8": 16, "int4_affine": 64,
-         "nvfp8_f16": 16, "mxint8": 32, "int8": 64, "int8_f16": 64, "int4": 64, "int4_f16": 64}
+         "nvfp8_f16": 16, "mxint8": 32, "int8": 64, "int8_f16": 64, "int4": 64, "int4_f16": 64, "mxfp4x2": 32}
 ELEM_BITS = {"mxfp4": 4, "nvfp4": 4, "mxfp8_e4m3": 8, "mxfp8_e5m2": 8, "nvfp8": 8, "int4_affine": 4, "nvfp8_f16": 8,
-             "mxint8": 8, "int8": 8, "int8_f16": 8, "int4": 4, "int4_f16": 4}
+             "mxint8": 8, "int8": 8, "int8_f16": 8, "int4": 4, "int4_f16": 4,
+             "mxfp4x2": 8}                                   # bits per weight (mxfp4x2: two nibbles)
 SCALE_BYTES = {"mxfp4": 1, "nvfp4": 1, "mxfp8_e4m3": 1, "mxfp8_e5m2": 1, "nvfp8": 4, "int4_affine": 4,
-               "nvfp8_f16": 2, "mxint8": 1, "int8": 4, "int8_f16": 2, "int4": 4, "int4_f16": 2}
+               "nvfp8_f16": 2, "mxint8": 1, "int8": 4, "int8_f16": 2, "int4": 4, "int4_f16": 2,
+               "mxfp4x2": 8}                                 # bytes per block (mxfp4x2: s0 and s1)
 _ELEM = {"mxfp4": ("e2m1", codec.E2M1_MAX), "nvfp4": ("e2m1", codec.E2M1_MAX),
          "mxfp8_e4m3": ("e4m3", codec.E4M3_MAX), "mxfp8_e5m2": ("e5m2", codec.E5M2_MAX),
          "nvfp8": ("e4m3", codec.E4M3_MAX), "nvfp8_f16": ("e4m3", codec.E4M3_MAX), "mxint8": ("int8", 127.0),
@@ -141,6 +152,8 @@ def pack(fmt: str, w: np.ndarray):
 
     if fmt == "int4_affine":
         return _pack_int4_affine(wb, n, k)
+    if fmt == "mxfp4x2":
+        return _pack_mxfp4x2(wb, n, k)
 
     elem, maxf = _ELEM[fmt]
     if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8"):
@@ -184,6 +197,24 @@ def pack(fmt: str, w: np.ndarray):
     codes_b = _pack_nibbles(codes) if ELEM_BITS[fmt] == 4 else codes.astype(np.uint8)
     scales_b = np.ascontiguousarray(scales).view(np.uint8).reshape(n, -1)
     return codes_b, scales_b, F32(glob)
+
+
+def _pack_mxfp4x2(wb: np.ndarray, n: int, k: int):
+    planes, scales = [], []
+    r = wb.astype(F32)
+    for _level in range(2):
+        amax = np.max(np.abs(r), axis=2).astype(F32)
+        s = np.where(amax > 0, amax / F32(6.0), F32(1.0)).astype(F32)
+        if not np.all(np.isfinite(s)):
+            raise ValueError("scale overflows float32")
+        c = _quantize(r, s, "e2m1")                                    # 0 where s underflowed to 0
+        planes.append(_pack_nibbles(c.reshape(n, k)))
+        scales.append(s)
+        approx = (s[..., None] * codec.E2M1_TABLE[c].astype(F32)).astype(F32)
+        r = (r - approx).astype(F32)                                   # the residual, float32
+    codes = np.stack(planes, axis=1).reshape(n, k)                     # [N, 2, K/2]
+    sc = np.ascontiguousarray(np.stack(scales, axis=1)).view(np.uint8).reshape(n, -1)   # [N, 2, nb] f32
+    return codes, sc, F32(1.0)
 
 
 def _round_half_away(v: np.ndarray) -> np.ndarray:

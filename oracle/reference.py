@@ -26,6 +26,10 @@ Value definitions (page title, then the section):
 * int4 / int4_f16: the same with q the signed nibble (sign-extended from its
   bit 3) -- PR #250, the symmetric intN formats (FP32 group 64) and the
   fp16-scale twin.
+* mxfp4x2: w = s0 e2m1(q0) + s1 e2m1(q1), the two residual planes' values
+  under their float32 block scales -- rlx-cpu ``dequant_matmul_mxfp4x2``
+  (codes [N, 2, K/2], scales [N, 2, K/32]; each product is exact in float64,
+  their sum is rounded once in float64, then once to float32 by dequant_f32).
 * int4 affine: w = scale * q + bias with q the LSB-first nibble, group 64 --
   metaltile-std ``tests/qmm_gpu_correctness.rs``, ``cpu_qmm_reference``;
   scale and bias are bf16.  float64 evaluation of s*q + b is exact or, when
@@ -109,6 +113,15 @@ def dequant_exact(fmt: str, codes, scales, global_scale, n: int, k: int) -> np.n
     if fmt not in FORMATS:
         raise ValueError(fmt)
     blk = BLOCK[fmt]
+    if fmt == "mxfp4x2":
+        b = np.asarray(codes, dtype=np.uint8).reshape(n, 2, k // 2)
+        s = np.ascontiguousarray(np.asarray(scales, dtype=np.uint8)).view(np.float32).reshape(n, 2, -1)
+        col = np.arange(k) // blk
+        w = np.zeros((n, k))
+        for p in range(2):
+            q = unpack_codes("mxfp4", b[:, p], n, k)
+            w = w + codec.E2M1_TABLE[q] * s[:, p, col].astype(np.float64)
+        return w
     e = element_values(fmt, unpack_codes(fmt, codes, n, k))
     mult, add = block_scales(fmt, scales, global_scale, n, k)
     col = np.arange(k) // blk                            # the block of every column (a ragged last one too)

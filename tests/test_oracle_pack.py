@@ -42,7 +42,7 @@ def test_byte_sizes():
         bits = 4 if fmt in ("mxfp4", "nvfp4", "int4_affine", "int4", "int4_f16") else 8
         assert c.nbytes == n * k * bits // 8 == pack.codes_nbytes(fmt, n, k)
         per_scale = {"nvfp8": 4, "int4_affine": 4, "nvfp8_f16": 2, "int8": 4, "int8_f16": 2, "int4": 4,
-                     "int4_f16": 2}.get(fmt, 1)
+                     "int4_f16": 2, "mxfp4x2": 8}.get(fmt, 1)
         assert s.nbytes == n * (k // pack.BLOCK[fmt]) * per_scale == pack.scales_nbytes(fmt, n, k)
         assert c.dtype == np.uint8 and s.dtype == np.uint8 and isinstance(g, np.float32)
 
@@ -71,7 +71,7 @@ def test_zero_blocks():
             assert (s == 127).all()
         elif fmt == "nvfp4":
             assert (s == 0x38).all() and g == 1.0
-        elif fmt in ("nvfp8", "int8", "int4"):
+        elif fmt in ("nvfp8", "int8", "int4", "mxfp4x2"):
             assert (s.view(np.float32) == 1.0).all()
         elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):
             assert (s.view(np.float16) == 1.0).all()
@@ -107,7 +107,7 @@ def test_exactly_representable_roundtrip_mx(fmt):
     assert np.array_equal(got[nz], codes[nz].astype(np.uint8))
 
 
-@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("fmt", [f for f in FMTS if f != "mxfp4x2"])   # a re-packed residual moves s0
 def test_value_idempotence(fmt):
     # Packing the dequantized weights again reproduces the same values (the codes
     # quantized against the effective scale are self-consistent, PR #250).
@@ -128,7 +128,7 @@ def test_value_idempotence(fmt):
 
 FLOORS = {"mxfp4": 0.98, "nvfp4": 0.98, "int4_affine": 0.99,
           "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999, "nvfp8_f16": 0.999, "mxint8": 0.999,
-          "int8": 0.9999, "int8_f16": 0.9999, "int4": 0.99, "int4_f16": 0.99}
+          "int8": 0.9999, "int8_f16": 0.9999, "int4": 0.99, "int4_f16": 0.99, "mxfp4x2": 0.9999}
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -349,3 +349,68 @@ def test_int4_nibble_eight_decodes_as_minus_eight():
     c = np.full((1, 32), 0x88, np.uint8)
     s = np.array([1.0], np.float32).view(np.uint8).reshape(1, -1)
     assert (reference.dequant_exact("int4", c, s, 1.0, 1, 64) == -8).all()
+
+
+def _x2_case(rng, n, k):
+    """W = s0 v0 + s1 v1 built so that both residual levels come back exactly:
+    v0, v1 on the E2M1 grid, +-6 in every block of each level (and v1 = 0 where
+    v0 = +-6, so amax(W) = 6 s0), s1 = s0 / 32 (so |s1 v1| stays under half
+    of the smallest E2M1 gap times s0 and level 0 rounds back to v0), s0 with
+    few significant bits (every product and sum exact in float32)."""
+    grid = codec.E2M1_TABLE[:8]                      # 0, .5, 1, 1.5, 2, 3, 4, 6
+    nb = k // 32
+    v0 = rng.choice(grid[:7], size=(n, k)) * rng.choice([-1, 1], size=(n, k))
+    v1 = rng.choice(grid, size=(n, k)) * rng.choice([-1, 1], size=(n, k))
+    v0[:, 0::32] = 6.0 * rng.choice([-1, 1], size=(n, nb))
+    v1[:, 0::32] = 0.0
+    v1[:, 1::32] = 6.0 * rng.choice([-1, 1], size=(n, nb))
+    s0 = rng.integers(64, 128, size=(n, nb)) * 2.0 ** rng.integers(-20, 0, size=(n, nb))
+    s1 = s0 / 32
+    w = v0 * np.repeat(s0, 32, axis=1) + v1 * np.repeat(s1, 32, axis=1)
+    return v0, v1, s0, s1, w.astype(np.float32)
+
+
+def test_mxfp4x2_two_levels_round_trip_exactly():
+    # rlx-cpu dequant_matmul_mxfp4x2 decodes w = s0 LUT[q0] + s1 LUT[q1]; the
+    # packer's two residual levels must recover v0, v1, s0, s1 and the layout
+    # [N, 2, K/2] codes, [N, 2, K/32] float32 scales.
+    rng = np.random.default_rng(51)
+    n, k = 5, 128
+    v0, v1, s0, s1, w = _x2_case(rng, n, k)
+    assert np.array_equal(w.astype(np.float64), v0 * np.repeat(s0, 32, axis=1) + v1 * np.repeat(s1, 32, axis=1))
+    c, s, g = pack.pack("mxfp4x2", w)
+    sc = s.view(np.float32).reshape(n, 2, k // 32)
+    assert np.array_equal(sc[:, 0], s0) and np.array_equal(sc[:, 1], s1)
+    planes = c.reshape(n, 2, k // 2)
+    for p, v in ((0, v0), (1, v1)):
+        q = reference.unpack_codes("mxfp4", planes[:, p], n, k)
+        assert np.array_equal(codec.E2M1_TABLE[q], v), p
+    assert np.array_equal(reference.dequant_exact("mxfp4x2", c, s, g, n, k), w.astype(np.float64))
+
+
+def test_mxfp4x2_on_grid_weights_leave_an_empty_residual():
+    # a block exactly on level 0's grid: plane 1 is all zero codes with scale 1.0
+    rng = np.random.default_rng(52)
+    n, k = 3, 64
+    v0 = rng.choice(codec.E2M1_TABLE[:16], size=(n, k))
+    v0[:, 0::32] = 6.0
+    w = (v0 * 2.0 ** -5).astype(np.float32)
+    c, s, _ = pack.pack("mxfp4x2", w)
+    sc = s.view(np.float32).reshape(n, 2, -1)
+    assert (sc[:, 0] == 2.0 ** -5).all() and (sc[:, 1] == 1.0).all()
+    assert not (c.reshape(n, 2, -1)[:, 1] & 0x77).any()     # only signed zeros in plane 1
+
+
+def test_mxfp4x2_error_within_second_level_step():
+    # the residual is packed by level 1, so the remaining error of a block is at
+    # most half the widest E2M1 gap (1.0) times s1, plus float32 rounding; and
+    # far below the one-level error
+    n, k = 32, 512
+    w = synth.weights(n, k, seed=53)
+    c, s, g = pack.pack("mxfp4x2", w)
+    err = np.abs(reference.dequant_exact("mxfp4x2", c, s, g, n, k) - w)
+    s1 = s.view(np.float32).reshape(n, 2, -1)[:, 1].astype(np.float64)
+    assert (err <= np.repeat(s1, 32, axis=1) * (1.0 + 1e-6) + 1e-30).all()
+    c1, s_1, g1 = pack.pack("mxfp4", w)
+    err1 = np.abs(reference.dequant_exact("mxfp4", c1, s_1, g1, n, k) - w)
+    assert err.max() < err1.max() / 8

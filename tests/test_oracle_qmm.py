@@ -63,6 +63,20 @@ def _lib_scale(fmt, sbytes, n, b):
     return f(s_bits), f(b_bits)
 
 
+def _x2_weight(codes_row, scales_row, kk, k):
+    # rlx-cpu dequant_matmul_mxfp4x2: s0 LUT[q0] + s1 LUT[q1]; a row holds its
+    # plane-0 nibbles, then its plane-1 nibbles, and its s0 floats, then its s1 floats
+    nb = k // 32
+    w = Fraction(0)
+    for p in range(2):
+        byte = codes_row[p * (k // 2) + kk // 2]
+        c = (byte >> (4 * (kk % 2))) & 0xF
+        o = 4 * (p * nb + kk // 32)
+        sc = Fraction(float(np.frombuffer(bytes(scales_row[o:o + 4]), "<f4")[0]))
+        w += _lib_elem("mxfp4", c) * sc
+    return w
+
+
 def _brute_qmm(fmt, codes, scales, g, x64, m, n, k):
     blk = pack.BLOCK[fmt]
     codes = [[int(v) for v in r] for r in np.asarray(codes).reshape(n, -1)]
@@ -71,6 +85,9 @@ def _brute_qmm(fmt, codes, scales, g, x64, m, n, k):
     for j in range(n):
         wrow = []
         for kk in range(k):
+            if fmt == "mxfp4x2":
+                wrow.append(_x2_weight(codes[j], scales[j], kk, k))
+                continue
             if fmt in ("mxfp4", "nvfp4", "int4_affine", "int4", "int4_f16"):
                 byte = codes[j][kk // 2]
                 c = (byte >> (4 * (kk % 2))) & 0xF
@@ -122,6 +139,10 @@ def test_dequant_f32_is_one_rounding_of_exact(fmt):
     blk = pack.BLOCK[fmt]
     for j in range(n):
         for kk in range(k):
+            if fmt == "mxfp4x2":
+                w = _x2_weight(codes[j], scales[j], kk, k)
+                assert wf[j, kk] == np.float32(float(w)), (fmt, j, kk)
+                continue
             four = pack.ELEM_BITS[fmt] == 4
             byte = codes[j][kk // 2] if four else codes[j][kk]
             cc = (byte >> (4 * (kk % 2))) & 0xF if four else byte

@@ -117,11 +117,9 @@ def dequant_exact(fmt: str, codes, scales, global_scale, n: int, k: int) -> np.n
         b = np.asarray(codes, dtype=np.uint8).reshape(n, 2, k // 2)
         s = np.ascontiguousarray(np.asarray(scales, dtype=np.uint8)).view(np.float32).reshape(n, 2, -1)
         col = np.arange(k) // blk
-        w = np.zeros((n, k))
-        for p in range(2):
-            q = unpack_codes("mxfp4", b[:, p], n, k)
-            w = w + codec.E2M1_TABLE[q] * s[:, p, col].astype(np.float64)
-        return w
+        t0, t1 = (codec.E2M1_TABLE[unpack_codes("mxfp4", b[:, p], n, k)] * s[:, p, col].astype(np.float64)
+                  for p in range(2))
+        return t0 + t1                                   # the IEEE sum (two signed zeros stay -0)
     e = element_values(fmt, unpack_codes(fmt, codes, n, k))
     mult, add = block_scales(fmt, scales, global_scale, n, k)
     col = np.arange(k) // blk                            # the block of every column (a ragged last one too)

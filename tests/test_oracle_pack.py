@@ -414,3 +414,15 @@ def test_mxfp4x2_error_within_second_level_step():
     c1, s_1, g1 = pack.pack("mxfp4", w)
     err1 = np.abs(reference.dequant_exact("mxfp4", c1, s_1, g1, n, k) - w)
     assert err.max() < err1.max() / 8
+
+
+def test_mxfp4x2_two_negative_zero_codes_give_negative_zero():
+    # s0 LUT[q0] + s1 LUT[q1] with both codes the sign-set zero (0x8) is the
+    # IEEE sum -0 + -0 = -0; one +0 code makes it +0
+    c = np.zeros((1, 2, 16), np.uint8)
+    c[0, :, 0] = 0x88                                  # k = 0, 1: -0 in both planes
+    c[0, 0, 1] = 0x08                                  # k = 2: -0 in plane 0, +0 in plane 1
+    s = np.array([[0.5, 0.25]], np.float32).view(np.uint8).reshape(1, -1)
+    w = reference.dequant_f32("mxfp4x2", c.reshape(1, -1), s, 1.0, 1, 32)
+    assert np.signbit(w[0, 0]) and np.signbit(w[0, 1]) and not np.signbit(w[0, 2])
+    assert (w == 0).all()

@@ -24,7 +24,7 @@ namespace qfmt_dev {
 
 enum Fmt {
   MXFP4 = 1, NVFP4 = 2, MXFP8_E4M3 = 3, MXFP8_E5M2 = 4, NVFP8 = 5, INT4_AFFINE = 6, NVFP8_F16 = 7, MXINT8 = 8,
-  INT8 = 9, INT8_F16 = 10, INT4 = 11, INT4_F16 = 12
+  INT8 = 9, INT8_F16 = 10, INT4 = 11, INT4_F16 = 12, MXFP4X2 = 13
 };
 
 template <int F> struct FmtTraits;
@@ -40,6 +40,10 @@ template <> struct FmtTraits<INT8> { static constexpr bool four = false; static 
 template <> struct FmtTraits<INT8_F16> { static constexpr bool four = false; static constexpr int block = 64; static constexpr int sbytes = 2; };
 template <> struct FmtTraits<INT4> { static constexpr bool four = true; static constexpr int block = 64; static constexpr int sbytes = 4; };
 template <> struct FmtTraits<INT4_F16> { static constexpr bool four = true; static constexpr int block = 64; static constexpr int sbytes = 2; };
+// mxfp4x2 as the kernels see it: 2N rows of E2M1 codes (row 2n the residual
+// plane 0 of output row n, row 2n + 1 its plane 1) with a float32 scale per
+// 32; an output is the sum of its two rows' products.
+template <> struct FmtTraits<MXFP4X2> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 4; };
 
 // 8-bit elements under an E8M0 scale per 32 (mxfp8 E4M3/E5M2, mxint8), and
 // every E8M0-scaled format (those and mxfp4)
@@ -65,7 +69,7 @@ constexpr bool is_i4() { return F == INT4_AFFINE || F == INT4 || F == INT4_F16; 
 template <int F>
 constexpr bool is_i4sym() { return F == INT4 || F == INT4_F16; }
 inline constexpr bool fmt_is_i4(int f) { return f == INT4_AFFINE || f == INT4 || f == INT4_F16; }
-inline constexpr bool fmt_is_four(int f) { return f == MXFP4 || f == NVFP4 || fmt_is_i4(f); }
+inline constexpr bool fmt_is_four(int f) { return f == MXFP4 || f == NVFP4 || f == MXFP4X2 || fmt_is_i4(f); }
 
 // Block scale idx of a float-scaled array as float32: the stored float32, or
 // the (exact) float32 of the stored IEEE half.
@@ -299,7 +303,7 @@ __device__ __forceinline__ PieceScale load_piece_scale(const uint8_t* scales, in
     s.a = __ldg(scales + base + k0 / 32);
   } else if constexpr (F == NVFP4) {
     s.a = __ldg(reinterpret_cast<const unsigned short*>(scales + base + k0 / 16));
-  } else if constexpr (is_fs8<F>()) {
+  } else if constexpr (is_fs8<F>() || F == MXFP4X2) {
     s.a = __float_as_uint(float_scale<F>(scales, base + k0 / FmtTraits<F>::block));
   } else {
     s.a = i4_word<F>(scales, base + k0 / 64);
@@ -434,7 +438,17 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
 template <int F>
 __device__ __forceinline__ void decode_piece_hilo(const uint4& v, const PieceScale& ps, uint32_t* hi, uint32_t* lo) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  if constexpr (is_fs8<F>()) {
+  if constexpr (F == MXFP4X2) {   // one residual plane's 32 E2M1 codes times its float32 block scale
+    const float s = __uint_as_float(ps.a);
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      #pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint32_t byte = (w[j] >> (8 * p)) & 0xFFu;
+        split_bf16x2(__fmul_rn(e2m1_f32(byte & 0xFu), s), __fmul_rn(e2m1_f32(byte >> 4), s), hi[4 * j + p], lo[4 * j + p]);
+      }
+    }
+  } else if constexpr (is_fs8<F>()) {
     const float s = __uint_as_float(ps.a);
     #pragma unroll
     for (int j = 0; j < 4; ++j) {

@@ -61,9 +61,26 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
        p += int64_t(gridDim.x) * blockDim.x) {
     const int64_t row = p / pieces_per_row;
     const int64_t k0 = (p - row * pieces_per_row) * PIECE;
+    float o[PIECE];
+    if constexpr (F == MXFP4X2) {
+      // the two residual planes of row `row` (plane 0, then plane 1, K/2 bytes
+      // each) under their float32 block scales: s0 e0 + s1 e1, the products
+      // exact in double, the sum rounded in double and then to float32
+      const int64_t j = p - row * pieces_per_row;
+      const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(codes) + 2 * row * pieces_per_row + j);
+      const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(codes) + (2 * row + 1) * pieces_per_row + j);
+      const float* sr = reinterpret_cast<const float*>(scales) + 2 * row * nblk;
+      const double s0 = __ldg(sr + k0 / 32), s1 = __ldg(sr + nblk + k0 / 32);
+      const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+      #pragma unroll
+      for (int i = 0; i < PIECE; ++i) {
+        const double e0 = e2m1_f32((w0[i >> 3] >> (4 * (i & 7))) & 0xFu);
+        const double e1 = e2m1_f32((w1[i >> 3] >> (4 * (i & 7))) & 0xFu);
+        o[i] = __double2float_rn(__dadd_rn(__dmul_rn(e0, s0), __dmul_rn(e1, s1)));
+      }
+    } else {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(codes) + p);
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-    float o[PIECE];
     float s = 0.0f, b = 0.0f;
     // blocks inside the piece: 4-bit: 32 codes = 1 (mx), 2 (nvfp4), 1/2 (int4) blocks;
     // 8-bit: 16 codes = 1/2 (mx) or 1 (nvfp8) block.
@@ -73,6 +90,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
       if (i == 0 || ((k0 + i) % T::block) == 0) dq_scale<F>(scales, blk, s, b);
       uint32_t code = T::four ? (wv[i >> 3] >> (4 * (i & 7))) & 0xFu : (wv[i >> 2] >> (8 * (i & 3))) & 0xFFu;
       o[i] = dq_value<F>(code, s, b, glob);
+    }
     }
     if constexpr (OUT_BF16) {
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + row * K + k0);
@@ -131,6 +149,7 @@ cudaError_t launch_dequant(int fmt, const void* codes, const void* scales, float
     case INT8_F16: return launch_dequant_fmt<INT8_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case INT4: return launch_dequant_fmt<INT4>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case INT4_F16: return launch_dequant_fmt<INT4_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case MXFP4X2: return launch_dequant_fmt<MXFP4X2>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     default: return launch_dequant_fmt<INT4_AFFINE>(codes, scales, glob, out, out_bf16, N, K, st, sms);
   }
 }

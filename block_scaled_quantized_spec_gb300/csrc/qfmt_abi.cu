@@ -38,6 +38,10 @@ int cuda_status(cudaError_t e, const char* what) {
   return fail(QFMT_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Code rows the kernels stream for N outputs: mxfp4x2 keeps two residual
+// planes per output row, which the kernels treat as rows 2n and 2n + 1.
+int64_t weight_rows(int fmt, int64_t N) { return fmt == QFMT_MXFP4X2 ? 2 * N : N; }
+
 int check_common(int fmt, const void* codes, const void* scales, float glob, int group) {
   int st = check_group(fmt, group);
   if (st) return st;
@@ -97,9 +101,11 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale, c
                                                  out, out_f32, M, N, K, s, sms),
                        "qmm (f32 activations) launch");
   if (M <= 16)
-    return cuda_status(qfmt_dev::launch_qgemv(fmt, codes, scales, global_scale, x, out, out_f32, M, N, K, s, sms),
+    return cuda_status(qfmt_dev::launch_qgemv(fmt, codes, scales, global_scale, x, out, out_f32, M,
+                                              weight_rows(fmt, N), K, s, sms),
                        "qgemv launch");
-  return cuda_status(qfmt_dev::launch_qgemm_tc(fmt, codes, scales, global_scale, x, out, out_f32, M, N, K, s, sms),
+  return cuda_status(qfmt_dev::launch_qgemm_tc(fmt, codes, scales, global_scale, x, out, out_f32, M,
+                                               weight_rows(fmt, N), K, s, sms),
                      "qgemm launch");
 }
 
@@ -117,7 +123,7 @@ int qmm_gather(int fmt, const void* codes, const void* scales, float global_scal
   if (st) return st;
   if ((st = check_shape(fmt, M, N, K))) return st;
   if (E < 1) return fail(QFMT_EINVAL, "expert count E=%lld must be >= 1", (long long)E);
-  if (E * N > (int64_t(1) << 31)) return fail(QFMT_ESHAPE, "E*N above 2^31");
+  if (E * weight_rows(fmt, N) > (int64_t(1) << 31)) return fail(QFMT_ESHAPE, "E*N code rows above 2^31");
   if (M > 65535) return fail(QFMT_ESHAPE, "M=%lld above 65535 rows", (long long)M);
   if (M == 0 || N == 0) return QFMT_OK;
   if ((st = check_ptr(out, 16, "out"))) return st;
@@ -129,7 +135,7 @@ int qmm_gather(int fmt, const void* codes, const void* scales, float global_scal
   if (!qfmt_dev::qgemv_m2_fits(fmt, 1, K))
     return fail(QFMT_EUNSUPPORTED, "K=%lld too long for the expert-routed GEMV", (long long)K);
   return cuda_status(qfmt_dev::launch_qgemv_gather(fmt, codes, scales, global_scale, x, expert_idx, out, false, M,
-                                                    N, K, E, s),
+                                                    weight_rows(fmt, N), K, E, s),
                      "qmm_gather launch");
 }
 
@@ -171,7 +177,7 @@ int qmm_batched(int fmt, int count, const void* const* codes, const void* const*
       c[live] = codes[i];
       sc[live] = scales[i];
       g[live] = global_scales[i];
-      n[live] = N[i];
+      n[live] = weight_rows(fmt, N[i]);
       o[live] = out[i];
       ++live;
     }
@@ -202,7 +208,8 @@ int qmm_rmsnorm(int fmt, const void* codes, const void* scales, float global_sca
     return fail(QFMT_EUNSUPPORTED, "K=%lld too long for the fused decode GEMV", (long long)K);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const float g = global_scale;
-  return cuda_status(qfmt_dev::launch_qgemv_multi(fmt, 1, &codes, &scales, &g, &N, x, norm_weight, eps, &out, false,
+  const int64_t nw = weight_rows(fmt, N);
+  return cuda_status(qfmt_dev::launch_qgemv_multi(fmt, 1, &codes, &scales, &g, &nw, x, norm_weight, eps, &out, false,
                                                    M, K, s),
                      "qmm_rmsnorm launch");
 }

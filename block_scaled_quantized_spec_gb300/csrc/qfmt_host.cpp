@@ -35,11 +35,11 @@ int fail(int status, const char* fmt, ...) {
 
 void clear_error() { g_err[0] = '\0'; }
 
-bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_INT4_F16; }
+bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_MXFP4X2; }
 
 int block_of(int fmt) {
   switch (fmt) {
-    case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: return 32;
+    case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: case QFMT_MXFP4X2: return 32;
     case QFMT_NVFP4: case QFMT_NVFP8: case QFMT_NVFP8_F16: return 16;
     case QFMT_INT4_AFFINE: case QFMT_INT8: case QFMT_INT8_F16: case QFMT_INT4: case QFMT_INT4_F16: return 64;
     default: return 0;
@@ -57,7 +57,7 @@ bool is_sym_int(int fmt) {
 // Largest finite element magnitude: amax / elem_max is the raw block scale.
 float elem_max(int fmt) {
   switch (fmt) {
-    case QFMT_MXFP4: case QFMT_NVFP4: return 6.0f;
+    case QFMT_MXFP4: case QFMT_NVFP4: case QFMT_MXFP4X2: return 6.0f;
     case QFMT_MXFP8_E5M2: return 57344.0f;
     case QFMT_MXINT8: case QFMT_INT8: case QFMT_INT8_F16: return 127.0f;
     case QFMT_INT4: case QFMT_INT4_F16: return 7.0f;
@@ -66,6 +66,7 @@ float elem_max(int fmt) {
 }
 
 int scale_entry_bytes(int fmt) {
+  if (fmt == QFMT_MXFP4X2) return 8;   // s0 and s1, float32 each (stored as two [nb] runs per row)
   if (fmt == QFMT_NVFP8 || fmt == QFMT_INT4_AFFINE || fmt == QFMT_INT8 || fmt == QFMT_INT4) return 4;
   return (fmt == QFMT_NVFP8_F16 || fmt == QFMT_INT8_F16 || fmt == QFMT_INT4_F16) ? 2 : 1;
 }
@@ -126,6 +127,11 @@ static uint32_t encode_minifloat(float v, int mbits, int bias, uint32_t max_code
 static inline uint32_t enc_e2m1(float v) { return encode_minifloat(v, 1, 1, 0x7, 6.0f, 0x8); }
 static inline uint32_t enc_e4m3(float v) { return encode_minifloat(v, 3, 7, 0x7E, 448.0f, 0x80); }
 static inline uint32_t enc_e5m2(float v) { return encode_minifloat(v, 2, 15, 0x7B, 57344.0f, 0x80); }
+// E2M1 code -> value: magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}, sign bit 3.
+static float dec_e2m1(uint32_t c) {
+  static const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+  return (c & 0x8u) ? -mag[c & 7u] : mag[c & 7u];
+}
 
 static inline uint32_t f32_bits(float f) { uint32_t u; std::memcpy(&u, &f, 4); return u; }
 static inline float bits_f32(uint32_t u) { float f; std::memcpy(&f, &u, 4); return f; }
@@ -197,7 +203,7 @@ using namespace qfmt;
 
 extern "C" {
 
-int qfmt_version(void) { return 104; }
+int qfmt_version(void) { return 105; }
 
 const char* qfmt_last_error(void) { return qfmt::g_err; }
 
@@ -258,6 +264,30 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
     for (int64_t n = r0; n < r1; ++n) {
       const float* w = W + n * K;
       uint8_t* crow = cb + n * row_bytes;
+      if (fmt == QFMT_MXFP4X2) {
+        // two residual E2M1 levels per block: level 0 packs w with s0 = amax/6,
+        // level 1 the float32 residual r = w - s0 e2m1(q0) with s1 = amax(r)/6;
+        // plane p's codes at byte p K/2 of the row, its scales at float p nb
+        float* srow = reinterpret_cast<float*>(sb) + n * 2 * nb;
+        std::vector<float> r(w, w + K);
+        for (int p = 0; p < 2; ++p) {
+          for (int64_t b = 0; b < nb; ++b) {
+            float* rb = r.data() + b * blk;
+            float amax = 0.0f;
+            for (int j = 0; j < blk; ++j) amax = std::max(amax, std::fabs(rb[j]));
+            const float sc = amax > 0.0f ? amax / 6.0f : 1.0f;
+            if (!std::isfinite(sc)) { bad = true; continue; }
+            srow[p * nb + b] = sc;
+            for (int j = 0; j < blk; ++j) {
+              const uint32_t code = sc != 0.0f ? enc_e2m1(rb[j] / sc) : 0u;
+              put_code(crow + p * (K / 2), b * blk + j, code, true);
+              const float approx = sc * dec_e2m1(code);
+              rb[j] = rb[j] - approx;
+            }
+          }
+        }
+        continue;
+      }
       for (int64_t b = 0; b < nb; ++b) {
         const float* wb = w + b * blk;
         const int len = int(std::min<int64_t>(blk, K - b * blk));

@@ -56,7 +56,7 @@ constexpr int B_BYTES = 256 * BK * 2;     // 32 KiB: 256 bf16 rows, or 128 hi ro
 // formats exact in bf16; 8 for nvfp8 and int4 affine, whose hi + lo tiles were
 // measured faster with eight.
 template <int F> struct Dec {
-  static constexpr int WARPS = (is_i4<F>() || is_fs8<F>()) ? 8 : 16;
+  static constexpr int WARPS = (is_i4<F>() || is_fs8<F>() || F == MXFP4X2) ? 8 : 16;
   static constexpr int THREADS = WARPS * 32;
   static constexpr int CTA_THREADS = (2 + WARPS) * 32;
 };
@@ -74,7 +74,7 @@ template <int MT> struct Pipe {
 // affine carry each weight as a hi + lo bf16 pair (two MMAs per K slice into
 // one accumulator) on a 128 x 128 tile, so a stage holds the same bytes.
 template <int F> struct Tile {
-  static constexpr bool split = is_fs8<F>() || is_i4<F>();
+  static constexpr bool split = is_fs8<F>() || is_i4<F>() || F == MXFP4X2;
   static constexpr int BN = split ? 128 : 256;
 };
 
@@ -455,6 +455,38 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
           v[j] = __uint_as_float(r[j]);
           if constexpr (F == NVFP4) v[j] *= p.glob;
         }
+        if constexpr (F == MXFP4X2) {   // columns 2j, 2j + 1: the residual planes of output column nb / 2 + j
+          const int no = p.N / 2, ob = nb / 2;
+          const int ncols = no - ob < 16 ? no - ob : 16;
+          float u[16];
+          #pragma unroll
+          for (int j = 0; j < 16; ++j) u[j] = v[2 * j] + v[2 * j + 1];
+          if (p.out_f32) {
+            float* o = static_cast<float*>(p.out) + int64_t(m) * no + ob;
+            if (ncols == 16 && (no & 3) == 0) {
+              #pragma unroll
+              for (int j = 0; j < 4; ++j)
+                reinterpret_cast<float4*>(o)[j] = make_float4(u[4 * j], u[4 * j + 1], u[4 * j + 2], u[4 * j + 3]);
+            } else {
+              for (int j = 0; j < ncols; ++j) o[j] = u[j];
+            }
+          } else {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + int64_t(m) * no + ob;
+            if (ncols == 16 && (no & 7) == 0) {
+              #pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                uint32_t h[4];
+                #pragma unroll
+                for (int t = 0; t < 4; ++t)
+                  h[t] = f32_to_bf16bits(u[8 * j + 2 * t]) | (f32_to_bf16bits(u[8 * j + 2 * t + 1]) << 16);
+                reinterpret_cast<uint4*>(o)[j] = make_uint4(h[0], h[1], h[2], h[3]);
+              }
+            } else {
+              for (int j = 0; j < ncols; ++j) o[j] = __float2bfloat16_rn(u[j]);
+            }
+          }
+          continue;
+        }
         const int ncols = p.N - nb < 32 ? p.N - nb : 32;
         if (p.out_f32) {
           float* o = static_cast<float*>(p.out) + int64_t(m) * p.N + nb;
@@ -505,6 +537,16 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
         v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
       }
       if constexpr (F == NVFP4) { v.x *= p.glob; v.y *= p.glob; v.z *= p.glob; v.w *= p.glob; }
+      if constexpr (F == MXFP4X2) {   // two output columns, each the sum of its two residual planes
+        const int no = p.N / 2;
+        const float u[2] = {v.x + v.y, v.z + v.w};
+        for (int j = 0; j < 2 && n / 2 + j < no; ++j) {
+          const int64_t oi = int64_t(m) * no + n / 2 + j;
+          if (p.out_f32) static_cast<float*>(p.out)[oi] = u[j];
+          else static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(u[j]);
+        }
+        continue;
+      }
       const float f4[4] = {v.x, v.y, v.z, v.w};
       const bool vec = n + 4 <= p.N && (p.N & 3) == 0;
       if (p.out_f32) {
@@ -666,6 +708,7 @@ cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, floa
     case INT8_F16: return tc::launch_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT4: return tc::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT4_F16: return tc::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXFP4X2: return tc::launch_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return tc::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }

@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
           wsc[rr * sst + e] = ok ? e8m0_f32(__ldg(scales + gi)) : 0.0f;
         } else if constexpr (F == NVFP4) {
           wsc[rr * sst + e] = __uint_as_float(ok ? e4m3_f16x2_splat(__ldg(scales + gi)) : 0u);
-        } else if constexpr (is_fs8<F>()) {
+        } else if constexpr (is_fs8<F>() || F == MXFP4X2) {
           wsc[rr * sst + e] = ok ? float_scale<F>(scales, gi) : 0.0f;
         } else {
           float sc, bi;
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
               for (int nb = 0; nb < NB; ++nb) {
                 const int m = min(nb * 8 + g, M - 1);
                 const uint4 xv = *reinterpret_cast<const uint4*>(xs + size_t(m) * xstride + u * 64 + sgm * 32 + 8 * t);
-                if constexpr (F == MXFP4) {
+                if constexpr (F == MXFP4 || F == MXFP4X2) {   // a block scale per segment
                   float d[4] = {0.f, 0.f, 0.f, 0.f};
                   mma_f16(d, fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
                   mma_f16(d, fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
@@ -429,14 +429,20 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
     }
   __syncthreads();
   if (!ok_all) return;   // an expired wait leaves this CTA's outputs unwritten (status word set)
-  for (int i = tid; i < ROWS * M; i += THREADS) {
-    const int r = i % ROWS, m = i / ROWS;
+  constexpr bool X2 = F == MXFP4X2;                                         // output row = rows 2r + 2r + 1
+  constexpr int OR = X2 ? ROWS / 2 : ROWS;                                  // output rows of the CTA
+  for (int i = tid; i < OR * M; i += THREADS) {
+    const int pr = i % OR, m = i / OR;
+    const int r = X2 ? 2 * pr : pr;
     if (row0 + r >= N) continue;
     float sum = 0.0f;
     #pragma unroll
-    for (int w = 0; w < WARPS; ++w) sum += red[(size_t(w) * ROWS + r) * RC + m];
+    for (int w = 0; w < WARPS; ++w) {
+      sum += red[(size_t(w) * ROWS + r) * RC + m];
+      if constexpr (X2) sum += red[(size_t(w) * ROWS + r + 1) * RC + m];    // the residual plane
+    }
     if constexpr (F == NVFP4) sum *= glob;
-    const int64_t o = int64_t(m) * N + row0 + r;
+    const int64_t o = X2 ? int64_t(m) * (N / 2) + row0 / 2 + pr : int64_t(m) * N + row0 + r;
     if (out_f32) static_cast<float*>(out)[o] = sum;
     else static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(sum);
   }
@@ -540,6 +546,7 @@ cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float g
     case INT8_F16: return gemv::launch_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case INT4: return gemv::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case INT4_F16: return gemv::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP4X2: return gemv::launch_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     default: return gemv::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }

@@ -96,7 +96,7 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int j) {
 // (8q+6, 8q+7); int4 the biased pairs (q_{8q+b}, q_{8q+b+4}), b = 0..3.
 template <int F>
 __device__ __forceinline__ void frags8(const uint4& v, int q, uint32_t r[4]) {
-  if constexpr (F == MXFP4 || F == NVFP4) {
+  if constexpr (F == MXFP4 || F == NVFP4 || F == MXFP4X2) {
     e2m1x8_f16(word(v, q), r);
   } else if constexpr (is_i4<F>()) {
     const uint32_t w = i4_u<F>(word(v, q));
@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   constexpr int P = chunks_per_warp<F, W>();
   constexpr int WARPS = W, THREADS = 32 * W;
   constexpr bool FOUR = S::four, I4 = is_i4<F>();
+  constexpr bool X2 = F == MXFP4X2;                                         // output row = rows 2r + 2r + 1
   constexpr int CODES = S::CODES, LANE = S::LANE;
   extern __shared__ __align__(16) uint8_t smem[];
   const int xst = xstride(K);
@@ -235,11 +236,13 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
     const int64_t m = blockIdx.y;
     const int e = __ldg(ex.eidx + m);
     x += m * K;
-    out = static_cast<uint8_t*>(out) + m * N * (out_f32 ? 4 : 2);
+    out = static_cast<uint8_t*>(out) + m * (X2 ? N / 2 : N) * (out_f32 ? 4 : 2);
     if (e < 0 || e >= ex.E) {                                               // a zero row, and the status bit
-      if (tid < 16 && row0 + tid < N) {
-        if (out_f32) static_cast<float*>(out)[row0 + tid] = 0.0f;
-        else static_cast<__nv_bfloat16*>(out)[row0 + tid] = __float2bfloat16_rn(0.0f);
+      constexpr int OR = X2 ? 8 : 16;                                       // output rows of the tile
+      const int o0 = X2 ? row0 / 2 : row0;
+      if (tid < OR && o0 + tid < (X2 ? N / 2 : N)) {
+        if (out_f32) static_cast<float*>(out)[o0 + tid] = 0.0f;
+        else static_cast<__nv_bfloat16*>(out)[o0 + tid] = __float2bfloat16_rn(0.0f);
       }
       if (tid == 0) atomicOr(&g_gather_status, 1u);
       return;
@@ -302,12 +305,12 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
       const uint32_t x2 = c0 ? __ldg(srb + e) : 127u;
       cs[i].a0 = prmt(x0, x2, 0x1410u) | 0x7F007F00u;                         // bytes 0 and 2 used, 1 and 3 = 127
       cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
-    } else if constexpr (is_fs8<F>()) {
-      constexpr int B = FmtTraits<F>::block;                                  // 16 (nvfp8) or 64 (int8)
+    } else if constexpr (is_fs8<F>() || F == MXFP4X2) {
+      constexpr int B = FmtTraits<F>::block;                                  // 16 (nvfp8), 32 (mxfp4x2), 64 (int8)
       const int e = k0 / B;
       cs[i].a0 = c0 ? __float_as_uint(float_scale<F>(sra, e)) : 0u;
       cs[i].b0 = c0 ? __float_as_uint(float_scale<F>(srb, e)) : 0u;
-      if constexpr (B == 16) {
+      if constexpr (B <= LANE) {                                              // quad lane a0 + 1: the next block
         cs[i].a1 = c1 ? __float_as_uint(float_scale<F>(sra, e + 1)) : 0u;
         cs[i].b1 = c1 ? __float_as_uint(float_scale<F>(srb, e + 1)) : 0u;
       } else {                                                                // a0, a0 + 1 share it
@@ -554,7 +557,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
         const float ca = __fmul_rn(qa, x0s), cb = __fmul_rn(qb, x0s);
         acc_a = __fmaf_rn(ca, d[ii][0] + d[ii][1], acc_a);
         acc_b = __fmaf_rn(cb, d[ii][2] + d[ii][3], acc_b);
-      } else if constexpr (is_fs8<F>()) {
+      } else if constexpr (is_fs8<F>() || F == MXFP4X2) {
         acc_a = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].a0), x0s), d[ii][0], acc_a);
         acc_a = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].a1), x1s), d[ii][1], acc_a);
         acc_b = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].b0), x0s), d[ii][2], acc_b);
@@ -604,12 +607,17 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
     }
   }
   __syncthreads();
-  if (tid < 16 * M) {
-    const int m = tid >> 4, rr = tid & 15;
+  constexpr int OR = X2 ? 8 : 16;                                           // output rows of the tile
+  if (tid < OR * M) {
+    const int m = tid / OR, pr = tid % OR;
+    const int rr = X2 ? 2 * pr : pr;
     if (row0 + rr < N) {
       float sum = 0.0f;
       #pragma unroll
-      for (int w = 0; w < WARPS; ++w) sum += red[(w * 2 + m) * 16 + rr];
+      for (int w = 0; w < WARPS; ++w) {
+        sum += red[(w * 2 + m) * 16 + rr];
+        if constexpr (X2) sum += red[(w * 2 + m) * 16 + rr + 1];             // the residual plane
+      }
       if constexpr (F == NVFP4) sum *= glob;
       if constexpr ((MODE & RMS) != 0) {
         float ss = 0.0f;
@@ -617,7 +625,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
         for (int w = 0; w < WARPS; ++w) ss += rss[w * 2 + m];
         sum *= rsqrtf(__fadd_rn(__fdiv_rn(ss, float(K)), ex.eps));
       }
-      const int64_t o = int64_t(m) * N + row0 + rr;
+      const int64_t o = X2 ? int64_t(m) * (N / 2) + row0 / 2 + pr : int64_t(m) * N + row0 + rr;
       if (out_f32) static_cast<float*>(out)[o] = sum;
       else static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(sum);
     }
@@ -733,6 +741,7 @@ cudaError_t launch_qgemv_m2(int fmt, const void* codes, const void* scales, floa
     case INT8_F16: return gemv_m2::launch_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT4: return gemv_m2::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT4_F16: return gemv_m2::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXFP4X2: return gemv_m2::launch_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_m2::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }
@@ -758,6 +767,8 @@ cudaError_t launch_qgemv_gather(int fmt, const void* codes, const void* scales, 
     case INT4: return gemv_m2::launch_gather_fmt<INT4>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
     case INT4_F16:
       return gemv_m2::launch_gather_fmt<INT4_F16>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    case MXFP4X2:
+      return gemv_m2::launch_gather_fmt<MXFP4X2>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
     default:
       return gemv_m2::launch_gather_fmt<INT4_AFFINE>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
   }
@@ -808,6 +819,7 @@ cudaError_t launch_qgemv_multi(int fmt, int count, const void* const* codes, con
     case INT8_F16: QFMT_MULTI(INT8_F16);
     case INT4: QFMT_MULTI(INT4);
     case INT4_F16: QFMT_MULTI(INT4_F16);
+    case MXFP4X2: QFMT_MULTI(MXFP4X2);
     default: QFMT_MULTI(INT4_AFFINE);
   }
 #undef QFMT_MULTI

@@ -43,7 +43,7 @@ constexpr size_t X_BUDGET = 40 * 1024;  // staged f16 activations per CTA (five 
 // 64-byte chunks per lane in flight: four; two for nvfp8 and int4 affine,
 // whose per-chunk scales (eight float32, four scale/bias pairs) stay in registers
 template <int F>
-constexpr int chunks_in_flight() { return (is_fs8<F>() || is_i4<F>()) ? 2 : 4; }
+constexpr int chunks_in_flight() { return (is_fs8<F>() || is_i4<F>() || F == MXFP4X2) ? 2 : 4; }
 
 template <int F>
 struct Shape {
@@ -163,7 +163,7 @@ inline size_t smem_bytes(int F, int M, int kr) {
 // Raw scale words a lane keeps per chunk: 2 (rows g, g + 8) for the byte
 // scales, 4 for int4 affine (two blocks), 8 for nvfp8 (four float32 blocks).
 template <int F>
-constexpr int scale_words() { return is_fs8<F>() ? 8 : (is_i4<F>() ? 4 : 2); }
+constexpr int scale_words() { return (is_fs8<F>() || F == MXFP4X2) ? 8 : (is_i4<F>() ? 4 : 2); }
 
 template <int F, int NB, bool UNI>
 __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __restrict__ codes,
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       }
       sc[i][0] = a;
       sc[i][1] = b;
-    } else if constexpr (is_fs8<F>()) {                                     // each segment's block scale
+    } else if constexpr (is_fs8<F>() || F == MXFP4X2) {                     // each segment's block scale
       #pragma unroll
       for (int sg = 0; sg < 4; ++sg) {
         const int k = kc + sg * SEG;
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       const int c = r * P + i;
       if (c < nch) {                                                        // uniform over the CTA
         float ac[NB][4], d[NB][4];
-        constexpr bool per_seg = F == MXFP4 || is_fs8<F>();                   // a scale per segment
+        constexpr bool per_seg = F == MXFP4 || F == MXFP4X2 || is_fs8<F>();   // a scale per segment
         constexpr bool per_pair = is_mx8<F>() || I4;  // a block per two segments
         #pragma unroll
         for (int sg = 0; sg < 4; ++sg) {
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             }
           }
           // block scales on the float32 MMA results (d rows g: e = 0, 1; g + 8: e = 2, 3)
-          constexpr bool per_seg = F == MXFP4 || is_fs8<F>();                   // a scale per segment
+          constexpr bool per_seg = F == MXFP4 || F == MXFP4X2 || is_fs8<F>();   // a scale per segment
           constexpr bool per_pair = is_mx8<F>() || I4;  // a block per two segments
           if (per_seg || (per_pair && (sg & 1))) {
             const bool first = sg < (per_seg ? 1 : 2);                      // the chunk's first block
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             if constexpr (F == MXFP4) {
               sa = e8m0_f32((sc[i][0] >> (8 * sg)) & 0xFFu);
               sb = e8m0_f32((sc[i][1] >> (8 * sg)) & 0xFFu);
-            } else if constexpr (is_fs8<F>()) {
+            } else if constexpr (is_fs8<F>() || F == MXFP4X2) {
               sa = __uint_as_float(sc[i][sg]);
               sb = __uint_as_float(sc[i][4 + sg]);
             } else if constexpr (I4) {                                      // s * D + (b - 128 s) * sum(x)
@@ -529,15 +529,19 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
     const int rpr = ROWS / int(csize);                                      // rows reduced by this CTA
+    constexpr bool X2 = F == MXFP4X2;                                       // output row = rows 2r + 2r + 1
     const uint32_t m_magic = 0xFFFFFFFFu / uint32_t(M) + 1u;                // i / M, exact for i < 2^16
-    for (int i = tid; i < rpr * M; i += THREADS) {
+    for (int i = tid; i < (X2 ? rpr / 2 : rpr) * M; i += THREADS) {
       const int iq = int(__umulhi(uint32_t(i), m_magic));
-      const int rr = int(rank) * rpr + iq, m = i - iq * M;
+      const int rr = int(rank) * rpr + (X2 ? 2 * iq : iq), m = i - iq * M;
       if (row0 + rr >= N) continue;
       float sum = 0.0f;
-      for (uint32_t q = 0; q < csize; ++q) sum += ld_cluster_f32(red + rr * 16 + m, q);
+      for (uint32_t q = 0; q < csize; ++q) {
+        sum += ld_cluster_f32(red + rr * 16 + m, q);
+        if constexpr (X2) sum += ld_cluster_f32(red + (rr + 1) * 16 + m, q);   // the residual plane
+      }
       if constexpr (F == NVFP4) sum *= glob;
-      const int64_t o = int64_t(m) * N + row0 + rr;
+      const int64_t o = X2 ? int64_t(m) * (N / 2) + (row0 + rr) / 2 : int64_t(m) * N + row0 + rr;
       if (out_f32) static_cast<float*>(out)[o] = sum;
       else static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(sum);
     }
@@ -620,6 +624,7 @@ cudaError_t launch_qgemv_mb(int fmt, const void* codes, const void* scales, floa
     case INT8_F16: return gemv_mb::launch_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT4: return gemv_mb::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT4_F16: return gemv_mb::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXFP4X2: return gemv_mb::launch_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_mb::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }

@@ -36,6 +36,23 @@ __global__ void __launch_bounds__(256) qmm_f32x_kernel(const uint8_t* __restrict
   const int64_t row_bytes = T::four ? K / 2 : K;
   const int64_t nblk = (K + T::block - 1) / T::block;   // int4 affine: a ragged last group
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if constexpr (F == MXFP4X2) {   // rows 2n and 2n + 1: the residual planes of output row n
+    for (int k0 = lane * PIECE; k0 < K; k0 += 32 * PIECE) {
+      const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(codes + (2 * int64_t(n)) * row_bytes + k0 / 2));
+      const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(codes + (2 * int64_t(n) + 1) * row_bytes + k0 / 2));
+      const float* sr = reinterpret_cast<const float*>(scales) + 2 * int64_t(n) * nblk;
+      const float s0 = sr[k0 / 32], s1 = sr[nblk + k0 / 32];
+      const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+      #pragma unroll
+      for (int i = 0; i < PIECE; ++i) {
+        const float w = __fmaf_rn(e2m1_f32((w1[i >> 3] >> (4 * (i & 7))) & 0xFu), s1,
+                                  __fmul_rn(e2m1_f32((w0[i >> 3] >> (4 * (i & 7))) & 0xFu), s0));
+        #pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (m0 + j < M) acc[j] = __fmaf_rn(x[int64_t(m0 + j) * K + k0 + i], w, acc[j]);
+      }
+    }
+  } else {
   for (int k0 = lane * PIECE; k0 < K; k0 += 32 * PIECE) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(codes + n * row_bytes + (T::four ? k0 / 2 : k0)));
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
@@ -58,6 +75,7 @@ __global__ void __launch_bounds__(256) qmm_f32x_kernel(const uint8_t* __restrict
       for (int j = 0; j < 8; ++j)
         if (m0 + j < M) acc[j] = __fmaf_rn(x[int64_t(m0 + j) * K + k], w, acc[j]);
     }
+  }
   }
   #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -100,6 +118,7 @@ cudaError_t launch_qmm_f32x(int fmt, const void* codes, const void* scales, floa
     case INT8_F16: return launch_f32x_fmt<INT8_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case INT4: return launch_f32x_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case INT4_F16: return launch_f32x_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXFP4X2: return launch_f32x_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     default: return launch_f32x_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }

@@ -33,6 +33,11 @@
  *                                                 intN, sign-extended from bit 3, +-7)
  *   QFMT_INT4_F16       signed 4-bit q     64     IEEE half (2 bytes): the fp16-scale twin
  *                                                 of QFMT_INT4
+ *   QFMT_MXFP4X2        two E2M1 planes    32     two FP32 (8 bytes): the two-level residual
+ *                                                 weight w = s0 e2m1(q0) + s1 e2m1(q1) (rlx-cpu
+ *                                                 dequant_matmul_mxfp4x2); level 0 packs w with
+ *                                                 s0 = amax/6, level 1 the float32 residual
+ *                                                 w - s0 e2m1(q0) with s1 = amax(residual)/6
  *
  * Memory layouts (all row-major, no padding, little-endian):
  *   codes   [N, K/2] bytes for 4-bit formats (mxfp4, nvfp4, int4 affine, int4): element k of a row sits in byte
@@ -44,6 +49,9 @@
  *           only the group-64 formats (int4 affine, int8, int4 and twins) can end in
  *           a ragged group (of 32 values, with its own scale and bias; PR
  *           #250: a ragged trailing block, the block count rounded up).
+ *           mxfp4x2: codes [N, 2, K/2] (a row's plane-0 nibbles, then its
+ *           plane-1 nibbles), scales [N, 2, K/32] float32 (a row's s0 of every
+ *           block, then its s1 of every block).
  *   X       [M, K] bf16 (or f32 through qmm_ex), out [M, N] bf16 (or f32).
  *
  * Element values: E2M1 {0,.5,1,1.5,2,3,4,6} with sign bit 3; E4M3 bias 7,
@@ -92,7 +100,8 @@ typedef enum {
   QFMT_INT8 = 9,
   QFMT_INT8_F16 = 10,
   QFMT_INT4 = 11,
-  QFMT_INT4_F16 = 12
+  QFMT_INT4_F16 = 12,
+  QFMT_MXFP4X2 = 13
 } qfmt_format;
 
 typedef enum { QFMT_F32 = 0, QFMT_BF16 = 1 } qfmt_dtype;

@@ -81,7 +81,7 @@ def test_dequant_all_codes_and_scales(fmt):
     sb = opack.scales_nbytes(fmt, n, k)
     if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "nvfp4"):
         scales = np.tile(np.arange(256, dtype=np.uint8), sb // 256 + 1)[:sb]
-    elif fmt in ("nvfp8", "int8", "int4"):
+    elif fmt in ("nvfp8", "int8", "int4", "mxfp4x2"):
         scales = np.concatenate([rng.standard_normal(sb // 4 - 4).astype(np.float32),
                                  np.array([1e-40, 3e38, 0.0, -2.5], np.float32)]).view(np.uint8)
     elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):   # evenly spaced half bit patterns: subnormals, +-inf, NaNs, both signs
@@ -237,6 +237,9 @@ FULL = [
     ("int4", 1, 11008, 4096, False),
     ("int4", 16, 11008, 4096, False),
     ("int4_f16", 4096, 11008, 4096, False),
+    ("mxfp4x2", 1, 4096, 4096, False),
+    ("mxfp4x2", 16, 4096, 4096, False),
+    ("mxfp4x2", 2048, 4096, 4096, False),
 ]
 
 

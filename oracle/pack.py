@@ -32,6 +32,8 @@ Readings taken where the pages are silent (each is listed in the design doc):
   extended from its top bit, clamped to +-(2^(N-1) - 1) -- under an E8M0 scale
   per 32): s = amax / 127 snapped up to a power of two as for mxfp8, q =
   clamp(round_half_away(w / s), -127, 127) stored as a two's-complement byte.
+* mxint4 (PR #250's MXINT4: the signed nibble under an E8M0 scale per 32):
+  as mxint8 with 7 in place of 127, the nibble stored LSB-first two per byte.
 * int8 / int8_f16 (PR #250's symmetric integer formats: "Int8 (symmetric
   affine, scale-only, group 64)" on the FP32 per-group scale path, the int8
   codec symmetric at +-127; the fp16-scale axis gives int8 its half-scale
@@ -71,22 +73,24 @@ import numpy as np
 from . import codec
 
 FORMATS = ("mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8", "int4_affine", "nvfp8_f16", "mxint8",
-           "int8", "int8_f16", "int4", "int4_f16", "mxfp4x2")
+           "int8", "int8_f16", "int4", "int4_f16", "mxfp4x2", "mxint4")
 RAGGED = ("int4_affine", "int8", "int8_f16", "int4", "int4_f16")   # block 64: K may end in a group of 32
 SYM_INT = ("int8", "int8_f16", "int4", "int4_f16")                 # symmetric integers, float scale per 64
 
 BLOCK = {"mxfp4": 32, "nvfp4": 16, "mxfp8_e4m3": 32, "mxfp8_e5m2": 32, "nvfp8": 16, "int4_affine": 64,
-         "nvfp8_f16": 16, "mxint8": 32, "int8": 64, "int8_f16": 64, "int4": 64, "int4_f16": 64, "mxfp4x2": 32}
+         "nvfp8_f16": 16, "mxint8": 32, "int8": 64, "int8_f16": 64, "int4": 64, "int4_f16": 64, "mxfp4x2": 32,
+         "mxint4": 32}
 ELEM_BITS = {"mxfp4": 4, "nvfp4": 4, "mxfp8_e4m3": 8, "mxfp8_e5m2": 8, "nvfp8": 8, "int4_affine": 4, "nvfp8_f16": 8,
              "mxint8": 8, "int8": 8, "int8_f16": 8, "int4": 4, "int4_f16": 4,
-             "mxfp4x2": 8}                                   # bits per weight (mxfp4x2: two nibbles)
+             "mxfp4x2": 8, "mxint4": 4}                      # bits per weight (mxfp4x2: two nibbles)
 SCALE_BYTES = {"mxfp4": 1, "nvfp4": 1, "mxfp8_e4m3": 1, "mxfp8_e5m2": 1, "nvfp8": 4, "int4_affine": 4,
                "nvfp8_f16": 2, "mxint8": 1, "int8": 4, "int8_f16": 2, "int4": 4, "int4_f16": 2,
-               "mxfp4x2": 8}                                 # bytes per block (mxfp4x2: s0 and s1)
+               "mxfp4x2": 8, "mxint4": 1}                    # bytes per block (mxfp4x2: s0 and s1)
 _ELEM = {"mxfp4": ("e2m1", codec.E2M1_MAX), "nvfp4": ("e2m1", codec.E2M1_MAX),
          "mxfp8_e4m3": ("e4m3", codec.E4M3_MAX), "mxfp8_e5m2": ("e5m2", codec.E5M2_MAX),
          "nvfp8": ("e4m3", codec.E4M3_MAX), "nvfp8_f16": ("e4m3", codec.E4M3_MAX), "mxint8": ("int8", 127.0),
-         "int8": ("int8", 127.0), "int8_f16": ("int8", 127.0), "int4": ("int4", 7.0), "int4_f16": ("int4", 7.0)}
+         "int8": ("int8", 127.0), "int8_f16": ("int8", 127.0), "int4": ("int4", 7.0), "int4_f16": ("int4", 7.0),
+         "mxint4": ("int4", 7.0)}
 
 F32 = np.float32
 
@@ -156,7 +160,7 @@ def pack(fmt: str, w: np.ndarray):
         return _pack_mxfp4x2(wb, n, k)
 
     elem, maxf = _ELEM[fmt]
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4"):
         s = np.where(amax > 0, amax / F32(maxf), F32(1.0)).astype(F32)   # step 2
         scode = codec.e8m0_encode_ceil(s)                                  # step 3
         eff = codec.E8M0_TABLE[scode].astype(F32)                          # exact power of two

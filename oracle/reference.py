@@ -8,8 +8,8 @@
 
 Value definitions (page title, then the section):
 
-* mxint8: w = q * 2^(scale_bits - 127), q the signed byte -- PR #250, the
-  MXINT axis (symmetric integer element, E8M0 block scale).
+* mxint8 / mxint4: w = q * 2^(scale_bits - 127), q the signed byte (nibble)
+  -- PR #250, the MXINT axis (symmetric integer element, E8M0 block scale).
 * mxfp4 / mxfp8: w = elem(code) * 2^(scale_bits - 127) -- metaltile PR #250,
   commit "First spec-conformant block-scaled dequant kernel: mt_mxfp4_dequant"
   and the commit completing the mxfp8 dequant kernels.
@@ -81,7 +81,7 @@ def block_scales(fmt: str, scales: np.ndarray, global_scale: float, n: int, k: i
     """
     nb = -(-k // BLOCK[fmt])
     s = np.asarray(scales, dtype=np.uint8).reshape(n, -1)
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4"):
         return codec.E8M0_TABLE[s.reshape(n, nb)], None
     if fmt == "nvfp4":
         return codec.E4M3_TABLE[s.reshape(n, nb)], None
@@ -102,7 +102,7 @@ def element_values(fmt: str, codes: np.ndarray) -> np.ndarray:
         return codec.E5M2_TABLE[codes]
     if fmt in ("mxint8", "int8", "int8_f16"):            # the two's-complement byte
         return codes.astype(np.uint8).view(np.int8).astype(np.float64)
-    if fmt in ("int4", "int4_f16"):                      # the two's-complement nibble, sign-extended from bit 3
+    if fmt in ("int4", "int4_f16", "mxint4"):            # the two's-complement nibble, sign-extended from bit 3
         c = codes.astype(np.int64)
         return np.where(c >= 8, c - 16, c).astype(np.float64)
     return codes.astype(np.float64)                      # int4 affine: q itself

@@ -27,7 +27,7 @@ def _elem_values_lib(fmt, codes_nk):
         return (codes_nk.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
     if fmt in ("mxint8", "int8", "int8_f16"):
         return torch.from_numpy(codes_nk.astype(np.uint8)).view(torch.int8).double().numpy()
-    if fmt in ("int4", "int4_f16"):     # the nibble in the top of a byte, arithmetic shift back down
+    if fmt in ("int4", "int4_f16", "mxint4"):     # the nibble in the top of a byte, arithmetic shift back down
         return torch.from_numpy((codes_nk.astype(np.uint8) << 4).astype(np.uint8)).view(torch.int8).double().numpy() / 16
     return codes_nk.astype(np.float64)
 
@@ -39,7 +39,7 @@ def test_byte_sizes():
     w = synth.weights(n, k, seed=5)
     for fmt in FMTS:
         c, s, g = pack.pack(fmt, w)
-        bits = 4 if fmt in ("mxfp4", "nvfp4", "int4_affine", "int4", "int4_f16") else 8
+        bits = 4 if fmt in ("mxfp4", "nvfp4", "int4_affine", "int4", "int4_f16", "mxint4") else 8
         assert c.nbytes == n * k * bits // 8 == pack.codes_nbytes(fmt, n, k)
         per_scale = {"nvfp8": 4, "int4_affine": 4, "nvfp8_f16": 2, "int8": 4, "int8_f16": 2, "int4": 4,
                      "int4_f16": 2, "mxfp4x2": 8}.get(fmt, 1)
@@ -67,7 +67,7 @@ def test_zero_blocks():
     for fmt in FMTS:
         c, s, g = pack.pack(fmt, w)
         assert not c.any(), fmt
-        if fmt in MX or fmt == "mxint8":
+        if fmt in MX or fmt in ("mxint8", "mxint4"):
             assert (s == 127).all()
         elif fmt == "nvfp4":
             assert (s == 0x38).all() and g == 1.0
@@ -128,7 +128,7 @@ def test_value_idempotence(fmt):
 
 FLOORS = {"mxfp4": 0.98, "nvfp4": 0.98, "int4_affine": 0.99,
           "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999, "nvfp8_f16": 0.999, "mxint8": 0.999,
-          "int8": 0.9999, "int8_f16": 0.9999, "int4": 0.99, "int4_f16": 0.99, "mxfp4x2": 0.9999}
+          "int8": 0.9999, "int8_f16": 0.9999, "int4": 0.99, "int4_f16": 0.99, "mxfp4x2": 0.9999, "mxint4": 0.98}
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -426,3 +426,29 @@ def test_mxfp4x2_two_negative_zero_codes_give_negative_zero():
     w = reference.dequant_f32("mxfp4x2", c.reshape(1, -1), s, 1.0, 1, 32)
     assert np.signbit(w[0, 0]) and np.signbit(w[0, 1]) and not np.signbit(w[0, 2])
     assert (w == 0).all()
+
+
+def test_mxint4_exactly_representable_roundtrip():
+    # W = q * 2^e with q in [-7, 7] and +-7 in every block of 32: the packer
+    # returns exactly those nibbles and E8M0 bytes (PR #250 MXINT4)
+    rng = np.random.default_rng(57)
+    n, k = 4, 128
+    q = rng.integers(-7, 8, size=(n, k))
+    q[:, ::32] = 7 * rng.choice([-1, 1], size=(n, k // 32))
+    e = rng.integers(-40, 30, size=(n, k // 32))
+    w = (q * np.repeat(2.0 ** e, 32, axis=1)).astype(np.float32)
+    c, s, g = pack.pack("mxint4", w)
+    assert np.array_equal(s.astype(np.int64), e + 127)
+    assert np.array_equal(c & 0xF, (q[:, 0::2] & 0xF).astype(np.uint8))
+    assert np.array_equal(c >> 4, (q[:, 1::2] & 0xF).astype(np.uint8))
+    assert np.array_equal(reference.dequant_exact("mxint4", c, s, g, n, k), w.astype(np.float64))
+
+
+def test_mxint4_scale_snaps_up_and_rounds_half_away():
+    # amax 6 -> 6 / 7 snapped up to 2^0; 2.5 -> 3, -2.5 -> -3, -0.5 -> -1
+    w = np.zeros((1, 32), np.float32)
+    w[0, 0] = 6.0
+    w[0, 1:4] = [2.5, -2.5, -0.5]
+    c, s, _ = pack.pack("mxint4", w)
+    assert s[0, 0] == 127
+    assert list(reference.dequant_exact("mxint4", c, s, 1.0, 1, 32)[0, :4]) == [6, 3, -3, -1]

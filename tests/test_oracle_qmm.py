@@ -42,13 +42,13 @@ def _lib_elem(fmt, c):
         return Fraction(float(np.array([c << 8], np.uint16).view(np.float16)[0]))
     if fmt in ("mxint8", "int8", "int8_f16"):
         return Fraction(c - 256 if c >= 128 else c)
-    if fmt in ("int4", "int4_f16"):
+    if fmt in ("int4", "int4_f16", "mxint4"):
         return Fraction(c - 16 if c >= 8 else c)
     return Fraction(c)
 
 
 def _lib_scale(fmt, sbytes, n, b):
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4"):
         return Fraction(2) ** (int(sbytes[n][b]) - 127), Fraction(0)
     if fmt == "nvfp4":
         v = torch.tensor([int(sbytes[n][b])], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()
@@ -88,7 +88,7 @@ def _brute_qmm(fmt, codes, scales, g, x64, m, n, k):
             if fmt == "mxfp4x2":
                 wrow.append(_x2_weight(codes[j], scales[j], kk, k))
                 continue
-            if fmt in ("mxfp4", "nvfp4", "int4_affine", "int4", "int4_f16"):
+            if pack.ELEM_BITS[fmt] == 4:
                 byte = codes[j][kk // 2]
                 c = (byte >> (4 * (kk % 2))) & 0xF
             else:

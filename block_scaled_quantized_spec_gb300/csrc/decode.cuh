@@ -24,7 +24,7 @@ namespace qfmt_dev {
 
 enum Fmt {
   MXFP4 = 1, NVFP4 = 2, MXFP8_E4M3 = 3, MXFP8_E5M2 = 4, NVFP8 = 5, INT4_AFFINE = 6, NVFP8_F16 = 7, MXINT8 = 8,
-  INT8 = 9, INT8_F16 = 10, INT4 = 11, INT4_F16 = 12, MXFP4X2 = 13
+  INT8 = 9, INT8_F16 = 10, INT4 = 11, INT4_F16 = 12, MXFP4X2 = 13, MXINT4 = 14
 };
 
 template <int F> struct FmtTraits;
@@ -44,13 +44,17 @@ template <> struct FmtTraits<INT4_F16> { static constexpr bool four = true; stat
 // plane 0 of output row n, row 2n + 1 its plane 1) with a float32 scale per
 // 32; an output is the sum of its two rows' products.
 template <> struct FmtTraits<MXFP4X2> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 4; };
+template <> struct FmtTraits<MXINT4> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 1; };
 
 // 8-bit elements under an E8M0 scale per 32 (mxfp8 E4M3/E5M2, mxint8), and
 // every E8M0-scaled format (those and mxfp4)
 template <int F>
 constexpr bool is_mx8() { return F == MXFP8_E4M3 || F == MXFP8_E5M2 || F == MXINT8; }
+// 4-bit elements under an E8M0 scale per 32 (mxfp4's E2M1, mxint4's signed nibble)
 template <int F>
-constexpr bool is_e8m0() { return F == MXFP4 || is_mx8<F>(); }
+constexpr bool is_mx4() { return F == MXFP4 || F == MXINT4; }
+template <int F>
+constexpr bool is_e8m0() { return is_mx4<F>() || is_mx8<F>(); }
 
 // 8-bit elements under a float block scale (float32 or IEEE half): nvfp8 and
 // its twin (E4M3, per 16), symmetric int8 and its twin (per 64)
@@ -69,7 +73,9 @@ constexpr bool is_i4() { return F == INT4_AFFINE || F == INT4 || F == INT4_F16; 
 template <int F>
 constexpr bool is_i4sym() { return F == INT4 || F == INT4_F16; }
 inline constexpr bool fmt_is_i4(int f) { return f == INT4_AFFINE || f == INT4 || f == INT4_F16; }
-inline constexpr bool fmt_is_four(int f) { return f == MXFP4 || f == NVFP4 || f == MXFP4X2 || fmt_is_i4(f); }
+inline constexpr bool fmt_is_four(int f) {
+  return f == MXFP4 || f == NVFP4 || f == MXFP4X2 || f == MXINT4 || fmt_is_i4(f);
+}
 
 // Block scale idx of a float-scaled array as float32: the stored float32, or
 // the (exact) float32 of the stored IEEE half.
@@ -191,6 +197,33 @@ __device__ __forceinline__ void e2m1x8_bf16(uint32_t w, uint32_t r[4]) {
   r[1] = prmt(l1, h1, 0x7351u) | ((w << 8) & 0x80008000u);
   r[2] = prmt(l2, h2, 0x6240u) | ((w << 4) & 0x80008000u);
   r[3] = prmt(l2, h2, 0x7351u) | (w & 0x80008000u);
+}
+
+// 8 signed two's-complement nibbles -> bf16x2 {q0,q4} {q1,q5} {q2,q6} {q3,q7}
+// (the pairing of e2m1x8_bf16), exact: the nibble with its sign bit flipped
+// is u = q + 8, 0x4300 | u the bf16 of 128 + u, less 136.
+__device__ __forceinline__ void sint4x8_bf16(uint32_t w, uint32_t r[4]) {
+  const uint32_t t = w ^ 0x88888888u;
+  #pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t u = ((t >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r[j]) : "r"(u), "r"(0x43084308u));
+  }
+}
+
+// 8 signed two's-complement nibbles (code i at bits 4i) -> f16x2 (q0,q1)
+// (q2,q3) (q4,q5) (q6,q7), exact: byte i spread to both halves, the low half
+// keeps its low nibble under the exponent of 1024 (1024 + u), the high half
+// its high nibble four bits up (1024 + 16 u); one fma by (1, 1/16) and
+// (-1032, -72) leaves u - 8 = q in each half (u: the nibble, sign bit flipped).
+__device__ __forceinline__ void sint4x8_f16(uint32_t w, uint32_t r[4]) {
+  const uint32_t t = w ^ 0x88888888u;
+  #pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t b = prmt(t, 0u, 0x4040u | (uint32_t(i) * 0x0101u));   // byte i in bytes 0 and 2
+    const uint32_t y = (b & 0x00F0000Fu) | 0x64006400u;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[i]) : "r"(y), "r"(0x2C003C00u), "r"(0xD480E408u));
+  }
 }
 
 // 8 unsigned 4-bit q (int4 affine) -> bf16x2 {q0,q4} {q1,q5} {q2,q6} {q3,q7},
@@ -318,9 +351,9 @@ template <int F>
 __device__ __forceinline__ void decode_piece(const uint4& v, const PieceScale& ps,
                                              uint32_t A[FmtTraits<F>::four ? 8 : 4][2]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  if constexpr (F == MXFP4 || F == NVFP4) {
+  if constexpr (F == MXFP4 || F == NVFP4 || F == MXINT4) {
     uint32_t sc0, sc1;
-    if constexpr (F == MXFP4) {
+    if constexpr (is_mx4<F>()) {
       sc0 = sc1 = bf16x2_splat(e8m0_bf16(ps.a));
     } else {
       sc0 = bf16x2_splat(f32_to_bf16bits(e4m3_f32(ps.a & 0xFFu)));
@@ -329,7 +362,8 @@ __device__ __forceinline__ void decode_piece(const uint4& v, const PieceScale& p
     #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t r[4];
-      e2m1x8_bf16(w[j], r);
+      if constexpr (F == MXINT4) sint4x8_bf16(w[j], r);
+      else e2m1x8_bf16(w[j], r);
       const uint32_t sc = j < 2 ? sc0 : sc1;
       A[2 * j][0] = hmul2(r[0], sc);
       A[2 * j][1] = hmul2(r[1], sc);

@@ -28,7 +28,7 @@ __device__ __forceinline__ float dq_value(uint32_t code, float s, float b, float
   if constexpr (F == MXFP8_E5M2) return __fmul_rn(e5m2_f32(code), s);
   if constexpr (is_int8<F>()) return __fmul_rn(float(int8_t(uint8_t(code))), s);
   if constexpr (is_fs8<F>()) return __fmul_rn(e4m3_f32(code), s);
-  if constexpr (is_i4sym<F>()) return __fmul_rn(float(int(code ^ 8u) - 8), s);         // the sign-extended nibble
+  if constexpr (is_i4sym<F>() || F == MXINT4) return __fmul_rn(float(int(code ^ 8u) - 8), s);   // the sign-extended nibble
   return __fmaf_rn(s, float(code), b);                                               // INT4_AFFINE
 }
 
@@ -150,6 +150,7 @@ cudaError_t launch_dequant(int fmt, const void* codes, const void* scales, float
     case INT4: return launch_dequant_fmt<INT4>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case INT4_F16: return launch_dequant_fmt<INT4_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case MXFP4X2: return launch_dequant_fmt<MXFP4X2>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case MXINT4: return launch_dequant_fmt<MXINT4>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     default: return launch_dequant_fmt<INT4_AFFINE>(codes, scales, glob, out, out_bf16, N, K, st, sms);
   }
 }

@@ -35,11 +35,12 @@ int fail(int status, const char* fmt, ...) {
 
 void clear_error() { g_err[0] = '\0'; }
 
-bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_MXFP4X2; }
+bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_MXINT4; }
 
 int block_of(int fmt) {
   switch (fmt) {
-    case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: case QFMT_MXFP4X2: return 32;
+    case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: case QFMT_MXFP4X2:
+    case QFMT_MXINT4: return 32;
     case QFMT_NVFP4: case QFMT_NVFP8: case QFMT_NVFP8_F16: return 16;
     case QFMT_INT4_AFFINE: case QFMT_INT8: case QFMT_INT8_F16: case QFMT_INT4: case QFMT_INT4_F16: return 64;
     default: return 0;
@@ -47,11 +48,13 @@ int block_of(int fmt) {
 }
 
 bool is_4bit(int fmt) {
-  return fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4 || fmt == QFMT_INT4_AFFINE || fmt == QFMT_INT4 || fmt == QFMT_INT4_F16;
+  return fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4 || fmt == QFMT_INT4_AFFINE || fmt == QFMT_INT4 || fmt == QFMT_INT4_F16 ||
+         fmt == QFMT_MXINT4;
 }
 
 bool is_sym_int(int fmt) {
-  return fmt == QFMT_MXINT8 || fmt == QFMT_INT8 || fmt == QFMT_INT8_F16 || fmt == QFMT_INT4 || fmt == QFMT_INT4_F16;
+  return fmt == QFMT_MXINT8 || fmt == QFMT_INT8 || fmt == QFMT_INT8_F16 || fmt == QFMT_INT4 || fmt == QFMT_INT4_F16 ||
+         fmt == QFMT_MXINT4;
 }
 
 // Largest finite element magnitude: amax / elem_max is the raw block scale.
@@ -60,7 +63,7 @@ float elem_max(int fmt) {
     case QFMT_MXFP4: case QFMT_NVFP4: case QFMT_MXFP4X2: return 6.0f;
     case QFMT_MXFP8_E5M2: return 57344.0f;
     case QFMT_MXINT8: case QFMT_INT8: case QFMT_INT8_F16: return 127.0f;
-    case QFMT_INT4: case QFMT_INT4_F16: return 7.0f;
+    case QFMT_INT4: case QFMT_INT4_F16: case QFMT_MXINT4: return 7.0f;
     default: return 448.0f;   // E4M3
   }
 }
@@ -203,7 +206,7 @@ using namespace qfmt;
 
 extern "C" {
 
-int qfmt_version(void) { return 105; }
+int qfmt_version(void) { return 106; }
 
 const char* qfmt_last_error(void) { return qfmt::g_err; }
 
@@ -316,7 +319,7 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
         for (int j = 0; j < len; ++j) amax = std::max(amax, std::fabs(wb[j]));
         float eff;
         switch (fmt) {
-          case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: {
+          case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: case QFMT_MXINT4: {
             const float s = amax > 0.0f ? amax / elem_max(fmt) : 1.0f;
             const uint32_t code = enc_e8m0_ceil(s);
             sb[n * nb + b] = uint8_t(code);

@@ -709,6 +709,7 @@ cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, floa
     case INT4: return tc::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT4_F16: return tc::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case MXFP4X2: return tc::launch_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXINT4: return tc::launch_fmt<MXINT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return tc::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }

@@ -344,8 +344,13 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
                 int4x8_f16_biased(i4_u<F>(wa), fa);
                 int4x8_f16_biased(i4_u<F>(wb), fb);
               } else {
-                e2m1x8_f16(wa, fa);
-                e2m1x8_f16(wb, fb);
+                if constexpr (F == MXINT4) {
+                  sint4x8_f16(wa, fa);
+                  sint4x8_f16(wb, fb);
+                } else {
+                  e2m1x8_f16(wa, fa);
+                  e2m1x8_f16(wb, fb);
+                }
                 if constexpr (F == NVFP4) {
                   // the lane's word of this segment lies in micro-block 2 sgm + t/2 of the unit
                   const uint32_t ca = __float_as_uint(sca[2 * sgm + (t >> 1)]);
@@ -361,7 +366,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
               for (int nb = 0; nb < NB; ++nb) {
                 const int m = min(nb * 8 + g, M - 1);
                 const uint4 xv = *reinterpret_cast<const uint4*>(xs + size_t(m) * xstride + u * 64 + sgm * 32 + 8 * t);
-                if constexpr (F == MXFP4 || F == MXFP4X2) {   // a block scale per segment
+                if constexpr (is_mx4<F>() || F == MXFP4X2) {   // a block scale per segment
                   float d[4] = {0.f, 0.f, 0.f, 0.f};
                   mma_f16(d, fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
                   mma_f16(d, fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
@@ -547,6 +552,7 @@ cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float g
     case INT4: return gemv::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case INT4_F16: return gemv::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case MXFP4X2: return gemv::launch_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXINT4: return gemv::launch_fmt<MXINT4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     default: return gemv::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }

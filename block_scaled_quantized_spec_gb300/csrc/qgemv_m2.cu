@@ -96,7 +96,9 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int j) {
 // (8q+6, 8q+7); int4 the biased pairs (q_{8q+b}, q_{8q+b+4}), b = 0..3.
 template <int F>
 __device__ __forceinline__ void frags8(const uint4& v, int q, uint32_t r[4]) {
-  if constexpr (F == MXFP4 || F == NVFP4 || F == MXFP4X2) {
+  if constexpr (F == MXINT4) {
+    sint4x8_f16(word(v, q), r);
+  } else if constexpr (F == MXFP4 || F == NVFP4 || F == MXFP4X2) {
     e2m1x8_f16(word(v, q), r);
   } else if constexpr (is_i4<F>()) {
     const uint32_t w = i4_u<F>(word(v, q));
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
     wb[i] = kin ? ldg_stream(pb + int64_t(c) * 64) : make_uint4(0, 0, 0, 0);
     // the block (or pair of blocks) of quad lanes a0 and a0 + 1 in this chunk;
     // a block outside the matrix reads as E8M0 127 / zero (its D column is zero)
-    if constexpr (F == MXFP4) {
+    if constexpr (is_mx4<F>()) {
       const int e = k0 / 32;                                                  // even
       if (uni) {
         const uint32_t pa2 = __ldg(reinterpret_cast<const uint16_t*>(sra) + e / 2);
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
       const int k0 = c * CODES + LANE * a0;
       const int s0 = min(k0 / 32, spans - 1), s1 = min((k0 + LANE) / 32, spans - 1);
       const float x0s = xsc[md * spans + s0], x1s = xsc[md * spans + s1];
-      if constexpr (F == MXFP4) {
+      if constexpr (is_mx4<F>()) {
         const uint32_t w4 = cs[i].a0;
         float q0, q1, q2, q3;
         if (exact) {
@@ -742,6 +744,7 @@ cudaError_t launch_qgemv_m2(int fmt, const void* codes, const void* scales, floa
     case INT4: return gemv_m2::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT4_F16: return gemv_m2::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case MXFP4X2: return gemv_m2::launch_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXINT4: return gemv_m2::launch_fmt<MXINT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_m2::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }
@@ -769,6 +772,7 @@ cudaError_t launch_qgemv_gather(int fmt, const void* codes, const void* scales, 
       return gemv_m2::launch_gather_fmt<INT4_F16>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
     case MXFP4X2:
       return gemv_m2::launch_gather_fmt<MXFP4X2>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
+    case MXINT4: return gemv_m2::launch_gather_fmt<MXINT4>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
     default:
       return gemv_m2::launch_gather_fmt<INT4_AFFINE>(codes, scales, glob, x, eidx, out, out_f32, m, n, k, e, st);
   }
@@ -820,6 +824,7 @@ cudaError_t launch_qgemv_multi(int fmt, int count, const void* const* codes, con
     case INT4: QFMT_MULTI(INT4);
     case INT4_F16: QFMT_MULTI(INT4_F16);
     case MXFP4X2: QFMT_MULTI(MXFP4X2);
+    case MXINT4: QFMT_MULTI(MXINT4);
     default: QFMT_MULTI(INT4_AFFINE);
   }
 #undef QFMT_MULTI

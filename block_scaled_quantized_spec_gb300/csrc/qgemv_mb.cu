@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
     }
     const int kc = k0 + c * CODES;                                          // first k of the chunk
     auto live = [&](int k) { return UNI || (c < nch && k < k1); };
-    if constexpr (F == MXFP4) {                                             // one E8M0 block per segment
+    if constexpr (is_mx4<F>()) {                                            // one E8M0 block per segment
       uint32_t a = 0, b = 0;
       #pragma unroll
       for (int sg = 0; sg < 4; ++sg) {
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       const int c = r * P + i;
       if (c < nch) {                                                        // uniform over the CTA
         float ac[NB][4], d[NB][4];
-        constexpr bool per_seg = F == MXFP4 || F == MXFP4X2 || is_fs8<F>();   // a scale per segment
+        constexpr bool per_seg = is_mx4<F>() || F == MXFP4X2 || is_fs8<F>();  // a scale per segment
         constexpr bool per_pair = is_mx8<F>() || I4;  // a block per two segments
         #pragma unroll
         for (int sg = 0; sg < 4; ++sg) {
@@ -404,8 +404,13 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
                 fb[b] = ((i4_u<F>(wb[i][sg]) >> (4 * b)) & 0x000F000Fu) | 0x43004300u;
               }
             } else {
-              e2m1x8_f16(wa[i][sg], fa);
-              e2m1x8_f16(wb[i][sg], fb);
+              if constexpr (F == MXINT4) {
+                sint4x8_f16(wa[i][sg], fa);
+                sint4x8_f16(wb[i][sg], fb);
+              } else {
+                e2m1x8_f16(wa[i][sg], fa);
+                e2m1x8_f16(wb[i][sg], fb);
+              }
               if constexpr (F == NVFP4) {                                   // E4M3 micro-scale, exact in f16
                 uint32_t s2a, s2b;
                 const uint32_t ba = (sc[i][0] >> (8 * sg)) & 0xFFu, bb = (sc[i][1] >> (8 * sg)) & 0xFFu;
@@ -443,12 +448,12 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             }
           }
           // block scales on the float32 MMA results (d rows g: e = 0, 1; g + 8: e = 2, 3)
-          constexpr bool per_seg = F == MXFP4 || F == MXFP4X2 || is_fs8<F>();   // a scale per segment
+          constexpr bool per_seg = is_mx4<F>() || F == MXFP4X2 || is_fs8<F>();  // a scale per segment
           constexpr bool per_pair = is_mx8<F>() || I4;  // a block per two segments
           if (per_seg || (per_pair && (sg & 1))) {
             const bool first = sg < (per_seg ? 1 : 2);                      // the chunk's first block
             float sa, sb, ba = 0.0f, bb = 0.0f, xm0[NB], xm1[NB];
-            if constexpr (F == MXFP4) {
+            if constexpr (is_mx4<F>()) {
               sa = e8m0_f32((sc[i][0] >> (8 * sg)) & 0xFFu);
               sb = e8m0_f32((sc[i][1] >> (8 * sg)) & 0xFFu);
             } else if constexpr (is_fs8<F>() || F == MXFP4X2) {
@@ -625,6 +630,7 @@ cudaError_t launch_qgemv_mb(int fmt, const void* codes, const void* scales, floa
     case INT4: return gemv_mb::launch_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case INT4_F16: return gemv_mb::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case MXFP4X2: return gemv_mb::launch_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case MXINT4: return gemv_mb::launch_fmt<MXINT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_mb::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }

@@ -17,7 +17,7 @@ __device__ __forceinline__ float exact_weight(uint32_t code, float s, float b) {
   if constexpr (is_int8<F>()) return __fmul_rn(float(int8_t(uint8_t(code))), s);
   if constexpr (F == MXFP8_E4M3 || is_fs8<F>()) return __fmul_rn(e4m3_f32(code), s);
   if constexpr (F == MXFP8_E5M2) return __fmul_rn(e5m2_f32(code), s);
-  if constexpr (is_i4sym<F>()) return __fmul_rn(float(int(code ^ 8u) - 8), s);
+  if constexpr (is_i4sym<F>() || F == MXINT4) return __fmul_rn(float(int(code ^ 8u) - 8), s);
   return __fmaf_rn(s, float(code), b);
 }
 
@@ -119,6 +119,7 @@ cudaError_t launch_qmm_f32x(int fmt, const void* codes, const void* scales, floa
     case INT4: return launch_f32x_fmt<INT4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case INT4_F16: return launch_f32x_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case MXFP4X2: return launch_f32x_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case MXINT4: return launch_f32x_fmt<MXINT4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     default: return launch_f32x_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }

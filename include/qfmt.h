@@ -24,6 +24,9 @@
  *                                                 packer clamps q to +-127 and rounds half
  *                                                 away from zero; a stored -128 decodes as
  *                                                 -128)
+ *   QFMT_MXINT4         signed 4-bit q     32     E8M0 byte: w = q * 2^(b-127), q the
+ *                                                 two's-complement nibble (PR #250's MXINT4;
+ *                                                 the packer clamps to +-7)
  *   QFMT_INT8           signed int8 q      64     FP32 (4 bytes): w = q * scale (PR #250's
  *                                                 symmetric int8, scale-only, +-127)
  *   QFMT_INT8_F16       signed int8 q      64     IEEE half (2 bytes): the fp16-scale twin
@@ -40,7 +43,7 @@
  *                                                 w - s0 e2m1(q0) with s1 = amax(residual)/6
  *
  * Memory layouts (all row-major, no padding, little-endian):
- *   codes   [N, K/2] bytes for 4-bit formats (mxfp4, nvfp4, int4 affine, int4): element k of a row sits in byte
+ *   codes   [N, K/2] bytes for 4-bit formats (mxfp4, nvfp4, int4 affine, int4, mxint4): element k of a row sits in byte
  *           k/2, low nibble for even k (LSB-first; 8 codes per u32 word);
  *           [N, K] bytes for 8-bit formats.
  *   scales  [N, ceil(K/block)] entries of the sizes above; int4 affine stores
@@ -101,7 +104,8 @@ typedef enum {
   QFMT_INT8_F16 = 10,
   QFMT_INT4 = 11,
   QFMT_INT4_F16 = 12,
-  QFMT_MXFP4X2 = 13
+  QFMT_MXFP4X2 = 13,
+  QFMT_MXINT4 = 14
 } qfmt_format;
 
 typedef enum { QFMT_F32 = 0, QFMT_BF16 = 1 } qfmt_dtype;

@@ -79,7 +79,7 @@ def test_dequant_all_codes_and_scales(fmt):
     cb = opack.codes_nbytes(fmt, n, k)
     codes = np.tile(np.arange(256, dtype=np.uint8), cb // 256 + 1)[:cb].reshape(n, -1)
     sb = opack.scales_nbytes(fmt, n, k)
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "nvfp4"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4", "nvfp4"):
         scales = np.tile(np.arange(256, dtype=np.uint8), sb // 256 + 1)[:sb]
     elif fmt in ("nvfp8", "int8", "int4", "mxfp4x2"):
         scales = np.concatenate([rng.standard_normal(sb // 4 - 4).astype(np.float32),
@@ -240,6 +240,9 @@ FULL = [
     ("mxfp4x2", 1, 4096, 4096, False),
     ("mxfp4x2", 16, 4096, 4096, False),
     ("mxfp4x2", 2048, 4096, 4096, False),
+    ("mxint4", 1, 4096, 4096, False),
+    ("mxint4", 8, 4096, 4096, False),
+    ("mxint4", 2048, 4096, 4096, False),
 ]
 
 
@@ -273,7 +276,7 @@ def test_full_size_sampled(fmt, m, n, k, outl):
     assert (err <= bound + np.abs(got) * 2.0 ** -9).all(), float((err / bound).max())
 
 
-@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8"])
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4"])
 @pytest.mark.parametrize("m", [1, 2, 5])
 def test_gemv_e8m0_special_scales(fmt, m):
     # E8M0 code 0 (2^-127, a float32 subnormal) among ordinary scales, then a
@@ -326,7 +329,7 @@ def test_gemv_fallback_long_k(fmt, m):
     _check_qmm(out, ref, bound, (fmt, m, k))
 
 
-@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "int4_affine", "int4"])
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "int4_affine", "int4", "mxint4"])
 @pytest.mark.parametrize("m", [1, 2])
 def test_wide_gemv_four_warp_ctas(fmt, m):
     # more 16-row tiles than two per SM: the 4-bit GEMV runs 4-warp CTAs; N

@@ -8,7 +8,7 @@
 // folds each block scale into a per-block partial sum, and lowp_scaled_matmul,
 // which factors both operands' block scales out of each block's sum).
 //
-// Dispatch: M <= 2 -> qgemv_m2.cu; 3 <= M <= 16 -> qgemv_mb.cu; otherwise the
+// Dispatch: M <= 2 -> qgemv_m2.cuh; 3 <= M <= 16 -> qgemv_mb.cu; otherwise the
 // kernel below, which takes K in passes:
 //  * a CTA owns 16 (M <= 2) or 32 weight rows; one thread bulk-copies the
 //    CTA's code rows for a pass into shared memory with cp.async.bulk on an

@@ -385,7 +385,7 @@ def run_reference(args):
 # kernel reports null until it is captured again).
 TRAFFIC = {
     "kernel_source": "block_scaled_quantized_spec_gb300/csrc/qgemv_m2.cuh",
-    "sha256_16": "cd6f13dabad9c0db",
+    "sha256_16": "57558de3ff7d0013",
     "bytes": 8940544,
     "profile": "profiles/qgemv_m2_mxfp4_M1_N4096_K4096.md",
 }

@@ -110,7 +110,7 @@ __device__ __forceinline__ void i4_scale_bias(uint32_t wd, float& s, float& b) {
 // two's-complement nibble q becomes u = q + 8 by flipping its sign bit.
 template <int F>
 __device__ __forceinline__ uint32_t i4_u(uint32_t w) {
-  if constexpr (is_i4sym<F>()) return w ^ 0x88888888u;
+  if constexpr (is_i4sym<F>() || F == MXINT4) return w ^ 0x88888888u;
   else return w;
 }
 

@@ -102,11 +102,9 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int j) {
 // (8q+6, 8q+7); int4 the biased pairs (q_{8q+b}, q_{8q+b+4}), b = 0..3.
 template <int F>
 __device__ __forceinline__ void frags8(const uint4& v, int q, uint32_t r[4]) {
-  if constexpr (F == MXINT4) {
-    sint4x8_f16(word(v, q), r);
-  } else if constexpr (F == MXFP4 || F == NVFP4 || F == MXFP4X2) {
+  if constexpr (F == MXFP4 || F == NVFP4 || F == MXFP4X2) {
     e2m1x8_f16(word(v, q), r);
-  } else if constexpr (is_i4<F>()) {
+  } else if constexpr (is_i4<F>() || F == MXINT4) {
     const uint32_t w = i4_u<F>(word(v, q));
     #pragma unroll
     for (int b = 0; b < 4; ++b) r[b] = ((w >> (4 * b)) & 0x000F000Fu) | 0x64006400u;
@@ -159,7 +157,7 @@ __host__ __device__ constexpr int xstride(int K) {
 
 inline size_t smem_bytes(int F, int M, int K, int warps = WARPS) {
   const int spans = K / 32;
-  return size_t(M) * xstride(K) * 2 + 64 + size_t(M) * spans * 4 * (fmt_is_i4(F) ? 2 : 1) +
+  return size_t(M) * xstride(K) * 2 + 64 + size_t(M) * spans * 4 * ((fmt_is_i4(F) || F == MXINT4) ? 2 : 1) +
          size_t(warps) * 2 * 16 * 4 + size_t(warps) * 2 * 4;
 }
 
@@ -207,7 +205,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   using S = Shape<F>;
   constexpr int P = chunks_per_warp<F, W>();
   constexpr int WARPS = W, THREADS = 32 * W;
-  constexpr bool FOUR = S::four, I4 = is_i4<F>();
+  constexpr bool FOUR = S::four, I4 = is_i4<F>() || F == MXINT4;   // int4 pairing, span sums of x
   constexpr bool X2 = F == MXFP4X2;                                         // output row = rows 2r + 2r + 1
   constexpr int CODES = S::CODES, LANE = S::LANE;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -555,6 +553,17 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
           q2 = e8m0_f32((w4 >> 16) & 0xFFu); q3 = e8m0_f32(w4 >> 24);
         } else {
           q0 = e8m0_fast<0>(w4); q1 = e8m0_fast<1>(w4); q2 = e8m0_fast<2>(w4); q3 = e8m0_fast<3>(w4);
+        }
+        if constexpr (F == MXINT4) {
+          // D = sum_k x~ (1024 + u) with u = q + 8: the span's sum is D - 1032 sum(x~);
+          // a span past K (a chunk slot past the warp's share, or the second span
+          // of the last chunk) has zero activations, so D = 0, and no sum either
+          const float m0 = k0 < K ? xsum[md * spans + s0] : 0.0f;
+          const float m1 = k0 + LANE < K ? xsum[md * spans + s1] : 0.0f;
+          d[ii][0] = __fmaf_rn(-1032.0f, m0, d[ii][0]);
+          d[ii][1] = __fmaf_rn(-1032.0f, m1, d[ii][1]);
+          d[ii][2] = __fmaf_rn(-1032.0f, m0, d[ii][2]);
+          d[ii][3] = __fmaf_rn(-1032.0f, m1, d[ii][3]);
         }
         acc_a = __fmaf_rn(__fmul_rn(q0, x0s), d[ii][0], acc_a);
         acc_a = __fmaf_rn(__fmul_rn(q1, x1s), d[ii][1], acc_a);

@@ -57,6 +57,11 @@ Readings taken where the pages are silent (each is listed in the design doc):
   way with s1 = amax(r) / 6 (1.0 for an all-zero residual).  Block 32 (the MX
   block).  Layout: codes [N, 2, K/2] (a row's plane-0 nibbles, then its
   plane-1 nibbles), scales [N, 2, K/32] float32 (s0 of every block, then s1).
+* fp4 / fp8_e4m3 / fp8_e5m2 (PR #250's legacy float formats: the E2M1 /
+  E4M3 / E5M2 element under a float32 scale per group of 32, "the existing F32
+  per-group scale path") and their fp16-scale twins *_f16: s = amax /
+  max_finite(element) in float32 (1.0 for an all-zero group), stored raw or
+  rounded once to an IEEE half (as nvfp8_f16); codes as step 4.
 * int4 affine (MLX style, group 64): s = (max - min) / 15 (1.0 when 0), stored
   as bf16 (RNE); bias = bf16(min); q = clamp(round_half_away((w - b) / s), 0, 15);
   scale and bias are interleaved per group as bf16 pairs [N, ceil(K/64), 2].
@@ -73,24 +78,31 @@ import numpy as np
 from . import codec
 
 FORMATS = ("mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8", "int4_affine", "nvfp8_f16", "mxint8",
-           "int8", "int8_f16", "int4", "int4_f16", "mxfp4x2", "mxint4")
+           "int8", "int8_f16", "int4", "int4_f16", "mxfp4x2", "mxint4",
+           "fp4", "fp4_f16", "fp8_e4m3", "fp8_e4m3_f16", "fp8_e5m2", "fp8_e5m2_f16")
 RAGGED = ("int4_affine", "int8", "int8_f16", "int4", "int4_f16")   # block 64: K may end in a group of 32
 SYM_INT = ("int8", "int8_f16", "int4", "int4_f16")                 # symmetric integers, float scale per 64
 
 BLOCK = {"mxfp4": 32, "nvfp4": 16, "mxfp8_e4m3": 32, "mxfp8_e5m2": 32, "nvfp8": 16, "int4_affine": 64,
          "nvfp8_f16": 16, "mxint8": 32, "int8": 64, "int8_f16": 64, "int4": 64, "int4_f16": 64, "mxfp4x2": 32,
-         "mxint4": 32}
+         "mxint4": 32, "fp4": 32, "fp4_f16": 32, "fp8_e4m3": 32, "fp8_e4m3_f16": 32, "fp8_e5m2": 32,
+         "fp8_e5m2_f16": 32}
 ELEM_BITS = {"mxfp4": 4, "nvfp4": 4, "mxfp8_e4m3": 8, "mxfp8_e5m2": 8, "nvfp8": 8, "int4_affine": 4, "nvfp8_f16": 8,
              "mxint8": 8, "int8": 8, "int8_f16": 8, "int4": 4, "int4_f16": 4,
-             "mxfp4x2": 8, "mxint4": 4}                      # bits per weight (mxfp4x2: two nibbles)
+             "mxfp4x2": 8, "mxint4": 4,                      # bits per weight (mxfp4x2: two nibbles)
+             "fp4": 4, "fp4_f16": 4, "fp8_e4m3": 8, "fp8_e4m3_f16": 8, "fp8_e5m2": 8, "fp8_e5m2_f16": 8}
 SCALE_BYTES = {"mxfp4": 1, "nvfp4": 1, "mxfp8_e4m3": 1, "mxfp8_e5m2": 1, "nvfp8": 4, "int4_affine": 4,
                "nvfp8_f16": 2, "mxint8": 1, "int8": 4, "int8_f16": 2, "int4": 4, "int4_f16": 2,
-               "mxfp4x2": 8, "mxint4": 1}                    # bytes per block (mxfp4x2: s0 and s1)
+               "mxfp4x2": 8, "mxint4": 1,                    # bytes per block (mxfp4x2: s0 and s1)
+               "fp4": 4, "fp4_f16": 2, "fp8_e4m3": 4, "fp8_e4m3_f16": 2, "fp8_e5m2": 4, "fp8_e5m2_f16": 2}
 _ELEM = {"mxfp4": ("e2m1", codec.E2M1_MAX), "nvfp4": ("e2m1", codec.E2M1_MAX),
          "mxfp8_e4m3": ("e4m3", codec.E4M3_MAX), "mxfp8_e5m2": ("e5m2", codec.E5M2_MAX),
          "nvfp8": ("e4m3", codec.E4M3_MAX), "nvfp8_f16": ("e4m3", codec.E4M3_MAX), "mxint8": ("int8", 127.0),
          "int8": ("int8", 127.0), "int8_f16": ("int8", 127.0), "int4": ("int4", 7.0), "int4_f16": ("int4", 7.0),
-         "mxint4": ("int4", 7.0)}
+         "mxint4": ("int4", 7.0),
+         "fp4": ("e2m1", codec.E2M1_MAX), "fp4_f16": ("e2m1", codec.E2M1_MAX),
+         "fp8_e4m3": ("e4m3", codec.E4M3_MAX), "fp8_e4m3_f16": ("e4m3", codec.E4M3_MAX),
+         "fp8_e5m2": ("e5m2", codec.E5M2_MAX), "fp8_e5m2_f16": ("e5m2", codec.E5M2_MAX)}
 
 F32 = np.float32
 
@@ -173,7 +185,7 @@ def pack(fmt: str, w: np.ndarray):
         ucode = np.where(amax > 0, ucode, np.uint8(0x38)).astype(np.uint8)
         eff = (codec.E4M3_TABLE[ucode].astype(F32) * glob).astype(F32)
         scales = ucode
-    elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):
+    elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16", "fp4_f16", "fp8_e4m3_f16", "fp8_e5m2_f16"):
         # the fp16-scale twin: amax / 448 rounded once to an IEEE half (nearest
         # even, subnormals kept, overflow to inf, rejected below)
         s = np.where(amax > 0, amax / F32(maxf), F32(1.0)).astype(F32)
@@ -181,7 +193,7 @@ def pack(fmt: str, w: np.ndarray):
             h = s.astype(np.float16)
         eff = h.astype(F32)
         scales = h
-    else:  # nvfp8: float32 scale stored raw
+    else:  # nvfp8 and the legacy float formats: float32 scale stored raw
         s = np.where(amax > 0, amax / F32(maxf), F32(1.0)).astype(F32)
         eff = s
         scales = s

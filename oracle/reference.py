@@ -30,6 +30,9 @@ Value definitions (page title, then the section):
   under their float32 block scales -- rlx-cpu ``dequant_matmul_mxfp4x2``
   (codes [N, 2, K/2], scales [N, 2, K/32]; each product is exact in float64,
   their sum is rounded once in float64, then once to float32 by dequant_f32).
+* fp4 / fp8_e4m3 / fp8_e5m2 and their *_f16 twins: w = elem(code) * scale,
+  a float32 (IEEE half) scale per 32 -- PR #250, the legacy float formats
+  on the FP32 per-group scale path and the fp16-scale axis.
 * int4 affine: w = scale * q + bias with q the LSB-first nibble, group 64 --
   metaltile-std ``tests/qmm_gpu_correctness.rs``, ``cpu_qmm_reference``;
   scale and bias are bf16.  float64 evaluation of s*q + b is exact or, when
@@ -85,20 +88,20 @@ def block_scales(fmt: str, scales: np.ndarray, global_scale: float, n: int, k: i
         return codec.E8M0_TABLE[s.reshape(n, nb)], None
     if fmt == "nvfp4":
         return codec.E4M3_TABLE[s.reshape(n, nb)], None
-    if fmt in ("nvfp8", "int8", "int4"):
+    if fmt in ("nvfp8", "int8", "int4", "fp4", "fp8_e4m3", "fp8_e5m2"):
         return np.ascontiguousarray(s).view(np.float32).reshape(n, nb).astype(np.float64), None
-    if fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):
+    if fmt in ("nvfp8_f16", "int8_f16", "int4_f16", "fp4_f16", "fp8_e4m3_f16", "fp8_e5m2_f16"):
         return np.ascontiguousarray(s).view(np.float16).reshape(n, nb).astype(np.float64), None
     pair = np.ascontiguousarray(s).view(np.uint16).reshape(n, nb, 2)
     return codec.decode_bf16(pair[..., 0]), codec.decode_bf16(pair[..., 1])
 
 
 def element_values(fmt: str, codes: np.ndarray) -> np.ndarray:
-    if fmt in ("mxfp4", "nvfp4"):
+    if fmt in ("mxfp4", "nvfp4", "fp4", "fp4_f16"):
         return codec.E2M1_TABLE[codes]
-    if fmt in ("mxfp8_e4m3", "nvfp8", "nvfp8_f16"):
+    if fmt in ("mxfp8_e4m3", "nvfp8", "nvfp8_f16", "fp8_e4m3", "fp8_e4m3_f16"):
         return codec.E4M3_TABLE[codes]
-    if fmt == "mxfp8_e5m2":
+    if fmt in ("mxfp8_e5m2", "fp8_e5m2", "fp8_e5m2_f16"):
         return codec.E5M2_TABLE[codes]
     if fmt in ("mxint8", "int8", "int8_f16"):            # the two's-complement byte
         return codes.astype(np.uint8).view(np.int8).astype(np.float64)

@@ -15,15 +15,15 @@ MX = ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2")          # float elements under E8M0 
 
 def _elem_values_lib(fmt, codes_nk):
     """Element values from library reinterpretations (not the oracle's tables)."""
-    if fmt in ("mxfp4", "nvfp4"):
+    if fmt in ("mxfp4", "nvfp4", "fp4", "fp4_f16"):
         c = codes_nk.astype(np.int64)
         c3 = c & 7
         e, m = c3 >> 1, c3 & 1
         two_m = np.where(e == 0, m, (m + 2) * (2 ** np.maximum(e - 1, 0)))
         return (1 - 2 * (c >> 3)) * two_m / 2.0
-    if fmt in ("mxfp8_e4m3", "nvfp8", "nvfp8_f16"):
+    if fmt in ("mxfp8_e4m3", "nvfp8", "nvfp8_f16", "fp8_e4m3", "fp8_e4m3_f16"):
         return torch.from_numpy(codes_nk.astype(np.uint8)).view(torch.float8_e4m3fn).double().numpy()
-    if fmt == "mxfp8_e5m2":
+    if fmt in ("mxfp8_e5m2", "fp8_e5m2", "fp8_e5m2_f16"):
         return (codes_nk.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
     if fmt in ("mxint8", "int8", "int8_f16"):
         return torch.from_numpy(codes_nk.astype(np.uint8)).view(torch.int8).double().numpy()
@@ -39,10 +39,11 @@ def test_byte_sizes():
     w = synth.weights(n, k, seed=5)
     for fmt in FMTS:
         c, s, g = pack.pack(fmt, w)
-        bits = 4 if fmt in ("mxfp4", "nvfp4", "int4_affine", "int4", "int4_f16", "mxint4") else 8
+        bits = pack.ELEM_BITS[fmt]
         assert c.nbytes == n * k * bits // 8 == pack.codes_nbytes(fmt, n, k)
         per_scale = {"nvfp8": 4, "int4_affine": 4, "nvfp8_f16": 2, "int8": 4, "int8_f16": 2, "int4": 4,
-                     "int4_f16": 2, "mxfp4x2": 8}.get(fmt, 1)
+                     "int4_f16": 2, "mxfp4x2": 8, "fp4": 4, "fp4_f16": 2, "fp8_e4m3": 4, "fp8_e4m3_f16": 2,
+                     "fp8_e5m2": 4, "fp8_e5m2_f16": 2}.get(fmt, 1)
         assert s.nbytes == n * (k // pack.BLOCK[fmt]) * per_scale == pack.scales_nbytes(fmt, n, k)
         assert c.dtype == np.uint8 and s.dtype == np.uint8 and isinstance(g, np.float32)
 
@@ -71,9 +72,9 @@ def test_zero_blocks():
             assert (s == 127).all()
         elif fmt == "nvfp4":
             assert (s == 0x38).all() and g == 1.0
-        elif fmt in ("nvfp8", "int8", "int4", "mxfp4x2"):
+        elif fmt in ("nvfp8", "int8", "int4", "mxfp4x2", "fp4", "fp8_e4m3", "fp8_e5m2"):
             assert (s.view(np.float32) == 1.0).all()
-        elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):
+        elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16", "fp4_f16", "fp8_e4m3_f16", "fp8_e5m2_f16"):
             assert (s.view(np.float16) == 1.0).all()
         else:
             pair = s.view(np.uint16).reshape(n, -1, 2)
@@ -128,7 +129,9 @@ def test_value_idempotence(fmt):
 
 FLOORS = {"mxfp4": 0.98, "nvfp4": 0.98, "int4_affine": 0.99,
           "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999, "nvfp8_f16": 0.999, "mxint8": 0.999,
-          "int8": 0.9999, "int8_f16": 0.9999, "int4": 0.99, "int4_f16": 0.99, "mxfp4x2": 0.9999, "mxint4": 0.98}
+          "int8": 0.9999, "int8_f16": 0.9999, "int4": 0.99, "int4_f16": 0.99, "mxfp4x2": 0.9999, "mxint4": 0.98,
+          "fp4": 0.98, "fp4_f16": 0.98, "fp8_e4m3": 0.999, "fp8_e4m3_f16": 0.999, "fp8_e5m2": 0.995,
+          "fp8_e5m2_f16": 0.995}
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -452,3 +455,42 @@ def test_mxint4_scale_snaps_up_and_rounds_half_away():
     c, s, _ = pack.pack("mxint4", w)
     assert s[0, 0] == 127
     assert list(reference.dequant_exact("mxint4", c, s, 1.0, 1, 32)[0, :4]) == [6, 3, -3, -1]
+
+
+LEGACY = {"fp4": ("e2m1", 6.0), "fp8_e4m3": ("e4m3", 448.0), "fp8_e5m2": ("e5m2", 57344.0)}
+
+
+@pytest.mark.parametrize("fmt", ["fp4", "fp8_e4m3", "fp8_e5m2", "fp4_f16", "fp8_e4m3_f16", "fp8_e5m2_f16"])
+def test_legacy_float_exactly_representable_roundtrip(fmt):
+    # PR #250 legacy float formats: the element under a float scale per 32 with
+    # s = amax / max_finite.  W built as grid values x s with the block maximum
+    # at the element max and s of few significant bits (a half for the twins):
+    # the packer must return exactly those codes and scales.
+    rng = np.random.default_rng(61)
+    base = fmt.replace("_f16", "")
+    elem, maxf = LEGACY[base]
+    table = {"e2m1": codec.E2M1_TABLE, "e4m3": codec.E4M3_TABLE, "e5m2": codec.E5M2_TABLE}[elem]
+    ncode = 16 if elem == "e2m1" else 256
+    finite = np.array([c for c in range(ncode) if np.isfinite(table[c])])
+    maxcode = int(finite[np.argmax(table[finite])])
+    n, k = 4, 128
+    codes = rng.choice(finite, size=(n, k))
+    codes[:, ::32] = maxcode
+    m = rng.integers(512, 1024, size=(n, k // 32)).astype(np.float64)
+    s = m * 2.0 ** rng.integers(-24, -12, size=(n, k // 32))      # 10 significant bits: a normal half
+    vals = _elem_values_lib(base if base != "fp4" else "mxfp4", codes).reshape(n, k // 32, 32) * s[..., None]
+    w = vals.reshape(n, k).astype(np.float32)
+    assert np.array_equal(w.astype(np.float64), vals.reshape(n, k))
+    c, sc, g = pack.pack(fmt, w)
+    got_s = sc.view(np.float16 if fmt.endswith("_f16") else np.float32).reshape(n, -1).astype(np.float64)
+    assert np.array_equal(got_s, s)
+    assert np.array_equal(reference.dequant_exact(fmt, c, sc, g, n, k), w.astype(np.float64))
+
+
+def test_legacy_float_scale_is_not_snapped():
+    # unlike the MX formats, the scale is amax / max_finite itself (no power of two)
+    w = np.zeros((1, 32), np.float32)
+    w[0, 0] = 5.0                                    # fp4: s = 5/6, not 1
+    c, s, _ = pack.pack("fp4", w)
+    assert s.view(np.float32)[0] == np.float32(5.0) / np.float32(6.0)
+    assert reference.dequant_f32("fp4", c, s, 1.0, 1, 32)[0, 0] == np.float32(6.0 * np.float64(s.view(np.float32)[0]))

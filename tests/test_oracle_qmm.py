@@ -29,16 +29,16 @@ FMTS = pack.FORMATS
 # ----- an independent decode: explicit loops + library reinterpretations -----
 
 def _lib_elem(fmt, c):
-    if fmt in ("mxfp4", "nvfp4"):
+    if fmt in ("mxfp4", "nvfp4", "fp4", "fp4_f16"):
         # fp_quantized_mma.rs two_m_int: subnormal 2m = mant, normal 2m = (mant+2) 2^(exp-1)
         c3, s = c & 7, 1 - 2 * (c >> 3)
         e, m = c3 >> 1, c3 & 1
         two_m = m if e == 0 else (m + 2) * 2 ** (e - 1)
         return Fraction(s * two_m, 2)
-    if fmt in ("mxfp8_e4m3", "nvfp8", "nvfp8_f16"):
+    if fmt in ("mxfp8_e4m3", "nvfp8", "nvfp8_f16", "fp8_e4m3", "fp8_e4m3_f16"):
         v = torch.tensor([c], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()
         return Fraction(v)
-    if fmt == "mxfp8_e5m2":
+    if fmt in ("mxfp8_e5m2", "fp8_e5m2", "fp8_e5m2_f16"):
         return Fraction(float(np.array([c << 8], np.uint16).view(np.float16)[0]))
     if fmt in ("mxint8", "int8", "int8_f16"):
         return Fraction(c - 256 if c >= 128 else c)
@@ -53,9 +53,9 @@ def _lib_scale(fmt, sbytes, n, b):
     if fmt == "nvfp4":
         v = torch.tensor([int(sbytes[n][b])], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()
         return Fraction(v), Fraction(0)
-    if fmt in ("nvfp8", "int8", "int4"):
+    if fmt in ("nvfp8", "int8", "int4", "fp4", "fp8_e4m3", "fp8_e5m2"):
         return Fraction(float(np.frombuffer(bytes(sbytes[n][4 * b:4 * b + 4]), "<f4")[0])), Fraction(0)
-    if fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):
+    if fmt in ("nvfp8_f16", "int8_f16", "int4_f16", "fp4_f16", "fp8_e4m3_f16", "fp8_e5m2_f16"):
         return Fraction(float(np.frombuffer(bytes(sbytes[n][2 * b:2 * b + 2]), "<f2")[0])), Fraction(0)
     raw = bytes(sbytes[n][4 * b:4 * b + 4])
     s_bits, b_bits = np.frombuffer(raw, "<u2")

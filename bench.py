@@ -14,7 +14,8 @@ prefill GEMM (M = 2048, N = K = 4096) and the int4-affine / mxfp8 E5M2 /
 nvfp8 sweep (M = 1, 16, 128, 4096; N = 11008, K = 4096), mxint8, int8 and
 int4 at M = 1 and 4096 and the fp16-scale int8 / int4 twins at M = 1 on the
 same N, K, the two-level residual mxfp4x2 and mxint4 at M = 1 and 2048
-(N = K = 4096) -- GEMV rows in GB/s,
+(N = K = 4096), the legacy float fp4 (M = 1), fp8 E5M2 (M = 1, N = 11008) and
+fp8 E4M3 (M = 2048) -- GEMV rows in GB/s,
 GEMM rows in TFLOP/s, each against its roofline.
 
 ``--impl reference`` times the CPU oracle (numpy decode -> float64 W ->
@@ -385,8 +386,8 @@ def run_reference(args):
 # kernel reports null until it is captured again).
 TRAFFIC = {
     "kernel_source": "block_scaled_quantized_spec_gb300/csrc/qgemv_m2.cuh",
-    "sha256_16": "57558de3ff7d0013",
-    "bytes": 8940544,
+    "sha256_16": "fe53a41e513a5704",
+    "bytes": 8940288,
     "profile": "profiles/qgemv_m2_mxfp4_M1_N4096_K4096.md",
 }
 
@@ -426,6 +427,7 @@ BREAKDOWN = [
     ("int8_f16", 1, 11008, 4096), ("int4_f16", 1, 11008, 4096),
     ("mxfp4x2", 1, 4096, 4096), ("mxfp4x2", 2048, 4096, 4096),
     ("mxint4", 1, 4096, 4096), ("mxint4", 2048, 4096, 4096),
+    ("fp4", 1, 4096, 4096), ("fp8_e5m2", 1, 11008, 4096), ("fp8_e4m3", 2048, 4096, 4096),
 ]
 
 
@@ -564,7 +566,7 @@ def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3):
         # the format's own tensor rate (fp8 2x, fp4 6x bf16); int8 elements against bf16 (this part's int8 rate is lower)
         fp_peak = {"mxfp8_e4m3": 2 * bf16, "mxfp8_e5m2": 2 * bf16, "nvfp8": 2 * bf16, "nvfp8_f16": 2 * bf16,
                    "mxint8": bf16, "int8": bf16, "int8_f16": bf16, "int4": bf16, "int4_f16": bf16,
-                   "mxfp4x2": bf16, "mxint4": bf16}.get(fmt, 6 * bf16)
+                   "mxfp4x2": bf16, "mxint4": bf16, "fp8_e4m3": 2 * bf16, "fp8_e5m2": 2 * bf16}.get(fmt, 6 * bf16)
         row["bf16_frac"] = round(tfl / bf16, 4)
         row["native_peak_frac"] = round(tfl / fp_peak, 4)
         # against the roofline at this arithmetic intensity: min(bf16 peak, FLOP/byte x HBM)

@@ -26,7 +26,8 @@ __all__ = [
 
 FORMATS = {"mxfp4": 1, "nvfp4": 2, "mxfp8_e4m3": 3, "mxfp8_e5m2": 4, "nvfp8": 5, "int4_affine": 6,
            "nvfp8_f16": 7, "mxint8": 8, "int8": 9, "int8_f16": 10,
-           "int4": 11, "int4_f16": 12, "mxfp4x2": 13, "mxint4": 14}
+           "int4": 11, "int4_f16": 12, "mxfp4x2": 13, "mxint4": 14,
+           "fp4": 15, "fp4_f16": 16, "fp8_e4m3": 17, "fp8_e4m3_f16": 18, "fp8_e5m2": 19, "fp8_e5m2_f16": 20}
 F32, BF16 = 0, 1
 STATUS = {0: "QFMT_OK", -1: "QFMT_EINVAL", -2: "QFMT_ESHAPE", -3: "QFMT_EALIGN", -4: "QFMT_EUNSUPPORTED",
           -5: "QFMT_ECUDA", -6: "QFMT_ETIMEOUT", -7: "QFMT_ENONFINITE", -8: "QFMT_ENOSPACE", -9: "QFMT_EINDEX"}

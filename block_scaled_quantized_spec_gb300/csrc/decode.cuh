@@ -24,7 +24,8 @@ namespace qfmt_dev {
 
 enum Fmt {
   MXFP4 = 1, NVFP4 = 2, MXFP8_E4M3 = 3, MXFP8_E5M2 = 4, NVFP8 = 5, INT4_AFFINE = 6, NVFP8_F16 = 7, MXINT8 = 8,
-  INT8 = 9, INT8_F16 = 10, INT4 = 11, INT4_F16 = 12, MXFP4X2 = 13, MXINT4 = 14
+  INT8 = 9, INT8_F16 = 10, INT4 = 11, INT4_F16 = 12, MXFP4X2 = 13, MXINT4 = 14,
+  FP4 = 15, FP4_F16 = 16, FP8_E4M3 = 17, FP8_E4M3_F16 = 18, FP8_E5M2 = 19, FP8_E5M2_F16 = 20
 };
 
 template <int F> struct FmtTraits;
@@ -45,6 +46,14 @@ template <> struct FmtTraits<INT4_F16> { static constexpr bool four = true; stat
 // 32; an output is the sum of its two rows' products.
 template <> struct FmtTraits<MXFP4X2> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 4; };
 template <> struct FmtTraits<MXINT4> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 1; };
+// the legacy float formats: an E2M1 / E4M3 / E5M2 element under a float32 (or
+// IEEE half) scale per 32
+template <> struct FmtTraits<FP4> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 4; };
+template <> struct FmtTraits<FP4_F16> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 2; };
+template <> struct FmtTraits<FP8_E4M3> { static constexpr bool four = false; static constexpr int block = 32; static constexpr int sbytes = 4; };
+template <> struct FmtTraits<FP8_E4M3_F16> { static constexpr bool four = false; static constexpr int block = 32; static constexpr int sbytes = 2; };
+template <> struct FmtTraits<FP8_E5M2> { static constexpr bool four = false; static constexpr int block = 32; static constexpr int sbytes = 4; };
+template <> struct FmtTraits<FP8_E5M2_F16> { static constexpr bool four = false; static constexpr int block = 32; static constexpr int sbytes = 2; };
 
 // 8-bit elements under an E8M0 scale per 32 (mxfp8 E4M3/E5M2, mxint8), and
 // every E8M0-scaled format (those and mxfp4)
@@ -59,7 +68,19 @@ constexpr bool is_e8m0() { return is_mx4<F>() || is_mx8<F>(); }
 // 8-bit elements under a float block scale (float32 or IEEE half): nvfp8 and
 // its twin (E4M3, per 16), symmetric int8 and its twin (per 64)
 template <int F>
-constexpr bool is_fs8() { return F == NVFP8 || F == NVFP8_F16 || F == INT8 || F == INT8_F16; }
+constexpr bool is_fs8() {
+  return F == NVFP8 || F == NVFP8_F16 || F == INT8 || F == INT8_F16 || F == FP8_E4M3 || F == FP8_E4M3_F16 ||
+         F == FP8_E5M2 || F == FP8_E5M2_F16;
+}
+
+// E5M2 elements (under any scale)
+template <int F>
+constexpr bool is_e5m2() { return F == MXFP8_E5M2 || F == FP8_E5M2 || F == FP8_E5M2_F16; }
+
+// E2M1 elements under a float scale per 32: the legacy fp4 (float32 or half
+// scale) and the residual planes of mxfp4x2
+template <int F>
+constexpr bool is_fp4f() { return F == FP4 || F == FP4_F16 || F == MXFP4X2; }
 
 // signed-int8 elements (under an E8M0 or a float scale)
 template <int F>
@@ -74,7 +95,7 @@ template <int F>
 constexpr bool is_i4sym() { return F == INT4 || F == INT4_F16; }
 inline constexpr bool fmt_is_i4(int f) { return f == INT4_AFFINE || f == INT4 || f == INT4_F16; }
 inline constexpr bool fmt_is_four(int f) {
-  return f == MXFP4 || f == NVFP4 || f == MXFP4X2 || f == MXINT4 || fmt_is_i4(f);
+  return f == MXFP4 || f == NVFP4 || f == MXFP4X2 || f == MXINT4 || f == FP4 || f == FP4_F16 || fmt_is_i4(f);
 }
 
 // Block scale idx of a float-scaled array as float32: the stored float32, or
@@ -287,7 +308,7 @@ __device__ __forceinline__ void elem8x4_f16(uint32_t w, uint32_t* r) {
     const uint32_t a = prmt(t, 0x64u, 0x4140u), b = prmt(t, 0x64u, 0x4342u);
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(a), "r"(0x64806480u));
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[1]) : "r"(b), "r"(0x64806480u));
-  } else if constexpr (F == MXFP8_E5M2) {
+  } else if constexpr (is_e5m2<F>()) {
     asm("{.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
         "cvt.rn.f16x2.e5m2x2 %0, h0;\n\tcvt.rn.f16x2.e5m2x2 %1, h1;}"
         : "=r"(r[0]), "=r"(r[1]) : "r"(w));
@@ -336,7 +357,7 @@ __device__ __forceinline__ PieceScale load_piece_scale(const uint8_t* scales, in
     s.a = __ldg(scales + base + k0 / 32);
   } else if constexpr (F == NVFP4) {
     s.a = __ldg(reinterpret_cast<const unsigned short*>(scales + base + k0 / 16));
-  } else if constexpr (is_fs8<F>() || F == MXFP4X2) {
+  } else if constexpr (is_fs8<F>() || is_fp4f<F>()) {
     s.a = __float_as_uint(float_scale<F>(scales, base + k0 / FmtTraits<F>::block));
   } else {
     s.a = i4_word<F>(scales, base + k0 / 64);
@@ -472,7 +493,7 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
 template <int F>
 __device__ __forceinline__ void decode_piece_hilo(const uint4& v, const PieceScale& ps, uint32_t* hi, uint32_t* lo) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  if constexpr (F == MXFP4X2) {   // one residual plane's 32 E2M1 codes times its float32 block scale
+  if constexpr (is_fp4f<F>()) {   // 32 E2M1 codes (a residual plane of mxfp4x2) times their float block scale
     const float s = __uint_as_float(ps.a);
     #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -491,6 +512,10 @@ __device__ __forceinline__ void decode_piece_hilo(const uint4& v, const PieceSca
         int8x4_bf16(w[j], r);                                                       // exact values
         e02 = r[0];
         e13 = r[1];
+      } else if constexpr (is_e5m2<F>()) {
+        e5m2x4_bf16_raw(w[j], r);
+        e02 = hmul2(r[0], 0x77807780u);                                             // x 2^112: exact values
+        e13 = hmul2(r[1], 0x77807780u);
       } else {
         e4m3x4_bf16_raw(w[j], r);
         e02 = hmul2(r[0], 0x7B807B80u);                                             // x 2^120: exact values

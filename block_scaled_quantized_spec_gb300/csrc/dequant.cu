@@ -22,10 +22,10 @@ namespace qfmt_dev {
 
 template <int F>
 __device__ __forceinline__ float dq_value(uint32_t code, float s, float b, float glob) {
-  if constexpr (F == MXFP4) return __fmul_rn(e2m1_f32(code), s);
+  if constexpr (F == MXFP4 || F == FP4 || F == FP4_F16) return __fmul_rn(e2m1_f32(code), s);
   if constexpr (F == NVFP4) return __fmul_rn(__fmul_rn(e2m1_f32(code), s), glob);   // (e2m1 * e4m3) exact
   if constexpr (F == MXFP8_E4M3) return __fmul_rn(e4m3_f32(code), s);
-  if constexpr (F == MXFP8_E5M2) return __fmul_rn(e5m2_f32(code), s);
+  if constexpr (is_e5m2<F>()) return __fmul_rn(e5m2_f32(code), s);
   if constexpr (is_int8<F>()) return __fmul_rn(float(int8_t(uint8_t(code))), s);
   if constexpr (is_fs8<F>()) return __fmul_rn(e4m3_f32(code), s);
   if constexpr (is_i4sym<F>() || F == MXINT4) return __fmul_rn(float(int(code ^ 8u) - 8), s);   // the sign-extended nibble
@@ -38,7 +38,7 @@ __device__ __forceinline__ void dq_scale(const uint8_t* scales, int64_t idx, flo
   b = 0.0f;
   if constexpr (is_e8m0<F>()) s = e8m0_f32(scales[idx]);
   else if constexpr (F == NVFP4) s = e4m3_f32(scales[idx]);
-  else if constexpr (is_fs8<F>() || is_i4sym<F>()) s = float_scale<F>(scales, idx);
+  else if constexpr (is_fs8<F>() || is_i4sym<F>() || is_fp4f<F>()) s = float_scale<F>(scales, idx);
   else {
     const uint32_t p = reinterpret_cast<const uint32_t*>(scales)[idx];
     s = bf16bits_f32(p & 0xFFFFu);
@@ -151,6 +151,12 @@ cudaError_t launch_dequant(int fmt, const void* codes, const void* scales, float
     case INT4_F16: return launch_dequant_fmt<INT4_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case MXFP4X2: return launch_dequant_fmt<MXFP4X2>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     case MXINT4: return launch_dequant_fmt<MXINT4>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case FP4: return launch_dequant_fmt<FP4>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case FP4_F16: return launch_dequant_fmt<FP4_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case FP8_E4M3: return launch_dequant_fmt<FP8_E4M3>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case FP8_E4M3_F16: return launch_dequant_fmt<FP8_E4M3_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case FP8_E5M2: return launch_dequant_fmt<FP8_E5M2>(codes, scales, glob, out, out_bf16, N, K, st, sms);
+    case FP8_E5M2_F16: return launch_dequant_fmt<FP8_E5M2_F16>(codes, scales, glob, out, out_bf16, N, K, st, sms);
     default: return launch_dequant_fmt<INT4_AFFINE>(codes, scales, glob, out, out_bf16, N, K, st, sms);
   }
 }

@@ -35,12 +35,13 @@ int fail(int status, const char* fmt, ...) {
 
 void clear_error() { g_err[0] = '\0'; }
 
-bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_MXINT4; }
+bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_FP8_E5M2_F16; }
 
 int block_of(int fmt) {
   switch (fmt) {
     case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: case QFMT_MXFP4X2:
-    case QFMT_MXINT4: return 32;
+    case QFMT_MXINT4: case QFMT_FP4: case QFMT_FP4_F16: case QFMT_FP8_E4M3: case QFMT_FP8_E4M3_F16: case QFMT_FP8_E5M2:
+    case QFMT_FP8_E5M2_F16: return 32;
     case QFMT_NVFP4: case QFMT_NVFP8: case QFMT_NVFP8_F16: return 16;
     case QFMT_INT4_AFFINE: case QFMT_INT8: case QFMT_INT8_F16: case QFMT_INT4: case QFMT_INT4_F16: return 64;
     default: return 0;
@@ -49,7 +50,7 @@ int block_of(int fmt) {
 
 bool is_4bit(int fmt) {
   return fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4 || fmt == QFMT_INT4_AFFINE || fmt == QFMT_INT4 || fmt == QFMT_INT4_F16 ||
-         fmt == QFMT_MXINT4;
+         fmt == QFMT_MXINT4 || fmt == QFMT_FP4 || fmt == QFMT_FP4_F16;
 }
 
 bool is_sym_int(int fmt) {
@@ -60,8 +61,8 @@ bool is_sym_int(int fmt) {
 // Largest finite element magnitude: amax / elem_max is the raw block scale.
 float elem_max(int fmt) {
   switch (fmt) {
-    case QFMT_MXFP4: case QFMT_NVFP4: case QFMT_MXFP4X2: return 6.0f;
-    case QFMT_MXFP8_E5M2: return 57344.0f;
+    case QFMT_MXFP4: case QFMT_NVFP4: case QFMT_MXFP4X2: case QFMT_FP4: case QFMT_FP4_F16: return 6.0f;
+    case QFMT_MXFP8_E5M2: case QFMT_FP8_E5M2: case QFMT_FP8_E5M2_F16: return 57344.0f;
     case QFMT_MXINT8: case QFMT_INT8: case QFMT_INT8_F16: return 127.0f;
     case QFMT_INT4: case QFMT_INT4_F16: case QFMT_MXINT4: return 7.0f;
     default: return 448.0f;   // E4M3
@@ -70,8 +71,13 @@ float elem_max(int fmt) {
 
 int scale_entry_bytes(int fmt) {
   if (fmt == QFMT_MXFP4X2) return 8;   // s0 and s1, float32 each (stored as two [nb] runs per row)
-  if (fmt == QFMT_NVFP8 || fmt == QFMT_INT4_AFFINE || fmt == QFMT_INT8 || fmt == QFMT_INT4) return 4;
-  return (fmt == QFMT_NVFP8_F16 || fmt == QFMT_INT8_F16 || fmt == QFMT_INT4_F16) ? 2 : 1;
+  if (fmt == QFMT_NVFP8 || fmt == QFMT_INT4_AFFINE || fmt == QFMT_INT8 || fmt == QFMT_INT4 || fmt == QFMT_FP4 ||
+      fmt == QFMT_FP8_E4M3 || fmt == QFMT_FP8_E5M2)
+    return 4;
+  return (fmt == QFMT_NVFP8_F16 || fmt == QFMT_INT8_F16 || fmt == QFMT_INT4_F16 || fmt == QFMT_FP4_F16 ||
+          fmt == QFMT_FP8_E4M3_F16 || fmt == QFMT_FP8_E5M2_F16)
+             ? 2
+             : 1;
 }
 
 int check_group(int fmt, int group) {
@@ -206,7 +212,7 @@ using namespace qfmt;
 
 extern "C" {
 
-int qfmt_version(void) { return 106; }
+int qfmt_version(void) { return 107; }
 
 const char* qfmt_last_error(void) { return qfmt::g_err; }
 
@@ -332,14 +338,15 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
             eff = dec_e4m3(u) * glob;
             break;
           }
-          case QFMT_NVFP8_F16: case QFMT_INT8_F16: case QFMT_INT4_F16: {  // an IEEE half, rounded to nearest even
+          case QFMT_NVFP8_F16: case QFMT_INT8_F16: case QFMT_INT4_F16: case QFMT_FP4_F16: case QFMT_FP8_E4M3_F16:
+          case QFMT_FP8_E5M2_F16: {  // an IEEE half, rounded to nearest even
             const float s = amax > 0.0f ? amax / elem_max(fmt) : 1.0f;
             const _Float16 h = static_cast<_Float16>(s);
             std::memcpy(sb + (n * nb + b) * 2, &h, 2);
             eff = static_cast<float>(h);
             break;
           }
-          default: {  // QFMT_NVFP8, QFMT_INT8, QFMT_INT4: the float32 scale stored raw
+          default: {  // QFMT_NVFP8, QFMT_INT8, QFMT_INT4 and the legacy float formats: the float32 scale raw
             const float s = amax > 0.0f ? amax / elem_max(fmt) : 1.0f;
             std::memcpy(sb + (n * nb + b) * 4, &s, 4);
             eff = s;
@@ -357,8 +364,9 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
               put_code(crow, b * blk + j, code, four);
               continue;
             }
-            code = fmt == QFMT_MXFP8_E5M2 ? enc_e5m2(v)
-                 : (fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4) ? enc_e2m1(v) : enc_e4m3(v);
+            const bool e5 = fmt == QFMT_MXFP8_E5M2 || fmt == QFMT_FP8_E5M2 || fmt == QFMT_FP8_E5M2_F16;
+            const bool e2 = fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4 || fmt == QFMT_FP4 || fmt == QFMT_FP4_F16;
+            code = e5 ? enc_e5m2(v) : e2 ? enc_e2m1(v) : enc_e4m3(v);
           }
           put_code(crow, b * blk + j, code, four);
         }

@@ -56,7 +56,7 @@ constexpr int B_BYTES = 256 * BK * 2;     // 32 KiB: 256 bf16 rows, or 128 hi ro
 // formats exact in bf16; 8 for nvfp8 and int4 affine, whose hi + lo tiles were
 // measured faster with eight.
 template <int F> struct Dec {
-  static constexpr int WARPS = (is_i4<F>() || is_fs8<F>() || F == MXFP4X2) ? 8 : 16;
+  static constexpr int WARPS = (is_i4<F>() || is_fs8<F>() || is_fp4f<F>()) ? 8 : 16;
   static constexpr int THREADS = WARPS * 32;
   static constexpr int CTA_THREADS = (2 + WARPS) * 32;
 };
@@ -74,7 +74,7 @@ template <int MT> struct Pipe {
 // affine carry each weight as a hi + lo bf16 pair (two MMAs per K slice into
 // one accumulator) on a 128 x 128 tile, so a stage holds the same bytes.
 template <int F> struct Tile {
-  static constexpr bool split = is_fs8<F>() || is_i4<F>() || F == MXFP4X2;
+  static constexpr bool split = is_fs8<F>() || is_i4<F>() || is_fp4f<F>();
   static constexpr int BN = split ? 128 : 256;
 };
 
@@ -710,6 +710,12 @@ cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, floa
     case INT4_F16: return tc::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case MXFP4X2: return tc::launch_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case MXINT4: return tc::launch_fmt<MXINT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP4: return tc::launch_fmt<FP4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP4_F16: return tc::launch_fmt<FP4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP8_E4M3: return tc::launch_fmt<FP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP8_E4M3_F16: return tc::launch_fmt<FP8_E4M3_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP8_E5M2: return tc::launch_fmt<FP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP8_E5M2_F16: return tc::launch_fmt<FP8_E5M2_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return tc::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }

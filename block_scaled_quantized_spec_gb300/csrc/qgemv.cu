@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
           wsc[rr * sst + e] = ok ? e8m0_f32(__ldg(scales + gi)) : 0.0f;
         } else if constexpr (F == NVFP4) {
           wsc[rr * sst + e] = __uint_as_float(ok ? e4m3_f16x2_splat(__ldg(scales + gi)) : 0u);
-        } else if constexpr (is_fs8<F>() || F == MXFP4X2) {
+        } else if constexpr (is_fs8<F>() || is_fp4f<F>()) {
           wsc[rr * sst + e] = ok ? float_scale<F>(scales, gi) : 0.0f;
         } else {
           float sc, bi;
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(THREADS) qgemv_kernel(const uint8_t* __restric
               for (int nb = 0; nb < NB; ++nb) {
                 const int m = min(nb * 8 + g, M - 1);
                 const uint4 xv = *reinterpret_cast<const uint4*>(xs + size_t(m) * xstride + u * 64 + sgm * 32 + 8 * t);
-                if constexpr (is_mx4<F>() || F == MXFP4X2) {   // a block scale per segment
+                if constexpr (is_mx4<F>() || is_fp4f<F>()) {   // a block scale per segment
                   float d[4] = {0.f, 0.f, 0.f, 0.f};
                   mma_f16(d, fa[0], fb[0], fa[1], fb[1], xv.x, xv.y);
                   mma_f16(d, fa[2], fb[2], fa[3], fb[3], xv.z, xv.w);
@@ -553,6 +553,12 @@ cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float g
     case INT4_F16: return gemv::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case MXFP4X2: return gemv::launch_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case MXINT4: return gemv::launch_fmt<MXINT4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP4: return gemv::launch_fmt<FP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP4_F16: return gemv::launch_fmt<FP4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP8_E4M3: return gemv::launch_fmt<FP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP8_E4M3_F16: return gemv::launch_fmt<FP8_E4M3_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP8_E5M2: return gemv::launch_fmt<FP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP8_E5M2_F16: return gemv::launch_fmt<FP8_E5M2_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     default: return gemv::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }

@@ -102,7 +102,7 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int j) {
 // (8q+6, 8q+7); int4 the biased pairs (q_{8q+b}, q_{8q+b+4}), b = 0..3.
 template <int F>
 __device__ __forceinline__ void frags8(const uint4& v, int q, uint32_t r[4]) {
-  if constexpr (F == MXFP4 || F == NVFP4 || F == MXFP4X2) {
+  if constexpr (F == MXFP4 || F == NVFP4 || is_fp4f<F>()) {
     e2m1x8_f16(word(v, q), r);
   } else if constexpr (is_i4<F>() || F == MXINT4) {
     const uint32_t w = i4_u<F>(word(v, q));
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
       const uint32_t x2 = c0 ? __ldg(srb + e) : 127u;
       cs[i].a0 = prmt(x0, x2, 0x1410u) | 0x7F007F00u;                         // bytes 0 and 2 used, 1 and 3 = 127
       cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
-    } else if constexpr (is_fs8<F>() || F == MXFP4X2) {
+    } else if constexpr (is_fs8<F>() || is_fp4f<F>()) {
       constexpr int B = FmtTraits<F>::block;                                  // 16 (nvfp8), 32 (mxfp4x2), 64 (int8)
       const int e = k0 / B;
       cs[i].a0 = c0 ? __float_as_uint(float_scale<F>(sra, e)) : 0u;
@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
         const float ca = __fmul_rn(qa, x0s), cb = __fmul_rn(qb, x0s);
         acc_a = __fmaf_rn(ca, d[ii][0] + d[ii][1], acc_a);
         acc_b = __fmaf_rn(cb, d[ii][2] + d[ii][3], acc_b);
-      } else if constexpr (is_fs8<F>() || F == MXFP4X2) {
+      } else if constexpr (is_fs8<F>() || is_fp4f<F>()) {
         acc_a = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].a0), x0s), d[ii][0], acc_a);
         acc_a = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].a1), x1s), d[ii][1], acc_a);
         acc_b = __fmaf_rn(__fmul_rn(__uint_as_float(cs[i].b0), x0s), d[ii][2], acc_b);
@@ -776,9 +776,9 @@ struct Group {
 };
 
 // The groups, one translation unit each.
-using GroupE2M1 = Group<MXFP4, NVFP4, MXFP4X2, MXINT4>;
+using GroupE2M1 = Group<MXFP4, NVFP4, MXFP4X2, MXINT4, FP4, FP4_F16>;
 using GroupInt = Group<INT4_AFFINE, INT4, INT4_F16, MXINT8, INT8, INT8_F16>;
-using GroupFp8 = Group<MXFP8_E4M3, MXFP8_E5M2, NVFP8, NVFP8_F16>;
+using GroupFp8 = Group<MXFP8_E4M3, MXFP8_E5M2, NVFP8, NVFP8_F16, FP8_E4M3, FP8_E4M3_F16, FP8_E5M2, FP8_E5M2_F16>;
 
 #define QFMT_M2_GROUP_API(G)                                                                                    \
   cudaError_t G##_launch(int fmt, const void* codes, const void* scales, float glob, const void* x, void* out, \

@@ -43,7 +43,7 @@ constexpr size_t X_BUDGET = 40 * 1024;  // staged f16 activations per CTA (five 
 // 64-byte chunks per lane in flight: four; two for nvfp8 and int4 affine,
 // whose per-chunk scales (eight float32, four scale/bias pairs) stay in registers
 template <int F>
-constexpr int chunks_in_flight() { return (is_fs8<F>() || is_i4<F>() || F == MXFP4X2) ? 2 : 4; }
+constexpr int chunks_in_flight() { return (is_fs8<F>() || is_i4<F>() || is_fp4f<F>()) ? 2 : 4; }
 
 template <int F>
 struct Shape {
@@ -163,7 +163,7 @@ inline size_t smem_bytes(int F, int M, int kr) {
 // Raw scale words a lane keeps per chunk: 2 (rows g, g + 8) for the byte
 // scales, 4 for int4 affine (two blocks), 8 for nvfp8 (four float32 blocks).
 template <int F>
-constexpr int scale_words() { return (is_fs8<F>() || F == MXFP4X2) ? 8 : (is_i4<F>() ? 4 : 2); }
+constexpr int scale_words() { return (is_fs8<F>() || is_fp4f<F>()) ? 8 : (is_i4<F>() ? 4 : 2); }
 
 template <int F, int NB, bool UNI>
 __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __restrict__ codes,
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       }
       sc[i][0] = a;
       sc[i][1] = b;
-    } else if constexpr (is_fs8<F>() || F == MXFP4X2) {                     // each segment's block scale
+    } else if constexpr (is_fs8<F>() || is_fp4f<F>()) {                     // each segment's block scale
       #pragma unroll
       for (int sg = 0; sg < 4; ++sg) {
         const int k = kc + sg * SEG;
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
       const int c = r * P + i;
       if (c < nch) {                                                        // uniform over the CTA
         float ac[NB][4], d[NB][4];
-        constexpr bool per_seg = is_mx4<F>() || F == MXFP4X2 || is_fs8<F>();  // a scale per segment
+        constexpr bool per_seg = is_mx4<F>() || is_fp4f<F>() || is_fs8<F>();  // a scale per segment
         constexpr bool per_pair = is_mx8<F>() || I4;  // a block per two segments
         #pragma unroll
         for (int sg = 0; sg < 4; ++sg) {
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             }
           }
           // block scales on the float32 MMA results (d rows g: e = 0, 1; g + 8: e = 2, 3)
-          constexpr bool per_seg = is_mx4<F>() || F == MXFP4X2 || is_fs8<F>();  // a scale per segment
+          constexpr bool per_seg = is_mx4<F>() || is_fp4f<F>() || is_fs8<F>();  // a scale per segment
           constexpr bool per_pair = is_mx8<F>() || I4;  // a block per two segments
           if (per_seg || (per_pair && (sg & 1))) {
             const bool first = sg < (per_seg ? 1 : 2);                      // the chunk's first block
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(THREADS, 5) qgemv_mb_kernel(const uint8_t* __r
             if constexpr (is_mx4<F>()) {
               sa = e8m0_f32((sc[i][0] >> (8 * sg)) & 0xFFu);
               sb = e8m0_f32((sc[i][1] >> (8 * sg)) & 0xFFu);
-            } else if constexpr (is_fs8<F>() || F == MXFP4X2) {
+            } else if constexpr (is_fs8<F>() || is_fp4f<F>()) {
               sa = __uint_as_float(sc[i][sg]);
               sb = __uint_as_float(sc[i][4 + sg]);
             } else if constexpr (I4) {                                      // s * D + (b - 128 s) * sum(x)
@@ -631,6 +631,12 @@ cudaError_t launch_qgemv_mb(int fmt, const void* codes, const void* scales, floa
     case INT4_F16: return gemv_mb::launch_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case MXFP4X2: return gemv_mb::launch_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     case MXINT4: return gemv_mb::launch_fmt<MXINT4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP4: return gemv_mb::launch_fmt<FP4>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP4_F16: return gemv_mb::launch_fmt<FP4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP8_E4M3: return gemv_mb::launch_fmt<FP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP8_E4M3_F16: return gemv_mb::launch_fmt<FP8_E4M3_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP8_E5M2: return gemv_mb::launch_fmt<FP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
+    case FP8_E5M2_F16: return gemv_mb::launch_fmt<FP8_E5M2_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
     default: return gemv_mb::launch_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st, sms);
   }
 }

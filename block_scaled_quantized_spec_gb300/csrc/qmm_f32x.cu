@@ -13,10 +13,10 @@ namespace qfmt_dev {
 
 template <int F>
 __device__ __forceinline__ float exact_weight(uint32_t code, float s, float b) {
-  if constexpr (F == MXFP4 || F == NVFP4) return __fmul_rn(e2m1_f32(code), s);
+  if constexpr (F == MXFP4 || F == NVFP4 || F == FP4 || F == FP4_F16) return __fmul_rn(e2m1_f32(code), s);
   if constexpr (is_int8<F>()) return __fmul_rn(float(int8_t(uint8_t(code))), s);
+  if constexpr (is_e5m2<F>()) return __fmul_rn(e5m2_f32(code), s);
   if constexpr (F == MXFP8_E4M3 || is_fs8<F>()) return __fmul_rn(e4m3_f32(code), s);
-  if constexpr (F == MXFP8_E5M2) return __fmul_rn(e5m2_f32(code), s);
   if constexpr (is_i4sym<F>() || F == MXINT4) return __fmul_rn(float(int(code ^ 8u) - 8), s);
   return __fmaf_rn(s, float(code), b);
 }
@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(256) qmm_f32x_kernel(const uint8_t* __restrict
       float s, b = 0.0f;
       if constexpr (is_e8m0<F>()) s = e8m0_f32(scales[bi]);
       else if constexpr (F == NVFP4) s = e4m3_f32(scales[bi]);
-      else if constexpr (is_fs8<F>() || is_i4sym<F>()) s = float_scale<F>(scales, bi);
+      else if constexpr (is_fs8<F>() || is_i4sym<F>() || is_fp4f<F>()) s = float_scale<F>(scales, bi);
       else {
         const uint32_t p = reinterpret_cast<const uint32_t*>(scales)[bi];
         s = bf16bits_f32(p & 0xFFFFu);
@@ -120,6 +120,12 @@ cudaError_t launch_qmm_f32x(int fmt, const void* codes, const void* scales, floa
     case INT4_F16: return launch_f32x_fmt<INT4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case MXFP4X2: return launch_f32x_fmt<MXFP4X2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     case MXINT4: return launch_f32x_fmt<MXINT4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP4: return launch_f32x_fmt<FP4>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP4_F16: return launch_f32x_fmt<FP4_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP8_E4M3: return launch_f32x_fmt<FP8_E4M3>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP8_E4M3_F16: return launch_f32x_fmt<FP8_E4M3_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP8_E5M2: return launch_f32x_fmt<FP8_E5M2>(codes, scales, glob, x, out, out_f32, m, n, k, st);
+    case FP8_E5M2_F16: return launch_f32x_fmt<FP8_E5M2_F16>(codes, scales, glob, x, out, out_f32, m, n, k, st);
     default: return launch_f32x_fmt<INT4_AFFINE>(codes, scales, glob, x, out, out_f32, m, n, k, st);
   }
 }

@@ -36,6 +36,12 @@
  *                                                 intN, sign-extended from bit 3, +-7)
  *   QFMT_INT4_F16       signed 4-bit q     64     IEEE half (2 bytes): the fp16-scale twin
  *                                                 of QFMT_INT4
+ *   QFMT_FP4            E2M1 (4-bit)       32     FP32 (4 bytes): PR #250's legacy float format,
+ *                                                 s = amax/6 unsnapped
+ *   QFMT_FP8_E4M3       E4M3 (8-bit)       32     FP32 (4 bytes): legacy, s = amax/448
+ *   QFMT_FP8_E5M2       E5M2 (8-bit)       32     FP32 (4 bytes): legacy, s = amax/57344
+ *   QFMT_FP4_F16, QFMT_FP8_E4M3_F16, QFMT_FP8_E5M2_F16: their fp16-scale twins
+ *                                                 (the scale an IEEE half, 2 bytes)
  *   QFMT_MXFP4X2        two E2M1 planes    32     two FP32 (8 bytes): the two-level residual
  *                                                 weight w = s0 e2m1(q0) + s1 e2m1(q1) (rlx-cpu
  *                                                 dequant_matmul_mxfp4x2); level 0 packs w with
@@ -43,7 +49,7 @@
  *                                                 w - s0 e2m1(q0) with s1 = amax(residual)/6
  *
  * Memory layouts (all row-major, no padding, little-endian):
- *   codes   [N, K/2] bytes for 4-bit formats (mxfp4, nvfp4, int4 affine, int4, mxint4): element k of a row sits in byte
+ *   codes   [N, K/2] bytes for 4-bit formats (mxfp4, nvfp4, int4 affine, int4, mxint4, fp4): element k of a row sits in byte
  *           k/2, low nibble for even k (LSB-first; 8 codes per u32 word);
  *           [N, K] bytes for 8-bit formats.
  *   scales  [N, ceil(K/block)] entries of the sizes above; int4 affine stores
@@ -105,7 +111,13 @@ typedef enum {
   QFMT_INT4 = 11,
   QFMT_INT4_F16 = 12,
   QFMT_MXFP4X2 = 13,
-  QFMT_MXINT4 = 14
+  QFMT_MXINT4 = 14,
+  QFMT_FP4 = 15,
+  QFMT_FP4_F16 = 16,
+  QFMT_FP8_E4M3 = 17,
+  QFMT_FP8_E4M3_F16 = 18,
+  QFMT_FP8_E5M2 = 19,
+  QFMT_FP8_E5M2_F16 = 20
 } qfmt_format;
 
 typedef enum { QFMT_F32 = 0, QFMT_BF16 = 1 } qfmt_dtype;

@@ -81,10 +81,10 @@ def test_dequant_all_codes_and_scales(fmt):
     sb = opack.scales_nbytes(fmt, n, k)
     if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4", "nvfp4"):
         scales = np.tile(np.arange(256, dtype=np.uint8), sb // 256 + 1)[:sb]
-    elif fmt in ("nvfp8", "int8", "int4", "mxfp4x2"):
+    elif fmt in ("nvfp8", "int8", "int4", "mxfp4x2", "fp4", "fp8_e4m3", "fp8_e5m2"):
         scales = np.concatenate([rng.standard_normal(sb // 4 - 4).astype(np.float32),
                                  np.array([1e-40, 3e38, 0.0, -2.5], np.float32)]).view(np.uint8)
-    elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16"):   # evenly spaced half bit patterns: subnormals, +-inf, NaNs, both signs
+    elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16", "fp4_f16", "fp8_e4m3_f16", "fp8_e5m2_f16"):   # evenly spaced half bit patterns: subnormals, +-inf, NaNs, both signs
         scales = np.arange(0, 65536, 65536 // (sb // 2), dtype=np.uint16)[:sb // 2].view(np.uint8)
     else:
         sc = synth.f32_to_bf16_bits(rng.standard_normal(sb // 2).astype(np.float32) * 1e-2)
@@ -243,6 +243,9 @@ FULL = [
     ("mxint4", 1, 4096, 4096, False),
     ("mxint4", 8, 4096, 4096, False),
     ("mxint4", 2048, 4096, 4096, False),
+    ("fp4", 1, 4096, 4096, False),
+    ("fp8_e5m2_f16", 16, 11008, 4096, False),
+    ("fp8_e4m3", 2048, 4096, 4096, False),
 ]
 
 

@@ -47,6 +47,10 @@ Value definitions (page title, then the section):
   sqrt(mean(x^2) + eps) -- PR #250, the fused RMSNorm + GEMV commit (phase 1
   the sum of squares and its inverse root, phase 2 the GEMV over
   x * norm_weight * inv_rms).
+* qmm_gated_rmsnorm: the qmm value of x * gamma * silu(gate) / sqrt(mean(x^2)
+  + eps), silu(z) = z sigmoid(z) -- PR #250, the fused gated-RMSNorm + GEMV
+  commit (a silu gate times the per-row inverse RMS times the norm weight,
+  staged, then the block-scaled GEMV over it); the RMS is of x alone.
 * qmm_gather: expert-routed rows over one stacked [E * N, K] weight, row m
   against rows [e N, e N + N) with e = expert_idx[m] -- PR #250, the MoE
   gather-qmm commit (weight row expert_ids[m] * out_dim + n, one stacked
@@ -206,6 +210,28 @@ def rmsnorm_values(x, x_dtype, gamma_bits, eps, m, k):
     g = codec.decode_bf16(np.asarray(gamma_bits, dtype=np.uint16)).reshape(k)
     inv = 1.0 / np.sqrt(np.mean(xv * xv, axis=1) + eps)
     return xv * g[None, :] * inv[:, None]
+
+
+def silu(z):
+    """z * sigmoid(z) = z / (1 + exp(-z)), float64 (0 in the limit z -> -inf)."""
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def gated_rmsnorm_values(x, gate, x_dtype, gamma_bits, eps, m, k):
+    """x * gamma * silu(gate) / sqrt(mean_k x^2 + eps), float64 [M, K]; the root mean square is of x."""
+    z = x_values(gate, x_dtype).reshape(m, k)
+    return rmsnorm_values(x, x_dtype, gamma_bits, eps, m, k) * silu(z)
+
+
+def qmm_gated_rmsnorm_ref(fmt, codes, scales, global_scale, x, gate, x_dtype, gamma_bits, eps, m, n, k):
+    """(ref, bound) for out = gated_rmsnorm(x, gate) . dequant(W)^T, bound on the gated activation."""
+    w = dequant_exact(fmt, codes, scales, global_scale, n, k)
+    xt = gated_rmsnorm_values(x, gate, x_dtype, gamma_bits, eps, m, k)
+    ref = xt @ w.T
+    bound = BOUND_REL * (np.abs(xt) @ np.abs(w).T) + BOUND_ABS
+    return ref, bound
 
 
 def qmm_rmsnorm_ref(fmt, codes, scales, global_scale, x, x_dtype, gamma_bits, eps, m, n, k):

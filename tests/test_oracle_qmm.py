@@ -454,6 +454,52 @@ def test_planted_rmsnorm_mistake_is_caught(monkeypatch):
             test_rmsnorm_ref_matches_decimal_brute_force("mxfp4")
 
 
+# ----- the gated RMSNorm (PR #250 fused gated-RMSNorm + GEMV) -----
+
+def _bf16(a):
+    return synth.f32_to_bf16_bits(np.asarray(a, dtype=np.float32))
+
+
+def test_gated_rmsnorm_zero_gate_gives_zero():
+    # silu(0) = 0: every gated value vanishes
+    m, k = 2, 64
+    x = synth.activations_bf16(m, k, seed=71)
+    v = reference.gated_rmsnorm_values(x, _bf16(np.zeros((m, k))), "bf16", _gamma_bits(k, 72), 1e-5, m, k)
+    assert not v.any()
+
+
+def test_gated_rmsnorm_large_gate_is_the_gate_times_rmsnorm():
+    # silu(z) = z / (1 + e^-z) equals z in float64 for z = 64 (e^-64 < 2^-53 relative):
+    # the gated values are 64 x the plain (separately pinned) RMSNorm values
+    m, k = 2, 128
+    x = synth.activations_bf16(m, k, seed=73)
+    gb = _gamma_bits(k, 74)
+    v = reference.gated_rmsnorm_values(x, _bf16(np.full((m, k), 64.0)), "bf16", gb, 1e-5, m, k)
+    assert np.array_equal(v, 64.0 * reference.rmsnorm_values(x, "bf16", gb, 1e-5, m, k))
+
+
+def test_gated_rmsnorm_odd_part_of_the_gate_is_linear():
+    # silu(z) - silu(-z) = z (sigmoid(z) + sigmoid(-z) = 1): a wrong activation
+    # (sigmoid alone, z (1 - sigmoid), a sign slip) breaks this identity
+    m, k = 2, 256
+    x = synth.activations_bf16(m, k, seed=75)
+    z = synth.activations_bf16(m, k, seed=76)
+    zneg = z ^ np.uint16(0x8000)
+    gb = _gamma_bits(k, 77)
+    a = reference.gated_rmsnorm_values(x, z, "bf16", gb, 1e-3, m, k)
+    b = reference.gated_rmsnorm_values(x, zneg, "bf16", gb, 1e-3, m, k)
+    zv = reference.x_values(z, "bf16").reshape(m, k)
+    want = zv * reference.rmsnorm_values(x, "bf16", gb, 1e-3, m, k)
+    assert np.allclose(a - b, want, rtol=1e-12, atol=1e-15)
+
+
+def test_gated_rmsnorm_large_negative_gate_vanishes():
+    m, k = 1, 32
+    x = synth.activations_bf16(m, k, seed=78)
+    v = reference.gated_rmsnorm_values(x, _bf16(np.full((m, k), -1000.0)), "bf16", _gamma_bits(k, 79), 0.0, m, k)
+    assert np.all(np.abs(v) < 1e-300)
+
+
 # ----- int4 affine with a ragged last group (K a multiple of 32, not of 64) -----
 
 @pytest.mark.parametrize("k", [32, 96, 160])

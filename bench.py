@@ -46,7 +46,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-breakdown", action="store_true")
-    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K, gather:fmt:M:N:K:E, batched:fmt:M:N1,N2:K or rmsnorm:fmt:M:N:K")
+    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K, gather:fmt:M:N:K:E, batched:fmt:M:N1,N2:K, rmsnorm:fmt:M:N:K "
+                   "or gated_rmsnorm:fmt:M:N:K")
     return p.parse_args()
 
 
@@ -386,7 +387,7 @@ def run_reference(args):
 # kernel reports null until it is captured again).
 TRAFFIC = {
     "kernel_source": "block_scaled_quantized_spec_gb300/csrc/qgemv_m2.cuh",
-    "sha256_16": "fe53a41e513a5704",
+    "sha256_16": "0ea978bf1488616d",
     "bytes": 8940288,
     "profile": "profiles/qgemv_m2_mxfp4_M1_N4096_K4096.md",
 }
@@ -471,7 +472,8 @@ class GatherProblem:
 
 # Fused decode forms: the Q/K/V projections of a grouped-query layer in one
 # launch, and RMSNorm in front of one mxfp4 [4096, 4096] GEMV.
-FUSED = [("batched", "mxfp4", 1, (4096, 1024, 1024), 4096), ("rmsnorm", "mxfp4", 1, (4096,), 4096)]
+FUSED = [("batched", "mxfp4", 1, (4096, 1024, 1024), 4096), ("rmsnorm", "mxfp4", 1, (4096,), 4096),
+         ("gated_rmsnorm", "mxfp4", 1, (4096,), 4096)]
 
 
 class FusedProblem:
@@ -491,9 +493,12 @@ class FusedProblem:
         xb = synth.activations_bf16(m, k, rng=rng)
         self.x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
         self.gamma = (1.0 + 0.1 * torch.randn(k, generator=torch.Generator().manual_seed(seed))).to(torch.bfloat16).cuda()
+        zb = synth.activations_bf16(m, k, rng=rng)                        # the gate (gated_rmsnorm)
+        self.gate = torch.from_numpy(zb.view(np.int16)).view(torch.bfloat16).cuda()
         self.outs = [[torch.empty((m, n), dtype=torch.bfloat16, device="cuda") for n in ns] for _ in range(copies)]
         self.copies = copies
-        self.bytes = sum(sizes(fmt, m, n, k) - 2 * m * k for n in ns) + 2 * m * k + (2 * k if kind == "rmsnorm" else 0)
+        self.bytes = (sum(sizes(fmt, m, n, k) - 2 * m * k for n in ns) + 2 * m * k
+                      + (2 * k if kind in ("rmsnorm", "gated_rmsnorm") else 0) + (2 * m * k if kind == "gated_rmsnorm" else 0))
 
     def step(self, separate=False):
         import block_scaled_quantized_spec_gb300 as q
@@ -501,6 +506,9 @@ class FusedProblem:
             w, o = self.w[i], self.outs[i]
             if self.kind == "rmsnorm":
                 q.qmm_rmsnorm(self.fmt, w[0][0], w[0][1], self.g[0], self.x, self.gamma, 1e-5, self.ns[0], out=o[0])
+            elif self.kind == "gated_rmsnorm":
+                q.qmm_gated_rmsnorm(self.fmt, w[0][0], w[0][1], self.g[0], self.x, self.gate, self.gamma, 1e-5,
+                                    self.ns[0], out=o[0])
             elif separate:
                 for j, n in enumerate(self.ns):
                     q.qmm(self.fmt, w[j][0], w[j][1], self.g[j], self.x, n, out=o[j])
@@ -599,7 +607,7 @@ def main():
             f, mm, nn, kk, ee = parts[1:]
             print(json.dumps(gather_row(f, int(mm), int(nn), int(kk), int(ee), hbm, args.steps, args.warmup)))
             return
-        if parts[0] in ("batched", "rmsnorm"):   # batched:fmt:M:N1,N2,..:K  /  rmsnorm:fmt:M:N:K
+        if parts[0] in ("batched", "rmsnorm", "gated_rmsnorm"):   # batched:fmt:M:N1,N2,..:K  /  rmsnorm:fmt:M:N:K
             f, mm, nn, kk = parts[1:]
             ns = tuple(int(v) for v in nn.split(","))
             print(json.dumps(fused_row(parts[0], f, int(mm), ns, int(kk), hbm, args.steps, args.warmup)))

@@ -20,6 +20,7 @@ __all__ = [
     "FORMATS", "QfmtError", "load", "lib_path",
     "qfmt_block_size", "qfmt_codes_bytes", "qfmt_scales_bytes",
     "qfmt_pack", "qfmt_dequant", "qmm", "qmm_ex", "qmm_workspace_bytes", "qmm_gather", "qmm_batched", "qmm_rmsnorm",
+    "qmm_gated_rmsnorm",
     "qfmt_last_error",
     "qfmt_version", "qfmt_device_status", "qfmt_debug_set",
 ]
@@ -74,6 +75,10 @@ _SIGS = {
     "qmm_rmsnorm": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]),
+    "qmm_gated_rmsnorm": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                                         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                         ctypes.c_void_p]),
     "qfmt_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "qfmt_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_int64]),
 }
@@ -258,5 +263,18 @@ def qmm_rmsnorm(fmt, codes, scales, global_scale: float, x, norm_weight, eps: fl
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _check(load().qmm_rmsnorm(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), _ptr(norm_weight),
                               float(eps), _ptr(out), M, N, K, group, _stream(stream)), "qmm_rmsnorm")
+    return out
+
+
+def qmm_gated_rmsnorm(fmt, codes, scales, global_scale: float, x, gate, norm_weight, eps: float, N: int, out=None,
+                      group: int = 0, stream=None):
+    """out [M, N] bf16 = (rmsnorm(x; norm_weight, eps) * silu(gate)) . dequant(W)^T, M <= 2 (bf16 x, gate)."""
+    import torch
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(load().qmm_gated_rmsnorm(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), _ptr(gate),
+                                    _ptr(norm_weight), float(eps), _ptr(out), M, N, K, group, _stream(stream)),
+           "qmm_gated_rmsnorm")
     return out
 

@@ -53,10 +53,12 @@ cudaError_t read_and_clear_gather_status(unsigned int* status);
 
 // Decode GEMV (M <= 2) over `count` (1..4) weight matrices sharing the
 // activations, one launch; with gamma != nullptr the activations are
-// RMS-normalised first (x * gamma / sqrt(mean(x^2) + eps)).
+// RMS-normalised first (x * gamma / sqrt(mean(x^2) + eps)); with gate !=
+// nullptr as well (count 1) they are also multiplied by silu(gate).
 cudaError_t launch_qgemv_multi(int fmt, int count, const void* const* codes, const void* const* scales,
                                const float* globs, const int64_t* Ns, const void* x, const void* gamma, float eps,
-                               void* const* outs, bool out_f32, int64_t M, int64_t K, cudaStream_t st);
+                               void* const* outs, bool out_f32, int64_t M, int64_t K, cudaStream_t st,
+                               const void* gate = nullptr);
 uint64_t wait_limit_ns();
 
 }  // namespace qfmt_dev

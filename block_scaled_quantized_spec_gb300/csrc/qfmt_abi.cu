@@ -189,14 +189,15 @@ int qmm_batched(int fmt, int count, const void* const* codes, const void* const*
   return QFMT_OK;
 }
 
-int qmm_rmsnorm(int fmt, const void* codes, const void* scales, float global_scale, const void* x,
-                const void* norm_weight, float eps, void* out, int64_t M, int64_t N, int64_t K, int group,
-                void* stream) {
+// The fused RMSNorm (gate == nullptr) and gated-RMSNorm decode GEMVs.
+static int rmsnorm_form(int fmt, const void* codes, const void* scales, float global_scale, const void* x,
+                 const void* gate, const void* norm_weight, float eps, void* out, int64_t M, int64_t N, int64_t K,
+                 int group, void* stream, const char* name) {
   clear_error();
   int st = check_group(fmt, group);
   if (st) return st;
   if ((st = check_shape(fmt, M, N, K))) return st;
-  if (M > 2) return fail(QFMT_EUNSUPPORTED, "qmm_rmsnorm is the decode form: M=%lld above 2", (long long)M);
+  if (M > 2) return fail(QFMT_EUNSUPPORTED, "%s is the decode form: M=%lld above 2", name, (long long)M);
   if (!(std::isfinite(eps) && eps >= 0.0f)) return fail(QFMT_EINVAL, "eps must be finite and >= 0");
   if (M == 0 || N == 0) return QFMT_OK;
   if (K == 0) return fail(QFMT_ESHAPE, "the RMS of an empty row is undefined (K = 0)");
@@ -204,14 +205,33 @@ int qmm_rmsnorm(int fmt, const void* codes, const void* scales, float global_sca
   if ((st = check_common(fmt, codes, scales, global_scale, group))) return st;
   if ((st = check_ptr(x, 16, "x"))) return st;
   if ((st = check_ptr(norm_weight, 16, "norm_weight"))) return st;
+  if (gate && (st = check_ptr(gate, 16, "gate"))) return st;
   if (!qfmt_dev::qgemv_m2_fits(fmt, M, K))
     return fail(QFMT_EUNSUPPORTED, "K=%lld too long for the fused decode GEMV", (long long)K);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const float g = global_scale;
   const int64_t nw = weight_rows(fmt, N);
   return cuda_status(qfmt_dev::launch_qgemv_multi(fmt, 1, &codes, &scales, &g, &nw, x, norm_weight, eps, &out, false,
-                                                   M, K, s),
-                     "qmm_rmsnorm launch");
+                                                   M, K, s, gate),
+                     name);
+}
+
+int qmm_rmsnorm(int fmt, const void* codes, const void* scales, float global_scale, const void* x,
+                const void* norm_weight, float eps, void* out, int64_t M, int64_t N, int64_t K, int group,
+                void* stream) {
+  return rmsnorm_form(fmt, codes, scales, global_scale, x, nullptr, norm_weight, eps, out, M, N, K, group, stream,
+                      "qmm_rmsnorm");
+}
+
+int qmm_gated_rmsnorm(int fmt, const void* codes, const void* scales, float global_scale, const void* x,
+                      const void* gate, const void* norm_weight, float eps, void* out, int64_t M, int64_t N,
+                      int64_t K, int group, void* stream) {
+  if (!gate) {
+    clear_error();
+    return fail(QFMT_EINVAL, "gate is NULL");
+  }
+  return rmsnorm_form(fmt, codes, scales, global_scale, x, gate, norm_weight, eps, out, M, N, K, group, stream,
+                      "qmm_gated_rmsnorm");
 }
 
 int qfmt_device_status(void* stream) {

@@ -39,7 +39,8 @@ cudaError_t read_and_clear_gather_status(unsigned int* status) {
 
 cudaError_t launch_qgemv_multi(int fmt, int count, const void* const* codes, const void* const* scales,
                                const float* globs, const int64_t* Ns, const void* x, const void* gamma, float eps,
-                               void* const* outs, bool out_f32, int64_t M, int64_t K, cudaStream_t st) {
+                               void* const* outs, bool out_f32, int64_t M, int64_t K, cudaStream_t st,
+                               const void* gate) {
   using namespace gemv_m2;
   Extra ex{};
   ex.count = count;
@@ -57,9 +58,10 @@ cudaError_t launch_qgemv_multi(int fmt, int count, const void* const* codes, con
   ex.tile0[4] = tiles;
   ex.gamma = static_cast<const uint16_t*>(gamma);
   ex.eps = eps;
+  ex.gate = static_cast<const uint16_t*>(gate);
   const int m = int(M), k = int(K);
   const bool rms = gamma != nullptr, batch = count > 1;
-  const int mode = rms ? (batch ? (BATCH | RMS) : RMS) : BATCH;
+  const int mode = gate != nullptr ? (RMS | GATE) : rms ? (batch ? (BATCH | RMS) : RMS) : BATCH;
   if (GroupE2M1::has(fmt)) return e2m1_multi(fmt, mode, ex, x, out_f32, m, k, tiles, st);
   if (GroupFp8::has(fmt)) return fp8_multi(fmt, mode, ex, x, out_f32, m, k, tiles, st);
   return intg_multi(fmt, mode, ex, x, out_f32, m, k, tiles, st);

@@ -179,10 +179,13 @@ static __device__ unsigned int g_gather_status;
 //    the router that wrote them), so the weight requests wait for it too;
 //  * BATCH: up to four weight matrices share the activations (the Q/K/V and
 //    4-way projections); the CTAs of matrix i are [tile0[i], tile0[i + 1]);
+//  * GATE (with RMS): the gated RMSNorm: x * gamma * silu(gate) is staged
+//    (silu(z) = z / (1 + e^-z), gate a bf16 [M, K] tensor read with X); the
+//    root mean square stays that of x;
 //  * RMS: the activations are RMS-normalised on the way in: x * gamma is
 //    staged, sum(x^2) is gathered over the CTA (whose warps cover all of K),
 //    and 1 / sqrt(mean(x^2) + eps) multiplies each output.
-constexpr int GATHER = 1, BATCH = 2, RMS = 4;
+constexpr int GATHER = 1, BATCH = 2, RMS = 4, GATE = 8;
 struct Extra {
   const int32_t* eidx;          // GATHER
   int E;
@@ -194,6 +197,7 @@ struct Extra {
   int n[4];
   int tile0[5];
   const uint16_t* gamma;        // RMS: bf16 [K]
+  const uint16_t* gate;         // GATE: bf16 [M, K]
   float eps;
 };
 
@@ -381,6 +385,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
     constexpr int TIF = (MR * P * TPC + 31) / 32;
     for (int j0 = 0; j0 < tasks; j0 += 32 * TIF) {
       uint4 v[TIF][2];
+      uint4 zv[(MODE & GATE) != 0 ? TIF : 1][2];                            // GATE: the gate's 16 values
       int kk[TIF], mm[TIF];
       bool lv[TIF];
       #pragma unroll
@@ -396,6 +401,11 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
         const uint4* src = reinterpret_cast<const uint4*>(x + int64_t(m) * K + k);
         v[u][0] = lv[u] ? __ldg(src) : make_uint4(0, 0, 0, 0);
         v[u][1] = lv[u] ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
+        if constexpr ((MODE & GATE) != 0) {   // requested with the activations
+          const uint4* zp = reinterpret_cast<const uint4*>(ex.gate + int64_t(m) * K + k);
+          zv[u][0] = lv[u] ? __ldg(zp) : make_uint4(0, 0, 0, 0);
+          zv[u][1] = lv[u] ? __ldg(zp + 1) : make_uint4(0, 0, 0, 0);
+        }
       }
       #pragma unroll
       for (int u = 0; u < TIF; ++u) {
@@ -417,6 +427,14 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
             const float x0 = __uint_as_float(h[q] << 16), x1 = __uint_as_float(h[q] & 0xFFFF0000u);
             f[2 * q] = __fmul_rn(x0, __uint_as_float(gw[q] << 16));
             f[2 * q + 1] = __fmul_rn(x1, __uint_as_float(gw[q] & 0xFFFF0000u));
+            if constexpr ((MODE & GATE) != 0) {
+              const uint32_t zw = q < 4 ? word(zv[u][0], q) : word(zv[u][1], q - 4);
+              const float za = __uint_as_float(zw << 16), zb = __uint_as_float(zw & 0xFFFF0000u);
+              // silu(z) = z / (1 + e^-z): CUDA's fast exponential and the IEEE reciprocal
+              // (e^-z = inf for z far below zero gives a reciprocal of 0, silu -0)
+              f[2 * q] = __fmul_rn(f[2 * q], __fmul_rn(za, __frcp_rn(__fadd_rn(1.0f, __expf(-za)))));
+              f[2 * q + 1] = __fmul_rn(f[2 * q + 1], __fmul_rn(zb, __frcp_rn(__fadd_rn(1.0f, __expf(-zb)))));
+            }
             sq = __fmaf_rn(x0, x0, sq);
             sq = __fmaf_rn(x1, x1, sq);
             mx = max(mx, __float_as_uint(f[2 * q]) & 0x7FFFFFFFu);
@@ -762,6 +780,7 @@ struct Group {
                            cudaStream_t st) {
     cudaError_t r = cudaErrorInvalidValue;
     (void)((fmt == Fs && ((r = mode == (BATCH | RMS) ? launch_multi_fmt<Fs, BATCH | RMS>(ex, x, out_f32, M, K, tiles, st)
+                             : mode == (RMS | GATE) ? launch_multi_fmt<Fs, RMS | GATE>(ex, x, out_f32, M, K, tiles, st)
                              : mode == RMS         ? launch_multi_fmt<Fs, RMS>(ex, x, out_f32, M, K, tiles, st)
                                                    : launch_multi_fmt<Fs, BATCH>(ex, x, out_f32, M, K, tiles, st)),
                            true)) || ...);

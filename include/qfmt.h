@@ -258,6 +258,21 @@ int qmm_rmsnorm(int fmt, const void* codes, const void* scales, float global_sca
                 int64_t M, int64_t N, int64_t K, int group, void* stream);
 
 /*
+ * qmm_gated_rmsnorm -- device, gated RMSNorm fused in front of the decode GEMV:
+ *   out[m, n] (bf16) = sum_k (x[m,k] * gamma[k] * silu(gate[m,k])
+ *                             / sqrt(mean_k x[m,k]^2 + eps)) * dequant(W)[n, k]
+ * with silu(z) = z / (1 + e^-z) (metaltile PR #250, the fused gated-RMSNorm +
+ * dequantizing GEMV commit: the silu gate times the per-row inverse RMS
+ * times the norm weight, staged, then the GEMV).  The root mean square is of
+ * x alone.  gate bf16 [M, K], 16-byte aligned (NULL is QFMT_EINVAL); every
+ * other argument, limit and the tolerance as qmm_rmsnorm, x~ the exactly
+ * gated and normalised activation.
+ */
+int qmm_gated_rmsnorm(int fmt, const void* codes, const void* scales, float global_scale, const void* x,
+                      const void* gate, const void* norm_weight, float eps, void* out, int64_t M, int64_t N,
+                      int64_t K, int group, void* stream);
+
+/*
  * qfmt_device_status -- waits for `stream`, then reads and clears the
  * library's device status word for the current device.  Every pipeline wait
  * inside the tensor-core GEMM is bounded in time; when one expires the kernel

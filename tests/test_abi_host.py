@@ -219,3 +219,13 @@ def test_batched_and_rmsnorm_validation_without_gpu(lib):
     assert rms(gamma=0x1008) == -3
     assert rms(gamma=None) == -1
     assert rms(M=0) == 0 and rms(N=0) == 0
+
+    def gated(M=1, eps=1e-5, gate=0x2000, gamma=0x1000, K=64, N=4):
+        return lib.qmm_gated_rmsnorm(1, 0x1000, 0x1000, 1.0, 0x1000, gate, gamma, eps, 0x1000, M, N, K, 0, None)
+
+    assert gated(gate=None) == -1
+    assert gated(gate=0x2004) == -3
+    assert gated(M=3) == -4
+    assert gated(eps=float("nan")) == -1
+    assert gated(K=0) == -2
+    assert gated(M=0) == 0

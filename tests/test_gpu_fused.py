@@ -4,7 +4,9 @@
   batched Q/K/V and 4-way projections of metaltile PR #250), one launch for
   M <= 2 and one qmm per matrix beyond;
 * qmm_rmsnorm: RMSNorm of the activation fused in front of the decode GEMV
-  (PR #250, the fused RMSNorm + GEMV commit).
+  (PR #250, the fused RMSNorm + GEMV commit);
+* qmm_gated_rmsnorm: the same times silu(gate) (the fused gated-RMSNorm +
+  GEMV commit).
 Tolerance as qmm (plus half an ulp of the bf16 output); inputs packed by the
 oracle's packer from seeded generators.
 """
@@ -121,3 +123,50 @@ def test_rmsnorm_rejects_batches_above_two():
     with pytest.raises(q.QfmtError) as e:
         q.qmm_rmsnorm(fmt, _dev(c), _dev(s), g, xt, gt, 1e-5, n)
     assert e.value.status == -4
+
+
+# ---- the gated RMSNorm (PR #250, the fused gated-RMSNorm + GEMV commit) ----
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("m", [1, 2])
+def test_gated_rmsnorm_parity(fmt, m):
+    n, k, eps = 200, 1024, 1e-5
+    c, s, g = opack.pack(fmt, synth.weights(n, k, seed=90, outliers=(fmt == "nvfp4")))
+    xb, xt = _x(m, k, seed=91 + m)
+    zb, zt = _x(m, k, seed=93 + m)
+    gb, gt = _gamma(k, 95)
+    out = q.qmm_gated_rmsnorm(fmt, _dev(c), _dev(s), g, xt, zt, gt, eps, n)
+    ref, bound = oref.qmm_gated_rmsnorm_ref(fmt, c, s, g, xb, zb, "bf16", gb, eps, m, n, k)
+    _check(out, ref, bound, (fmt, m))
+
+
+def test_gated_rmsnorm_extreme_gates_and_full_width():
+    # N = K = 4096; gates far negative (silu -> -0), zero, and large (silu -> z)
+    fmt, m, n, k, eps = "mxfp4", 2, 4096, 4096, 1e-6
+    c, s, g = opack.pack(fmt, synth.weights(n, k, seed=96))
+    xb, xt = _x(m, k, seed=97)
+    z = np.random.default_rng(98).standard_normal((m, k)).astype(np.float32) * 4
+    z[:, ::7] = -300.0
+    z[:, 1::7] = 0.0
+    z[:, 2::7] = 300.0
+    zb = synth.f32_to_bf16_bits(z)
+    zt = _dev(zb.view(np.int16)).view(torch.bfloat16)
+    gb, gt = _gamma(k, 99)
+    out = q.qmm_gated_rmsnorm(fmt, _dev(c), _dev(s), g, xt, zt, gt, eps, n)
+    ref, bound = oref.qmm_gated_rmsnorm_ref(fmt, c, s, g, xb, zb, "bf16", gb, eps, m, n, k)
+    _check(out, ref, bound, fmt)
+
+
+def test_gated_rmsnorm_with_a_zero_gate_is_zero_and_a_large_gate_scales_rmsnorm():
+    fmt, m, n, k, eps = "nvfp8", 1, 256, 512, 1e-5
+    c, s, g = opack.pack(fmt, synth.weights(n, k, seed=100))
+    xb, xt = _x(m, k, seed=101)
+    gb, gt = _gamma(k, 102)
+    zero = torch.zeros((m, k), dtype=torch.bfloat16, device=DEV)
+    assert not q.qmm_gated_rmsnorm(fmt, _dev(c), _dev(s), g, xt, zero, gt, eps, n).float().any()
+    big = torch.full((m, k), 64.0, dtype=torch.bfloat16, device=DEV)   # silu(64) = 64 in float32
+    a = q.qmm_gated_rmsnorm(fmt, _dev(c), _dev(s), g, xt, big, gt, eps, n).float()
+    b = q.qmm_rmsnorm(fmt, _dev(c), _dev(s), g, xt, gt, eps, n).float()
+    ref, bound = oref.qmm_rmsnorm_ref(fmt, c, s, g, xb, "bf16", gb, eps, m, n, k)
+    _check(a / 64.0, ref, bound, "gate 64")
+    _check(b, ref, bound, "plain")

@@ -123,7 +123,7 @@ int qmm_gather(int fmt, const void* codes, const void* scales, float global_scal
   if (st) return st;
   if ((st = check_shape(fmt, M, N, K))) return st;
   if (E < 1) return fail(QFMT_EINVAL, "expert count E=%lld must be >= 1", (long long)E);
-  if (E * weight_rows(fmt, N) > (int64_t(1) << 31)) return fail(QFMT_ESHAPE, "E*N code rows above 2^31");
+  if (E * weight_rows(fmt, N) >= (int64_t(1) << 31)) return fail(QFMT_ESHAPE, "E*N code rows of 2^31 or more");
   if (M > 65535) return fail(QFMT_ESHAPE, "M=%lld above 65535 rows", (long long)M);
   if (M == 0 || N == 0) return QFMT_OK;
   if ((st = check_ptr(out, 16, "out"))) return st;

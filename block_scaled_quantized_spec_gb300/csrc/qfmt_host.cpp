@@ -93,8 +93,10 @@ int check_shape(int fmt, int64_t M, int64_t N, int64_t K) {
                                            (long long)M, (long long)N, (long long)K);
   // int4 affine (group 64) may end in a ragged group of 32 (ceil(K/64) groups)
   if (K % 32) return fail(QFMT_ESHAPE, "K=%lld must be a multiple of 32", (long long)K);
-  if (N > (int64_t(1) << 31) || M > (int64_t(1) << 31) || K > (int64_t(1) << 31))
-    return fail(QFMT_ESHAPE, "size above 2^31");
+  // the kernels index rows and columns with 32-bit ints; mxfp4x2 streams 2N code rows
+  const int64_t lim = int64_t(1) << 31;
+  const int64_t rows = fmt == QFMT_MXFP4X2 ? 2 * N : N;
+  if (rows >= lim || M >= lim || K >= lim) return fail(QFMT_ESHAPE, "size of 2^31 or more");
   return QFMT_OK;
 }
 

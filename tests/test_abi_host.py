@@ -53,6 +53,11 @@ def test_sizes_and_blocks(lib):
     assert q.qfmt_codes_bytes("mxfp4", 4, 48) == -1           # K not a multiple of 32
     assert q.qfmt_codes_bytes("int4_affine", 4, 80) == -1     # K not a multiple of 32
     assert q.qfmt_scales_bytes("int4_affine", 4, 96) == 4 * 2 * 4   # a ragged last group of 32
+    # 32-bit row and column indices: 2^31 rows (or mxfp4x2's 2N planes) are refused
+    assert q.qfmt_codes_bytes("mxfp8_e4m3", 1 << 31, 32) == -1
+    assert q.qfmt_codes_bytes("mxfp8_e4m3", (1 << 31) - 1, 32) == ((1 << 31) - 1) * 32
+    assert q.qfmt_codes_bytes("mxfp4x2", 1 << 30, 32) == -1
+    assert q.qfmt_codes_bytes("mxfp4x2", (1 << 30) - 1, 32) == ((1 << 30) - 1) * 32
 
 
 CASES = [
@@ -178,6 +183,7 @@ def test_gather_entry_validation_without_gpu(lib):
     assert _call_gather(lib, E=0) == -1
     assert _call_gather(lib, M=70000) == -2
     assert _call_gather(lib, E=1 << 20, N=1 << 12) == -2          # E * N above 2^31
+    assert _call_gather(lib, E=1 << 19, N=1 << 12) == -2          # E * N = 2^31
     assert _call_gather(lib, K=48) == -2
     assert _call_gather(lib, idx=None) == -1
     assert _call_gather(lib, idx=0x2002) == -3

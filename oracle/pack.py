@@ -17,7 +17,7 @@ the spec-conformant nvfp4/mxfp4/mxfp8/nvfp8 formats"; rlx-cpu
 5. pack codes LSB-first (two 4-bit codes per byte, element 2i in the low
    nibble; one byte per 8-bit code).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * E8M0 snapping is ceil(log2 s): the smallest power of two >= amax/max_finite,
   so no element needs to clip.

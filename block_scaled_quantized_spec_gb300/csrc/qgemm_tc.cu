@@ -228,19 +228,21 @@ struct Params {
   int drop_arrivals;   // test hook: decoders never signal a stage (the waits must expire)
 };
 
-template <int F, int MT>
+template <int F, int MT, int BN = Tile<F>::BN>
 __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                           const Params p) {
   constexpr int DEC_WARPS = Dec<F>::WARPS, DEC_THREADS = Dec<F>::THREADS, THREADS = Dec<F>::CTA_THREADS;
   using T = FmtTraits<F>;
   constexpr bool SPLIT = Tile<F>::split;
-  constexpr int BN = Tile<F>::BN;
-  constexpr int TMEM_COLS = BN * MT;
+  // accumulator columns: BN rounded up to a power of two (BN = 224 fills a
+  // 152-SM wave where 256 leaves SMs idle), the allocation a power of two
+  constexpr int ACC = BN > 128 ? 256 : BN;
+  constexpr int TMEM_COLS = ACC * MT;
   constexpr int STAGES = Pipe<MT>::STAGES, STAGE_BYTES = Pipe<MT>::STAGE_BYTES, A_BYTES = Pipe<MT>::A_BYTES;
   constexpr uint32_t IDESC = idesc_bf16<BN>();
   constexpr int PIECE = T::four ? 32 : 16;                 // codes per 16-byte piece
   constexpr int PIECES_PER_ROW = BK / PIECE;               // 2 or 4 per K step
-  constexpr int PIECES_PER_THREAD = BN * PIECES_PER_ROW / DEC_THREADS;   // 1, 2 or 4
+  constexpr int PIECES_PER_THREAD = (BN * PIECES_PER_ROW + DEC_THREADS - 1) / DEC_THREADS;   // 1, 2 or 4
   constexpr int ROWS_PER_PASS = DEC_THREADS / PIECES_PER_ROW;            // 128 or 64
   constexpr int NREG = T::four ? 16 : 8;
   constexpr uint32_t LO_OFF = uint32_t(BN) * BK * 2;       // lo rows follow the hi rows
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
           #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             const uint64_t ad = desc_sw128(stage_a(s) + uint32_t(mt * BM * BK * 2));
-            const uint32_t d = tmem + uint32_t(mt * BN);
+            const uint32_t d = tmem + uint32_t(mt * ACC);
             mma_f16(d, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), IDESC, (j | kk) != 0);
             if constexpr (SPLIT) mma_f16(d, ad + uint64_t(2 * kk), ld + uint64_t(2 * kk), IDESC, 1u);
           }
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
         const int r = rbase + i * ROWS_PER_PASS;
         const int n = n0 + r;
         const int64_t k0 = int64_t(kb) * BK + sub * PIECE;
-        const bool ok = kb < kb1 && n < p.N && k0 < p.K;
+        const bool ok = kb < kb1 && r < BN && n < p.N && k0 < p.K;   // rows past BN (224): zero, unused
         v[i] = ok ? ldg_stream(p.codes + int64_t(n) * row_bytes + (T::four ? k0 / 2 : k0)) : make_uint4(0, 0, 0, 0);
         sc[i] = load_piece_scale<F>(p.scales, n, nblk, k0, ok);
       }
@@ -438,7 +440,7 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
       #pragma unroll 1
       for (int cb = 0; cb < BN / 32; ++cb) {
         uint32_t r[32];
-        tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(mt * BN + cb * 32), r);
+        tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(mt * ACC + cb * 32), r);
         if (split_k) {   // this split's partial tile into the (drained) stage memory
           float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(smem) + (q * 32 + lane) * PSTRIDE + cb * 32);
           #pragma unroll
@@ -596,7 +598,7 @@ static EncodeTiledFn encode_fn() {
 static std::atomic<uint64_t> g_limit_ns{2000000000ull};
 static std::atomic<int> g_drop{0};
 
-template <int F, int MT>
+template <int F, int MT, int BN = Tile<F>::BN>
 static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* scales, float glob, const void* x,
                              void* out, bool out_f32, int M, int N, int K, cudaStream_t st, int S) {
   static std::atomic<int> attr_done[64];
@@ -604,7 +606,7 @@ static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* s
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
-    e = cudaFuncSetAttribute(qgemm_tc_kernel<F, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(qgemm_tc_kernel<F, MT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Pipe<MT>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done[dev].store(1);
@@ -641,13 +643,13 @@ static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* s
   at[1].val.clusterDim.x = 1;
   at[1].val.clusterDim.y = 1;
   at[1].val.clusterDim.z = unsigned(S);
-  lc.gridDim = dim3((N + Tile<F>::BN - 1) / Tile<F>::BN, (M + BM * MT - 1) / (BM * MT), S);
+  lc.gridDim = dim3((N + BN - 1) / BN, (M + BM * MT - 1) / (BM * MT), S);
   lc.blockDim = dim3(Dec<F>::CTA_THREADS);
   lc.dynamicSmemBytes = Pipe<MT>::SMEM_BYTES;
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 2;
-  return cudaLaunchKernelEx(&lc, qgemm_tc_kernel<F, MT>, map, prm);
+  return cudaLaunchKernelEx(&lc, qgemm_tc_kernel<F, MT, BN>, map, prm);
 }
 
 // Tile shape (MT 128-row accumulators per CTA) and K split S, by the estimated
@@ -656,27 +658,36 @@ static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* s
 // the waves of one-CTA-per-SM work, plus ~8 K steps for a split's partial-tile
 // reduction.  No split may be left empty.
 struct GemmPlan {
-  int MT, S;
+  int MT, S, BN;
 };
-inline GemmPlan plan_gemm(int BN, int M, int N, int K, int sms) {
-  const int ntiles = (N + BN - 1) / BN;
+inline GemmPlan plan_gemm(bool split, int M, int N, int K, int sms) {
   const int nkb = (K + BK - 1) / BK;
-  GemmPlan best{1, 1};
+  GemmPlan best{1, 1, split ? 128 : 256};
   double best_cost = 1e300;
+  // the formats exact in bf16 may also take 224-wide tiles without a K split
+  // (152 SMs hold 19 x 8 tiles of 224 x 256 in one wave where 16 x 8 tiles of
+  // 256 leave 24 idle; a K step then costs about 224/256 of a 256-wide one)
+  for (int bn : {256, 224, 128}) {
+  if (split ? bn != 128 : bn == 128) continue;
+  const int ntiles = (N + bn - 1) / bn;
   for (int mt = 1; mt <= 2; ++mt) {
     if (mt == 2 && M <= BM) continue;
     const int64_t mtiles = (M + int64_t(BM) * mt - 1) / (int64_t(BM) * mt);
     for (int s = 1; s <= (mt == 1 ? 4 : 1); ++s) {
       const int per = (nkb + s - 1) / s;
       if (s > 1 && (s - 1) * per >= nkb) continue;
+      // a K split runs as clusters of s CTAs, packed per GPC: 224-wide tiles
+      // would overflow the co-resident clusters of a wave (measured slower)
+      if (bn == 224 && s > 1) continue;
       const int64_t ctas = int64_t(ntiles) * mtiles * s;
       const int64_t waves = (ctas + sms - 1) / sms;
-      const double cost = double(waves) * per * (mt == 2 ? 1.1 : 1.0) + (s > 1 ? 8.0 : 0.0);
+      const double cost = double(waves) * per * (mt == 2 ? 1.1 : 1.0) * (split ? 1.0 : bn / 256.0) + (s > 1 ? 8.0 : 0.0);
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
-        best = {mt, s};
+        best = {mt, s, bn};
       }
     }
+  }
   }
   return best;
 }
@@ -686,7 +697,13 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, float glob,
                               bool out_f32, int M, int N, int K, cudaStream_t st, int sms) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  const GemmPlan pl = plan_gemm(Tile<F>::BN, M, N, K, sms > 0 ? sms : 1);
+  const GemmPlan pl = plan_gemm(Tile<F>::split, M, N, K, sms > 0 ? sms : 1);
+  if constexpr (!Tile<F>::split) {
+    if (pl.BN == 224) {
+      if (pl.MT == 2) return launch_mt<F, 2, 224>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st, 1);
+      return launch_mt<F, 1, 224>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st, pl.S);
+    }
+  }
   if (pl.MT == 2) return launch_mt<F, 2>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st, 1);
   return launch_mt<F, 1>(enc, codes, scales, glob, x, out, out_f32, M, N, K, st, pl.S);
 }

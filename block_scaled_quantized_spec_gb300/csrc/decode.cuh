@@ -41,9 +41,10 @@ template <> struct FmtTraits<INT8> { static constexpr bool four = false; static 
 template <> struct FmtTraits<INT8_F16> { static constexpr bool four = false; static constexpr int block = 64; static constexpr int sbytes = 2; };
 template <> struct FmtTraits<INT4> { static constexpr bool four = true; static constexpr int block = 64; static constexpr int sbytes = 4; };
 template <> struct FmtTraits<INT4_F16> { static constexpr bool four = true; static constexpr int block = 64; static constexpr int sbytes = 2; };
-// mxfp4x2 as the kernels see it: 2N rows of E2M1 codes (row 2n the residual
+// mxfp4x2 as the GEMVs see it: 2N rows of E2M1 codes (row 2n the residual
 // plane 0 of output row n, row 2n + 1 its plane 1) with a float32 scale per
-// 32; an output is the sum of its two rows' products.
+// 32, an output the sum of its two rows' products; the GEMM decodes both
+// planes of an output row into one weight (decode_x2_hilo).
 template <> struct FmtTraits<MXFP4X2> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 4; };
 template <> struct FmtTraits<MXINT4> { static constexpr bool four = true; static constexpr int block = 32; static constexpr int sbytes = 1; };
 // the legacy float formats: an E2M1 / E4M3 / E5M2 element under a float32 (or
@@ -486,6 +487,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16x2(a, b);
   lo = pack_bf16x2(__fsub_rn(a, __uint_as_float(hi << 16)), __fsub_rn(b, __uint_as_float(hi & 0xFFFF0000u)));
+}
+
+// One piece of 32 k of an mxfp4x2 row, both residual planes (a: plane 0, b:
+// plane 1, 16 bytes each) and their float32 block scales (ps.a, ps.b): the
+// weight s0 e2m1(q0) + s1 e2m1(q1) (one fma, one rounding) as hi/lo bf16 pairs
+// in natural k order (16 registers each).
+__device__ __forceinline__ void decode_x2_hilo(const uint4& va, const uint4& vb, const PieceScale& ps, uint32_t* hi,
+                                               uint32_t* lo) {
+  const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+  const float s0 = __uint_as_float(ps.a), s1 = __uint_as_float(ps.b);
+  #pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    #pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint32_t ba = (wa[j] >> (8 * p)) & 0xFFu, bb = (wb[j] >> (8 * p)) & 0xFFu;
+      const float w0 = __fmaf_rn(e2m1_f32(bb & 0xFu), s1, __fmul_rn(e2m1_f32(ba & 0xFu), s0));
+      const float w1 = __fmaf_rn(e2m1_f32(bb >> 4), s1, __fmul_rn(e2m1_f32(ba >> 4), s0));
+      split_bf16x2(w0, w1, hi[4 * j + p], lo[4 * j + p]);
+    }
+  }
 }
 
 // One 16-byte piece of a float-scaled 8-bit (16 codes) or int4-affine (32

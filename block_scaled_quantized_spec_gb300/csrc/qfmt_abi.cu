@@ -104,8 +104,8 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale, c
     return cuda_status(qfmt_dev::launch_qgemv(fmt, codes, scales, global_scale, x, out, out_f32, M,
                                               weight_rows(fmt, N), K, s, sms),
                        "qgemv launch");
-  return cuda_status(qfmt_dev::launch_qgemm_tc(fmt, codes, scales, global_scale, x, out, out_f32, M,
-                                               weight_rows(fmt, N), K, s, sms),
+  // the GEMM decodes both mxfp4x2 planes of an output row together: N output rows
+  return cuda_status(qfmt_dev::launch_qgemm_tc(fmt, codes, scales, global_scale, x, out, out_f32, M, N, K, s, sms),
                      "qgemm launch");
 }
 

@@ -39,6 +39,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <type_traits>
 #include <mutex>
 
 #include "decode.cuh"
@@ -228,6 +229,14 @@ struct Params {
   int drop_arrivals;   // test hook: decoders never signal a stage (the waits must expire)
 };
 
+// The codes a decoder thread holds for one piece: 16 bytes of one row, or for
+// mxfp4x2 the 16 bytes of each residual plane of one output row.
+struct PiecePair {
+  uint4 a, b;
+};
+template <int F>
+using PieceCodes = std::conditional_t<F == MXFP4X2, PiecePair, uint4>;
+
 template <int F, int MT, int BN = Tile<F>::BN>
 __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                           const Params p) {
@@ -351,28 +360,44 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
     const int64_t nblk = (p.K + T::block - 1) / T::block;   // int4 affine: a ragged last group
     const int sub = dt % PIECES_PER_ROW;                   // piece index within the row's K step
     const int rbase = dt / PIECES_PER_ROW;
-    uint4 cur[PIECES_PER_THREAD], nxt[PIECES_PER_THREAD];
+    using PC = PieceCodes<F>;
+    PC cur[PIECES_PER_THREAD], nxt[PIECES_PER_THREAD];
     PieceScale cs[PIECES_PER_THREAD], ns[PIECES_PER_THREAD];
-    auto load = [&](int kb, uint4 (&v)[PIECES_PER_THREAD], PieceScale (&sc)[PIECES_PER_THREAD]) {
+    auto load = [&](int kb, PC (&v)[PIECES_PER_THREAD], PieceScale (&sc)[PIECES_PER_THREAD]) {
       #pragma unroll
       for (int i = 0; i < PIECES_PER_THREAD; ++i) {
         const int r = rbase + i * ROWS_PER_PASS;
         const int n = n0 + r;
         const int64_t k0 = int64_t(kb) * BK + sub * PIECE;
         const bool ok = kb < kb1 && r < BN && n < p.N && k0 < p.K;   // rows past BN (224): zero, unused
-        v[i] = ok ? ldg_stream(p.codes + int64_t(n) * row_bytes + (T::four ? k0 / 2 : k0)) : make_uint4(0, 0, 0, 0);
-        sc[i] = load_piece_scale<F>(p.scales, n, nblk, k0, ok);
+        if constexpr (F == MXFP4X2) {   // output row n: plane 0, then plane 1, K/2 bytes each
+          const uint8_t* pa = p.codes + int64_t(n) * p.K + k0 / 2;
+          v[i].a = ok ? ldg_stream(pa) : make_uint4(0, 0, 0, 0);
+          v[i].b = ok ? ldg_stream(pa + p.K / 2) : make_uint4(0, 0, 0, 0);
+          const float* sr = reinterpret_cast<const float*>(p.scales) + int64_t(n) * 2 * nblk + k0 / 32;
+          sc[i].a = ok ? __float_as_uint(__ldg(sr)) : 0u;
+          sc[i].b = ok ? __float_as_uint(__ldg(sr + nblk)) : 0u;
+        } else {
+          v[i] = ok ? ldg_stream(p.codes + int64_t(n) * row_bytes + (T::four ? k0 / 2 : k0)) : make_uint4(0, 0, 0, 0);
+          sc[i] = load_piece_scale<F>(p.scales, n, nblk, k0, ok);
+        }
       }
     };
     // one M tile: this CTA's weight slab [kb0, kb1) towards L2 now (one row
     // per thread); with more M tiles the other tiles' CTAs share it
     if (gridDim.y == 1 && dt < BN && n0 + dt < p.N && nloc > 0) {
       const int64_t kbeg = int64_t(kb0) * BK, kend = min(int64_t(kb1) * BK, int64_t(p.K));
-      const uint8_t* src = p.codes + int64_t(n0 + dt) * row_bytes + (T::four ? kbeg / 2 : kbeg);
-      prefetch_l2(src, uint64_t(T::four ? (kend - kbeg) / 2 : (kend - kbeg)));
+      if constexpr (F == MXFP4X2) {   // both planes of the row
+        const uint8_t* src = p.codes + int64_t(n0 + dt) * p.K + kbeg / 2;
+        prefetch_l2(src, uint64_t((kend - kbeg) / 2));
+        prefetch_l2(src + p.K / 2, uint64_t((kend - kbeg) / 2));
+      } else {
+        const uint8_t* src = p.codes + int64_t(n0 + dt) * row_bytes + (T::four ? kbeg / 2 : kbeg);
+        prefetch_l2(src, uint64_t(T::four ? (kend - kbeg) / 2 : (kend - kbeg)));
+      }
     }
     // codes three K steps ahead in flight (cur, nxt, nx2 loaded; nx3 issued per step)
-    uint4 nx2[PIECES_PER_THREAD];
+    PC nx2[PIECES_PER_THREAD];
     PieceScale ns2[PIECES_PER_THREAD];
     load(kb0, cur, cs);
     load(kb0 + 1, nxt, ns);
@@ -390,7 +415,7 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
         aborted = true;
         break;
       }
-      uint4 nx3[PIECES_PER_THREAD];
+      PC nx3[PIECES_PER_THREAD];
       PieceScale ns3[PIECES_PER_THREAD];
       load(kb + 3, nx3, ns3);
       const uint32_t bs = stage_b(s);
@@ -399,7 +424,8 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
         const int r = rbase + i * ROWS_PER_PASS;
         if constexpr (SPLIT) {
           uint32_t hi[NREG], lo[NREG];
-          decode_piece_hilo<F>(cur[i], cs[i], hi, lo);
+          if constexpr (F == MXFP4X2) decode_x2_hilo(cur[i].a, cur[i].b, cs[i], hi, lo);
+          else decode_piece_hilo<F>(cur[i], cs[i], hi, lo);
           #pragma unroll
           for (int c = 0; c < NREG / 4; ++c) {
             const uint32_t off = sw128_off(r, sub * (NREG / 4) + c);
@@ -457,38 +483,6 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
           v[j] = __uint_as_float(r[j]);
           if constexpr (F == NVFP4) v[j] *= p.glob;
         }
-        if constexpr (F == MXFP4X2) {   // columns 2j, 2j + 1: the residual planes of output column nb / 2 + j
-          const int no = p.N / 2, ob = nb / 2;
-          const int ncols = no - ob < 16 ? no - ob : 16;
-          float u[16];
-          #pragma unroll
-          for (int j = 0; j < 16; ++j) u[j] = v[2 * j] + v[2 * j + 1];
-          if (p.out_f32) {
-            float* o = static_cast<float*>(p.out) + int64_t(m) * no + ob;
-            if (ncols == 16 && (no & 3) == 0) {
-              #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                reinterpret_cast<float4*>(o)[j] = make_float4(u[4 * j], u[4 * j + 1], u[4 * j + 2], u[4 * j + 3]);
-            } else {
-              for (int j = 0; j < ncols; ++j) o[j] = u[j];
-            }
-          } else {
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + int64_t(m) * no + ob;
-            if (ncols == 16 && (no & 7) == 0) {
-              #pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                uint32_t h[4];
-                #pragma unroll
-                for (int t = 0; t < 4; ++t)
-                  h[t] = f32_to_bf16bits(u[8 * j + 2 * t]) | (f32_to_bf16bits(u[8 * j + 2 * t + 1]) << 16);
-                reinterpret_cast<uint4*>(o)[j] = make_uint4(h[0], h[1], h[2], h[3]);
-              }
-            } else {
-              for (int j = 0; j < ncols; ++j) o[j] = __float2bfloat16_rn(u[j]);
-            }
-          }
-          continue;
-        }
         const int ncols = p.N - nb < 32 ? p.N - nb : 32;
         if (p.out_f32) {
           float* o = static_cast<float*>(p.out) + int64_t(m) * p.N + nb;
@@ -539,16 +533,6 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
         v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
       }
       if constexpr (F == NVFP4) { v.x *= p.glob; v.y *= p.glob; v.z *= p.glob; v.w *= p.glob; }
-      if constexpr (F == MXFP4X2) {   // two output columns, each the sum of its two residual planes
-        const int no = p.N / 2;
-        const float u[2] = {v.x + v.y, v.z + v.w};
-        for (int j = 0; j < 2 && n / 2 + j < no; ++j) {
-          const int64_t oi = int64_t(m) * no + n / 2 + j;
-          if (p.out_f32) static_cast<float*>(p.out)[oi] = u[j];
-          else static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(u[j]);
-        }
-        continue;
-      }
       const float f4[4] = {v.x, v.y, v.z, v.w};
       const bool vec = n + 4 <= p.N && (p.N & 3) == 0;
       if (p.out_f32) {

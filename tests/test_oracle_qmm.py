@@ -286,6 +286,41 @@ def test_planted_mistakes_are_caught(monkeypatch):
             _check_brute("mxfp8_e4m3")
 
 
+def test_planted_mistakes_in_the_added_formats_are_caught(monkeypatch):
+    """Plausible decode bugs of the formats beyond the first six -- a signed
+    element read unsigned, the mxfp4x2 planes' scales swapped, a half scale read
+    as bfloat16 -- must each fail the exact rational brute force."""
+    orig_elem = reference.element_values
+    orig_scales = reference.block_scales
+    orig_exact = reference.dequant_exact
+
+    def unsigned_ints(fmt, codes):
+        if fmt in ("mxint8", "int8", "int4", "mxint4"):
+            return codes.astype(np.float64)
+        return orig_elem(fmt, codes)
+
+    def swapped_planes(fmt, codes, scales, g, n, k):
+        if fmt == "mxfp4x2":
+            sc = np.ascontiguousarray(np.asarray(scales, dtype=np.uint8)).view(np.float32).reshape(n, 2, -1)
+            scales = np.ascontiguousarray(sc[:, ::-1]).view(np.uint8).reshape(n, -1)
+        return orig_exact(fmt, codes, scales, g, n, k)
+
+    def half_as_bf16(fmt, scales, g, n, k):
+        if fmt in ("int8_f16", "nvfp8_f16", "fp4_f16"):
+            s = np.ascontiguousarray(np.asarray(scales, dtype=np.uint8)).view(np.uint16).reshape(n, -1)
+            return reference.codec.decode_bf16(s), None
+        return orig_scales(fmt, scales, g, n, k)
+
+    plants = [("element_values", unsigned_ints, "mxint8"), ("element_values", unsigned_ints, "int4"),
+              ("element_values", unsigned_ints, "mxint4"), ("dequant_exact", swapped_planes, "mxfp4x2"),
+              ("block_scales", half_as_bf16, "int8_f16"), ("block_scales", half_as_bf16, "fp4_f16")]
+    for name, fn, fmt in plants:
+        with monkeypatch.context() as mp:
+            mp.setattr(reference, name, fn)
+            with pytest.raises(AssertionError):
+                _check_brute(fmt)
+
+
 # ----- expert-routed rows (MoE gather-qmm) -----
 
 def _gather_case(fmt, m, n, k, e, seed):

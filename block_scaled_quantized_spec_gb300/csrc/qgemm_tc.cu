@@ -652,26 +652,27 @@ inline GemmPlan plan_gemm(bool split, int M, int N, int K, int sms) {
   // (152 SMs hold 19 x 8 tiles of 224 x 256 in one wave where 16 x 8 tiles of
   // 256 leave 24 idle; a K step then costs about 224/256 of a 256-wide one)
   for (int bn : {256, 224, 128}) {
-  if (split ? bn != 128 : bn == 128) continue;
-  const int ntiles = (N + bn - 1) / bn;
-  for (int mt = 1; mt <= 2; ++mt) {
-    if (mt == 2 && M <= BM) continue;
-    const int64_t mtiles = (M + int64_t(BM) * mt - 1) / (int64_t(BM) * mt);
-    for (int s = 1; s <= (mt == 1 ? 4 : 1); ++s) {
-      const int per = (nkb + s - 1) / s;
-      if (s > 1 && (s - 1) * per >= nkb) continue;
-      // a K split runs as clusters of s CTAs, packed per GPC: 224-wide tiles
-      // would overflow the co-resident clusters of a wave (measured slower)
-      if (bn == 224 && s > 1) continue;
-      const int64_t ctas = int64_t(ntiles) * mtiles * s;
-      const int64_t waves = (ctas + sms - 1) / sms;
-      const double cost = double(waves) * per * (mt == 2 ? 1.1 : 1.0) * (split ? 1.0 : bn / 256.0) + (s > 1 ? 8.0 : 0.0);
-      if (cost < best_cost - 1e-9) {
-        best_cost = cost;
-        best = {mt, s, bn};
+    if (split ? bn != 128 : bn == 128) continue;
+    const int ntiles = (N + bn - 1) / bn;
+    for (int mt = 1; mt <= 2; ++mt) {
+      if (mt == 2 && M <= BM) continue;
+      const int64_t mtiles = (M + int64_t(BM) * mt - 1) / (int64_t(BM) * mt);
+      for (int s = 1; s <= (mt == 1 ? 4 : 1); ++s) {
+        const int per = (nkb + s - 1) / s;
+        if (s > 1 && (s - 1) * per >= nkb) continue;
+        // a K split runs as clusters of s CTAs, packed per GPC: 224-wide tiles
+        // would overflow the co-resident clusters of a wave (measured slower)
+        if (bn == 224 && s > 1) continue;
+        const int64_t ctas = int64_t(ntiles) * mtiles * s;
+        const int64_t waves = (ctas + sms - 1) / sms;
+        const double width = split ? 1.0 : bn / 256.0;
+        const double cost = double(waves) * per * (mt == 2 ? 1.1 : 1.0) * width + (s > 1 ? 8.0 : 0.0);
+        if (cost < best_cost - 1e-9) {
+          best_cost = cost;
+          best = {mt, s, bn};
+        }
       }
     }
-  }
   }
   return best;
 }

@@ -62,6 +62,14 @@ Readings taken where the pages are silent:
   per-group scale path") and their fp16-scale twins *_f16: s = amax /
   max_finite(element) in float32 (1.0 for an all-zero group), stored raw or
   rounded once to an IEEE half (as nvfp8_f16); codes as step 4.
+* int2 / int3 / int5 / int6 (PR #250's symmetric intN on the FP32 group-64
+  scale path), their fp16-scale twins *_f16, and mxint2 / mxint3 / mxint5 /
+  mxint6 (the signed N-bit element under an E8M0 scale per 32): as int4 /
+  mxint4 with 2^(N-1) - 1 in place of 7; the N-bit two's-complement codes of
+  a row form one LSB-first bit stream (code j in bits [jN, jN + N) of the
+  row's little-endian bit sequence; a 4-bit stream is the nibble layout).  K
+  a multiple of 32 makes every row a whole number of 32-bit words, so no code
+  straddles two rows.
 * int4 affine (MLX style, group 64): s = (max - min) / 15 (1.0 when 0), stored
   as bf16 (RNE); bias = bf16(min); q = clamp(round_half_away((w - b) / s), 0, 15);
   scale and bias are interleaved per group as bf16 pairs [N, ceil(K/64), 2].
@@ -79,9 +87,14 @@ from . import codec
 
 FORMATS = ("mxfp4", "nvfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp8", "int4_affine", "nvfp8_f16", "mxint8",
            "int8", "int8_f16", "int4", "int4_f16", "mxfp4x2", "mxint4",
-           "fp4", "fp4_f16", "fp8_e4m3", "fp8_e4m3_f16", "fp8_e5m2", "fp8_e5m2_f16")
-RAGGED = ("int4_affine", "int8", "int8_f16", "int4", "int4_f16")   # block 64: K may end in a group of 32
-SYM_INT = ("int8", "int8_f16", "int4", "int4_f16")                 # symmetric integers, float scale per 64
+           "fp4", "fp4_f16", "fp8_e4m3", "fp8_e4m3_f16", "fp8_e5m2", "fp8_e5m2_f16",
+           "int2", "int3", "int5", "int6", "int2_f16", "int3_f16", "int5_f16", "int6_f16",
+           "mxint2", "mxint3", "mxint5", "mxint6")
+INTN = {f: int(f.split("_")[0][-1]) for f in FORMATS if f.split("_")[0] in ("int2", "int3", "int5", "int6",
+                                                                            "mxint2", "mxint3", "mxint5", "mxint6")}
+RAGGED = ("int4_affine", "int8", "int8_f16", "int4", "int4_f16",   # block 64: K may end in a group of 32
+          "int2", "int3", "int5", "int6", "int2_f16", "int3_f16", "int5_f16", "int6_f16")
+SYM_INT = RAGGED[1:]                                                # symmetric integers, float scale per 64
 
 BLOCK = {"mxfp4": 32, "nvfp4": 16, "mxfp8_e4m3": 32, "mxfp8_e5m2": 32, "nvfp8": 16, "int4_affine": 64,
          "nvfp8_f16": 16, "mxint8": 32, "int8": 64, "int8_f16": 64, "int4": 64, "int4_f16": 64, "mxfp4x2": 32,
@@ -104,6 +117,12 @@ _ELEM = {"mxfp4": ("e2m1", codec.E2M1_MAX), "nvfp4": ("e2m1", codec.E2M1_MAX),
          "fp8_e4m3": ("e4m3", codec.E4M3_MAX), "fp8_e4m3_f16": ("e4m3", codec.E4M3_MAX),
          "fp8_e5m2": ("e5m2", codec.E5M2_MAX), "fp8_e5m2_f16": ("e5m2", codec.E5M2_MAX)}
 
+for _f, _b in INTN.items():
+    BLOCK[_f] = 32 if _f.startswith("mx") else 64
+    ELEM_BITS[_f] = _b
+    SCALE_BYTES[_f] = 1 if _f.startswith("mx") else (2 if _f.endswith("_f16") else 4)
+    _ELEM[_f] = (f"int{_b}", float(2 ** (_b - 1) - 1))
+
 F32 = np.float32
 
 
@@ -124,6 +143,13 @@ def _pack_nibbles(codes: np.ndarray) -> np.ndarray:
     """[N, K] uint8 codes (0..15) -> [N, K/2] bytes, element 2i in the low nibble."""
     c = codes.astype(np.uint8)
     return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def pack_bits(codes: np.ndarray, bits: int) -> np.ndarray:
+    """[N, K] codes of `bits` bits -> [N, K * bits / 8] bytes, one LSB-first bit stream per row."""
+    c = np.asarray(codes, dtype=np.uint8)
+    stream = ((c[..., None] >> np.arange(bits, dtype=np.uint8)) & 1).reshape(c.shape[0], -1)
+    return np.packbits(stream, axis=1, bitorder="little")
 
 
 def _quantize(w_blocks: np.ndarray, eff: np.ndarray, elem: str) -> np.ndarray:
@@ -172,7 +198,7 @@ def pack(fmt: str, w: np.ndarray):
         return _pack_mxfp4x2(wb, n, k)
 
     elem, maxf = _ELEM[fmt]
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4") or fmt.startswith("mxint"):
         s = np.where(amax > 0, amax / F32(maxf), F32(1.0)).astype(F32)   # step 2
         scode = codec.e8m0_encode_ceil(s)                                  # step 3
         eff = codec.E8M0_TABLE[scode].astype(F32)                          # exact power of two
@@ -185,7 +211,7 @@ def pack(fmt: str, w: np.ndarray):
         ucode = np.where(amax > 0, ucode, np.uint8(0x38)).astype(np.uint8)
         eff = (codec.E4M3_TABLE[ucode].astype(F32) * glob).astype(F32)
         scales = ucode
-    elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16", "fp4_f16", "fp8_e4m3_f16", "fp8_e5m2_f16"):
+    elif fmt.endswith("_f16"):
         # the fp16-scale twin: amax / 448 rounded once to an IEEE half (nearest
         # even, subnormals kept, overflow to inf, rejected below)
         s = np.where(amax > 0, amax / F32(maxf), F32(1.0)).astype(F32)
@@ -200,15 +226,18 @@ def pack(fmt: str, w: np.ndarray):
     if not np.all(np.isfinite(eff)):
         raise ValueError("scale overflows float32")
 
-    if elem in ("int8", "int4"):   # symmetric integer element: round half away from zero, clamp to +-maxf
+    if elem.startswith("int"):   # symmetric integer element: round half away from zero, clamp to +-maxf
         safe = np.where(eff == 0, F32(1.0), eff).astype(F32)
         v = (wb / safe[..., None]).astype(F32)
         q = np.clip(_round_half_away(v), -maxf, maxf)
         q = np.where((eff == 0)[..., None], 0, q).astype(np.int8).reshape(n, k)
         scales_b = np.ascontiguousarray(scales).view(np.uint8).reshape(n, -1)
-        if elem == "int4":      # 4-bit two's complement, two per byte
+        bits = ELEM_BITS[fmt]
+        if bits == 4:           # 4-bit two's complement, two per byte
             return _pack_nibbles(q.view(np.uint8) & np.uint8(0x0F)), scales_b, F32(glob)
-        return q.view(np.uint8), scales_b, F32(glob)
+        if bits == 8:
+            return q.view(np.uint8), scales_b, F32(glob)
+        return pack_bits(q.view(np.uint8) & np.uint8((1 << bits) - 1), bits), scales_b, F32(glob)
     codes = _quantize(wb, eff, elem).reshape(n, k)                        # step 4
     codes_b = _pack_nibbles(codes) if ELEM_BITS[fmt] == 4 else codes.astype(np.uint8)
     scales_b = np.ascontiguousarray(scales).view(np.uint8).reshape(n, -1)

@@ -33,6 +33,10 @@ Value definitions (page title, then the section):
 * fp4 / fp8_e4m3 / fp8_e5m2 and their *_f16 twins: w = elem(code) * scale,
   a float32 (IEEE half) scale per 32 -- PR #250, the legacy float formats
   on the FP32 per-group scale path and the fp16-scale axis.
+* int2 / int3 / int5 / int6 (and *_f16) and mxint2 / 3 / 5 / 6: w = q * scale
+  with q the N-bit code of the row's LSB-first bit stream, sign-extended from
+  bit N-1 -- PR #250, the symmetric intN / MXINT formats and the sub-byte
+  bit-stream packing.
 * int4 affine: w = scale * q + bias with q the LSB-first nibble, group 64 --
   metaltile-std ``tests/qmm_gpu_correctness.rs``, ``cpu_qmm_reference``;
   scale and bias are bf16.  float64 evaluation of s*q + b is exact or, when
@@ -62,7 +66,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import codec
-from .pack import BLOCK, ELEM_BITS, FORMATS, SCALE_BYTES
+from .pack import BLOCK, ELEM_BITS, FORMATS, INTN, SCALE_BYTES
 
 BOUND_REL = 2e-3
 BOUND_ABS = 1e-6
@@ -73,6 +77,10 @@ def unpack_codes(fmt: str, codes: np.ndarray, n: int, k: int) -> np.ndarray:
     b = np.asarray(codes, dtype=np.uint8).reshape(n, -1)
     if ELEM_BITS[fmt] == 8:
         return b.reshape(n, k)
+    if ELEM_BITS[fmt] not in (4, 8):   # a row's LSB-first bit stream of `bits`-bit codes
+        bits = ELEM_BITS[fmt]
+        stream = np.unpackbits(b, axis=1, bitorder="little")[:, : k * bits].reshape(n, k, bits)
+        return (stream.astype(np.uint32) << np.arange(bits, dtype=np.uint32)).sum(axis=2).astype(np.uint8)
     out = np.empty((n, k), dtype=np.uint8)
     out[:, 0::2] = b & 0x0F
     out[:, 1::2] = b >> 4
@@ -88,13 +96,13 @@ def block_scales(fmt: str, scales: np.ndarray, global_scale: float, n: int, k: i
     """
     nb = -(-k // BLOCK[fmt])
     s = np.asarray(scales, dtype=np.uint8).reshape(n, -1)
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4") or fmt.startswith("mxint"):
         return codec.E8M0_TABLE[s.reshape(n, nb)], None
     if fmt == "nvfp4":
         return codec.E4M3_TABLE[s.reshape(n, nb)], None
-    if fmt in ("nvfp8", "int8", "int4", "fp4", "fp8_e4m3", "fp8_e5m2"):
+    if fmt in ("nvfp8", "int8", "int4", "fp4", "fp8_e4m3", "fp8_e5m2") or fmt in ("int2", "int3", "int5", "int6"):
         return np.ascontiguousarray(s).view(np.float32).reshape(n, nb).astype(np.float64), None
-    if fmt in ("nvfp8_f16", "int8_f16", "int4_f16", "fp4_f16", "fp8_e4m3_f16", "fp8_e5m2_f16"):
+    if fmt.endswith("_f16"):
         return np.ascontiguousarray(s).view(np.float16).reshape(n, nb).astype(np.float64), None
     pair = np.ascontiguousarray(s).view(np.uint16).reshape(n, nb, 2)
     return codec.decode_bf16(pair[..., 0]), codec.decode_bf16(pair[..., 1])
@@ -112,6 +120,10 @@ def element_values(fmt: str, codes: np.ndarray) -> np.ndarray:
     if fmt in ("int4", "int4_f16", "mxint4"):            # the two's-complement nibble, sign-extended from bit 3
         c = codes.astype(np.int64)
         return np.where(c >= 8, c - 16, c).astype(np.float64)
+    if fmt in INTN:                                      # N-bit two's complement, sign-extended from bit N-1
+        bits = INTN[fmt]
+        c = codes.astype(np.int64)
+        return np.where(c >= 1 << (bits - 1), c - (1 << bits), c).astype(np.float64)
     return codes.astype(np.float64)                      # int4 affine: q itself
 
 

@@ -43,7 +43,8 @@ def test_byte_sizes():
         assert c.nbytes == n * k * bits // 8 == pack.codes_nbytes(fmt, n, k)
         per_scale = {"nvfp8": 4, "int4_affine": 4, "nvfp8_f16": 2, "int8": 4, "int8_f16": 2, "int4": 4,
                      "int4_f16": 2, "mxfp4x2": 8, "fp4": 4, "fp4_f16": 2, "fp8_e4m3": 4, "fp8_e4m3_f16": 2,
-                     "fp8_e5m2": 4, "fp8_e5m2_f16": 2}.get(fmt, 1)
+                     "fp8_e5m2": 4, "fp8_e5m2_f16": 2, "int2": 4, "int3": 4, "int5": 4, "int6": 4,
+                     "int2_f16": 2, "int3_f16": 2, "int5_f16": 2, "int6_f16": 2}.get(fmt, 1)
         assert s.nbytes == n * (k // pack.BLOCK[fmt]) * per_scale == pack.scales_nbytes(fmt, n, k)
         assert c.dtype == np.uint8 and s.dtype == np.uint8 and isinstance(g, np.float32)
 
@@ -68,13 +69,13 @@ def test_zero_blocks():
     for fmt in FMTS:
         c, s, g = pack.pack(fmt, w)
         assert not c.any(), fmt
-        if fmt in MX or fmt in ("mxint8", "mxint4"):
+        if fmt in MX or fmt.startswith("mxint"):
             assert (s == 127).all()
         elif fmt == "nvfp4":
             assert (s == 0x38).all() and g == 1.0
-        elif fmt in ("nvfp8", "int8", "int4", "mxfp4x2", "fp4", "fp8_e4m3", "fp8_e5m2"):
+        elif fmt in ("nvfp8", "int8", "int4", "mxfp4x2", "fp4", "fp8_e4m3", "fp8_e5m2", "int2", "int3", "int5", "int6"):
             assert (s.view(np.float32) == 1.0).all()
-        elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16", "fp4_f16", "fp8_e4m3_f16", "fp8_e5m2_f16"):
+        elif fmt.endswith("_f16"):
             assert (s.view(np.float16) == 1.0).all()
         else:
             pair = s.view(np.uint16).reshape(n, -1, 2)
@@ -131,7 +132,9 @@ FLOORS = {"mxfp4": 0.98, "nvfp4": 0.98, "int4_affine": 0.99,
           "mxfp8_e5m2": 0.995, "mxfp8_e4m3": 0.999, "nvfp8": 0.999, "nvfp8_f16": 0.999, "mxint8": 0.999,
           "int8": 0.9999, "int8_f16": 0.9999, "int4": 0.99, "int4_f16": 0.99, "mxfp4x2": 0.9999, "mxint4": 0.98,
           "fp4": 0.98, "fp4_f16": 0.98, "fp8_e4m3": 0.999, "fp8_e4m3_f16": 0.999, "fp8_e5m2": 0.995,
-          "fp8_e5m2_f16": 0.995}
+          "fp8_e5m2_f16": 0.995, "int2": 0.75, "int3": 0.95, "int5": 0.998, "int6": 0.9995, "int2_f16": 0.75,
+          "int3_f16": 0.95, "int5_f16": 0.998, "int6_f16": 0.9995, "mxint2": 0.6, "mxint3": 0.92, "mxint5": 0.997,
+          "mxint6": 0.999}
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -494,3 +497,71 @@ def test_legacy_float_scale_is_not_snapped():
     c, s, _ = pack.pack("fp4", w)
     assert s.view(np.float32)[0] == np.float32(5.0) / np.float32(6.0)
     assert reference.dequant_f32("fp4", c, s, 1.0, 1, 32)[0, 0] == np.float32(6.0 * np.float64(s.view(np.float32)[0]))
+
+
+
+# ----- the sub-byte integer widths (PR #250: int2-6, mxint2-6, one LSB-first bit stream) -----
+
+SUBBYTE = ["int2", "int3", "int5", "int6", "int3_f16", "mxint2", "mxint3", "mxint5", "mxint6"]
+
+
+def test_bit_stream_layout_against_integer_arithmetic():
+    # code j of a row occupies bits [j N, j N + N) of the row bytes read as one
+    # little-endian integer: built here with Python integers, not numpy bits
+    rng = np.random.default_rng(81)
+    for bits in (2, 3, 5, 6, 4):
+        n, k = 3, 64
+        codes = rng.integers(0, 1 << bits, size=(n, k)).astype(np.uint8)
+        got = pack.pack_bits(codes, bits)
+        for r in range(n):
+            v = 0
+            for j in range(k):
+                v |= int(codes[r, j]) << (j * bits)
+            assert bytes(got[r]) == v.to_bytes(k * bits // 8, "little"), bits
+        assert np.array_equal(reference.unpack_codes({2: "int2", 3: "int3", 5: "int5", 6: "int6", 4: "mxfp4"}[bits],
+                                                     got, n, k), codes)
+
+
+def test_four_bit_stream_is_the_nibble_layout():
+    # PR #250: "a 4-bit stream is byte-identical to the old nibble layout"
+    rng = np.random.default_rng(82)
+    codes = rng.integers(0, 16, size=(4, 96)).astype(np.uint8)
+    assert np.array_equal(pack.pack_bits(codes, 4), pack._pack_nibbles(codes))
+
+
+@pytest.mark.parametrize("fmt", SUBBYTE)
+def test_subbyte_exactly_representable_roundtrip(fmt):
+    # W = q * s per block with +-(2^(N-1) - 1) in every block and s of few
+    # significant bits (a power of two for mxint): codes, scales and values back exactly
+    rng = np.random.default_rng(83 + len(fmt))
+    bits = pack.INTN[fmt]
+    qmax = (1 << (bits - 1)) - 1
+    n, k, blk = 4, 128, pack.BLOCK[fmt]
+    nb = k // blk
+    q = rng.integers(-qmax, qmax + 1, size=(n, k))
+    q[:, ::blk] = qmax * rng.choice([-1, 1], size=(n, nb))
+    if fmt.startswith("mx"):
+        e = rng.integers(-30, 20, size=(n, nb))
+        s = 2.0 ** e
+    else:
+        s = rng.integers(512, 1024, size=(n, nb)) * 2.0 ** rng.integers(-24, -12, size=(n, nb))
+    w = (q * np.repeat(s, blk, axis=1)).astype(np.float32)
+    c, sc, g = pack.pack(fmt, w)
+    assert c.shape == (n, k * bits // 8)
+    assert np.array_equal(reference.unpack_codes(fmt, c, n, k), (q & ((1 << bits) - 1)).astype(np.uint8))
+    if fmt.startswith("mx"):
+        assert np.array_equal(sc.astype(np.int64), e + 127)
+    else:
+        got_s = sc.view(np.float16 if fmt.endswith("_f16") else np.float32).reshape(n, -1).astype(np.float64)
+        assert np.array_equal(got_s, s)
+    assert np.array_equal(reference.dequant_exact(fmt, c, sc, g, n, k), w.astype(np.float64))
+
+
+def test_subbyte_ragged_last_group():
+    # int3 over K = 96: a group of 64 and a ragged group of 32 with its own scale
+    n, k = 2, 96
+    w = synth.weights(n, k, seed=84)
+    c, s, g = pack.pack("int3", w)
+    assert c.shape == (n, 36) and s.view(np.float32).shape == (n, 2)
+    sc = s.view(np.float32).reshape(n, 2)
+    assert np.array_equal(sc[:, 1], (np.abs(w[:, 64:]).max(axis=1) / np.float32(3.0)).astype(np.float32))

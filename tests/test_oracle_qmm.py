@@ -44,23 +44,33 @@ def _lib_elem(fmt, c):
         return Fraction(c - 256 if c >= 128 else c)
     if fmt in ("int4", "int4_f16", "mxint4"):
         return Fraction(c - 16 if c >= 8 else c)
+    if fmt in pack.INTN:                                  # sign bit N - 1 of an N-bit code
+        nb = pack.INTN[fmt]
+        return Fraction(c - (1 << nb) if c >> (nb - 1) else c)
     return Fraction(c)
 
 
 def _lib_scale(fmt, sbytes, n, b):
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4", "mxint2", "mxint3", "mxint5", "mxint6"):
         return Fraction(2) ** (int(sbytes[n][b]) - 127), Fraction(0)
     if fmt == "nvfp4":
         v = torch.tensor([int(sbytes[n][b])], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()
         return Fraction(v), Fraction(0)
-    if fmt in ("nvfp8", "int8", "int4", "fp4", "fp8_e4m3", "fp8_e5m2"):
+    if fmt in ("nvfp8", "int8", "int4", "fp4", "fp8_e4m3", "fp8_e5m2", "int2", "int3", "int5", "int6"):
         return Fraction(float(np.frombuffer(bytes(sbytes[n][4 * b:4 * b + 4]), "<f4")[0])), Fraction(0)
-    if fmt in ("nvfp8_f16", "int8_f16", "int4_f16", "fp4_f16", "fp8_e4m3_f16", "fp8_e5m2_f16"):
+    if fmt.endswith("_f16"):
         return Fraction(float(np.frombuffer(bytes(sbytes[n][2 * b:2 * b + 2]), "<f2")[0])), Fraction(0)
     raw = bytes(sbytes[n][4 * b:4 * b + 4])
     s_bits, b_bits = np.frombuffer(raw, "<u2")
     f = lambda h: Fraction(float((np.array([h], np.uint32) << 16).view(np.float32)[0]))  # noqa: E731
     return f(s_bits), f(b_bits)
+
+
+def _code(fmt, row, kk):
+    # code kk of a row: bits [kk N, kk N + N) of the row bytes read as one
+    # little-endian integer (4-bit: the nibble layout; 8-bit: the byte)
+    nb = pack.ELEM_BITS[fmt]
+    return (int.from_bytes(bytes(row), "little") >> (kk * nb)) & ((1 << nb) - 1)
 
 
 def _x2_weight(codes_row, scales_row, kk, k):
@@ -88,11 +98,7 @@ def _brute_qmm(fmt, codes, scales, g, x64, m, n, k):
             if fmt == "mxfp4x2":
                 wrow.append(_x2_weight(codes[j], scales[j], kk, k))
                 continue
-            if pack.ELEM_BITS[fmt] == 4:
-                byte = codes[j][kk // 2]
-                c = (byte >> (4 * (kk % 2))) & 0xF
-            else:
-                c = codes[j][kk]
+            c = _code(fmt, codes[j], kk)
             mul, add = _lib_scale(fmt, scales, j, kk // blk)
             w = _lib_elem(fmt, c) * mul + add
             if fmt == "nvfp4":
@@ -143,9 +149,7 @@ def test_dequant_f32_is_one_rounding_of_exact(fmt):
                 w = _x2_weight(codes[j], scales[j], kk, k)
                 assert wf[j, kk] == np.float32(float(w)), (fmt, j, kk)
                 continue
-            four = pack.ELEM_BITS[fmt] == 4
-            byte = codes[j][kk // 2] if four else codes[j][kk]
-            cc = (byte >> (4 * (kk % 2))) & 0xF if four else byte
+            cc = _code(fmt, codes[j], kk)
             mul, add = _lib_scale(fmt, scales, j, kk // blk)
             w = _lib_elem(fmt, cc) * mul + add
             if fmt == "nvfp4":

@@ -135,12 +135,14 @@ typedef enum {
   QFMT_EINDEX = -9         /* qmm_gather met an expert index outside [0, E) (see qfmt_device_status) */
 } qfmt_status;
 
-/* Block (group) size of a format along K: 32, 16, 32, 32, 16, 64; 0 for an
- * unknown format. */
+/* Block (group) size of a format along K, as in the table above (16 for the
+ * nv formats, 64 for the int4 affine / int8 / int4 groups, 32 for the rest);
+ * 0 for an unknown format. */
 int qfmt_block_size(int fmt);
 
-/* Bytes of the codes / scales buffers for an [N, K] weight; -1 on a bad
- * format or shape (see QFMT_ESHAPE). */
+/* Bytes of the codes / scales buffers for an [N, K] weight (codes: K/2 or K
+ * bytes a row, mxfp4x2 K; scales: ceil(K/block) entries a row of the entry
+ * size in the table); -1 on a bad format or shape (see QFMT_ESHAPE). */
 int64_t qfmt_codes_bytes(int fmt, int64_t N, int64_t K);
 int64_t qfmt_scales_bytes(int fmt, int64_t N, int64_t K);
 

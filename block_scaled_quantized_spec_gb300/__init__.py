@@ -50,9 +50,9 @@ def lib_path() -> str:
 _SIGS = {
     "qfmt_version": (ctypes.c_int, []),
     "qfmt_last_error": (ctypes.c_char_p, []),
-    "qfmt_block_size": (ctypes.c_int, [ctypes.c_int]),
-    "qfmt_codes_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
-    "qfmt_scales_bytes": (ctypes.c_int64, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
+    "qfmt_block_size": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "qfmt_codes_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int]),
+    "qfmt_scales_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int]),
     "qfmt_pack": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)]),
     "qfmt_dequant": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
@@ -64,7 +64,7 @@ _SIGS = {
     "qmm_ex": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
                               ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                               ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
-    "qmm_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]),
+    "qmm_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
     "qmm_gather": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                   ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]),
@@ -150,20 +150,32 @@ def qfmt_debug_set(key: int, value: int) -> None:
     _check(load().qfmt_debug_set(key, value), "qfmt_debug_set")
 
 
-def qfmt_block_size(fmt) -> int:
-    return load().qfmt_block_size(_fmt(fmt))
+SIZE_ERROR = (1 << (8 * ctypes.sizeof(ctypes.c_size_t))) - 1   # SIZE_MAX: a size query's error return
 
 
-def qfmt_codes_bytes(fmt, N: int, K: int) -> int:
-    return load().qfmt_codes_bytes(_fmt(fmt), N, K)
+def qfmt_block_size(fmt, group: int = 0) -> int:
+    """The block along K (0 for an unknown format or a group the format does not take)."""
+    return load().qfmt_block_size(_fmt(fmt), group)
 
 
-def qfmt_scales_bytes(fmt, N: int, K: int) -> int:
-    return load().qfmt_scales_bytes(_fmt(fmt), N, K)
+def _size(v: int, where: str) -> int:
+    if v == SIZE_ERROR:
+        raise QfmtError(-2, where, load().qfmt_last_error().decode())
+    return v
 
 
-def qmm_workspace_bytes(fmt, M: int, N: int, K: int) -> int:
-    return load().qmm_workspace_bytes(_fmt(fmt), M, N, K)
+def qfmt_codes_bytes(fmt, N: int, K: int, group: int = 0) -> int:
+    """Bytes of the packed codes of an [N, K] weight; raises QfmtError where the C call returns SIZE_MAX."""
+    return _size(load().qfmt_codes_bytes(_fmt(fmt), N, K, group), "qfmt_codes_bytes")
+
+
+def qfmt_scales_bytes(fmt, N: int, K: int, group: int = 0) -> int:
+    """Bytes of the block scales of an [N, K] weight; raises QfmtError where the C call returns SIZE_MAX."""
+    return _size(load().qfmt_scales_bytes(_fmt(fmt), N, K, group), "qfmt_scales_bytes")
+
+
+def qmm_workspace_bytes(fmt, M: int, K: int) -> int:
+    return load().qmm_workspace_bytes(_fmt(fmt), M, K)
 
 
 def qfmt_pack(fmt, W: np.ndarray, group: int = 0):
@@ -172,9 +184,11 @@ def qfmt_pack(fmt, W: np.ndarray, group: int = 0):
     f = _fmt(fmt)
     W = np.ascontiguousarray(W, dtype=np.float32)
     N, K = W.shape
-    cb, sb = lib.qfmt_codes_bytes(f, N, K), lib.qfmt_scales_bytes(f, N, K)
-    if cb < 0 or sb < 0:
-        raise QfmtError(-2, "qfmt_pack", f"bad format/shape {fmt} {N}x{K}")
+    cb, sb = lib.qfmt_codes_bytes(f, N, K, group), lib.qfmt_scales_bytes(f, N, K, group)
+    g = ctypes.c_float(0.0)
+    if cb == SIZE_ERROR or sb == SIZE_ERROR:   # the packer's own status for the refused format / group / shape
+        _check(lib.qfmt_pack(f, _ptr(W), N, K, group, None, None, ctypes.byref(g)), "qfmt_pack")
+        raise QfmtError(-2, "qfmt_pack", f"bad format/group/shape {fmt} {N}x{K}")
     codes = np.zeros(cb, np.uint8)
     scales = np.zeros(sb, np.uint8)
     g = ctypes.c_float(0.0)
@@ -182,41 +196,116 @@ def qfmt_pack(fmt, W: np.ndarray, group: int = 0):
     return codes.reshape(N, -1) if N else codes, scales.reshape(N, -1) if N else scales, float(g.value)
 
 
+def _fail(where: str, msg: str, status: int = -1):
+    raise QfmtError(status, where, msg)
+
+
+def _tensor(t, where: str, name: str, dtype=None, nbytes=None, shape=None):
+    """Check one tensor's layout, dtype, shape and size before its pointer crosses the C ABI."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        _fail(where, f"{name} must be a torch tensor")
+    if not t.is_contiguous():
+        _fail(where, f"{name} must be contiguous (row-major)")
+    if dtype is not None and t.dtype != dtype:
+        _fail(where, f"{name} must be {dtype} (is {t.dtype})")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        _fail(where, f"{name} must have shape {tuple(shape)} (has {tuple(t.shape)})")
+    if nbytes is not None and t.numel() * t.element_size() < nbytes:
+        _fail(where, f"{name} holds {t.numel() * t.element_size()} bytes, the call reads {nbytes}")
+
+
+def _on_device(where: str, **tensors):
+    """Every tensor is a CUDA tensor on the device of the first one."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            _fail(where, f"{name} must be a CUDA tensor (is on {t.device})")
+        dev = dev or t.device
+        if t.device != dev:
+            _fail(where, f"{name} is on {t.device}, the call runs on {dev}")
+
+
+def _weights(where, fmt, codes, scales, rows, K, group):
+    """codes / scales: device tensors holding at least the packed bytes of a [rows, K] weight."""
+    cb = _size(load().qfmt_codes_bytes(_fmt(fmt), rows, K, group), where)
+    sb = _size(load().qfmt_scales_bytes(_fmt(fmt), rows, K, group), where)
+    _tensor(codes, where, "codes", nbytes=cb)
+    _tensor(scales, where, "scales", nbytes=sb)
+
+
+def _activations(where, x, dtypes=None):
+    import torch
+    dtypes = dtypes or (torch.bfloat16,)
+    if not isinstance(x, torch.Tensor):
+        _fail(where, "x must be a torch tensor")
+    if x.dim() != 2:
+        _fail(where, f"x must be 2-D [M, K] (has {x.dim()} dimensions)")
+    if x.dtype not in dtypes:
+        _fail(where, f"x must be {' or '.join(str(d) for d in dtypes)} (is {x.dtype})")
+    _tensor(x, where, "x")
+    return x.shape[0], x.shape[1]
+
+
 def qfmt_dequant(fmt, codes, scales, global_scale: float, N: int, K: int, out=None, out_dtype=None,
                  group: int = 0, stream=None):
     """Device dequant into ``out`` (a new [N, K] tensor if None); float32 unless out_dtype is bf16."""
     import torch
+    where = "qfmt_dequant"
+    _weights(where, fmt, codes, scales, N, K, group)
     if out is None:
         out = torch.empty((N, K), dtype=out_dtype or torch.float32, device=codes.device)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        _fail(where, f"out must be float32 or bfloat16 (is {out.dtype})")
+    _tensor(out, where, "out", shape=(N, K))
+    _on_device(where, codes=codes, scales=scales, out=out)
     od = BF16 if out.dtype == torch.bfloat16 else F32
     _check(load().qfmt_dequant(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(out), od,
-                               N, K, group, _stream(stream)), "qfmt_dequant")
+                               N, K, group, _stream(stream)), where)
     return out
 
 
 def qmm(fmt, codes, scales, global_scale: float, x, N: int, out=None, group: int = 0, stream=None):
     """out [M, N] bf16 = x [M, K] bf16 . dequant(W)^T on the device."""
     import torch
-    M, K = x.shape
+    where = "qmm"
+    M, K = _activations(where, x)
+    _weights(where, fmt, codes, scales, N, K, group)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _tensor(out, where, "out", dtype=torch.bfloat16, shape=(M, N))
+    _on_device(where, x=x, codes=codes, scales=scales, out=out)
     _check(load().qmm(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), _ptr(out),
-                      M, N, K, group, _stream(stream)), "qmm")
+                      M, N, K, group, _stream(stream)), where)
     return out
 
 
 def qmm_ex(fmt, codes, scales, global_scale: float, x, N: int, out=None, out_dtype=None, group: int = 0,
            workspace=None, stream=None):
-    """qmm with x in bf16 or float32 and out in bf16 or float32 (default: x's dtype)."""
+    """qmm with x in bf16 or float32 and out in bf16 or float32 (default: x's dtype).
+
+    ``workspace``: None, or a device tensor of at least ``qmm_workspace_bytes(fmt, M, K)`` bytes.
+    """
     import torch
-    M, K = x.shape
+    where = "qmm_ex"
+    M, K = _activations(where, x, (torch.bfloat16, torch.float32))
+    _weights(where, fmt, codes, scales, N, K, group)
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype or x.dtype, device=x.device)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        _fail(where, f"out must be float32 or bfloat16 (is {out.dtype})")
+    _tensor(out, where, "out", shape=(M, N))
+    ws_bytes = 0
+    if workspace is not None:
+        _tensor(workspace, where, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _on_device(where, x=x, codes=codes, scales=scales, out=out, workspace=workspace)
     xd = F32 if x.dtype == torch.float32 else BF16
     od = F32 if out.dtype == torch.float32 else BF16
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().qmm_ex(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), xd, _ptr(out), od,
-                         M, N, K, group, _ptr(workspace), ws_bytes, _stream(stream)), "qmm_ex")
+                         M, N, K, group, _ptr(workspace), ws_bytes, _stream(stream)), where)
     return out
 
 
@@ -227,54 +316,83 @@ def qmm_gather(fmt, codes, scales, global_scale: float, x, expert_idx, N: int, E
     ``expert_idx`` is a device int32 tensor [M].
     """
     import torch
-    M, K = x.shape
-    if expert_idx.dtype != torch.int32 or expert_idx.numel() != M:
-        raise QfmtError(-1, "qmm_gather", "expert_idx must be an int32 tensor of M entries")
+    where = "qmm_gather"
+    M, K = _activations(where, x)
+    if E < 1:
+        _fail(where, f"expert count E={E} must be >= 1")
+    _weights(where, fmt, codes, scales, E * N, K, group)
+    _tensor(expert_idx, where, "expert_idx", dtype=torch.int32)
+    if expert_idx.numel() != M:
+        _fail(where, "expert_idx must be an int32 tensor of M entries")
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _tensor(out, where, "out", dtype=torch.bfloat16, shape=(M, N))
+    _on_device(where, x=x, codes=codes, scales=scales, expert_idx=expert_idx, out=out)
     _check(load().qmm_gather(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), _ptr(expert_idx),
-                             _ptr(out), M, N, K, E, group, _stream(stream)), "qmm_gather")
+                             _ptr(out), M, N, K, E, group, _stream(stream)), where)
     return out
 
 
 def qmm_batched(fmt, codes, scales, global_scales, x, Ns, outs=None, group: int = 0, stream=None):
     """Products of up to four weights with one activation: outs[i] [M, Ns[i]] bf16 = x . dequant(W_i)^T."""
     import torch
-    M, K = x.shape
+    where = "qmm_batched"
+    M, K = _activations(where, x)
     count = len(codes)
     if not (len(scales) == len(global_scales) == len(Ns) == count):
-        raise QfmtError(-1, "qmm_batched", "codes, scales, global_scales and Ns differ in length")
+        _fail(where, "codes, scales, global_scales and Ns differ in length")
+    if not 1 <= count <= 4:
+        _fail(where, f"count={count} must be 1..4")
+    for c, sc, n in zip(codes, scales, Ns):
+        _weights(where, fmt, c, sc, int(n), K, group)
     if outs is None:
         outs = [torch.empty((M, n), dtype=torch.bfloat16, device=x.device) for n in Ns]
+    if len(outs) != count:
+        _fail(where, "outs differs in length from codes")
+    for o, n in zip(outs, Ns):
+        _tensor(o, where, "out", dtype=torch.bfloat16, shape=(M, int(n)))
+    _on_device(where, x=x, **{f"codes[{i}]": t for i, t in enumerate(codes)},
+               **{f"scales[{i}]": t for i, t in enumerate(scales)}, **{f"outs[{i}]": t for i, t in enumerate(outs)})
     arr = lambda ts: (ctypes.c_void_p * count)(*[t.data_ptr() for t in ts])  # noqa: E731
     _check(load().qmm_batched(_fmt(fmt), count, arr(codes), arr(scales),
                               (ctypes.c_float * count)(*[float(g) for g in global_scales]),
                               (ctypes.c_int64 * count)(*[int(n) for n in Ns]), _ptr(x), arr(outs), M, K, group,
-                              _stream(stream)), "qmm_batched")
+                              _stream(stream)), where)
     return outs
+
+
+def _norm_args(where, fmt, codes, scales, x, norm_weight, N, out, group, gate=None):
+    import torch
+    M, K = _activations(where, x)
+    _weights(where, fmt, codes, scales, N, K, group)
+    _tensor(norm_weight, where, "norm_weight", dtype=torch.bfloat16, shape=(K,))
+    if gate is not None:
+        _tensor(gate, where, "gate", dtype=torch.bfloat16, shape=(M, K))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _tensor(out, where, "out", dtype=torch.bfloat16, shape=(M, N))
+    _on_device(where, x=x, codes=codes, scales=scales, norm_weight=norm_weight, gate=gate, out=out)
+    return M, K, out
 
 
 def qmm_rmsnorm(fmt, codes, scales, global_scale: float, x, norm_weight, eps: float, N: int, out=None,
                 group: int = 0, stream=None):
     """out [M, N] bf16 = rmsnorm(x; norm_weight, eps) . dequant(W)^T, M <= 2 (x and norm_weight bf16)."""
-    import torch
-    M, K = x.shape
-    if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    where = "qmm_rmsnorm"
+    M, K, out = _norm_args(where, fmt, codes, scales, x, norm_weight, N, out, group)
     _check(load().qmm_rmsnorm(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), _ptr(norm_weight),
-                              float(eps), _ptr(out), M, N, K, group, _stream(stream)), "qmm_rmsnorm")
+                              float(eps), _ptr(out), M, N, K, group, _stream(stream)), where)
     return out
 
 
 def qmm_gated_rmsnorm(fmt, codes, scales, global_scale: float, x, gate, norm_weight, eps: float, N: int, out=None,
                       group: int = 0, stream=None):
     """out [M, N] bf16 = (rmsnorm(x; norm_weight, eps) * silu(gate)) . dequant(W)^T, M <= 2 (bf16 x, gate)."""
-    import torch
-    M, K = x.shape
-    if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    where = "qmm_gated_rmsnorm"
+    if gate is None:
+        _fail(where, "gate is None")
+    M, K, out = _norm_args(where, fmt, codes, scales, x, norm_weight, N, out, group, gate=gate)
     _check(load().qmm_gated_rmsnorm(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), _ptr(gate),
                                     _ptr(norm_weight), float(eps), _ptr(out), M, N, K, group, _stream(stream)),
-           "qmm_gated_rmsnorm")
+           where)
     return out
-

@@ -287,6 +287,15 @@ __device__ __forceinline__ void e5m2x4_bf16_raw(uint32_t w, uint32_t r[2]) {
   r[1] = ((w >> 3) & 0x0FE00FE0u) | (w & 0x80008000u);
 }
 
+// The codes these bit placements do not map to their value: the E4M3 NaNs
+// (S.1111.111) and the E5M2 infinities and NaNs (S.11111.mm).  Bit 7 of byte i
+// of the result is set when code i of `w` is one (no carry crosses a byte).
+template <int F>
+__device__ __forceinline__ uint32_t special8_mask(uint32_t w) {
+  if constexpr (is_e5m2<F>()) return ((w & 0x7C7C7C7Cu) + 0x04040404u) & 0x80808080u;
+  else return ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+}
+
 // 4 signed-int8 codes -> bf16x2 {c0,c2} {c1,c3}, exact: each byte with its
 // sign bit flipped is 128 + q, placed under the float32 exponent of 2^23 and
 // rebased by 2^23 + 128 in float32, then packed (|q| <= 128 is exact in bf16).
@@ -444,6 +453,22 @@ __device__ __forceinline__ void decode_piece(const uint4& v, const PieceScale& p
         A[j][0] = hmul2(A[j][0], m2);
         A[j][1] = hmul2(A[j][1], m2);
       }
+      if constexpr (!is_int8<F>()) {
+        // a NaN / Inf code (outside the packer's range): its value times the
+        // block scale in float32, rounded to bf16 (NaN, or +-inf)
+        const uint32_t sm = special8_mask<F>(w[j]);
+        if (sm) {
+          const float s = is_mx8<F>() ? e8m0_f32(ps.a) : __uint_as_float(ps.a);
+          #pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (!(sm & (0x80u << (8 * i)))) continue;
+            const uint32_t c = (w[j] >> (8 * i)) & 0xFFu;
+            const uint32_t h = f32_to_bf16bits(__fmul_rn(is_e5m2<F>() ? e5m2_f32(c) : e4m3_f32(c), s));
+            uint32_t& dst = A[j][i & 1];
+            dst = (i & 2) ? ((dst & 0x0000FFFFu) | (h << 16)) : ((dst & 0xFFFF0000u) | h);
+          }
+        }
+      }
     }
   }
 }
@@ -542,8 +567,19 @@ __device__ __forceinline__ void decode_piece_hilo(const uint4& v, const PieceSca
         e02 = hmul2(r[0], 0x7B807B80u);                                             // x 2^120: exact values
         e13 = hmul2(r[1], 0x7B807B80u);
       }
-      const float v0 = __fmul_rn(__uint_as_float(e02 << 16), s), v2 = __fmul_rn(__uint_as_float(e02 & 0xFFFF0000u), s);
-      const float v1 = __fmul_rn(__uint_as_float(e13 << 16), s), v3 = __fmul_rn(__uint_as_float(e13 & 0xFFFF0000u), s);
+      float v0 = __fmul_rn(__uint_as_float(e02 << 16), s), v2 = __fmul_rn(__uint_as_float(e02 & 0xFFFF0000u), s);
+      float v1 = __fmul_rn(__uint_as_float(e13 << 16), s), v3 = __fmul_rn(__uint_as_float(e13 & 0xFFFF0000u), s);
+      if constexpr (!is_int8<F>()) {
+        if (special8_mask<F>(w[j])) {   // NaN / Inf codes: their value times the scale
+          auto fix = [&](float& v, uint32_t c) {
+            if (special8_mask<F>(c)) v = __fmul_rn(is_e5m2<F>() ? e5m2_f32(c) : e4m3_f32(c), s);
+          };
+          fix(v0, w[j] & 0xFFu);
+          fix(v1, (w[j] >> 8) & 0xFFu);
+          fix(v2, (w[j] >> 16) & 0xFFu);
+          fix(v3, w[j] >> 24);
+        }
+      }
       split_bf16x2(v0, v1, hi[2 * j], lo[2 * j]);
       split_bf16x2(v2, v3, hi[2 * j + 1], lo[2 * j + 1]);
     }

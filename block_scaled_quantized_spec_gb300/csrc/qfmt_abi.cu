@@ -93,6 +93,9 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale, c
     return cuda_status(cudaMemsetAsync(out, 0, size_t(M) * size_t(N) * (out_f32 ? 4 : 2), s), "memset");
   if ((st = check_common(fmt, codes, scales, global_scale, group))) return st;
   if ((st = check_ptr(x, 16, "x"))) return st;
+  // the GEMM's 128-row tiles run along the grid's y dimension (at most 65535)
+  if (x_dtype == QFMT_BF16 && M > 16 && (M + 127) / 128 > 65535)
+    return fail(QFMT_ESHAPE, "M=%lld: more than 65535 row tiles of 128", (long long)M);
   int err = QFMT_OK;
   const int sms = device_sms(&err);
   if (err) return err;
@@ -262,8 +265,8 @@ int qfmt_debug_set(int key, int64_t value) {
   return fail(QFMT_EINVAL, "unknown debug key %d", key);
 }
 
-size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K) {
-  (void)fmt; (void)M; (void)N; (void)K;
+size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t K) {
+  (void)fmt; (void)M; (void)K;
   return 0;
 }
 

@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdint>
 #include <cstring>
 #include <thread>
 #include <vector>
@@ -218,16 +219,22 @@ int qfmt_version(void) { return 107; }
 
 const char* qfmt_last_error(void) { return qfmt::g_err; }
 
-int qfmt_block_size(int fmt) { return block_of(fmt); }
-
-int64_t qfmt_codes_bytes(int fmt, int64_t N, int64_t K) {
-  if (!valid_format(fmt) || check_shape(fmt, 0, N, K) != QFMT_OK) return -1;
-  return is_4bit(fmt) ? N * K / 2 : N * K;
+int qfmt_block_size(int fmt, int group) {
+  clear_error();
+  if (check_group(fmt, group) != QFMT_OK) return 0;
+  return block_of(fmt);
 }
 
-int64_t qfmt_scales_bytes(int fmt, int64_t N, int64_t K) {
-  if (!valid_format(fmt) || check_shape(fmt, 0, N, K) != QFMT_OK) return -1;
-  return N * ((K + block_of(fmt) - 1) / block_of(fmt)) * scale_entry_bytes(fmt);
+size_t qfmt_codes_bytes(int fmt, int64_t N, int64_t K, int group) {
+  clear_error();
+  if (check_group(fmt, group) != QFMT_OK || check_shape(fmt, 0, N, K) != QFMT_OK) return SIZE_MAX;
+  return size_t(is_4bit(fmt) ? N * K / 2 : N * K);
+}
+
+size_t qfmt_scales_bytes(int fmt, int64_t N, int64_t K, int group) {
+  clear_error();
+  if (check_group(fmt, group) != QFMT_OK || check_shape(fmt, 0, N, K) != QFMT_OK) return SIZE_MAX;
+  return size_t(N * ((K + block_of(fmt) - 1) / block_of(fmt)) * scale_entry_bytes(fmt));
 }
 
 int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* codes,

@@ -135,16 +135,21 @@ typedef enum {
   QFMT_EINDEX = -9         /* qmm_gather met an expert index outside [0, E) (see qfmt_device_status) */
 } qfmt_status;
 
-/* Block (group) size of a format along K, as in the table above (16 for the
- * nv formats, 64 for the int4 affine / int8 / int4 groups, 32 for the rest);
- * 0 for an unknown format. */
-int qfmt_block_size(int fmt);
+/* Block (group) size along K of format `fmt` packed with `group` (0 = the
+ * format's default; the only other accepted value is that default itself):
+ * 16 for the nv formats, 64 for the int4 affine / int8 / int4 groups, 32 for
+ * the rest (metaltile PR #250 format table).  0 for an unknown format or a
+ * group the format does not take (qfmt_last_error says which). */
+int qfmt_block_size(int fmt, int group);
 
-/* Bytes of the codes / scales buffers for an [N, K] weight (codes: K/2 or K
- * bytes a row, mxfp4x2 K; scales: ceil(K/block) entries a row of the entry
- * size in the table); -1 on a bad format or shape (see QFMT_ESHAPE). */
-int64_t qfmt_codes_bytes(int fmt, int64_t N, int64_t K);
-int64_t qfmt_scales_bytes(int fmt, int64_t N, int64_t K);
+/* Bytes of the codes / scales buffers of an [N, K] weight packed with `group`
+ * (codes: K/2 or K bytes a row, mxfp4x2 K; scales: ceil(K/block) entries a
+ * row of the entry size in the table).  SIZE_MAX on an unknown format, a
+ * group the format does not take, or a shape qfmt_pack rejects (negative
+ * size, K not a multiple of 32, 2^31 or more code rows); qfmt_last_error
+ * says which. */
+size_t qfmt_codes_bytes(int fmt, int64_t N, int64_t K, int group);
+size_t qfmt_scales_bytes(int fmt, int64_t N, int64_t K, int group);
 
 /*
  * qfmt_pack -- host packer: float32 W [N, K] (host) -> codes, scales (host
@@ -202,7 +207,7 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale,
            int64_t M, int64_t N, int64_t K, int group,
            void* workspace, size_t workspace_bytes, void* stream);
 
-size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t N, int64_t K);
+size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t K);
 
 /*
  * qmm_gather -- device, expert-routed rows (mixture of experts):

@@ -46,18 +46,38 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_sizes_and_blocks(lib):
     for name, f in q.FORMATS.items():
-        assert q.qfmt_block_size(name) == opack.BLOCK[name]
+        blk = opack.BLOCK[name]
+        assert q.qfmt_block_size(name) == blk
+        assert q.qfmt_block_size(name, blk) == blk            # the format's own block, stated
         assert q.qfmt_codes_bytes(name, 7, 256) == opack.codes_nbytes(name, 7, 256)
         assert q.qfmt_scales_bytes(name, 7, 256) == opack.scales_nbytes(name, 7, 256)
-    assert q.qfmt_block_size(99) == 0
-    assert q.qfmt_codes_bytes("mxfp4", 4, 48) == -1           # K not a multiple of 32
-    assert q.qfmt_codes_bytes("int4_affine", 4, 80) == -1     # K not a multiple of 32
+        assert q.qfmt_codes_bytes(name, 7, 256, blk) == opack.codes_nbytes(name, 7, 256)
     assert q.qfmt_scales_bytes("int4_affine", 4, 96) == 4 * 2 * 4   # a ragged last group of 32
-    # 32-bit row and column indices: 2^31 rows (or mxfp4x2's 2N planes) are refused
-    assert q.qfmt_codes_bytes("mxfp8_e4m3", 1 << 31, 32) == -1
     assert q.qfmt_codes_bytes("mxfp8_e4m3", (1 << 31) - 1, 32) == ((1 << 31) - 1) * 32
-    assert q.qfmt_codes_bytes("mxfp4x2", 1 << 30, 32) == -1
     assert q.qfmt_codes_bytes("mxfp4x2", (1 << 30) - 1, 32) == ((1 << 30) - 1) * 32
+
+
+def test_size_queries_error_returns(lib):
+    # every size query through the C ABI: 0 (block) or SIZE_MAX (bytes) on an
+    # unknown format, a group the format does not take, or a shape the packer
+    # refuses, with the reason in qfmt_last_error
+    SMAX = q.SIZE_ERROR
+    assert lib.qfmt_block_size(99, 0) == 0 and b"unknown format" in lib.qfmt_last_error()
+    assert lib.qfmt_block_size(1, 64) == 0 and b"group" in lib.qfmt_last_error()
+    assert lib.qfmt_block_size(6, 32) == 0
+    assert lib.qfmt_last_error() != b""
+    assert lib.qfmt_block_size(6, 0) == 64 and lib.qfmt_last_error() == b""
+    for fn in (lib.qfmt_codes_bytes, lib.qfmt_scales_bytes):
+        assert fn(99, 4, 64, 0) == SMAX and b"unknown format" in lib.qfmt_last_error()
+        assert fn(1, 4, 64, 16) == SMAX and b"group" in lib.qfmt_last_error()
+        assert fn(1, 4, 48, 0) == SMAX and b"multiple" in lib.qfmt_last_error()     # K not a multiple of 32
+        assert fn(6, 4, 80, 0) == SMAX                                               # int4 affine too
+        assert fn(1, -1, 64, 0) == SMAX and b"negative" in lib.qfmt_last_error()
+        assert fn(3, 1 << 31, 32, 0) == SMAX                                         # 2^31 code rows
+        assert fn(13, 1 << 30, 32, 0) == SMAX                                        # mxfp4x2: 2N code rows
+        assert fn(1, 0, 64, 0) == 0 and lib.qfmt_last_error() == b""
+    with pytest.raises(q.QfmtError):
+        q.qfmt_codes_bytes("mxfp4", 4, 48)
 
 
 CASES = [
@@ -161,13 +181,15 @@ def test_device_entry_validation_without_gpu(lib):
     assert _call_qmm(lib, fmt=2, g=float("nan")) == -1
     assert _call_qmm(lib, fmt=6, K=80) == -2
     assert b"multiple" in lib.qfmt_last_error()
+    # more 128-row GEMM tiles than the grid's y dimension holds: refused before any launch
+    assert _call_qmm(lib, M=65535 * 128 + 1) == -2
+    assert b"65535" in lib.qfmt_last_error()
     # empty problems are legal no-ops
     assert _call_qmm(lib, M=0) == 0
     assert _call_qmm(lib, N=0) == 0
     assert lib.qfmt_dequant(1, None, None, 1.0, None, 0, 0, 64, 0, None) == 0
     assert lib.qfmt_dequant(1, 0x1000, 0x1000, 1.0, 0x1000, 3, 4, 64, 0, None) == -1
     assert lib.qfmt_dequant(1, 0x1000, 0x1000, 1.0, 0x1004, 0, 4, 64, 0, None) == -3
-    assert lib.qmm_workspace_bytes(1, 16, 16, 64) == 0
 
 
 def _call_gather(lib, **kw):
@@ -235,3 +257,44 @@ def test_batched_and_rmsnorm_validation_without_gpu(lib):
     assert gated(eps=float("nan")) == -1
     assert gated(K=0) == -2
     assert gated(M=0) == 0
+
+
+def test_binding_rejects_bad_tensors_before_the_call(lib):
+    # the binding checks every tensor before a pointer crosses the C ABI:
+    # contiguity, dtype, shape, buffer size, then the device (CPU tensors here,
+    # so every rejection below happens on the host)
+    import torch
+    fmt, n, k = "mxfp4", 8, 64
+    codes = torch.zeros(q.qfmt_codes_bytes(fmt, n, k), dtype=torch.uint8)
+    scales = torch.zeros(q.qfmt_scales_bytes(fmt, n, k), dtype=torch.uint8)
+    x = torch.zeros((2, k), dtype=torch.bfloat16)
+
+    def rejects(fn, *a, match, **kw):
+        with pytest.raises(q.QfmtError) as e:
+            fn(*a, **kw)
+        assert match in str(e.value), (match, str(e.value))
+
+    rejects(q.qmm, fmt, codes, scales, 1.0, x.float(), n, match="must be torch.bfloat16")
+    rejects(q.qmm, fmt, codes, scales, 1.0, torch.zeros((2, 2 * k), dtype=torch.bfloat16)[:, ::2], n,
+            match="contiguous")
+    rejects(q.qmm, fmt, codes, scales, 1.0, torch.zeros((2, 1, k), dtype=torch.bfloat16), n, match="2-D")
+    rejects(q.qmm, fmt, codes[:-1], scales, 1.0, x, n, match="codes holds")
+    rejects(q.qmm, fmt, codes, scales[:-1], 1.0, x, n, match="scales holds")
+    rejects(q.qmm, fmt, codes, scales, 1.0, x, n, out=torch.zeros((2, n), dtype=torch.float32),
+            match="out must be torch.bfloat16")
+    rejects(q.qmm, fmt, codes, scales, 1.0, x, n, out=torch.zeros((2, n + 1), dtype=torch.bfloat16),
+            match="shape")
+    rejects(q.qmm, fmt, codes, scales, 1.0, x, n, match="CUDA tensor")
+    rejects(q.qmm, fmt, codes, scales, 1.0, torch.zeros((2, 48), dtype=torch.bfloat16), n, match="multiple")
+    rejects(q.qmm_ex, fmt, codes, scales, 1.0, x.to(torch.float16), n, match="must be")
+    rejects(q.qfmt_dequant, fmt, codes, scales, 1.0, n, k, out=torch.zeros((n, k), dtype=torch.float16),
+            match="float32 or bfloat16")
+    rejects(q.qmm_gather, fmt, codes, scales, 1.0, x, torch.zeros(2, dtype=torch.int64), n, 1,
+            match="int32")
+    rejects(q.qmm_gather, fmt, codes, scales, 1.0, x, torch.zeros(2, dtype=torch.int32), n, 2,
+            match="codes holds")                                  # two experts need twice the codes
+    rejects(q.qmm_rmsnorm, fmt, codes, scales, 1.0, x, torch.zeros(k + 1, dtype=torch.bfloat16), 1e-5, n,
+            match="norm_weight must have shape")
+    rejects(q.qmm_gated_rmsnorm, fmt, codes, scales, 1.0, x, torch.zeros((2, k), dtype=torch.float32),
+            torch.zeros(k, dtype=torch.bfloat16), 1e-5, n, match="gate must be torch.bfloat16")
+    rejects(q.qmm_batched, fmt, [codes] * 5, [scales] * 5, [1.0] * 5, x, [n] * 5, match="1..4")

@@ -15,6 +15,7 @@ import block_scaled_quantized_spec_gb300 as q  # noqa: E402
 from block_scaled_quantized_spec_gb300 import synth  # noqa: E402
 from oracle import pack as opack  # noqa: E402
 from oracle import reference as oref  # noqa: E402
+from tolerance import check_tensor  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 FMTS = list(q.FORMATS)
@@ -44,11 +45,7 @@ def _case(fmt, m, n, k, e, seed):
 
 
 def _check(out_t, ref, bound, what):
-    out = out_t.float().cpu().numpy().astype(np.float64)
-    err = np.abs(out - ref)
-    ok = err <= bound + np.abs(out) * 2.0 ** -9
-    assert np.isfinite(out).all(), what
-    assert ok.all(), (what, float((err / bound).max()), np.argwhere(~ok)[:5].tolist())
+    return check_tensor(out_t, ref, bound, what)
 
 
 @pytest.mark.parametrize("fmt", FMTS)

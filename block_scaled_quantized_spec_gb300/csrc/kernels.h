@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace qfmt_dev {
@@ -37,6 +38,18 @@ cudaError_t launch_qmm_f32x(int fmt, const void* codes, const void* scales, floa
 cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, float glob,
                             const void* x, void* out, bool out_f32, int64_t M, int64_t N,
                             int64_t K, cudaStream_t st, int sms);
+
+// Block-scaled tensor-core GEMM (tcgen05 kind::mxf8f6f4) for mxfp4 / mxfp8
+// E4M3 / E5M2 weights: X is split into two MXFP8 E4M3 terms in `workspace`
+// (qgemm_mx_workspace_bytes), then both go through the block-scaled MMA
+// against the weights as stored.  M > 16, K a multiple of 128.
+bool qgemm_mx_supported(int fmt, int64_t M, int64_t K);
+size_t qgemm_mx_workspace_bytes(int64_t M, int64_t K);
+cudaError_t launch_qgemm_mx(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
+                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st);
+void set_mx_wait_limit_ns(uint64_t ns);
+void set_mx_drop_arrivals(int on);
+cudaError_t read_and_clear_mx_status(unsigned int* status);
 
 // Bounded-wait test hooks and the device status word of the tensor-core GEMM.
 void set_wait_limit_ns(uint64_t ns);

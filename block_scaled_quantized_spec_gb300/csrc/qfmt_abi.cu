@@ -7,6 +7,7 @@
 // tensor-core GEMM, float32 activations the CUDA-core path.
 #include <atomic>
 #include <cmath>
+#include <cstdint>
 
 #include <cuda_runtime.h>
 
@@ -78,8 +79,6 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale, c
            void* out, int out_dtype, int64_t M, int64_t N, int64_t K, int group, void* workspace,
            size_t workspace_bytes, void* stream) {
   clear_error();
-  (void)workspace;
-  (void)workspace_bytes;
   int st = check_group(fmt, group);
   if (st) return st;
   if ((st = check_shape(fmt, M, N, K))) return st;
@@ -107,6 +106,17 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale, c
     return cuda_status(qfmt_dev::launch_qgemv(fmt, codes, scales, global_scale, x, out, out_f32, M,
                                               weight_rows(fmt, N), K, s, sms),
                        "qgemv launch");
+  // With a workspace, the MX formats the block-scaled MMA reads as stored take
+  // it (the E2M1 codes' tensor map needs a 32-byte aligned base).
+  if (workspace && qfmt_dev::qgemm_mx_supported(fmt, M, K) &&
+      !(fmt == QFMT_MXFP4 && (reinterpret_cast<uintptr_t>(codes) & 31u))) {
+    const size_t need = qfmt_dev::qgemm_mx_workspace_bytes(M, K);
+    if (workspace_bytes < need)
+      return fail(QFMT_ENOSPACE, "workspace of %zu bytes, the block-scaled GEMM needs %zu", workspace_bytes, need);
+    if ((st = check_ptr(workspace, 128, "workspace"))) return st;
+    return cuda_status(qfmt_dev::launch_qgemm_mx(fmt, codes, scales, x, out, out_f32, M, N, K, workspace, s),
+                       "block-scaled qgemm launch");
+  }
   // the GEMM decodes both mxfp4x2 planes of an output row together: N output rows
   return cuda_status(qfmt_dev::launch_qgemm_tc(fmt, codes, scales, global_scale, x, out, out_f32, M, N, K, s, sms),
                      "qgemm launch");
@@ -244,9 +254,11 @@ int qfmt_device_status(void* stream) {
   unsigned int word = 0, gw = 0;
   if ((st = cuda_status(qfmt_dev::read_and_clear_device_status(&word), "device status"))) return st;
   if ((st = cuda_status(qfmt_dev::read_and_clear_gemv_status(&gw), "device status"))) return st;
-  unsigned int gx = 0;
+  unsigned int gx = 0, mw = 0;
   if ((st = cuda_status(qfmt_dev::read_and_clear_gather_status(&gx), "device status"))) return st;
+  if ((st = cuda_status(qfmt_dev::read_and_clear_mx_status(&mw), "device status"))) return st;
   if (word) return fail(QFMT_ETIMEOUT, "a tensor-core GEMM pipeline wait expired (status 0x%x)", word);
+  if (mw) return fail(QFMT_ETIMEOUT, "a block-scaled GEMM pipeline wait expired (status 0x%x)", mw);
   if (gw) return fail(QFMT_ETIMEOUT, "a GEMV weight-copy wait expired (status 0x%x)", gw);
   if (gx) return fail(QFMT_EINDEX, "qmm_gather: an expert index outside [0, E) (its output row was zeroed)");
   return QFMT_OK;
@@ -256,18 +268,21 @@ int qfmt_debug_set(int key, int64_t value) {
   clear_error();
   if (key == 1) {
     qfmt_dev::set_wait_limit_ns(value > 0 ? uint64_t(value) : 2000000000ull);
+    qfmt_dev::set_mx_wait_limit_ns(value > 0 ? uint64_t(value) : 2000000000ull);
     return QFMT_OK;
   }
   if (key == 2) {
     qfmt_dev::set_drop_arrivals(value ? 1 : 0);
+    qfmt_dev::set_mx_drop_arrivals(value ? 1 : 0);
     return QFMT_OK;
   }
   return fail(QFMT_EINVAL, "unknown debug key %d", key);
 }
 
 size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t K) {
-  (void)fmt; (void)M; (void)K;
-  return 0;
+  clear_error();
+  if (!valid_format(fmt) || M < 0 || K < 0) return 0;
+  return qfmt_dev::qgemm_mx_supported(fmt, M, K) ? qfmt_dev::qgemm_mx_workspace_bytes(M, K) : 0;
 }
 
 }  // extern "C"

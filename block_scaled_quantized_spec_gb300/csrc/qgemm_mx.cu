@@ -1,0 +1,570 @@
+// Prefill GEMM on the block-scaled tensor cores (tcgen05.mma kind::mxf8f6f4),
+// the weights fed as stored, M > 16:
+//   out[M, N] = X[M, K] (bf16) . dequant(W[N, K])^T, float32 accumulation,
+// for the MX formats whose element the hardware reads directly: mxfp4 (E2M1),
+// mxfp8 E4M3 and E5M2, each with an E8M0 scale per 32 along K.
+//
+// The block-factored value it computes is rlx-cpu thunk/ops/quant.rs
+// lowp_scaled_matmul: per K block, acc += (a_s . b_s) . sum_k dec(a) dec(b),
+// with both operands block-scaled; metaltile PR #250 names Blackwell tcgen05
+// scaled-MMA (MXFP) as the CUDA payoff of its formats.  Here the activation
+// side is made block-scaled exactly enough for the bf16 contract:
+//
+//  * xquant (one kernel) splits X into two MXFP8 E4M3 terms per block of 32:
+//      s1 = 2^e1, the smallest power of two with amax(x) <= 448 s1;
+//      hi = E4M3_rne_sat(x / s1);  r = x - hi s1 (exact in float32);
+//      s2 = 2^e2 from amax(r) the same way;  lo = E4M3_rne_sat(r / s2).
+//    A bf16 value has 8 significant bits and hi keeps the top 4 (rounded), so
+//    r has at most 3 and hi s1 + lo s2 = x exactly whenever hi and lo are
+//    normal E4M3 values (x within 2^14 of its block's largest); smaller values
+//    carry an absolute error below 2^-21 amax of the block.  The codes go to
+//    the workspace as [M, K] bytes (hi, then lo) and the scales as 512-byte
+//    atoms of 128 rows x 4 K blocks (umma::sf_atom_offset), the layout
+//    tcgen05.cp copies into tensor memory.
+//  * the GEMM kernel, CTA tile 128 (M) x 256 (N), K step 128, three stages:
+//      warp 0  one thread issues TMA loads of the hi and lo X tiles and the W
+//              code tile (128B-swizzled, K-major; E2M1 codes through the
+//              16U4_ALIGN16B type, which places 16 codes in each 16-byte
+//              unit's low 8 bytes, the layout kind::mxf8f6f4 reads for E2M1)
+//              and bulk-copies the two X scale atoms; it owns the TMEM
+//              allocation;
+//      warp 1  one thread copies the stage's scale atoms into tensor memory
+//              (tcgen05.cp .32x128b.warpx4) and issues, per K block of 32,
+//              two MMAs into one accumulator: hi . W under (s1, s_w) and
+//              lo . W under (s2, s_w);
+//      warp 2  gathers the stage's W scales (one 32-bit word = 4 K blocks per
+//              row) into two scale atoms in shared memory;
+//      warps 4-7 drain the accumulator (tcgen05.ld) and store bf16/float32.
+//
+// Every mbarrier wait is bounded; on expiry the kernel records it in the
+// device status word, lets issued copies and MMAs land, frees its tensor
+// memory and exits without writing its tile.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "decode.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace qfmt_dev {
+
+__device__ unsigned int g_mx_status;
+
+namespace mx {
+
+using namespace tc;
+
+constexpr int BM = 128, BN = 256, BK = 128;   // BK: K elements (= bytes of an 8-bit code row) per stage
+constexpr int STAGES = 3;
+constexpr int A_BYTES = BM * BK;              // 16 KiB: one X term
+constexpr int B_BYTES = BN * BK;              // 32 KiB: 256 rows of 128 codes (E2M1: 16 in each 16-byte unit)
+constexpr int SF_BYTES = 512;                 // one scale atom: 128 rows x 4 K blocks
+constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
+constexpr int SF_STAGE = 4 * SF_BYTES;        // hi atom, lo atom, two W atoms (rows 0-127, 128-255)
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGES * SF_STAGE + 256;
+constexpr int THREADS = 256;
+constexpr int TMEM_COLS = 512;                // accumulator 256 columns + 16 scale columns a stage
+constexpr int SF_COL0 = 256;
+
+// Workspace layout (bytes) for M rows and K columns: hi codes, lo codes, hi
+// scale atoms, lo scale atoms; each part 1024-byte aligned.
+struct WsLayout {
+  size_t hi, lo, sf_hi, sf_lo, total;
+};
+inline size_t align1k(size_t v) { return (v + 1023) & ~size_t(1023); }
+inline WsLayout ws_layout(int64_t M, int64_t K) {
+  WsLayout w;
+  const size_t codes = size_t(M) * size_t(K);
+  const size_t sf = size_t((M + BM - 1) / BM) * size_t(K / BK) * SF_BYTES;
+  w.hi = 0;
+  w.lo = align1k(codes);
+  w.sf_hi = w.lo + align1k(codes);
+  w.sf_lo = w.sf_hi + align1k(sf);
+  w.total = w.sf_lo + align1k(sf);
+  return w;
+}
+
+// --------------------------------------------------------------- xquant ---
+
+// E8M0 exponent of the smallest power of two s with amax <= 448 s, from the
+// float32 bits of amax (>= 0, finite): amax = 1.m 2^E fits 448 2^(E-8) =
+// 1.75 2^E when 1.m <= 1.75, else takes 2^(E-7); below 2^-119 the smallest
+// scale 2^-127 already fits.  Returns the biased byte (e + 127).
+__device__ __forceinline__ uint32_t e8m0_for_e4m3(float amax) {
+  const uint32_t a = __float_as_uint(amax);
+  if (a >= 0x7F800000u) return 255u;                       // Inf / NaN in the block: a NaN scale
+  if (a < 0x04000000u) return 0u;
+  const int e = int(a >> 23) - 127 - 8 + ((a & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  return uint32_t(min(max(e, -127), 127) + 127);
+}
+
+// 2^-(b - 127) as a float32 (b <= 254): the exact reciprocal of the scale.
+__device__ __forceinline__ float e8m0_recip(uint32_t b) {
+  const int e = 127 - int(b);                               // exponent of the reciprocal, -127 .. 127
+  return e >= -126 ? __uint_as_float(uint32_t(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Two float32 -> two E4M3 bytes (round to nearest even, saturating to +-448),
+// `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
+  return h;
+}
+
+// Two E4M3 bytes (low byte first) -> their values as float32 (exact).
+__device__ __forceinline__ void e4m3x2_f32(uint32_t two, float& lo, float& hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(uint16_t(two)));
+  lo = __half2float(__ushort_as_half(uint16_t(r & 0xFFFFu)));
+  hi = __half2float(__ushort_as_half(uint16_t(r >> 16)));
+}
+
+// One warp per (row, 32 consecutive blocks of 32): lane l takes block b0 + l.
+// Rows past M (up to the 128-row tile) get neutral scale words only.
+__global__ void __launch_bounds__(256) xquant_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ ws,
+                                                     WsLayout lay, int M, int K) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nblk = K / 32, chunks = (nblk + 31) / 32;
+  const int mpad = (M + BM - 1) / BM * BM;
+  const int m = warp / chunks, b = (warp - m * chunks) * 32 + lane;
+  if (m >= mpad) return;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const bool live = b < nblk;
+  uint32_t c1 = 127u, c2 = 127u;
+  if (live && m < M) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + int64_t(m) * K + int64_t(b) * 32);
+    uint32_t w[16];
+    #pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = __ldg(src + i);
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+    float v[32];
+    float amax = 0.0f;
+    #pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+    }
+    // an infinity gives the block the NaN scale (255); a NaN element (which
+    // fmaxf passes over) stays a NaN code: either way its outputs are NaN
+    c1 = e8m0_for_e4m3(amax);
+    const float s1 = e8m0_f32(c1), r1 = c1 == 255u ? 0.0f : e8m0_recip(c1);
+    uint32_t hi[8], lo[8];
+    float ramax = 0.0f;
+    #pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t h = e4m3x2(__fmul_rn(v[2 * i], r1), __fmul_rn(v[2 * i + 1], r1));
+      float h0, h1;
+      e4m3x2_f32(h, h0, h1);
+      v[2 * i] = __fmaf_rn(-h0, s1, v[2 * i]);               // exact residuals
+      v[2 * i + 1] = __fmaf_rn(-h1, s1, v[2 * i + 1]);
+      ramax = fmaxf(ramax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+      if (i & 1) hi[i >> 1] |= h << 16;
+      else hi[i >> 1] = h;
+    }
+    c2 = c1 == 255u ? 255u : e8m0_for_e4m3(ramax);
+    const float r2 = c2 == 255u ? 0.0f : e8m0_recip(c2);
+    #pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t l = e4m3x2(__fmul_rn(v[2 * i], r2), __fmul_rn(v[2 * i + 1], r2));
+      if (i & 1) lo[i >> 1] |= l << 16;
+      else lo[i >> 1] = l;
+    }
+    uint4* dh = reinterpret_cast<uint4*>(ws + lay.hi + size_t(m) * K + size_t(b) * 32);
+    uint4* dl = reinterpret_cast<uint4*>(ws + lay.lo + size_t(m) * K + size_t(b) * 32);
+    dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+  }
+  // four blocks of one row share a 32-bit scale cell of the atom
+  uint32_t w1 = c1, w2 = c2;
+  #pragma unroll
+  for (int d = 1; d < 4; ++d) {
+    w1 |= __shfl_down_sync(0xFFFFFFFFu, c1, d) << (8 * d);
+    w2 |= __shfl_down_sync(0xFFFFFFFFu, c2, d) << (8 * d);
+  }
+  if (live && (lane & 3) == 0) {
+    const size_t atom = size_t(m / BM) * size_t(K / BK) + size_t(b / 4);
+    const uint32_t off = umma::sf_atom_offset(uint32_t(m % BM), 0);
+    *reinterpret_cast<uint32_t*>(ws + lay.sf_hi + atom * SF_BYTES + off) = w1;
+    *reinterpret_cast<uint32_t*>(ws + lay.sf_lo + atom * SF_BYTES + off) = w2;
+  }
+}
+
+// ----------------------------------------------------------------- GEMM ---
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+struct MxParams {
+  const uint8_t* wscales;   // [N, K/32] E8M0
+  const uint8_t* sf_hi;     // X scale atoms (workspace)
+  const uint8_t* sf_lo;
+  void* out;
+  int M, N, K;
+  int out_f32;
+  uint64_t limit_ns;
+  int drop_arrivals;
+};
+
+template <int F> constexpr uint32_t b_type() {
+  return F == MXFP4 ? umma::F8F6F4_E2M1 : (F == MXFP8_E5M2 ? umma::F8F6F4_E5M2 : umma::F8F6F4_E4M3);
+}
+
+template <int F>
+__global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_constant__ CUtensorMap xhi_map,
+                                                              const __grid_constant__ CUtensorMap xlo_map,
+                                                              const __grid_constant__ CUtensorMap w_map,
+                                                              const MxParams p) {
+  // bytes a stage's copies deliver: the two X terms, the W codes (E2M1: the
+  // 8 data bytes of every 16-byte unit, the gaps are not written) and the two
+  // X scale atoms
+  constexpr uint32_t TX_BYTES = 2 * A_BYTES + (F == MXFP4 ? B_BYTES / 2 : B_BYTES) + 2 * SF_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sf_area = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_area + STAGES * SF_STAGE);
+  // bars[0..S): stage copies landed (TMA and bulk bytes), [S..2S): stage W scales written (the scale warp),
+  // [2S..3S): stage empty (MMA commit), [3S]: accumulator done
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 3 * STAGES + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int nk = p.K / BK;
+  const uint32_t sbase = smem_u32(smem), sfbase = smem_u32(sf_area), bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto sf_full = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  const uint32_t done_bar = bar0 + 8u * (3 * STAGES);
+  auto a_hi = [&](int s) { return sbase + uint32_t(s * STAGE_BYTES); };
+  auto a_lo = [&](int s) { return sbase + uint32_t(s * STAGE_BYTES + A_BYTES); };
+  auto b_tile = [&](int s) { return sbase + uint32_t(s * STAGE_BYTES + 2 * A_BYTES); };
+  auto sf_s = [&](int s, int i) { return sfbase + uint32_t(s * SF_STAGE + i * SF_BYTES); };   // i: 0 hi, 1 lo, 2-3 W
+  auto fail = [&]() {
+    *abort_flag = 1u;
+    atomicOr(&g_mx_status, 1u);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(sf_full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xhi_map)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xlo_map)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&w_map)) : "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((const void*)tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");   // the workspace comes from the preceding xquant
+      const uint8_t* sfh = p.sf_hi + size_t(blockIdx.y) * size_t(nk) * SF_BYTES;
+      const uint8_t* sfl = p.sf_lo + size_t(blockIdx.y) * size_t(nk) * SF_BYTES;
+      int issued = 0;
+      for (int j = 0; j < nk; ++j) {
+        const int s = j % STAGES;
+        const uint32_t ph = (j / STAGES) & 1;
+        if (*abort_flag) break;
+        if (!mbar_wait(empty(s), ph ^ 1u, p.limit_ns)) { fail(); break; }
+        mbar_arrive_expect_tx(full(s), TX_BYTES);
+        tma_load_2d(a_hi(s), &xhi_map, j * BK, m0, full(s));
+        tma_load_2d(a_lo(s), &xlo_map, j * BK, m0, full(s));
+        tma_load_2d(b_tile(s), &w_map, j * BK, n0, full(s));
+        bulk_load(sf_s(s, 0), sfh + size_t(j) * SF_BYTES, SF_BYTES, full(s));
+        bulk_load(sf_s(s, 1), sfl + size_t(j) * SF_BYTES, SF_BYTES, full(s));
+        issued = j + 1;
+      }
+      // every issued copy lands before the CTA may exit
+      for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+        if (!mbar_wait(full(j % STAGES), (j / STAGES) & 1, p.limit_ns)) fail();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t BT = b_type<F>();
+      for (int j = 0; j < p.K / BK; ++j) {
+        const int s = j % STAGES;
+        const uint32_t ph = (j / STAGES) & 1;
+        if (*abort_flag) break;
+        if (!mbar_wait(full(s), ph, p.limit_ns) || !mbar_wait(sf_full(s), ph, p.limit_ns)) { fail(); break; }
+        tc_fence_after();
+        const uint32_t sfc = tmem + uint32_t(SF_COL0 + 16 * s);   // hi: +0, lo: +4, W: +8 (rows 0-127), +12 (128-255)
+        tmem_cp_sf(sfc + 0, umma::smem_desc_sf32x16(sf_s(s, 0)));
+        tmem_cp_sf(sfc + 4, umma::smem_desc_sf32x16(sf_s(s, 1)));
+        tmem_cp_sf(sfc + 8, umma::smem_desc_sf32x16(sf_s(s, 2)));
+        tmem_cp_sf(sfc + 12, umma::smem_desc_sf32x16(sf_s(s, 3)));
+        const uint64_t dh = desc_sw128(a_hi(s)), dl = desc_sw128(a_lo(s)), db = desc_sw128(b_tile(s));
+        #pragma unroll
+        for (int kk = 0; kk < BK / 32; ++kk) {   // +32 bytes along K per instruction
+          const uint32_t id = umma::idesc_mxf8f6f4(umma::F8F6F4_E4M3, BT, BM, BN, uint32_t(kk), uint32_t(kk));
+          mma_mx(tmem, dh + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 0, sfc + 8, (j | kk) != 0);
+          mma_mx(tmem, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 4, sfc + 8, 1u);
+        }
+        mma_commit(empty(s));
+      }
+      mma_commit(done_bar);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------- W scales -> scale atoms
+    // lane l gathers rows n0 + l + 32 i (i = 0..7): the 4 E8M0 bytes of K
+    // blocks 4j..4j+3 are one aligned 32-bit word of the row (K % 128 == 0)
+    const int row_words = p.K / 128;
+    const uint32_t* ws32 = reinterpret_cast<const uint32_t*>(p.wscales);
+    auto load = [&](int j, uint32_t (&v)[8]) {
+      #pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int n = n0 + lane + 32 * i;
+        v[i] = (j < nk && n < p.N) ? __ldg(ws32 + int64_t(n) * row_words + j) : 0u;
+      }
+    };
+    uint32_t cur[8], nxt[8];
+    load(0, cur);
+    load(1, nxt);
+    for (int j = 0; j < nk; ++j) {
+      const int s = j % STAGES;
+      const uint32_t ph = (j / STAGES) & 1;
+      int ok = 1;
+      if (lane == 0) ok = (*abort_flag == 0u) && mbar_wait(empty(s), ph ^ 1u, p.limit_ns);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0 && *abort_flag == 0u) fail();
+        break;
+      }
+      uint32_t nx2[8];
+      load(j + 2, nx2);
+      #pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t dst = sf_s(s, 2 + i / 4) + umma::sf_atom_offset(uint32_t(lane + 32 * (i % 4)), 0);
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst), "r"(cur[i]) : "memory");
+        cur[i] = nxt[i];
+        nxt[i] = nx2[i];
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0 && !p.drop_arrivals) mbar_arrive(sf_full(s));
+    }
+  } else if (warp >= 4) {
+    // --------------------------------------------------------------- epilogue
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(done_bar, 0, p.limit_ns);
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok && lane == 0) fail();
+    tc_fence_after();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int q = warp & 3;
+    const int m = m0 + q * 32 + lane;
+    const bool live = ok && *abort_flag == 0u;
+    #pragma unroll 1
+    for (int cb = 0; cb < BN / 32; ++cb) {
+      uint32_t r[32];
+      tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(cb * 32), r);
+      const int nb = n0 + cb * 32;
+      if (!live || m >= p.M || nb >= p.N) continue;
+      const int ncols = p.N - nb < 32 ? p.N - nb : 32;
+      if (p.out_f32) {
+        float* o = static_cast<float*>(p.out) + int64_t(m) * p.N + nb;
+        if (ncols == 32 && (p.N & 3) == 0) {
+          #pragma unroll
+          for (int j = 0; j < 8; ++j)
+            reinterpret_cast<float4*>(o)[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        } else {
+          for (int j = 0; j < ncols; ++j) o[j] = __uint_as_float(r[j]);
+        }
+      } else {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + int64_t(m) * p.N + nb;
+        if (ncols == 32 && (p.N & 7) == 0) {
+          #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t h[4];
+            #pragma unroll
+            for (int t = 0; t < 4; ++t)
+              h[t] = f32_to_bf16bits(__uint_as_float(r[8 * j + 2 * t])) |
+                     (f32_to_bf16bits(__uint_as_float(r[8 * j + 2 * t + 1])) << 16);
+            reinterpret_cast<uint4*>(o)[j] = make_uint4(h[0], h[1], h[2], h[3]);
+          }
+        } else {
+          for (int j = 0; j < ncols; ++j) o[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host ---
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// A K-major [rows, K] map with 128-element x `box_rows` boxes, 128B swizzle.
+static bool make_map(EncodeTiledFn enc, CUtensorMap* map, CUtensorMapDataType dt, const void* base, int64_t K,
+                     int64_t rows, int64_t row_bytes, uint32_t box_rows) {
+  const cuuint64_t gdim[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  const cuuint64_t gstride[1] = {cuuint64_t(row_bytes)};
+  const cuuint32_t box[2] = {cuuint32_t(BK), box_rows};
+  const cuuint32_t estride[2] = {1, 1};
+  return enc(map, dt, 2, const_cast<void*>(base), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+static std::atomic<uint64_t> g_limit_ns{2000000000ull};
+static std::atomic<int> g_drop{0};
+
+template <int F>
+static cudaError_t launch_fmt(const void* codes, const void* scales, const void* x, void* out, bool out_f32, int M,
+                              int N, int K, void* ws, cudaStream_t st) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  static std::atomic<int> attr_done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
+    e = cudaFuncSetAttribute(qgemm_mx_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done[dev].store(1);
+  }
+  const WsLayout lay = ws_layout(M, K);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  // activations -> hi / lo MXFP8 terms (one warp per row and 1024 columns)
+  {
+    const int mpad = (M + BM - 1) / BM * BM;
+    const int64_t warps = int64_t(mpad) * ((K / 32 + 31) / 32);
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.gridDim = dim3(unsigned((warps + 7) / 8));
+    lc.blockDim = dim3(256);
+    lc.stream = st;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&lc, xquant_kernel, static_cast<const __nv_bfloat16*>(x), w8, lay, M, K);
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap mhi, mlo, mw;
+  if (!make_map(enc, &mhi, CU_TENSOR_MAP_DATA_TYPE_UINT8, w8 + lay.hi, K, M, K, BM) ||
+      !make_map(enc, &mlo, CU_TENSOR_MAP_DATA_TYPE_UINT8, w8 + lay.lo, K, M, K, BM))
+    return cudaErrorInvalidValue;
+  const bool ok = F == MXFP4
+                      ? make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, K, N, K / 2, BN)
+                      : make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, N, K, BN);
+  if (!ok) return cudaErrorInvalidValue;
+  MxParams prm;
+  prm.wscales = static_cast<const uint8_t*>(scales);
+  prm.sf_hi = w8 + lay.sf_hi;
+  prm.sf_lo = w8 + lay.sf_lo;
+  prm.out = out;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.out_f32 = out_f32 ? 1 : 0;
+  prm.limit_ns = g_limit_ns.load();
+  prm.drop_arrivals = g_drop.load();
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.gridDim = dim3((N + BN - 1) / BN, (M + BM - 1) / BM);
+  lc.blockDim = dim3(THREADS);
+  lc.dynamicSmemBytes = SMEM_BYTES;
+  lc.stream = st;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, qgemm_mx_kernel<F>, mhi, mlo, mw, prm);
+}
+
+}  // namespace mx
+
+bool qgemm_mx_supported(int fmt, int64_t M, int64_t K) {
+  return (fmt == MXFP4 || fmt == MXFP8_E4M3 || fmt == MXFP8_E5M2) && M > 16 && K > 0 && K % mx::BK == 0;
+}
+
+size_t qgemm_mx_workspace_bytes(int64_t M, int64_t K) { return mx::ws_layout(M, K).total; }
+
+cudaError_t launch_qgemm_mx(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
+                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st) {
+  const int m = int(M), n = int(N), k = int(K);
+  switch (fmt) {
+    case MXFP4: return mx::launch_fmt<MXFP4>(codes, scales, x, out, out_f32, m, n, k, workspace, st);
+    case MXFP8_E4M3: return mx::launch_fmt<MXFP8_E4M3>(codes, scales, x, out, out_f32, m, n, k, workspace, st);
+    case MXFP8_E5M2: return mx::launch_fmt<MXFP8_E5M2>(codes, scales, x, out, out_f32, m, n, k, workspace, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+void set_mx_wait_limit_ns(uint64_t ns) { mx::g_limit_ns.store(ns); }
+void set_mx_drop_arrivals(int on) { mx::g_drop.store(on); }
+
+cudaError_t read_and_clear_mx_status(unsigned int* status) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, g_mx_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_mx_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace qfmt_dev

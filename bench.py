@@ -46,8 +46,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-breakdown", action="store_true")
-    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K, gather:fmt:M:N:K:E, batched:fmt:M:N1,N2:K, rmsnorm:fmt:M:N:K "
-                   "or gated_rmsnorm:fmt:M:N:K")
+    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K[:A], gather:fmt:M:N:K:E, batched:fmt:M:N1,N2:K, "
+                   "rmsnorm:fmt:M:N:K, gated_rmsnorm:fmt:M:N:K or dequant:fmt:N:K:f32|bf16")
     return p.parse_args()
 
 
@@ -160,9 +160,14 @@ def job_throughput(per_rank_bytes, per_rank_ms, world):
 
 
 class Problem:
-    """L copies of one packed weight in HBM, their activations and outputs."""
+    """L copies of one packed weight in HBM, their activations and outputs.
 
-    def __init__(self, fmt, m, n, k, copies, seed=0):
+    path "auto": a workspace when the call can use one (the block-scaled
+    tensor-core GEMM of the MX formats, M > 16), the call a user makes with
+    one; "A": no workspace (the bf16-decode GEMM).
+    """
+
+    def __init__(self, fmt, m, n, k, copies, seed=0, path="auto"):
         import numpy as np
         import torch
         import block_scaled_quantized_spec_gb300 as q
@@ -185,11 +190,20 @@ class Problem:
         self.copies = copies
         self.bytes = sizes(fmt, m, n, k)
         self.flops = 2.0 * m * n * k
+        wsb = q.qmm_workspace_bytes(fmt, m, k) if path == "auto" else 0
+        # one workspace serves every layer: each call's activation split waits
+        # for the previous call to finish before it writes
+        self.ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+        self.path = "B" if wsb else ("A" if m > 16 else "GEMV")
 
     def step(self):
         import block_scaled_quantized_spec_gb300 as q
         for i in range(self.copies):
-            q.qmm(self.fmt, self.codes[i], self.scales[i], self.g, self.x[i], self.n, out=self.out[i])
+            if self.ws is not None:
+                q.qmm_ex(self.fmt, self.codes[i], self.scales[i], self.g, self.x[i], self.n, out=self.out[i],
+                         workspace=self.ws)
+            else:
+                q.qmm(self.fmt, self.codes[i], self.scales[i], self.g, self.x[i], self.n, out=self.out[i])
 
     def graph(self):
         import torch
@@ -429,7 +443,22 @@ BREAKDOWN = [
     ("mxfp4x2", 1, 4096, 4096), ("mxfp4x2", 2048, 4096, 4096),
     ("mxint4", 1, 4096, 4096), ("mxint4", 2048, 4096, 4096),
     ("fp4", 1, 4096, 4096), ("fp8_e5m2", 1, 11008, 4096), ("fp8_e4m3", 2048, 4096, 4096),
+    # the MX formats' GEMM rows again without a workspace (the bf16-decode GEMM), and mxfp4's prefill GEMM
+    ("mxfp8_e4m3", 2048, 4096, 4096, "A"), ("mxfp8_e5m2", 128, 11008, 4096, "A"),
+    ("mxfp8_e5m2", 4096, 11008, 4096, "A"),
+    ("mxfp4", 2048, 4096, 4096), ("mxfp4", 2048, 4096, 4096, "A"),
 ]
+
+# The standalone dequant kernel: [4096, 4096] weights to float32 and bf16.
+DEQUANT = [("mxfp4", 4096, 4096, "f32"), ("mxfp4", 4096, 4096, "bf16"), ("nvfp4", 14336, 4096, "f32"),
+           ("mxfp8_e4m3", 4096, 4096, "f32")]
+
+# The five workloads of the method, each timed once through the CPU oracle
+# (a bounded sample: whole calls within a small budget, at least one).
+ORACLE_CONFIGS = [("mxfp4", 8, 16, 512, "f32"), ("mxfp4", 1, 4096, 4096, "bf16"),
+                  ("nvfp4", 1, 14336, 4096, "bf16"), ("nvfp4", 8, 14336, 4096, "bf16"),
+                  ("mxfp8_e4m3", 2048, 4096, 4096, "bf16")] + \
+                 [(f, mm, 11008, 4096, "bf16") for f in ("int4_affine", "mxfp8_e5m2", "nvfp8") for mm in (1, 16, 128, 4096)]
 
 
 # Expert-routed rows (MoE gather-qmm): one token's top-8 routing over 8 experts
@@ -555,16 +584,87 @@ def gather_row(fmt, m, n, k, e, hbm, steps=10, warmup=3):
     return row
 
 
-def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3):
+class DequantProblem:
+    """L copies of one packed weight and their dequantized outputs."""
+
+    def __init__(self, fmt, n, k, out_dtype, copies, seed=0):
+        import numpy as np
+        import torch
+        import block_scaled_quantized_spec_gb300 as q
+        from block_scaled_quantized_spec_gb300 import synth
+        self.fmt, self.n, self.k = fmt, n, k
+        c, s, g = q.qfmt_pack(fmt, synth.weights(n, k, seed=seed, outliers=(fmt == "nvfp4")))
+        self.g = g
+        dc, ds = torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda()
+        self.codes = [dc] + [dc.clone() for _ in range(copies - 1)]
+        self.scales = [ds] + [ds.clone() for _ in range(copies - 1)]
+        dt = torch.float32 if out_dtype == "f32" else torch.bfloat16
+        self.out = [torch.empty((n, k), dtype=dt, device="cuda") for _ in range(copies)]
+        self.copies = copies
+        self.bytes = q.qfmt_codes_bytes(fmt, n, k) + q.qfmt_scales_bytes(fmt, n, k) + n * k * (4 if dt == torch.float32 else 2)
+
+    def step(self):
+        import block_scaled_quantized_spec_gb300 as q
+        for i in range(self.copies):
+            q.qfmt_dequant(self.fmt, self.codes[i], self.scales[i], self.g, self.n, self.k, out=self.out[i])
+
+    graph = Problem.graph
+
+
+def dequant_row(fmt, n, k, out_dtype, hbm, steps=10, warmup=3):
+    import torch
+    import block_scaled_quantized_spec_gb300 as q
+    per_call = q.qfmt_codes_bytes(fmt, n, k) + q.qfmt_scales_bytes(fmt, n, k) + n * k * (4 if out_dtype == "f32" else 2)
+    copies = max(2, -(-3 * L2_BYTES // per_call))
+    prob = DequantProblem(fmt, n, k, out_dtype, copies)
+    g = prob.graph()
+    ms, _ = time_graph(g, steps, warmup, 1)
+    per = ms / copies
+    gbs = prob.bytes / (per * 1e-3) / 1e9
+    row = {"op": "qfmt_dequant", "fmt": fmt, "N": n, "K": k, "out": out_dtype, "us": round(per * 1e3, 2),
+           "copies": copies, "GB/s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4), "bytes": prob.bytes}
+    del prob, g
+    torch.cuda.empty_cache()
+    return row
+
+
+def oracle_per_config(budget_s=1.0):
+    """The CPU oracle timed on each workload of the method: median of whole calls within the budget."""
+    rows = []
+    for fmt, m, n, k, xd in ORACLE_CONFIGS:
+        import numpy as np
+        from block_scaled_quantized_spec_gb300 import synth
+        from oracle import pack as opack
+        from oracle import reference as oref
+        rng = np.random.default_rng(0)
+        c, s, g = opack.pack(fmt, synth.weights(n, k, rng=rng, outliers=(fmt == "nvfp4")))
+        x = synth.activations_f32(m, k, rng=rng) if xd == "f32" else synth.activations_bf16(m, k, rng=rng)
+        times = []
+        t_end = time.perf_counter() + budget_s
+        while not times or time.perf_counter() < t_end:
+            t0 = time.perf_counter()
+            oref.qmm_ref(fmt, c, s, g, x, xd, m, n, k)
+            times.append(time.perf_counter() - t0)
+        t = statistics.median(times)
+        nbytes = opack.codes_nbytes(fmt, n, k) + opack.scales_nbytes(fmt, n, k) + (4 if xd == "f32" else 2) * (m * k + m * n)
+        rows.append({"fmt": fmt, "M": m, "N": n, "K": k, "calls": len(times), "ms": round(t * 1e3, 2),
+                     "GB/s": round(nbytes / t / 1e9, 4), "GFLOP/s": round(2.0 * m * n * k / t / 1e9, 2)})
+    return {"kind": "oracle", "cores": _blas_threads(), "host_cpus": os.cpu_count(), "rows": rows,
+            "note": "numpy decode (single-threaded) + float64 BLAS matmul; the result and its error bound per call"}
+
+
+def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3, path="auto"):
     import torch
     nbytes = sizes(fmt, m, n, k)
     copies = copies_for(nbytes, m)
-    prob = Problem(fmt, m, n, k, copies)
+    prob = Problem(fmt, m, n, k, copies, path=path)
     g = prob.graph()
     ms, _ = time_graph(g, steps, warmup, 1)
     per = ms / copies
     prob_flops_per_byte = prob.flops / nbytes
-    row = {"fmt": fmt, "M": m, "N": n, "K": k, "us": round(per * 1e3, 2), "copies": copies}
+    row = {"fmt": fmt, "M": m, "N": n, "K": k, "us": round(per * 1e3, 2), "copies": copies,
+           "path": {"B": "block-scaled tcgen05 GEMM (X split + kind::mxf8f6f4)", "A": "bf16-decode tcgen05 GEMM",
+                    "GEMV": "decode GEMV"}[prob.path]}
     gbs = nbytes / (per * 1e-3) / 1e9
     tfl = prob.flops / (per * 1e-3) / 1e12
     row["GB/s"] = round(gbs, 1)
@@ -612,9 +712,13 @@ def main():
             ns = tuple(int(v) for v in nn.split(","))
             print(json.dumps(fused_row(parts[0], f, int(mm), ns, int(kk), hbm, args.steps, args.warmup)))
             return
-        f, mm, nn, kk = parts
+        if parts[0] == "dequant":         # dequant:fmt:N:K:f32|bf16
+            f, nn, kk, od = parts[1:]
+            print(json.dumps(dequant_row(f, int(nn), int(kk), od, hbm, args.steps, args.warmup)))
+            return
+        f, mm, nn, kk = parts[:4]         # fmt:M:N:K[:A]
         print(json.dumps(breakdown_row(f, int(mm), int(nn), int(kk), hbm, bf16, kind, args.steps,
-                                       args.warmup)))
+                                       args.warmup, path=parts[4] if len(parts) > 4 else "auto")))
         return
     prob = Problem(fmt, m, n, k, copies, seed=rank)
     graph = prob.graph()
@@ -645,8 +749,11 @@ def main():
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_breakdown and world == 1:
         rows = []
-        for (f, mm, nn, kk) in BREAKDOWN:
-            rows.append(breakdown_row(f, mm, nn, kk, hbm, bf16, kind))
+        for row in BREAKDOWN:
+            f, mm, nn, kk = row[:4]
+            rows.append(breakdown_row(f, mm, nn, kk, hbm, bf16, kind, path=row[4] if len(row) > 4 else "auto"))
+        for (f, nn, kk, od) in DEQUANT:
+            rows.append(dequant_row(f, nn, kk, od, hbm))
         for (f, mm, nn, kk, ee) in GATHER:
             rows.append(gather_row(f, mm, nn, kk, ee, hbm))
         for (kind, f, mm, ns, kk) in FUSED:
@@ -654,6 +761,8 @@ def main():
         line["breakdown"] = rows
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(fmt, m, n, k)
+        if not args.no_breakdown:
+            line["cpu_baseline_per_config"] = oracle_per_config()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

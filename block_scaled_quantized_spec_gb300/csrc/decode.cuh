@@ -453,12 +453,15 @@ __device__ __forceinline__ void decode_piece(const uint4& v, const PieceScale& p
         A[j][0] = hmul2(A[j][0], m2);
         A[j][1] = hmul2(A[j][1], m2);
       }
-      if constexpr (!is_int8<F>()) {
-        // a NaN / Inf code (outside the packer's range): its value times the
-        // block scale in float32, rounded to bf16 (NaN, or +-inf)
-        const uint32_t sm = special8_mask<F>(w[j]);
-        if (sm) {
-          const float s = is_mx8<F>() ? e8m0_f32(ps.a) : __uint_as_float(ps.a);
+    }
+    if constexpr (!is_int8<F>()) {
+      // a NaN / Inf code (outside the packer's range; one test per piece):
+      // its value times the block scale in float32, rounded to bf16
+      if (special8_mask<F>(w[0]) | special8_mask<F>(w[1]) | special8_mask<F>(w[2]) | special8_mask<F>(w[3])) {
+        const float s = is_mx8<F>() ? e8m0_f32(ps.a) : __uint_as_float(ps.a);
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t sm = special8_mask<F>(w[j]);
           #pragma unroll
           for (int i = 0; i < 4; ++i) {
             if (!(sm & (0x80u << (8 * i)))) continue;

@@ -20,7 +20,7 @@ __all__ = [
     "FORMATS", "QfmtError", "load", "lib_path",
     "qfmt_block_size", "qfmt_codes_bytes", "qfmt_scales_bytes",
     "qfmt_pack", "qfmt_dequant", "qmm", "qmm_ex", "qmm_workspace_bytes", "qmm_gather", "qmm_batched", "qmm_rmsnorm",
-    "qmm_gated_rmsnorm",
+    "qmm_gated_rmsnorm", "qmm_noalloc",
     "qfmt_last_error",
     "qfmt_version", "qfmt_device_status", "qfmt_debug_set",
 ]
@@ -65,6 +65,9 @@ _SIGS = {
                               ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                               ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "qmm_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
+    "qmm_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                   ctypes.c_void_p]),
     "qmm_gather": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                   ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]),
@@ -306,6 +309,21 @@ def qmm_ex(fmt, codes, scales, global_scale: float, x, N: int, out=None, out_dty
     od = F32 if out.dtype == torch.float32 else BF16
     _check(load().qmm_ex(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), xd, _ptr(out), od,
                          M, N, K, group, _ptr(workspace), ws_bytes, _stream(stream)), where)
+    return out
+
+
+def qmm_noalloc(fmt, codes, scales, x, N: int, out=None, group: int = 0, stream=None):
+    """qmm_ex's block-scaled GEMM with the library's static scratch instead of a workspace (no allocation)."""
+    import torch
+    where = "qmm_noalloc"
+    M, K = _activations(where, x)
+    _weights(where, fmt, codes, scales, N, K, group)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _tensor(out, where, "out", dtype=torch.bfloat16, shape=(M, N))
+    _on_device(where, x=x, codes=codes, scales=scales, out=out)
+    _check(load().qmm_noalloc(_fmt(fmt), _ptr(codes), _ptr(scales), 1.0, _ptr(x), _ptr(out), M, N, K, group,
+                              _stream(stream)), where)
     return out
 
 

@@ -210,6 +210,33 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale,
 size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t K);
 
 /*
+ * qmm_noalloc -- qmm_ex's block-scaled tensor-core GEMM (mxfp4, mxfp8 E4M3 /
+ * E5M2; M > 16; K a multiple of 128; bf16 X and out) for callers that cannot
+ * allocate device memory for scratch: an inference engine's plugin interface
+ * that hands an op only its inputs and outputs, or a latency-critical path
+ * that cannot take cudaMalloc's implicit device-wide synchronisation.  It
+ * allocates nothing.  The scratch (X split into two E4M3 code planes and
+ * their scale atoms, qmm_workspace_bytes(fmt, M, K) bytes) lives in one
+ * static device array of QMM_NOALLOC_SCRATCH_BYTES inside this library,
+ * present on every GPU that loads the library until the process exits.
+ * The method's pages have no counterpart to this call; the arithmetic and
+ * the result are qmm_ex's with a workspace.
+ *   - The first call on a device looks up the array's device address there
+ *     (cudaGetSymbolAddress with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the array and leaves its contents behind; each call
+ *     writes all the scratch it reads before reading it.  Calls that overlap
+ *     on the GPU (on different streams) race on the array.
+ *   - QFMT_EUNSUPPORTED for another format, M <= 16 or K not a multiple of
+ *     128; QFMT_ENOSPACE when the scratch needed exceeds the array; codes
+ *     32-byte aligned for mxfp4 (16 otherwise), else QFMT_EALIGN; the other
+ *     arguments and errors as qmm (global_scale is ignored).
+ */
+#define QMM_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int qmm_noalloc(int fmt, const void* codes, const void* scales, float global_scale, const void* x, void* out,
+                int64_t M, int64_t N, int64_t K, int group, void* stream);
+
+/*
  * qmm_gather -- device, expert-routed rows (mixture of experts):
  *   out[m, n] (bf16) = sum_k X[m, k] (bf16) . dequant(W)[expert_idx[m] * N + n, k]
  * where the E experts' [N, K] weights are stacked row-wise into one packed

@@ -6,13 +6,13 @@
 // 8-bit elements with E8M0 (mxfp8) or FP32 (nvfp8) block scales; the int4
 // affine value scale * q + bias of metaltile-std tests/qmm_gpu_correctness.rs.
 //
-// GB300 layout: one thread owns one 16-byte piece of codes (32 four-bit or 16
-// eight-bit codes, always inside one row since K is a multiple of 32), loads it
-// with one 128-bit load and writes its 32 (16) outputs with 128-bit stores, so
-// a warp streams 512 contiguous code bytes in and 4 KiB (2 KiB) out.  The
-// kernel is bound by the output write; the grid is a multiple of the SM count
-// and strides over the pieces.  Every product rounds once in float32 (no
-// flush-to-zero), which is the bit-exact contract.
+// GB300 layout: a thread writes 16 bytes of output per step (4 float32 or 8
+// bf16 values of one row, inside one block since every block size is a
+// multiple of 8), reading their 2-8 code bytes and one scale; consecutive
+// lanes take consecutive steps, so each warp instruction stores 512
+// contiguous bytes.  The kernel is bound by the output write; the grid fills
+// every SM and strides over the steps.  Every product rounds once in float32
+// (no flush-to-zero), which is the bit-exact contract.
 #include <cuda_runtime.h>
 
 #include "decode.cuh"
@@ -46,66 +46,102 @@ __device__ __forceinline__ void dq_scale(const uint8_t* scales, int64_t idx, flo
   }
 }
 
+// A warp takes 32 consecutive 16-byte code pieces (pieces run in row-major
+// order over [N, K], so their outputs are one contiguous run of out): each
+// lane loads one piece with a 128-bit load into shared memory, then the warp
+// writes the run 512 bytes per instruction, lane l taking the V (4 float32 or
+// 8 bf16) outputs at l V of each 32 V.
 template <int F, bool OUT_BF16>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ codes,
                                                       const uint8_t* __restrict__ scales, float glob,
                                                       void* __restrict__ out, int64_t N, int64_t K) {
   using T = FmtTraits<F>;
-  constexpr int PIECE = T::four ? 32 : 16;     // codes per 16-byte piece
-  const int64_t pieces_per_row = K / PIECE;
-  const int64_t total = N * pieces_per_row;
-  const int64_t nblk = (K + T::block - 1) / T::block;   // int4 affine: a ragged last group
+  constexpr int PIECE = T::four ? 32 : 16;            // codes per 16-byte piece
+  constexpr int V = OUT_BF16 ? 8 : 4;                 // outputs per lane and store: 16 bytes
+  constexpr int BITS = T::four ? 4 : 8;
+  constexpr int STEPS = 32 * PIECE / (32 * V);        // store instructions per warp run
+  __shared__ uint4 stage[8][32];
+  __shared__ uint4 stage1[F == MXFP4X2 ? 8 : 1][32];   // mxfp4x2: the plane-1 pieces
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t pieces = N * (K / PIECE);             // mxfp4x2: pieces of plane 0, one per 32 outputs
+  const int64_t nblk = (K + T::block - 1) / T::block; // int4 affine: a ragged last group
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (int64_t p = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; p < total;
-       p += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t row = p / pieces_per_row;
-    const int64_t k0 = (p - row * pieces_per_row) * PIECE;
-    float o[PIECE];
+  const int64_t wstride = int64_t(gridDim.x) * (blockDim.x >> 5) * 32;
+  for (int64_t base = (int64_t(blockIdx.x) * (blockDim.x >> 5) + warp) * 32; base < pieces; base += wstride) {
+    const int64_t p = base + lane;
+    const int64_t e0 = base * PIECE;                  // first output element of the run
+    const int64_t row0 = e0 / K;
     if constexpr (F == MXFP4X2) {
-      // the two residual planes of row `row` (plane 0, then plane 1, K/2 bytes
-      // each) under their float32 block scales: s0 e0 + s1 e1, the products
-      // exact in double, the sum rounded in double and then to float32
-      const int64_t j = p - row * pieces_per_row;
-      const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(codes) + 2 * row * pieces_per_row + j);
-      const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(codes) + (2 * row + 1) * pieces_per_row + j);
-      const float* sr = reinterpret_cast<const float*>(scales) + 2 * row * nblk;
-      const double s0 = __ldg(sr + k0 / 32), s1 = __ldg(sr + nblk + k0 / 32);
-      const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
-      #pragma unroll
-      for (int i = 0; i < PIECE; ++i) {
-        const double e0 = e2m1_f32((w0[i >> 3] >> (4 * (i & 7))) & 0xFu);
-        const double e1 = e2m1_f32((w1[i >> 3] >> (4 * (i & 7))) & 0xFu);
-        o[i] = __double2float_rn(__dadd_rn(__dmul_rn(e0, s0), __dmul_rn(e1, s1)));
+      // the residual planes of a row sit side by side: plane q of row r is
+      // code row 2r + q; both planes' pieces are staged
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+      if (p < pieces) {
+        const int64_t r = p / (K / PIECE), j = p - r * (K / PIECE);
+        v0 = __ldg(reinterpret_cast<const uint4*>(codes) + (2 * r) * (K / PIECE) + j);
+        v1 = __ldg(reinterpret_cast<const uint4*>(codes) + (2 * r + 1) * (K / PIECE) + j);
       }
-    } else {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(codes) + p);
-    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-    float s = 0.0f, b = 0.0f;
-    // blocks inside the piece: 4-bit: 32 codes = 1 (mx), 2 (nvfp4), 1/2 (int4) blocks;
-    // 8-bit: 16 codes = 1/2 (mx) or 1 (nvfp8) block.
-    #pragma unroll
-    for (int i = 0; i < PIECE; ++i) {
-      const int64_t blk = row * nblk + (k0 + i) / T::block;
-      if (i == 0 || ((k0 + i) % T::block) == 0) dq_scale<F>(scales, blk, s, b);
-      uint32_t code = T::four ? (wv[i >> 3] >> (4 * (i & 7))) & 0xFu : (wv[i >> 2] >> (8 * (i & 3))) & 0xFFu;
-      o[i] = dq_value<F>(code, s, b, glob);
-    }
-    }
-    if constexpr (OUT_BF16) {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + row * K + k0);
+      stage[warp][lane] = v0;
+      stage1[warp][lane] = v1;
+      __syncwarp();
+      const uint32_t* sw0 = reinterpret_cast<const uint32_t*>(&stage[warp][0]);
+      const uint32_t* sw1 = reinterpret_cast<const uint32_t*>(&stage1[warp][0]);
       #pragma unroll
-      for (int q = 0; q < PIECE / 8; ++q) {
-        uint32_t h[4];
+      for (int q = 0; q < STEPS; ++q) {
+        const int off = q * 32 * V + lane * V;          // element offset in the run
+        const int64_t e = e0 + off;
+        if (e >= N * K) break;
+        const int sh = 4 * (off % 8);
+        const uint32_t w0 = sw0[off / 8], w1 = sw1[off / 8];
+        const int64_t r = row0 + int64_t(uint32_t(e - row0 * K) / uint32_t(K)), k = e - r * K;
+        const float* sr = reinterpret_cast<const float*>(scales) + 2 * r * nblk;
+        const double s0 = __ldg(sr + k / 32), s1 = __ldg(sr + nblk + k / 32);
+        float o[V];
         #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          h[j] = f32_to_bf16bits(o[8 * q + 2 * j]) | (f32_to_bf16bits(o[8 * q + 2 * j + 1]) << 16);
-        dst[q] = make_uint4(h[0], h[1], h[2], h[3]);
+        for (int i = 0; i < V; ++i) {
+          const double a = e2m1_f32((w0 >> (sh + 4 * i)) & 0xFu);
+          const double b = e2m1_f32((w1 >> (sh + 4 * i)) & 0xFu);
+          o[i] = __double2float_rn(__dadd_rn(__dmul_rn(a, s0), __dmul_rn(b, s1)));
+        }
+        if constexpr (OUT_BF16) {
+          uint32_t h[4];
+          #pragma unroll
+          for (int t = 0; t < 4; ++t) h[t] = f32_to_bf16bits(o[2 * t]) | (f32_to_bf16bits(o[2 * t + 1]) << 16);
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + e) = make_uint4(h[0], h[1], h[2], h[3]);
+        } else {
+          *reinterpret_cast<float4*>(static_cast<float*>(out) + e) = make_float4(o[0], o[1], o[2], o[3]);
+        }
       }
+      __syncwarp();
     } else {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + row * K + k0);
+      stage[warp][lane] = p < pieces ? __ldg(reinterpret_cast<const uint4*>(codes) + p) : make_uint4(0, 0, 0, 0);
+      __syncwarp();
+      const uint8_t* sb = reinterpret_cast<const uint8_t*>(&stage[warp][0]);
       #pragma unroll
-      for (int q = 0; q < PIECE / 4; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      for (int q = 0; q < STEPS; ++q) {
+        const int off = q * 32 * V + lane * V;          // element offset in the run
+        const int64_t e = e0 + off;
+        if (e >= N * K) break;
+        const int64_t r = row0 + int64_t(uint32_t(e - row0 * K) / uint32_t(K)), k = e - r * K;
+        float s, b;
+        dq_scale<F>(scales, r * nblk + k / T::block, s, b);
+        uint64_t w;
+        if constexpr (BITS * V == 16) w = *reinterpret_cast<const unsigned short*>(sb + off / 2);
+        else if constexpr (BITS * V == 32) w = *reinterpret_cast<const unsigned int*>(sb + off * BITS / 8);
+        else w = *reinterpret_cast<const unsigned long long*>(sb + off);
+        float o[V];
+        #pragma unroll
+        for (int i = 0; i < V; ++i) o[i] = dq_value<F>(uint32_t(w >> (BITS * i)) & ((1u << BITS) - 1u), s, b, glob);
+        if constexpr (OUT_BF16) {
+          uint32_t h[4];
+          #pragma unroll
+          for (int t = 0; t < 4; ++t) h[t] = f32_to_bf16bits(o[2 * t]) | (f32_to_bf16bits(o[2 * t + 1]) << 16);
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + e) = make_uint4(h[0], h[1], h[2], h[3]);
+        } else {
+          *reinterpret_cast<float4*>(static_cast<float*>(out) + e) = make_float4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      __syncwarp();
     }
   }
 }
@@ -113,11 +149,19 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
 template <int F>
 static cudaError_t launch_dequant_fmt(const void* codes, const void* scales, float glob, void* out,
                                       bool bf16, int64_t N, int64_t K, cudaStream_t st, int sms) {
-  constexpr int PIECE = FmtTraits<F>::four ? 32 : 16;
-  const int64_t total = N * (K / PIECE);
+  const int64_t total = N * (K / (FmtTraits<F>::four ? 32 : 16));   // 16-byte pieces, one a lane
   const int threads = 256;
   int64_t want = (total + threads - 1) / threads;
-  int64_t cap = int64_t(sms) * 8;
+  // as many CTAs as the SMs hold at once (the loop strides over the rest)
+  static int per_sm[2] = {0, 0};
+  int& ps = per_sm[bf16 ? 1 : 0];
+  if (ps == 0) {
+    int v = 0;
+    const cudaError_t e = bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, dequant_kernel<F, true>, threads, 0)
+                               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, dequant_kernel<F, false>, threads, 0);
+    ps = (e == cudaSuccess && v > 0) ? v : 4;
+  }
+  int64_t cap = int64_t(sms) * ps;
   int grid = int(want < cap ? want : cap);
   if (grid < 1) grid = 1;
   auto c = static_cast<const uint8_t*>(codes);

@@ -46,9 +46,10 @@ cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, floa
 bool qgemm_mx_supported(int fmt, int64_t M, int64_t K);
 size_t qgemm_mx_workspace_bytes(int64_t M, int64_t K);
 cudaError_t launch_qgemm_mx(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
-                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st);
+                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st, int sms);
 void set_mx_wait_limit_ns(uint64_t ns);
 void set_mx_drop_arrivals(int on);
+void set_mx_plan(int bn, int s);   // measurement hook: force the tile width (224/256) and K split (1-4); 0 = planner
 cudaError_t read_and_clear_mx_status(unsigned int* status);
 
 // Bounded-wait test hooks and the device status word of the tensor-core GEMM.

@@ -114,7 +114,7 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale, c
     if (workspace_bytes < need)
       return fail(QFMT_ENOSPACE, "workspace of %zu bytes, the block-scaled GEMM needs %zu", workspace_bytes, need);
     if ((st = check_ptr(workspace, 128, "workspace"))) return st;
-    return cuda_status(qfmt_dev::launch_qgemm_mx(fmt, codes, scales, x, out, out_f32, M, N, K, workspace, s),
+    return cuda_status(qfmt_dev::launch_qgemm_mx(fmt, codes, scales, x, out, out_f32, M, N, K, workspace, s, sms),
                        "block-scaled qgemm launch");
   }
   // the GEMM decodes both mxfp4x2 planes of an output row together: N output rows
@@ -274,6 +274,12 @@ int qfmt_debug_set(int key, int64_t value) {
   if (key == 2) {
     qfmt_dev::set_drop_arrivals(value ? 1 : 0);
     qfmt_dev::set_mx_drop_arrivals(value ? 1 : 0);
+    return QFMT_OK;
+  }
+  if (key == 3 || key == 4) {   // the block-scaled GEMM's tile width (224, 256) / K split (1-4); 0 = planner
+    static std::atomic<int> bn{0}, sk{0};
+    (key == 3 ? bn : sk).store(int(value));
+    qfmt_dev::set_mx_plan(bn.load(), sk.load());
     return QFMT_OK;
   }
   return fail(QFMT_EINVAL, "unknown debug key %d", key);

@@ -57,10 +57,10 @@ namespace mx {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 256, BK = 128;   // BK: K elements (= bytes of an 8-bit code row) per stage
+constexpr int BM = 128, BN_MAX = 256, BK = 128;   // BK: K elements (= bytes of an 8-bit code row) per stage
 constexpr int STAGES = 3;
 constexpr int A_BYTES = BM * BK;              // 16 KiB: one X term
-constexpr int B_BYTES = BN * BK;              // 32 KiB: 256 rows of 128 codes (E2M1: 16 in each 16-byte unit)
+constexpr int B_BYTES = BN_MAX * BK;          // 32 KiB: up to 256 rows of 128 codes (E2M1: 16 in each 16-byte unit)
 constexpr int SF_BYTES = 512;                 // one scale atom: 128 rows x 4 K blocks
 constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
 constexpr int SF_STAGE = 4 * SF_BYTES;        // hi atom, lo atom, two W atoms (rows 0-127, 128-255)
@@ -228,6 +228,7 @@ struct MxParams {
   void* out;
   int M, N, K;
   int out_f32;
+  int kb_per;               // K steps per split (grid z = the splits of one cluster)
   uint64_t limit_ns;
   int drop_arrivals;
 };
@@ -236,15 +237,21 @@ template <int F> constexpr uint32_t b_type() {
   return F == MXFP4 ? umma::F8F6F4_E2M1 : (F == MXFP8_E5M2 ? umma::F8F6F4_E5M2 : umma::F8F6F4_E4M3);
 }
 
-template <int F>
+// BN: the tile's N (256, or 224 where that fills the waves of 152 SMs better).
+// A K split runs its splits as a cluster along z; each split's float32
+// partial tile goes to its drained stage memory and the cluster sums them
+// through distributed shared memory in rank order.
+template <int F, int BN>
 __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_constant__ CUtensorMap xhi_map,
                                                               const __grid_constant__ CUtensorMap xlo_map,
                                                               const __grid_constant__ CUtensorMap w_map,
                                                               const MxParams p) {
+  static_assert(BN % 32 == 0 && BN <= BN_MAX && BN > 128, "two W scale atoms a stage");
   // bytes a stage's copies deliver: the two X terms, the W codes (E2M1: the
   // 8 data bytes of every 16-byte unit, the gaps are not written) and the two
   // X scale atoms
-  constexpr uint32_t TX_BYTES = 2 * A_BYTES + (F == MXFP4 ? B_BYTES / 2 : B_BYTES) + 2 * SF_BYTES;
+  constexpr uint32_t TX_BYTES = 2 * A_BYTES + (F == MXFP4 ? BN * BK / 2 : BN * BK) + 2 * SF_BYTES;
+  constexpr int PSTRIDE = BN + 4;                 // floats per partial-tile row (K split)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sf_area = smem + STAGES * STAGE_BYTES;
@@ -257,6 +264,9 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
   const int nk = p.K / BK;
+  const int j0 = blockIdx.z * p.kb_per, j1 = min(nk, j0 + p.kb_per);   // this split's K steps
+  const int nloc = j1 - j0;
+  const bool split_k = gridDim.z > 1;
   const uint32_t sbase = smem_u32(smem), sfbase = smem_u32(sf_area), bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto sf_full = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -303,9 +313,9 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
       const uint8_t* sfh = p.sf_hi + size_t(blockIdx.y) * size_t(nk) * SF_BYTES;
       const uint8_t* sfl = p.sf_lo + size_t(blockIdx.y) * size_t(nk) * SF_BYTES;
       int issued = 0;
-      for (int j = 0; j < nk; ++j) {
-        const int s = j % STAGES;
-        const uint32_t ph = (j / STAGES) & 1;
+      for (int i = 0; i < nloc; ++i) {
+        const int s = i % STAGES, j = j0 + i;
+        const uint32_t ph = (i / STAGES) & 1;
         if (*abort_flag) break;
         if (!mbar_wait(empty(s), ph ^ 1u, p.limit_ns)) { fail(); break; }
         mbar_arrive_expect_tx(full(s), TX_BYTES);
@@ -314,19 +324,19 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         tma_load_2d(b_tile(s), &w_map, j * BK, n0, full(s));
         bulk_load(sf_s(s, 0), sfh + size_t(j) * SF_BYTES, SF_BYTES, full(s));
         bulk_load(sf_s(s, 1), sfl + size_t(j) * SF_BYTES, SF_BYTES, full(s));
-        issued = j + 1;
+        issued = i + 1;
       }
       // every issued copy lands before the CTA may exit
-      for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
-        if (!mbar_wait(full(j % STAGES), (j / STAGES) & 1, p.limit_ns)) fail();
+      for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+        if (!mbar_wait(full(i % STAGES), (i / STAGES) & 1, p.limit_ns)) fail();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t BT = b_type<F>();
-      for (int j = 0; j < p.K / BK; ++j) {
-        const int s = j % STAGES;
-        const uint32_t ph = (j / STAGES) & 1;
+      for (int i = 0; i < nloc; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
         if (*abort_flag) break;
         if (!mbar_wait(full(s), ph, p.limit_ns) || !mbar_wait(sf_full(s), ph, p.limit_ns)) { fail(); break; }
         tc_fence_after();
@@ -339,7 +349,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         #pragma unroll
         for (int kk = 0; kk < BK / 32; ++kk) {   // +32 bytes along K per instruction
           const uint32_t id = umma::idesc_mxf8f6f4(umma::F8F6F4_E4M3, BT, BM, BN, uint32_t(kk), uint32_t(kk));
-          mma_mx(tmem, dh + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 0, sfc + 8, (j | kk) != 0);
+          mma_mx(tmem, dh + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 0, sfc + 8, (i | kk) != 0);
           mma_mx(tmem, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 4, sfc + 8, 1u);
         }
         mma_commit(empty(s));
@@ -352,19 +362,19 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     // blocks 4j..4j+3 are one aligned 32-bit word of the row (K % 128 == 0)
     const int row_words = p.K / 128;
     const uint32_t* ws32 = reinterpret_cast<const uint32_t*>(p.wscales);
-    auto load = [&](int j, uint32_t (&v)[8]) {
+    auto load = [&](int i, uint32_t (&v)[8]) {
       #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int n = n0 + lane + 32 * i;
-        v[i] = (j < nk && n < p.N) ? __ldg(ws32 + int64_t(n) * row_words + j) : 0u;
+      for (int t = 0; t < 8; ++t) {
+        const int r = lane + 32 * t, n = n0 + r;
+        v[t] = (i < nloc && r < BN && n < p.N) ? __ldg(ws32 + int64_t(n) * row_words + j0 + i) : 0u;
       }
     };
     uint32_t cur[8], nxt[8];
     load(0, cur);
     load(1, nxt);
-    for (int j = 0; j < nk; ++j) {
-      const int s = j % STAGES;
-      const uint32_t ph = (j / STAGES) & 1;
+    for (int i = 0; i < nloc; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
       int ok = 1;
       if (lane == 0) ok = (*abort_flag == 0u) && mbar_wait(empty(s), ph ^ 1u, p.limit_ns);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -373,13 +383,13 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         break;
       }
       uint32_t nx2[8];
-      load(j + 2, nx2);
+      load(i + 2, nx2);
       #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t dst = sf_s(s, 2 + i / 4) + umma::sf_atom_offset(uint32_t(lane + 32 * (i % 4)), 0);
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst), "r"(cur[i]) : "memory");
-        cur[i] = nxt[i];
-        nxt[i] = nx2[i];
+      for (int t = 0; t < 8; ++t) {
+        const uint32_t dst = sf_s(s, 2 + t / 4) + umma::sf_atom_offset(uint32_t(lane + 32 * (t % 4)), 0);
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst), "r"(cur[t]) : "memory");
+        cur[t] = nxt[t];
+        nxt[t] = nx2[t];
       }
       fence_proxy_async();
       __syncwarp();
@@ -400,6 +410,14 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     for (int cb = 0; cb < BN / 32; ++cb) {
       uint32_t r[32];
       tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(cb * 32), r);
+      if (split_k) {   // this split's partial tile into the drained stage memory
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(smem) + (q * 32 + lane) * PSTRIDE + cb * 32);
+        #pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                               __uint_as_float(r[4 * j + 3]));
+        continue;
+      }
       const int nb = n0 + cb * 32;
       if (!live || m >= p.M || nb >= p.N) continue;
       const int ncols = p.N - nb < 32 ? p.N - nb : 32;
@@ -430,6 +448,48 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         }
       }
     }
+  }
+
+  if (split_k) {
+    // The splits of one tile form a cluster: each CTA sums a slice of the tile
+    // over the cluster's partial tiles (rank order) and stores it; a CTA whose
+    // wait expired holds no valid partial, and then no CTA writes its slice.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    cluster_sync();
+    uint32_t rank, csize;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
+    uint32_t any_abort = 0u;
+    for (uint32_t r = 0; r < csize; ++r) any_abort |= ld_cluster_u32(smem_u32((const void*)abort_flag), r);
+    constexpr int E = BM * (BN / 4);                       // float4 elements of the tile
+    const int e0 = int(rank) * E / int(csize), e1 = any_abort ? e0 : (int(rank) + 1) * E / int(csize);
+    for (int e = e0 + int(threadIdx.x); e < e1; e += THREADS) {
+      const int row = e / (BN / 4), c4 = e - row * (BN / 4);
+      const int m = m0 + row, n = n0 + 4 * c4;
+      if (m >= p.M || n >= p.N) continue;
+      const uint32_t sa = sbase + uint32_t((row * PSTRIDE + 4 * c4) * 4);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (uint32_t r = 0; r < csize; ++r) {
+        const float4 w = ld_cluster_f32x4(sa, r);
+        v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+      }
+      const float f4[4] = {v.x, v.y, v.z, v.w};
+      const bool vec = n + 4 <= p.N && (p.N & 3) == 0;
+      if (p.out_f32) {
+        float* o = static_cast<float*>(p.out) + int64_t(m) * p.N + n;
+        if (vec) *reinterpret_cast<float4*>(o) = v;
+        else for (int j = 0; j < 4 && n + j < p.N; ++j) o[j] = f4[j];
+      } else {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + int64_t(m) * p.N + n;
+        if (vec) {
+          *reinterpret_cast<uint2*>(o) = make_uint2(f32_to_bf16bits(v.x) | (f32_to_bf16bits(v.y) << 16),
+                                                    f32_to_bf16bits(v.z) | (f32_to_bf16bits(v.w) << 16));
+        } else {
+          for (int j = 0; j < 4 && n + j < p.N; ++j) o[j] = __float2bfloat16_rn(f4[j]);
+        }
+      }
+    }
+    cluster_sync();   // no CTA leaves while the others still read its partial tile
   }
 
   tc_fence_before();
@@ -473,21 +533,115 @@ static bool make_map(EncodeTiledFn enc, CUtensorMap* map, CUtensorMapDataType dt
 
 static std::atomic<uint64_t> g_limit_ns{2000000000ull};
 static std::atomic<int> g_drop{0};
+static std::atomic<int> g_force_bn{0}, g_force_s{0};   // plan overrides for measurements (0: the planner's)
+
+// Tile width and K split, by the estimated time in K steps of one CTA:
+// waves of co-resident tiles (a split tile runs as a cluster of S CTAs, and
+// clusters are placed whole, so the device holds fewer of them at once) times
+// the K steps of a split plus, for a split, ~6 K steps of partial-tile
+// reduction in every wave.  A 224-wide tile's K step costs ~0.95 of a
+// 256-wide one (the step waits on the X tiles, whose size it shares).
+// Measured on 2048 x 4096 x 4096, 4096 x 11008 x 4096 and 128..512 x N.
+// No split may be left empty.
+struct MxPlan {
+  int BN, S;
+};
+
+template <int F, int BN>
+static cudaError_t set_smem(int dev) {
+  static std::atomic<int> done[64];
+  if (dev < 0 || dev >= 64 || done[dev].load()) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) done[dev].store(1);
+  return e;
+}
+
+// Clusters of S CTAs (of this kernel's shared memory) the device holds at once.
+template <int F>
+static int cluster_capacity(int dev, int S, int sms) {
+  static std::atomic<int> cache[64][5];
+  if (S == 1 || dev < 0 || dev >= 64) return sms;
+  int v = cache[dev][S].load();
+  if (v > 0) return v;
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = unsigned(S);
+  lc.gridDim = dim3(1, 1, unsigned(S));
+  lc.blockDim = dim3(THREADS);
+  lc.dynamicSmemBytes = SMEM_BYTES;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, qgemm_mx_kernel<F, 256>, &lc) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / S;
+  }
+  cache[dev][S].store(n);
+  return n;
+}
+
+template <int F>
+static MxPlan plan_mx(int dev, int M, int N, int K, int sms) {
+  const int nk = K / BK;
+  const int64_t mtiles = (M + BM - 1) / BM;
+  MxPlan best{256, 1};
+  double best_cost = 1e300;
+  for (int bn : {256, 224}) {
+    const int64_t tiles = int64_t((N + bn - 1) / bn) * mtiles;
+    for (int s = 1; s <= 4; ++s) {
+      const int per = (nk + s - 1) / s;
+      if (s > 1 && (s - 1) * per >= nk) continue;
+      const int64_t cap = cluster_capacity<F>(dev, s, sms);
+      const int64_t waves = (tiles + cap - 1) / cap;
+      const double cost = double(waves) * (per + (s > 1 ? 6.0 : 0.0)) * (bn == 224 ? 0.95 : 1.0);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = {bn, s};
+      }
+    }
+  }
+  return best;
+}
+
+template <int F, int BN>
+static cudaError_t launch_tile(const CUtensorMap& mhi, const CUtensorMap& mlo, const CUtensorMap& mw, MxParams prm,
+                               int M, int N, int S, cudaStream_t st) {
+  const int nk = prm.K / BK;
+  prm.kb_per = (nk + S - 1) / S;
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = 1;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = unsigned(S);
+  lc.gridDim = dim3((N + BN - 1) / BN, (M + BM - 1) / BM, S);
+  lc.blockDim = dim3(THREADS);
+  lc.dynamicSmemBytes = SMEM_BYTES;
+  lc.stream = st;
+  lc.attrs = at;
+  lc.numAttrs = 2;
+  return cudaLaunchKernelEx(&lc, qgemm_mx_kernel<F, BN>, mhi, mlo, mw, prm);
+}
 
 template <int F>
 static cudaError_t launch_fmt(const void* codes, const void* scales, const void* x, void* out, bool out_f32, int M,
-                              int N, int K, void* ws, cudaStream_t st) {
+                              int N, int K, void* ws, cudaStream_t st, int sms) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  static std::atomic<int> attr_done[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
-    e = cudaFuncSetAttribute(qgemm_mx_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done[dev].store(1);
-  }
+  if ((e = set_smem<F, 256>(dev)) != cudaSuccess || (e = set_smem<F, 224>(dev)) != cudaSuccess) return e;
+  MxPlan pl = plan_mx<F>(dev, M, N, K, sms > 0 ? sms : 1);
+  if (g_force_bn.load() == 224 || g_force_bn.load() == 256) pl.BN = g_force_bn.load();
+  if (g_force_s.load() >= 1 && g_force_s.load() <= 4 && (g_force_s.load() - 1) * ((K / BK + g_force_s.load() - 1) / g_force_s.load()) < K / BK)
+    pl.S = g_force_s.load();
   const WsLayout lay = ws_layout(M, K);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   // activations -> hi / lo MXFP8 terms (one warp per row and 1024 columns)
@@ -511,8 +665,8 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, const void*
       !make_map(enc, &mlo, CU_TENSOR_MAP_DATA_TYPE_UINT8, w8 + lay.lo, K, M, K, BM))
     return cudaErrorInvalidValue;
   const bool ok = F == MXFP4
-                      ? make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, K, N, K / 2, BN)
-                      : make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, N, K, BN);
+                      ? make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, K, N, K / 2, uint32_t(pl.BN))
+                      : make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, N, K, uint32_t(pl.BN));
   if (!ok) return cudaErrorInvalidValue;
   MxParams prm;
   prm.wscales = static_cast<const uint8_t*>(scales);
@@ -523,19 +677,11 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, const void*
   prm.N = N;
   prm.K = K;
   prm.out_f32 = out_f32 ? 1 : 0;
+  prm.kb_per = K / BK;
   prm.limit_ns = g_limit_ns.load();
   prm.drop_arrivals = g_drop.load();
-  cudaLaunchConfig_t lc = {};
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.gridDim = dim3((N + BN - 1) / BN, (M + BM - 1) / BM);
-  lc.blockDim = dim3(THREADS);
-  lc.dynamicSmemBytes = SMEM_BYTES;
-  lc.stream = st;
-  lc.attrs = at;
-  lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, qgemm_mx_kernel<F>, mhi, mlo, mw, prm);
+  if (pl.BN == 224) return launch_tile<F, 224>(mhi, mlo, mw, prm, M, N, pl.S, st);
+  return launch_tile<F, 256>(mhi, mlo, mw, prm, M, N, pl.S, st);
 }
 
 }  // namespace mx
@@ -547,17 +693,21 @@ bool qgemm_mx_supported(int fmt, int64_t M, int64_t K) {
 size_t qgemm_mx_workspace_bytes(int64_t M, int64_t K) { return mx::ws_layout(M, K).total; }
 
 cudaError_t launch_qgemm_mx(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
-                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st) {
+                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st, int sms) {
   const int m = int(M), n = int(N), k = int(K);
   switch (fmt) {
-    case MXFP4: return mx::launch_fmt<MXFP4>(codes, scales, x, out, out_f32, m, n, k, workspace, st);
-    case MXFP8_E4M3: return mx::launch_fmt<MXFP8_E4M3>(codes, scales, x, out, out_f32, m, n, k, workspace, st);
-    case MXFP8_E5M2: return mx::launch_fmt<MXFP8_E5M2>(codes, scales, x, out, out_f32, m, n, k, workspace, st);
+    case MXFP4: return mx::launch_fmt<MXFP4>(codes, scales, x, out, out_f32, m, n, k, workspace, st, sms);
+    case MXFP8_E4M3: return mx::launch_fmt<MXFP8_E4M3>(codes, scales, x, out, out_f32, m, n, k, workspace, st, sms);
+    case MXFP8_E5M2: return mx::launch_fmt<MXFP8_E5M2>(codes, scales, x, out, out_f32, m, n, k, workspace, st, sms);
     default: return cudaErrorInvalidValue;
   }
 }
 
 void set_mx_wait_limit_ns(uint64_t ns) { mx::g_limit_ns.store(ns); }
+void set_mx_plan(int bn, int s) {
+  mx::g_force_bn.store(bn);
+  mx::g_force_s.store(s);
+}
 void set_mx_drop_arrivals(int on) { mx::g_drop.store(on); }
 
 cudaError_t read_and_clear_mx_status(unsigned int* status) {

@@ -87,8 +87,11 @@ extern "C" int qmm_noalloc(int fmt, const void* codes, const void* scales, float
   if ((st = check_ptr(out, 16, "out"))) return st;
   void* ws = scratch_address(&st);
   if (!ws) return st;
-  const cudaError_t e = qfmt_dev::launch_qgemm_mx(fmt, codes, scales, x, out, false, M, N, K, ws,
-                                                  static_cast<cudaStream_t>(stream));
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(QFMT_ECUDA, "device query: %s", cudaGetErrorString(e));
+  e = qfmt_dev::launch_qgemm_mx(fmt, codes, scales, x, out, false, M, N, K, ws, static_cast<cudaStream_t>(stream), sms);
   if (e != cudaSuccess) return fail(QFMT_ECUDA, "qmm_noalloc launch: %s", cudaGetErrorString(e));
   return QFMT_OK;
 }

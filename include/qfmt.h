@@ -322,7 +322,9 @@ int qfmt_device_status(void* stream);
  * to launches made afterwards): key 1 sets the wait limit in nanoseconds
  * (value <= 0 restores the default of 2 s); key 2 with value 1 makes the GEMM's
  * decoder warps skip signalling their stages, so the MMA warp's waits expire
- * (value 0 restores normal operation).  Returns QFMT_EINVAL for other keys.
+ * (value 0 restores normal operation); keys 3 and 4 force the block-scaled
+ * GEMM's tile width (224 or 256) and K split (1-4), value 0 restoring its own
+ * plan (for measurements).  Returns QFMT_EINVAL for other keys.
  */
 int qfmt_debug_set(int key, int64_t value);
 

@@ -47,9 +47,16 @@ bool qgemm_mx_supported(int fmt, int64_t M, int64_t K);
 size_t qgemm_mx_workspace_bytes(int64_t M, int64_t K);
 cudaError_t launch_qgemm_mx(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
                             int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st, int sms);
+// Decode GEMV on the same block-scaled MMA (M <= 16, K a multiple of 128 up to
+// 1024, mxfp4 codes 32-byte aligned): weights as stored, activations split in
+// the CTA; no workspace.
+bool qgemv_mx_supported(int fmt, int64_t M, int64_t N, int64_t K, const void* codes);
+cudaError_t launch_qgemv_mx(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
+                            int64_t M, int64_t N, int64_t K, cudaStream_t st);
 void set_mx_wait_limit_ns(uint64_t ns);
 void set_mx_drop_arrivals(int on);
-void set_mx_plan(int bn, int s);   // measurement hook: force the tile width (224/256) and K split (1-4); 0 = planner
+void set_mx_plan(int bn, int s);
+void set_mx_gemv(int off, int s);  // measurement hook: 1 = the mma.sync GEMVs for the MX formats; forced K split   // measurement hook: force the tile width (224/256) and K split (1-4); 0 = planner
 cudaError_t read_and_clear_mx_status(unsigned int* status);
 
 // Bounded-wait test hooks and the device status word of the tensor-core GEMM.

@@ -102,10 +102,16 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale, c
     return cuda_status(qfmt_dev::launch_qmm_f32x(fmt, codes, scales, global_scale, static_cast<const float*>(x),
                                                  out, out_f32, M, N, K, s, sms),
                        "qmm (f32 activations) launch");
-  if (M <= 16)
+  if (M <= 16) {
+    // the MX formats the block-scaled MMA reads as stored: the tensor-core
+    // decode GEMV (no ALU decode); the rest: the mma.sync decode GEMVs
+    if (qfmt_dev::qgemv_mx_supported(fmt, M, N, K, codes))
+      return cuda_status(qfmt_dev::launch_qgemv_mx(fmt, codes, scales, x, out, out_f32, M, N, K, s),
+                         "block-scaled qgemv launch");
     return cuda_status(qfmt_dev::launch_qgemv(fmt, codes, scales, global_scale, x, out, out_f32, M,
                                               weight_rows(fmt, N), K, s, sms),
                        "qgemv launch");
+  }
   // With a workspace, the MX formats the block-scaled MMA reads as stored take
   // it (the E2M1 codes' tensor map needs a 32-byte aligned base).
   if (workspace && qfmt_dev::qgemm_mx_supported(fmt, M, K) &&
@@ -280,6 +286,12 @@ int qfmt_debug_set(int key, int64_t value) {
     static std::atomic<int> bn{0}, sk{0};
     (key == 3 ? bn : sk).store(int(value));
     qfmt_dev::set_mx_plan(bn.load(), sk.load());
+    return QFMT_OK;
+  }
+  if (key == 5 || key == 6) {   // decode GEMV of the MX formats: 5 = use the mma.sync GEMVs; 6 = K split
+    static std::atomic<int> off{0}, sk{0};
+    (key == 5 ? off : sk).store(int(value));
+    qfmt_dev::set_mx_gemv(off.load(), sk.load());
     return QFMT_OK;
   }
   return fail(QFMT_EINVAL, "unknown debug key %d", key);

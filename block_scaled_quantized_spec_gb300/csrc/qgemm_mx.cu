@@ -123,6 +123,54 @@ __device__ __forceinline__ void e4m3x2_f32(uint32_t two, float& lo, float& hi) {
   hi = __half2float(__ushort_as_half(uint16_t(r >> 16)));
 }
 
+// One block of 32 bf16 activations (16 words, value 2i in the low half of
+// word i) -> hi and lo E4M3 codes (8 words each, code i in byte i % 4 of word
+// i / 4) and their E8M0 scale bytes c1, c2 (see the file comment).
+__device__ __forceinline__ void split_block(const uint32_t (&w)[16], uint32_t& c1, uint32_t& c2, uint32_t (&hi)[8],
+                                            uint32_t (&lo)[8]) {
+  float v[32];
+  float amax = 0.0f;
+  #pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+  }
+  // an infinity gives the block the NaN scale (255); a NaN element (which
+  // fmaxf passes over) stays a NaN code: either way its outputs are NaN
+  c1 = e8m0_for_e4m3(amax);
+  const float s1 = e8m0_f32(c1), r1 = c1 == 255u ? 0.0f : e8m0_recip(c1);
+  float ramax = 0.0f;
+  #pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t h = e4m3x2(__fmul_rn(v[2 * i], r1), __fmul_rn(v[2 * i + 1], r1));
+    float h0, h1;
+    e4m3x2_f32(h, h0, h1);
+    v[2 * i] = __fmaf_rn(-h0, s1, v[2 * i]);               // exact residuals
+    v[2 * i + 1] = __fmaf_rn(-h1, s1, v[2 * i + 1]);
+    ramax = fmaxf(ramax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+    if (i & 1) hi[i >> 1] |= h << 16;
+    else hi[i >> 1] = h;
+  }
+  c2 = c1 == 255u ? 255u : e8m0_for_e4m3(ramax);
+  const float r2 = c2 == 255u ? 0.0f : e8m0_recip(c2);
+  #pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t l = e4m3x2(__fmul_rn(v[2 * i], r2), __fmul_rn(v[2 * i + 1], r2));
+    if (i & 1) lo[i >> 1] |= l << 16;
+    else lo[i >> 1] = l;
+  }
+}
+
+__device__ __forceinline__ void load_block(const __nv_bfloat16* src, uint32_t (&w)[16]) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  #pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = __ldg(s4 + i);
+    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+  }
+}
+
 // One warp per (row, 32 consecutive blocks of 32): lane l takes block b0 + l.
 // Rows past M (up to the 128-row tile) get neutral scale words only.
 __global__ void __launch_bounds__(256) xquant_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ ws,
@@ -137,46 +185,9 @@ __global__ void __launch_bounds__(256) xquant_kernel(const __nv_bfloat16* __rest
   const bool live = b < nblk;
   uint32_t c1 = 127u, c2 = 127u;
   if (live && m < M) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + int64_t(m) * K + int64_t(b) * 32);
-    uint32_t w[16];
-    #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = __ldg(src + i);
-      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-    }
-    float v[32];
-    float amax = 0.0f;
-    #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-      amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
-    }
-    // an infinity gives the block the NaN scale (255); a NaN element (which
-    // fmaxf passes over) stays a NaN code: either way its outputs are NaN
-    c1 = e8m0_for_e4m3(amax);
-    const float s1 = e8m0_f32(c1), r1 = c1 == 255u ? 0.0f : e8m0_recip(c1);
-    uint32_t hi[8], lo[8];
-    float ramax = 0.0f;
-    #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t h = e4m3x2(__fmul_rn(v[2 * i], r1), __fmul_rn(v[2 * i + 1], r1));
-      float h0, h1;
-      e4m3x2_f32(h, h0, h1);
-      v[2 * i] = __fmaf_rn(-h0, s1, v[2 * i]);               // exact residuals
-      v[2 * i + 1] = __fmaf_rn(-h1, s1, v[2 * i + 1]);
-      ramax = fmaxf(ramax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
-      if (i & 1) hi[i >> 1] |= h << 16;
-      else hi[i >> 1] = h;
-    }
-    c2 = c1 == 255u ? 255u : e8m0_for_e4m3(ramax);
-    const float r2 = c2 == 255u ? 0.0f : e8m0_recip(c2);
-    #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t l = e4m3x2(__fmul_rn(v[2 * i], r2), __fmul_rn(v[2 * i + 1], r2));
-      if (i & 1) lo[i >> 1] |= l << 16;
-      else lo[i >> 1] = l;
-    }
+    uint32_t w[16], hi[8], lo[8];
+    load_block(x + int64_t(m) * K + int64_t(b) * 32, w);
+    split_block(w, c1, c2, hi, lo);
     uint4* dh = reinterpret_cast<uint4*>(ws + lay.hi + size_t(m) * K + size_t(b) * 32);
     uint4* dl = reinterpret_cast<uint4*>(ws + lay.lo + size_t(m) * K + size_t(b) * 32);
     dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -534,6 +545,7 @@ static bool make_map(EncodeTiledFn enc, CUtensorMap* map, CUtensorMapDataType dt
 static std::atomic<uint64_t> g_limit_ns{2000000000ull};
 static std::atomic<int> g_drop{0};
 static std::atomic<int> g_force_bn{0}, g_force_s{0};   // plan overrides for measurements (0: the planner's)
+static std::atomic<int> g_gemv_off{0}, g_gemv_s{0};     // decode GEMV: off (mma.sync GEMVs), forced K split
 
 // Tile width and K split, by the estimated time in K steps of one CTA:
 // waves of co-resident tiles (a split tile runs as a cluster of S CTAs, and
@@ -684,6 +696,271 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, const void*
   return launch_tile<F, 256>(mhi, mlo, mw, prm, M, N, pl.S, st);
 }
 
+// ------------------------------------------------ decode GEMV, M <= 16 ---
+//
+// The same block-scaled MMA with the roles set for a decode step: A = a tile
+// of 128 weight rows over KC columns (TMA-loaded as stored before the
+// dependent wait, like every weight read here), B = the activations split
+// in the CTA into hi and lo E4M3 rows (row 2m = hi of activation row m, row
+// 2m + 1 its lo; the MMA's N is 16 for M <= 8, 32 for M <= 16), D = 128 x N
+// float32 in tensor memory, out[m][n] = D[n][2m] + D[n][2m + 1].  Nothing is
+// decoded on the ALUs.  K may be split over a cluster of S CTAs (KC = K / S <=
+// 512); the partial columns meet through distributed shared memory.
+constexpr int GV_THREADS = 128, GV_ROWS = 128, GV_KC_MAX = 512;
+constexpr int GV_SLABS = GV_KC_MAX / BK;                    // 128-column slabs per CTA, at most
+constexpr int GV_W_BYTES = GV_SLABS * GV_ROWS * BK;        // 64 KiB
+constexpr int GV_X_BYTES = GV_SLABS * 32 * BK;             // 16 KiB (N up to 32)
+constexpr int GV_SMEM = 1024 + GV_W_BYTES + GV_X_BYTES + 2 * GV_SLABS * SF_BYTES + 128;
+constexpr int GV_TMEM_COLS = 64;                           // D 0-31, W scales 32-47, X scales 48-63
+
+struct GvParams {
+  const uint8_t* wscales;        // [N, K/32] E8M0
+  const __nv_bfloat16* x;        // [M, K]
+  void* out;                     // [M, N]
+  int M, N, K, KC;
+  int out_f32;
+  uint64_t limit_ns;
+};
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int F, int NP>
+__global__ void __launch_bounds__(GV_THREADS) qgemv_mx_kernel(const __grid_constant__ CUtensorMap w_map,
+                                                              const GvParams p) {
+  static_assert(NP == 16 || NP == 32, "the MMA's N: two rows per activation row");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* wt = smem;                                     // [slab][128 rows x 128 B], 128B-swizzled
+  uint8_t* xt = wt + GV_W_BYTES;                          // [slab][NP rows x 128 B], 128B-swizzled
+  uint8_t* sfa = xt + GV_X_BYTES;                         // [slab] W scale atoms
+  uint8_t* sfb = sfa + GV_SLABS * SF_BYTES;               // [slab] X scale atoms
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sfb + GV_SLABS * SF_BYTES);   // [0]: W landed, [1]: MMAs done
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 2);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  float* part = reinterpret_cast<float*>(wt);             // [128][17] partial sums (the drained W tile)
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = gridDim.x, split = blockIdx.x;            // K split = the cluster along x
+  const int n0 = blockIdx.y * GV_ROWS, k0 = split * p.KC;
+  const int nsl = p.KC / BK;
+  const uint32_t w_bar = smem_u32(bars), done_bar = w_bar + 8u;
+  auto fail = [&]() {
+    *abort_flag = 1u;
+    atomicOr(&g_mx_status, 1u);
+  };
+
+  if (tid == 0) {
+    mbar_init(w_bar, 1);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&w_map)) : "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((const void*)tmem_slot)),
+                 "r"(GV_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // ---- the weights (not the preceding kernel's output): before the wait ---
+  if (tid == 0) {
+    mbar_arrive_expect_tx(w_bar, uint32_t(nsl) * (F == MXFP4 ? GV_ROWS * BK / 2 : GV_ROWS * BK));
+    for (int j = 0; j < nsl; ++j) tma_load_2d(smem_u32(wt + j * GV_ROWS * BK), &w_map, k0 + j * BK, n0, w_bar);
+  }
+  {
+    // row tid's E8M0 scales: one 32-bit word = 4 blocks of a slab
+    const int n = n0 + tid;
+    const uint32_t* ws32 = reinterpret_cast<const uint32_t*>(p.wscales) + int64_t(n) * (p.K / 128) + k0 / 128;
+    for (int j = 0; j < nsl; ++j) {
+      const uint32_t v = n < p.N ? __ldg(ws32 + j) : 0u;
+      *reinterpret_cast<uint32_t*>(sfa + j * SF_BYTES + umma::sf_atom_offset(uint32_t(tid), 0)) = v;
+    }
+  }
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // ---- the activations: split into hi / lo E4M3 rows of the B tile ----------
+  {
+    const int bps = p.KC / 32;                                  // blocks per row in this split
+    for (int task = tid; task < p.M * bps; task += GV_THREADS) {
+      const int m = task / bps, b = task - m * bps;
+      uint32_t w[16], hi[8], lo[8], c1, c2;
+      load_block(p.x + int64_t(m) * p.K + k0 + 32 * b, w);
+      split_block(w, c1, c2, hi, lo);
+      const int j = b >> 2, c = (b & 3) * 2;                    // slab, first 16-byte chunk of the 128-byte row
+      uint8_t* slab = xt + j * NP * BK;
+      const int rh = 2 * m, rl = 2 * m + 1;
+      *reinterpret_cast<uint4*>(slab + tc::sw128_off(rh, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(slab + tc::sw128_off(rh, c + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+      *reinterpret_cast<uint4*>(slab + tc::sw128_off(rl, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(slab + tc::sw128_off(rl, c + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+      sfb[j * SF_BYTES + umma::sf_atom_offset(uint32_t(rh), uint32_t(b & 3))] = uint8_t(c1);
+      sfb[j * SF_BYTES + umma::sf_atom_offset(uint32_t(rl), uint32_t(b & 3))] = uint8_t(c2);
+    }
+  }
+  fence_proxy_async();                                          // generic stores -> tensor-core reads
+  __syncthreads();
+
+  if (tid == 0) {
+    if (!mbar_wait(w_bar, 0, p.limit_ns)) {
+      fail();
+    } else {
+      tc_fence_after();
+      for (int j = 0; j < nsl; ++j) {
+        tmem_cp_sf(tmem + 32u + 4u * j, umma::smem_desc_sf32x16(smem_u32(sfa + j * SF_BYTES)));
+        tmem_cp_sf(tmem + 48u + 4u * j, umma::smem_desc_sf32x16(smem_u32(sfb + j * SF_BYTES)));
+      }
+      for (int j = 0; j < nsl; ++j) {
+        const uint64_t da = desc_sw128(smem_u32(wt + j * GV_ROWS * BK)), db = desc_sw128(smem_u32(xt + j * NP * BK));
+        #pragma unroll
+        for (int kk = 0; kk < BK / 32; ++kk) {
+          const uint32_t id = umma::idesc_mxf8f6f4(b_type<F>(), umma::F8F6F4_E4M3, GV_ROWS, NP, uint32_t(kk), uint32_t(kk));
+          mma_mx(tmem, da + uint64_t(2 * kk), db + uint64_t(2 * kk), id, tmem + 32u + 4u * j, tmem + 48u + 4u * j,
+                 (j | kk) != 0);
+        }
+      }
+    }
+    mma_commit(done_bar);   // fires once the MMAs above (if any) have completed
+  }
+
+  // ---- drain: row 32 warp + lane of the tile ---------------------------------
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(done_bar, 0, p.limit_ns);
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  if (!ok && lane == 0) fail();
+  tc_fence_after();
+  float v[16];
+  {
+    uint32_t r[NP];
+    if constexpr (NP == 16) tmem_ld16(tmem + (uint32_t(warp * 32) << 16), r);
+    else tmem_ld32(tmem + (uint32_t(warp * 32) << 16), r);
+    #pragma unroll
+    for (int m = 0; m < NP / 2; ++m) v[m] = __uint_as_float(r[2 * m]) + __uint_as_float(r[2 * m + 1]);
+  }
+  const int row = tid;
+  auto store = [&](int m, int n, float val) {
+    if (p.out_f32) static_cast<float*>(p.out)[int64_t(m) * p.N + n] = val;
+    else static_cast<__nv_bfloat16*>(p.out)[int64_t(m) * p.N + n] = __float2bfloat16_rn(val);
+  };
+  if (S == 1) {
+    if (ok && *abort_flag == 0u && n0 + row < p.N)
+      for (int m = 0; m < p.M; ++m) store(m, n0 + row, v[m]);
+  } else {
+    #pragma unroll
+    for (int m = 0; m < NP / 2; ++m) part[row * 17 + m] = v[m];
+    cluster_sync();
+    uint32_t any_abort = 0u;
+    for (int q = 0; q < S; ++q) any_abort |= ld_cluster_u32(smem_u32((const void*)abort_flag), uint32_t(q));
+    // this CTA sums rows [split * 128 / S, (split + 1) * 128 / S) over the cluster's partials, in rank order
+    const int r0 = split * GV_ROWS / S, r1 = (split + 1) * GV_ROWS / S;
+    if (!any_abort) {
+      for (int e = tid; e < (r1 - r0) * p.M; e += GV_THREADS) {   // consecutive threads: consecutive outputs
+        const int m = e / (r1 - r0), rr = r0 + e - m * (r1 - r0);
+        if (n0 + rr >= p.N) continue;
+        float sum = 0.0f;
+        for (int q = 0; q < S; ++q)
+          sum += __uint_as_float(ld_cluster_u32(smem_u32(part + rr * 17 + m), uint32_t(q)));
+        store(m, n0 + rr, sum);
+      }
+    }
+    cluster_sync();   // no CTA leaves while the others still read its partials
+  }
+
+  // a CTA that gave up waiting for its weight tile still lets the copy land before it exits
+  if (tid == 0 && *abort_flag) mbar_wait(w_bar, 0, p.limit_ns);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(GV_TMEM_COLS) : "memory");
+  }
+}
+
+// K split for the decode GEMV: one CTA per 128 rows up to K = 512, a pair of
+// CTAs up to K = 1024; 0 (the mma.sync decode GEMVs) beyond.  Measured against
+// those GEMVs (mxfp4 / mxfp8 E4M3, M = 1 and 8): 1.6-4x faster at K <= 1024;
+// at K = 4096 an 8-way split runs 6.5 us against 3.4 us (N = 4096): 256 CTAs of
+// two per SM leave most of a launch unable to start, and so to request its
+// weights, before the preceding launch ends, and the split's cluster reduction
+// adds ~2 us.
+inline int gemv_splits(int K) {
+  if (K <= 0 || K % BK) return 0;
+  const int slabs = K / BK;
+  if (slabs <= GV_SLABS) return 1;
+  if (slabs <= 2 * GV_SLABS && slabs % 2 == 0) return 2;
+  return 0;
+}
+
+template <int F, int NP>
+static cudaError_t launch_gemv_np(const void* codes, const void* scales, const void* x, void* out, bool out_f32, int M,
+                                  int N, int K, cudaStream_t st) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  static std::atomic<int> done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && !done[dev].load()) {
+    e = cudaFuncSetAttribute(qgemv_mx_kernel<F, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, GV_SMEM);
+    if (e != cudaSuccess) return e;
+    done[dev].store(1);
+  }
+  int S = gemv_splits(K);
+  const int fs = g_gemv_s.load();
+  if (fs >= 1 && fs <= 8 && (K / BK) % fs == 0 && (K / BK) / fs <= GV_SLABS) S = fs;
+  if (S == 0) return cudaErrorInvalidValue;
+  CUtensorMap mw;
+  const bool ok = F == MXFP4 ? make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, K, N, K / 2, GV_ROWS)
+                             : make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, N, K, GV_ROWS);
+  if (!ok) return cudaErrorInvalidValue;
+  GvParams prm;
+  prm.wscales = static_cast<const uint8_t*>(scales);
+  prm.x = static_cast<const __nv_bfloat16*>(x);
+  prm.out = out;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.KC = K / S;
+  prm.out_f32 = out_f32 ? 1 : 0;
+  prm.limit_ns = g_limit_ns.load();
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = unsigned(S);
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  lc.gridDim = dim3(unsigned(S), unsigned((N + GV_ROWS - 1) / GV_ROWS));
+  lc.blockDim = dim3(GV_THREADS);
+  lc.dynamicSmemBytes = GV_SMEM;
+  lc.stream = st;
+  lc.attrs = at;
+  lc.numAttrs = 2;
+  return cudaLaunchKernelEx(&lc, qgemv_mx_kernel<F, NP>, mw, prm);
+}
+
+template <int F>
+static cudaError_t launch_gemv(const void* codes, const void* scales, const void* x, void* out, bool out_f32, int M,
+                               int N, int K, cudaStream_t st) {
+  if (M <= 8) return launch_gemv_np<F, 16>(codes, scales, x, out, out_f32, M, N, K, st);
+  return launch_gemv_np<F, 32>(codes, scales, x, out, out_f32, M, N, K, st);
+}
+
 }  // namespace mx
 
 bool qgemm_mx_supported(int fmt, int64_t M, int64_t K) {
@@ -703,7 +980,27 @@ cudaError_t launch_qgemm_mx(int fmt, const void* codes, const void* scales, cons
   }
 }
 
+bool qgemv_mx_supported(int fmt, int64_t M, int64_t N, int64_t K, const void* codes) {
+  return !mx::g_gemv_off.load() && (fmt == MXFP4 || fmt == MXFP8_E4M3 || fmt == MXFP8_E5M2) && M >= 1 && M <= 16 && N <= 65535LL * mx::GV_ROWS &&
+         mx::gemv_splits(int(K)) > 0 && !(fmt == MXFP4 && (reinterpret_cast<uintptr_t>(codes) & 31u));
+}
+
+cudaError_t launch_qgemv_mx(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
+                            int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+  const int m = int(M), n = int(N), k = int(K);
+  switch (fmt) {
+    case MXFP4: return mx::launch_gemv<MXFP4>(codes, scales, x, out, out_f32, m, n, k, st);
+    case MXFP8_E4M3: return mx::launch_gemv<MXFP8_E4M3>(codes, scales, x, out, out_f32, m, n, k, st);
+    case MXFP8_E5M2: return mx::launch_gemv<MXFP8_E5M2>(codes, scales, x, out, out_f32, m, n, k, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 void set_mx_wait_limit_ns(uint64_t ns) { mx::g_limit_ns.store(ns); }
+void set_mx_gemv(int off, int s) {
+  mx::g_gemv_off.store(off);
+  mx::g_gemv_s.store(s);
+}
 void set_mx_plan(int bn, int s) {
   mx::g_force_bn.store(bn);
   mx::g_force_s.store(s);

@@ -204,3 +204,27 @@ def test_chained_layers_block_scaled(fmt):
         xin = outs[i].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
         ref, bound = oref.qmm_ref(fmt, c, s, g, xin, "bf16", m, n, n)
         check_tensor(outs[i + 1], ref, bound, (fmt, "layer", i))
+
+
+@pytest.mark.parametrize("fmt", MXB)
+@pytest.mark.parametrize("m", [1, 2, 8, 9, 16])
+@pytest.mark.parametrize("k", [128, 384, 512, 768, 1024])
+def test_tensor_core_decode_gemv(fmt, m, k):
+    # M <= 16 with K <= 1024: the decode GEMV on the block-scaled MMA (weights
+    # as stored, activations split in the CTA, one CTA per 128 rows or a pair
+    # summed through distributed shared memory); N ends inside a 128-row tile
+    n = 300
+    c, s, g = opack.pack(fmt, synth.weights(n, k, seed=m + k))
+    xb, xt = _x(m, k, seed=m * k)
+    dc, ds = _dev(c), _dev(s)
+    out = q.qmm(fmt, dc, ds, g, xt, n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    check_tensor(out, ref, bound, (fmt, m, k))
+    # the same rows through the mma.sync decode GEMV (measurement hook 5)
+    q.qfmt_debug_set(5, 1)
+    try:
+        other = q.qmm(fmt, dc, ds, g, xt, n).float().cpu().numpy()
+    finally:
+        q.qfmt_debug_set(5, 0)
+    a = out.float().cpu().numpy()
+    assert (np.abs(a - other) <= 2 * bound + bf16_half_ulp(a) + bf16_half_ulp(other)).all()

@@ -187,10 +187,13 @@ int qfmt_dequant(int fmt, const void* codes, const void* scales, float global_sc
  * qmm -- device: out[M,N] (bf16) = X[M,K] (bf16) . dequant(W[N,K])^T with
  * float32 accumulation (metaltile PR #250 qgemv/qmm/qmm-MMA commits:
  * output[m,n] = sum_k dequant(weight[n,k]) * x[m,k]; rlx-cpu
- * dequant_matmul_nvfp4 for the nvfp4 value).  M <= 16 runs the
- * HBM-streaming decode GEMV; larger M the tensor-core GEMM.  Result within
- * 2e-3 * sum_k |x||w| + 1e-6 of the exact value.  M == 0 or N == 0 is a
- * no-op; K == 0 writes zeros.  No workspace is needed.
+ * dequant_matmul_nvfp4 for the nvfp4 value).  M <= 16 runs a decode GEMV
+ * (for mxfp4 / mxfp8 with K a multiple of 128 up to 1024, on the
+ * block-scaled tensor cores; otherwise the HBM-streaming mma.sync GEMV);
+ * larger M the tensor-core GEMM that decodes the weights to bf16.  Result
+ * within 2e-3 * sum_k |x||w| + 1e-6 of the exact value, before the final
+ * rounding of the bf16 output.  M == 0 or N == 0 is a no-op; K == 0 writes
+ * zeros.  No workspace is needed.
  */
 int qmm(int fmt, const void* codes, const void* scales, float global_scale,
         const void* x, void* out, int64_t M, int64_t N, int64_t K, int group,
@@ -198,15 +201,29 @@ int qmm(int fmt, const void* codes, const void* scales, float global_scale,
 
 /*
  * qmm_ex -- qmm with explicit activation and output dtypes (QFMT_BF16 or
- * QFMT_F32 each).  A float32 X takes a CUDA-core float32 path (exact
- * products, float32 accumulation) at any M.  workspace/workspace_bytes are
- * reserved: pass NULL/0 (qmm_workspace_bytes() returns 0).
+ * QFMT_F32 each) and an optional device workspace.  A float32 X takes a
+ * CUDA-core float32 path (exact products, float32 accumulation) at any M.
+ * With bf16 X, M > 16, a format the block-scaled MMA reads as stored (mxfp4,
+ * mxfp8 E4M3 / E5M2), K a multiple of 128 and a workspace of at least
+ * qmm_workspace_bytes(fmt, M, K) bytes (128-byte aligned; mxfp4 codes 32-byte
+ * aligned), the product runs on tcgen05.mma kind::mxf8f6f4 (rlx-cpu
+ * thunk/ops/quant.rs lowp_scaled_matmul, acc += (a_s b_s) sum dec(a) dec(b);
+ * metaltile PR #250's "Blackwell tcgen05 scaled-MMA (MXFP)"): X is first
+ * split into two MXFP8 E4M3 terms in the workspace (exact for every
+ * activation within 2^14 of its block's largest).  A smaller workspace there
+ * is QFMT_ENOSPACE; NULL (or any other case) takes the paths of qmm.  The
+ * workspace is scratch: its contents are not kept between calls, and calls
+ * sharing one must be ordered on one stream.
  */
 int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale,
            const void* x, int x_dtype, void* out, int out_dtype,
            int64_t M, int64_t N, int64_t K, int group,
            void* workspace, size_t workspace_bytes, void* stream);
 
+/* Workspace bytes qmm_ex uses for the block-scaled GEMM at this format and
+ * shape: 2 M K (the two E4M3 code planes of X) plus 2 M' K / 32 (their E8M0
+ * scales, M' = M rounded up to 128), each part 1 KiB aligned; 0 where qmm_ex
+ * takes no workspace (another format, M <= 16, K not a multiple of 128). */
 size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t K);
 
 /*

@@ -55,6 +55,13 @@ Value definitions (page title, then the section):
   + eps), silu(z) = z sigmoid(z) -- PR #250, the fused gated-RMSNorm + GEMV
   commit (a silu gate times the per-row inverse RMS times the norm weight,
   staged, then the block-scaled GEMV over it); the RMS is of x alone.
+* quantize_activations / qmm_a8_ref: both operands quantized (rlx-cpu
+  ``thunk/ops/quant.rs``: ``lowp_compute_scales`` / ``lowp_snap_scale`` /
+  ``lowp_quantize`` applied to the activation, then ``lowp_scaled_matmul``,
+  acc += (a_s * b_s) * sum_k dec(a) dec(b)): the activation is packed exactly
+  as a weight of that format (amax / max_finite in float32, E8M0 snapped up,
+  round-to-nearest-even saturating codes) and the product of the two exact
+  dequantized operands is taken in float64.
 * qmm_gather: expert-routed rows over one stacked [E * N, K] weight, row m
   against rows [e N, e N + N) with e = expert_idx[m] -- PR #250, the MoE
   gather-qmm commit (weight row expert_ids[m] * out_dim + n, one stacked
@@ -66,10 +73,14 @@ from __future__ import annotations
 import numpy as np
 
 from . import codec
-from .pack import BLOCK, ELEM_BITS, FORMATS, INTN, SCALE_BYTES
+from .pack import BLOCK, ELEM_BITS, FORMATS, INTN, SCALE_BYTES, pack
 
 BOUND_REL = 2e-3
 BOUND_ABS = 1e-6
+# The quantized-activation product is exact up to float32 accumulation: K
+# terms summed in float32 are within K u (u = 2^-24) of the exact sum, relative
+# to the sum of the terms' magnitudes; K <= 4096 gives 2^-12.
+A8_REL = 2.0 ** -12
 
 
 def unpack_codes(fmt: str, codes: np.ndarray, n: int, k: int) -> np.ndarray:
@@ -254,3 +265,27 @@ def qmm_rmsnorm_ref(fmt, codes, scales, global_scale, x, x_dtype, gamma_bits, ep
     bound = BOUND_REL * (np.abs(xt) @ np.abs(w).T) + BOUND_ABS
     return ref, bound
 
+
+
+def quantize_activations(fmt, x, x_dtype, m, k):
+    """(codes, scales) of the activation X [M, K] packed as a weight of ``fmt`` (mxfp4 / mxfp8 E4M3 / E5M2).
+
+    bf16 and float32 values are exact in float32, so the packer sees X itself.
+    """
+    if fmt not in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2"):
+        raise ValueError(fmt)
+    xv = x_values(x, x_dtype).reshape(m, k).astype(np.float32)
+    c, s, _ = pack(fmt, xv)
+    return c, s
+
+
+def qmm_a8_ref(fmt, codes, scales, global_scale, x, x_dtype, m, n, k):
+    """(ref, bound) of the both-operands-quantized product: X8 . dequant(W)^T, X8 the MXFP8 E4M3 activation.
+
+    ref is exact in float64; the bound is the float32 accumulation's,
+    A8_REL * sum_k |x8||w| + BOUND_ABS.
+    """
+    xc, xs = quantize_activations("mxfp8_e4m3", x, x_dtype, m, k)
+    x8 = dequant_exact("mxfp8_e4m3", xc, xs, 1.0, m, k)
+    w = dequant_exact(fmt, codes, scales, global_scale, n, k)
+    return x8 @ w.T, A8_REL * (np.abs(x8) @ np.abs(w).T) + BOUND_ABS

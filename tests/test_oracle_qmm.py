@@ -563,3 +563,126 @@ def test_ragged_int4_group_round_trips_exactly():
     c, s_, g = pack.pack("int4_affine", w)
     assert c.shape == (n, k // 2) and s_.shape == (n, 2 * 4)
     assert np.array_equal(reference.dequant_exact("int4_affine", c, s_, g, n, k), w.astype(np.float64))
+
+
+# ------------------- both operands quantized: the W . A8 product ---------------
+
+_E4M3_VALUES = None
+
+
+def _e4m3_table():
+    """Every finite E4M3 code and its exact value, from torch's float8_e4m3fn (a library decode)."""
+    global _E4M3_VALUES
+    if _E4M3_VALUES is None:
+        codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+        vals = codes.view(torch.float8_e4m3fn).double().numpy()
+        _E4M3_VALUES = [(int(c), Fraction(float(v))) for c, v in enumerate(vals) if np.isfinite(v)]
+    return _E4M3_VALUES
+
+
+def _brute_e4m3(v: Fraction) -> int:
+    # nearest finite E4M3 value, an exact tie to the code with mantissa bit 0,
+    # beyond +-448 the largest; the sign bit copies v's sign (zero keeps +)
+    best = None
+    for c, val in _e4m3_table():
+        if (c & 0x80) != (0x80 if v < 0 else 0):
+            continue
+        d = abs(val - v)
+        key = (d, c & 1)
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1]
+
+
+def _brute_activation_quant(xrow):
+    # one row: per block of 32, s = float32(amax / 448) (1 for a zero block),
+    # e = the smallest integer with 2^e >= s, codes of float32(x / 2^e)
+    codes, scodes = [], []
+    for b in range(0, len(xrow), 32):
+        blk = np.asarray(xrow[b:b + 32], np.float32)
+        amax = np.float32(np.max(np.abs(blk)))
+        s = Fraction(float(np.float32(amax / np.float32(448.0)))) if amax > 0 else Fraction(1)
+        e = -127
+        while Fraction(2) ** e < s:
+            e += 1
+        scodes.append(e + 127)
+        for v in blk:
+            q = np.float32(v) / np.float32(2.0 ** e)
+            codes.append(_brute_e4m3(Fraction(float(q))))
+    return codes, scodes
+
+
+def test_activation_quantizer_matches_brute_force():
+    rng = np.random.default_rng(3)
+    m, k = 3, 96
+    x = rng.standard_normal((m, k)).astype(np.float32)
+    x[0] *= np.float32(1e-3)
+    x[1, 32:64] = 0.0                                                    # a zero block: scale 1.0
+    x[2, :32] = np.float32(448.0) * np.float32(2.0 ** -5)                # amax / 448 exactly a power of two
+    xb = synth.f32_to_bf16_bits(x)
+    c, s = reference.quantize_activations("mxfp8_e4m3", xb, "bf16", m, k)
+    xv = reference.x_values(xb, "bf16").reshape(m, k)
+    for i in range(m):
+        bc, bs = _brute_activation_quant(xv[i])
+        assert list(c[i]) == bc, i
+        assert list(s[i]) == bs, i
+
+
+def test_a8_product_matches_exact_rational_brute_force():
+    fmt, m, n, k = "mxfp4", 2, 3, 64
+    cw, sw, g = _tiny_case(fmt, m=m, n=n, k=k, seed=4)[:3]
+    xb = synth.activations_bf16(m, k, seed=5)
+    ref, bound = reference.qmm_a8_ref(fmt, cw, sw, g, xb, "bf16", m, n, k)
+    xv = reference.x_values(xb, "bf16").reshape(m, k)
+    for i in range(m):
+        xc, xs = _brute_activation_quant(xv[i])
+        vals = dict(_e4m3_table())
+        x8 = [vals[xc[kk]] * Fraction(2) ** (xs[kk // 32] - 127) for kk in range(k)]
+        for j in range(n):
+            exact = sum(x8[kk] * _lib_elem(fmt, _code(fmt, cw[j], kk)) * _lib_scale(fmt, sw, j, kk // 32)[0]
+                        for kk in range(k))
+            assert ref[i, j] == float(exact)
+            assert bound[i, j] > 0
+
+
+def _representable_activations(m, k, seed):
+    # every block: E4M3 values times one power of two, its largest magnitude in
+    # (224, 448], so the packer's scale is that power and the codes its values
+    rng = np.random.default_rng(seed)
+    finite = np.array([float(v) for c, v in _e4m3_table() if c < 0x7F], np.float64)
+    x = np.empty((m, k), np.float32)
+    for i in range(m):
+        for b in range(0, k, 32):
+            e = int(rng.integers(-20, 20))
+            v = rng.choice(finite, 32) * rng.choice([-1.0, 1.0], 32)
+            v[int(rng.integers(0, 32))] = rng.choice([256.0, 288.0, 448.0, 240.0])
+            x[i, b:b + 32] = (v * 2.0 ** e).astype(np.float32)
+    return synth.f32_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8_e4m3", "nvfp4", "int4_affine"])
+def test_a8_is_the_exact_product_when_x_is_representable(fmt):
+    # quantizing an activation that is already MXFP8 E4M3 changes nothing: the
+    # W . A8 reference equals the exact bf16-activation reference bit for bit
+    m, n, k = 3, 7, 128
+    xb = _representable_activations(m, k, seed=6)
+    c, s, g = pack.pack(fmt, synth.weights(n, k, seed=7, outliers=(fmt == "nvfp4")))
+    a8, _ = reference.qmm_a8_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    exact, _ = reference.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    assert np.array_equal(a8, exact)
+
+
+def test_planted_activation_quantizer_mistake_is_caught(monkeypatch):
+    # snapping the activation scale down (floor) instead of up saturates the
+    # block maximum: the representable-activation identity fails
+    from oracle import codec
+    real = codec.e8m0_encode_ceil
+
+    def floor_snap(s):
+        c = real(s)
+        exact_pow2 = np.asarray(codec.E8M0_TABLE[c], np.float32) == np.asarray(s, np.float32)
+        return np.where(exact_pow2, c, c - 1).astype(c.dtype)
+
+    monkeypatch.setattr(codec, "e8m0_encode_ceil", floor_snap)
+    with pytest.raises(AssertionError):
+        test_a8_is_the_exact_product_when_x_is_representable("mxfp4")

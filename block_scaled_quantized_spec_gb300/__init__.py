@@ -20,7 +20,7 @@ __all__ = [
     "FORMATS", "QfmtError", "load", "lib_path",
     "qfmt_block_size", "qfmt_codes_bytes", "qfmt_scales_bytes",
     "qfmt_pack", "qfmt_dequant", "qmm", "qmm_ex", "qmm_workspace_bytes", "qmm_gather", "qmm_batched", "qmm_rmsnorm",
-    "qmm_gated_rmsnorm", "qmm_noalloc",
+    "qmm_gated_rmsnorm", "qmm_noalloc", "qfmt_quantize", "qmm_a8", "qmm_a8_workspace_bytes",
     "qfmt_last_error",
     "qfmt_version", "qfmt_device_status", "qfmt_debug_set",
 ]
@@ -65,6 +65,12 @@ _SIGS = {
                               ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                               ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "qmm_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
+    "qfmt_quantize": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
+    "qmm_a8": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                              ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                              ctypes.c_size_t, ctypes.c_void_p]),
+    "qmm_a8_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
     "qmm_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                    ctypes.c_void_p]),
@@ -309,6 +315,50 @@ def qmm_ex(fmt, codes, scales, global_scale: float, x, N: int, out=None, out_dty
     od = F32 if out.dtype == torch.float32 else BF16
     _check(load().qmm_ex(_fmt(fmt), _ptr(codes), _ptr(scales), float(global_scale), _ptr(x), xd, _ptr(out), od,
                          M, N, K, group, _ptr(workspace), ws_bytes, _stream(stream)), where)
+    return out
+
+
+def qfmt_quantize(fmt, x, codes=None, scales=None, stream=None):
+    """Device: an activation [M, K] (bf16 or float32) packed as a weight of an MX format -> (codes, scales)."""
+    import torch
+    where = "qfmt_quantize"
+    M, K = _activations(where, x, (torch.bfloat16, torch.float32))
+    cb = _size(load().qfmt_codes_bytes(_fmt(fmt), M, K, 0), where)
+    sb = _size(load().qfmt_scales_bytes(_fmt(fmt), M, K, 0), where)
+    if codes is None:
+        codes = torch.empty((M, cb // max(M, 1)), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((M, sb // max(M, 1)), dtype=torch.uint8, device=x.device)
+    _tensor(codes, where, "codes", nbytes=cb)
+    _tensor(scales, where, "scales", nbytes=sb)
+    _on_device(where, x=x, codes=codes, scales=scales)
+    _check(load().qfmt_quantize(_fmt(fmt), _ptr(x), F32 if x.dtype == torch.float32 else BF16, _ptr(codes),
+                                _ptr(scales), M, K, _stream(stream)), where)
+    return codes, scales
+
+
+def qmm_a8_workspace_bytes(fmt, M: int, K: int) -> int:
+    return load().qmm_a8_workspace_bytes(_fmt(fmt), M, K)
+
+
+def qmm_a8(fmt, codes, scales, x, N: int, out=None, out_dtype=None, workspace=None, stream=None):
+    """out [M, N] = Q(x) . dequant(W)^T, Q(x) the activation packed to MXFP8 E4M3 (both operands quantized)."""
+    import torch
+    where = "qmm_a8"
+    M, K = _activations(where, x)
+    _weights(where, fmt, codes, scales, N, K, 0)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=x.device)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        _fail(where, f"out must be float32 or bfloat16 (is {out.dtype})")
+    _tensor(out, where, "out", shape=(M, N))
+    if workspace is None:
+        workspace = torch.empty(max(1, qmm_a8_workspace_bytes(fmt, M, K)), dtype=torch.uint8, device=x.device)
+    _tensor(workspace, where, "workspace")
+    _on_device(where, x=x, codes=codes, scales=scales, out=out, workspace=workspace)
+    _check(load().qmm_a8(_fmt(fmt), _ptr(codes), _ptr(scales), _ptr(x), _ptr(out),
+                         F32 if out.dtype == torch.float32 else BF16, M, N, K, _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(stream)), where)
     return out
 
 

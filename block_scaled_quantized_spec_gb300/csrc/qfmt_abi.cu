@@ -297,6 +297,59 @@ int qfmt_debug_set(int key, int64_t value) {
   return fail(QFMT_EINVAL, "unknown debug key %d", key);
 }
 
+int qfmt_quantize(int fmt, const void* x, int x_dtype, void* codes, void* scales, int64_t M, int64_t K,
+                  void* stream) {
+  clear_error();
+  int st = check_group(fmt, 0);
+  if (st) return st;
+  if (fmt != QFMT_MXFP4 && fmt != QFMT_MXFP8_E4M3 && fmt != QFMT_MXFP8_E5M2)
+    return fail(QFMT_EUNSUPPORTED, "qfmt_quantize takes mxfp4, mxfp8 E4M3 or E5M2 (format %d)", fmt);
+  if ((st = check_shape(fmt, 0, M, K))) return st;
+  if (x_dtype != QFMT_F32 && x_dtype != QFMT_BF16) return fail(QFMT_EINVAL, "bad x_dtype %d", x_dtype);
+  if (M == 0 || K == 0) return QFMT_OK;
+  if ((st = check_ptr(x, 16, "x"))) return st;
+  if ((st = check_ptr(codes, 16, "codes"))) return st;
+  if ((st = check_ptr(scales, 1, "scales"))) return st;
+  return cuda_status(qfmt_dev::launch_quantize(fmt, x, x_dtype == QFMT_F32, codes, scales, M, K,
+                                               static_cast<cudaStream_t>(stream)),
+                     "quantize launch");
+}
+
+size_t qmm_a8_workspace_bytes(int fmt, int64_t M, int64_t K) {
+  clear_error();
+  if (fmt != QFMT_MXFP4 && fmt != QFMT_MXFP8_E4M3 && fmt != QFMT_MXFP8_E5M2) return 0;
+  if (M <= 0 || K <= 0 || K % 128) return 0;
+  return qfmt_dev::qgemm_a8_workspace_bytes(M, K);
+}
+
+int qmm_a8(int fmt, const void* codes, const void* scales, const void* x, void* out, int out_dtype, int64_t M,
+           int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  int st = check_group(fmt, 0);
+  if (st) return st;
+  if (fmt != QFMT_MXFP4 && fmt != QFMT_MXFP8_E4M3 && fmt != QFMT_MXFP8_E5M2)
+    return fail(QFMT_EUNSUPPORTED, "qmm_a8 takes mxfp4, mxfp8 E4M3 or E5M2 weights (format %d)", fmt);
+  if ((st = check_shape(fmt, M, N, K))) return st;
+  if (out_dtype != QFMT_F32 && out_dtype != QFMT_BF16) return fail(QFMT_EINVAL, "bad out_dtype %d", out_dtype);
+  if (M == 0 || N == 0) return QFMT_OK;
+  if (K % 128) return fail(QFMT_ESHAPE, "qmm_a8: K=%lld must be a multiple of 128", (long long)K);
+  if (M > 65535LL * 128) return fail(QFMT_ESHAPE, "M=%lld: more than 65535 row tiles of 128", (long long)M);
+  const size_t need = qfmt_dev::qgemm_a8_workspace_bytes(M, K);
+  if (!workspace || workspace_bytes < need)
+    return fail(QFMT_ENOSPACE, "workspace of %zu bytes, qmm_a8 needs %zu", workspace_bytes, need);
+  if ((st = check_ptr(codes, fmt == QFMT_MXFP4 ? 32 : 16, "codes"))) return st;
+  if ((st = check_ptr(scales, 4, "scales"))) return st;
+  if ((st = check_ptr(x, 16, "x"))) return st;
+  if ((st = check_ptr(out, 16, "out"))) return st;
+  if ((st = check_ptr(workspace, 128, "workspace"))) return st;
+  int err = QFMT_OK;
+  const int sms = device_sms(&err);
+  if (err) return err;
+  return cuda_status(qfmt_dev::launch_qgemm_a8(fmt, codes, scales, x, out, out_dtype == QFMT_F32, M, N, K, workspace,
+                                               static_cast<cudaStream_t>(stream), sms),
+                     "qmm_a8 launch");
+}
+
 size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t K) {
   clear_error();
   if (!valid_format(fmt) || M < 0 || K < 0) return 0;

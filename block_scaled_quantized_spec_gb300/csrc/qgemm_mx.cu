@@ -249,10 +249,12 @@ template <int F> constexpr uint32_t b_type() {
 }
 
 // BN: the tile's N (256, or 224 where that fills the waves of 152 SMs better).
+// TWO: the activations as two E4M3 terms (hi + lo, two MMAs per block), else
+// one (the quantized-activation product: one MMA per block).
 // A K split runs its splits as a cluster along z; each split's float32
 // partial tile goes to its drained stage memory and the cluster sums them
 // through distributed shared memory in rank order.
-template <int F, int BN>
+template <int F, int BN, bool TWO = true>
 __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_constant__ CUtensorMap xhi_map,
                                                               const __grid_constant__ CUtensorMap xlo_map,
                                                               const __grid_constant__ CUtensorMap w_map,
@@ -261,7 +263,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
   // bytes a stage's copies deliver: the two X terms, the W codes (E2M1: the
   // 8 data bytes of every 16-byte unit, the gaps are not written) and the two
   // X scale atoms
-  constexpr uint32_t TX_BYTES = 2 * A_BYTES + (F == MXFP4 ? BN * BK / 2 : BN * BK) + 2 * SF_BYTES;
+  constexpr int TERMS = TWO ? 2 : 1;
+  constexpr uint32_t TX_BYTES = TERMS * (A_BYTES + SF_BYTES) + (F == MXFP4 ? BN * BK / 2 : BN * BK);
   constexpr int PSTRIDE = BN + 4;                 // floats per partial-tile row (K split)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -331,10 +334,10 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         if (!mbar_wait(empty(s), ph ^ 1u, p.limit_ns)) { fail(); break; }
         mbar_arrive_expect_tx(full(s), TX_BYTES);
         tma_load_2d(a_hi(s), &xhi_map, j * BK, m0, full(s));
-        tma_load_2d(a_lo(s), &xlo_map, j * BK, m0, full(s));
+        if constexpr (TWO) tma_load_2d(a_lo(s), &xlo_map, j * BK, m0, full(s));
         tma_load_2d(b_tile(s), &w_map, j * BK, n0, full(s));
         bulk_load(sf_s(s, 0), sfh + size_t(j) * SF_BYTES, SF_BYTES, full(s));
-        bulk_load(sf_s(s, 1), sfl + size_t(j) * SF_BYTES, SF_BYTES, full(s));
+        if constexpr (TWO) bulk_load(sf_s(s, 1), sfl + size_t(j) * SF_BYTES, SF_BYTES, full(s));
         issued = i + 1;
       }
       // every issued copy lands before the CTA may exit
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         tc_fence_after();
         const uint32_t sfc = tmem + uint32_t(SF_COL0 + 16 * s);   // hi: +0, lo: +4, W: +8 (rows 0-127), +12 (128-255)
         tmem_cp_sf(sfc + 0, umma::smem_desc_sf32x16(sf_s(s, 0)));
-        tmem_cp_sf(sfc + 4, umma::smem_desc_sf32x16(sf_s(s, 1)));
+        if constexpr (TWO) tmem_cp_sf(sfc + 4, umma::smem_desc_sf32x16(sf_s(s, 1)));
         tmem_cp_sf(sfc + 8, umma::smem_desc_sf32x16(sf_s(s, 2)));
         tmem_cp_sf(sfc + 12, umma::smem_desc_sf32x16(sf_s(s, 3)));
         const uint64_t dh = desc_sw128(a_hi(s)), dl = desc_sw128(a_lo(s)), db = desc_sw128(b_tile(s));
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         for (int kk = 0; kk < BK / 32; ++kk) {   // +32 bytes along K per instruction
           const uint32_t id = umma::idesc_mxf8f6f4(umma::F8F6F4_E4M3, BT, BM, BN, uint32_t(kk), uint32_t(kk));
           mma_mx(tmem, dh + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 0, sfc + 8, (i | kk) != 0);
-          mma_mx(tmem, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 4, sfc + 8, 1u);
+          if constexpr (TWO) mma_mx(tmem, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 4, sfc + 8, 1u);
         }
         mma_commit(empty(s));
       }
@@ -559,12 +562,12 @@ struct MxPlan {
   int BN, S;
 };
 
-template <int F, int BN>
+template <int F, int BN, bool TWO = true>
 static cudaError_t set_smem(int dev) {
   static std::atomic<int> done[64];
   if (dev < 0 || dev >= 64 || done[dev].load()) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[dev].store(1);
   return e;
 }
@@ -619,7 +622,7 @@ static MxPlan plan_mx(int dev, int M, int N, int K, int sms) {
   return best;
 }
 
-template <int F, int BN>
+template <int F, int BN, bool TWO = true>
 static cudaError_t launch_tile(const CUtensorMap& mhi, const CUtensorMap& mlo, const CUtensorMap& mw, MxParams prm,
                                int M, int N, int S, cudaStream_t st) {
   const int nk = prm.K / BK;
@@ -638,7 +641,7 @@ static cudaError_t launch_tile(const CUtensorMap& mhi, const CUtensorMap& mlo, c
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 2;
-  return cudaLaunchKernelEx(&lc, qgemm_mx_kernel<F, BN>, mhi, mlo, mw, prm);
+  return cudaLaunchKernelEx(&lc, qgemm_mx_kernel<F, BN, TWO>, mhi, mlo, mw, prm);
 }
 
 template <int F>
@@ -694,6 +697,50 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, const void*
   prm.drop_arrivals = g_drop.load();
   if (pl.BN == 224) return launch_tile<F, 224>(mhi, mlo, mw, prm, M, N, pl.S, st);
   return launch_tile<F, 256>(mhi, mlo, mw, prm, M, N, pl.S, st);
+}
+
+// The quantized-activation product (both operands block-scaled): X packed to
+// MXFP8 E4M3 by the packer's rule into the workspace (codes, then scale
+// atoms), then one MMA per block.
+inline size_t a8_codes_bytes(int64_t M, int64_t K) { return align1k(size_t(M) * size_t(K)); }
+inline size_t a8_workspace_bytes(int64_t M, int64_t K) {
+  return a8_codes_bytes(M, K) + align1k(size_t((M + BM - 1) / BM) * size_t(K / BK) * SF_BYTES);
+}
+
+template <int F>
+static cudaError_t launch_a8(const void* codes, const void* scales, const void* x, void* out, bool out_f32, int M,
+                             int N, int K, void* ws, cudaStream_t st, int sms) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = set_smem<F, 256>(dev)) != cudaSuccess || (e = set_smem<F, 256, false>(dev)) != cudaSuccess ||
+      (e = set_smem<F, 224, false>(dev)) != cudaSuccess)
+    return e;
+  MxPlan pl = plan_mx<F>(dev, M, N, K, sms > 0 ? sms : 1);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  if ((e = launch_quantize_e4m3_atoms(x, w8, w8 + a8_codes_bytes(M, K), M, K, st)) != cudaSuccess) return e;
+  CUtensorMap mx8, mw;
+  if (!make_map(enc, &mx8, CU_TENSOR_MAP_DATA_TYPE_UINT8, w8, K, M, K, BM)) return cudaErrorInvalidValue;
+  const bool ok = F == MXFP4
+                      ? make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, K, N, K / 2, uint32_t(pl.BN))
+                      : make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, N, K, uint32_t(pl.BN));
+  if (!ok) return cudaErrorInvalidValue;
+  MxParams prm;
+  prm.wscales = static_cast<const uint8_t*>(scales);
+  prm.sf_hi = w8 + a8_codes_bytes(M, K);
+  prm.sf_lo = prm.sf_hi;
+  prm.out = out;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.out_f32 = out_f32 ? 1 : 0;
+  prm.kb_per = K / BK;
+  prm.limit_ns = g_limit_ns.load();
+  prm.drop_arrivals = g_drop.load();
+  if (pl.BN == 224) return launch_tile<F, 224, false>(mx8, mx8, mw, prm, M, N, pl.S, st);
+  return launch_tile<F, 256, false>(mx8, mx8, mw, prm, M, N, pl.S, st);
 }
 
 // ------------------------------------------------ decode GEMV, M <= 16 ---
@@ -992,6 +1039,19 @@ cudaError_t launch_qgemv_mx(int fmt, const void* codes, const void* scales, cons
     case MXFP4: return mx::launch_gemv<MXFP4>(codes, scales, x, out, out_f32, m, n, k, st);
     case MXFP8_E4M3: return mx::launch_gemv<MXFP8_E4M3>(codes, scales, x, out, out_f32, m, n, k, st);
     case MXFP8_E5M2: return mx::launch_gemv<MXFP8_E5M2>(codes, scales, x, out, out_f32, m, n, k, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+size_t qgemm_a8_workspace_bytes(int64_t M, int64_t K) { return mx::a8_workspace_bytes(M, K); }
+
+cudaError_t launch_qgemm_a8(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
+                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st, int sms) {
+  const int m = int(M), n = int(N), k = int(K);
+  switch (fmt) {
+    case MXFP4: return mx::launch_a8<MXFP4>(codes, scales, x, out, out_f32, m, n, k, workspace, st, sms);
+    case MXFP8_E4M3: return mx::launch_a8<MXFP8_E4M3>(codes, scales, x, out, out_f32, m, n, k, workspace, st, sms);
+    case MXFP8_E5M2: return mx::launch_a8<MXFP8_E5M2>(codes, scales, x, out, out_f32, m, n, k, workspace, st, sms);
     default: return cudaErrorInvalidValue;
   }
 }

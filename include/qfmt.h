@@ -227,6 +227,43 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale,
 size_t qmm_workspace_bytes(int fmt, int64_t M, int64_t K);
 
 /*
+ * qfmt_quantize -- device: an activation X [M, K] (bf16 or float32, per
+ * x_dtype; 16-byte aligned) packed as a weight of `fmt` (QFMT_MXFP4,
+ * QFMT_MXFP8_E4M3 or QFMT_MXFP8_E5M2): codes [M, K] bytes (mxfp4: [M, K/2],
+ * 16-byte aligned) and E8M0 scales [M, K/32], the same bytes qfmt_pack gives
+ * for that matrix (rlx-cpu thunk/ops/quant.rs lowp_compute_scales /
+ * lowp_snap_scale / lowp_quantize, the activation side of lowp_scaled_matmul:
+ * per block of 32, s = amax / max_finite in float32, 1.0 for a zero block;
+ * the scale the smallest power of two >= s; codes the nearest-even,
+ * saturating encoding of x / scale).  A block holding an infinity or a NaN
+ * gets the scale 255 (NaN).  K a multiple of 32.  Asynchronous on `stream`.
+ */
+int qfmt_quantize(int fmt, const void* x, int x_dtype, void* codes, void* scales, int64_t M, int64_t K,
+                  void* stream);
+
+/*
+ * qmm_a8 -- device, both operands quantized (rlx-cpu thunk/ops/quant.rs
+ * lowp_scaled_matmul: acc += (a_s * b_s) * sum_k dec(a) dec(b)):
+ *   out[M, N] = Q(X) . dequant(W)^T
+ * with Q(X) the activation packed to MXFP8 E4M3 as qfmt_quantize packs it,
+ * W mxfp4 / mxfp8 E4M3 / E5M2, one tcgen05.mma kind::mxf8f6f4 per block of
+ * 32 (the FP8 rate; qmm_ex's exact path takes two).  This is a different
+ * product from qmm's: the activation carries E4M3's rounding (up to 2^-4 of
+ * each value).  Result within 2^-12 * sum_k |q(x)||w| + 1e-6 of the exact
+ * Q(X) . W^T (float32 accumulation).  x bf16 [M, K]; out bf16 or float32
+ * per out_dtype; K a multiple of 128; workspace of at least
+ * qmm_a8_workspace_bytes(fmt, M, K) bytes, 128-byte aligned, else
+ * QFMT_ENOSPACE (scratch: ordered on one stream between calls); mxfp4 codes
+ * 32-byte aligned.  Any M >= 1.
+ */
+int qmm_a8(int fmt, const void* codes, const void* scales, const void* x, void* out, int out_dtype, int64_t M,
+           int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream);
+/* Workspace bytes of qmm_a8: align(M K) + align(M' K / 32), M' = M rounded
+ * up to 128, each part 1 KiB aligned; 0 for another format or K not a
+ * positive multiple of 128. */
+size_t qmm_a8_workspace_bytes(int fmt, int64_t M, int64_t K);
+
+/*
  * qmm_noalloc -- qmm_ex's block-scaled tensor-core GEMM (mxfp4, mxfp8 E4M3 /
  * E5M2; M > 16; K a multiple of 128; bf16 X and out) for callers that cannot
  * allocate device memory for scratch: an inference engine's plugin interface

@@ -462,8 +462,11 @@ ORACLE_CONFIGS = [("mxfp4", 8, 16, 512, "f32"), ("mxfp4", 1, 4096, 4096, "bf16")
 
 
 # Expert-routed rows (MoE gather-qmm): one token's top-8 routing over 8 experts
-# of [4096, 4096] mxfp4 weights, each row to a different expert.
+# of [4096, 4096] mxfp4 weights, each row to a different expert; and prefill
+# batches of 64 and 512 rows routed uniformly over the 8 experts, grouped by
+# expert on the tensor cores (qmm_grouped).
 GATHER = [("mxfp4", 8, 4096, 4096, 8)]
+GROUPED = [("mxfp4", 64, 4096, 4096, 8), ("mxfp4", 512, 4096, 4096, 8)]
 
 
 class GatherProblem:
@@ -483,18 +486,27 @@ class GatherProblem:
         self.scales = [ds] + [ds.clone() for _ in range(copies - 1)]
         xb = synth.activations_bf16(m, k, rng=rng)
         self.x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
-        self.idx = [torch.from_numpy(rng.permutation(e)[:m].astype(np.int32)).cuda() for _ in range(copies)]
+        if m <= e:   # one token's routing: m distinct experts
+            self.idx = [torch.from_numpy(rng.permutation(e)[:m].astype(np.int32)).cuda() for _ in range(copies)]
+        else:        # a prefill batch routed uniformly
+            self.idx = [torch.from_numpy(rng.integers(0, e, m).astype(np.int32)).cuda() for _ in range(copies)]
         self.out = [torch.empty((m, n), dtype=torch.bfloat16, device="cuda") for _ in range(copies)]
         self.copies = copies
         experts = len(set(int(v) for v in self.idx[0].cpu()))
         self.bytes = experts * (sizes(fmt, 0, n, k) - (4 if fmt == "nvfp4" else 0)) + 2 * m * k + 2 * m * n + \
             4 * m + (4 if fmt == "nvfp4" else 0)
 
+    grouped = False
+
     def step(self):
         import block_scaled_quantized_spec_gb300 as q
         for i in range(self.copies):
-            q.qmm_gather(self.fmt, self.codes[i], self.scales[i], self.g, self.x, self.idx[i], self.n, self.e,
-                         out=self.out[i])
+            if self.grouped:
+                q.qmm_grouped(self.fmt, self.codes[i], self.scales[i], self.x, self.idx[i], self.n, self.e,
+                              out=self.out[i], workspace=self.ws)
+            else:
+                q.qmm_gather(self.fmt, self.codes[i], self.scales[i], self.g, self.x, self.idx[i], self.n, self.e,
+                             out=self.out[i])
 
     graph = Problem.graph
 
@@ -568,15 +580,20 @@ def fused_row(kind, fmt, m, ns, k, hbm, steps=10, warmup=3):
     return row
 
 
-def gather_row(fmt, m, n, k, e, hbm, steps=10, warmup=3):
+def gather_row(fmt, m, n, k, e, hbm, steps=10, warmup=3, grouped=False):
     import torch
+    import block_scaled_quantized_spec_gb300 as q
     per_call = sizes(fmt, 0, n, k) * min(m, e)
     prob = GatherProblem(fmt, m, n, k, e, max(2, -(-3 * L2_BYTES // per_call)))
+    if grouped:
+        prob.grouped = True
+        prob.ws = torch.empty(q.qmm_grouped_workspace_bytes(fmt, m, k, e), dtype=torch.uint8, device="cuda")
     g = prob.graph()
     ms, _ = time_graph(g, steps, warmup, 1)
     per = ms / prob.copies
     gbs = prob.bytes / (per * 1e-3) / 1e9
-    row = {"op": "qmm_gather", "fmt": fmt, "M": m, "N": n, "K": k, "E": e, "us": round(per * 1e3, 2),
+    row = {"op": "qmm_grouped" if grouped else "qmm_gather", "fmt": fmt, "M": m, "N": n, "K": k, "E": e,
+           "us": round(per * 1e3, 2),
            "copies": prob.copies, "GB/s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
            "bytes": prob.bytes}
     del prob, g
@@ -703,9 +720,10 @@ def main():
     copies = copies_for(nbytes, m) if args.only is None else 4
     if args.only:
         parts = args.only.split(":")
-        if parts[0] == "gather":          # gather:fmt:M:N:K:E
+        if parts[0] in ("gather", "grouped"):   # gather:fmt:M:N:K:E / grouped:fmt:M:N:K:E
             f, mm, nn, kk, ee = parts[1:]
-            print(json.dumps(gather_row(f, int(mm), int(nn), int(kk), int(ee), hbm, args.steps, args.warmup)))
+            print(json.dumps(gather_row(f, int(mm), int(nn), int(kk), int(ee), hbm, args.steps, args.warmup,
+                                        grouped=parts[0] == "grouped")))
             return
         if parts[0] in ("batched", "rmsnorm", "gated_rmsnorm"):   # batched:fmt:M:N1,N2,..:K  /  rmsnorm:fmt:M:N:K
             f, mm, nn, kk = parts[1:]
@@ -756,6 +774,8 @@ def main():
             rows.append(dequant_row(f, nn, kk, od, hbm))
         for (f, mm, nn, kk, ee) in GATHER:
             rows.append(gather_row(f, mm, nn, kk, ee, hbm))
+        for (f, mm, nn, kk, ee) in GROUPED:
+            rows.append(gather_row(f, mm, nn, kk, ee, hbm, grouped=True))
         for (kind, f, mm, ns, kk) in FUSED:
             rows.append(fused_row(kind, f, mm, ns, kk, hbm))
         line["breakdown"] = rows

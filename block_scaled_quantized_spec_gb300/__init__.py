@@ -20,7 +20,8 @@ __all__ = [
     "FORMATS", "QfmtError", "load", "lib_path",
     "qfmt_block_size", "qfmt_codes_bytes", "qfmt_scales_bytes",
     "qfmt_pack", "qfmt_dequant", "qmm", "qmm_ex", "qmm_workspace_bytes", "qmm_gather", "qmm_batched", "qmm_rmsnorm",
-    "qmm_gated_rmsnorm", "qmm_noalloc", "qfmt_quantize", "qmm_a8", "qmm_a8_workspace_bytes",
+    "qmm_gated_rmsnorm", "qmm_noalloc", "qfmt_quantize", "qmm_a8", "qmm_a8_workspace_bytes", "qmm_grouped",
+    "qmm_grouped_workspace_bytes",
     "qfmt_last_error",
     "qfmt_version", "qfmt_device_status", "qfmt_debug_set",
 ]
@@ -71,6 +72,10 @@ _SIGS = {
                               ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                               ctypes.c_size_t, ctypes.c_void_p]),
     "qmm_a8_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
+    "qmm_grouped": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "qmm_grouped_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]),
     "qmm_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                    ctypes.c_void_p]),
@@ -359,6 +364,37 @@ def qmm_a8(fmt, codes, scales, x, N: int, out=None, out_dtype=None, workspace=No
     _check(load().qmm_a8(_fmt(fmt), _ptr(codes), _ptr(scales), _ptr(x), _ptr(out),
                          F32 if out.dtype == torch.float32 else BF16, M, N, K, _ptr(workspace),
                          workspace.numel() * workspace.element_size(), _stream(stream)), where)
+    return out
+
+
+def qmm_grouped_workspace_bytes(fmt, M: int, K: int, E: int) -> int:
+    return load().qmm_grouped_workspace_bytes(_fmt(fmt), M, K, E)
+
+
+def qmm_grouped(fmt, codes, scales, x, expert_idx, N: int, E: int, out=None, out_dtype=None, workspace=None,
+                stream=None):
+    """out [M, N]: row m = x[m] . dequant(W[expert_idx[m] N : + N])^T, rows of one expert grouped on the tensor cores."""
+    import torch
+    where = "qmm_grouped"
+    M, K = _activations(where, x)
+    if E < 1:
+        _fail(where, f"expert count E={E} must be >= 1")
+    _weights(where, fmt, codes, scales, E * N, K, 0)
+    _tensor(expert_idx, where, "expert_idx", dtype=torch.int32)
+    if expert_idx.numel() != M:
+        _fail(where, "expert_idx must be an int32 tensor of M entries")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=x.device)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        _fail(where, f"out must be float32 or bfloat16 (is {out.dtype})")
+    _tensor(out, where, "out", shape=(M, N))
+    if workspace is None:
+        workspace = torch.empty(max(1, qmm_grouped_workspace_bytes(fmt, M, K, E)), dtype=torch.uint8, device=x.device)
+    _tensor(workspace, where, "workspace")
+    _on_device(where, x=x, codes=codes, scales=scales, expert_idx=expert_idx, out=out, workspace=workspace)
+    _check(load().qmm_grouped(_fmt(fmt), _ptr(codes), _ptr(scales), _ptr(x), _ptr(expert_idx), _ptr(out),
+                              F32 if out.dtype == torch.float32 else BF16, M, N, K, E, _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream)), where)
     return out
 
 

@@ -51,6 +51,13 @@ cudaError_t launch_qgemm_mx(int fmt, const void* codes, const void* scales, cons
 // 1024, mxfp4 codes 32-byte aligned): weights as stored, activations split in
 // the CTA; no workspace.
 bool qgemv_mx_supported(int fmt, int64_t M, int64_t N, int64_t K, const void* codes);
+// Expert-grouped rows on the block-scaled GEMM: a stacked [E N, K] MX weight,
+// row m against expert idx[m]; rows of one expert share the expert's tiles.
+size_t qgemm_grouped_workspace_bytes(int64_t M, int64_t K, int64_t E);
+int qgemm_grouped_max_experts();
+cudaError_t launch_qgemm_grouped(int fmt, const void* codes, const void* scales, const void* x, const int32_t* idx,
+                                 void* out, bool out_f32, int64_t M, int64_t N, int64_t K, int64_t E, void* workspace,
+                                 cudaStream_t st, int sms);
 // The quantized-activation product: X packed to MXFP8 E4M3 (the packer's
 // rule) in `workspace`, then one block-scaled MMA per block (any M >= 1).
 size_t qgemm_a8_workspace_bytes(int64_t M, int64_t K);

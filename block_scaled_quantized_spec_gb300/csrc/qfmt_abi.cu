@@ -264,9 +264,10 @@ int qfmt_device_status(void* stream) {
   if ((st = cuda_status(qfmt_dev::read_and_clear_gather_status(&gx), "device status"))) return st;
   if ((st = cuda_status(qfmt_dev::read_and_clear_mx_status(&mw), "device status"))) return st;
   if (word) return fail(QFMT_ETIMEOUT, "a tensor-core GEMM pipeline wait expired (status 0x%x)", word);
-  if (mw) return fail(QFMT_ETIMEOUT, "a block-scaled GEMM pipeline wait expired (status 0x%x)", mw);
+  if (mw & 1u) return fail(QFMT_ETIMEOUT, "a block-scaled GEMM pipeline wait expired (status 0x%x)", mw);
   if (gw) return fail(QFMT_ETIMEOUT, "a GEMV weight-copy wait expired (status 0x%x)", gw);
-  if (gx) return fail(QFMT_EINDEX, "qmm_gather: an expert index outside [0, E) (its output row was zeroed)");
+  if (gx || (mw & 2u))
+    return fail(QFMT_EINDEX, "qmm_gather / qmm_grouped: an expert index outside [0, E) (its output row was zeroed)");
   return QFMT_OK;
 }
 
@@ -295,6 +296,46 @@ int qfmt_debug_set(int key, int64_t value) {
     return QFMT_OK;
   }
   return fail(QFMT_EINVAL, "unknown debug key %d", key);
+}
+
+size_t qmm_grouped_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t E) {
+  clear_error();
+  if (fmt != QFMT_MXFP4 && fmt != QFMT_MXFP8_E4M3 && fmt != QFMT_MXFP8_E5M2) return 0;
+  if (M <= 0 || K <= 0 || K % 128 || E < 1 || E > qfmt_dev::qgemm_grouped_max_experts()) return 0;
+  return qfmt_dev::qgemm_grouped_workspace_bytes(M, K, E);
+}
+
+int qmm_grouped(int fmt, const void* codes, const void* scales, const void* x, const int32_t* expert_idx, void* out,
+                int out_dtype, int64_t M, int64_t N, int64_t K, int64_t E, void* workspace, size_t workspace_bytes,
+                void* stream) {
+  clear_error();
+  int st = check_group(fmt, 0);
+  if (st) return st;
+  if (fmt != QFMT_MXFP4 && fmt != QFMT_MXFP8_E4M3 && fmt != QFMT_MXFP8_E5M2)
+    return fail(QFMT_EUNSUPPORTED, "qmm_grouped takes mxfp4, mxfp8 E4M3 or E5M2 weights (format %d)", fmt);
+  if ((st = check_shape(fmt, M, N, K))) return st;
+  if (E < 1 || E > qfmt_dev::qgemm_grouped_max_experts())
+    return fail(QFMT_EINVAL, "expert count E=%lld must be in 1..%d", (long long)E, qfmt_dev::qgemm_grouped_max_experts());
+  if (E * N >= (int64_t(1) << 31)) return fail(QFMT_ESHAPE, "E*N weight rows of 2^31 or more");
+  if (out_dtype != QFMT_F32 && out_dtype != QFMT_BF16) return fail(QFMT_EINVAL, "bad out_dtype %d", out_dtype);
+  if (M == 0 || N == 0) return QFMT_OK;
+  if (K % 128) return fail(QFMT_ESHAPE, "qmm_grouped: K=%lld must be a multiple of 128", (long long)K);
+  if (M > 65535LL * 128 / 2) return fail(QFMT_ESHAPE, "M=%lld too large for the grouped tile grid", (long long)M);
+  const size_t need = qfmt_dev::qgemm_grouped_workspace_bytes(M, K, E);
+  if (!workspace || workspace_bytes < need)
+    return fail(QFMT_ENOSPACE, "workspace of %zu bytes, qmm_grouped needs %zu", workspace_bytes, need);
+  if ((st = check_ptr(codes, fmt == QFMT_MXFP4 ? 32 : 16, "codes"))) return st;
+  if ((st = check_ptr(scales, 4, "scales"))) return st;
+  if ((st = check_ptr(x, 16, "x"))) return st;
+  if ((st = check_ptr(out, 16, "out"))) return st;
+  if ((st = check_ptr(expert_idx, 4, "expert_idx"))) return st;
+  if ((st = check_ptr(workspace, 128, "workspace"))) return st;
+  int err = QFMT_OK;
+  const int sms = device_sms(&err);
+  if (err) return err;
+  return cuda_status(qfmt_dev::launch_qgemm_grouped(fmt, codes, scales, x, expert_idx, out, out_dtype == QFMT_F32, M, N,
+                                                    K, E, workspace, static_cast<cudaStream_t>(stream), sms),
+                     "qmm_grouped launch");
 }
 
 int qfmt_quantize(int fmt, const void* x, int x_dtype, void* codes, void* scales, int64_t M, int64_t K,

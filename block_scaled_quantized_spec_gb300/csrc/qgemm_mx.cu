@@ -42,6 +42,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -173,8 +174,12 @@ __device__ __forceinline__ void load_block(const __nv_bfloat16* src, uint32_t (&
 
 // One warp per (row, 32 consecutive blocks of 32): lane l takes block b0 + l.
 // Rows past M (up to the 128-row tile) get neutral scale words only.
+// Grouped rows (row_of != nullptr): workspace row m holds activation row
+// row_of[m] (-1: a padding row, zero), for m below *total (the routing
+// kernel's output).
 __global__ void __launch_bounds__(256) xquant_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ ws,
-                                                     WsLayout lay, int M, int K) {
+                                                     WsLayout lay, int M, int K, const int* __restrict__ row_of,
+                                                     const int* __restrict__ total) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nblk = K / 32, chunks = (nblk + 31) / 32;
@@ -182,11 +187,14 @@ __global__ void __launch_bounds__(256) xquant_kernel(const __nv_bfloat16* __rest
   const int m = warp / chunks, b = (warp - m * chunks) * 32 + lane;
   if (m >= mpad) return;
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (row_of && m >= __ldg(total)) return;
+  const int src = row_of ? __ldg(row_of + m) : m;
   const bool live = b < nblk;
   uint32_t c1 = 127u, c2 = 127u;
   if (live && m < M) {
     uint32_t w[16], hi[8], lo[8];
-    load_block(x + int64_t(m) * K + int64_t(b) * 32, w);
+    if (src >= 0) load_block(x + int64_t(src) * K + int64_t(b) * 32, w);
+    else for (int i = 0; i < 16; ++i) w[i] = 0u;
     split_block(w, c1, c2, hi, lo);
     uint4* dh = reinterpret_cast<uint4*>(ws + lay.hi + size_t(m) * K + size_t(b) * 32);
     uint4* dl = reinterpret_cast<uint4*>(ws + lay.lo + size_t(m) * K + size_t(b) * 32);
@@ -233,7 +241,7 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t
 }
 
 struct MxParams {
-  const uint8_t* wscales;   // [N, K/32] E8M0
+  const uint8_t* wscales;   // [N, K/32] E8M0 (grouped: [E N, K/32])
   const uint8_t* sf_hi;     // X scale atoms (workspace)
   const uint8_t* sf_lo;
   void* out;
@@ -242,6 +250,12 @@ struct MxParams {
   int kb_per;               // K steps per split (grid z = the splits of one cluster)
   uint64_t limit_ns;
   int drop_arrivals;
+  // grouped rows (expert-routed): nullptr otherwise.  route_off[0..E] are the
+  // 128-aligned row offsets of each expert's segment of the workspace rows,
+  // row_of[m] the activation (and output) row of workspace row m (-1: padding)
+  const int* route_off;
+  const int* row_of;
+  int E;
 };
 
 template <int F> constexpr uint32_t b_type() {
@@ -277,6 +291,17 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  // grouped rows: the tile's expert (its weights are rows [e N, e N + N) of the
+  // stacked matrix); tiles past the last segment have nothing to do (every CTA
+  // of a K-split cluster shares blockIdx.y, so a cluster leaves whole)
+  int wrow0 = 0;
+  if (p.route_off) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the routing kernel's tables
+    if (m0 >= __ldg(p.route_off + p.E)) return;
+    int e = 0;
+    while (e + 1 < p.E && __ldg(p.route_off + e + 1) <= m0) ++e;
+    wrow0 = e * p.N;
+  }
   const int nk = p.K / BK;
   const int j0 = blockIdx.z * p.kb_per, j1 = min(nk, j0 + p.kb_per);   // this split's K steps
   const int nloc = j1 - j0;
@@ -335,7 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         mbar_arrive_expect_tx(full(s), TX_BYTES);
         tma_load_2d(a_hi(s), &xhi_map, j * BK, m0, full(s));
         if constexpr (TWO) tma_load_2d(a_lo(s), &xlo_map, j * BK, m0, full(s));
-        tma_load_2d(b_tile(s), &w_map, j * BK, n0, full(s));
+        tma_load_2d(b_tile(s), &w_map, j * BK, wrow0 + n0, full(s));
         bulk_load(sf_s(s, 0), sfh + size_t(j) * SF_BYTES, SF_BYTES, full(s));
         if constexpr (TWO) bulk_load(sf_s(s, 1), sfl + size_t(j) * SF_BYTES, SF_BYTES, full(s));
         issued = i + 1;
@@ -380,7 +405,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
       #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const int r = lane + 32 * t, n = n0 + r;
-        v[t] = (i < nloc && r < BN && n < p.N) ? __ldg(ws32 + int64_t(n) * row_words + j0 + i) : 0u;
+        v[t] = (i < nloc && r < BN && n < p.N) ? __ldg(ws32 + int64_t(wrow0 + n) * row_words + j0 + i) : 0u;
       }
     };
     uint32_t cur[8], nxt[8];
@@ -418,8 +443,10 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     tc_fence_after();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int q = warp & 3;
-    const int m = m0 + q * 32 + lane;
-    const bool live = ok && *abort_flag == 0u;
+    // the output row of this lane's accumulator row (grouped: through row_of)
+    int m = m0 + q * 32 + lane;
+    if (p.route_off) m = m < __ldg(p.route_off + p.E) ? __ldg(p.row_of + m) : -1;
+    const bool live = ok && *abort_flag == 0u && m >= 0;
     #pragma unroll 1
     for (int cb = 0; cb < BN / 32; ++cb) {
       uint32_t r[32];
@@ -479,8 +506,10 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     const int e0 = int(rank) * E / int(csize), e1 = any_abort ? e0 : (int(rank) + 1) * E / int(csize);
     for (int e = e0 + int(threadIdx.x); e < e1; e += THREADS) {
       const int row = e / (BN / 4), c4 = e - row * (BN / 4);
-      const int m = m0 + row, n = n0 + 4 * c4;
-      if (m >= p.M || n >= p.N) continue;
+      int m = m0 + row;
+      const int n = n0 + 4 * c4;
+      if (p.route_off) m = m < __ldg(p.route_off + p.E) ? __ldg(p.row_of + m) : -1;
+      if (m < 0 || m >= p.M || n >= p.N) continue;
       const uint32_t sa = sbase + uint32_t((row * PSTRIDE + 4 * c4) * 4);
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       for (uint32_t r = 0; r < csize; ++r) {
@@ -672,7 +701,8 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, const void*
     lc.stream = st;
     lc.attrs = at;
     lc.numAttrs = 1;
-    e = cudaLaunchKernelEx(&lc, xquant_kernel, static_cast<const __nv_bfloat16*>(x), w8, lay, M, K);
+    e = cudaLaunchKernelEx(&lc, xquant_kernel, static_cast<const __nv_bfloat16*>(x), w8, lay, M, K,
+                           static_cast<const int*>(nullptr), static_cast<const int*>(nullptr));
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mhi, mlo, mw;
@@ -683,7 +713,7 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, const void*
                       ? make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, K, N, K / 2, uint32_t(pl.BN))
                       : make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, N, K, uint32_t(pl.BN));
   if (!ok) return cudaErrorInvalidValue;
-  MxParams prm;
+  MxParams prm{};
   prm.wscales = static_cast<const uint8_t*>(scales);
   prm.sf_hi = w8 + lay.sf_hi;
   prm.sf_lo = w8 + lay.sf_lo;
@@ -727,7 +757,7 @@ static cudaError_t launch_a8(const void* codes, const void* scales, const void* 
                       ? make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, K, N, K / 2, uint32_t(pl.BN))
                       : make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, N, K, uint32_t(pl.BN));
   if (!ok) return cudaErrorInvalidValue;
-  MxParams prm;
+  MxParams prm{};
   prm.wscales = static_cast<const uint8_t*>(scales);
   prm.sf_hi = w8 + a8_codes_bytes(M, K);
   prm.sf_lo = prm.sf_hi;
@@ -741,6 +771,155 @@ static cudaError_t launch_a8(const void* codes, const void* scales, const void* 
   prm.drop_arrivals = g_drop.load();
   if (pl.BN == 224) return launch_tile<F, 224, false>(mx8, mx8, mw, prm, M, N, pl.S, st);
   return launch_tile<F, 256, false>(mx8, mx8, mw, prm, M, N, pl.S, st);
+}
+
+// ------------------------------------------------- expert-grouped rows ---
+//
+// MoE rows routed to one expert run through the GEMM together (rlx-cpu
+// thunk/ops/quant.rs lowp_scaled_grouped_matmul; metaltile PR #250's MoE
+// gather-qmm): a routing kernel buckets the rows by expert into segments of
+// whole 128-row tiles (route_off[e] .. route_off[e + 1], padding rows -1 in
+// row_of), the activation split reads its rows through row_of, and each GEMM
+// tile takes its expert's weight rows, so every expert's weights stream
+// once per 128 rows routed to it.
+
+// One CTA: counts per expert, 128-aligned segment offsets, then each row's
+// slot (rows keep no particular order inside a segment: each output row is
+// computed on its own).  A row whose expert index lies outside [0, E) gets a
+// zero output row and status bit 2.
+__global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__ idx, int M, int E,
+                                                     int* __restrict__ off, int* __restrict__ row_of,
+                                                     void* __restrict__ out, int N, int out_f32) {
+  extern __shared__ int sh[];
+  int* cnt = sh;
+  int* cur = sh + E;
+  int* poff = sh + 2 * E;            // E + 1
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the router may be the preceding kernel
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = cur[e] = 0;
+  __syncthreads();
+  for (int r = tid; r < M; r += blockDim.x) {
+    const int e = __ldg(idx + r);
+    if (e >= 0 && e < E) {
+      atomicAdd(&cnt[e], 1);
+    } else {
+      atomicOr(&g_mx_status, 2u);
+      for (int n = 0; n < N; ++n) {
+        if (out_f32) static_cast<float*>(out)[int64_t(r) * N + n] = 0.0f;
+        else static_cast<__nv_bfloat16*>(out)[int64_t(r) * N + n] = __float2bfloat16_rn(0.0f);
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int p = 0;
+    for (int e = 0; e < E; ++e) {
+      poff[e] = p;
+      p += (cnt[e] + BM - 1) / BM * BM;
+    }
+    poff[E] = p;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) off[e] = poff[e];
+  for (int m = tid; m < poff[E]; m += blockDim.x) row_of[m] = -1;
+  __syncthreads();
+  for (int r = tid; r < M; r += blockDim.x) {
+    const int e = __ldg(idx + r);
+    if (e >= 0 && e < E) row_of[poff[e] + atomicAdd(&cur[e], 1)] = r;
+  }
+}
+
+constexpr int ROUTE_MAX_E = 1024;
+
+// Workspace rows: every segment rounded up to whole 128-row tiles.
+inline int64_t grouped_rows(int64_t M, int64_t E) { return (M + 127 * std::min<int64_t>(E, M) + BM - 1) / BM * BM; }
+
+struct GroupedLayout {
+  size_t off, row_of, total;
+  WsLayout x;     // relative to `base`
+  size_t base;
+};
+inline GroupedLayout grouped_layout(int64_t M, int64_t K, int64_t E) {
+  GroupedLayout g;
+  const int64_t R = grouped_rows(M, E);
+  g.off = 0;
+  g.row_of = align1k(size_t(E + 1) * 4);
+  g.base = g.row_of + align1k(size_t(R) * 4);
+  g.x = ws_layout(R, K);
+  g.total = g.base + g.x.total;
+  return g;
+}
+
+template <int F>
+static cudaError_t launch_grouped(const void* codes, const void* scales, const void* x, const int32_t* idx, void* out,
+                                  bool out_f32, int M, int N, int K, int E, void* ws, cudaStream_t st, int sms) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = set_smem<F, 256>(dev)) != cudaSuccess || (e = set_smem<F, 224>(dev)) != cudaSuccess) return e;
+  const GroupedLayout gl = grouped_layout(M, K, E);
+  const int R = int(grouped_rows(M, E));
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  int* off = reinterpret_cast<int*>(w8 + gl.off);
+  int* row_of = reinterpret_cast<int*>(w8 + gl.row_of);
+  uint8_t* xb = w8 + gl.base;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(1);
+    lc.blockDim = dim3(1024);
+    lc.dynamicSmemBytes = size_t(3 * E + 1) * sizeof(int);
+    lc.stream = st;
+    lc.attrs = pdl;
+    lc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&lc, route_kernel, idx, M, E, off, row_of, out, N, int(out_f32));
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const int64_t warps = int64_t(R) * ((K / 32 + 31) / 32);
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(unsigned((warps + 7) / 8));
+    lc.blockDim = dim3(256);
+    lc.stream = st;
+    lc.attrs = pdl;
+    lc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&lc, xquant_kernel, static_cast<const __nv_bfloat16*>(x), xb, gl.x, R, K,
+                           static_cast<const int*>(row_of), static_cast<const int*>(off + E));
+    if (e != cudaSuccess) return e;
+  }
+  const MxPlan pl = plan_mx<F>(dev, R, N, K, sms > 0 ? sms : 1);
+  CUtensorMap mhi, mlo, mw;
+  if (!make_map(enc, &mhi, CU_TENSOR_MAP_DATA_TYPE_UINT8, xb + gl.x.hi, K, R, K, BM) ||
+      !make_map(enc, &mlo, CU_TENSOR_MAP_DATA_TYPE_UINT8, xb + gl.x.lo, K, R, K, BM))
+    return cudaErrorInvalidValue;
+  const int64_t wrows = int64_t(E) * N;
+  const bool ok = F == MXFP4
+                      ? make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, K, wrows, K / 2, uint32_t(pl.BN))
+                      : make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, wrows, K, uint32_t(pl.BN));
+  if (!ok) return cudaErrorInvalidValue;
+  MxParams prm{};
+  prm.wscales = static_cast<const uint8_t*>(scales);
+  prm.sf_hi = xb + gl.x.sf_hi;
+  prm.sf_lo = xb + gl.x.sf_lo;
+  prm.out = out;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.out_f32 = out_f32 ? 1 : 0;
+  prm.kb_per = K / BK;
+  prm.limit_ns = g_limit_ns.load();
+  prm.drop_arrivals = g_drop.load();
+  prm.route_off = off;
+  prm.row_of = row_of;
+  prm.E = E;
+  // the grid covers R rows of tiles; the tiles past the routed segments leave at once
+  if (pl.BN == 224) return launch_tile<F, 224>(mhi, mlo, mw, prm, R, N, pl.S, st);
+  return launch_tile<F, 256>(mhi, mlo, mw, prm, R, N, pl.S, st);
 }
 
 // ------------------------------------------------ decode GEMV, M <= 16 ---
@@ -1052,6 +1231,23 @@ cudaError_t launch_qgemm_a8(int fmt, const void* codes, const void* scales, cons
     case MXFP4: return mx::launch_a8<MXFP4>(codes, scales, x, out, out_f32, m, n, k, workspace, st, sms);
     case MXFP8_E4M3: return mx::launch_a8<MXFP8_E4M3>(codes, scales, x, out, out_f32, m, n, k, workspace, st, sms);
     case MXFP8_E5M2: return mx::launch_a8<MXFP8_E5M2>(codes, scales, x, out, out_f32, m, n, k, workspace, st, sms);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+size_t qgemm_grouped_workspace_bytes(int64_t M, int64_t K, int64_t E) { return mx::grouped_layout(M, K, E).total; }
+int qgemm_grouped_max_experts() { return mx::ROUTE_MAX_E; }
+
+cudaError_t launch_qgemm_grouped(int fmt, const void* codes, const void* scales, const void* x, const int32_t* idx,
+                                 void* out, bool out_f32, int64_t M, int64_t N, int64_t K, int64_t E, void* workspace,
+                                 cudaStream_t st, int sms) {
+  const int m = int(M), n = int(N), k = int(K), e = int(E);
+  switch (fmt) {
+    case MXFP4: return mx::launch_grouped<MXFP4>(codes, scales, x, idx, out, out_f32, m, n, k, e, workspace, st, sms);
+    case MXFP8_E4M3:
+      return mx::launch_grouped<MXFP8_E4M3>(codes, scales, x, idx, out, out_f32, m, n, k, e, workspace, st, sms);
+    case MXFP8_E5M2:
+      return mx::launch_grouped<MXFP8_E5M2>(codes, scales, x, idx, out, out_f32, m, n, k, e, workspace, st, sms);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -314,6 +314,32 @@ int qmm_gather(int fmt, const void* codes, const void* scales, float global_scal
                int64_t M, int64_t N, int64_t K, int64_t E, int group, void* stream);
 
 /*
+ * qmm_grouped -- device, expert-routed rows grouped by expert (rlx-cpu
+ * thunk/ops/quant.rs lowp_scaled_grouped_matmul; metaltile PR #250's MoE
+ * gather-qmm: weight row expert_ids[m] * out_dim + n of one stacked packed
+ * tensor): the product of qmm_gather, for prefill batches.  A routing kernel
+ * buckets the rows by expert on the device (no host synchronisation), every
+ * expert's rows run through the block-scaled tensor-core GEMM together (the
+ * activation split into two MXFP8 E4M3 terms as in qmm_ex), so each expert's
+ * weights are read once per 128 rows routed to it rather than once per row.
+ * Formats mxfp4, mxfp8 E4M3 / E5M2; K a multiple of 128; 1 <= E <= 1024; out
+ * bf16 or float32 per out_dtype; workspace of at least
+ * qmm_grouped_workspace_bytes(fmt, M, K, E) bytes (128-byte aligned; scratch
+ * ordered on one stream), else QFMT_ENOSPACE; mxfp4 codes 32-byte aligned.
+ * expert_idx: device int32 [M], read after every preceding kernel in the
+ * stream has completed; an index outside [0, E) zeroes its output row and is
+ * reported by the next qfmt_device_status (QFMT_EINDEX).  Tolerance as qmm.
+ */
+int qmm_grouped(int fmt, const void* codes, const void* scales, const void* x, const int32_t* expert_idx, void* out,
+                int out_dtype, int64_t M, int64_t N, int64_t K, int64_t E, void* workspace, size_t workspace_bytes,
+                void* stream);
+/* Workspace bytes of qmm_grouped: the routing tables ((E + 1) + R int32),
+ * then qmm_ex's workspace for R rows, R = M + 127 min(E, M) rounded up to 128
+ * (every expert's rows padded to whole 128-row tiles); 0 for another format,
+ * K not a positive multiple of 128, or E outside 1..1024. */
+size_t qmm_grouped_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t E);
+
+/*
  * qmm_batched -- device: `count` (1..4) products sharing one activation:
  *   out[i][M, N[i]] (bf16) = X[M, K] (bf16) . dequant(W_i[N[i], K])^T
  * (metaltile PR #250, the batched Q/K/V and batched-4 dequantizing GEMV

@@ -194,7 +194,7 @@ class Problem:
         # one workspace serves every layer: each call's activation split waits
         # for the previous call to finish before it writes
         self.ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
-        self.path = "B" if wsb else ("A" if m > 16 else "GEMV")
+        self.path = "SUB" if fmt in q.SUB_BYTE else ("B" if wsb else ("A" if m > 16 else "GEMV"))
 
     def step(self):
         import block_scaled_quantized_spec_gb300 as q
@@ -447,6 +447,8 @@ BREAKDOWN = [
     ("mxfp8_e4m3", 2048, 4096, 4096, "A"), ("mxfp8_e5m2", 128, 11008, 4096, "A"),
     ("mxfp8_e5m2", 4096, 11008, 4096, "A"),
     ("mxfp4", 2048, 4096, 4096), ("mxfp4", 2048, 4096, 4096, "A"),
+    # the 2/3/5/6-bit bit streams
+    ("int3", 1, 11008, 4096), ("mxint5", 16, 4096, 4096),
 ]
 
 # The standalone dequant kernel: [4096, 4096] weights to float32 and bf16.
@@ -681,7 +683,7 @@ def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3, path="auto"
     prob_flops_per_byte = prob.flops / nbytes
     row = {"fmt": fmt, "M": m, "N": n, "K": k, "us": round(per * 1e3, 2), "copies": copies,
            "path": {"B": "block-scaled tcgen05 GEMM (X split + kind::mxf8f6f4)", "A": "bf16-decode tcgen05 GEMM",
-                    "GEMV": "decode GEMV"}[prob.path]}
+                    "GEMV": "decode GEMV", "SUB": "CUDA-core sub-byte kernel"}[prob.path]}
     gbs = nbytes / (per * 1e-3) / 1e9
     tfl = prob.flops / (per * 1e-3) / 1e12
     row["GB/s"] = round(gbs, 1)

@@ -29,7 +29,12 @@ __all__ = [
 FORMATS = {"mxfp4": 1, "nvfp4": 2, "mxfp8_e4m3": 3, "mxfp8_e5m2": 4, "nvfp8": 5, "int4_affine": 6,
            "nvfp8_f16": 7, "mxint8": 8, "int8": 9, "int8_f16": 10,
            "int4": 11, "int4_f16": 12, "mxfp4x2": 13, "mxint4": 14,
-           "fp4": 15, "fp4_f16": 16, "fp8_e4m3": 17, "fp8_e4m3_f16": 18, "fp8_e5m2": 19, "fp8_e5m2_f16": 20}
+           "fp4": 15, "fp4_f16": 16, "fp8_e4m3": 17, "fp8_e4m3_f16": 18, "fp8_e5m2": 19, "fp8_e5m2_f16": 20,
+           "int2": 21, "int3": 22, "int5": 23, "int6": 24, "int2_f16": 25, "int3_f16": 26, "int5_f16": 27,
+           "int6_f16": 28, "mxint2": 29, "mxint3": 30, "mxint5": 31, "mxint6": 32}
+# the 2/3/5/6-bit formats (one bit stream per row): qmm / qmm_ex and dequant only
+SUB_BYTE = ("int2", "int3", "int5", "int6", "int2_f16", "int3_f16", "int5_f16", "int6_f16",
+            "mxint2", "mxint3", "mxint5", "mxint6")
 F32, BF16 = 0, 1
 STATUS = {0: "QFMT_OK", -1: "QFMT_EINVAL", -2: "QFMT_ESHAPE", -3: "QFMT_EALIGN", -4: "QFMT_EUNSUPPORTED",
           -5: "QFMT_ECUDA", -6: "QFMT_ETIMEOUT", -7: "QFMT_ENONFINITE", -8: "QFMT_ENOSPACE", -9: "QFMT_EINDEX"}

@@ -39,6 +39,14 @@ cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, floa
                             const void* x, void* out, bool out_f32, int64_t M, int64_t N,
                             int64_t K, cudaStream_t st, int sms);
 
+// The 2/3/5/6-bit integer formats (ids 21-32): dequant and the dequantizing
+// matmul on CUDA cores (any M; bf16 or float32 activations).
+bool is_sub_byte(int fmt);
+cudaError_t launch_dequant_sub(int fmt, const void* codes, const void* scales, void* out, bool out_bf16, int64_t N,
+                               int64_t K, cudaStream_t st, int sms);
+cudaError_t launch_qmm_sub(int fmt, const void* codes, const void* scales, const void* x, bool x_f32, void* out,
+                           bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st);
+
 // Block-scaled tensor-core GEMM (tcgen05 kind::mxf8f6f4) for mxfp4 / mxfp8
 // E4M3 / E5M2 weights: X is split into two MXFP8 E4M3 terms in `workspace`
 // (qgemm_mx_workspace_bytes), then both go through the block-scaled MMA

@@ -70,6 +70,10 @@ int qfmt_dequant(int fmt, const void* codes, const void* scales, float global_sc
   int err = QFMT_OK;
   const int sms = device_sms(&err);
   if (err) return err;
+  if (qfmt_dev::is_sub_byte(fmt))
+    return cuda_status(qfmt_dev::launch_dequant_sub(fmt, codes, scales, out, out_dtype == QFMT_BF16, N, K,
+                                                    static_cast<cudaStream_t>(stream), sms),
+                       "dequant launch");
   return cuda_status(qfmt_dev::launch_dequant(fmt, codes, scales, global_scale, out, out_dtype == QFMT_BF16,
                                               N, K, static_cast<cudaStream_t>(stream), sms),
                      "dequant launch");
@@ -98,6 +102,9 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale, c
   int err = QFMT_OK;
   const int sms = device_sms(&err);
   if (err) return err;
+  if (qfmt_dev::is_sub_byte(fmt))   // the 2/3/5/6-bit codes: one CUDA-core kernel for every M and X dtype
+    return cuda_status(qfmt_dev::launch_qmm_sub(fmt, codes, scales, x, x_dtype == QFMT_F32, out, out_f32, M, N, K, s),
+                       "qmm (sub-byte codes) launch");
   if (x_dtype == QFMT_F32)
     return cuda_status(qfmt_dev::launch_qmm_f32x(fmt, codes, scales, global_scale, static_cast<const float*>(x),
                                                  out, out_f32, M, N, K, s, sms),
@@ -134,12 +141,20 @@ int qmm(int fmt, const void* codes, const void* scales, float global_scale, cons
                 stream);
 }
 
+// The fused decode forms run on the mma.sync decode GEMV, which takes the
+// byte- and nibble-aligned formats; the 2/3/5/6-bit ones take qmm.
+static int refuse_sub_byte(int fmt, const char* name) {
+  if (!qfmt_dev::is_sub_byte(fmt)) return QFMT_OK;
+  return fail(QFMT_EUNSUPPORTED, "%s: the 2/3/5/6-bit formats run through qmm / qmm_ex only", name);
+}
+
 int qmm_gather(int fmt, const void* codes, const void* scales, float global_scale, const void* x,
                const int32_t* expert_idx, void* out, int64_t M, int64_t N, int64_t K, int64_t E, int group,
                void* stream) {
   clear_error();
   int st = check_group(fmt, group);
   if (st) return st;
+  if ((st = refuse_sub_byte(fmt, "qmm_gather"))) return st;
   if ((st = check_shape(fmt, M, N, K))) return st;
   if (E < 1) return fail(QFMT_EINVAL, "expert count E=%lld must be >= 1", (long long)E);
   if (E * weight_rows(fmt, N) >= (int64_t(1) << 31)) return fail(QFMT_ESHAPE, "E*N code rows of 2^31 or more");
@@ -164,6 +179,7 @@ int qmm_batched(int fmt, int count, const void* const* codes, const void* const*
   clear_error();
   int st = check_group(fmt, group);
   if (st) return st;
+  if ((st = refuse_sub_byte(fmt, "qmm_batched"))) return st;
   if (count < 1 || count > 4) return fail(QFMT_EINVAL, "count=%d must be 1..4", count);
   if (!codes || !scales || !global_scales || !N || !out) return fail(QFMT_EINVAL, "NULL pointer array");
   for (int i = 0; i < count; ++i) {
@@ -215,6 +231,7 @@ static int rmsnorm_form(int fmt, const void* codes, const void* scales, float gl
   clear_error();
   int st = check_group(fmt, group);
   if (st) return st;
+  if ((st = refuse_sub_byte(fmt, name))) return st;
   if ((st = check_shape(fmt, M, N, K))) return st;
   if (M > 2) return fail(QFMT_EUNSUPPORTED, "%s is the decode form: M=%lld above 2", name, (long long)M);
   if (!(std::isfinite(eps) && eps >= 0.0f)) return fail(QFMT_EINVAL, "eps must be finite and >= 0");

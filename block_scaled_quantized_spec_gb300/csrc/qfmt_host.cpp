@@ -36,7 +36,21 @@ int fail(int status, const char* fmt, ...) {
 
 void clear_error() { g_err[0] = '\0'; }
 
-bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_FP8_E5M2_F16; }
+bool valid_format(int fmt) { return fmt >= QFMT_MXFP4 && fmt <= QFMT_MXINT6; }
+
+// Bits per code of the sub-byte integer formats (2, 3, 5, 6); 0 for the rest.
+int sub_bits(int fmt) {
+  switch (fmt) {
+    case QFMT_INT2: case QFMT_INT2_F16: case QFMT_MXINT2: return 2;
+    case QFMT_INT3: case QFMT_INT3_F16: case QFMT_MXINT3: return 3;
+    case QFMT_INT5: case QFMT_INT5_F16: case QFMT_MXINT5: return 5;
+    case QFMT_INT6: case QFMT_INT6_F16: case QFMT_MXINT6: return 6;
+    default: return 0;
+  }
+}
+
+static bool is_mxint_sub(int fmt) { return fmt >= QFMT_MXINT2 && fmt <= QFMT_MXINT6; }
+static bool is_f16_sub(int fmt) { return fmt >= QFMT_INT2_F16 && fmt <= QFMT_INT6_F16; }
 
 int block_of(int fmt) {
   switch (fmt) {
@@ -45,7 +59,9 @@ int block_of(int fmt) {
     case QFMT_FP8_E5M2_F16: return 32;
     case QFMT_NVFP4: case QFMT_NVFP8: case QFMT_NVFP8_F16: return 16;
     case QFMT_INT4_AFFINE: case QFMT_INT8: case QFMT_INT8_F16: case QFMT_INT4: case QFMT_INT4_F16: return 64;
-    default: return 0;
+    default:
+      if (sub_bits(fmt)) return is_mxint_sub(fmt) ? 32 : 64;
+      return 0;
   }
 }
 
@@ -56,8 +72,11 @@ bool is_4bit(int fmt) {
 
 bool is_sym_int(int fmt) {
   return fmt == QFMT_MXINT8 || fmt == QFMT_INT8 || fmt == QFMT_INT8_F16 || fmt == QFMT_INT4 || fmt == QFMT_INT4_F16 ||
-         fmt == QFMT_MXINT4;
+         fmt == QFMT_MXINT4 || sub_bits(fmt) != 0;
 }
+
+// Bits per code: 4, 8, or a sub-byte width (mxfp4x2: its two planes, 8 a weight).
+int code_bits(int fmt) { return sub_bits(fmt) ? sub_bits(fmt) : (is_4bit(fmt) ? 4 : 8); }
 
 // Largest finite element magnitude: amax / elem_max is the raw block scale.
 float elem_max(int fmt) {
@@ -66,15 +85,18 @@ float elem_max(int fmt) {
     case QFMT_MXFP8_E5M2: case QFMT_FP8_E5M2: case QFMT_FP8_E5M2_F16: return 57344.0f;
     case QFMT_MXINT8: case QFMT_INT8: case QFMT_INT8_F16: return 127.0f;
     case QFMT_INT4: case QFMT_INT4_F16: case QFMT_MXINT4: return 7.0f;
-    default: return 448.0f;   // E4M3
+    default:
+      if (sub_bits(fmt)) return float((1 << (sub_bits(fmt) - 1)) - 1);
+      return 448.0f;   // E4M3
   }
 }
 
 int scale_entry_bytes(int fmt) {
   if (fmt == QFMT_MXFP4X2) return 8;   // s0 and s1, float32 each (stored as two [nb] runs per row)
   if (fmt == QFMT_NVFP8 || fmt == QFMT_INT4_AFFINE || fmt == QFMT_INT8 || fmt == QFMT_INT4 || fmt == QFMT_FP4 ||
-      fmt == QFMT_FP8_E4M3 || fmt == QFMT_FP8_E5M2)
+      fmt == QFMT_FP8_E4M3 || fmt == QFMT_FP8_E5M2 || (fmt >= QFMT_INT2 && fmt <= QFMT_INT6))
     return 4;
+  if (is_f16_sub(fmt)) return 2;
   return (fmt == QFMT_NVFP8_F16 || fmt == QFMT_INT8_F16 || fmt == QFMT_INT4_F16 || fmt == QFMT_FP4_F16 ||
           fmt == QFMT_FP8_E4M3_F16 || fmt == QFMT_FP8_E5M2_F16)
              ? 2
@@ -209,6 +231,16 @@ static inline void put_code(uint8_t* row, int64_t k, uint32_t code, bool four_bi
   else row[k >> 1] = uint8_t(code & 0xF);
 }
 
+// Code k of a row's LSB-first bit stream of `bits`-bit codes (the row's bytes
+// zeroed beforehand): bits [k bits, k bits + bits) of the little-endian bit
+// sequence, which may straddle two bytes.
+static inline void put_bits(uint8_t* row, int64_t k, uint32_t code, int bits) {
+  const int64_t p = k * bits;
+  const uint32_t v = (code & ((1u << bits) - 1u)) << (p & 7);
+  row[p >> 3] |= uint8_t(v);
+  if ((p & 7) + bits > 8) row[(p >> 3) + 1] |= uint8_t(v >> 8);
+}
+
 }  // namespace qfmt
 
 using namespace qfmt;
@@ -228,7 +260,7 @@ int qfmt_block_size(int fmt, int group) {
 size_t qfmt_codes_bytes(int fmt, int64_t N, int64_t K, int group) {
   clear_error();
   if (check_group(fmt, group) != QFMT_OK || check_shape(fmt, 0, N, K) != QFMT_OK) return SIZE_MAX;
-  return size_t(is_4bit(fmt) ? N * K / 2 : N * K);
+  return size_t(N * K * code_bits(fmt) / 8);
 }
 
 size_t qfmt_scales_bytes(int fmt, int64_t N, int64_t K, int group) {
@@ -252,8 +284,10 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
   const int blk = block_of(fmt);
   const int64_t nb = (K + blk - 1) / blk;   // int4 affine: a ragged last group of K - 64 (nb - 1) values
   const bool four = is_4bit(fmt);
-  const int64_t row_bytes = four ? K / 2 : K;
+  const int sbits = sub_bits(fmt);
+  const int64_t row_bytes = K * code_bits(fmt) / 8;
   uint8_t* cb = static_cast<uint8_t*>(codes);
+  if (sbits) std::memset(cb, 0, size_t(N * row_bytes));   // put_bits ORs into zeroed rows
   uint8_t* sb = static_cast<uint8_t*>(scales);
 
   // Reject NaN/Inf weights up front (the block statistics assume finite input).
@@ -334,7 +368,8 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
         for (int j = 0; j < len; ++j) amax = std::max(amax, std::fabs(wb[j]));
         float eff;
         switch (fmt) {
-          case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: case QFMT_MXINT4: {
+          case QFMT_MXFP4: case QFMT_MXFP8_E4M3: case QFMT_MXFP8_E5M2: case QFMT_MXINT8: case QFMT_MXINT4:
+          case QFMT_MXINT2: case QFMT_MXINT3: case QFMT_MXINT5: case QFMT_MXINT6: {
             const float s = amax > 0.0f ? amax / elem_max(fmt) : 1.0f;
             const uint32_t code = enc_e8m0_ceil(s);
             sb[n * nb + b] = uint8_t(code);
@@ -348,7 +383,8 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
             break;
           }
           case QFMT_NVFP8_F16: case QFMT_INT8_F16: case QFMT_INT4_F16: case QFMT_FP4_F16: case QFMT_FP8_E4M3_F16:
-          case QFMT_FP8_E5M2_F16: {  // an IEEE half, rounded to nearest even
+          case QFMT_FP8_E5M2_F16: case QFMT_INT2_F16: case QFMT_INT3_F16: case QFMT_INT5_F16:
+          case QFMT_INT6_F16: {  // an IEEE half, rounded to nearest even
             const float s = amax > 0.0f ? amax / elem_max(fmt) : 1.0f;
             const _Float16 h = static_cast<_Float16>(s);
             std::memcpy(sb + (n * nb + b) * 2, &h, 2);
@@ -369,15 +405,19 @@ int qfmt_pack(int fmt, const float* W, int64_t N, int64_t K, int group, void* co
             const float v = wb[j] / eff;
             if (is_sym_int(fmt)) {  // symmetric: round half away from zero, clamp to +-max, two's complement
               const float qm = elem_max(fmt);
-              code = uint32_t(uint8_t(int8_t(std::max(-qm, std::min(qm, std::round(v)))))) & (four ? 0xFu : 0xFFu);
-              put_code(crow, b * blk + j, code, four);
+              code = uint32_t(uint8_t(int8_t(std::max(-qm, std::min(qm, std::round(v)))))) &
+                     ((1u << code_bits(fmt)) - 1u);
+              if (sbits) put_bits(crow, b * blk + j, code, sbits);
+              else put_code(crow, b * blk + j, code, four);
               continue;
             }
             const bool e5 = fmt == QFMT_MXFP8_E5M2 || fmt == QFMT_FP8_E5M2 || fmt == QFMT_FP8_E5M2_F16;
             const bool e2 = fmt == QFMT_MXFP4 || fmt == QFMT_NVFP4 || fmt == QFMT_FP4 || fmt == QFMT_FP4_F16;
             code = e5 ? enc_e5m2(v) : e2 ? enc_e2m1(v) : enc_e4m3(v);
           }
-          put_code(crow, b * blk + j, code, four);
+          // (eff == 0: a half scale that underflowed; the code is 0)
+          if (sbits) put_bits(crow, b * blk + j, code, sbits);
+          else put_code(crow, b * blk + j, code, four);
         }
       }
     }

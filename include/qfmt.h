@@ -42,6 +42,10 @@
  *   QFMT_FP8_E5M2       E5M2 (8-bit)       32     FP32 (4 bytes): legacy, s = amax/57344
  *   QFMT_FP4_F16, QFMT_FP8_E4M3_F16, QFMT_FP8_E5M2_F16: their fp16-scale twins
  *                                                 (the scale an IEEE half, 2 bytes)
+ *   QFMT_INT2/3/5/6     signed N-bit q     64     FP32 (4 bytes): w = q * scale (PR #250's symmetric
+ *                                                 intN, sign-extended from bit N-1, +-(2^(N-1)-1))
+ *   QFMT_INT2/3/5/6_F16                     64     IEEE half (2 bytes): their fp16-scale twins
+ *   QFMT_MXINT2/3/5/6   signed N-bit q     32     E8M0 byte: w = q * 2^(b-127) (PR #250's MXINT axis)
  *   QFMT_MXFP4X2        two E2M1 planes    32     two FP32 (8 bytes): the two-level residual
  *                                                 weight w = s0 e2m1(q0) + s1 e2m1(q1) (rlx-cpu
  *                                                 dequant_matmul_mxfp4x2); level 0 packs w with
@@ -51,7 +55,11 @@
  * Memory layouts (all row-major, no padding, little-endian):
  *   codes   [N, K/2] bytes for 4-bit formats (mxfp4, nvfp4, int4 affine, int4, mxint4, fp4): element k of a row sits in byte
  *           k/2, low nibble for even k (LSB-first; 8 codes per u32 word);
- *           [N, K] bytes for 8-bit formats.
+ *           [N, K] bytes for 8-bit formats;
+ *           [N, K N_bits / 8] bytes for the 2/3/5/6-bit formats: one LSB-first
+ *           bit stream per row, code k at bits [k N, k N + N) of the row's
+ *           little-endian bit sequence (PR #250's sub-byte packing; K a
+ *           multiple of 32 makes every row whole 32-bit words).
  *   scales  [N, ceil(K/block)] entries of the sizes above; int4 affine stores
  *           the (scale, bias) bf16 pair of each group adjacently:
  *           [N, ceil(K/64), 2].  K is a multiple of 32 for every format, so
@@ -117,7 +125,19 @@ typedef enum {
   QFMT_FP8_E4M3 = 17,
   QFMT_FP8_E4M3_F16 = 18,
   QFMT_FP8_E5M2 = 19,
-  QFMT_FP8_E5M2_F16 = 20
+  QFMT_FP8_E5M2_F16 = 20,
+  QFMT_INT2 = 21,
+  QFMT_INT3 = 22,
+  QFMT_INT5 = 23,
+  QFMT_INT6 = 24,
+  QFMT_INT2_F16 = 25,
+  QFMT_INT3_F16 = 26,
+  QFMT_INT5_F16 = 27,
+  QFMT_INT6_F16 = 28,
+  QFMT_MXINT2 = 29,
+  QFMT_MXINT3 = 30,
+  QFMT_MXINT5 = 31,
+  QFMT_MXINT6 = 32
 } qfmt_format;
 
 typedef enum { QFMT_F32 = 0, QFMT_BF16 = 1 } qfmt_dtype;

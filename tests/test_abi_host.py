@@ -166,7 +166,7 @@ def _call_qmm(lib, **kw):
 def test_device_entry_validation_without_gpu(lib):
     # each of these fails in host-side validation, before any CUDA call
     assert _call_qmm(lib, fmt=0) == -1
-    assert _call_qmm(lib, fmt=21) == -1
+    assert _call_qmm(lib, fmt=33) == -1
     assert _call_qmm(lib, K=48) == -2
     assert _call_qmm(lib, M=-1) == -2
     assert _call_qmm(lib, group=64) == -4

@@ -22,7 +22,7 @@ from oracle import reference as oref  # noqa: E402
 from tolerance import check_tensor  # noqa: E402
 
 pytestmark = pytest.mark.gpu
-FMTS = list(q.FORMATS)
+FMTS = [f for f in q.FORMATS if f not in q.SUB_BYTE]   # the 2/3/5/6-bit formats take qmm only
 DEV = "cuda:0"
 
 
@@ -167,3 +167,17 @@ def test_gated_rmsnorm_with_a_zero_gate_is_zero_and_a_large_gate_scales_rmsnorm(
     ref, bound = oref.qmm_rmsnorm_ref(fmt, c, s, g, xb, "bf16", gb, eps, m, n, k)
     _check(a / 64.0, ref, bound, "gate 64")
     _check(b, ref, bound, "plain")
+
+
+@pytest.mark.parametrize("fmt", ["int3", "mxint5", "int6_f16"])
+def test_sub_byte_formats_are_refused_by_the_fused_forms(fmt):
+    m, n, k = 1, 64, 256
+    c, s, g = opack.pack(fmt, synth.weights(n, k, seed=1))
+    xb, xt = _x(m, k, seed=2)
+    gamma = torch.ones(k, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(q.QfmtError) as e:
+        q.qmm_rmsnorm(fmt, _dev(c), _dev(s), g, xt, gamma, 1e-5, n)
+    assert e.value.status == -4
+    with pytest.raises(q.QfmtError) as e:
+        q.qmm_batched(fmt, [_dev(c)], [_dev(s)], [g], xt, [n])
+    assert e.value.status == -4

@@ -20,7 +20,8 @@ from tolerance import bf16_half_ulp, check, check_tensor  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 FMTS = list(q.FORMATS)
-GROUP64 = ["int4_affine", "int8", "int8_f16", "int4", "int4_f16"]          # group of 64: K may end in a group of 32
+GROUP64 = ["int4_affine", "int8", "int8_f16", "int4", "int4_f16",         # group of 64: K may end in a group of 32
+           "int2", "int3", "int5", "int6", "int2_f16", "int3_f16", "int5_f16", "int6_f16"]
 DEV = "cuda:0"
 
 
@@ -74,12 +75,12 @@ def test_dequant_all_codes_and_scales(fmt):
     cb = opack.codes_nbytes(fmt, n, k)
     codes = np.tile(np.arange(256, dtype=np.uint8), cb // 256 + 1)[:cb].reshape(n, -1)
     sb = opack.scales_nbytes(fmt, n, k)
-    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4", "nvfp4"):
+    if fmt in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "mxint8", "mxint4", "nvfp4") or fmt.startswith("mxint"):
         scales = np.tile(np.arange(256, dtype=np.uint8), sb // 256 + 1)[:sb]
-    elif fmt in ("nvfp8", "int8", "int4", "mxfp4x2", "fp4", "fp8_e4m3", "fp8_e5m2"):
+    elif fmt in ("nvfp8", "int8", "int4", "mxfp4x2", "fp4", "fp8_e4m3", "fp8_e5m2", "int2", "int3", "int5", "int6"):
         scales = np.concatenate([rng.standard_normal(sb // 4 - 4).astype(np.float32),
                                  np.array([1e-40, 3e38, 0.0, -2.5], np.float32)]).view(np.uint8)
-    elif fmt in ("nvfp8_f16", "int8_f16", "int4_f16", "fp4_f16", "fp8_e4m3_f16", "fp8_e5m2_f16"):   # evenly spaced half bit patterns: subnormals, +-inf, NaNs, both signs
+    elif fmt.endswith("_f16"):   # evenly spaced half bit patterns: subnormals, +-inf, NaNs, both signs
         scales = np.arange(0, 65536, 65536 // (sb // 2), dtype=np.uint16)[:sb // 2].view(np.uint8)
     else:
         sc = synth.f32_to_bf16_bits(rng.standard_normal(sb // 2).astype(np.float32) * 1e-2)
@@ -247,6 +248,10 @@ FULL = [
     ("fp4", 1, 4096, 4096, False),
     ("fp8_e5m2_f16", 16, 11008, 4096, False),
     ("fp8_e4m3", 2048, 4096, 4096, False),
+    ("int3", 1, 11008, 4096, False),          # the sub-byte bit streams on their CUDA-core kernel
+    ("mxint5", 16, 4096, 4096, False),
+    ("int6_f16", 128, 4096, 4096, False),
+    ("int2", 1, 4096, 4096, False),
 ]
 
 

@@ -99,20 +99,28 @@ inline constexpr bool fmt_is_four(int f) {
   return f == MXFP4 || f == NVFP4 || f == MXFP4X2 || f == MXINT4 || f == FP4 || f == FP4_F16 || fmt_is_i4(f);
 }
 
+// A read-only value from global memory (G) or any state space (a copy in
+// shared memory).
+template <bool G, typename T>
+__device__ __forceinline__ T ld_ro(const T* p) {
+  if constexpr (G) return __ldg(p);
+  else return *p;
+}
+
 // Block scale idx of a float-scaled array as float32: the stored float32, or
 // the (exact) float32 of the stored IEEE half.
-template <int F>
+template <int F, bool G = true>
 __device__ __forceinline__ float float_scale(const uint8_t* scales, int64_t idx) {
-  if constexpr (FmtTraits<F>::sbytes == 4) return __ldg(reinterpret_cast<const float*>(scales) + idx);
-  else return __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(scales) + idx)));
+  if constexpr (FmtTraits<F>::sbytes == 4) return ld_ro<G>(reinterpret_cast<const float*>(scales) + idx);
+  else return __half2float(__ushort_as_half(ld_ro<G>(reinterpret_cast<const unsigned short*>(scales) + idx)));
 }
 
 // Raw scale word of group idx of a 4-bit integer format: int4 affine's
 // (scale, bias) bf16 pair, the float32 bits, or the half bits (zero-extended).
-template <int F>
+template <int F, bool G = true>
 __device__ __forceinline__ uint32_t i4_word(const uint8_t* scales, int64_t idx) {
-  if constexpr (FmtTraits<F>::sbytes == 2) return __ldg(reinterpret_cast<const unsigned short*>(scales) + idx);
-  else return __ldg(reinterpret_cast<const uint32_t*>(scales) + idx);
+  if constexpr (FmtTraits<F>::sbytes == 2) return ld_ro<G>(reinterpret_cast<const unsigned short*>(scales) + idx);
+  else return ld_ro<G>(reinterpret_cast<const uint32_t*>(scales) + idx);
 }
 
 // (scale, bias) of a group from its raw word, for the unsigned u of i4_u:

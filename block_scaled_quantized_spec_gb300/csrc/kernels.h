@@ -82,13 +82,14 @@ cudaError_t launch_qgemv_mx(int fmt, const void* codes, const void* scales, cons
                             int64_t M, int64_t N, int64_t K, cudaStream_t st);
 void set_mx_wait_limit_ns(uint64_t ns);
 void set_mx_drop_arrivals(int on);
-void set_mx_plan(int bn, int s);
-void set_mx_gemv(int off, int s);  // measurement hook: 1 = the mma.sync GEMVs for the MX formats; forced K split   // measurement hook: force the tile width (224/256) and K split (1-4); 0 = planner
+void set_mx_plan(int bn, int s);   // measurement hook: force the tile width (224/256) and K split (1-4); 0 = planner
+void set_mx_gemv(int off, int s);  // measurement hook: 1 = the mma.sync GEMVs for the MX formats; forced K split
 cudaError_t read_and_clear_mx_status(unsigned int* status);
 
 // Bounded-wait test hooks and the device status word of the tensor-core GEMM.
 void set_wait_limit_ns(uint64_t ns);
 void set_drop_arrivals(int on);
+int drop_arrivals();
 cudaError_t read_and_clear_device_status(unsigned int* status);
 cudaError_t read_and_clear_gemv_status(unsigned int* status);
 

@@ -283,7 +283,8 @@ int qfmt_device_status(void* stream) {
   if (word) return fail(QFMT_ETIMEOUT, "a tensor-core GEMM pipeline wait expired (status 0x%x)", word);
   if (mw & 1u) return fail(QFMT_ETIMEOUT, "a block-scaled GEMM pipeline wait expired (status 0x%x)", mw);
   if (gw) return fail(QFMT_ETIMEOUT, "a GEMV weight-copy wait expired (status 0x%x)", gw);
-  if (gx || (mw & 2u))
+  if (gx & 2u) return fail(QFMT_ETIMEOUT, "a decode GEMV weight-copy wait expired (status 0x%x)", gx);
+  if ((gx & 1u) || (mw & 2u))
     return fail(QFMT_EINDEX, "qmm_gather / qmm_grouped: an expert index outside [0, E) (its output row was zeroed)");
   return QFMT_OK;
 }

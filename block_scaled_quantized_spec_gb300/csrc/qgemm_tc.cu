@@ -593,6 +593,7 @@ cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, floa
 void set_wait_limit_ns(uint64_t ns) { tc::g_limit_ns.store(ns); }
 uint64_t wait_limit_ns() { return tc::g_limit_ns.load(); }
 void set_drop_arrivals(int on) { tc::g_drop.store(on); }
+int drop_arrivals() { return tc::g_drop.load(); }
 
 cudaError_t read_and_clear_device_status(unsigned int* status) {
   cudaError_t e = cudaMemcpyFromSymbol(status, g_device_status, sizeof(unsigned int));

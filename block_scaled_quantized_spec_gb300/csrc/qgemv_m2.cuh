@@ -41,6 +41,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "decode.cuh"
@@ -161,6 +162,41 @@ inline size_t smem_bytes(int F, int M, int K, int warps = WARPS) {
          size_t(warps) * 2 * 16 * 4 + size_t(warps) * 2 * 4;
 }
 
+// STAGE: row strides of the weight and scale copies in shared memory (a
+// 64-byte offset between rows puts rows g and g + 1 in different halves of
+// the banks; 16 bytes between scale rows spread rows 0-7 over the banks).
+__host__ __device__ constexpr int64_t stage_wstride(int64_t rowbytes) { return rowbytes + 64; }
+__host__ __device__ constexpr int64_t stage_sstride(int64_t srowbytes) { return (srowbytes + 15) / 16 * 16 + 16; }
+constexpr int STAGE_WARPS = 16;                                              // two groups of 8, one per tile
+inline size_t stage_offset(int F, int M, int K) { return (smem_bytes(F, M, K, STAGE_WARPS) + 127) / 128 * 128; }
+constexpr int STAGE_ROWS = 32;                                              // two 16-row tiles
+constexpr size_t STAGE_SMEM_LIMIT = 112 * 1024;                             // two CTAs an SM
+inline size_t stage_smem_bytes(int F, int M, int K, int64_t rowbytes, int64_t srowbytes) {
+  return stage_offset(F, M, K) + STAGE_ROWS * size_t(stage_wstride(rowbytes)) +
+         STAGE_ROWS * size_t(stage_sstride(srowbytes)) + 16;
+}
+
+// Bounded wait for the phase of the given parity of a shared-memory mbarrier.
+__device__ __forceinline__ bool mbar_wait_parity(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  auto done = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+  };
+  if (done()) return true;
+  uint64_t t0, t1;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (!done()) {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+    if (t1 - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
 // Per-chunk scale words a D-holding lane keeps: the weight block scales of
 // the two columns it holds, for rows g and g + 8 (raw encodings).
 struct ChunkScales {
@@ -185,7 +221,19 @@ static __device__ unsigned int g_gather_status;
 //  * RMS: the activations are RMS-normalised on the way in: x * gamma is
 //    staged, sum(x^2) is gathered over the CTA (whose warps cover all of K),
 //    and 1 / sqrt(mean(x^2) + eps) multiplies each output.
-constexpr int GATHER = 1, BATCH = 2, RMS = 4, GATE = 8;
+//  * STAGE: one 16-warp CTA per SM takes two 16-row tiles (tile b and
+//    b + grid), one per group of 8 warps; the 32 weight rows and their scale
+//    rows are bulk-copied into shared memory as the kernel starts (L2
+//    evict-first: read once) and the lanes read their spans from there.  Two
+//    such CTAs fit on an SM, so every CTA of the next launch of a decode
+//    chain starts, and requests its weights, while this launch still runs --
+//    exactly one beside each of this launch's, which keeps the launch's work
+//    even over the SMs (with two 16-row CTAs an SM most of the next launch
+//    starts only as this launch's CTAs leave; with smaller CTAs the scheduler
+//    stacks up to four of one launch on an SM).  Group 0 stages the
+//    activations for both.  A copy that does not land within the wait limit
+//    sets bit 1 of the status word and the CTA stores nothing.
+constexpr int GATHER = 1, BATCH = 2, RMS = 4, GATE = 8, STAGE = 16;
 struct Extra {
   const int32_t* eidx;          // GATHER
   int E;
@@ -199,16 +247,21 @@ struct Extra {
   const uint16_t* gamma;        // RMS: bf16 [K]
   const uint16_t* gate;         // GATE: bf16 [M, K]
   float eps;
+  uint64_t limit_ns;            // STAGE: the copies' wait limit
+  int drop;                     // STAGE fault hook: the copies are not issued, so the wait expires
 };
 
 template <int F, int MR, bool UNI, int W, int MODE = 0>
-__global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const uint8_t* __restrict__ codes,
+__global__ void __launch_bounds__(32 * W, W == 4 ? 3 : 2) qgemv_m2_kernel(const uint8_t* __restrict__ codes,
                                                            const uint8_t* __restrict__ scales, float glob,
                                                            const uint16_t* __restrict__ x, void* __restrict__ out,
                                                            int out_f32, int M, int N, int K, const Extra ex) {
   using S = Shape<F>;
-  constexpr int P = chunks_per_warp<F, W>();
-  constexpr int WARPS = W, THREADS = 32 * W;
+  constexpr bool STG = (MODE & STAGE) != 0;
+  constexpr int P = STG ? 2 : chunks_per_warp<F, W>();
+  constexpr int WARPS = W;
+  constexpr int GROUPS = STG ? 2 : 1;                                       // STAGE: a warp group per tile
+  constexpr int WK = W / GROUPS;                                            // warps sharing a tile's K range
   constexpr bool FOUR = S::four, I4 = is_i4<F>() || F == MXINT4;   // int4 pairing, span sums of x
   constexpr bool X2 = F == MXFP4X2;                                         // output row = rows 2r + 2r + 1
   constexpr int CODES = S::CODES, LANE = S::LANE;
@@ -225,8 +278,48 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kw = warp % WK, jt = warp / WK;                                 // K-range warp, tile group
   const int g = lane >> 2, t = lane & 3;
   int row0 = blockIdx.x * 16;
+  // STAGE: the weight and scale rows of this CTA in shared memory
+  const int64_t stage_rowb = FmtTraits<F>::four ? K / 2 : K;
+  const int64_t stage_srowb = int64_t((K + FmtTraits<F>::block - 1) / FmtTraits<F>::block) * FmtTraits<F>::sbytes;
+  uint8_t* wsm = smem + ((reinterpret_cast<uintptr_t>(rss + WARPS * 2) - reinterpret_cast<uintptr_t>(smem) + 127) & ~uintptr_t(127));
+  uint8_t* ssm = wsm + STAGE_ROWS * stage_wstride(stage_rowb);
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(ssm + STAGE_ROWS * stage_sstride(stage_srowb));
+  const int tile1 = int(blockIdx.x) + int(gridDim.x);                       // STAGE: the second tile
+  const int stage_tiles = STG && tile1 < (N + 15) / 16 ? 2 : 1;
+  if constexpr (STG) {
+    if (warp == 0) {
+      const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(wbar));
+      const int nr0 = min(16, N - row0), nr1 = stage_tiles > 1 ? min(16, N - 16 * tile1) : 0;
+      if (lane == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"(uint32_t(nr0 + nr1) * uint32_t(stage_rowb + stage_srowb))
+                     : "memory");
+      }
+      __syncwarp();
+      uint64_t pol;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+      const int r = lane & 15;
+      const bool sc = lane >= 16;
+      #pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int base = j == 0 ? row0 : 16 * tile1;
+        if (r < (j == 0 ? nr0 : nr1) && !ex.drop) {
+          const uint8_t* src = sc ? scales + int64_t(base + r) * stage_srowb : codes + int64_t(base + r) * stage_rowb;
+          uint8_t* dst = sc ? ssm + (16 * j + r) * stage_sstride(stage_srowb) : wsm + (16 * j + r) * stage_wstride(stage_rowb);
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+              ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))), "l"(src),
+              "r"(uint32_t(sc ? stage_srowb : stage_rowb)), "r"(bar), "l"(pol)
+              : "memory");
+        }
+      }
+    }
+  }
   if constexpr ((MODE & BATCH) != 0) {    // this CTA's matrix: unrolled selects, no indexed parameters
     int i = 0;
     #pragma unroll
@@ -262,13 +355,14 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
     codes += int64_t(e) * N * (FmtTraits<F>::four ? K / 2 : K);
     scales += int64_t(e) * N * ((K + FmtTraits<F>::block - 1) / FmtTraits<F>::block) * FmtTraits<F>::sbytes;
   }
-  const int ra = row0 + g, rb = row0 + g + 8;
-  const bool va = ra < N, vb = rb < N;
+  int ra = row0 + g, rb = row0 + g + 8;
+  bool va = ra < N, vb = rb < N;
   const int64_t rowbytes = FOUR ? K / 2 : K;
-  const uint8_t* pa = codes + int64_t(va ? ra : 0) * rowbytes + 16 * t;
-  const uint8_t* pb = codes + int64_t(vb ? rb : 0) * rowbytes + 16 * t;
+  const uint8_t* pa = STG ? wsm + g * stage_wstride(rowbytes) + 16 * t : codes + int64_t(va ? ra : 0) * rowbytes + 16 * t;
+  const uint8_t* pb =
+      STG ? wsm + (g + 8) * stage_wstride(rowbytes) + 16 * t : codes + int64_t(vb ? rb : 0) * rowbytes + 16 * t;
   const int nchunk = (K + CODES - 1) / CODES;
-  const int mine = nchunk > warp ? (nchunk - warp + WARPS - 1) / WARPS : 0;   // chunks of this warp
+  const int mine = nchunk > kw ? (nchunk - kw + WK - 1) / WK : 0;            // chunks of this warp
   const int a0 = (2 * t) & 3;                                                 // first column's quad lane
   const int64_t nblk = (K + FmtTraits<F>::block - 1) / FmtTraits<F>::block;   // int4 affine: a ragged last group
 
@@ -282,62 +376,68 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   // paired E8M0 bytes come in one 16-bit load.
   constexpr bool uni = UNI;
   constexpr int SB = FmtTraits<F>::sbytes;
-  const uint8_t* sra = scales + int64_t(va ? ra : 0) * nblk * SB;           // row g's scales
-  const uint8_t* srb = scales + int64_t(vb ? rb : 0) * nblk * SB;           // row g + 8's scales
+  const uint8_t* sra = STG ? ssm + g * stage_sstride(nblk * SB) : scales + int64_t(va ? ra : 0) * nblk * SB;   // row g's
+  const uint8_t* srb = STG ? ssm + (g + 8) * stage_sstride(nblk * SB) : scales + int64_t(vb ? rb : 0) * nblk * SB;
+  constexpr bool GL = !STG;                                                 // scale reads: global (else shared)
 
   // chunk slot i of round r: codes of rows g and g + 8 and their scales
   auto load_chunk = [&](int r, int i) {
-    const int c = warp + WARPS * (r * P + i);
+    const int c = kw + WK * (r * P + i);
     const int ks = c * CODES + LANE * t;                                     // this lane's first k
     const int k0 = c * CODES + LANE * a0;                                    // quad lane a0's first k
     const bool live = uni || r * P + i < mine;
     const bool kin = uni || (live && ks < K);
     const bool c0 = uni || (live && k0 < K), c1 = uni || (live && k0 + LANE < K);
-    wa[i] = kin ? ldg_stream(pa + int64_t(c) * 64) : make_uint4(0, 0, 0, 0);
-    wb[i] = kin ? ldg_stream(pb + int64_t(c) * 64) : make_uint4(0, 0, 0, 0);
+    if constexpr (STG) {
+      wa[i] = kin ? *reinterpret_cast<const uint4*>(pa + c * 64) : make_uint4(0, 0, 0, 0);
+      wb[i] = kin ? *reinterpret_cast<const uint4*>(pb + c * 64) : make_uint4(0, 0, 0, 0);
+    } else {
+      wa[i] = kin ? ldg_stream(pa + int64_t(c) * 64) : make_uint4(0, 0, 0, 0);
+      wb[i] = kin ? ldg_stream(pb + int64_t(c) * 64) : make_uint4(0, 0, 0, 0);
+    }
     // the block (or pair of blocks) of quad lanes a0 and a0 + 1 in this chunk;
     // a block outside the matrix reads as E8M0 127 / zero (its D column is zero)
     if constexpr (is_mx4<F>()) {
       const int e = k0 / 32;                                                  // even
       if (uni) {
-        const uint32_t pa2 = __ldg(reinterpret_cast<const uint16_t*>(sra) + e / 2);
-        const uint32_t pb2 = __ldg(reinterpret_cast<const uint16_t*>(srb) + e / 2);
+        const uint32_t pa2 = ld_ro<GL>(reinterpret_cast<const uint16_t*>(sra) + e / 2);
+        const uint32_t pb2 = ld_ro<GL>(reinterpret_cast<const uint16_t*>(srb) + e / 2);
         cs[i].a0 = prmt(pa2, pb2, 0x5410u);                                   // four E8M0 bytes
       } else {
-        const uint32_t x0 = c0 ? __ldg(sra + e) : 127u;
-        const uint32_t x1 = c1 ? __ldg(sra + e + 1) : 127u;
-        const uint32_t x2 = c0 ? __ldg(srb + e) : 127u;
-        const uint32_t x3 = c1 ? __ldg(srb + e + 1) : 127u;
+        const uint32_t x0 = c0 ? ld_ro<GL>(sra + e) : 127u;
+        const uint32_t x1 = c1 ? ld_ro<GL>(sra + e + 1) : 127u;
+        const uint32_t x2 = c0 ? ld_ro<GL>(srb + e) : 127u;
+        const uint32_t x3 = c1 ? ld_ro<GL>(srb + e + 1) : 127u;
         cs[i].a0 = x0 | (x1 << 8) | (x2 << 16) | (x3 << 24);
       }
       cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
     } else if constexpr (is_mx8<F>()) {
       const int e = k0 / 32;                                                  // a0, a0 + 1 share it
-      const uint32_t x0 = c0 ? __ldg(sra + e) : 127u;
-      const uint32_t x2 = c0 ? __ldg(srb + e) : 127u;
+      const uint32_t x0 = c0 ? ld_ro<GL>(sra + e) : 127u;
+      const uint32_t x2 = c0 ? ld_ro<GL>(srb + e) : 127u;
       cs[i].a0 = prmt(x0, x2, 0x1410u) | 0x7F007F00u;                         // bytes 0 and 2 used, 1 and 3 = 127
       cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
     } else if constexpr (is_fs8<F>() || is_fp4f<F>()) {
       constexpr int B = FmtTraits<F>::block;                                  // 16 (nvfp8), 32 (mxfp4x2), 64 (int8)
       const int e = k0 / B;
-      cs[i].a0 = c0 ? __float_as_uint(float_scale<F>(sra, e)) : 0u;
-      cs[i].b0 = c0 ? __float_as_uint(float_scale<F>(srb, e)) : 0u;
+      cs[i].a0 = c0 ? __float_as_uint(float_scale<F, GL>(sra, e)) : 0u;
+      cs[i].b0 = c0 ? __float_as_uint(float_scale<F, GL>(srb, e)) : 0u;
       if constexpr (B <= LANE) {                                              // quad lane a0 + 1: the next block
-        cs[i].a1 = c1 ? __float_as_uint(float_scale<F>(sra, e + 1)) : 0u;
-        cs[i].b1 = c1 ? __float_as_uint(float_scale<F>(srb, e + 1)) : 0u;
+        cs[i].a1 = c1 ? __float_as_uint(float_scale<F, GL>(sra, e + 1)) : 0u;
+        cs[i].b1 = c1 ? __float_as_uint(float_scale<F, GL>(srb, e + 1)) : 0u;
       } else {                                                                // a0, a0 + 1 share it
         cs[i].a1 = c1 ? cs[i].a0 : 0u;
         cs[i].b1 = c1 ? cs[i].b0 : 0u;
       }
     } else if constexpr (is_i4<F>()) {
       const int e = k0 / 64;                                                  // a0, a0 + 1 share it
-      cs[i].a0 = c0 ? i4_word<F>(sra, e) : 0u;
-      cs[i].b0 = c0 ? i4_word<F>(srb, e) : 0u;
+      cs[i].a0 = c0 ? i4_word<F, GL>(sra, e) : 0u;
+      cs[i].b0 = c0 ? i4_word<F, GL>(srb, e) : 0u;
       cs[i].a1 = cs[i].b1 = 0u;
     } else {   // NVFP4: the lane's own two micro-blocks, one 16-bit pair per row
       const int e = ks / 32;                                                  // pair index (16-code blocks / 2)
-      const uint32_t ma = kin ? __ldg(reinterpret_cast<const uint16_t*>(sra) + e) : 0u;
-      const uint32_t mb2 = kin ? __ldg(reinterpret_cast<const uint16_t*>(srb) + e) : 0u;
+      const uint32_t ma = kin ? ld_ro<GL>(reinterpret_cast<const uint16_t*>(sra) + e) : 0u;
+      const uint32_t mb2 = kin ? ld_ro<GL>(reinterpret_cast<const uint16_t*>(srb) + e) : 0u;
       ms[i] = prmt(ma, mb2, 0x5410u);
       cs[i].a0 = cs[i].a1 = cs[i].b0 = cs[i].b1 = 0u;
     }
@@ -348,9 +448,9 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   };
 
   const int rounds = (mine + P - 1) / P;
-  load_round(0);
+  if constexpr (!STG) load_round(0);
   // chunks past the first round: start them towards L2 now
-  if (rounds > 1 && tid < 16 && row0 + tid < N) {
+  if (!STG && rounds > 1 && tid < 16 && row0 + tid < N) {
     const int64_t first = int64_t(WARPS) * P * 64;
     if (rowbytes > first) {
       const uint8_t* p = codes + int64_t(row0 + tid) * rowbytes + first;
@@ -361,7 +461,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
 
   // Any E8M0 scale byte of this round equal to 0 or 255 sends the warp down the exact decode.
   bool exact = false;
-  if constexpr (is_e8m0<F>()) {
+  if constexpr (is_e8m0<F>() && !STG) {
     bool sp = false;
     #pragma unroll
     for (int i = 0; i < P; ++i) sp |= has_byte_00_or_ff(cs[i].a0);
@@ -377,7 +477,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   // 16 values per task, tasks 2s and 2s+1 (lanes l and l^1) share a 32-span;
   // the span's shift puts its largest |x| in [2^14, 2^15).
   float ssq[2] = {0.0f, 0.0f};                                               // RMS: this lane's sum of x^2 per row
-  {
+  if (jt == 0) {
     constexpr int TPC = CODES / 16;                                            // tasks per chunk and row
     const int per_m = mine * TPC;
     const int tasks = M * per_m;
@@ -393,7 +493,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
         const int j = j0 + lane + 32 * u;
         const int m = j >= per_m ? 1 : 0;
         const int rem = j - m * per_m;
-        const int c = warp + WARPS * (rem / TPC);
+        const int c = kw + WK * (rem / TPC);
         const int k = c * CODES + (rem % TPC) * 16;
         lv[u] = j < tasks && k < K;
         kk[u] = k;
@@ -493,10 +593,42 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   }
   __syncwarp();
 
+  if constexpr (STG) {   // the weight copies requested at the start (bounded wait; the CTA agrees)
+    const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(wbar));
+    if (!__syncthreads_and(mbar_wait_parity(bar, 0, ex.limit_ns))) {
+      if (tid == 0) {   // nothing stored; the copies land before the CTA leaves
+        atomicOr(&g_gather_status, 2u);
+        mbar_wait_parity(bar, 0, ex.limit_ns);
+      }
+      return;
+    }
+  }
+
   // B-operand lanes: (g == t) supplies activation row 0, (g == t + 4) row 1.
   const int mb = g == t ? 0 : (g == t + 4 ? 1 : -1);
   const bool bl = mb >= 0 && mb < M;
   const int md = (t >> 1) < M ? (t >> 1) : M - 1;   // the activation row of this lane's D columns
+
+  const bool tile_live = jt < stage_tiles;
+  if (tile_live) {
+  if constexpr (STG) {   // tile jt's rows in shared memory
+    row0 = jt == 0 ? int(blockIdx.x) * 16 : 16 * tile1;
+    ra = row0 + g;
+    rb = ra + 8;
+    va = ra < N;
+    vb = rb < N;
+    pa = wsm + (16 * jt + g) * stage_wstride(rowbytes) + 16 * t;
+    pb = pa + 8 * stage_wstride(rowbytes);
+    sra = ssm + (16 * jt + g) * stage_sstride(nblk * SB);
+    srb = sra + 8 * stage_sstride(nblk * SB);
+    load_round(0);
+    if constexpr (is_e8m0<F>()) {
+      bool sp = false;
+      #pragma unroll
+      for (int i = 0; i < P; ++i) sp |= has_byte_00_or_ff(cs[i].a0);
+      exact = __any_sync(0xFFFFFFFFu, sp);
+    }
+  }
 
   float acc_a = 0.0f, acc_b = 0.0f;
   for (int r = 0; r < rounds; ++r) {
@@ -519,7 +651,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
     #pragma unroll
     for (int ii = 0; ii < 2; ++ii) {
       const int i = ip + ii;
-      const int c = warp + WARPS * (r * P + i);
+      const int c = kw + WK * (r * P + i);
       const int ks = c * CODES + LANE * t;
       xo[ii] = (bl && r * P + i < mine && ks < K) ? mb * xst + xoff(ks) : M * xst;   // M * xst: the zero block
       d[ii][0] = d[ii][1] = d[ii][2] = d[ii][3] = 0.0f;
@@ -559,7 +691,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
     for (int ii = 0; ii < 2; ++ii) {
       const int i = ip + ii;
       // D columns 2t, 2t+1 hold quad lanes a0, a0 + 1 of activation row md
-      const int c = warp + WARPS * (r * P + i);
+      const int c = kw + WK * (r * P + i);
       const int k0 = c * CODES + LANE * a0;
       const int s0 = min(k0 / 32, spans - 1), s1 = min((k0 + LANE) / 32, spans - 1);
       const float x0s = xsc[md * spans + s0], x1s = xsc[md * spans + s1];
@@ -634,6 +766,7 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
     red[(warp * 2 + (t >> 1)) * 16 + g] = acc_a;
     red[(warp * 2 + (t >> 1)) * 16 + g + 8] = acc_b;
   }
+  }   // tile_live
   if constexpr ((MODE & RMS) != 0) {
     #pragma unroll
     for (int mm = 0; mm < 2; ++mm) {
@@ -645,13 +778,14 @@ __global__ void __launch_bounds__(32 * W, W == 8 ? 2 : 3) qgemv_m2_kernel(const 
   }
   __syncthreads();
   constexpr int OR = X2 ? 8 : 16;                                           // output rows of the tile
-  if (tid < OR * M) {
-    const int m = tid / OR, pr = tid % OR;
+  const int gt = tid - jt * 32 * WK;                                        // thread of the tile's group
+  if (tile_live && gt < OR * M) {
+    const int m = gt / OR, pr = gt % OR;
     const int rr = X2 ? 2 * pr : pr;
     if (row0 + rr < N) {
       float sum = 0.0f;
       #pragma unroll
-      for (int w = 0; w < WARPS; ++w) {
+      for (int w = jt * WK; w < jt * WK + WK; ++w) {
         sum += red[(w * 2 + m) * 16 + rr];
         if constexpr (X2) sum += red[(w * 2 + m) * 16 + rr + 1];             // the residual plane
       }
@@ -674,16 +808,23 @@ static cudaError_t launch_mr(const void* codes, const void* scales, float glob, 
                               bool out_f32, int M, int N, int K, cudaStream_t st, const Extra& ex = Extra{},
                               int tiles = 0, int rows = 1) {
   static std::atomic<int> attr_done[64];
-  const size_t sm = smem_bytes(F, M, K, W);
+  const size_t sm = (MODE & STAGE) != 0
+                        ? stage_smem_bytes(F, M, K, FmtTraits<F>::four ? K / 2 : K,
+                                           int64_t((K + FmtTraits<F>::block - 1) / FmtTraits<F>::block) *
+                                               FmtTraits<F>::sbytes)
+                        : smem_bytes(F, M, K, W);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_done[dev].load()) {
     e = cudaFuncSetAttribute(qgemv_m2_kernel<F, MR, UNI, W, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(SMEM_LIMIT));
+                             int((MODE & STAGE) != 0 ? STAGE_SMEM_LIMIT : SMEM_LIMIT));
     if (e != cudaSuccess) return e;
     attr_done[dev].store(1);
   }
+  Extra exl = ex;
+  exl.limit_ns = wait_limit_ns();
+  exl.drop = drop_arrivals();
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -696,7 +837,23 @@ static cudaError_t launch_mr(const void* codes, const void* scales, float glob, 
   lc.numAttrs = 1;
   return cudaLaunchKernelEx(&lc, qgemv_m2_kernel<F, MR, UNI, W, MODE>, static_cast<const uint8_t*>(codes),
                             static_cast<const uint8_t*>(scales), glob, static_cast<const uint16_t*>(x), out,
-                            int(out_f32), M, N, K, ex);
+                            int(out_f32), M, N, K, exl);
+}
+
+// The staged-weight form (STAGE) where it pays and fits: a launch of at most
+// two CTAs an SM (a larger grid streams its weights anyway), four CTAs'
+// copies within an SM's shared memory, and 16-byte aligned rows.
+template <int F>
+static bool stage_fits(const void* codes, const void* scales, int M, int N, int K, int sms) {
+  // measured (decode chains of 4096 x 4096 layers): faster for the E2M1
+  // formats (mxfp4 3.30 against 3.42 us, fp4 3.30 against 3.68 us), slower
+  // for mxint4, whose int4 pairing needs more registers than a 16-warp CTA has
+  if constexpr (!(F == MXFP4 || F == NVFP4 || F == FP4 || F == FP4_F16)) return false;
+  const int64_t rowb = FmtTraits<F>::four ? K / 2 : K;
+  const int64_t srowb = int64_t((K + FmtTraits<F>::block - 1) / FmtTraits<F>::block) * FmtTraits<F>::sbytes;
+  return (N + 15) / 16 <= 2 * sms && rowb % 16 == 0 && srowb % 16 == 0 &&
+         (reinterpret_cast<uintptr_t>(codes) & 15u) == 0 && (reinterpret_cast<uintptr_t>(scales) & 15u) == 0 &&
+         stage_smem_bytes(F, M, K, rowb, srowb) <= STAGE_SMEM_LIMIT;
 }
 
 // 8-warp CTAs (two per SM); E2M1 formats whose grid exceeds two CTAs per SM
@@ -718,6 +875,15 @@ static cudaError_t launch_fmt(const void* codes, const void* scales, float glob,
                : launch_mr<F, 2, false, 4>(codes, scales, glob, x, out, out_f32, M, N, K, st);
   }
   const bool uni = K % (WARPS * CODES) == 0 && (nchunk / WARPS) % chunks_in_flight<F>() == 0;
+  // the staged form holds two chunks a warp at a time: whole rounds of two
+  const bool stage_uni = K % (WARPS * CODES) == 0 && (nchunk / WARPS) % 2 == 0;
+  if (stage_uni && stage_fits<F>(codes, scales, M, N, K, sms)) {
+    const int grid = std::min((N + 15) / 16, sms);   // one CTA an SM, two tiles where there are enough
+    return M == 1 ? launch_mr<F, 1, true, STAGE_WARPS, STAGE>(codes, scales, glob, x, out, out_f32, M, N, K, st,
+                                                              Extra{}, grid)
+                  : launch_mr<F, 2, true, STAGE_WARPS, STAGE>(codes, scales, glob, x, out, out_f32, M, N, K, st,
+                                                              Extra{}, grid);
+  }
   if (M == 1)
     return uni ? launch_mr<F, 1, true>(codes, scales, glob, x, out, out_f32, M, N, K, st)
                : launch_mr<F, 1, false>(codes, scales, glob, x, out, out_f32, M, N, K, st);

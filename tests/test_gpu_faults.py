@@ -1,8 +1,10 @@
 """Failure detection on the GPU without a fault: every pipeline wait of the
-tensor-core GEMM is bounded.  A test hook makes the decoder warps skip
-signalling their stages (a flag that nothing sets), the MMA warp's wait runs
-out after a short limit, the kernel records QFMT_ETIMEOUT in the device status
-word and exits cleanly; the context stays usable for the next correct call."""
+tensor-core GEMMs and every weight-copy wait of the decode GEMV is bounded.
+A test hook makes a stage never signal (the GEMMs' decoder or scale warps skip
+their arrivals; the decode GEMV does not issue its weight copies), the wait
+runs out after a short limit, the kernel records QFMT_ETIMEOUT in the device
+status word and stores nothing; the context stays usable for the next correct
+call."""
 import numpy as np
 import pytest
 
@@ -29,6 +31,8 @@ def _lib():
 @pytest.mark.parametrize("fmt,m,n,k", [
     ("mxfp8_e4m3", 128, 256, 512),     # one CTA a tile (no K split)
     ("mxfp4", 128, 2048, 4096),        # 8 tiles of one M row: K split over clusters of CTAs
+    ("mxfp4", 1, 4096, 4096),          # the decode GEMV's staged weight copies (not issued)
+    ("nvfp4", 2, 1000, 2048),          # the same, M = 2, a ragged last tile
 ])
 def test_expired_wait_reports_timeout_and_context_survives(fmt, m, n, k):
     w = synth.weights(n, k, seed=3)

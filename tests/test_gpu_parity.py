@@ -371,6 +371,45 @@ def test_gemv_fallback_long_k(fmt, m):
     _check_qmm(out, ref, bound, (fmt, m, k))
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("m", [1, 2])
+@pytest.mark.parametrize("n", [1000, 4000])
+def test_staged_weight_gemv(fmt, m, n):
+    # at most two 16-row tiles an SM and whole rounds of chunks: the E2M1
+    # formats' M <= 2 GEMV bulk-copies each 16-warp CTA's two tiles of weight
+    # and scale rows into shared memory as it starts (one tile a CTA at N =
+    # 1000, two for most CTAs at N = 4000); N ends inside a tile, whose rows
+    # past N are not copied; the other formats take the register form
+    k = 2048
+    c, s, g = _packed(fmt, n, k, seed=70 + m)
+    xb, xt = _x(m, k, seed=71 + m)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+    assert q.qfmt_device_status() == 0
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, m))
+
+
+@pytest.mark.parametrize("fmt", MX_FMTS)
+@pytest.mark.parametrize("m", [1, 2])
+def test_staged_weight_gemv_special_scales(fmt, m):
+    # the staged GEMV's exact E8M0 decode: zero scales among ordinary ones,
+    # then a NaN scale that reaches exactly its row's outputs
+    n, k = 300, 2048
+    c, s, g = _packed(fmt, n, k, seed=75)
+    s = s.copy()
+    s[np.random.default_rng(76).random(s.shape) < 0.2] = 0
+    s[7, :] = 0
+    xb, xt = _x(m, k, seed=77)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, m, "zero scales"))
+    s[9, 40] = 255
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n).float().cpu().numpy()
+    assert np.isnan(out[:, 9]).all()
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _nonfinite_rows_only(out, ref, bound, [9], (fmt, m, "NaN scale"))
+
+
 @pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "int4_affine", "int4", "mxint4"])
 @pytest.mark.parametrize("m", [1, 2])
 def test_wide_gemv_four_warp_ctas(fmt, m):

@@ -110,4 +110,12 @@ cudaError_t launch_qgemv_multi(int fmt, int count, const void* const* codes, con
                                const void* gate = nullptr);
 uint64_t wait_limit_ns();
 
+// Batch decode GEMV, 3 <= M <= 16: one decode of each weight block serves
+// every activation row (qgemv_rb.cuh); where it fits (qgemv_rb_fits).
+bool qgemv_rb_fits(int fmt, int64_t M, int64_t N, int64_t K, int sms);
+cudaError_t launch_qgemv_rb(int fmt, const void* codes, const void* scales, float glob, const void* x, void* out,
+                            bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms);
+void set_gemv_rb(int off);   // measurement hook: 1 = the K-split batch GEMV instead
+cudaError_t read_and_clear_rb_status(unsigned int* status);
+
 }  // namespace qfmt_dev

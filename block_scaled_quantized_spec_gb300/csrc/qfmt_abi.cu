@@ -277,13 +277,15 @@ int qfmt_device_status(void* stream) {
   unsigned int word = 0, gw = 0;
   if ((st = cuda_status(qfmt_dev::read_and_clear_device_status(&word), "device status"))) return st;
   if ((st = cuda_status(qfmt_dev::read_and_clear_gemv_status(&gw), "device status"))) return st;
-  unsigned int gx = 0, mw = 0;
+  unsigned int gx = 0, mw = 0, rb = 0;
   if ((st = cuda_status(qfmt_dev::read_and_clear_gather_status(&gx), "device status"))) return st;
+  if ((st = cuda_status(qfmt_dev::read_and_clear_rb_status(&rb), "device status"))) return st;
   if ((st = cuda_status(qfmt_dev::read_and_clear_mx_status(&mw), "device status"))) return st;
   if (word) return fail(QFMT_ETIMEOUT, "a tensor-core GEMM pipeline wait expired (status 0x%x)", word);
   if (mw & 1u) return fail(QFMT_ETIMEOUT, "a block-scaled GEMM pipeline wait expired (status 0x%x)", mw);
   if (gw) return fail(QFMT_ETIMEOUT, "a GEMV weight-copy wait expired (status 0x%x)", gw);
   if (gx & 2u) return fail(QFMT_ETIMEOUT, "a decode GEMV weight-copy wait expired (status 0x%x)", gx);
+  if (rb) return fail(QFMT_ETIMEOUT, "a batch decode GEMV activation-copy wait expired (status 0x%x)", rb);
   if ((gx & 1u) || (mw & 2u))
     return fail(QFMT_EINDEX, "qmm_gather / qmm_grouped: an expert index outside [0, E) (its output row was zeroed)");
   return QFMT_OK;
@@ -311,6 +313,10 @@ int qfmt_debug_set(int key, int64_t value) {
     static std::atomic<int> off{0}, sk{0};
     (key == 5 ? off : sk).store(int(value));
     qfmt_dev::set_mx_gemv(off.load(), sk.load());
+    return QFMT_OK;
+  }
+  if (key == 7) {   // the batch decode GEMV (3 <= M <= 16): 1 = the K-split kernel instead of the one-decode one
+    qfmt_dev::set_gemv_rb(value ? 1 : 0);
     return QFMT_OK;
   }
   return fail(QFMT_EINVAL, "unknown debug key %d", key);

@@ -533,9 +533,10 @@ cudaError_t read_and_clear_gemv_status(unsigned int* status) {
 
 cudaError_t launch_qgemv(int fmt, const void* codes, const void* scales, float glob, const void* x, void* out,
                          bool out_f32, int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms) {
-  (void)sms;
   if (qgemv_m2_fits(fmt, M, K))
     return launch_qgemv_m2(fmt, codes, scales, glob, x, out, out_f32, M, N, K, st, sms);
+  if (qgemv_rb_fits(fmt, M, N, K, sms))
+    return launch_qgemv_rb(fmt, codes, scales, glob, x, out, out_f32, M, N, K, st, sms);
   if (M >= 3 && qgemv_mb_fits(fmt, M, K))
     return launch_qgemv_mb(fmt, codes, scales, glob, x, out, out_f32, M, N, K, st, sms);
   const int m = int(M), n = int(N), k = int(K);

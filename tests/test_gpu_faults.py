@@ -1,7 +1,8 @@
 """Failure detection on the GPU without a fault: every pipeline wait of the
 tensor-core GEMMs and every weight-copy wait of the decode GEMV is bounded.
 A test hook makes a stage never signal (the GEMMs' decoder or scale warps skip
-their arrivals; the decode GEMV does not issue its weight copies), the wait
+their arrivals; the decode GEMVs do not issue their weight or activation
+copies), the wait
 runs out after a short limit, the kernel records QFMT_ETIMEOUT in the device
 status word and stores nothing; the context stays usable for the next correct
 call."""
@@ -33,6 +34,7 @@ def _lib():
     ("mxfp4", 128, 2048, 4096),        # 8 tiles of one M row: K split over clusters of CTAs
     ("mxfp4", 1, 4096, 4096),          # the decode GEMV's staged weight copies (not issued)
     ("nvfp4", 2, 1000, 2048),          # the same, M = 2, a ragged last tile
+    ("mxint8", 8, 1300, 1024),         # the one-decode batch GEMV's activation copies (not issued)
 ])
 def test_expired_wait_reports_timeout_and_context_survives(fmt, m, n, k):
     w = synth.weights(n, k, seed=3)

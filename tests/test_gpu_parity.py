@@ -410,6 +410,79 @@ def test_staged_weight_gemv_special_scales(fmt, m):
     _nonfinite_rows_only(out, ref, bound, [9], (fmt, m, "NaN scale"))
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("m", [3, 8, 9, 16])
+def test_batch_gemv_one_decode(fmt, m):
+    # 3 <= M <= 16 with K a multiple of 256 and at least 76 16-row tiles: one
+    # decode of each weight block serves every activation row (the rows are
+    # the MMA's columns, 8 a set); N ends inside a tile
+    n, k = 1300, 1024
+    c, s, g = _packed(fmt, n, k, seed=90 + m)
+    xb, xt = _x(m, k, seed=91 + m)
+    dc, ds = _dev(c), _dev(s)
+    out = q.qmm(fmt, dc, ds, g, xt, n)
+    assert q.qfmt_device_status() == 0
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, m))
+    q.qfmt_debug_set(7, 1)                 # the same rows through the K-split batch GEMV
+    try:
+        other = q.qmm(fmt, dc, ds, g, xt, n).float().cpu().numpy()
+    finally:
+        q.qfmt_debug_set(7, 0)
+    a = out.float().cpu().numpy()
+    assert (np.abs(a - other) <= 2 * bound + bf16_half_ulp(a) + bf16_half_ulp(other)).all()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "int4_affine", "mxint4", "mxfp8_e5m2", "nvfp8", "int8", "mxfp4x2"])
+def test_batch_gemv_several_tiles_a_cta(fmt):
+    # 313 tiles over one CTA an SM: up to three tiles a CTA, two blocks a warp,
+    # so the loads run ahead across tile ends; float32 output
+    m, n, k = 16, 5000, 512
+    c, s, g = _packed(fmt, n, k, seed=95)
+    xb, xt = _x(m, k, seed=96)
+    out = q.qmm_ex(fmt, _dev(c), _dev(s), g, xt, n, out_dtype=torch.float32)
+    assert q.qfmt_device_status() == 0
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, fmt)
+
+
+@pytest.mark.parametrize("fmt", MX_FMTS)
+def test_batch_gemv_special_scales(fmt):
+    # E8M0 0 and 255 scales on the one-decode batch GEMV
+    m, n, k = 5, 1300, 512
+    c, s, g = _packed(fmt, n, k, seed=97)
+    s = s.copy()
+    s[np.random.default_rng(98).random(s.shape) < 0.2] = 0
+    s[11, :] = 0
+    xb, xt = _x(m, k, seed=99)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _check_qmm(out, ref, bound, (fmt, "zero scales"))
+    s[13, 3] = 255
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n).float().cpu().numpy()
+    assert np.isnan(out[:, 13]).all()
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _nonfinite_rows_only(out, ref, bound, [13], (fmt, "NaN scale"))
+
+
+@pytest.mark.parametrize("fmt", list(SPECIAL_CODES))
+def test_batch_gemv_special_element_codes(fmt):
+    # NaN / Inf element codes on the one-decode batch GEMV: exactly their rows'
+    # outputs are non-finite
+    m, n, k = 5, 1300, 512
+    c, s, g = _packed(fmt, n, k, seed=36)
+    c = c.copy()
+    rows = []
+    for i, code in enumerate(SPECIAL_CODES[fmt]):
+        r = 17 + 101 * i
+        c[r, 45 + 64 * i] = code
+        rows.append(r)
+    xb, xt = _x(m, k, seed=37)
+    out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n).float().cpu().numpy()
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    _nonfinite_rows_only(out, ref, bound, rows, (fmt, m))
+
+
 @pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "int4_affine", "int4", "mxint4"])
 @pytest.mark.parametrize("m", [1, 2])
 def test_wide_gemv_four_warp_ctas(fmt, m):

@@ -401,8 +401,8 @@ def run_reference(args):
 # kernel reports null until it is captured again).
 TRAFFIC = {
     "kernel_source": "block_scaled_quantized_spec_gb300/csrc/qgemv_m2.cuh",
-    "sha256_16": "0ea978bf1488616d",
-    "bytes": 8940288,
+    "sha256_16": "1c718fb308e9a9d9",
+    "bytes": 8937472,
     "profile": "profiles/qgemv_m2_mxfp4_M1_N4096_K4096.md",
 }
 
@@ -423,7 +423,8 @@ def roofline_gemv(prob, ms_step, hbm, kind):
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "traffic": measured_traffic(),
             "traffic_source": TRAFFIC["profile"], "peak_kind": f"{kind} (STREAM copy, burst)",
-            "kernel": f"qgemv_m2_kernel<{prob.fmt}>", "per_launch_us": round(per_launch_ms * 1e3, 3),
+            "kernel": f"qgemv_m2_kernel<{prob.fmt}, 1 row, 16 warps, staged weights>",
+            "per_launch_us": round(per_launch_ms * 1e3, 3),
             "algorithmic_bytes_per_launch": prob.bytes}
 
 
@@ -449,6 +450,8 @@ BREAKDOWN = [
     ("mxfp4", 2048, 4096, 4096), ("mxfp4", 2048, 4096, 4096, "A"),
     # the 2/3/5/6-bit bit streams
     ("int3", 1, 11008, 4096), ("mxint5", 16, 4096, 4096),
+    # batch decode rows on [4096, 4096] (one decode per weight block for every activation row)
+    ("mxfp4", 8, 4096, 4096), ("mxfp8_e4m3", 8, 4096, 4096), ("int8", 8, 4096, 4096),
 ]
 
 # The standalone dequant kernel: [4096, 4096] weights to float32 and bf16.

@@ -470,7 +470,9 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
             reinterpret_cast<float4*>(o)[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                                           __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
         } else {
-          for (int j = 0; j < ncols; ++j) o[j] = __uint_as_float(r[j]);
+          #pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < ncols) o[j] = __uint_as_float(r[j]);
         }
       } else {
         __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + int64_t(m) * p.N + nb;
@@ -485,7 +487,9 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
             reinterpret_cast<uint4*>(o)[j] = make_uint4(h[0], h[1], h[2], h[3]);
           }
         } else {
-          for (int j = 0; j < ncols; ++j) o[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+          #pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < ncols) o[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
         }
       }
     }

@@ -424,7 +424,11 @@ int qfmt_device_status(void* stream);
  * decoder warps skip signalling their stages, so the MMA warp's waits expire
  * (value 0 restores normal operation); keys 3 and 4 force the block-scaled
  * GEMM's tile width (224 or 256) and K split (1-4), value 0 restoring its own
- * plan (for measurements).  Returns QFMT_EINVAL for other keys.
+ * plan; key 5 with value 1 sends the MX formats' decode GEMV (M <= 16) to the
+ * mma.sync kernels instead of the block-scaled tensor-core one, key 6 forces
+ * that kernel's K split; key 7 with value 1 sends the batch decode GEMV
+ * (3 <= M <= 16) to the K-split kernel -- all for measurements and tests.
+ * Returns QFMT_EINVAL for other keys.
  */
 int qfmt_debug_set(int key, int64_t value);
 

@@ -298,3 +298,14 @@ def test_binding_rejects_bad_tensors_before_the_call(lib):
     rejects(q.qmm_gated_rmsnorm, fmt, codes, scales, 1.0, x, torch.zeros((2, k), dtype=torch.float32),
             torch.zeros(k, dtype=torch.bfloat16), 1e-5, n, match="gate must be torch.bfloat16")
     rejects(q.qmm_batched, fmt, [codes] * 5, [scales] * 5, [1.0] * 5, x, [n] * 5, match="1..4")
+
+
+def test_debug_keys_without_gpu(lib):
+    # the test and measurement settings are host state: every documented key
+    # takes its default value, unknown keys are refused
+    for key in range(1, 8):
+        q.qfmt_debug_set(key, 0)
+    for key, value in ((0, 0), (8, 0), (-1, 1)):
+        with pytest.raises(q.QfmtError) as e:
+            q.qfmt_debug_set(key, value)
+        assert e.value.status == -1

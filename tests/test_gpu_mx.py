@@ -161,11 +161,12 @@ def test_workspace_query_and_errors():
     assert e.value.status == -8
 
 
-def test_expired_wait_block_scaled():
+@pytest.mark.parametrize("m,n,k", [(256, 512, 1024), (2000, 2300, 256)])
+def test_expired_wait_block_scaled(m, n, k):
     # the W-scale warp never signals (test hook): the MMA warp's bounded wait
     # expires, the status word reports it, no output is written, and the next
-    # call is correct
-    fmt, m, n, k = "mxfp8_e4m3", 256, 512, 1024
+    # call is correct (a K-split cluster; 176 tiles of two K steps)
+    fmt = "mxfp8_e4m3"
     c, s, g = opack.pack(fmt, synth.weights(n, k, seed=5))
     xb, xt = _x(m, k, seed=6)
     dc, ds = _dev(c), _dev(s)
@@ -228,3 +229,31 @@ def test_tensor_core_decode_gemv(fmt, m, k):
         q.qfmt_debug_set(5, 0)
     a = out.float().cpu().numpy()
     assert (np.abs(a - other) <= 2 * bound + bf16_half_ulp(a) + bf16_half_ulp(other)).all()
+
+
+@pytest.mark.parametrize("fmt", MXB)
+@pytest.mark.parametrize("m,n,k", [(130, 300, 128), (300, 520, 384), (2000, 2300, 640), (1200, 4100, 1152)])
+def test_stage_ring_wraps(fmt, m, n, k):
+    # three stages: 1, 3, 5 and 9 K steps leave the stage ring at every
+    # offset; the planner's tiles and forced tile widths and K splits (debug
+    # keys 3, 4) all agree with the oracle, and the quantized-activation
+    # product runs the same ring
+    c, s, g = opack.pack(fmt, synth.weights(n, k, seed=m + 1))
+    xb, xt = _x(m, k, seed=m + 2)
+    dc, ds = _dev(c), _dev(s)
+    ws = torch.empty(q.qmm_workspace_bytes(fmt, m, k), dtype=torch.uint8, device=DEV)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    try:
+        for bn, sk in ((0, 0), (224, 1), (256, 2), (256, 3)):
+            q.qfmt_debug_set(3, bn)
+            q.qfmt_debug_set(4, sk)
+            out = q.qmm_ex(fmt, dc, ds, g, xt, n, workspace=ws)
+            assert q.qfmt_device_status() == 0
+            check_tensor(out, ref, bound, (fmt, m, n, k, bn, sk))
+    finally:
+        q.qfmt_debug_set(3, 0)
+        q.qfmt_debug_set(4, 0)
+    out8 = q.qmm_a8(fmt, dc, ds, xt, n)
+    assert q.qfmt_device_status() == 0
+    ref8, bound8 = oref.qmm_a8_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    check_tensor(out8, ref8, bound8, (fmt, "a8", m, n, k))

@@ -90,6 +90,7 @@ struct Params {
   int kb_per;          // K steps per split (grid z = the splits of one cluster)
   uint64_t limit_ns;   // bound on every wait
   int drop_arrivals;   // test hook: decoders never signal a stage (the waits must expire)
+  int mfast;           // tile order: blockIdx.x the M tile, y the N tile (else x = N tile, y = M tile)
 };
 
 // The codes a decoder thread holds for one piece: 16 bytes of one row, or for
@@ -128,7 +129,12 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM * MT;
+  // consecutive CTAs walk the N tiles of an M tile (its X tile shared, the
+  // whole W streamed per M tile) or, mfast, the M tiles of an N tile (its W
+  // tile shared, the whole X streamed per N tile): the host picks the order
+  // that streams the smaller operand again, the larger one once
+  const int n0 = (p.mfast ? blockIdx.y : blockIdx.x) * BN, m0 = (p.mfast ? blockIdx.x : blockIdx.y) * BM * MT;
+  const int mtiles = p.mfast ? gridDim.x : gridDim.y;
   const int nkb = (p.K + BK - 1) / BK;
   // K split: this CTA accumulates K steps [kb0, kb1) (one split per cluster rank along z)
   const int kb0 = blockIdx.z * p.kb_per;
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
     };
     // one M tile: this CTA's weight slab [kb0, kb1) towards L2 now (one row
     // per thread); with more M tiles the other tiles' CTAs share it
-    if (gridDim.y == 1 && dt < BN && n0 + dt < p.N && nloc > 0) {
+    if (mtiles == 1 && dt < BN && n0 + dt < p.N && nloc > 0) {
       const int64_t kbeg = int64_t(kb0) * BK, kend = min(int64_t(kb1) * BK, int64_t(p.K));
       if constexpr (F == MXFP4X2) {   // both planes of the row
         const uint8_t* src = p.codes + int64_t(n0 + dt) * p.K + kbeg / 2;
@@ -448,6 +454,7 @@ static EncodeTiledFn encode_fn() {
 
 static std::atomic<uint64_t> g_limit_ns{2000000000ull};
 static std::atomic<int> g_drop{0};
+static std::atomic<int> g_order{0};   // tile order override for measurements: 0 the host's choice, 1 N tiles first, 2 M tiles first
 
 template <int F, int MT, int BN = Tile<F>::BN>
 static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* scales, float glob, const void* x,
@@ -494,7 +501,17 @@ static cudaError_t launch_mt(EncodeTiledFn enc, const void* codes, const void* s
   at[1].val.clusterDim.x = 1;
   at[1].val.clusterDim.y = 1;
   at[1].val.clusterDim.z = unsigned(S);
-  lc.gridDim = dim3((N + BN - 1) / BN, (M + BM * MT - 1) / (BM * MT), S);
+  // Tile order (no K split): M tiles first when the activations are the
+  // smaller operand, so that each wave streams a band of W once and every CTA
+  // of the band re-reads X from L2 (nvfp8 M = 4096, N = 11008: X 34 MB, W 45 MB
+  // read once per M tile in the N-first order)
+  const int64_t ntl = (N + BN - 1) / BN, mtl = (M + BM * MT - 1) / (BM * MT);
+  const double xbytes = 2.0 * double(M) * double(K);
+  const double wbytes = double(N) * double(K) * (FmtTraits<F>::four && F != MXFP4X2 ? 0.5 : 1.0);
+  prm.mfast = S == 1 && mtl > 1 && ntl <= 65535 && xbytes < wbytes ? 1 : 0;
+  if (S == 1 && g_order.load() == 1) prm.mfast = 0;
+  if (S == 1 && g_order.load() == 2 && ntl <= 65535) prm.mfast = 1;
+  lc.gridDim = prm.mfast ? dim3(unsigned(mtl), unsigned(ntl), 1) : dim3(unsigned(ntl), unsigned(mtl), S);
   lc.blockDim = dim3(Dec<F>::CTA_THREADS);
   lc.dynamicSmemBytes = Pipe<MT>::SMEM_BYTES;
   lc.stream = st;
@@ -593,6 +610,7 @@ cudaError_t launch_qgemm_tc(int fmt, const void* codes, const void* scales, floa
 void set_wait_limit_ns(uint64_t ns) { tc::g_limit_ns.store(ns); }
 uint64_t wait_limit_ns() { return tc::g_limit_ns.load(); }
 void set_drop_arrivals(int on) { tc::g_drop.store(on); }
+void set_tc_order(int v) { tc::g_order.store(v); }
 int drop_arrivals() { return tc::g_drop.load(); }
 
 cudaError_t read_and_clear_device_status(unsigned int* status) {

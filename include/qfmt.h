@@ -427,8 +427,10 @@ int qfmt_device_status(void* stream);
  * plan; key 5 with value 1 sends the MX formats' decode GEMV (M <= 16) to the
  * mma.sync kernels instead of the block-scaled tensor-core one, key 6 forces
  * that kernel's K split; key 7 with value 1 sends the batch decode GEMV
- * (3 <= M <= 16) to the K-split kernel -- all for measurements and tests.
- * Returns QFMT_EINVAL for other keys.
+ * (3 <= M <= 16) to the K-split kernel; key 8 sets the order in which the
+ * bf16-decode GEMM walks its tiles (0 its own choice, 1 N tiles first, 2 M
+ * tiles first) -- all for measurements and tests.  Returns QFMT_EINVAL for
+ * other keys and values.
  */
 int qfmt_debug_set(int key, int64_t value);
 

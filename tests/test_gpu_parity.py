@@ -125,6 +125,29 @@ def test_qgemm_parity(fmt, m):
     _check_qmm(out, ref, bound, (fmt, m))
 
 
+@pytest.mark.parametrize("fmt", FMTS[:20])
+def test_qgemm_tile_orders(fmt):
+    # the bf16-decode GEMM walks the M tiles of an N tile first when the
+    # activations are the smaller operand (here X 0.5 MB, W 0.6-1.3 MB), the N
+    # tiles of an M tile first otherwise; both orders forced (debug key 8) over
+    # 4 x 20-40 tiles with ragged last M and N tiles agree with the oracle and,
+    # accumulating in the same order, with each other bit for bit
+    m, n, k = 1000, 5000, 256
+    c, s, g = _packed(fmt, n, k, seed=31)
+    xb, xt = _x(m, k, seed=32)
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    outs = []
+    try:
+        for order in (0, 1, 2):
+            q.qfmt_debug_set(8, order)
+            out = q.qmm(fmt, _dev(c), _dev(s), g, xt, n)
+            _check_qmm(out, ref, bound, (fmt, "order", order))
+            outs.append(out.float().cpu().numpy())
+    finally:
+        q.qfmt_debug_set(8, 0)
+    assert np.array_equal(outs[1], outs[2])
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("m", [3, 40, 130])
 def test_short_and_odd_k(fmt, m):

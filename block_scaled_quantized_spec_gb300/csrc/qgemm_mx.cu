@@ -1087,8 +1087,11 @@ __global__ void __launch_bounds__(GV_THREADS) qgemv_mx_kernel(const __grid_const
     else static_cast<__nv_bfloat16*>(p.out)[int64_t(m) * p.N + n] = __float2bfloat16_rn(val);
   };
   if (S == 1) {
-    if (ok && *abort_flag == 0u && n0 + row < p.N)
-      for (int m = 0; m < p.M; ++m) store(m, n0 + row, v[m]);
+    if (ok && *abort_flag == 0u && n0 + row < p.N) {
+      #pragma unroll
+      for (int m = 0; m < NP / 2; ++m)
+        if (m < p.M) store(m, n0 + row, v[m]);
+    }
   } else {
     #pragma unroll
     for (int m = 0; m < NP / 2; ++m) part[row * 17 + m] = v[m];

@@ -360,7 +360,9 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
             for (int j = 0; j < 8; ++j)
               reinterpret_cast<float4*>(o)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           } else {
-            for (int j = 0; j < ncols; ++j) o[j] = v[j];
+            #pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < ncols) o[j] = v[j];
           }
         } else {
           __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + int64_t(m) * p.N + nb;
@@ -374,7 +376,9 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
               reinterpret_cast<uint4*>(o)[j] = make_uint4(h[0], h[1], h[2], h[3]);
             }
           } else {
-            for (int j = 0; j < ncols; ++j) o[j] = __float2bfloat16_rn(v[j]);
+            #pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < ncols) o[j] = __float2bfloat16_rn(v[j]);
           }
         }
       }

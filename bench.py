@@ -46,7 +46,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-breakdown", action="store_true")
-    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K[:A], gather:fmt:M:N:K:E, batched:fmt:M:N1,N2:K, "
+    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K[:A|:A8], gather:fmt:M:N:K:E, batched:fmt:M:N1,N2:K, "
                    "rmsnorm:fmt:M:N:K, gated_rmsnorm:fmt:M:N:K or dequant:fmt:N:K:f32|bf16")
     return p.parse_args()
 
@@ -164,7 +164,9 @@ class Problem:
 
     path "auto": a workspace when the call can use one (the block-scaled
     tensor-core GEMM of the MX formats, M > 16), the call a user makes with
-    one; "A": no workspace (the bf16-decode GEMM).
+    one; "A": no workspace (the bf16-decode GEMM); "A8": both operands
+    quantized (qmm_a8: the activations packed to MXFP8 E4M3, one
+    block-scaled MMA per block).
     """
 
     def __init__(self, fmt, m, n, k, copies, seed=0, path="auto"):
@@ -190,16 +192,19 @@ class Problem:
         self.copies = copies
         self.bytes = sizes(fmt, m, n, k)
         self.flops = 2.0 * m * n * k
-        wsb = q.qmm_workspace_bytes(fmt, m, k) if path == "auto" else 0
+        self.a8 = path == "A8"
+        wsb = q.qmm_a8_workspace_bytes(fmt, m, k) if self.a8 else (q.qmm_workspace_bytes(fmt, m, k) if path == "auto" else 0)
         # one workspace serves every layer: each call's activation split waits
         # for the previous call to finish before it writes
         self.ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
-        self.path = "SUB" if fmt in q.SUB_BYTE else ("B" if wsb else ("A" if m > 16 else "GEMV"))
+        self.path = "A8" if self.a8 else ("SUB" if fmt in q.SUB_BYTE else ("B" if wsb else ("A" if m > 16 else "GEMV")))
 
     def step(self):
         import block_scaled_quantized_spec_gb300 as q
         for i in range(self.copies):
-            if self.ws is not None:
+            if self.a8:
+                q.qmm_a8(self.fmt, self.codes[i], self.scales[i], self.x[i], self.n, out=self.out[i], workspace=self.ws)
+            elif self.ws is not None:
                 q.qmm_ex(self.fmt, self.codes[i], self.scales[i], self.g, self.x[i], self.n, out=self.out[i],
                          workspace=self.ws)
             else:
@@ -448,6 +453,9 @@ BREAKDOWN = [
     ("mxfp8_e4m3", 2048, 4096, 4096, "A"), ("mxfp8_e5m2", 128, 11008, 4096, "A"),
     ("mxfp8_e5m2", 4096, 11008, 4096, "A"),
     ("mxfp4", 2048, 4096, 4096), ("mxfp4", 2048, 4096, 4096, "A"),
+    # both operands quantized (W . A8)
+    ("mxfp8_e4m3", 2048, 4096, 4096, "A8"), ("mxfp4", 2048, 4096, 4096, "A8"),
+    ("mxfp8_e5m2", 4096, 11008, 4096, "A8"),
     # the 2/3/5/6-bit bit streams
     ("int3", 1, 11008, 4096), ("mxint5", 16, 4096, 4096),
     # batch decode rows on [4096, 4096] (one decode per weight block for every activation row)
@@ -686,6 +694,7 @@ def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3, path="auto"
     prob_flops_per_byte = prob.flops / nbytes
     row = {"fmt": fmt, "M": m, "N": n, "K": k, "us": round(per * 1e3, 2), "copies": copies,
            "path": {"B": "block-scaled tcgen05 GEMM (X split + kind::mxf8f6f4)", "A": "bf16-decode tcgen05 GEMM",
+                    "A8": "both operands quantized (X to MXFP8 E4M3, one kind::mxf8f6f4 MMA per block)",
                     "GEMV": "decode GEMV", "SUB": "CUDA-core sub-byte kernel"}[prob.path]}
     gbs = nbytes / (per * 1e-3) / 1e9
     tfl = prob.flops / (per * 1e-3) / 1e12
@@ -697,6 +706,8 @@ def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3, path="auto"
         fp_peak = {"mxfp8_e4m3": 2 * bf16, "mxfp8_e5m2": 2 * bf16, "nvfp8": 2 * bf16, "nvfp8_f16": 2 * bf16,
                    "mxint8": bf16, "int8": bf16, "int8_f16": bf16, "int4": bf16, "int4_f16": bf16,
                    "mxfp4x2": bf16, "mxint4": bf16, "fp8_e4m3": 2 * bf16, "fp8_e5m2": 2 * bf16}.get(fmt, 6 * bf16)
+        if prob.path == "A8":   # FP8 operands on both sides: the FP8 rate
+            fp_peak = 2 * bf16
         row["bf16_frac"] = round(tfl / bf16, 4)
         row["native_peak_frac"] = round(tfl / fp_peak, 4)
         # against the roofline at this arithmetic intensity: min(bf16 peak, FLOP/byte x HBM)

@@ -83,6 +83,7 @@ cudaError_t launch_qgemv_mx(int fmt, const void* codes, const void* scales, cons
 void set_mx_wait_limit_ns(uint64_t ns);
 void set_mx_drop_arrivals(int on);
 void set_mx_plan(int bn, int s);   // measurement hook: force the tile width (224/256) and K split (1-4); 0 = planner
+void set_mx_tall(int v);           // measurement hook: quantized-activation GEMM tall tiles: 0 = planner, 1 = never, 2 = where allowed
 void set_tc_order(int v);          // measurement hook: bf16-decode GEMM tile order: 0 = host's choice, 1 = N first, 2 = M first
 void set_mx_gemv(int off, int s);  // measurement hook: 1 = the mma.sync GEMVs for the MX formats; forced K split
 cudaError_t read_and_clear_mx_status(unsigned int* status);

@@ -319,6 +319,11 @@ int qfmt_debug_set(int key, int64_t value) {
     qfmt_dev::set_gemv_rb(value ? 1 : 0);
     return QFMT_OK;
   }
+  if (key == 9) {   // the quantized-activation GEMM's tall tiles: 0 = its plan, 1 = never, 2 = wherever allowed
+    if (value < 0 || value > 2) return fail(QFMT_EINVAL, "debug key 9 takes 0, 1 or 2");
+    qfmt_dev::set_mx_tall(int(value));
+    return QFMT_OK;
+  }
   if (key == 8) {   // the bf16-decode GEMM's tile order: 0 = the host's choice, 1 = N tiles first, 2 = M tiles first
     if (value < 0 || value > 2) return fail(QFMT_EINVAL, "debug key 8 takes 0, 1 or 2");
     qfmt_dev::set_tc_order(int(value));

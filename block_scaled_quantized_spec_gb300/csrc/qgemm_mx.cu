@@ -265,19 +265,25 @@ template <int F> constexpr uint32_t b_type() {
 // BN: the tile's N (256, or 224 where that fills the waves of 152 SMs better).
 // TWO: the activations as two E4M3 terms (hi + lo, two MMAs per block), else
 // one (the quantized-activation product: one MMA per block).
+// TALL (one term only): a CTA takes two 128-row M tiles (256 x BN) into two
+// accumulators sharing each stage's W tile, the second X tile in the stage
+// memory the lo term uses otherwise: 60 KiB land per K step for twice the
+// output of a 44 KiB single-tile step.  Tensor memory: accumulators at
+// columns 0 and 256, the stages' scale slots at 224, 240 and 480.
 // A K split runs its splits as a cluster along z; each split's float32
 // partial tile goes to its drained stage memory and the cluster sums them
 // through distributed shared memory in rank order.
-template <int F, int BN, bool TWO = true>
+template <int F, int BN, bool TWO = true, bool TALL = false>
 __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_constant__ CUtensorMap xhi_map,
                                                               const __grid_constant__ CUtensorMap xlo_map,
                                                               const __grid_constant__ CUtensorMap w_map,
                                                               const MxParams p) {
   static_assert(BN % 32 == 0 && BN <= BN_MAX && BN > 128, "two W scale atoms a stage");
-  // bytes a stage's copies deliver: the two X terms, the W codes (E2M1: the
-  // 8 data bytes of every 16-byte unit, the gaps are not written) and the two
-  // X scale atoms
-  constexpr int TERMS = TWO ? 2 : 1;
+  static_assert(!TALL || (!TWO && BN == 224), "tall tiles: one term, 224 columns");
+  // bytes a stage's copies deliver: the two X tiles (terms, or M halves), the
+  // W codes (E2M1: the 8 data bytes of every 16-byte unit, the gaps are not
+  // written) and the two X scale atoms
+  constexpr int TERMS = (TWO || TALL) ? 2 : 1;
   constexpr uint32_t TX_BYTES = TERMS * (A_BYTES + SF_BYTES) + (F == MXFP4 ? BN * BK / 2 : BN * BK);
   constexpr int PSTRIDE = BN + 4;                 // floats per partial-tile row (K split)
   extern __shared__ uint8_t smem_raw[];
@@ -290,7 +296,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM * (TALL ? 2 : 1);
   // grouped rows: the tile's expert (its weights are rows [e N, e N + N) of the
   // stacked matrix); tiles past the last segment have nothing to do (every CTA
   // of a K-split cluster shares blockIdx.y, so a cluster leaves whole)
@@ -349,8 +355,13 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
       asm volatile("griddepcontrol.wait;" ::: "memory");   // the workspace comes from the preceding xquant
-      const uint8_t* sfh = p.sf_hi + size_t(blockIdx.y) * size_t(nk) * SF_BYTES;
-      const uint8_t* sfl = p.sf_lo + size_t(blockIdx.y) * size_t(nk) * SF_BYTES;
+      // the X scale atoms of this tile's 128-row M tile(s); a second M half
+      // past M has none (its rows are zeros and stored nowhere): the first
+      // half's atoms stand in
+      const size_t mt0 = TALL ? size_t(2 * blockIdx.y) : size_t(blockIdx.y);
+      const uint8_t* sfh = p.sf_hi + mt0 * size_t(nk) * SF_BYTES;
+      const uint8_t* sfl = TALL ? (m0 + BM < p.M ? sfh + size_t(nk) * SF_BYTES : sfh)
+                                : p.sf_lo + size_t(blockIdx.y) * size_t(nk) * SF_BYTES;
       int issued = 0;
       for (int i = 0; i < nloc; ++i) {
         const int s = i % STAGES, j = j0 + i;
@@ -360,9 +371,10 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         mbar_arrive_expect_tx(full(s), TX_BYTES);
         tma_load_2d(a_hi(s), &xhi_map, j * BK, m0, full(s));
         if constexpr (TWO) tma_load_2d(a_lo(s), &xlo_map, j * BK, m0, full(s));
+        if constexpr (TALL) tma_load_2d(a_lo(s), &xhi_map, j * BK, m0 + BM, full(s));   // the second M half
         tma_load_2d(b_tile(s), &w_map, j * BK, wrow0 + n0, full(s));
         bulk_load(sf_s(s, 0), sfh + size_t(j) * SF_BYTES, SF_BYTES, full(s));
-        if constexpr (TWO) bulk_load(sf_s(s, 1), sfl + size_t(j) * SF_BYTES, SF_BYTES, full(s));
+        if constexpr (TWO || TALL) bulk_load(sf_s(s, 1), sfl + size_t(j) * SF_BYTES, SF_BYTES, full(s));
         issued = i + 1;
       }
       // every issued copy lands before the CTA may exit
@@ -379,9 +391,10 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         if (*abort_flag) break;
         if (!mbar_wait(full(s), ph, p.limit_ns) || !mbar_wait(sf_full(s), ph, p.limit_ns)) { fail(); break; }
         tc_fence_after();
-        const uint32_t sfc = tmem + uint32_t(SF_COL0 + 16 * s);   // hi: +0, lo: +4, W: +8 (rows 0-127), +12 (128-255)
+        // hi (first M half): +0, lo (second M half): +4, W: +8 (rows 0-127), +12 (128-255)
+        const uint32_t sfc = tmem + uint32_t(TALL ? (s < 2 ? 224 + 16 * s : 480) : SF_COL0 + 16 * s);
         tmem_cp_sf(sfc + 0, umma::smem_desc_sf32x16(sf_s(s, 0)));
-        if constexpr (TWO) tmem_cp_sf(sfc + 4, umma::smem_desc_sf32x16(sf_s(s, 1)));
+        if constexpr (TWO || TALL) tmem_cp_sf(sfc + 4, umma::smem_desc_sf32x16(sf_s(s, 1)));
         tmem_cp_sf(sfc + 8, umma::smem_desc_sf32x16(sf_s(s, 2)));
         tmem_cp_sf(sfc + 12, umma::smem_desc_sf32x16(sf_s(s, 3)));
         const uint64_t dh = desc_sw128(a_hi(s)), dl = desc_sw128(a_lo(s)), db = desc_sw128(b_tile(s));
@@ -390,6 +403,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
           const uint32_t id = umma::idesc_mxf8f6f4(umma::F8F6F4_E4M3, BT, BM, BN, uint32_t(kk), uint32_t(kk));
           mma_mx(tmem, dh + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 0, sfc + 8, (i | kk) != 0);
           if constexpr (TWO) mma_mx(tmem, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 4, sfc + 8, 1u);
+          if constexpr (TALL)
+            mma_mx(tmem + 256u, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 4, sfc + 8, (i | kk) != 0);
         }
         mma_commit(empty(s));
       }
@@ -443,14 +458,16 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     tc_fence_after();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int q = warp & 3;
+    #pragma unroll 1
+    for (int hf = 0; hf < (TALL ? 2 : 1); ++hf) {   // the accumulators: M halves of a tall tile
     // the output row of this lane's accumulator row (grouped: through row_of)
-    int m = m0 + q * 32 + lane;
+    int m = m0 + hf * BM + q * 32 + lane;
     if (p.route_off) m = m < __ldg(p.route_off + p.E) ? __ldg(p.row_of + m) : -1;
     const bool live = ok && *abort_flag == 0u && m >= 0;
     #pragma unroll 1
     for (int cb = 0; cb < BN / 32; ++cb) {
       uint32_t r[32];
-      tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(cb * 32), r);
+      tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(hf * 256 + cb * 32), r);
       if (split_k) {   // this split's partial tile into the drained stage memory
         float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(smem) + (q * 32 + lane) * PSTRIDE + cb * 32);
         #pragma unroll
@@ -493,6 +510,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         }
       }
     }
+    }   // hf
   }
 
   if (split_k) {
@@ -581,6 +599,7 @@ static bool make_map(EncodeTiledFn enc, CUtensorMap* map, CUtensorMapDataType dt
 static std::atomic<uint64_t> g_limit_ns{2000000000ull};
 static std::atomic<int> g_drop{0};
 static std::atomic<int> g_force_bn{0}, g_force_s{0};   // plan overrides for measurements (0: the planner's)
+static std::atomic<int> g_force_tall{0};                // quantized-activation GEMM: 0 plan, 1 no tall tiles, 2 tall where allowed
 static std::atomic<int> g_gemv_off{0}, g_gemv_s{0};     // decode GEMV: off (mma.sync GEMVs), forced K split
 
 // Tile width and K split, by the estimated time in K steps of one CTA:
@@ -595,12 +614,14 @@ struct MxPlan {
   int BN, S;
 };
 
-template <int F, int BN, bool TWO = true>
+template <int F, int BN, bool TWO = true, bool TALL = false>
 static cudaError_t set_smem(int dev) {
   static std::atomic<int> done[64];
   if (dev < 0 || dev >= 64 || done[dev].load()) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e =
+      cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO, TALL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO, TALL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[dev].store(1);
   return e;
 }
@@ -655,7 +676,7 @@ static MxPlan plan_mx(int dev, int M, int N, int K, int sms) {
   return best;
 }
 
-template <int F, int BN, bool TWO = true>
+template <int F, int BN, bool TWO = true, bool TALL = false>
 static cudaError_t launch_tile(const CUtensorMap& mhi, const CUtensorMap& mlo, const CUtensorMap& mw, MxParams prm,
                                int M, int N, int S, cudaStream_t st) {
   const int nk = prm.K / BK;
@@ -668,13 +689,14 @@ static cudaError_t launch_tile(const CUtensorMap& mhi, const CUtensorMap& mlo, c
   at[1].val.clusterDim.x = 1;
   at[1].val.clusterDim.y = 1;
   at[1].val.clusterDim.z = unsigned(S);
-  lc.gridDim = dim3((N + BN - 1) / BN, (M + BM - 1) / BM, S);
+  constexpr int TM = TALL ? 2 * BM : BM;
+  lc.gridDim = dim3((N + BN - 1) / BN, (M + TM - 1) / TM, S);
   lc.blockDim = dim3(THREADS);
   lc.dynamicSmemBytes = SMEM_BYTES;
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 2;
-  return cudaLaunchKernelEx(&lc, qgemm_mx_kernel<F, BN, TWO>, mhi, mlo, mw, prm);
+  return cudaLaunchKernelEx(&lc, qgemm_mx_kernel<F, BN, TWO, TALL>, mhi, mlo, mw, prm);
 }
 
 template <int F>
@@ -753,13 +775,21 @@ static cudaError_t launch_a8(const void* codes, const void* scales, const void* 
       (e = set_smem<F, 224, false>(dev)) != cudaSuccess)
     return e;
   MxPlan pl = plan_mx<F>(dev, M, N, K, sms > 0 ? sms : 1);
+  if (g_force_bn.load() == 224 || g_force_bn.load() == 256) pl.BN = g_force_bn.load();
+  if (g_force_s.load() >= 1 && g_force_s.load() <= 4 && (g_force_s.load() - 1) * ((K / BK + g_force_s.load() - 1) / g_force_s.load()) < K / BK)
+    pl.S = g_force_s.load();
+  // tall tiles (256 x 224, one CTA for two M tiles) without a K split, where
+  // they still give every SM a tile
+  const int ft = g_force_tall.load();
+  const int64_t tall_ctas = int64_t((N + 223) / 224) * ((M + 2 * BM - 1) / (2 * BM));
+  const bool tall = ft != 1 && pl.S == 1 && M > BM && (ft == 2 || tall_ctas >= int64_t(sms > 0 ? sms : 1));
+  const uint32_t wbox = tall ? 224u : uint32_t(pl.BN);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   if ((e = launch_quantize_e4m3_atoms(x, w8, w8 + a8_codes_bytes(M, K), M, K, st)) != cudaSuccess) return e;
   CUtensorMap mx8, mw;
   if (!make_map(enc, &mx8, CU_TENSOR_MAP_DATA_TYPE_UINT8, w8, K, M, K, BM)) return cudaErrorInvalidValue;
-  const bool ok = F == MXFP4
-                      ? make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, K, N, K / 2, uint32_t(pl.BN))
-                      : make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, N, K, uint32_t(pl.BN));
+  const bool ok = F == MXFP4 ? make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, K, N, K / 2, wbox)
+                             : make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, N, K, wbox);
   if (!ok) return cudaErrorInvalidValue;
   MxParams prm{};
   prm.wscales = static_cast<const uint8_t*>(scales);
@@ -773,6 +803,10 @@ static cudaError_t launch_a8(const void* codes, const void* scales, const void* 
   prm.kb_per = K / BK;
   prm.limit_ns = g_limit_ns.load();
   prm.drop_arrivals = g_drop.load();
+  if (tall) {
+    if ((e = set_smem<F, 224, false, true>(dev)) != cudaSuccess) return e;
+    return launch_tile<F, 224, false, true>(mx8, mx8, mw, prm, M, N, 1, st);
+  }
   if (pl.BN == 224) return launch_tile<F, 224, false>(mx8, mx8, mw, prm, M, N, pl.S, st);
   return launch_tile<F, 256, false>(mx8, mx8, mw, prm, M, N, pl.S, st);
 }
@@ -1269,6 +1303,7 @@ void set_mx_plan(int bn, int s) {
   mx::g_force_s.store(s);
 }
 void set_mx_drop_arrivals(int on) { mx::g_drop.store(on); }
+void set_mx_tall(int v) { mx::g_force_tall.store(v); }
 
 cudaError_t read_and_clear_mx_status(unsigned int* status) {
   cudaError_t e = cudaMemcpyFromSymbol(status, g_mx_status, sizeof(unsigned int));

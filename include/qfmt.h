@@ -429,8 +429,10 @@ int qfmt_device_status(void* stream);
  * that kernel's K split; key 7 with value 1 sends the batch decode GEMV
  * (3 <= M <= 16) to the K-split kernel; key 8 sets the order in which the
  * bf16-decode GEMM walks its tiles (0 its own choice, 1 N tiles first, 2 M
- * tiles first) -- all for measurements and tests.  Returns QFMT_EINVAL for
- * other keys and values.
+ * tiles first); key 9 sets the quantized-activation GEMM's 256-row tiles
+ * (0 its own plan, 1 never, 2 wherever the plan has no K split and M > 128)
+ * -- all for measurements and tests.  Returns QFMT_EINVAL for other keys and
+ * values.
  */
 int qfmt_debug_set(int key, int64_t value);
 

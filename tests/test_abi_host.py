@@ -303,11 +303,12 @@ def test_binding_rejects_bad_tensors_before_the_call(lib):
 def test_debug_keys_without_gpu(lib):
     # the test and measurement settings are host state: every documented key
     # takes its default value, unknown keys and values are refused
-    for key in range(1, 9):
+    for key in range(1, 10):
         q.qfmt_debug_set(key, 0)
-    for value in (1, 2, 0):
-        q.qfmt_debug_set(8, value)
-    for key, value in ((0, 0), (9, 0), (-1, 1), (8, 3), (8, -1)):
+    for key in (8, 9):
+        for value in (1, 2, 0):
+            q.qfmt_debug_set(key, value)
+    for key, value in ((0, 0), (10, 0), (-1, 1), (8, 3), (8, -1), (9, 3)):
         with pytest.raises(q.QfmtError) as e:
             q.qfmt_debug_set(key, value)
         assert e.value.status == -1

@@ -112,6 +112,65 @@ def test_qmm_a8_full_size_every_output(fmt, m, n, k):
           f"median {float(np.median(np.abs(o - exact) / qbound)):.4f}")
 
 
+@pytest.mark.parametrize("fmt", MXB)
+@pytest.mark.parametrize("m,n,k", [(300, 5000, 512), (1000, 700, 1024), (129, 2300, 256)])
+def test_qmm_a8_tall_tiles(fmt, m, n, k):
+    # 256-row tiles (two 128-row accumulators sharing each stage's W tile),
+    # forced on and off (debug key 9): the last tile's second M half lies
+    # wholly past M (m = 300), ends inside it (m = 1000) or holds one row
+    # (m = 129); against the oracle, and bit for bit against single tiles (the
+    # same accumulation order)
+    c, s, g = opack.pack(fmt, synth.weights(n, k, seed=m + 3))
+    xb = synth.activations_bf16(m, k, seed=m + 4)
+    xt = _dev(xb.view(np.int16)).view(torch.bfloat16)
+    dc, ds = _dev(c), _dev(s)
+    ref, bound = oref.qmm_a8_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    outs = []
+    try:
+        for tall in (2, 1):
+            q.qfmt_debug_set(9, tall)
+            q.qfmt_debug_set(4, 1)   # no K split: the tall form's condition
+            out = q.qmm_a8(fmt, dc, ds, xt, n)
+            assert q.qfmt_device_status() == 0
+            check_tensor(out, ref, bound, (fmt, m, n, k, tall))
+            outs.append(out.float().cpu().numpy())
+    finally:
+        q.qfmt_debug_set(9, 0)
+        q.qfmt_debug_set(4, 0)
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_qmm_a8_tall_expired_wait():
+    # the W-scale warp never signals (test hook) in a tall-tile launch: the
+    # bounded waits expire, the status word reports it, nothing is stored, and
+    # the next call is correct
+    fmt, m, n, k = "mxfp8_e4m3", 600, 2300, 512
+    c, s, g = opack.pack(fmt, synth.weights(n, k, seed=8))
+    xb = synth.activations_bf16(m, k, seed=9)
+    xt = _dev(xb.view(np.int16)).view(torch.bfloat16)
+    dc, ds = _dev(c), _dev(s)
+    assert q.qfmt_device_status() == 0
+    sentinel = torch.full((m, n), 3.0, dtype=torch.bfloat16, device=DEV)
+    q.qfmt_debug_set(9, 2)
+    q.qfmt_debug_set(1, 20_000_000)
+    q.qfmt_debug_set(2, 1)
+    try:
+        q.qmm_a8(fmt, dc, ds, xt, n, out=sentinel)
+        st = q.qfmt_device_status()
+    finally:
+        q.qfmt_debug_set(2, 0)
+        q.qfmt_debug_set(1, 0)
+    try:
+        assert st == -6
+        assert (sentinel.float() == 3.0).all()
+        out = q.qmm_a8(fmt, dc, ds, xt, n)
+        assert q.qfmt_device_status() == 0
+    finally:
+        q.qfmt_debug_set(9, 0)
+    ref, bound = oref.qmm_a8_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    check_tensor(out, ref, bound, (fmt, "after the expired wait"))
+
+
 def test_qmm_a8_workspace_and_errors():
     assert q.qmm_a8_workspace_bytes("mxfp8_e4m3", 300, 1024) >= 300 * 1024 + 384 * 1024 // 32
     assert q.qmm_a8_workspace_bytes("nvfp4", 300, 1024) == 0

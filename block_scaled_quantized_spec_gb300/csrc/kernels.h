@@ -58,7 +58,7 @@ cudaError_t launch_qgemm_mx(int fmt, const void* codes, const void* scales, cons
 // Decode GEMV on the same block-scaled MMA (M <= 16, K a multiple of 128 up to
 // 1024, mxfp4 codes 32-byte aligned): weights as stored, activations split in
 // the CTA; no workspace.
-bool qgemv_mx_supported(int fmt, int64_t M, int64_t N, int64_t K, const void* codes);
+bool qgemv_mx_supported(int fmt, int64_t M, int64_t N, int64_t K, const void* codes, int sms);
 // Expert-grouped rows on the block-scaled GEMM: a stacked [E N, K] MX weight,
 // row m against expert idx[m]; rows of one expert share the expert's tiles.
 size_t qgemm_grouped_workspace_bytes(int64_t M, int64_t K, int64_t E);
@@ -79,7 +79,7 @@ cudaError_t launch_quantize(int fmt, const void* x, bool x_f32, void* codes, voi
 cudaError_t launch_quantize_e4m3_atoms(const void* x, void* codes, void* atoms, int64_t M, int64_t K,
                                        cudaStream_t st);
 cudaError_t launch_qgemv_mx(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
-                            int64_t M, int64_t N, int64_t K, cudaStream_t st);
+                            int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms);
 void set_mx_wait_limit_ns(uint64_t ns);
 void set_mx_drop_arrivals(int on);
 void set_mx_plan(int bn, int s);   // measurement hook: force the tile width (224/256) and K split (1-4); 0 = planner

@@ -112,8 +112,8 @@ int qmm_ex(int fmt, const void* codes, const void* scales, float global_scale, c
   if (M <= 16) {
     // the MX formats the block-scaled MMA reads as stored: the tensor-core
     // decode GEMV (no ALU decode); the rest: the mma.sync decode GEMVs
-    if (qfmt_dev::qgemv_mx_supported(fmt, M, N, K, codes))
-      return cuda_status(qfmt_dev::launch_qgemv_mx(fmt, codes, scales, x, out, out_f32, M, N, K, s),
+    if (qfmt_dev::qgemv_mx_supported(fmt, M, N, K, codes, sms))
+      return cuda_status(qfmt_dev::launch_qgemv_mx(fmt, codes, scales, x, out, out_f32, M, N, K, s, sms),
                          "block-scaled qgemv launch");
     return cuda_status(qfmt_dev::launch_qgemv(fmt, codes, scales, global_scale, x, out, out_f32, M,
                                               weight_rows(fmt, N), K, s, sms),

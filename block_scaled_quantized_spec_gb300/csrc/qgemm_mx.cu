@@ -1158,23 +1158,34 @@ __global__ void __launch_bounds__(GV_THREADS) qgemv_mx_kernel(const __grid_const
 }
 
 // K split for the decode GEMV: one CTA per 128 rows up to K = 512, a pair of
-// CTAs up to K = 1024; 0 (the mma.sync decode GEMVs) beyond.  Measured against
-// those GEMVs (mxfp4 / mxfp8 E4M3, M = 1 and 8): 1.6-4x faster at K <= 1024;
-// at K = 4096 an 8-way split runs 6.5 us against 3.4 us (N = 4096): 256 CTAs of
-// two per SM leave most of a launch unable to start, and so to request its
-// weights, before the preceding launch ends, and the split's cluster reduction
-// adds ~2 us.
-inline int gemv_splits(int K) {
+// CTAs up to K = 1024; 0 (the mma.sync decode GEMVs) beyond, except for 3 to
+// 16 activation rows where a split into 512-column slabs gives a grid 1.5-2
+// CTAs deep on every SM (two fit an SM).  Measured against the CUDA-core
+// GEMVs (mxfp4 / mxfp8 E4M3, M = 1 and 8): 1.6-4x faster at K <= 1024.  At
+// K = 4096, M = 1, an 8-way split runs 6.5 us against 3.4 us (N = 4096): 256
+// CTAs of two per SM leave most of a launch unable to start, and so to
+// request its weights, before the preceding launch ends, and the split's
+// cluster reduction adds ~2 us; for M = 3-16 the same split at N = K = 4096
+// runs 0.73-0.84x the batch GEMV (mxfp4, mxfp8 E4M3 / E5M2), while at 128 or
+// 384 CTAs (N = 2048 or 6144, or K = 2048) it measured 0.91-1.26x.
+inline int gemv_plan(int M, int64_t N, int K, int sms) {
   if (K <= 0 || K % BK) return 0;
   const int slabs = K / BK;
+  const int fs = g_gemv_s.load();   // a forced split (measurements)
+  if (fs >= 1 && fs <= 8 && slabs % fs == 0 && slabs / fs <= GV_SLABS) return fs;
   if (slabs <= GV_SLABS) return 1;
   if (slabs <= 2 * GV_SLABS && slabs % 2 == 0) return 2;
+  if (M >= 3 && slabs % GV_SLABS == 0 && slabs / GV_SLABS <= 8) {
+    const int S = slabs / GV_SLABS;
+    const int64_t ctas = (N + GV_ROWS - 1) / GV_ROWS * S;
+    if (2 * ctas >= 3 * int64_t(sms) && ctas <= 2 * int64_t(sms)) return S;
+  }
   return 0;
 }
 
 template <int F, int NP>
 static cudaError_t launch_gemv_np(const void* codes, const void* scales, const void* x, void* out, bool out_f32, int M,
-                                  int N, int K, cudaStream_t st) {
+                                  int N, int K, cudaStream_t st, int sms) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   static std::atomic<int> done[64];
@@ -1186,9 +1197,7 @@ static cudaError_t launch_gemv_np(const void* codes, const void* scales, const v
     if (e != cudaSuccess) return e;
     done[dev].store(1);
   }
-  int S = gemv_splits(K);
-  const int fs = g_gemv_s.load();
-  if (fs >= 1 && fs <= 8 && (K / BK) % fs == 0 && (K / BK) / fs <= GV_SLABS) S = fs;
+  const int S = gemv_plan(M, N, K, sms);
   if (S == 0) return cudaErrorInvalidValue;
   CUtensorMap mw;
   const bool ok = F == MXFP4 ? make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, codes, K, N, K / 2, GV_ROWS)
@@ -1223,9 +1232,9 @@ static cudaError_t launch_gemv_np(const void* codes, const void* scales, const v
 
 template <int F>
 static cudaError_t launch_gemv(const void* codes, const void* scales, const void* x, void* out, bool out_f32, int M,
-                               int N, int K, cudaStream_t st) {
-  if (M <= 8) return launch_gemv_np<F, 16>(codes, scales, x, out, out_f32, M, N, K, st);
-  return launch_gemv_np<F, 32>(codes, scales, x, out, out_f32, M, N, K, st);
+                               int N, int K, cudaStream_t st, int sms) {
+  if (M <= 8) return launch_gemv_np<F, 16>(codes, scales, x, out, out_f32, M, N, K, st, sms);
+  return launch_gemv_np<F, 32>(codes, scales, x, out, out_f32, M, N, K, st, sms);
 }
 
 }  // namespace mx
@@ -1247,18 +1256,19 @@ cudaError_t launch_qgemm_mx(int fmt, const void* codes, const void* scales, cons
   }
 }
 
-bool qgemv_mx_supported(int fmt, int64_t M, int64_t N, int64_t K, const void* codes) {
-  return !mx::g_gemv_off.load() && (fmt == MXFP4 || fmt == MXFP8_E4M3 || fmt == MXFP8_E5M2) && M >= 1 && M <= 16 && N <= 65535LL * mx::GV_ROWS &&
-         mx::gemv_splits(int(K)) > 0 && !(fmt == MXFP4 && (reinterpret_cast<uintptr_t>(codes) & 31u));
+bool qgemv_mx_supported(int fmt, int64_t M, int64_t N, int64_t K, const void* codes, int sms) {
+  return !mx::g_gemv_off.load() && (fmt == MXFP4 || fmt == MXFP8_E4M3 || fmt == MXFP8_E5M2) && M >= 1 && M <= 16 &&
+         N <= 65535LL * mx::GV_ROWS && K <= (int64_t(1) << 20) && mx::gemv_plan(int(M), N, int(K), sms) > 0 &&
+         !(fmt == MXFP4 && (reinterpret_cast<uintptr_t>(codes) & 31u));
 }
 
 cudaError_t launch_qgemv_mx(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
-                            int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+                            int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms) {
   const int m = int(M), n = int(N), k = int(K);
   switch (fmt) {
-    case MXFP4: return mx::launch_gemv<MXFP4>(codes, scales, x, out, out_f32, m, n, k, st);
-    case MXFP8_E4M3: return mx::launch_gemv<MXFP8_E4M3>(codes, scales, x, out, out_f32, m, n, k, st);
-    case MXFP8_E5M2: return mx::launch_gemv<MXFP8_E5M2>(codes, scales, x, out, out_f32, m, n, k, st);
+    case MXFP4: return mx::launch_gemv<MXFP4>(codes, scales, x, out, out_f32, m, n, k, st, sms);
+    case MXFP8_E4M3: return mx::launch_gemv<MXFP8_E4M3>(codes, scales, x, out, out_f32, m, n, k, st, sms);
+    case MXFP8_E5M2: return mx::launch_gemv<MXFP8_E5M2>(codes, scales, x, out, out_f32, m, n, k, st, sms);
     default: return cudaErrorInvalidValue;
   }
 }

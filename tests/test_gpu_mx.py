@@ -232,6 +232,29 @@ def test_tensor_core_decode_gemv(fmt, m, k):
 
 
 @pytest.mark.parametrize("fmt", MXB)
+@pytest.mark.parametrize("m,n,k", [(3, 4096, 4096), (9, 4000, 4096), (16, 4096, 3072)])
+def test_tensor_core_decode_gemv_long_k(fmt, m, n, k):
+    # 3-16 activation rows at long K: the tensor-core decode GEMV split into
+    # 512-column slabs (8 and 6 CTAs a cluster) where that grid lands 1.5-2
+    # CTAs on every SM (N = 4000 ends inside a tile); against the oracle at
+    # every output and against the CUDA-core batch GEMV (hook 5)
+    c, s, g = opack.pack(fmt, synth.weights(n, k, seed=m + 11))
+    xb, xt = _x(m, k, seed=m + 12)
+    dc, ds = _dev(c), _dev(s)
+    out = q.qmm(fmt, dc, ds, g, xt, n)
+    assert q.qfmt_device_status() == 0
+    ref, bound = oref.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    check_tensor(out, ref, bound, (fmt, m, n, k))
+    q.qfmt_debug_set(5, 1)
+    try:
+        other = q.qmm(fmt, dc, ds, g, xt, n).float().cpu().numpy()
+    finally:
+        q.qfmt_debug_set(5, 0)
+    a = out.float().cpu().numpy()
+    assert (np.abs(a - other) <= 2 * bound + bf16_half_ulp(a) + bf16_half_ulp(other)).all()
+
+
+@pytest.mark.parametrize("fmt", MXB)
 @pytest.mark.parametrize("m,n,k", [(130, 300, 128), (300, 520, 384), (2000, 2300, 640), (1200, 4100, 1152)])
 def test_stage_ring_wraps(fmt, m, n, k):
     # three stages: 1, 3, 5 and 9 K steps leave the stage ring at every

@@ -270,16 +270,6 @@ __device__ __forceinline__ void int4x8_affine_bf16(uint32_t w, uint32_t s2, uint
   }
 }
 
-// 8 unsigned 4-bit q -> bf16x2 {128+q0,128+q4} {128+q1,128+q5} {128+q2,128+q6}
-// {128+q3,128+q7}: exact, one logic op per pair (0x4300 | q is bf16 128 + q).
-// Callers remove the 128 offset in float32 with the block's activation sum.
-__device__ __forceinline__ void int4x8_biased_bf16(uint32_t w, uint32_t r[4]) {
-  r[0] = (w & 0x000F000Fu) | 0x43004300u;
-  r[1] = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
-  r[2] = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
-  r[3] = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
-}
-
 // 4 E4M3 codes (code i in byte i) -> bf16x2 {c0,c2} {c1,c3} holding the
 // value times 2^-120: the 7 magnitude bits land in the low exponent and the
 // top mantissa bits of a bf16, which represents every E4M3 value (subnormals

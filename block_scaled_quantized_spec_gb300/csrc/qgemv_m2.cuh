@@ -256,6 +256,7 @@ __global__ void __launch_bounds__(32 * W, W == 4 ? 3 : 2) qgemv_m2_kernel(const 
                                                            const uint8_t* __restrict__ scales, float glob,
                                                            const uint16_t* __restrict__ x, void* __restrict__ out,
                                                            int out_f32, int M, int N, int K, const Extra ex) {
+  (void)glob;   // nvfp4's global scale; the other formats have none
   using S = Shape<F>;
   constexpr bool STG = (MODE & STAGE) != 0;
   constexpr int P = STG ? 2 : chunks_per_warp<F, W>();

@@ -55,13 +55,14 @@ Value definitions (page title, then the section):
   + eps), silu(z) = z sigmoid(z) -- PR #250, the fused gated-RMSNorm + GEMV
   commit (a silu gate times the per-row inverse RMS times the norm weight,
   staged, then the block-scaled GEMV over it); the RMS is of x alone.
-* quantize_activations / qmm_a8_ref: both operands quantized (rlx-cpu
+* quantize_activations / qmm_a8_ref / qmm_a4_ref: both operands quantized (rlx-cpu
   ``thunk/ops/quant.rs``: ``lowp_compute_scales`` / ``lowp_snap_scale`` /
   ``lowp_quantize`` applied to the activation, then ``lowp_scaled_matmul``,
   acc += (a_s * b_s) * sum_k dec(a) dec(b)): the activation is packed exactly
   as a weight of that format (amax / max_finite in float32, E8M0 snapped up,
   round-to-nearest-even saturating codes) and the product of the two exact
-  dequantized operands is taken in float64.
+  dequantized operands is taken in float64.  qmm_a8_ref packs the activation
+  as MXFP8 E4M3, qmm_a4_ref as MXFP4 (E2M1 elements: the all-FP4 product).
 * qmm_gather: expert-routed rows over one stacked [E * N, K] weight, row m
   against rows [e N, e N + N) with e = expert_idx[m] -- PR #250, the MoE
   gather-qmm commit (weight row expert_ids[m] * out_dim + n, one stacked
@@ -279,13 +280,25 @@ def quantize_activations(fmt, x, x_dtype, m, k):
     return c, s
 
 
+def _qmm_quantized_x_ref(act_fmt, fmt, codes, scales, global_scale, x, x_dtype, m, n, k):
+    xc, xs = quantize_activations(act_fmt, x, x_dtype, m, k)
+    xq = dequant_exact(act_fmt, xc, xs, 1.0, m, k)
+    w = dequant_exact(fmt, codes, scales, global_scale, n, k)
+    return xq @ w.T, A8_REL * (np.abs(xq) @ np.abs(w).T) + BOUND_ABS
+
+
 def qmm_a8_ref(fmt, codes, scales, global_scale, x, x_dtype, m, n, k):
     """(ref, bound) of the both-operands-quantized product: X8 . dequant(W)^T, X8 the MXFP8 E4M3 activation.
 
     ref is exact in float64; the bound is the float32 accumulation's,
     A8_REL * sum_k |x8||w| + BOUND_ABS.
     """
-    xc, xs = quantize_activations("mxfp8_e4m3", x, x_dtype, m, k)
-    x8 = dequant_exact("mxfp8_e4m3", xc, xs, 1.0, m, k)
-    w = dequant_exact(fmt, codes, scales, global_scale, n, k)
-    return x8 @ w.T, A8_REL * (np.abs(x8) @ np.abs(w).T) + BOUND_ABS
+    return _qmm_quantized_x_ref("mxfp8_e4m3", fmt, codes, scales, global_scale, x, x_dtype, m, n, k)
+
+
+def qmm_a4_ref(fmt, codes, scales, global_scale, x, x_dtype, m, n, k):
+    """(ref, bound) of X4 . dequant(W)^T, X4 the activation packed as MXFP4 (E2M1, E8M0 scale per 32).
+
+    The same float32-accumulation bound as qmm_a8_ref: A8_REL * sum_k |x4||w| + BOUND_ABS.
+    """
+    return _qmm_quantized_x_ref("mxfp4", fmt, codes, scales, global_scale, x, x_dtype, m, n, k)

@@ -686,3 +686,119 @@ def test_planted_activation_quantizer_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(codec, "e8m0_encode_ceil", floor_snap)
     with pytest.raises(AssertionError):
         test_a8_is_the_exact_product_when_x_is_representable("mxfp4")
+
+
+# ------------------- both operands quantized: the all-FP4 W . A4 product -------------
+
+
+def _brute_e2m1(v: Fraction) -> int:
+    # nearest E2M1 value (the two_m_int decode above), an exact tie to the code
+    # with mantissa bit 0, beyond +-6 the largest; the sign bit copies v's sign
+    best = None
+    for c in range(16):
+        if (c & 8) != (8 if v < 0 else 0):
+            continue
+        key = (abs(_lib_elem("mxfp4", c) - v), c & 1)
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1]
+
+
+def _brute_activation_quant_e2m1(xrow):
+    # per block of 32: s = float32(amax / 6) (1 for a zero block), e = the
+    # smallest integer with 2^e >= s, codes of float32(x / 2^e)
+    codes, scodes = [], []
+    for b in range(0, len(xrow), 32):
+        blk = np.asarray(xrow[b:b + 32], np.float32)
+        amax = np.float32(np.max(np.abs(blk)))
+        s = Fraction(float(np.float32(amax / np.float32(6.0)))) if amax > 0 else Fraction(1)
+        e = -127
+        while Fraction(2) ** e < s:
+            e += 1
+        scodes.append(e + 127)
+        for v in blk:
+            codes.append(_brute_e2m1(Fraction(float(np.float32(v) / np.float32(2.0 ** e)))))
+    return codes, scodes
+
+
+def _a4_activations(m, k, seed):
+    # N(0, 1) values, then in every row's first block the grid's midpoints
+    # (0.25, 1.25, 1.75, 2.5, 3.5, 5, of either sign) under a block maximum of 6
+    # times a power of two, so that the ties are exact
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((m, k)).astype(np.float32)
+    mids = np.array([6.0, 0.25, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -2.5, -5.0, -1.75, 0.75], np.float32)
+    for i in range(m):
+        x[i, :len(mids)] = mids * np.float32(2.0 ** (i - 1))
+    return synth.f32_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8_e4m3"])
+def test_a4_product_matches_exact_rational_brute_force(fmt):
+    m, n, k = 2, 3, 64
+    cw, sw, g = _tiny_case(fmt, m=m, n=n, k=k, seed=11)[:3]
+    xb = _a4_activations(m, k, seed=12)
+    ref, bound = reference.qmm_a4_ref(fmt, cw, sw, g, xb, "bf16", m, n, k)
+    xv = reference.x_values(xb, "bf16").reshape(m, k)
+    for i in range(m):
+        xc, xs = _brute_activation_quant_e2m1(xv[i])
+        x4 = [_lib_elem("mxfp4", xc[kk]) * Fraction(2) ** (xs[kk // 32] - 127) for kk in range(k)]
+        for j in range(n):
+            exact = sum(x4[kk] * _lib_elem(fmt, _code(fmt, cw[j], kk)) * _lib_scale(fmt, sw, j, kk // 32)[0]
+                        for kk in range(k))
+            assert ref[i, j] == float(exact), (fmt, i, j)
+            assert bound[i, j] > 0
+
+
+def _e2m1_representable_activations(m, k, seed):
+    # every block: E2M1 values times one power of two, its largest magnitude
+    # in (3, 6], so the packer's scale is that power and the codes its values
+    rng = np.random.default_rng(seed)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    x = np.empty((m, k), np.float32)
+    for i in range(m):
+        for b in range(0, k, 32):
+            e = int(rng.integers(-20, 20))
+            v = rng.choice(grid, 32) * rng.choice([-1.0, 1.0], 32)
+            v[int(rng.integers(0, 32))] = rng.choice([4.0, 6.0, -4.0, -6.0])
+            x[i, b:b + 32] = (v * 2.0 ** e).astype(np.float32)
+    return synth.f32_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8_e4m3", "nvfp4", "int4_affine"])
+def test_a4_is_the_exact_product_when_x_is_representable(fmt):
+    # quantizing an activation that is already MXFP4 changes nothing: the
+    # W . A4 reference equals the exact bf16-activation reference bit for bit
+    m, n, k = 3, 7, 128
+    xb = _e2m1_representable_activations(m, k, seed=13)
+    c, s, g = pack.pack(fmt, synth.weights(n, k, seed=14, outliers=(fmt == "nvfp4")))
+    a4, _ = reference.qmm_a4_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    exact, _ = reference.qmm_ref(fmt, c, s, g, xb, "bf16", m, n, k)
+    assert np.array_equal(a4, exact)
+
+
+def test_planted_e2m1_tie_mistake_is_caught(monkeypatch):
+    # ties rounded away from zero instead of to the even code (every input
+    # nudged one float32 ulp outward): the brute force over the grid's
+    # midpoints catches it
+    from oracle import codec
+    real = codec.encode_rne_sat
+
+    def away(v, fmt):
+        if fmt != "e2m1":
+            return real(v, fmt)
+        v = np.asarray(v, np.float32)
+        return real(np.nextafter(v, np.sign(v) * np.float32(np.inf)).astype(np.float32), fmt)
+
+    monkeypatch.setattr(codec, "encode_rne_sat", away)
+    with pytest.raises(AssertionError):
+        test_a4_product_matches_exact_rational_brute_force("mxfp4")
+
+
+def test_planted_a4_scale_divisor_mistake_is_caught(monkeypatch):
+    # the MXFP4 scale taken from amax / 448 (E4M3's largest) instead of amax / 6:
+    # the block maxima saturate and the representable-activation identity fails
+    from oracle import pack as opack
+    monkeypatch.setitem(opack._ELEM, "mxfp4", ("e2m1", 448.0))
+    with pytest.raises(AssertionError):
+        test_a4_is_the_exact_product_when_x_is_representable("mxfp4")

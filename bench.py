@@ -46,7 +46,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-breakdown", action="store_true")
-    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K[:A|:A8], gather:fmt:M:N:K:E, batched:fmt:M:N1,N2:K, "
+    p.add_argument("--only", default=None, help="run one breakdown row: fmt:M:N:K[:A|:A8|:A4], gather:fmt:M:N:K:E, batched:fmt:M:N1,N2:K, "
                    "rmsnorm:fmt:M:N:K, gated_rmsnorm:fmt:M:N:K or dequant:fmt:N:K:f32|bf16")
     return p.parse_args()
 
@@ -166,7 +166,8 @@ class Problem:
     tensor-core GEMM of the MX formats, M > 16), the call a user makes with
     one; "A": no workspace (the bf16-decode GEMM); "A8": both operands
     quantized (qmm_a8: the activations packed to MXFP8 E4M3, one
-    block-scaled MMA per block).
+    block-scaled MMA per block); "A4": the all-FP4 product (qmm_a4: the
+    activations packed to MXFP4, kind::mxf4).
     """
 
     def __init__(self, fmt, m, n, k, copies, seed=0, path="auto"):
@@ -193,17 +194,26 @@ class Problem:
         self.bytes = sizes(fmt, m, n, k)
         self.flops = 2.0 * m * n * k
         self.a8 = path == "A8"
-        wsb = q.qmm_a8_workspace_bytes(fmt, m, k) if self.a8 else (q.qmm_workspace_bytes(fmt, m, k) if path == "auto" else 0)
+        self.a4 = path == "A4"
+        if self.a8:
+            wsb = q.qmm_a8_workspace_bytes(fmt, m, k)
+        elif self.a4:
+            wsb = q.qmm_a4_workspace_bytes(fmt, m, k)
+        else:
+            wsb = q.qmm_workspace_bytes(fmt, m, k) if path == "auto" else 0
         # one workspace serves every layer: each call's activation split waits
         # for the previous call to finish before it writes
         self.ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
-        self.path = "A8" if self.a8 else ("SUB" if fmt in q.SUB_BYTE else ("B" if wsb else ("A" if m > 16 else "GEMV")))
+        self.path = ("A8" if self.a8 else "A4" if self.a4 else
+                     ("SUB" if fmt in q.SUB_BYTE else ("B" if wsb else ("A" if m > 16 else "GEMV"))))
 
     def step(self):
         import block_scaled_quantized_spec_gb300 as q
         for i in range(self.copies):
             if self.a8:
                 q.qmm_a8(self.fmt, self.codes[i], self.scales[i], self.x[i], self.n, out=self.out[i], workspace=self.ws)
+            elif self.a4:
+                q.qmm_a4(self.fmt, self.codes[i], self.scales[i], self.x[i], self.n, out=self.out[i], workspace=self.ws)
             elif self.ws is not None:
                 q.qmm_ex(self.fmt, self.codes[i], self.scales[i], self.g, self.x[i], self.n, out=self.out[i],
                          workspace=self.ws)
@@ -456,6 +466,8 @@ BREAKDOWN = [
     # both operands quantized (W . A8)
     ("mxfp8_e4m3", 2048, 4096, 4096, "A8"), ("mxfp4", 2048, 4096, 4096, "A8"),
     ("mxfp8_e5m2", 4096, 11008, 4096, "A8"),
+    # the all-FP4 product (W . A4)
+    ("mxfp4", 2048, 4096, 4096, "A4"), ("mxfp4", 4096, 11008, 4096, "A4"),
     # the 2/3/5/6-bit bit streams
     ("int3", 1, 11008, 4096), ("mxint5", 16, 4096, 4096),
     # batch decode rows on [4096, 4096] (one decode per weight block for every activation row)
@@ -695,6 +707,7 @@ def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3, path="auto"
     row = {"fmt": fmt, "M": m, "N": n, "K": k, "us": round(per * 1e3, 2), "copies": copies,
            "path": {"B": "block-scaled tcgen05 GEMM (X split + kind::mxf8f6f4)", "A": "bf16-decode tcgen05 GEMM",
                     "A8": "both operands quantized (X to MXFP8 E4M3, one kind::mxf8f6f4 MMA per block)",
+                    "A4": "all-FP4 (X to MXFP4, one kind::mxf4 MMA per 64 K)",
                     "GEMV": "decode GEMV", "SUB": "CUDA-core sub-byte kernel"}[prob.path]}
     gbs = nbytes / (per * 1e-3) / 1e9
     tfl = prob.flops / (per * 1e-3) / 1e12
@@ -708,6 +721,8 @@ def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3, path="auto"
                    "mxfp4x2": bf16, "mxint4": bf16, "fp8_e4m3": 2 * bf16, "fp8_e5m2": 2 * bf16}.get(fmt, 6 * bf16)
         if prob.path == "A8":   # FP8 operands on both sides: the FP8 rate
             fp_peak = 2 * bf16
+        if prob.path == "A4":   # FP4 operands on both sides: the FP4 rate
+            fp_peak = 6 * bf16
         row["bf16_frac"] = round(tfl / bf16, 4)
         row["native_peak_frac"] = round(tfl / fp_peak, 4)
         # against the roofline at this arithmetic intensity: min(bf16 peak, FLOP/byte x HBM)

@@ -20,8 +20,8 @@ __all__ = [
     "FORMATS", "QfmtError", "load", "lib_path",
     "qfmt_block_size", "qfmt_codes_bytes", "qfmt_scales_bytes",
     "qfmt_pack", "qfmt_dequant", "qmm", "qmm_ex", "qmm_workspace_bytes", "qmm_gather", "qmm_batched", "qmm_rmsnorm",
-    "qmm_gated_rmsnorm", "qmm_noalloc", "qfmt_quantize", "qmm_a8", "qmm_a8_workspace_bytes", "qmm_grouped",
-    "qmm_grouped_workspace_bytes",
+    "qmm_gated_rmsnorm", "qmm_noalloc", "qfmt_quantize", "qmm_a8", "qmm_a8_workspace_bytes", "qmm_a4",
+    "qmm_a4_workspace_bytes", "qmm_grouped", "qmm_grouped_workspace_bytes",
     "qfmt_last_error",
     "qfmt_version", "qfmt_device_status", "qfmt_debug_set",
 ]
@@ -77,6 +77,10 @@ _SIGS = {
                               ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                               ctypes.c_size_t, ctypes.c_void_p]),
     "qmm_a8_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
+    "qmm_a4": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                              ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                              ctypes.c_size_t, ctypes.c_void_p]),
+    "qmm_a4_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
     "qmm_grouped": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -351,10 +355,22 @@ def qmm_a8_workspace_bytes(fmt, M: int, K: int) -> int:
     return load().qmm_a8_workspace_bytes(_fmt(fmt), M, K)
 
 
+def qmm_a4_workspace_bytes(fmt, M: int, K: int) -> int:
+    return load().qmm_a4_workspace_bytes(_fmt(fmt), M, K)
+
+
 def qmm_a8(fmt, codes, scales, x, N: int, out=None, out_dtype=None, workspace=None, stream=None):
     """out [M, N] = Q(x) . dequant(W)^T, Q(x) the activation packed to MXFP8 E4M3 (both operands quantized)."""
+    return _qmm_quantized_x("qmm_a8", fmt, codes, scales, x, N, out, out_dtype, workspace, stream)
+
+
+def qmm_a4(fmt, codes, scales, x, N: int, out=None, out_dtype=None, workspace=None, stream=None):
+    """out [M, N] = Q4(x) . dequant(W)^T, Q4(x) the activation packed to MXFP4 (the all-FP4 product; mxfp4 W)."""
+    return _qmm_quantized_x("qmm_a4", fmt, codes, scales, x, N, out, out_dtype, workspace, stream)
+
+
+def _qmm_quantized_x(where, fmt, codes, scales, x, N, out, out_dtype, workspace, stream):
     import torch
-    where = "qmm_a8"
     M, K = _activations(where, x)
     _weights(where, fmt, codes, scales, N, K, 0)
     if out is None:
@@ -362,13 +378,15 @@ def qmm_a8(fmt, codes, scales, x, N: int, out=None, out_dtype=None, workspace=No
     if out.dtype not in (torch.float32, torch.bfloat16):
         _fail(where, f"out must be float32 or bfloat16 (is {out.dtype})")
     _tensor(out, where, "out", shape=(M, N))
+    lib = load()
+    wsb = getattr(lib, where + "_workspace_bytes")
     if workspace is None:
-        workspace = torch.empty(max(1, qmm_a8_workspace_bytes(fmt, M, K)), dtype=torch.uint8, device=x.device)
+        workspace = torch.empty(max(1, wsb(_fmt(fmt), M, K)), dtype=torch.uint8, device=x.device)
     _tensor(workspace, where, "workspace")
     _on_device(where, x=x, codes=codes, scales=scales, out=out, workspace=workspace)
-    _check(load().qmm_a8(_fmt(fmt), _ptr(codes), _ptr(scales), _ptr(x), _ptr(out),
-                         F32 if out.dtype == torch.float32 else BF16, M, N, K, _ptr(workspace),
-                         workspace.numel() * workspace.element_size(), _stream(stream)), where)
+    _check(getattr(lib, where)(_fmt(fmt), _ptr(codes), _ptr(scales), _ptr(x), _ptr(out),
+                               F32 if out.dtype == torch.float32 else BF16, M, N, K, _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream)), where)
     return out
 
 

@@ -28,13 +28,22 @@
 //              unit's low 8 bytes, the layout kind::mxf8f6f4 reads for E2M1)
 //              and bulk-copies the two X scale atoms; it owns the TMEM
 //              allocation;
-//      warp 1  one thread copies the stage's scale atoms into tensor memory
-//              (tcgen05.cp .32x128b.warpx4) and issues, per K block of 32,
-//              two MMAs into one accumulator: hi . W under (s1, s_w) and
-//              lo . W under (s2, s_w);
+//      warp 1  walks the stages as a warp (lane 0 waits on the barriers and
+//              broadcasts the outcome, so the stage addresses stay
+//              warp-uniform); one elected lane copies the stage's scale
+//              atoms into tensor memory (tcgen05.cp .32x128b.warpx4) and
+//              issues, per K block of 32, two MMAs into one accumulator:
+//              hi . W under (s1, s_w) and lo . W under (s2, s_w).  Issued
+//              from a single lane's branch, each tcgen05 instruction cost
+//              ~67 cycles of the issuing thread; from the converged warp ~50;
 //      warp 2  gathers the stage's W scales (one 32-bit word = 4 K blocks per
 //              row) into two scale atoms in shared memory;
 //      warps 4-7 drain the accumulator (tcgen05.ld) and store bf16/float32.
+//
+// The same kernel serves the quantized-activation products: one E4M3 term
+// (W . A8, kind::mxf8f6f4), and the all-FP4 product (W . A4: X packed to
+// MXFP4, both operands E2M1 two codes to a byte, kind::mxf4 with two scales
+// per row and instruction), each optionally on tall 256-row tiles.
 //
 // Every mbarrier wait is bounded; on expiry the kernel records it in the
 // device status word, lets issued copies and MMAs land, frees its tensor
@@ -65,7 +74,9 @@ constexpr int B_BYTES = BN_MAX * BK;          // 32 KiB: up to 256 rows of 128 c
 constexpr int SF_BYTES = 512;                 // one scale atom: 128 rows x 4 K blocks
 constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
 constexpr int SF_STAGE = 4 * SF_BYTES;        // hi atom, lo atom, two W atoms (rows 0-127, 128-255)
+constexpr int SF_STAGE_A4 = 8 * SF_BYTES;     // all-FP4 form: two K atoms each of two X tiles and two W row groups
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGES * SF_STAGE + 256;
+constexpr int SMEM_BYTES_A4 = 1024 + STAGES * STAGE_BYTES + STAGES * SF_STAGE_A4 + 256;
 constexpr int THREADS = 256;
 constexpr int TMEM_COLS = 512;                // accumulator 256 columns + 16 scale columns a stage
 constexpr int SF_COL0 = 256;
@@ -240,6 +251,18 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// Both operands E2M1 packed two codes to a byte, K 64 an instruction, two
+// E8M0 scales of each row (the scale cell's bytes from the descriptor's id).
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
 struct MxParams {
   const uint8_t* wscales;   // [N, K/32] E8M0 (grouped: [E N, K/32])
   const uint8_t* sf_hi;     // X scale atoms (workspace)
@@ -270,26 +293,40 @@ template <int F> constexpr uint32_t b_type() {
 // memory the lo term uses otherwise: 60 KiB land per K step for twice the
 // output of a 44 KiB single-tile step.  Tensor memory: accumulators at
 // columns 0 and 256, the stages' scale slots at 224, 240 and 480.
+// A4 (one term, mxfp4 weights): the all-FP4 product.  The activation tile is
+// E2M1 packed two to a byte like the weights, and both enter kind::mxf4 as
+// stored: a stage's 128-byte rows hold 256 codes (K 64 an instruction), so it
+// carries twice the K of an 8-bit stage in the same bytes, with two K atoms
+// of scales per tile.  Tensor memory: 32 scale columns a stage slot (X tile 0
+// at +0 / +4, tile 1 at +8 / +12, W at +16 .. +31: rows 0-127 and 128-255 of
+// K atom 0, then of K atom 1); with tall tiles only two slots fit (columns
+// 224 and 480) and a slot is refilled once the MMAs of the stage before last
+// have completed.
 // A K split runs its splits as a cluster along z; each split's float32
 // partial tile goes to its drained stage memory and the cluster sums them
 // through distributed shared memory in rank order.
-template <int F, int BN, bool TWO = true, bool TALL = false>
+template <int F, int BN, bool TWO = true, bool TALL = false, bool A4 = false>
 __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_constant__ CUtensorMap xhi_map,
                                                               const __grid_constant__ CUtensorMap xlo_map,
                                                               const __grid_constant__ CUtensorMap w_map,
                                                               const MxParams p) {
   static_assert(BN % 32 == 0 && BN <= BN_MAX && BN > 128, "two W scale atoms a stage");
   static_assert(!TALL || (!TWO && BN == 224), "tall tiles: one term, 224 columns");
+  static_assert(!A4 || (!TWO && F == MXFP4), "the all-FP4 form: one E2M1 activation term, mxfp4 weights");
   // bytes a stage's copies deliver: the two X tiles (terms, or M halves), the
-  // W codes (E2M1: the 8 data bytes of every 16-byte unit, the gaps are not
-  // written) and the two X scale atoms
+  // W codes (E2M1 through 16U4_ALIGN16B: the 8 data bytes of every 16-byte
+  // unit, the gaps are not written; packed A4 tiles: every byte) and the X
+  // scale atoms (A4: two K atoms a tile)
   constexpr int TERMS = (TWO || TALL) ? 2 : 1;
-  constexpr uint32_t TX_BYTES = TERMS * (A_BYTES + SF_BYTES) + (F == MXFP4 ? BN * BK / 2 : BN * BK);
+  constexpr int XA = A4 ? 2 : 1;
+  constexpr int SFS = A4 ? SF_STAGE_A4 : SF_STAGE;
+  constexpr uint32_t TX_BYTES =
+      TERMS * (A_BYTES + XA * SF_BYTES) + ((F == MXFP4 && !A4) ? BN * BK / 2 : BN * BK);
   constexpr int PSTRIDE = BN + 4;                 // floats per partial-tile row (K split)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sf_area = smem + STAGES * STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_area + STAGES * SF_STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_area + STAGES * SFS);
   // bars[0..S): stage copies landed (TMA and bulk bytes), [S..2S): stage W scales written (the scale warp),
   // [2S..3S): stage empty (MMA commit), [3S]: accumulator done
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 3 * STAGES + 1);
@@ -308,7 +345,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     while (e + 1 < p.E && __ldg(p.route_off + e + 1) <= m0) ++e;
     wrow0 = e * p.N;
   }
-  const int nk = p.K / BK;
+  const int nk = p.K / (A4 ? 2 * BK : BK);        // K steps (A4: 256 codes in a 128-byte row)
+  const int katoms = p.K / BK;                      // scale atoms (4 K blocks) along a row
   const int j0 = blockIdx.z * p.kb_per, j1 = min(nk, j0 + p.kb_per);   // this split's K steps
   const int nloc = j1 - j0;
   const bool split_k = gridDim.z > 1;
@@ -320,7 +358,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
   auto a_hi = [&](int s) { return sbase + uint32_t(s * STAGE_BYTES); };
   auto a_lo = [&](int s) { return sbase + uint32_t(s * STAGE_BYTES + A_BYTES); };
   auto b_tile = [&](int s) { return sbase + uint32_t(s * STAGE_BYTES + 2 * A_BYTES); };
-  auto sf_s = [&](int s, int i) { return sfbase + uint32_t(s * SF_STAGE + i * SF_BYTES); };   // i: 0 hi, 1 lo, 2-3 W
+  // i: 0 hi, 1 lo, 2-3 W (A4: 0-1 X tile 0, 2-3 X tile 1, 4-7 W; two K atoms each)
+  auto sf_s = [&](int s, int i) { return sfbase + uint32_t(s * SFS + i * SF_BYTES); };
   auto fail = [&]() {
     *abort_flag = 1u;
     atomicOr(&g_mx_status, 1u);
@@ -359,9 +398,9 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
       // past M has none (its rows are zeros and stored nowhere): the first
       // half's atoms stand in
       const size_t mt0 = TALL ? size_t(2 * blockIdx.y) : size_t(blockIdx.y);
-      const uint8_t* sfh = p.sf_hi + mt0 * size_t(nk) * SF_BYTES;
-      const uint8_t* sfl = TALL ? (m0 + BM < p.M ? sfh + size_t(nk) * SF_BYTES : sfh)
-                                : p.sf_lo + size_t(blockIdx.y) * size_t(nk) * SF_BYTES;
+      const uint8_t* sfh = p.sf_hi + mt0 * size_t(katoms) * SF_BYTES;
+      const uint8_t* sfl = TALL ? (m0 + BM < p.M ? sfh + size_t(katoms) * SF_BYTES : sfh)
+                                : p.sf_lo + size_t(blockIdx.y) * size_t(katoms) * SF_BYTES;
       int issued = 0;
       for (int i = 0; i < nloc; ++i) {
         const int s = i % STAGES, j = j0 + i;
@@ -373,8 +412,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         if constexpr (TWO) tma_load_2d(a_lo(s), &xlo_map, j * BK, m0, full(s));
         if constexpr (TALL) tma_load_2d(a_lo(s), &xhi_map, j * BK, m0 + BM, full(s));   // the second M half
         tma_load_2d(b_tile(s), &w_map, j * BK, wrow0 + n0, full(s));
-        bulk_load(sf_s(s, 0), sfh + size_t(j) * SF_BYTES, SF_BYTES, full(s));
-        if constexpr (TWO || TALL) bulk_load(sf_s(s, 1), sfl + size_t(j) * SF_BYTES, SF_BYTES, full(s));
+        bulk_load(sf_s(s, 0), sfh + size_t(j) * XA * SF_BYTES, XA * SF_BYTES, full(s));
+        if constexpr (TWO || TALL) bulk_load(sf_s(s, XA), sfl + size_t(j) * XA * SF_BYTES, XA * SF_BYTES, full(s));
         issued = i + 1;
       }
       // every issued copy lands before the CTA may exit
@@ -383,47 +422,94 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t BT = b_type<F>();
-      for (int i = 0; i < nloc; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
-        if (*abort_flag) break;
-        if (!mbar_wait(full(s), ph, p.limit_ns) || !mbar_wait(sf_full(s), ph, p.limit_ns)) { fail(); break; }
-        tc_fence_after();
-        // hi (first M half): +0, lo (second M half): +4, W: +8 (rows 0-127), +12 (128-255)
-        const uint32_t sfc = tmem + uint32_t(TALL ? (s < 2 ? 224 + 16 * s : 480) : SF_COL0 + 16 * s);
-        tmem_cp_sf(sfc + 0, umma::smem_desc_sf32x16(sf_s(s, 0)));
-        if constexpr (TWO || TALL) tmem_cp_sf(sfc + 4, umma::smem_desc_sf32x16(sf_s(s, 1)));
-        tmem_cp_sf(sfc + 8, umma::smem_desc_sf32x16(sf_s(s, 2)));
-        tmem_cp_sf(sfc + 12, umma::smem_desc_sf32x16(sf_s(s, 3)));
-        const uint64_t dh = desc_sw128(a_hi(s)), dl = desc_sw128(a_lo(s)), db = desc_sw128(b_tile(s));
-        #pragma unroll
-        for (int kk = 0; kk < BK / 32; ++kk) {   // +32 bytes along K per instruction
-          const uint32_t id = umma::idesc_mxf8f6f4(umma::F8F6F4_E4M3, BT, BM, BN, uint32_t(kk), uint32_t(kk));
-          mma_mx(tmem, dh + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 0, sfc + 8, (i | kk) != 0);
-          if constexpr (TWO) mma_mx(tmem, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 4, sfc + 8, 1u);
-          if constexpr (TALL)
-            mma_mx(tmem + 256u, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 4, sfc + 8, (i | kk) != 0);
+    // The warp walks the loop together (lane 0 waits, the outcome is
+    // broadcast), so the stage addresses are warp-uniform; one elected lane
+    // issues the tensor-core instructions.
+    const bool leader = elect_one();
+    constexpr uint32_t BT = b_type<F>();
+    // scale slots in tensor memory: one a stage, but two for A4 tall tiles
+    constexpr int SLOTS = (A4 && TALL) ? 2 : STAGES;
+    for (int i = 0; i < nloc; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
+      int go = 1;
+      if (lane == 0) {
+        go = *abort_flag == 0u;
+        if (go && !(mbar_wait(full(s), ph, p.limit_ns) && mbar_wait(sf_full(s), ph, p.limit_ns))) {
+          fail();
+          go = 0;
+        }
+        if constexpr (SLOTS < STAGES) {
+          // the slot's previous user, step i - SLOTS: its MMAs (which read the
+          // slot) complete before the slot is copied over.  Its commit is the
+          // newest phase of that stage's empty barrier this thread has issued.
+          if (go && i >= SLOTS) {
+            const int pi = i - SLOTS;
+            if (!mbar_wait(empty(pi % STAGES), uint32_t(pi / STAGES) & 1u, p.limit_ns)) {
+              fail();
+              go = 0;
+            }
+          }
+        }
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, go, 0)) break;
+      tc_fence_after();
+      const uint64_t dh = desc_sw128(a_hi(s)), dl = desc_sw128(a_lo(s)), db = desc_sw128(b_tile(s));
+      if (leader) {
+        if constexpr (A4) {
+          const uint32_t slot = tmem + uint32_t(TALL ? ((i % SLOTS) == 0 ? 224 : 480) : BN_MAX + 32 * s);
+          #pragma unroll
+          for (int a = 0; a < 8; ++a)
+            if (TALL || a < 2 || a >= 4) tmem_cp_sf(slot + uint32_t(4 * a), umma::smem_desc_sf32x16(sf_s(s, a)));
+          #pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {   // K 64 (+32 bytes) an instruction: K atom kk / 2, bytes 2 (kk % 2) + 0, 1
+            const uint32_t a = uint32_t(kk >> 1), sid = 2u * uint32_t(kk & 1);
+            const uint32_t id = umma::idesc_mxf4(BM, BN, sid, sid);
+            mma_mxf4(tmem, dh + uint64_t(2 * kk), db + uint64_t(2 * kk), id, slot + 4u * a, slot + 16u + 8u * a,
+                     (i | kk) != 0);
+            if constexpr (TALL)
+              mma_mxf4(tmem + 256u, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, slot + 8u + 4u * a,
+                       slot + 16u + 8u * a, (i | kk) != 0);
+          }
+        } else {
+          // hi (first M half): +0, lo (second M half): +4, W: +8 (rows 0-127), +12 (128-255)
+          const uint32_t sfc = tmem + uint32_t(TALL ? (s < 2 ? 224 + 16 * s : 480) : SF_COL0 + 16 * s);
+          tmem_cp_sf(sfc + 0, umma::smem_desc_sf32x16(sf_s(s, 0)));
+          if constexpr (TWO || TALL) tmem_cp_sf(sfc + 4, umma::smem_desc_sf32x16(sf_s(s, 1)));
+          tmem_cp_sf(sfc + 8, umma::smem_desc_sf32x16(sf_s(s, 2)));
+          tmem_cp_sf(sfc + 12, umma::smem_desc_sf32x16(sf_s(s, 3)));
+          #pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {   // +32 bytes along K per instruction
+            const uint32_t id = umma::idesc_mxf8f6f4(umma::F8F6F4_E4M3, BT, BM, BN, uint32_t(kk), uint32_t(kk));
+            mma_mx(tmem, dh + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 0, sfc + 8, (i | kk) != 0);
+            if constexpr (TWO) mma_mx(tmem, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 4, sfc + 8, 1u);
+            if constexpr (TALL)
+              mma_mx(tmem + 256u, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, sfc + 4, sfc + 8, (i | kk) != 0);
+          }
         }
         mma_commit(empty(s));
       }
-      mma_commit(done_bar);
+      __syncwarp();
     }
+    if (leader) mma_commit(done_bar);
   } else if (warp == 2) {
     // ------------------------------------------- W scales -> scale atoms
     // lane l gathers rows n0 + l + 32 i (i = 0..7): the 4 E8M0 bytes of K
-    // blocks 4j..4j+3 are one aligned 32-bit word of the row (K % 128 == 0)
+    // blocks 4j..4j+3 are one aligned 32-bit word of the row (K % 128 == 0);
+    // an A4 step takes two consecutive words (K % 256 == 0)
     const int row_words = p.K / 128;
     const uint32_t* ws32 = reinterpret_cast<const uint32_t*>(p.wscales);
-    auto load = [&](int i, uint32_t (&v)[8]) {
+    auto load = [&](int i, uint2 (&v)[8]) {
       #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const int r = lane + 32 * t, n = n0 + r;
-        v[t] = (i < nloc && r < BN && n < p.N) ? __ldg(ws32 + int64_t(wrow0 + n) * row_words + j0 + i) : 0u;
+        const bool in = i < nloc && r < BN && n < p.N;
+        const uint32_t* row = ws32 + int64_t(wrow0 + n) * row_words;
+        if constexpr (A4) v[t] = in ? __ldg(reinterpret_cast<const uint2*>(row) + j0 + i) : make_uint2(0u, 0u);
+        else v[t] = make_uint2(in ? __ldg(row + j0 + i) : 0u, 0u);
       }
     };
-    uint32_t cur[8], nxt[8];
+    uint2 cur[8], nxt[8];
     load(0, cur);
     load(1, nxt);
     for (int i = 0; i < nloc; ++i) {
@@ -436,12 +522,17 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         if (lane == 0 && *abort_flag == 0u) fail();
         break;
       }
-      uint32_t nx2[8];
+      uint2 nx2[8];
       load(i + 2, nx2);
       #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        const uint32_t dst = sf_s(s, 2 + t / 4) + umma::sf_atom_offset(uint32_t(lane + 32 * (t % 4)), 0);
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst), "r"(cur[t]) : "memory");
+        const uint32_t off = umma::sf_atom_offset(uint32_t(lane + 32 * (t % 4)), 0);
+        const uint32_t dst = sf_s(s, (A4 ? 4 : 2) + t / 4) + off;   // row group t / 4
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst), "r"(cur[t].x) : "memory");
+        if constexpr (A4) {   // K atom 1 of the step
+          const uint32_t dst1 = sf_s(s, 6 + t / 4) + off;
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst1), "r"(cur[t].y) : "memory");
+        }
         cur[t] = nxt[t];
         nxt[t] = nx2[t];
       }
@@ -614,14 +705,14 @@ struct MxPlan {
   int BN, S;
 };
 
-template <int F, int BN, bool TWO = true, bool TALL = false>
+template <int F, int BN, bool TWO = true, bool TALL = false, bool A4 = false>
 static cudaError_t set_smem(int dev) {
   static std::atomic<int> done[64];
   if (dev < 0 || dev >= 64 || done[dev].load()) return cudaSuccess;
-  cudaError_t e =
-      cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO, TALL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO, TALL, A4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       A4 ? SMEM_BYTES_A4 : SMEM_BYTES);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO, TALL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO, TALL, A4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[dev].store(1);
   return e;
 }
@@ -676,10 +767,10 @@ static MxPlan plan_mx(int dev, int M, int N, int K, int sms) {
   return best;
 }
 
-template <int F, int BN, bool TWO = true, bool TALL = false>
+template <int F, int BN, bool TWO = true, bool TALL = false, bool A4 = false>
 static cudaError_t launch_tile(const CUtensorMap& mhi, const CUtensorMap& mlo, const CUtensorMap& mw, MxParams prm,
                                int M, int N, int S, cudaStream_t st) {
-  const int nk = prm.K / BK;
+  const int nk = prm.K / (A4 ? 2 * BK : BK);
   prm.kb_per = (nk + S - 1) / S;
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute at[2];
@@ -692,11 +783,11 @@ static cudaError_t launch_tile(const CUtensorMap& mhi, const CUtensorMap& mlo, c
   constexpr int TM = TALL ? 2 * BM : BM;
   lc.gridDim = dim3((N + BN - 1) / BN, (M + TM - 1) / TM, S);
   lc.blockDim = dim3(THREADS);
-  lc.dynamicSmemBytes = SMEM_BYTES;
+  lc.dynamicSmemBytes = A4 ? SMEM_BYTES_A4 : SMEM_BYTES;
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 2;
-  return cudaLaunchKernelEx(&lc, qgemm_mx_kernel<F, BN, TWO, TALL>, mhi, mlo, mw, prm);
+  return cudaLaunchKernelEx(&lc, qgemm_mx_kernel<F, BN, TWO, TALL, A4>, mhi, mlo, mw, prm);
 }
 
 template <int F>
@@ -809,6 +900,61 @@ static cudaError_t launch_a8(const void* codes, const void* scales, const void* 
   }
   if (pl.BN == 224) return launch_tile<F, 224, false>(mx8, mx8, mw, prm, M, N, pl.S, st);
   return launch_tile<F, 256, false>(mx8, mx8, mw, prm, M, N, pl.S, st);
+}
+
+// The all-FP4 product: X packed to MXFP4 by the packer's rule into the
+// workspace (codes [M, K/2], then scale atoms), mxfp4 weights, one kind::mxf4
+// MMA per 64 K.  Both operand tiles are plain bytes to the copy engine (two
+// codes a byte, as stored).  K a multiple of 256 (one step).
+inline size_t a4_codes_bytes(int64_t M, int64_t K) { return align1k(size_t(M) * size_t(K / 2)); }
+inline size_t a4_workspace_bytes(int64_t M, int64_t K) {
+  return a4_codes_bytes(M, K) + align1k(size_t((M + BM - 1) / BM) * size_t(K / BK) * SF_BYTES);
+}
+
+static cudaError_t launch_a4(const void* codes, const void* scales, const void* x, void* out, bool out_f32, int M,
+                             int N, int K, void* ws, cudaStream_t st, int sms) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = set_smem<MXFP4, 256, false, false, true>(dev)) != cudaSuccess ||
+      (e = set_smem<MXFP4, 224, false, false, true>(dev)) != cudaSuccess)
+    return e;
+  // the planner counts K steps: an A4 step holds 256 codes, an 8-bit one 128
+  const int nk = K / (2 * BK);
+  MxPlan pl = plan_mx<MXFP4>(dev, M, N, K / 2, sms > 0 ? sms : 1);
+  if (g_force_bn.load() == 224 || g_force_bn.load() == 256) pl.BN = g_force_bn.load();
+  const int fs = g_force_s.load();
+  if (fs >= 1 && fs <= 4 && (fs - 1) * ((nk + fs - 1) / fs) < nk) pl.S = fs;
+  const int ft = g_force_tall.load();
+  const int64_t tall_ctas = int64_t((N + 223) / 224) * ((M + 2 * BM - 1) / (2 * BM));
+  const bool tall = ft != 1 && pl.S == 1 && M > BM && (ft == 2 || tall_ctas >= int64_t(sms > 0 ? sms : 1));
+  const uint32_t wbox = tall ? 224u : uint32_t(pl.BN);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  if ((e = launch_quantize_mxfp4_atoms(x, w8, w8 + a4_codes_bytes(M, K), M, K, st)) != cudaSuccess) return e;
+  CUtensorMap mx4, mw;
+  if (!make_map(enc, &mx4, CU_TENSOR_MAP_DATA_TYPE_UINT8, w8, K / 2, M, K / 2, BM) ||
+      !make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, N, K / 2, wbox))
+    return cudaErrorInvalidValue;
+  MxParams prm{};
+  prm.wscales = static_cast<const uint8_t*>(scales);
+  prm.sf_hi = w8 + a4_codes_bytes(M, K);
+  prm.sf_lo = prm.sf_hi;
+  prm.out = out;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.out_f32 = out_f32 ? 1 : 0;
+  prm.kb_per = nk;
+  prm.limit_ns = g_limit_ns.load();
+  prm.drop_arrivals = g_drop.load();
+  if (tall) {
+    if ((e = set_smem<MXFP4, 224, false, true, true>(dev)) != cudaSuccess) return e;
+    return launch_tile<MXFP4, 224, false, true, true>(mx4, mx4, mw, prm, M, N, 1, st);
+  }
+  if (pl.BN == 224) return launch_tile<MXFP4, 224, false, false, true>(mx4, mx4, mw, prm, M, N, pl.S, st);
+  return launch_tile<MXFP4, 256, false, false, true>(mx4, mx4, mw, prm, M, N, pl.S, st);
 }
 
 // ------------------------------------------------- expert-grouped rows ---
@@ -1284,6 +1430,14 @@ cudaError_t launch_qgemm_a8(int fmt, const void* codes, const void* scales, cons
     case MXFP8_E5M2: return mx::launch_a8<MXFP8_E5M2>(codes, scales, x, out, out_f32, m, n, k, workspace, st, sms);
     default: return cudaErrorInvalidValue;
   }
+}
+
+size_t qgemm_a4_workspace_bytes(int64_t M, int64_t K) { return mx::a4_workspace_bytes(M, K); }
+
+cudaError_t launch_qgemm_a4(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
+                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st, int sms) {
+  if (fmt != MXFP4) return cudaErrorInvalidValue;
+  return mx::launch_a4(codes, scales, x, out, out_f32, int(M), int(N), int(K), workspace, st, sms);
 }
 
 size_t qgemm_grouped_workspace_bytes(int64_t M, int64_t K, int64_t E) { return mx::grouped_layout(M, K, E).total; }

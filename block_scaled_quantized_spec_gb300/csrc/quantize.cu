@@ -8,9 +8,9 @@
 //   format's nearest-even, saturating encoding of x / 2^e (cvt.rn.satfinite).
 // One thread per block (a warp takes a row's 32 consecutive blocks).  Two
 // output layouts: the library's weight layout (codes [M, K] or [M, K/2]
-// bytes, scales [M, K/32]), and for the quantized-activation GEMM the
-// workspace layout (codes [M, K], scales in 512-byte atoms of 128 rows x 4
-// blocks, the source layout of tcgen05.cp).
+// bytes, scales [M, K/32]), and for the quantized-activation GEMMs the
+// workspace layout (codes as in the weight layout, scales in 512-byte atoms
+// of 128 rows x 4 blocks, the source layout of tcgen05.cp).
 #include <cuda_runtime.h>
 
 #include "decode.cuh"
@@ -90,8 +90,9 @@ __device__ __forceinline__ void load32(const void* x, int64_t m, int64_t K, int 
   }
 }
 
-// ATOMS: the workspace layout of the quantized-activation GEMM (E4M3 only);
-// rows past M up to the 128-row tile then get neutral scale words.
+// ATOMS: the workspace layout of the quantized-activation GEMMs (E4M3 codes
+// [M, K], or mxfp4 codes [M, K/2]); rows past M up to the 128-row tile then
+// get neutral scale words.
 template <int F, bool IN_F32, bool ATOMS>
 __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ x, uint8_t* __restrict__ codes,
                                                        uint8_t* __restrict__ scales, int M, int K) {
@@ -191,6 +192,11 @@ cudaError_t launch_quantize(int fmt, const void* x, bool x_f32, void* codes, voi
 cudaError_t launch_quantize_e4m3_atoms(const void* x, void* codes, void* atoms, int64_t M, int64_t K,
                                        cudaStream_t st) {
   return quant::launch<MXFP8_E4M3, false, true>(x, codes, atoms, int(M), int(K), st);
+}
+
+cudaError_t launch_quantize_mxfp4_atoms(const void* x, void* codes, void* atoms, int64_t M, int64_t K,
+                                        cudaStream_t st) {
+  return quant::launch<MXFP4, false, true>(x, codes, atoms, int(M), int(K), st);
 }
 
 }  // namespace qfmt_dev

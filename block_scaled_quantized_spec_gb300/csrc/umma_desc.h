@@ -33,6 +33,15 @@ QFMT_HD constexpr uint32_t idesc_mxf8f6f4(uint32_t atype, uint32_t btype, uint32
          (((m >> 4) & 31u) << 24) | ((sfa_id & 3u) << 29);
 }
 
+// kind::mxf4.block_scale.scale_vec::2X: both operands E2M1 packed two to a
+// byte (the type field's E2M1 is 1 in this kind), K = 64 per instruction, so
+// each instruction reads two consecutive bytes of every row's 32-bit scale
+// cell, starting at data id 0 or 2; bit 31 (0) selects the dense K of 64.
+enum : uint32_t { MXF4_E2M1 = 1 };
+QFMT_HD constexpr uint32_t idesc_mxf4(uint32_t m, uint32_t n, uint32_t sfa_id, uint32_t sfb_id) {
+  return idesc_mxf8f6f4(MXF4_E2M1, MXF4_E2M1, m, n, sfa_id, sfb_id);
+}
+
 // Instruction descriptor of tcgen05.mma ... kind::f16: float32 accumulator
 // (bits 4-5 = 1), A and B bf16 (bits 7-9 and 10-12 = 1), both K-major,
 // N >> 3 at bit 17, M >> 4 at bit 24.

@@ -1225,26 +1225,35 @@ __global__ void __launch_bounds__(GV_THREADS) qgemv_mx_kernel(const __grid_const
   fence_proxy_async();                                          // generic stores -> tensor-core reads
   __syncthreads();
 
-  if (tid == 0) {
-    if (!mbar_wait(w_bar, 0, p.limit_ns)) {
-      fail();
+  if (warp == 0) {
+    // the converged warp waits (lane 0) and one elected lane issues
+    int wok = 1;
+    if (lane == 0) wok = mbar_wait(w_bar, 0, p.limit_ns);
+    wok = __shfl_sync(0xFFFFFFFFu, wok, 0);
+    const bool leader = elect_one();
+    if (!wok) {
+      if (leader) fail();
     } else {
       tc_fence_after();
-      for (int j = 0; j < nsl; ++j) {
-        tmem_cp_sf(tmem + 32u + 4u * j, umma::smem_desc_sf32x16(smem_u32(sfa + j * SF_BYTES)));
-        tmem_cp_sf(tmem + 48u + 4u * j, umma::smem_desc_sf32x16(smem_u32(sfb + j * SF_BYTES)));
-      }
-      for (int j = 0; j < nsl; ++j) {
-        const uint64_t da = desc_sw128(smem_u32(wt + j * GV_ROWS * BK)), db = desc_sw128(smem_u32(xt + j * NP * BK));
-        #pragma unroll
-        for (int kk = 0; kk < BK / 32; ++kk) {
-          const uint32_t id = umma::idesc_mxf8f6f4(b_type<F>(), umma::F8F6F4_E4M3, GV_ROWS, NP, uint32_t(kk), uint32_t(kk));
-          mma_mx(tmem, da + uint64_t(2 * kk), db + uint64_t(2 * kk), id, tmem + 32u + 4u * j, tmem + 48u + 4u * j,
-                 (j | kk) != 0);
+      if (leader) {
+        for (int j = 0; j < nsl; ++j) {
+          tmem_cp_sf(tmem + 32u + 4u * j, umma::smem_desc_sf32x16(smem_u32(sfa + j * SF_BYTES)));
+          tmem_cp_sf(tmem + 48u + 4u * j, umma::smem_desc_sf32x16(smem_u32(sfb + j * SF_BYTES)));
+        }
+        for (int j = 0; j < nsl; ++j) {
+          const uint64_t da = desc_sw128(smem_u32(wt + j * GV_ROWS * BK)), db = desc_sw128(smem_u32(xt + j * NP * BK));
+          #pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint32_t id =
+                umma::idesc_mxf8f6f4(b_type<F>(), umma::F8F6F4_E4M3, GV_ROWS, NP, uint32_t(kk), uint32_t(kk));
+            mma_mx(tmem, da + uint64_t(2 * kk), db + uint64_t(2 * kk), id, tmem + 32u + 4u * j, tmem + 48u + 4u * j,
+                   (j | kk) != 0);
+          }
         }
       }
+      __syncwarp();
     }
-    mma_commit(done_bar);   // fires once the MMAs above (if any) have completed
+    if (leader) mma_commit(done_bar);   // fires once the MMAs above (if any) have completed
   }
 
   // ---- drain: row 32 warp + lane of the tile ---------------------------------

@@ -200,14 +200,25 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      for (int j = 0; j < nloc; ++j) {
-        const int s = j % STAGES;
-        const uint32_t ph = (j / STAGES) & 1;
-        if (*abort_flag) break;
-        if (!mbar_wait(a_full(s), ph, p.limit_ns) || !mbar_wait(b_full(s), ph, p.limit_ns)) { fail(); break; }
-        tc_fence_after();
-        const uint64_t bd = desc_sw128(stage_b(s)), ld = desc_sw128(stage_b(s) + LO_OFF);
+    // The warp walks the stages together (lane 0 waits, the outcome is
+    // broadcast), so the stage addresses are warp-uniform; one elected lane
+    // issues the MMAs (from one lane's branch each cost that thread ~67 cycles).
+    const bool leader = elect_one();
+    for (int j = 0; j < nloc; ++j) {
+      const int s = j % STAGES;
+      const uint32_t ph = (j / STAGES) & 1;
+      int go = 1;
+      if (lane == 0) {
+        go = *abort_flag == 0u;
+        if (go && !(mbar_wait(a_full(s), ph, p.limit_ns) && mbar_wait(b_full(s), ph, p.limit_ns))) {
+          fail();
+          go = 0;
+        }
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, go, 0)) break;
+      tc_fence_after();
+      const uint64_t bd = desc_sw128(stage_b(s)), ld = desc_sw128(stage_b(s) + LO_OFF);
+      if (leader) {
         #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {  // +32 bytes along K per instruction
           #pragma unroll
@@ -220,8 +231,9 @@ __global__ void __launch_bounds__(Dec<F>::CTA_THREADS, 1) qgemm_tc_kernel(const 
         }
         mma_commit(empty(s));
       }
-      mma_commit(done_bar);   // fires once every MMA issued above has completed
+      __syncwarp();
     }
+    if (leader) mma_commit(done_bar);   // fires once every MMA issued above has completed
   } else {
     // -------------------------------------------------------------- decoders
     const int dt = threadIdx.x - 64;                       // 0 .. DEC_THREADS-1

@@ -62,7 +62,8 @@ Value definitions (page title, then the section):
   as a weight of that format (amax / max_finite in float32, E8M0 snapped up,
   round-to-nearest-even saturating codes) and the product of the two exact
   dequantized operands is taken in float64.  qmm_a8_ref packs the activation
-  as MXFP8 E4M3, qmm_a4_ref as MXFP4 (E2M1 elements: the all-FP4 product).
+  as MXFP8 E4M3, qmm_a4_ref in the weight's FP4 family (the all-FP4 product:
+  MXFP4 against mxfp4, NVFP4 with the activation's own global against nvfp4).
 * qmm_gather: expert-routed rows over one stacked [E * N, K] weight, row m
   against rows [e N, e N + N) with e = expert_idx[m] -- PR #250, the MoE
   gather-qmm commit (weight row expert_ids[m] * out_dim + n, one stacked
@@ -268,21 +269,30 @@ def qmm_rmsnorm_ref(fmt, codes, scales, global_scale, x, x_dtype, gamma_bits, ep
 
 
 
-def quantize_activations(fmt, x, x_dtype, m, k):
-    """(codes, scales) of the activation X [M, K] packed as a weight of ``fmt`` (mxfp4 / mxfp8 E4M3 / E5M2).
+def quantize_activations_global(fmt, x, x_dtype, m, k):
+    """(codes, scales, global) of the activation X [M, K] packed as a weight of ``fmt``.
 
-    bf16 and float32 values are exact in float32, so the packer sees X itself.
+    mxfp4 / mxfp8 E4M3 / E5M2 (global 1.0), or nvfp4: the whole X is one
+    tensor to the packer, so its global is amax(X) / (6 * 448).  bf16 and
+    float32 values are exact in float32, so the packer sees X itself.
     """
-    if fmt not in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2"):
+    if fmt not in ("mxfp4", "mxfp8_e4m3", "mxfp8_e5m2", "nvfp4"):
         raise ValueError(fmt)
     xv = x_values(x, x_dtype).reshape(m, k).astype(np.float32)
-    c, s, _ = pack(fmt, xv)
+    return pack(fmt, xv)
+
+
+def quantize_activations(fmt, x, x_dtype, m, k):
+    """(codes, scales) of the activation X [M, K] packed as a weight of ``fmt`` (mxfp4 / mxfp8 E4M3 / E5M2)."""
+    if fmt == "nvfp4":
+        raise ValueError("nvfp4 carries a global: quantize_activations_global")
+    c, s, _ = quantize_activations_global(fmt, x, x_dtype, m, k)
     return c, s
 
 
 def _qmm_quantized_x_ref(act_fmt, fmt, codes, scales, global_scale, x, x_dtype, m, n, k):
-    xc, xs = quantize_activations(act_fmt, x, x_dtype, m, k)
-    xq = dequant_exact(act_fmt, xc, xs, 1.0, m, k)
+    xc, xs, xg = quantize_activations_global(act_fmt, x, x_dtype, m, k)
+    xq = dequant_exact(act_fmt, xc, xs, xg, m, k)
     w = dequant_exact(fmt, codes, scales, global_scale, n, k)
     return xq @ w.T, A8_REL * (np.abs(xq) @ np.abs(w).T) + BOUND_ABS
 
@@ -297,8 +307,12 @@ def qmm_a8_ref(fmt, codes, scales, global_scale, x, x_dtype, m, n, k):
 
 
 def qmm_a4_ref(fmt, codes, scales, global_scale, x, x_dtype, m, n, k):
-    """(ref, bound) of X4 . dequant(W)^T, X4 the activation packed as MXFP4 (E2M1, E8M0 scale per 32).
+    """(ref, bound) of X4 . dequant(W)^T, the all-FP4 product.
 
-    The same float32-accumulation bound as qmm_a8_ref: A8_REL * sum_k |x4||w| + BOUND_ABS.
+    X4 is the activation packed in W's own FP4 family: MXFP4 (E2M1, E8M0
+    scale per 32) against mxfp4 weights, NVFP4 (E2M1, E4M3 scale per 16, the
+    tensor's global) against nvfp4 weights.  The same float32-accumulation
+    bound as qmm_a8_ref: A8_REL * sum_k |x4||w| + BOUND_ABS.
     """
-    return _qmm_quantized_x_ref("mxfp4", fmt, codes, scales, global_scale, x, x_dtype, m, n, k)
+    act = "nvfp4" if fmt == "nvfp4" else "mxfp4"
+    return _qmm_quantized_x_ref(act, fmt, codes, scales, global_scale, x, x_dtype, m, n, k)

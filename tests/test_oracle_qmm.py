@@ -765,7 +765,7 @@ def _e2m1_representable_activations(m, k, seed):
     return synth.f32_to_bf16_bits(x)
 
 
-@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8_e4m3", "nvfp4", "int4_affine"])
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8_e4m3", "int4_affine"])
 def test_a4_is_the_exact_product_when_x_is_representable(fmt):
     # quantizing an activation that is already MXFP4 changes nothing: the
     # W . A4 reference equals the exact bf16-activation reference bit for bit
@@ -802,3 +802,129 @@ def test_planted_a4_scale_divisor_mistake_is_caught(monkeypatch):
     monkeypatch.setitem(opack._ELEM, "mxfp4", ("e2m1", 448.0))
     with pytest.raises(AssertionError):
         test_a4_is_the_exact_product_when_x_is_representable("mxfp4")
+
+
+# ------------------- the all-FP4 product over nvfp4: NVFP4 activations -------------------
+
+
+def _brute_activation_quant_nvfp4(x):
+    # the whole X is one tensor: global g = float32(amax(X) / 2688) (1 for a
+    # zero X); per block of 16: t = float32(float32(amax / 6) / g), its scale
+    # the nearest E4M3 code (a zero block: 0x38 = 1.0), eff = float32(E4M3 * g),
+    # codes the nearest E2M1 of float32(x / eff) (eff = 0: code 0)
+    x = np.asarray(x, np.float32)
+    amax_t = np.float32(np.max(np.abs(x)))
+    g = np.float32(amax_t / np.float32(2688.0)) if amax_t > 0 else np.float32(1.0)
+    vals = dict(_e4m3_table())
+    codes, scodes = [], []
+    for row in x:
+        rc, rs = [], []
+        for b in range(0, len(row), 16):
+            blk = row[b:b + 16]
+            amax = np.float32(np.max(np.abs(blk)))
+            if amax > 0:
+                t = np.float32(np.float32(amax / np.float32(6.0)) / g)
+                sc = _brute_e4m3(Fraction(float(t)))
+            else:
+                sc = 0x38
+            rs.append(sc)
+            eff = np.float32(np.float32(float(vals[sc])) * g)
+            for v in blk:
+                rc.append(0 if eff == 0 else _brute_e2m1(Fraction(float(np.float32(v / eff)))))
+        codes.append(rc)
+        scodes.append(rs)
+    return codes, scodes, g
+
+
+def test_nvfp4_activation_quantizer_matches_brute_force():
+    m, k = 3, 64
+    xb = _a4_activations(m, k, seed=71)
+    c, s, g = reference.quantize_activations_global("nvfp4", xb, "bf16", m, k)
+    xv = reference.x_values(xb, "bf16").reshape(m, k)
+    bc, bs, bg = _brute_activation_quant_nvfp4(xv)
+    assert np.float32(g) == bg
+    for i in range(m):
+        assert [_code("nvfp4", c[i], kk) for kk in range(k)] == bc[i], i
+        assert list(s[i]) == bs[i], i
+
+
+def test_a4_nvfp4_product_matches_exact_rational_brute_force():
+    m, n, k = 2, 3, 64
+    cw, sw, gw = _tiny_case("nvfp4", m=m, n=n, k=k, seed=72)[:3]
+    xb = _a4_activations(m, k, seed=73)
+    ref, bound = reference.qmm_a4_ref("nvfp4", cw, sw, gw, xb, "bf16", m, n, k)
+    xv = reference.x_values(xb, "bf16").reshape(m, k)
+    bc, bs, bg = _brute_activation_quant_nvfp4(xv)
+    vals = dict(_e4m3_table())
+    for i in range(m):
+        x4 = [_lib_elem("nvfp4", bc[i][kk]) * vals[bs[i][kk // 16]] * Fraction(float(bg)) for kk in range(k)]
+        for j in range(n):
+            exact = sum(x4[kk] * _lib_elem("nvfp4", _code("nvfp4", cw[j], kk)) * _lib_scale("nvfp4", sw, j, kk // 16)[0]
+                        for kk in range(k)) * Fraction(float(gw))
+            # ref is an fp64 matmul: within a few fp64 ulps of the exact rational sum
+            scale = sum(abs(x4[kk] * _lib_elem("nvfp4", _code("nvfp4", cw[j], kk))
+                            * _lib_scale("nvfp4", sw, j, kk // 16)[0]) for kk in range(k)) * Fraction(float(gw))
+            assert abs(Fraction(ref[i, j]) - exact) <= Fraction(1, 2 ** 48) * scale, (i, j)
+            assert bound[i, j] > 0
+
+
+def _nvfp4_representable_activations(m, k, seed):
+    # g = 2^-3: one block holds 6 * 448 * g (the tensor maximum, so the
+    # global is g exactly); every block is E2M1 values times s_b g with s_b an
+    # E4M3 value and one element 6 s_b g, so its scale is s_b and its codes
+    # its values
+    rng = np.random.default_rng(seed)
+    g = 2.0 ** -3
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    e4 = [float(v) for c, v in _e4m3_table() if 0 < c < 0x7F and float(v) >= 2.0 ** -6]
+    x = np.empty((m, k), np.float32)
+    for i in range(m):
+        for b in range(0, k, 16):
+            sb = 448.0 if (i, b) == (0, 0) else float(rng.choice(e4))
+            v = rng.choice(grid, 16) * rng.choice([-1.0, 1.0], 16)
+            v[int(rng.integers(0, 16))] = rng.choice([6.0, -6.0])
+            x[i, b:b + 16] = (v * sb * g).astype(np.float32)
+    return synth.f32_to_bf16_bits(x)
+
+
+def test_a4_nvfp4_is_the_exact_product_when_x_is_representable():
+    m, n, k = 3, 7, 128
+    xb = _nvfp4_representable_activations(m, k, seed=74)
+    assert np.array_equal(reference.x_values(xb, "bf16").reshape(m, k).astype(np.float32),
+                          reference.x_values(xb, "bf16").reshape(m, k))   # bf16-exact construction
+    c, s, g = pack.pack("nvfp4", synth.weights(n, k, seed=75, outliers=True))
+    a4, _ = reference.qmm_a4_ref("nvfp4", c, s, g, xb, "bf16", m, n, k)
+    exact, _ = reference.qmm_ref("nvfp4", c, s, g, xb, "bf16", m, n, k)
+    assert np.array_equal(a4, exact)
+
+
+def test_planted_dropped_activation_global_is_caught(monkeypatch):
+    # the NVFP4 activation dequantized without its global: the identity fails
+    real = reference.quantize_activations_global
+
+    def no_global(fmt, x, x_dtype, m, k):
+        c, s, g = real(fmt, x, x_dtype, m, k)
+        return c, s, np.float32(1.0)
+
+    monkeypatch.setattr(reference, "quantize_activations_global", no_global)
+    with pytest.raises(AssertionError):
+        test_a4_nvfp4_is_the_exact_product_when_x_is_representable()
+
+
+def test_planted_nvfp4_scale_rounding_mistake_is_caught(monkeypatch):
+    # the E4M3 block scale truncated toward zero instead of rounded to nearest:
+    # the brute-force quantizer catches it
+    from oracle import codec
+    real = codec.encode_rne_sat
+
+    def trunc(v, fmt):
+        if fmt != "e4m3":
+            return real(v, fmt)
+        v = np.asarray(v, np.float32)
+        c = real(v, fmt)
+        over = np.abs(codec.E4M3_TABLE[c]) > np.abs(v.astype(np.float64))
+        return np.where(over & (c & 0x7F > 0), c - 1, c).astype(np.uint8)
+
+    monkeypatch.setattr(codec, "encode_rne_sat", trunc)
+    with pytest.raises(AssertionError):
+        test_nvfp4_activation_quantizer_matches_brute_force()

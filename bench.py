@@ -213,7 +213,8 @@ class Problem:
             if self.a8:
                 q.qmm_a8(self.fmt, self.codes[i], self.scales[i], self.x[i], self.n, out=self.out[i], workspace=self.ws)
             elif self.a4:
-                q.qmm_a4(self.fmt, self.codes[i], self.scales[i], self.x[i], self.n, out=self.out[i], workspace=self.ws)
+                q.qmm_a4(self.fmt, self.codes[i], self.scales[i], self.g, self.x[i], self.n, out=self.out[i],
+                         workspace=self.ws)
             elif self.ws is not None:
                 q.qmm_ex(self.fmt, self.codes[i], self.scales[i], self.g, self.x[i], self.n, out=self.out[i],
                          workspace=self.ws)
@@ -467,7 +468,7 @@ BREAKDOWN = [
     ("mxfp8_e4m3", 2048, 4096, 4096, "A8"), ("mxfp4", 2048, 4096, 4096, "A8"),
     ("mxfp8_e5m2", 4096, 11008, 4096, "A8"),
     # the all-FP4 product (W . A4)
-    ("mxfp4", 2048, 4096, 4096, "A4"), ("mxfp4", 4096, 11008, 4096, "A4"),
+    ("mxfp4", 2048, 4096, 4096, "A4"), ("mxfp4", 4096, 11008, 4096, "A4"), ("nvfp4", 2048, 4096, 4096, "A4"),
     # the 2/3/5/6-bit bit streams
     ("int3", 1, 11008, 4096), ("mxint5", 16, 4096, 4096),
     # batch decode rows on [4096, 4096] (one decode per weight block for every activation row)
@@ -707,7 +708,7 @@ def breakdown_row(fmt, m, n, k, hbm, bf16, kind, steps=10, warmup=3, path="auto"
     row = {"fmt": fmt, "M": m, "N": n, "K": k, "us": round(per * 1e3, 2), "copies": copies,
            "path": {"B": "block-scaled tcgen05 GEMM (X split + kind::mxf8f6f4)", "A": "bf16-decode tcgen05 GEMM",
                     "A8": "both operands quantized (X to MXFP8 E4M3, one kind::mxf8f6f4 MMA per block)",
-                    "A4": "all-FP4 (X to MXFP4, one kind::mxf4 MMA per 64 K)",
+                    "A4": "all-FP4 (X in W's FP4 family, kind::mxf4 / mxf4nvf4 per 64 K)",
                     "GEMV": "decode GEMV", "SUB": "CUDA-core sub-byte kernel"}[prob.path]}
     gbs = nbytes / (per * 1e-3) / 1e9
     tfl = prob.flops / (per * 1e-3) / 1e12

@@ -77,9 +77,9 @@ _SIGS = {
                               ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                               ctypes.c_size_t, ctypes.c_void_p]),
     "qmm_a8_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
-    "qmm_a4": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                              ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
-                              ctypes.c_size_t, ctypes.c_void_p]),
+    "qmm_a4": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                              ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                              ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "qmm_a4_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
     "qmm_grouped": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
@@ -364,12 +364,14 @@ def qmm_a8(fmt, codes, scales, x, N: int, out=None, out_dtype=None, workspace=No
     return _qmm_quantized_x("qmm_a8", fmt, codes, scales, x, N, out, out_dtype, workspace, stream)
 
 
-def qmm_a4(fmt, codes, scales, x, N: int, out=None, out_dtype=None, workspace=None, stream=None):
-    """out [M, N] = Q4(x) . dequant(W)^T, Q4(x) the activation packed to MXFP4 (the all-FP4 product; mxfp4 W)."""
-    return _qmm_quantized_x("qmm_a4", fmt, codes, scales, x, N, out, out_dtype, workspace, stream)
+def qmm_a4(fmt, codes, scales, global_scale: float, x, N: int, out=None, out_dtype=None, workspace=None, stream=None):
+    """out [M, N] = Q4(x) . dequant(W)^T, the all-FP4 product: Q4(x) the activation packed in W's FP4
+    family (MXFP4 for mxfp4 W; NVFP4 with its own global for nvfp4 W, whose global is global_scale)."""
+    return _qmm_quantized_x("qmm_a4", fmt, codes, scales, x, N, out, out_dtype, workspace, stream,
+                            global_scale=global_scale)
 
 
-def _qmm_quantized_x(where, fmt, codes, scales, x, N, out, out_dtype, workspace, stream):
+def _qmm_quantized_x(where, fmt, codes, scales, x, N, out, out_dtype, workspace, stream, global_scale=None):
     import torch
     M, K = _activations(where, x)
     _weights(where, fmt, codes, scales, N, K, 0)
@@ -384,9 +386,9 @@ def _qmm_quantized_x(where, fmt, codes, scales, x, N, out, out_dtype, workspace,
         workspace = torch.empty(max(1, wsb(_fmt(fmt), M, K)), dtype=torch.uint8, device=x.device)
     _tensor(workspace, where, "workspace")
     _on_device(where, x=x, codes=codes, scales=scales, out=out, workspace=workspace)
-    _check(getattr(lib, where)(_fmt(fmt), _ptr(codes), _ptr(scales), _ptr(x), _ptr(out),
-                               F32 if out.dtype == torch.float32 else BF16, M, N, K, _ptr(workspace),
-                               workspace.numel() * workspace.element_size(), _stream(stream)), where)
+    head = (_fmt(fmt), _ptr(codes), _ptr(scales)) + (() if global_scale is None else (float(global_scale),))
+    _check(getattr(lib, where)(*head, _ptr(x), _ptr(out), F32 if out.dtype == torch.float32 else BF16, M, N, K,
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)), where)
     return out
 
 

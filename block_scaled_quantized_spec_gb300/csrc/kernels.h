@@ -71,11 +71,13 @@ cudaError_t launch_qgemm_grouped(int fmt, const void* codes, const void* scales,
 size_t qgemm_a8_workspace_bytes(int64_t M, int64_t K);
 cudaError_t launch_qgemm_a8(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
                             int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st, int sms);
-// The all-FP4 product: X packed to MXFP4 in `workspace`, mxfp4 weights, one
-// kind::mxf4 MMA per 64 K (any M >= 1; K a multiple of 256).
-size_t qgemm_a4_workspace_bytes(int64_t M, int64_t K);
-cudaError_t launch_qgemm_a4(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
-                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st, int sms);
+// The all-FP4 product: X packed in W's FP4 family in `workspace` (MXFP4
+// against mxfp4, one kind::mxf4 MMA per 64 K; NVFP4 with its global against
+// nvfp4, kind::mxf4nvf4), any M >= 1, K a multiple of 256.
+size_t qgemm_a4_workspace_bytes(int fmt, int64_t M, int64_t K);
+cudaError_t launch_qgemm_a4(int fmt, const void* codes, const void* scales, float global_scale, const void* x,
+                            void* out, bool out_f32, int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st,
+                            int sms);
 // The activation quantizer: X [M, K] (bf16 or float32) -> codes + E8M0 scales
 // of mxfp4 / mxfp8 E4M3 / E5M2 in the weight layout, or (E4M3, mxfp4) the
 // workspace layout of the quantized-activation products.
@@ -85,6 +87,12 @@ cudaError_t launch_quantize_e4m3_atoms(const void* x, void* codes, void* atoms, 
                                        cudaStream_t st);
 cudaError_t launch_quantize_mxfp4_atoms(const void* x, void* codes, void* atoms, int64_t M, int64_t K,
                                         cudaStream_t st);
+// NVFP4 activations for the all-FP4 product over nvfp4: per-CTA maxima of |x|
+// into `partials` (quantize_nvfp4_partials(M) floats), then codes [M, K/2],
+// E4M3 scale atoms (4 blocks of 16 a cell) and the global into *g_out.
+int quantize_nvfp4_partials(int64_t M);
+cudaError_t launch_quantize_nvfp4_atoms(const void* x, void* codes, void* atoms, float* partials, float* g_out,
+                                        int64_t M, int64_t K, cudaStream_t st);
 cudaError_t launch_qgemv_mx(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
                             int64_t M, int64_t N, int64_t K, cudaStream_t st, int sms);
 void set_mx_wait_limit_ns(uint64_t ns);

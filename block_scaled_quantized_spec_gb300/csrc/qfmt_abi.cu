@@ -427,35 +427,36 @@ int qmm_a8(int fmt, const void* codes, const void* scales, const void* x, void* 
 
 size_t qmm_a4_workspace_bytes(int fmt, int64_t M, int64_t K) {
   clear_error();
-  if (fmt != QFMT_MXFP4) return 0;
+  if (fmt != QFMT_MXFP4 && fmt != QFMT_NVFP4) return 0;
   if (M <= 0 || K <= 0 || K % 256) return 0;
-  return qfmt_dev::qgemm_a4_workspace_bytes(M, K);
+  return qfmt_dev::qgemm_a4_workspace_bytes(fmt, M, K);
 }
 
-int qmm_a4(int fmt, const void* codes, const void* scales, const void* x, void* out, int out_dtype, int64_t M,
-           int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
+int qmm_a4(int fmt, const void* codes, const void* scales, float global_scale, const void* x, void* out,
+           int out_dtype, int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
   int st = check_group(fmt, 0);
   if (st) return st;
-  if (fmt != QFMT_MXFP4) return fail(QFMT_EUNSUPPORTED, "qmm_a4 takes mxfp4 weights (format %d)", fmt);
+  if (fmt != QFMT_MXFP4 && fmt != QFMT_NVFP4)
+    return fail(QFMT_EUNSUPPORTED, "qmm_a4 takes mxfp4 or nvfp4 weights (format %d)", fmt);
   if ((st = check_shape(fmt, M, N, K))) return st;
   if (out_dtype != QFMT_F32 && out_dtype != QFMT_BF16) return fail(QFMT_EINVAL, "bad out_dtype %d", out_dtype);
   if (M == 0 || N == 0) return QFMT_OK;
   if (K % 256) return fail(QFMT_ESHAPE, "qmm_a4: K=%lld must be a multiple of 256", (long long)K);
   if (M > 65535LL * 128) return fail(QFMT_ESHAPE, "M=%lld: more than 65535 row tiles of 128", (long long)M);
-  const size_t need = qfmt_dev::qgemm_a4_workspace_bytes(M, K);
+  const size_t need = qfmt_dev::qgemm_a4_workspace_bytes(fmt, M, K);
   if (!workspace || workspace_bytes < need)
     return fail(QFMT_ENOSPACE, "workspace of %zu bytes, qmm_a4 needs %zu", workspace_bytes, need);
   if ((st = check_ptr(codes, 16, "codes"))) return st;
-  if ((st = check_ptr(scales, 8, "scales"))) return st;
+  if ((st = check_ptr(scales, fmt == QFMT_NVFP4 ? 16 : 8, "scales"))) return st;
   if ((st = check_ptr(x, 16, "x"))) return st;
   if ((st = check_ptr(out, 16, "out"))) return st;
   if ((st = check_ptr(workspace, 128, "workspace"))) return st;
   int err = QFMT_OK;
   const int sms = device_sms(&err);
   if (err) return err;
-  return cuda_status(qfmt_dev::launch_qgemm_a4(fmt, codes, scales, x, out, out_dtype == QFMT_F32, M, N, K, workspace,
-                                               static_cast<cudaStream_t>(stream), sms),
+  return cuda_status(qfmt_dev::launch_qgemm_a4(fmt, codes, scales, global_scale, x, out, out_dtype == QFMT_F32, M, N,
+                                               K, workspace, static_cast<cudaStream_t>(stream), sms),
                      "qmm_a4 launch");
 }
 

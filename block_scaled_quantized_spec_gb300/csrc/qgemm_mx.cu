@@ -54,6 +54,7 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include "decode.cuh"
 #include "kernels.h"
@@ -77,6 +78,8 @@ constexpr int SF_STAGE = 4 * SF_BYTES;        // hi atom, lo atom, two W atoms (
 constexpr int SF_STAGE_A4 = 8 * SF_BYTES;     // all-FP4 form: two K atoms each of two X tiles and two W row groups
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGES * SF_STAGE + 256;
 constexpr int SMEM_BYTES_A4 = 1024 + STAGES * STAGE_BYTES + STAGES * SF_STAGE_A4 + 256;
+constexpr int SF_STAGE_NV = 12 * SF_BYTES;    // nvfp4 all-FP4: four K atoms of the X tile, eight of W
+constexpr int SMEM_BYTES_NV = 1024 + STAGES * STAGE_BYTES + STAGES * SF_STAGE_NV + 256;
 constexpr int THREADS = 256;
 constexpr int TMEM_COLS = 512;                // accumulator 256 columns + 16 scale columns a stage
 constexpr int SF_COL0 = 256;
@@ -251,6 +254,18 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// Both operands E2M1 packed two codes to a byte, K 64 an instruction, four
+// UE4M3 scales of each row (one a block of 16: the whole scale cell).
+__device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
 // Both operands E2M1 packed two codes to a byte, K 64 an instruction, two
 // E8M0 scales of each row (the scale cell's bytes from the descriptor's id).
 __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -279,6 +294,10 @@ struct MxParams {
   const int* route_off;
   const int* row_of;
   int E;
+  // nvfp4 all-FP4 form: the output is scaled by the weight's global times the
+  // activation's (computed on the device, read after the dependent wait)
+  float gw;
+  const float* gx;
 };
 
 template <int F> constexpr uint32_t b_type() {
@@ -302,24 +321,32 @@ template <int F> constexpr uint32_t b_type() {
 // K atom 0, then of K atom 1); with tall tiles only two slots fit (columns
 // 224 and 480) and a slot is refilled once the MMAs of the stage before last
 // have completed.
+// NV (with A4; nvfp4 weights): the NVFP4 form, kind::mxf4nvf4 with UE4M3
+// scales per 16 values.  A K step carries 16 blocks a row: four scale cells,
+// so four K atoms for the X tile and eight for W (48 columns a slot at 256 +
+// 48 s: X at +0 .. +15, then W's row groups 0 and 1 of K atom a at +16 + 8a
+// and +20 + 8a); each MMA reads a whole cell.  Single 128-row tiles only (a
+// tall tile's 64 scale columns a step would leave one slot).  The epilogue
+// multiplies by the two tensors' globals.
 // A K split runs its splits as a cluster along z; each split's float32
 // partial tile goes to its drained stage memory and the cluster sums them
 // through distributed shared memory in rank order.
-template <int F, int BN, bool TWO = true, bool TALL = false, bool A4 = false>
+template <int F, int BN, bool TWO = true, bool TALL = false, bool A4 = false, bool NV = false>
 __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_constant__ CUtensorMap xhi_map,
                                                               const __grid_constant__ CUtensorMap xlo_map,
                                                               const __grid_constant__ CUtensorMap w_map,
                                                               const MxParams p) {
   static_assert(BN % 32 == 0 && BN <= BN_MAX && BN > 128, "two W scale atoms a stage");
   static_assert(!TALL || (!TWO && BN == 224), "tall tiles: one term, 224 columns");
-  static_assert(!A4 || (!TWO && F == MXFP4), "the all-FP4 form: one E2M1 activation term, mxfp4 weights");
+  static_assert(!A4 || (!TWO && F == (NV ? NVFP4 : MXFP4)), "the all-FP4 form: one E2M1 activation term");
+  static_assert(!NV || (A4 && !TALL), "the NVFP4 form: single tiles");
   // bytes a stage's copies deliver: the two X tiles (terms, or M halves), the
   // W codes (E2M1 through 16U4_ALIGN16B: the 8 data bytes of every 16-byte
   // unit, the gaps are not written; packed A4 tiles: every byte) and the X
   // scale atoms (A4: two K atoms a tile)
   constexpr int TERMS = (TWO || TALL) ? 2 : 1;
-  constexpr int XA = A4 ? 2 : 1;
-  constexpr int SFS = A4 ? SF_STAGE_A4 : SF_STAGE;
+  constexpr int XA = NV ? 4 : (A4 ? 2 : 1);
+  constexpr int SFS = NV ? SF_STAGE_NV : (A4 ? SF_STAGE_A4 : SF_STAGE);
   constexpr uint32_t TX_BYTES =
       TERMS * (A_BYTES + XA * SF_BYTES) + ((F == MXFP4 && !A4) ? BN * BK / 2 : BN * BK);
   constexpr int PSTRIDE = BN + 4;                 // floats per partial-tile row (K split)
@@ -346,7 +373,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     wrow0 = e * p.N;
   }
   const int nk = p.K / (A4 ? 2 * BK : BK);        // K steps (A4: 256 codes in a 128-byte row)
-  const int katoms = p.K / BK;                      // scale atoms (4 K blocks) along a row
+  const int katoms = p.K / (NV ? 64 : BK);          // scale atoms (4 K blocks) along a row
   const int j0 = blockIdx.z * p.kb_per, j1 = min(nk, j0 + p.kb_per);   // this split's K steps
   const int nloc = j1 - j0;
   const bool split_k = gridDim.z > 1;
@@ -358,7 +385,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
   auto a_hi = [&](int s) { return sbase + uint32_t(s * STAGE_BYTES); };
   auto a_lo = [&](int s) { return sbase + uint32_t(s * STAGE_BYTES + A_BYTES); };
   auto b_tile = [&](int s) { return sbase + uint32_t(s * STAGE_BYTES + 2 * A_BYTES); };
-  // i: 0 hi, 1 lo, 2-3 W (A4: 0-1 X tile 0, 2-3 X tile 1, 4-7 W; two K atoms each)
+  // i: 0 hi, 1 lo, 2-3 W (A4: 0-1 X tile 0, 2-3 X tile 1, 4-7 W; two K atoms
+  // each; NV: 0-3 X, 4-11 W: K atom a, row group g at 4 + 2a + g)
   auto sf_s = [&](int s, int i) { return sfbase + uint32_t(s * SFS + i * SF_BYTES); };
   auto fail = [&]() {
     *abort_flag = 1u;
@@ -456,7 +484,16 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
       tc_fence_after();
       const uint64_t dh = desc_sw128(a_hi(s)), dl = desc_sw128(a_lo(s)), db = desc_sw128(b_tile(s));
       if (leader) {
-        if constexpr (A4) {
+        if constexpr (NV) {
+          const uint32_t slot = tmem + uint32_t(BN_MAX + 48 * s);
+          #pragma unroll
+          for (int a = 0; a < 12; ++a) tmem_cp_sf(slot + uint32_t(4 * a), umma::smem_desc_sf32x16(sf_s(s, a)));
+          constexpr uint32_t id = umma::idesc_mxf4nvf4(BM, BN);
+          #pragma unroll
+          for (int kk = 0; kk < 4; ++kk)   // K 64 (+32 bytes) an instruction: the whole cell of K atom kk
+            mma_mxf4nvf4(tmem, dh + uint64_t(2 * kk), db + uint64_t(2 * kk), id, slot + 4u * kk, slot + 16u + 8u * kk,
+                         (i | kk) != 0);
+        } else if constexpr (A4) {
           const uint32_t slot = tmem + uint32_t(TALL ? ((i % SLOTS) == 0 ? 224 : 480) : BN_MAX + 32 * s);
           #pragma unroll
           for (int a = 0; a < 8; ++a)
@@ -496,20 +533,23 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     // ------------------------------------------- W scales -> scale atoms
     // lane l gathers rows n0 + l + 32 i (i = 0..7): the 4 E8M0 bytes of K
     // blocks 4j..4j+3 are one aligned 32-bit word of the row (K % 128 == 0);
-    // an A4 step takes two consecutive words (K % 256 == 0)
-    const int row_words = p.K / 128;
+    // an A4 step takes two consecutive words (K % 256 == 0); an NV step the
+    // 16 E4M3 bytes of its 16 blocks, four words
+    const int row_words = p.K / (NV ? 64 : 128);
     const uint32_t* ws32 = reinterpret_cast<const uint32_t*>(p.wscales);
-    auto load = [&](int i, uint2 (&v)[8]) {
+    using SW = typename std::conditional<NV, uint4, uint2>::type;
+    auto load = [&](int i, SW (&v)[8]) {
       #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const int r = lane + 32 * t, n = n0 + r;
         const bool in = i < nloc && r < BN && n < p.N;
         const uint32_t* row = ws32 + int64_t(wrow0 + n) * row_words;
-        if constexpr (A4) v[t] = in ? __ldg(reinterpret_cast<const uint2*>(row) + j0 + i) : make_uint2(0u, 0u);
+        if constexpr (NV) v[t] = in ? __ldg(reinterpret_cast<const uint4*>(row) + j0 + i) : make_uint4(0u, 0u, 0u, 0u);
+        else if constexpr (A4) v[t] = in ? __ldg(reinterpret_cast<const uint2*>(row) + j0 + i) : make_uint2(0u, 0u);
         else v[t] = make_uint2(in ? __ldg(row + j0 + i) : 0u, 0u);
       }
     };
-    uint2 cur[8], nxt[8];
+    SW cur[8], nxt[8];
     load(0, cur);
     load(1, nxt);
     for (int i = 0; i < nloc; ++i) {
@@ -522,16 +562,25 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         if (lane == 0 && *abort_flag == 0u) fail();
         break;
       }
-      uint2 nx2[8];
+      SW nx2[8];
       load(i + 2, nx2);
       #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const uint32_t off = umma::sf_atom_offset(uint32_t(lane + 32 * (t % 4)), 0);
-        const uint32_t dst = sf_s(s, (A4 ? 4 : 2) + t / 4) + off;   // row group t / 4
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst), "r"(cur[t].x) : "memory");
-        if constexpr (A4) {   // K atom 1 of the step
-          const uint32_t dst1 = sf_s(s, 6 + t / 4) + off;
-          asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst1), "r"(cur[t].y) : "memory");
+        if constexpr (NV) {   // K atom a of row group t / 4 at 4 + 2a + t / 4
+          const uint32_t w4[4] = {cur[t].x, cur[t].y, cur[t].z, cur[t].w};
+          #pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            const uint32_t dst = sf_s(s, 4 + 2 * a + t / 4) + off;
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst), "r"(w4[a]) : "memory");
+          }
+        } else {
+          const uint32_t dst = sf_s(s, (A4 ? 4 : 2) + t / 4) + off;   // row group t / 4
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst), "r"(cur[t].x) : "memory");
+          if constexpr (A4) {   // K atom 1 of the step
+            const uint32_t dst1 = sf_s(s, 6 + t / 4) + off;
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst1), "r"(cur[t].y) : "memory");
+          }
         }
         cur[t] = nxt[t];
         nxt[t] = nx2[t];
@@ -549,6 +598,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     tc_fence_after();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int q = warp & 3;
+    float gsc = 1.0f;                               // NV: the two globals (the activation's from the quantizer)
+    if constexpr (NV) gsc = __fmul_rn(p.gw, *p.gx);
     #pragma unroll 1
     for (int hf = 0; hf < (TALL ? 2 : 1); ++hf) {   // the accumulators: M halves of a tall tile
     // the output row of this lane's accumulator row (grouped: through row_of)
@@ -559,6 +610,10 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     for (int cb = 0; cb < BN / 32; ++cb) {
       uint32_t r[32];
       tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(hf * 256 + cb * 32), r);
+      if constexpr (NV) {
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), gsc));
+      }
       if (split_k) {   // this split's partial tile into the drained stage memory
         float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(smem) + (q * 32 + lane) * PSTRIDE + cb * 32);
         #pragma unroll
@@ -705,14 +760,16 @@ struct MxPlan {
   int BN, S;
 };
 
-template <int F, int BN, bool TWO = true, bool TALL = false, bool A4 = false>
+template <int F, int BN, bool TWO = true, bool TALL = false, bool A4 = false, bool NV = false>
 static cudaError_t set_smem(int dev) {
   static std::atomic<int> done[64];
   if (dev < 0 || dev >= 64 || done[dev].load()) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO, TALL, A4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       A4 ? SMEM_BYTES_A4 : SMEM_BYTES);
+  cudaError_t e =
+      cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO, TALL, A4, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           NV ? SMEM_BYTES_NV : (A4 ? SMEM_BYTES_A4 : SMEM_BYTES));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO, TALL, A4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(qgemm_mx_kernel<F, BN, TWO, TALL, A4, NV>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1);
   if (e == cudaSuccess) done[dev].store(1);
   return e;
 }
@@ -767,7 +824,7 @@ static MxPlan plan_mx(int dev, int M, int N, int K, int sms) {
   return best;
 }
 
-template <int F, int BN, bool TWO = true, bool TALL = false, bool A4 = false>
+template <int F, int BN, bool TWO = true, bool TALL = false, bool A4 = false, bool NV = false>
 static cudaError_t launch_tile(const CUtensorMap& mhi, const CUtensorMap& mlo, const CUtensorMap& mw, MxParams prm,
                                int M, int N, int S, cudaStream_t st) {
   const int nk = prm.K / (A4 ? 2 * BK : BK);
@@ -783,11 +840,11 @@ static cudaError_t launch_tile(const CUtensorMap& mhi, const CUtensorMap& mlo, c
   constexpr int TM = TALL ? 2 * BM : BM;
   lc.gridDim = dim3((N + BN - 1) / BN, (M + TM - 1) / TM, S);
   lc.blockDim = dim3(THREADS);
-  lc.dynamicSmemBytes = A4 ? SMEM_BYTES_A4 : SMEM_BYTES;
+  lc.dynamicSmemBytes = NV ? SMEM_BYTES_NV : (A4 ? SMEM_BYTES_A4 : SMEM_BYTES);
   lc.stream = st;
   lc.attrs = at;
   lc.numAttrs = 2;
-  return cudaLaunchKernelEx(&lc, qgemm_mx_kernel<F, BN, TWO, TALL, A4>, mhi, mlo, mw, prm);
+  return cudaLaunchKernelEx(&lc, qgemm_mx_kernel<F, BN, TWO, TALL, A4, NV>, mhi, mlo, mw, prm);
 }
 
 template <int F>
@@ -910,6 +967,17 @@ inline size_t a4_codes_bytes(int64_t M, int64_t K) { return align1k(size_t(M) * 
 inline size_t a4_workspace_bytes(int64_t M, int64_t K) {
   return a4_codes_bytes(M, K) + align1k(size_t((M + BM - 1) / BM) * size_t(K / BK) * SF_BYTES);
 }
+// nvfp4: codes, scale atoms of 64 K each, then the quantizer's partial maxima
+// and, in the last word of that part, the activation's global.
+inline size_t nv_atoms_bytes(int64_t M, int64_t K) {
+  return align1k(size_t((M + BM - 1) / BM) * size_t(K / 64) * SF_BYTES);
+}
+inline size_t nv_global_offset(int64_t M, int64_t K) {
+  return a4_codes_bytes(M, K) + nv_atoms_bytes(M, K) + 4 * 1024;
+}
+inline size_t nv_workspace_bytes(int64_t M, int64_t K) {
+  return a4_codes_bytes(M, K) + nv_atoms_bytes(M, K) + align1k(4 * 1025);
+}
 
 static cudaError_t launch_a4(const void* codes, const void* scales, const void* x, void* out, bool out_f32, int M,
                              int N, int K, void* ws, cudaStream_t st, int sms) {
@@ -955,6 +1023,50 @@ static cudaError_t launch_a4(const void* codes, const void* scales, const void* 
   }
   if (pl.BN == 224) return launch_tile<MXFP4, 224, false, false, true>(mx4, mx4, mw, prm, M, N, pl.S, st);
   return launch_tile<MXFP4, 256, false, false, true>(mx4, mx4, mw, prm, M, N, pl.S, st);
+}
+
+// The all-FP4 product over nvfp4 weights: X packed to NVFP4 (the packer's
+// rule over the whole X: two kernels, the amax then the codes), single tiles.
+static cudaError_t launch_a4_nv(const void* codes, const void* scales, float gw, const void* x, void* out,
+                                bool out_f32, int M, int N, int K, void* ws, cudaStream_t st, int sms) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = set_smem<NVFP4, 256, false, false, true, true>(dev)) != cudaSuccess ||
+      (e = set_smem<NVFP4, 224, false, false, true, true>(dev)) != cudaSuccess)
+    return e;
+  const int nk = K / (2 * BK);
+  MxPlan pl = plan_mx<MXFP4>(dev, M, N, K / 2, sms > 0 ? sms : 1);
+  if (g_force_bn.load() == 224 || g_force_bn.load() == 256) pl.BN = g_force_bn.load();
+  const int fs = g_force_s.load();
+  if (fs >= 1 && fs <= 4 && (fs - 1) * ((nk + fs - 1) / fs) < nk) pl.S = fs;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  uint8_t* atoms = w8 + a4_codes_bytes(M, K);
+  float* partials = reinterpret_cast<float*>(atoms + nv_atoms_bytes(M, K));
+  float* gx = reinterpret_cast<float*>(w8 + nv_global_offset(M, K));
+  if ((e = launch_quantize_nvfp4_atoms(x, w8, atoms, partials, gx, M, K, st)) != cudaSuccess) return e;
+  CUtensorMap mx4, mw;
+  if (!make_map(enc, &mx4, CU_TENSOR_MAP_DATA_TYPE_UINT8, w8, K / 2, M, K / 2, BM) ||
+      !make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, N, K / 2, uint32_t(pl.BN)))
+    return cudaErrorInvalidValue;
+  MxParams prm{};
+  prm.wscales = static_cast<const uint8_t*>(scales);
+  prm.sf_hi = atoms;
+  prm.sf_lo = atoms;
+  prm.out = out;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.out_f32 = out_f32 ? 1 : 0;
+  prm.kb_per = nk;
+  prm.limit_ns = g_limit_ns.load();
+  prm.drop_arrivals = g_drop.load();
+  prm.gw = gw;
+  prm.gx = gx;
+  if (pl.BN == 224) return launch_tile<NVFP4, 224, false, false, true, true>(mx4, mx4, mw, prm, M, N, pl.S, st);
+  return launch_tile<NVFP4, 256, false, false, true, true>(mx4, mx4, mw, prm, M, N, pl.S, st);
 }
 
 // ------------------------------------------------- expert-grouped rows ---
@@ -1441,10 +1553,15 @@ cudaError_t launch_qgemm_a8(int fmt, const void* codes, const void* scales, cons
   }
 }
 
-size_t qgemm_a4_workspace_bytes(int64_t M, int64_t K) { return mx::a4_workspace_bytes(M, K); }
+size_t qgemm_a4_workspace_bytes(int fmt, int64_t M, int64_t K) {
+  return fmt == NVFP4 ? mx::nv_workspace_bytes(M, K) : mx::a4_workspace_bytes(M, K);
+}
 
-cudaError_t launch_qgemm_a4(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,
-                            int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st, int sms) {
+cudaError_t launch_qgemm_a4(int fmt, const void* codes, const void* scales, float global_scale, const void* x,
+                            void* out, bool out_f32, int64_t M, int64_t N, int64_t K, void* workspace, cudaStream_t st,
+                            int sms) {
+  if (fmt == NVFP4)
+    return mx::launch_a4_nv(codes, scales, global_scale, x, out, out_f32, int(M), int(N), int(K), workspace, st, sms);
   if (fmt != MXFP4) return cudaErrorInvalidValue;
   return mx::launch_a4(codes, scales, x, out, out_f32, int(M), int(N), int(K), workspace, st, sms);
 }

@@ -153,6 +153,131 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   }
 }
 
+// ---- NVFP4 activations (the all-FP4 product over nvfp4 weights) ----------
+//
+// The packer's nvfp4 rule over the whole X as one tensor: global g =
+// amax(X) / (6 * 448) (1.0 for a zero X); per block of 16, t = (amax / 6) / g
+// in float32, its E4M3 code by nearest-even saturating conversion (a zero
+// block: 0x38 = 1.0), eff = E4M3(code) * g, codes = E2M1(x / eff) (eff = 0:
+// code 0).  Two kernels: per-CTA maxima of |x|, then (every CTA reducing the
+// maxima) the codes and the scale atoms; CTA 0 stores g.  A non-finite X
+// makes g, hence every output, NaN.
+
+constexpr int NV_PARTIALS = 1024;
+
+// CTA c takes rows c, c + gridDim.x, ...: the largest |x| it saw.
+__global__ void __launch_bounds__(256) amax_partial_kernel(const __nv_bfloat16* __restrict__ x, int M, int K,
+                                                           float* __restrict__ partial) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float red[8];
+  float a = 0.0f;
+  bool finite = true;
+  const int chunks = K / 8;                                   // 16-byte chunks of a row
+  for (int m = blockIdx.x; m < M; m += gridDim.x) {
+    const uint4* row = reinterpret_cast<const uint4*>(x + int64_t(m) * K);
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+      const uint4 v = __ldg(row + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      #pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = fabsf(__uint_as_float(w[j] << 16)), hi = fabsf(__uint_as_float(w[j] & 0xFFFF0000u));
+        finite &= lo <= 3.4028235e38f && hi <= 3.4028235e38f;  // false for an infinity or a NaN
+        a = fmaxf(a, fmaxf(lo, hi));
+      }
+    }
+  }
+  if (!finite) a = __uint_as_float(0x7FC00000u);
+  #pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    const float o = __shfl_xor_sync(0xFFFFFFFFu, a, d);
+    a = (a != a || o != o) ? __uint_as_float(0x7FC00000u) : fmaxf(a, o);
+  }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = red[0];
+    for (int i = 1; i < int(blockDim.x >> 5); ++i) r = (r != r || red[i] != red[i]) ? __uint_as_float(0x7FC00000u) : fmaxf(r, red[i]);
+    partial[blockIdx.x] = r;
+  }
+}
+
+// Codes [M, K/2] and E4M3 scales in 512-byte atoms (128 rows x 4 blocks of
+// 16: a 32-bit cell covers 64 K); one thread per 32 values (two blocks), a
+// warp per row and 1,024 columns; rows past M up to the 128-row tile get
+// neutral scales (1.0).  `nparts` maxima from amax_partial_kernel.
+__global__ void __launch_bounds__(256) quantize_nv_atoms_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                uint8_t* __restrict__ codes,
+                                                                uint8_t* __restrict__ atoms,
+                                                                const float* __restrict__ partial, int nparts,
+                                                                float* __restrict__ g_out, int M, int K) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float red[8];
+  __shared__ float gsh;
+  float a = 0.0f;
+  for (int i = threadIdx.x; i < nparts; i += blockDim.x) {
+    const float v = __ldg(partial + i);
+    a = (a != a || v != v) ? __uint_as_float(0x7FC00000u) : fmaxf(a, v);
+  }
+  #pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    const float o = __shfl_xor_sync(0xFFFFFFFFu, a, d);
+    a = (a != a || o != o) ? __uint_as_float(0x7FC00000u) : fmaxf(a, o);
+  }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = red[0];
+    for (int i = 1; i < int(blockDim.x >> 5); ++i) r = (r != r || red[i] != red[i]) ? __uint_as_float(0x7FC00000u) : fmaxf(r, red[i]);
+    const float g = r != r ? r : (r > 0.0f ? __fdiv_rn(r, 2688.0f) : 1.0f);
+    gsh = g;
+    if (blockIdx.x == 0) *g_out = g;
+  }
+  __syncthreads();
+  const float g = gsh;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nchunk = K / 32, chunks = (nchunk + 31) / 32;
+  const int rows = (M + 127) / 128 * 128;
+  const int m = warp / chunks, b = (warp - m * chunks) * 32 + lane;   // b: 32-value chunk of the row
+  if (m >= rows || b >= nchunk) return;
+  uint32_t sc[2] = {0x38u, 0x38u};
+  if (m < M) {
+    float v[32];
+    load32<false>(x, m, K, b, v);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    #pragma unroll
+    for (int h = 0; h < 2; ++h) {                               // the two blocks of 16
+      float amax = 0.0f;
+      #pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[16 * h + i]));
+      uint32_t code = 0x38u;
+      if (amax > 0.0f) {
+        const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+        uint16_t two;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(two) : "f"(0.0f), "f"(t));
+        code = two & 0xFFu;
+      }
+      if (h) sc[1] = code;
+      else sc[0] = code;
+      const float eff = __fmul_rn(e4m3_f32(code), g);
+      #pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t byte = eff == 0.0f ? 0u
+                                          : Elem<MXFP4>::pair(__fdiv_rn(v[16 * h + 2 * i], eff),
+                                                              __fdiv_rn(v[16 * h + 2 * i + 1], eff));
+        w[2 * h + i / 4] |= byte << (8 * (i % 4));
+      }
+    }
+    *reinterpret_cast<uint4*>(codes + int64_t(m) * (K / 2) + 16 * int64_t(b)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  // blocks 2b, 2b + 1: bytes (2b) % 4, (2b + 1) % 4 of cell (2b) / 4
+  const size_t atom = size_t(m / 128) * size_t(K / 64) + size_t(b / 2);
+  uint8_t* cell = atoms + atom * 512 + umma::sf_atom_offset(uint32_t(m % 128), uint32_t((2 * b) & 3));
+  cell[0] = uint8_t(sc[0]);
+  cell[1] = uint8_t(sc[1]);
+}
+
 template <int F, bool IN_F32, bool ATOMS>
 static cudaError_t launch(const void* x, void* codes, void* scales, int M, int K, cudaStream_t st) {
   const int rows = ATOMS ? (M + 127) / 128 * 128 : M;
@@ -197,6 +322,31 @@ cudaError_t launch_quantize_e4m3_atoms(const void* x, void* codes, void* atoms, 
 cudaError_t launch_quantize_mxfp4_atoms(const void* x, void* codes, void* atoms, int64_t M, int64_t K,
                                         cudaStream_t st) {
   return quant::launch<MXFP4, false, true>(x, codes, atoms, int(M), int(K), st);
+}
+
+int quantize_nvfp4_partials(int64_t M) { return int(M < quant::NV_PARTIALS ? M : quant::NV_PARTIALS); }
+
+cudaError_t launch_quantize_nvfp4_atoms(const void* x, void* codes, void* atoms, float* partials, float* g_out,
+                                        int64_t M, int64_t K, cudaStream_t st) {
+  const int m = int(M), k = int(K), np = quantize_nvfp4_partials(M);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(unsigned(np));
+  lc.blockDim = dim3(256);
+  lc.stream = st;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&lc, quant::amax_partial_kernel, static_cast<const __nv_bfloat16*>(x), m, k,
+                                     partials);
+  if (e != cudaSuccess) return e;
+  const int rows = (m + 127) / 128 * 128;
+  const int64_t warps = int64_t(rows) * ((k / 32 + 31) / 32);
+  lc.gridDim = dim3(unsigned((warps + 7) / 8));
+  return cudaLaunchKernelEx(&lc, quant::quantize_nv_atoms_kernel, static_cast<const __nv_bfloat16*>(x),
+                            static_cast<uint8_t*>(codes), static_cast<uint8_t*>(atoms),
+                            static_cast<const float*>(partials), np, g_out, m, k);
 }
 
 }  // namespace qfmt_dev

@@ -42,6 +42,13 @@ QFMT_HD constexpr uint32_t idesc_mxf4(uint32_t m, uint32_t n, uint32_t sfa_id, u
   return idesc_mxf8f6f4(MXF4_E2M1, MXF4_E2M1, m, n, sfa_id, sfb_id);
 }
 
+// kind::mxf4nvf4.block_scale.scale_vec::4X: both operands E2M1 packed, K = 64
+// an instruction, one UE4M3 scale per 16 values (bit 23 = 0), so each
+// instruction reads all four bytes of every row's 32-bit scale cell (id 0).
+QFMT_HD constexpr uint32_t idesc_mxf4nvf4(uint32_t m, uint32_t n) {
+  return idesc_mxf8f6f4(MXF4_E2M1, MXF4_E2M1, m, n, 0u, 0u) & ~(1u << 23);
+}
+
 // Instruction descriptor of tcgen05.mma ... kind::f16: float32 accumulator
 // (bits 4-5 = 1), A and B bf16 (bits 7-9 and 10-12 = 1), both K-major,
 // N >> 3 at bit 17, M >> 4 at bit 24.

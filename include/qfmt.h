@@ -286,26 +286,36 @@ size_t qmm_a8_workspace_bytes(int fmt, int64_t M, int64_t K);
 /*
  * qmm_a4 -- device, the all-FP4 product (rlx-cpu thunk/ops/quant.rs
  * lowp_quantize on the activation, then lowp_scaled_matmul; metaltile PR
- * #250 names Blackwell tcgen05 scaled MMA over its MXFP formats):
+ * #250 names Blackwell tcgen05 scaled MMA over its MXFP / NVFP formats):
  *   out[M, N] = Q4(X) . dequant(W)^T
- * with Q4(X) the activation packed to MXFP4 (E2M1 codes, E8M0 scale per 32)
- * as qfmt_quantize packs it, and W mxfp4.  Both operands enter one
- * tcgen05.mma kind::mxf4 per 64 K packed two codes to a byte, as stored.
- * The activation carries E2M1's rounding (up to 2^-2 of each value
- * relative to its block's largest), a different product from qmm's.  Result
- * within 2^-12 * sum_k |q4(x)||w| + 1e-6 of the exact Q4(X) . W^T (float32
- * accumulation).  x bf16 [M, K]; out bf16 or float32 per out_dtype; K a
- * multiple of 256 (else QFMT_ESHAPE); another weight format gives
- * QFMT_EUNSUPPORTED; workspace of at least qmm_a4_workspace_bytes(fmt, M, K)
- * bytes, 128-byte aligned, else QFMT_ENOSPACE (scratch: ordered on one stream
- * between calls); codes 16-byte and scales 8-byte aligned.  Any M >= 1.
- * Asynchronous on `stream`.
+ * with Q4(X) the activation packed in W's FP4 family by the packer's rule:
+ *   - W mxfp4: X as MXFP4 (E2M1 codes, E8M0 scale per 32, as qfmt_quantize
+ *     packs it); one tcgen05.mma kind::mxf4 per 64 K;
+ *   - W nvfp4 (global_scale its global): X as NVFP4 over the whole X as one
+ *     tensor (its own global amax(X) / (6 * 448), an E4M3 scale per 16, E2M1
+ *     codes); one kind::mxf4nvf4 per 64 K, the output times both globals.
+ *     A non-finite X gives NaN outputs.
+ * Both operands enter the tensor cores packed two codes to a byte, as stored.
+ * The activation carries E2M1's rounding (one mantissa bit), a different
+ * product from qmm's.  Result within 2^-12 * sum_k |q4(x)||w| + 1e-6 of the
+ * exact Q4(X) . W^T (float32 accumulation).  x bf16 [M, K]; out bf16 or
+ * float32 per out_dtype; K a multiple of 256 (else QFMT_ESHAPE); another
+ * weight format gives QFMT_EUNSUPPORTED; global_scale is read for nvfp4 only.
+ * Workspace of at least qmm_a4_workspace_bytes(fmt, M, K) bytes, 128-byte
+ * aligned, else QFMT_ENOSPACE (scratch: ordered on one stream between calls);
+ * after the call it holds Q4(X): the codes [M, K/2] at offset 0, then (1 KiB
+ * aligned) the scales in 512-byte atoms of 128 rows x 4 blocks (16-byte chunk
+ * r % 32 holds rows r, r + 32, r + 64, r + 96, byte j of each 4-byte word is
+ * block j of the atom's 4), atoms ordered by 128-row tile then along K; for
+ * nvfp4 then (1 KiB aligned) 1,024 float32 words of scratch and the
+ * activation's global.  codes 16-byte, scales 8-byte (nvfp4: 16-byte)
+ * aligned.  Any M >= 1.  Asynchronous on `stream`.
  */
-int qmm_a4(int fmt, const void* codes, const void* scales, const void* x, void* out, int out_dtype, int64_t M,
-           int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream);
-/* Workspace bytes of qmm_a4: align(M K / 2) + align(M' K / 32), M' = M
- * rounded up to 128, each part 1 KiB aligned; 0 for another format or K not a
- * positive multiple of 256. */
+int qmm_a4(int fmt, const void* codes, const void* scales, float global_scale, const void* x, void* out,
+           int out_dtype, int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream);
+/* Workspace bytes of qmm_a4: align(M K / 2) + align(M' K / 32) (mxfp4) or
+ * align(M' K / 16) + align(4100) (nvfp4), M' = M rounded up to 128, each part
+ * 1 KiB aligned; 0 for another format or K not a positive multiple of 256. */
 size_t qmm_a4_workspace_bytes(int fmt, int64_t M, int64_t K);
 
 /*

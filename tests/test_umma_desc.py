@@ -3,7 +3,7 @@
 The header is plain C++: a small host program built here with g++ prints
 each encoder's output for a set of arguments, and every field is checked
 against the bit positions the PTX ISA's tcgen05 sections give (instruction
-descriptor of kind::f16, kind::mxf8f6f4 and kind::mxf4 with block scaling; shared-memory
+descriptor of kind::f16, kind::mxf8f6f4, kind::mxf4 and kind::mxf4nvf4 with block scaling; shared-memory
 matrix descriptor), restated below field by field.  A wrong shift or mask in
 the encoder fails here before any kernel built on it runs on a GPU.
 """
@@ -29,6 +29,8 @@ int main() {
         std::printf("mx %u %u %u %u %u %u %u\n", a, b, m, n, sa, sb, idesc_mxf8f6f4(a, b, m, n, sa, sb));
   for (unsigned m : {64u, 128u}) for (unsigned n : {8u, 224u, 256u}) for (unsigned sa : {0u, 2u})
     for (unsigned sb : {0u, 2u}) std::printf("m4 %u %u %u %u %u\n", m, n, sa, sb, idesc_mxf4(m, n, sa, sb));
+  for (unsigned m : {64u, 128u}) for (unsigned n : {8u, 224u, 256u})
+    std::printf("n4 %u %u %u\n", m, n, idesc_mxf4nvf4(m, n));
   for (unsigned m : {64u, 128u}) for (unsigned n : {16u, 128u, 224u, 256u})
     std::printf("bf %u %u %u\n", m, n, idesc_bf16(m, n));
   for (unsigned addr : {0u, 1024u, 0x12340u, 0x3FFF0u})
@@ -95,6 +97,16 @@ def test_mxf4_instruction_descriptor(encoded):
         assert bits(d, 7, 3) == 1 and bits(d, 10, 3) == 1 and bits(d, 13, 4) == 0
         assert bits(d, 17, 6) == n >> 3 and bits(d, 23, 1) == 1 and bits(d, 24, 5) == m >> 4
         assert bits(d, 29, 2) == sa and bits(d, 31, 1) == 0
+
+
+def test_mxf4nvf4_instruction_descriptor(encoded):
+    # kind::mxf4nvf4 (scale_vec::4X): both types E2M1 (1), scale type UE4M3
+    # (bit 23 = 0), both scale-factor ids 0 (the instruction reads the whole cell)
+    assert len(encoded["n4"]) == 2 * 3
+    for m, n, d in encoded["n4"]:
+        assert bits(d, 0, 7) == 0 and bits(d, 7, 3) == 1 and bits(d, 10, 3) == 1 and bits(d, 13, 4) == 0
+        assert bits(d, 17, 6) == n >> 3 and bits(d, 23, 1) == 0 and bits(d, 24, 5) == m >> 4
+        assert bits(d, 29, 3) == 0
 
 
 def test_bf16_instruction_descriptor(encoded):

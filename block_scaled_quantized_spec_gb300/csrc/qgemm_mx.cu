@@ -78,7 +78,7 @@ constexpr int SF_STAGE = 4 * SF_BYTES;        // hi atom, lo atom, two W atoms (
 constexpr int SF_STAGE_A4 = 8 * SF_BYTES;     // all-FP4 form: two K atoms each of two X tiles and two W row groups
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGES * SF_STAGE + 256;
 constexpr int SMEM_BYTES_A4 = 1024 + STAGES * STAGE_BYTES + STAGES * SF_STAGE_A4 + 256;
-constexpr int SF_STAGE_NV = 12 * SF_BYTES;    // nvfp4 all-FP4: four K atoms of the X tile, eight of W
+constexpr int SF_STAGE_NV = 16 * SF_BYTES;    // nvfp4 all-FP4: four K atoms of each X tile, eight of W
 constexpr int SMEM_BYTES_NV = 1024 + STAGES * STAGE_BYTES + STAGES * SF_STAGE_NV + 256;
 constexpr int THREADS = 256;
 constexpr int TMEM_COLS = 512;                // accumulator 256 columns + 16 scale columns a stage
@@ -325,9 +325,11 @@ template <int F> constexpr uint32_t b_type() {
 // scales per 16 values.  A K step carries 16 blocks a row: four scale cells,
 // so four K atoms for the X tile and eight for W (48 columns a slot at 256 +
 // 48 s: X at +0 .. +15, then W's row groups 0 and 1 of K atom a at +16 + 8a
-// and +20 + 8a); each MMA reads a whole cell.  Single 128-row tiles only (a
-// tall tile's 64 scale columns a step would leave one slot).  The epilogue
-// multiplies by the two tensors' globals.
+// and +20 + 8a); each MMA reads a whole cell.  With tall tiles a step's 64
+// scale columns fit once, split over the two gaps beside the accumulators
+// (X tiles at 224 .. 255, W at 480 .. 511): the slot is refilled after the
+// MMAs of the step before have completed.  The epilogue multiplies by the two
+// tensors' globals.
 // A K split runs its splits as a cluster along z; each split's float32
 // partial tile goes to its drained stage memory and the cluster sums them
 // through distributed shared memory in rank order.
@@ -339,13 +341,14 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
   static_assert(BN % 32 == 0 && BN <= BN_MAX && BN > 128, "two W scale atoms a stage");
   static_assert(!TALL || (!TWO && BN == 224), "tall tiles: one term, 224 columns");
   static_assert(!A4 || (!TWO && F == (NV ? NVFP4 : MXFP4)), "the all-FP4 form: one E2M1 activation term");
-  static_assert(!NV || (A4 && !TALL), "the NVFP4 form: single tiles");
+  static_assert(!NV || A4, "the NVFP4 form is an all-FP4 form");
   // bytes a stage's copies deliver: the two X tiles (terms, or M halves), the
   // W codes (E2M1 through 16U4_ALIGN16B: the 8 data bytes of every 16-byte
   // unit, the gaps are not written; packed A4 tiles: every byte) and the X
   // scale atoms (A4: two K atoms a tile)
   constexpr int TERMS = (TWO || TALL) ? 2 : 1;
   constexpr int XA = NV ? 4 : (A4 ? 2 : 1);
+  constexpr int X2 = NV ? 12 : XA;                  // scale atoms of the second X tile (NV: after W's)
   constexpr int SFS = NV ? SF_STAGE_NV : (A4 ? SF_STAGE_A4 : SF_STAGE);
   constexpr uint32_t TX_BYTES =
       TERMS * (A_BYTES + XA * SF_BYTES) + ((F == MXFP4 && !A4) ? BN * BK / 2 : BN * BK);
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
         if constexpr (TALL) tma_load_2d(a_lo(s), &xhi_map, j * BK, m0 + BM, full(s));   // the second M half
         tma_load_2d(b_tile(s), &w_map, j * BK, wrow0 + n0, full(s));
         bulk_load(sf_s(s, 0), sfh + size_t(j) * XA * SF_BYTES, XA * SF_BYTES, full(s));
-        if constexpr (TWO || TALL) bulk_load(sf_s(s, XA), sfl + size_t(j) * XA * SF_BYTES, XA * SF_BYTES, full(s));
+        if constexpr (TWO || TALL) bulk_load(sf_s(s, X2), sfl + size_t(j) * XA * SF_BYTES, XA * SF_BYTES, full(s));
         issued = i + 1;
       }
       // every issued copy lands before the CTA may exit
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     const bool leader = elect_one();
     constexpr uint32_t BT = b_type<F>();
     // scale slots in tensor memory: one a stage, but two for A4 tall tiles
-    constexpr int SLOTS = (A4 && TALL) ? 2 : STAGES;
+    constexpr int SLOTS = (A4 && TALL) ? (NV ? 1 : 2) : STAGES;
     for (int i = 0; i < nloc; ++i) {
       const int s = i % STAGES;
       const uint32_t ph = (i / STAGES) & 1;
@@ -484,7 +487,25 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
       tc_fence_after();
       const uint64_t dh = desc_sw128(a_hi(s)), dl = desc_sw128(a_lo(s)), db = desc_sw128(b_tile(s));
       if (leader) {
-        if constexpr (NV) {
+        if constexpr (NV && TALL) {
+          // X tile 0 atoms at 224 + 4a, tile 1 at 240 + 4a, W (row group g, K atom a) at 480 + 8a + 4g
+          const uint32_t xs = tmem + 224u, wsl = tmem + 480u;
+          #pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            tmem_cp_sf(xs + uint32_t(4 * a), umma::smem_desc_sf32x16(sf_s(s, a)));
+            tmem_cp_sf(xs + uint32_t(16 + 4 * a), umma::smem_desc_sf32x16(sf_s(s, 12 + a)));
+          }
+          #pragma unroll
+          for (int a = 0; a < 8; ++a) tmem_cp_sf(wsl + uint32_t(4 * a), umma::smem_desc_sf32x16(sf_s(s, 4 + a)));
+          constexpr uint32_t id = umma::idesc_mxf4nvf4(BM, BN);
+          #pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {   // K 64 (+32 bytes) an instruction: the whole cell of K atom kk
+            mma_mxf4nvf4(tmem, dh + uint64_t(2 * kk), db + uint64_t(2 * kk), id, xs + 4u * kk, wsl + 8u * kk,
+                         (i | kk) != 0);
+            mma_mxf4nvf4(tmem + 256u, dl + uint64_t(2 * kk), db + uint64_t(2 * kk), id, xs + 16u + 4u * kk,
+                         wsl + 8u * kk, (i | kk) != 0);
+          }
+        } else if constexpr (NV) {
           const uint32_t slot = tmem + uint32_t(BN_MAX + 48 * s);
           #pragma unroll
           for (int a = 0; a < 12; ++a) tmem_cp_sf(slot + uint32_t(4 * a), umma::smem_desc_sf32x16(sf_s(s, a)));
@@ -1042,6 +1063,10 @@ static cudaError_t launch_a4_nv(const void* codes, const void* scales, float gw,
   if (g_force_bn.load() == 224 || g_force_bn.load() == 256) pl.BN = g_force_bn.load();
   const int fs = g_force_s.load();
   if (fs >= 1 && fs <= 4 && (fs - 1) * ((nk + fs - 1) / fs) < nk) pl.S = fs;
+  // tall tiles (one scale slot, see the kernel) where they still give every SM a tile
+  const int ft = g_force_tall.load();
+  const int64_t tall_ctas = int64_t((N + 223) / 224) * ((M + 2 * BM - 1) / (2 * BM));
+  const bool tall = ft != 1 && pl.S == 1 && M > BM && (ft == 2 || tall_ctas >= int64_t(sms > 0 ? sms : 1));
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   uint8_t* atoms = w8 + a4_codes_bytes(M, K);
   float* partials = reinterpret_cast<float*>(atoms + nv_atoms_bytes(M, K));
@@ -1049,7 +1074,7 @@ static cudaError_t launch_a4_nv(const void* codes, const void* scales, float gw,
   if ((e = launch_quantize_nvfp4_atoms(x, w8, atoms, partials, gx, M, K, st)) != cudaSuccess) return e;
   CUtensorMap mx4, mw;
   if (!make_map(enc, &mx4, CU_TENSOR_MAP_DATA_TYPE_UINT8, w8, K / 2, M, K / 2, BM) ||
-      !make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, N, K / 2, uint32_t(pl.BN)))
+      !make_map(enc, &mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, N, K / 2, tall ? 224u : uint32_t(pl.BN)))
     return cudaErrorInvalidValue;
   MxParams prm{};
   prm.wscales = static_cast<const uint8_t*>(scales);
@@ -1065,6 +1090,10 @@ static cudaError_t launch_a4_nv(const void* codes, const void* scales, float gw,
   prm.drop_arrivals = g_drop.load();
   prm.gw = gw;
   prm.gx = gx;
+  if (tall) {
+    if ((e = set_smem<NVFP4, 224, false, true, true, true>(dev)) != cudaSuccess) return e;
+    return launch_tile<NVFP4, 224, false, true, true, true>(mx4, mx4, mw, prm, M, N, 1, st);
+  }
   if (pl.BN == 224) return launch_tile<NVFP4, 224, false, false, true, true>(mx4, mx4, mw, prm, M, N, pl.S, st);
   return launch_tile<NVFP4, 256, false, false, true, true>(mx4, mx4, mw, prm, M, N, pl.S, st);
 }

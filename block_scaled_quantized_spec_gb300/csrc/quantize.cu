@@ -261,11 +261,24 @@ __global__ void __launch_bounds__(256) quantize_nv_atoms_kernel(const __nv_bfloa
       if (h) sc[1] = code;
       else sc[0] = code;
       const float eff = __fmul_rn(e4m3_f32(code), g);
+      // The code of float32(x / eff) without a division per value: q = x * r
+      // (r the rounded reciprocal) is within 3 * 2^-24 of float32(x / eff),
+      // relative; the E2M1 rounding is monotone, so where q (1 - 2^-20) and
+      // q (1 + 2^-20) take the same code, that is the code (a tie, i.e. a
+      // quotient on a midpoint, always falls between them).  Otherwise, and
+      // for a non-finite q, the pair is divided.
+      const float r = __frcp_rn(eff);
       #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint32_t byte = eff == 0.0f ? 0u
-                                          : Elem<MXFP4>::pair(__fdiv_rn(v[16 * h + 2 * i], eff),
-                                                              __fdiv_rn(v[16 * h + 2 * i + 1], eff));
+        const float a = v[16 * h + 2 * i], b = v[16 * h + 2 * i + 1];
+        uint32_t byte = 0u;
+        if (eff != 0.0f) {
+          const float qa = __fmul_rn(a, r), qb = __fmul_rn(b, r);
+          const uint32_t lo = Elem<MXFP4>::pair(__fmul_rn(qa, 1.0f - 0x1p-20f), __fmul_rn(qb, 1.0f - 0x1p-20f));
+          const uint32_t hi = Elem<MXFP4>::pair(__fmul_rn(qa, 1.0f + 0x1p-20f), __fmul_rn(qb, 1.0f + 0x1p-20f));
+          const bool fin = fabsf(qa) <= 3.4028235e38f && fabsf(qb) <= 3.4028235e38f;
+          byte = (lo == hi && fin) ? lo : Elem<MXFP4>::pair(__fdiv_rn(a, eff), __fdiv_rn(b, eff));
+        }
         w[2 * h + i / 4] |= byte << (8 * (i % 4));
       }
     }

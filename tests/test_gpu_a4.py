@@ -6,8 +6,8 @@ both operands enter the tensor cores packed two codes to a byte (kind::mxf4,
 kind::mxf4nvf4); the result must lie within the float32-accumulation bound
 2^-12 sum |q4(x)||w| + 1e-6 of the oracle's exact Q4(X) . W^T (plus the bf16
 output's half ulp), element by element.  The forms covered: single 128-row
-tiles at both widths, tall 256-row tiles (mxfp4: two accumulators, two scale
-slots in tensor memory refilled behind the MMAs), K splits over a cluster,
+tiles at both widths, tall 256-row tiles (two accumulators; two scale slots
+in tensor memory for mxfp4, one for nvfp4, refilled behind the MMAs), K splits over a cluster,
 ragged M and N, float32 output, an expired wait; and the quantized
 activation the call leaves in its workspace, byte for byte against the
 oracle's packer.
@@ -122,15 +122,15 @@ def test_qmm_a4_quantized_activation_bit_exact(fmt, m, k):
     assert np.array_equal(got_c, want_c), (fmt, np.argwhere(got_c != want_c)[:5].tolist())
 
 
+@pytest.mark.parametrize("fmt", FP4)
 @pytest.mark.parametrize("m,n,k", [(300, 5000, 512), (1000, 700, 1024), (129, 2300, 256), (777, 450, 2048)])
-def test_qmm_a4_tall_tiles(m, n, k):
-    # mxfp4: 256-row tiles forced on and off (debug key 9) without a K split
-    # (key 4): the last tile's second M half wholly past M (m = 300), ending
-    # inside it (1000, 777) or holding one row (129); K = 256 is one step and
-    # 2048 eight, so the two tensor-memory scale slots wrap several times;
-    # against the oracle, and bit for bit against single tiles (the same
-    # accumulation order)
-    fmt = "mxfp4"
+def test_qmm_a4_tall_tiles(fmt, m, n, k):
+    # 256-row tiles forced on and off (debug key 9) without a K split (key
+    # 4): the last tile's second M half wholly past M (m = 300), ending inside
+    # it (1000, 777) or holding one row (129); K = 256 is one step and 2048
+    # eight, so the tensor-memory scale slots (two for mxfp4, one for nvfp4)
+    # are refilled several times; against the oracle, and bit for bit against
+    # single tiles (the same accumulation order)
     c, s, g, xb, xt = _case(fmt, m, n, k, seed=m + 5)
     dc, ds = _dev(c), _dev(s)
     ref, bound = oref.qmm_a4_ref(fmt, c, s, g, xb, "bf16", m, n, k)

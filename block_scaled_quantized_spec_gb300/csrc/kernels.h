@@ -88,9 +88,9 @@ cudaError_t launch_quantize_e4m3_atoms(const void* x, void* codes, void* atoms, 
 cudaError_t launch_quantize_mxfp4_atoms(const void* x, void* codes, void* atoms, int64_t M, int64_t K,
                                         cudaStream_t st);
 // NVFP4 activations for the all-FP4 product over nvfp4: per-CTA maxima of |x|
-// into `partials` (quantize_nvfp4_partials(M) floats), then codes [M, K/2],
+// into `partials` (quantize_nvfp4_partials(M, K) <= 1024 floats), then codes [M, K/2],
 // E4M3 scale atoms (4 blocks of 16 a cell) and the global into *g_out.
-int quantize_nvfp4_partials(int64_t M);
+int quantize_nvfp4_partials(int64_t M, int64_t K);
 cudaError_t launch_quantize_nvfp4_atoms(const void* x, void* codes, void* atoms, float* partials, float* g_out,
                                         int64_t M, int64_t K, cudaStream_t st);
 cudaError_t launch_qgemv_mx(int fmt, const void* codes, const void* scales, const void* x, void* out, bool out_f32,

@@ -165,7 +165,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
 
 constexpr int NV_PARTIALS = 1024;
 
-// CTA c takes rows c, c + gridDim.x, ...: the largest |x| it saw.
+// CTA c's largest |x| over the 16-byte chunks of X taken grid-stride (X is
+// [M, K] contiguous), four independent loads in flight a thread.
 __global__ void __launch_bounds__(256) amax_partial_kernel(const __nv_bfloat16* __restrict__ x, int M, int K,
                                                            float* __restrict__ partial) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -173,20 +174,27 @@ __global__ void __launch_bounds__(256) amax_partial_kernel(const __nv_bfloat16* 
   __shared__ float red[8];
   float a = 0.0f;
   bool finite = true;
-  const int chunks = K / 8;                                   // 16-byte chunks of a row
-  for (int m = blockIdx.x; m < M; m += gridDim.x) {
-    const uint4* row = reinterpret_cast<const uint4*>(x + int64_t(m) * K);
-    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
-      const uint4 v = __ldg(row + c);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float lo = fabsf(__uint_as_float(w[j] << 16)), hi = fabsf(__uint_as_float(w[j] & 0xFFFF0000u));
-        finite &= lo <= 3.4028235e38f && hi <= 3.4028235e38f;  // false for an infinity or a NaN
-        a = fmaxf(a, fmaxf(lo, hi));
-      }
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  const int64_t chunks = int64_t(M) * (K / 8), stride = int64_t(gridDim.x) * blockDim.x;
+  auto take = [&](const uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = fabsf(__uint_as_float(w[j] << 16)), hi = fabsf(__uint_as_float(w[j] & 0xFFFF0000u));
+      finite &= lo <= 3.4028235e38f && hi <= 3.4028235e38f;   // false for an infinity or a NaN
+      a = fmaxf(a, fmaxf(lo, hi));
     }
+  };
+  int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; c + 3 * stride < chunks; c += 4 * stride) {
+    const uint4 v0 = __ldg(xv + c), v1 = __ldg(xv + c + stride), v2 = __ldg(xv + c + 2 * stride),
+                v3 = __ldg(xv + c + 3 * stride);
+    take(v0);
+    take(v1);
+    take(v2);
+    take(v3);
   }
+  for (; c < chunks; c += stride) take(__ldg(xv + c));
   if (!finite) a = __uint_as_float(0x7FC00000u);
   #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
@@ -337,11 +345,15 @@ cudaError_t launch_quantize_mxfp4_atoms(const void* x, void* codes, void* atoms,
   return quant::launch<MXFP4, false, true>(x, codes, atoms, int(M), int(K), st);
 }
 
-int quantize_nvfp4_partials(int64_t M) { return int(M < quant::NV_PARTIALS ? M : quant::NV_PARTIALS); }
+// CTAs of the maxima pass: ~16 KiB of X each, at most NV_PARTIALS
+int quantize_nvfp4_partials(int64_t M, int64_t K) {
+  const int64_t c = (M * K * 2 + 16383) / 16384;
+  return int(c < quant::NV_PARTIALS ? (c > 0 ? c : 1) : quant::NV_PARTIALS);
+}
 
 cudaError_t launch_quantize_nvfp4_atoms(const void* x, void* codes, void* atoms, float* partials, float* g_out,
                                         int64_t M, int64_t K, cudaStream_t st) {
-  const int m = int(M), k = int(K), np = quantize_nvfp4_partials(M);
+  const int m = int(M), k = int(K), np = quantize_nvfp4_partials(M, K);
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;

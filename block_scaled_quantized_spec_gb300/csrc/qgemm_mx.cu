@@ -424,6 +424,14 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
+      // the first stages' W tiles do not depend on the preceding kernel: in
+      // flight before the dependent wait (each stage's barrier takes the
+      // whole step's bytes now; its X parts follow after the wait)
+      const int pre = nloc < STAGES ? nloc : STAGES;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(full(i), TX_BYTES);
+        tma_load_2d(b_tile(i), &w_map, (j0 + i) * BK, wrow0 + n0, full(i));
+      }
       asm volatile("griddepcontrol.wait;" ::: "memory");   // the workspace comes from the preceding xquant
       // the X scale atoms of this tile's 128-row M tile(s); a second M half
       // past M has none (its rows are zeros and stored nowhere): the first
@@ -432,20 +440,22 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
       const uint8_t* sfh = p.sf_hi + mt0 * size_t(katoms) * SF_BYTES;
       const uint8_t* sfl = TALL ? (m0 + BM < p.M ? sfh + size_t(katoms) * SF_BYTES : sfh)
                                 : p.sf_lo + size_t(blockIdx.y) * size_t(katoms) * SF_BYTES;
-      int issued = 0;
+      int issued = pre;
       for (int i = 0; i < nloc; ++i) {
         const int s = i % STAGES, j = j0 + i;
         const uint32_t ph = (i / STAGES) & 1;
         if (*abort_flag) break;
-        if (!mbar_wait(empty(s), ph ^ 1u, p.limit_ns)) { fail(); break; }
-        mbar_arrive_expect_tx(full(s), TX_BYTES);
+        if (i >= pre) {
+          if (!mbar_wait(empty(s), ph ^ 1u, p.limit_ns)) { fail(); break; }
+          mbar_arrive_expect_tx(full(s), TX_BYTES);
+          tma_load_2d(b_tile(s), &w_map, j * BK, wrow0 + n0, full(s));
+        }
         tma_load_2d(a_hi(s), &xhi_map, j * BK, m0, full(s));
         if constexpr (TWO) tma_load_2d(a_lo(s), &xlo_map, j * BK, m0, full(s));
         if constexpr (TALL) tma_load_2d(a_lo(s), &xhi_map, j * BK, m0 + BM, full(s));   // the second M half
-        tma_load_2d(b_tile(s), &w_map, j * BK, wrow0 + n0, full(s));
         bulk_load(sf_s(s, 0), sfh + size_t(j) * XA * SF_BYTES, XA * SF_BYTES, full(s));
         if constexpr (TWO || TALL) bulk_load(sf_s(s, X2), sfl + size_t(j) * XA * SF_BYTES, XA * SF_BYTES, full(s));
-        issued = i + 1;
+        issued = i + 1 > pre ? i + 1 : pre;
       }
       // every issued copy lands before the CTA may exit
       for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
@@ -610,8 +620,13 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
       __syncwarp();
       if (lane == 0 && !p.drop_arrivals) mbar_arrive(sf_full(s));
     }
-  } else if (warp >= 4) {
+  }
+  if (warp >= 4 || (TALL && warp < 4)) {
     // --------------------------------------------------------------- epilogue
+    // warps 4-7 drain accumulator 0; with tall tiles warps 0-3, done with
+    // their roles, drain accumulator 1 at the same time (a warp reads the
+    // tensor-memory lanes of its own quadrant, warp % 4)
+    __syncwarp();
     int ok = 1;
     if (lane == 0) ok = mbar_wait(done_bar, 0, p.limit_ns);
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -621,8 +636,9 @@ __global__ void __launch_bounds__(THREADS, 1) qgemm_mx_kernel(const __grid_const
     const int q = warp & 3;
     float gsc = 1.0f;                               // NV: the two globals (the activation's from the quantizer)
     if constexpr (NV) gsc = __fmul_rn(p.gw, *p.gx);
+    const int hf0 = (TALL && warp < 4) ? 1 : 0;
     #pragma unroll 1
-    for (int hf = 0; hf < (TALL ? 2 : 1); ++hf) {   // the accumulators: M halves of a tall tile
+    for (int hf = hf0; hf < hf0 + 1; ++hf) {        // this warp's accumulator: an M half of a tall tile
     // the output row of this lane's accumulator row (grouped: through row_of)
     int m = m0 + hf * BM + q * 32 + lane;
     if (p.route_off) m = m < __ldg(p.route_off + p.E) ? __ldg(p.row_of + m) : -1;

@@ -41,9 +41,11 @@
 //      warps 4-7 drain the accumulator (tcgen05.ld) and store bf16/float32.
 //
 // The same kernel serves the quantized-activation products: one E4M3 term
-// (W . A8, kind::mxf8f6f4), and the all-FP4 product (W . A4: X packed to
-// MXFP4, both operands E2M1 two codes to a byte, kind::mxf4 with two scales
-// per row and instruction), each optionally on tall 256-row tiles.
+// (W . A8, kind::mxf8f6f4), and the all-FP4 product (W . A4: X packed in W's
+// FP4 family, both operands E2M1 two codes to a byte: MXFP4 on kind::mxf4
+// with two E8M0 scales per row and instruction, or NVFP4 on kind::mxf4nvf4
+// with four UE4M3 scales and the two tensors' globals in the epilogue), each
+// optionally on tall 256-row tiles.
 //
 // Every mbarrier wait is bounded; on expiry the kernel records it in the
 // device status word, lets issued copies and MMAs land, frees its tensor

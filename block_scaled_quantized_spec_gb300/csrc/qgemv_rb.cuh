@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_rb_kernel(const uint8_t* __r
         if (live && t == 0) xsum[(bw0 + sp) * 16 + m] = sm;
       }
       if (live && t == 0) xsc[(bw0 + sp) * 16 + m] = __uint_as_float(uint32_t(127 - sh) << 23);
-      m += dm;                                                              // the task 8 on
+      m += dm;                                                              // the work item 8 further on
       sp += dsp;
       if (sp >= nbw) {
         sp -= nbw;

@@ -312,3 +312,27 @@ def test_debug_keys_without_gpu(lib):
         with pytest.raises(q.QfmtError) as e:
             q.qfmt_debug_set(key, value)
         assert e.value.status == -1
+
+
+def test_quantized_activation_workspace_sizes(lib):
+    # codes, then 512-byte scale atoms per 128-row tile (a 4-byte cell per row
+    # covers 128 K for E8M0 per 32, 64 K for nvfp4's E4M3 per 16), then for
+    # nvfp4 the maxima scratch and the global; each part 1 KiB aligned
+    al = lambda v: (v + 1023) // 1024 * 1024  # noqa: E731
+    for m, k in [(1, 256), (300, 1024), (2048, 4096)]:
+        mp = (m + 127) // 128 * 128
+        assert q.qmm_a8_workspace_bytes("mxfp8_e4m3", m, k) == al(m * k) + al(mp * k // 32)
+        assert q.qmm_a4_workspace_bytes("mxfp4", m, k) == al(m * k // 2) + al(mp * k // 32)
+        assert q.qmm_a4_workspace_bytes("nvfp4", m, k) == al(m * k // 2) + al(mp * k // 16) + al(4 * 1025)
+    assert q.qmm_a4_workspace_bytes("mxfp8_e4m3", 8, 256) == 0
+    assert q.qmm_a4_workspace_bytes("mxfp4", 8, 384) == 0
+    assert q.qmm_a4_workspace_bytes("nvfp4", 0, 256) == 0
+
+
+def test_qmm_a4_rejects_before_device_work(lib):
+    f = q.FORMATS
+    args = lambda fmt, m, k: (f[fmt], None, None, 1.0, None, None, 1, m, 64, k, None, 0, None)  # noqa: E731
+    assert lib.qmm_a4(*args("mxfp8_e4m3", 8, 256)) == -4     # a weight format with no FP4 pairing
+    assert lib.qmm_a4(*args("mxfp4", 8, 384)) == -2          # K not a multiple of 256
+    assert lib.qmm_a4(*args("nvfp4", 8, 256)) == -8          # no workspace
+    assert lib.qmm_a4(*args("mxfp4", 0, 256)) == 0           # M = 0: nothing to do

@@ -27,3 +27,31 @@ def test_reference_arm_prints_one_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_breakdown_rows_are_calls_the_library_takes():
+    # every breakdown row names a format and shape the library's own host-side
+    # queries accept for the path the row's tag selects (no GPU): the
+    # quantized-activation rows get a workspace size, the path-B rows (the MX
+    # formats with a workspace) too, and every format is one of the library's
+    sys.path.insert(0, ROOT)
+    import bench
+    import block_scaled_quantized_spec_gb300 as q
+    from block_scaled_quantized_spec_gb300 import build
+    build.build()
+    q.load()
+    for row in bench.BREAKDOWN:
+        fmt, m, n, k = row[:4]
+        tag = row[4] if len(row) > 4 else "auto"
+        assert fmt in q.FORMATS, row
+        assert m >= 1 and n >= 1 and k % 32 == 0, row
+        if tag == "A8":
+            assert q.qmm_a8_workspace_bytes(fmt, m, k) > 0, row
+        elif tag == "A4":
+            assert q.qmm_a4_workspace_bytes(fmt, m, k) > 0, row
+        elif tag == "A":
+            assert m > 16 and fmt not in q.SUB_BYTE, row
+        else:
+            assert tag == "auto", row
+    for fmt, m, n, k, e in bench.GATHER + bench.GROUPED:
+        assert q.qmm_grouped_workspace_bytes(fmt, m, k, e) > 0
